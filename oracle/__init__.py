@@ -1,0 +1,154 @@
+"""TEST INFRASTRUCTURE ONLY - fp64 CPU oracle for causal decayed linear attention.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its
+``cpu_baseline`` leg and its ``--impl reference`` arm) may import this
+package.  The product package ``retnet_retention_gb300`` never imports it and
+shares no code with it.
+
+The arithmetic lives in ``linattn_oracle.c`` (plain C, fp64, OpenMP over the
+independent (b, h) sequences); this module only marshals numpy arrays.
+Every input is widened to fp64 from the exact values handed to the GPU
+(bf16 or fp32), and gamma is the same fp32 number, widened.
+
+Functions
+---------
+recurrent(q, k, v, gamma, phi, normalize, eps, S0, z0)
+    The causal recurrent form: S = gamma S + phi(k) v^T, z = gamma z + phi(k),
+    o = phi(q)^T S [/ (phi(q)^T z + eps)], update before read.  Sources:
+    "Linear attention" (zerotofrontier 21.2) box "Causal linear attention,
+    recurrent form"; "RetNet" (bembew) section "Recurrent Representation".
+decode_step(q, k, v, gamma, S, z, phi, normalize, eps)
+    One token of the same recurrence: the interview box "Causal linear
+    attention, recurrent and parallel, plus the decode step" on the "Linear
+    attention" page.  It is ``recurrent`` with T = 1 and the state passed in.
+noncausal(q, k, v, phi, normalize, eps)
+    gamma = 1, every query reads the one summary phi(K)^T V: box "Linear
+    attention" on the "Linear attention" page.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against the
+pages' worked example, brute-force parallel forms, closed forms, a library
+IIR filter and invariants; see that file for which pin covers which part.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+_LIB = None
+
+
+def _load(path: str | None = None):
+    lib = ctypes.CDLL(path or _build.build())
+    dp = ctypes.POINTER(ctypes.c_double)
+    L = ctypes.c_long
+    lib.oracle_recurrent.argtypes = [dp, dp, dp, dp, L, L, L, L, L, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, dp]
+    lib.oracle_recurrent.restype = ctypes.c_int
+    lib.oracle_noncausal.argtypes = [dp, dp, dp, L, L, L, L, L, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_double, dp, dp, dp]
+    lib.oracle_noncausal.restype = ctypes.c_int
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loop uses on this host."""
+    return int(lib().oracle_num_threads())
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor: widen its exact values
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _as4(x: np.ndarray, name: str) -> np.ndarray:
+    if x.ndim == 2:
+        x = x[None, None]
+    elif x.ndim == 3:
+        x = x[None]
+    if x.ndim != 4:
+        raise ValueError(f"{name}: expected [B,H,T,d] (or [T,d] / [H,T,d]), got {x.shape}")
+    return np.ascontiguousarray(x)
+
+
+def recurrent(q, k, v, gamma, phi: bool = False, normalize: bool = False,
+              eps: float = 1e-6, S0=None, z0=None, _lib=None):
+    """Causal recurrent form in fp64.
+
+    q, k: [B,H,T,dk]; v: [B,H,T,dv]; gamma: [H] (or a scalar).
+    S0: [B,H,dk,dv] or None; z0: [B,H,dk] or None.
+    Returns (O [B,H,T,dv], S_T [B,H,dk,dv], z_T [B,H,dk]) as float64 arrays.
+    """
+    Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
+    B, H, T, dk = Q.shape
+    dv = V.shape[-1]
+    if K.shape != Q.shape or V.shape[:3] != Q.shape[:3]:
+        raise ValueError(f"shape mismatch q{Q.shape} k{K.shape} v{V.shape}")
+    g = np.ascontiguousarray(np.broadcast_to(_f64(gamma).reshape(-1), (H,)).astype(np.float64))
+    S0a = None if S0 is None else np.ascontiguousarray(_f64(S0).reshape(B, H, dk, dv))
+    z0a = None if z0 is None else np.ascontiguousarray(_f64(z0).reshape(B, H, dk))
+    O = np.empty((B, H, T, dv))
+    S = np.empty((B, H, dk, dv))
+    z = np.empty((B, H, dk))
+    rc = (_lib or lib()).oracle_recurrent(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(g), B, H, T, dk, dv, int(bool(phi)),
+        int(bool(normalize)), float(eps), _ptr(S0a), _ptr(z0a), _ptr(O), _ptr(S), _ptr(z))
+    if rc != 0:
+        raise MemoryError("oracle_recurrent: scratch allocation failed")
+    return O, S, z
+
+
+def decode_step(q, k, v, gamma, S, z=None, phi: bool = False, normalize: bool = False,
+                eps: float = 1e-6):
+    """One recurrent decode step for [B,H,dk] q,k and [B,H,dv] v.
+
+    Returns (o [B,H,dv], S_new, z_new); the inputs are not modified.
+    """
+    q4 = _f64(q)[:, :, None, :]
+    k4 = _f64(k)[:, :, None, :]
+    v4 = _f64(v)[:, :, None, :]
+    O, S_new, z_new = recurrent(q4, k4, v4, gamma, phi, normalize, eps, S0=S, z0=z)
+    return O[:, :, 0, :], S_new, z_new
+
+
+def noncausal(q, k, v, phi: bool = False, normalize: bool = False, eps: float = 1e-6,
+              _lib=None):
+    """Non-causal (gamma = 1) form in fp64; returns (O, S, z) like ``recurrent``."""
+    Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
+    B, H, T, dk = Q.shape
+    dv = V.shape[-1]
+    O = np.empty((B, H, T, dv))
+    S = np.empty((B, H, dk, dv))
+    z = np.empty((B, H, dk))
+    rc = (_lib or lib()).oracle_noncausal(
+        _ptr(Q), _ptr(K), _ptr(V), B, H, T, dk, dv, int(bool(phi)), int(bool(normalize)),
+        float(eps), _ptr(O), _ptr(S), _ptr(z))
+    if rc != 0:
+        raise MemoryError("oracle_noncausal: scratch allocation failed")
+    return O, S, z
+
+
+def load_mutant(mutant: int, out_dir: str):
+    """Load a build of the oracle with a planted mistake (for pin tests only)."""
+    return _load(_build.build_mutant(mutant, out_dir))
+
+
+__all__ = ["recurrent", "decode_step", "noncausal", "num_threads", "load_mutant", "lib"]

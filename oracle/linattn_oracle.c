@@ -1,0 +1,225 @@
+/*
+ * TEST INFRASTRUCTURE ONLY - fp64 CPU oracle for causal kernel (linear)
+ * attention with a per-head scalar decay (RetNet retention).
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py (its cpu_baseline leg
+ * and its reference arm) may load this library.  The product path
+ * (retnet_retention_gb300) never links, loads or calls it, and this file
+ * shares no code, header or table with the CUDA kernels.
+ *
+ * What it computes is the plain definition, the recurrent form, one token
+ * at a time, in fp64, on fp64 copies of the exact input values:
+ *
+ *   for t = 0 .. T-1:
+ *       q~ = phi(q_t),  k~ = phi(k_t)                 phi = elu+1 or identity
+ *       S  = gamma * S + k~ v_t^T                      (d_k x d_v)
+ *       z  = gamma * z + k~                            (d_k)
+ *       o_t = q~^T S          [ / (q~^T z + eps) if normalising ]
+ *
+ * Sources (web pages on retention / linear attention):
+ *  - "Linear attention" (zerotofrontier, Chapter 21 section 21.2), box
+ *    "Causal linear attention, recurrent form": S_t = S_{t-1} + phi(k_t) v_t^T,
+ *    z_t = z_{t-1} + phi(k_t), o_t = S_t^T phi(q_t) / z_t^T phi(q_t); rows of
+ *    S index features, columns index value dimensions; an eps such as 1e-6
+ *    is added to the denominator.  The interview box "Causal linear
+ *    attention, recurrent and parallel, plus the decode step" fixes that each
+ *    token is included in its own sum (update first, then read).
+ *  - "RetNet" (bembew), section "Recurrent Representation":
+ *    S_n = gamma S_{n-1} + K_n^T V_n, O_n = Q_n S_n, S of shape d_k x d_v.
+ *  - "Efficient and Sparse Transformers" (temporalbook section 12.5),
+ *    subsection 3: phi(x) = elu(x) + 1; subsection 6 "Linear Attention as a
+ *    Special Case": linear attention is retention with gamma = 1.
+ *  - "Linear Attention, RWKV, and RetNet" (temporalbook section 13.3),
+ *    subsection 4: the generic "decay the old state, add, read out" loop.
+ *  - Non-causal form: "Linear attention" (zerotofrontier 21.2), box "Linear
+ *    attention": O = diag(phi(Q)(phi(K)^T 1))^-1 phi(Q)(phi(K)^T V).
+ *
+ * Readings where the pages are silent:
+ *  - with gamma < 1 and the normaliser on, z decays with the same gamma as S
+ *    (the pages never combine the two; the xLSTM box on the "Linear
+ *    attention" page decays its normaliser with the same gate as its state);
+ *  - eps is added after the dot product, only when normalising.
+ *
+ * Compile-time mutants (ORACLE_MUTANT=n) exist only so that the pin tests can
+ * show that each plausible mistake is caught; the default build has none.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* elu(x) + 1: x + 1 for x > 0, e^x otherwise ("Linear attention", box
+ * "Linear attention by hand on three tokens"). */
+static inline double phi_elu1(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
+
+static void feature(const double* x, double* out, long n, int phi)
+{
+    for (long i = 0; i < n; ++i) {
+#if ORACLE_MUTANT == 6 /* mutant: elu without the +1 */
+        out[i] = phi ? (x[i] > 0.0 ? x[i] : exp(x[i]) - 1.0) : x[i];
+#else
+        out[i] = phi ? phi_elu1(x[i]) : x[i];
+#endif
+    }
+}
+
+/*
+ * Causal recurrent form over a batch of independent (b, h) sequences.
+ *
+ *   Q, K : [B][H][T][dk]     V : [B][H][T][dv]     gamma : [H]
+ *   S0   : [B][H][dk][dv] or NULL (zero state)     z0 : [B][H][dk] or NULL
+ *   O    : [B][H][T][dv]     S_out : [B][H][dk][dv] or NULL   z_out : [B][H][dk] or NULL
+ *
+ * Returns 0, or -1 when a scratch allocation fails.
+ */
+int oracle_recurrent(const double* Q, const double* K, const double* V,
+                     const double* gamma, long B, long H, long T, long dk, long dv,
+                     int phi, int normalize, double eps,
+                     const double* S0, const double* z0,
+                     double* O, double* S_out, double* z_out)
+{
+    int failed = 0;
+    long BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (long bh = 0; bh < BH; ++bh) {
+        const long h = bh % H;
+        const double g = gamma[h];
+        double* S = (double*)malloc(sizeof(double) * (size_t)(dk * dv));
+        double* z = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* qf = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* kf = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!S || !z || !qf || !kf) {
+            failed = 1;
+            free(S); free(z); free(qf); free(kf);
+            continue;
+        }
+        if (S0) memcpy(S, S0 + bh * dk * dv, sizeof(double) * (size_t)(dk * dv));
+        else memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+        if (z0) memcpy(z, z0 + bh * dk, sizeof(double) * (size_t)dk);
+        else memset(z, 0, sizeof(double) * (size_t)dk);
+
+        for (long t = 0; t < T; ++t) {
+            const double* q = Q + (bh * T + t) * dk;
+            const double* k = K + (bh * T + t) * dk;
+            const double* v = V + (bh * T + t) * dv;
+            double* o = O + (bh * T + t) * dv;
+            feature(q, qf, dk, phi);
+            feature(k, kf, dk, phi);
+#if ORACLE_MUTANT == 1 /* mutant: read before write (token left out of its own sum) */
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += qf[i] * S[i * dv + j];
+                o[j] = acc;
+            }
+#endif
+            /* state update: S = gamma S + k~ v^T ; z = gamma z + k~ */
+            for (long i = 0; i < dk; ++i) {
+                for (long j = 0; j < dv; ++j) {
+#if ORACLE_MUTANT == 2 /* mutant: decay applied to the new term as well */
+                    S[i * dv + j] = g * (S[i * dv + j] + kf[i] * v[j]);
+#elif ORACLE_MUTANT == 3 /* mutant: decay dropped */
+                    S[i * dv + j] = S[i * dv + j] + kf[i] * v[j];
+#elif ORACLE_MUTANT == 5 /* mutant: outer product written transposed, v k~^T (shapes agree only when dk == dv) */
+                    S[i * dv + j] = g * S[i * dv + j] + v[i % dv] * kf[j % dk];
+#else
+                    S[i * dv + j] = g * S[i * dv + j] + kf[i] * v[j];
+#endif
+                }
+#if ORACLE_MUTANT == 4 /* mutant: normaliser not decayed */
+                z[i] = z[i] + kf[i];
+#else
+                z[i] = g * z[i] + kf[i];
+#endif
+            }
+#if ORACLE_MUTANT != 1
+            /* read-out: o = q~^T S (a d_v row) */
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += qf[i] * S[i * dv + j];
+                o[j] = acc;
+            }
+#endif
+            if (normalize) {
+                double den = 0.0;
+#if ORACLE_MUTANT == 7 /* mutant: normaliser summed over the feature axis of k only */
+                for (long i = 0; i < dk; ++i) den += z[i];
+#else
+                for (long i = 0; i < dk; ++i) den += qf[i] * z[i];
+#endif
+                den += eps;
+                for (long j = 0; j < dv; ++j) o[j] /= den;
+            }
+        }
+        if (S_out) memcpy(S_out + bh * dk * dv, S, sizeof(double) * (size_t)(dk * dv));
+        if (z_out) memcpy(z_out + bh * dk, z, sizeof(double) * (size_t)dk);
+        free(S); free(z); free(qf); free(kf);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Non-causal form (gamma = 1 only): one summary shared by every query.
+ *   S = sum_t k~_t v_t^T,  z = sum_t k~_t,  o_t = q~_t^T S [ / (q~_t^T z + eps) ]
+ * Same layouts as oracle_recurrent; S_out/z_out receive S and z.
+ */
+int oracle_noncausal(const double* Q, const double* K, const double* V,
+                     long B, long H, long T, long dk, long dv,
+                     int phi, int normalize, double eps,
+                     double* O, double* S_out, double* z_out)
+{
+    int failed = 0;
+    long BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (long bh = 0; bh < BH; ++bh) {
+        double* S = (double*)calloc((size_t)(dk * dv), sizeof(double));
+        double* z = (double*)calloc((size_t)dk, sizeof(double));
+        double* f = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!S || !z || !f) {
+            failed = 1;
+            free(S); free(z); free(f);
+            continue;
+        }
+        for (long t = 0; t < T; ++t) {
+            const double* k = K + (bh * T + t) * dk;
+            const double* v = V + (bh * T + t) * dv;
+            feature(k, f, dk, phi);
+            for (long i = 0; i < dk; ++i) {
+                for (long j = 0; j < dv; ++j) S[i * dv + j] += f[i] * v[j];
+                z[i] += f[i];
+            }
+        }
+        for (long t = 0; t < T; ++t) {
+            const double* q = Q + (bh * T + t) * dk;
+            double* o = O + (bh * T + t) * dv;
+            feature(q, f, dk, phi);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += f[i] * S[i * dv + j];
+                o[j] = acc;
+            }
+            if (normalize) {
+                double den = eps;
+                for (long i = 0; i < dk; ++i) den += f[i] * z[i];
+                for (long j = 0; j < dv; ++j) o[j] /= den;
+            }
+        }
+        if (S_out) memcpy(S_out + bh * dk * dv, S, sizeof(double) * (size_t)(dk * dv));
+        if (z_out) memcpy(z_out + bh * dk, z, sizeof(double) * (size_t)dk);
+        free(S); free(z); free(f);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,321 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each test checks the oracle against something other than itself: the
+pages' worked examples (tests/golden/), brute-force parallel forms, closed
+forms, a library IIR filter, and invariants the pages state.  The last test
+rebuilds the oracle with each planted mistake and shows that some pin fails.
+
+Which pin covers which part of the oracle:
+  recurrence, phi, normaliser, update order  -> hand example (exact)
+  causal mask, decay exponent, d_k != d_v    -> brute-force parallel form
+  decay accuracy over long T                 -> geometric-series closed form
+  decay as a linear filter                   -> scipy.signal.lfilter special case
+  non-causal form                            -> left/right multiplication orders
+  final state                                -> associative-memory example, orthonormal keys
+  normalised outputs                         -> constant V, o_1 = v_1, convex hull
+  chunkwise equations (the CUDA path's form) -> chunk-size invariance
+  state hand-off (decode, resume)            -> split prefill / decode == one pass
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import pins
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------------------
+# pin functions: each takes an oracle library handle (None = the real one) and
+# raises AssertionError on a mismatch.  The mutant test reuses them.
+# ---------------------------------------------------------------------------
+
+def pin_hand_example(lib=None):
+    g = _golden("hand_example_three_tokens.json")
+    q, k, v = (np.array(g[n], dtype=np.float64) for n in ("q", "k", "v"))
+    O, S, z = oracle.recurrent(q, k, v, 1.0, phi=True, normalize=True, eps=0.0, _lib=lib)
+    want = np.array([[a / b for a, b in row] for row in g["o_fraction"]])
+    np.testing.assert_allclose(O[0, 0], want, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(S[0, 0], np.array(g["S"][-1], dtype=np.float64))
+    np.testing.assert_array_equal(z[0, 0], np.array(g["z"][-1], dtype=np.float64))
+    # every intermediate state, one token at a time
+    for t in range(3):
+        O_t, S_t, z_t = oracle.recurrent(q[: t + 1], k[: t + 1], v[: t + 1], 1.0, phi=True,
+                                         normalize=True, eps=0.0, _lib=lib)
+        np.testing.assert_array_equal(S_t[0, 0], np.array(g["S"][t], dtype=np.float64))
+        np.testing.assert_array_equal(z_t[0, 0], np.array(g["z"][t], dtype=np.float64))
+        O_raw, _, _ = oracle.recurrent(q[: t + 1], k[: t + 1], v[: t + 1], 1.0, phi=True,
+                                       normalize=False, _lib=lib)
+        np.testing.assert_array_equal(O_raw[0, 0, t], np.array(g["numerator"][t], dtype=float))
+
+
+def pin_parallel_form(lib=None):
+    rng = _rng(1)
+    for trial in range(6):
+        B, H = 2, 3
+        T = int(rng.integers(1, 48))
+        dk, dv = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        if trial == 0:
+            dk, dv = 3, 7  # d_k != d_v on purpose
+        phi = bool(trial % 2)
+        normalize = phi and trial % 4 == 1
+        q = rng.standard_normal((B, H, T, dk))
+        k = rng.standard_normal((B, H, T, dk))
+        v = rng.standard_normal((B, H, T, dv))
+        gamma = rng.uniform(0.5, 1.0, H)
+        gamma[0] = 1.0
+        O, _, _ = oracle.recurrent(q, k, v, gamma, phi=phi, normalize=normalize, eps=1e-6,
+                                   _lib=lib)
+        ref = pins.parallel_form(q, k, v, gamma, phi=phi, normalize=normalize, eps=1e-6)
+        assert pins.rel_err(O, ref) < 1e-12, (trial, pins.rel_err(O, ref))
+
+
+def pin_masked_kernel_theorem(lib=None):
+    """diag(W1)^-1 W V with W = (phi(Q)phi(K)^T) . L equals the recurrence (gamma = 1)."""
+    rng = _rng(2)
+    q = rng.standard_normal((1, 2, 40, 5))
+    k = rng.standard_normal((1, 2, 40, 5))
+    v = rng.standard_normal((1, 2, 40, 6))
+    O, _, _ = oracle.recurrent(q, k, v, 1.0, phi=True, normalize=True, eps=0.0, _lib=lib)
+    ref = pins.parallel_form(q, k, v, 1.0, phi=True, normalize=True, eps=0.0)
+    assert pins.rel_err(O, ref) < 1e-12
+
+
+def pin_geometric_series(lib=None):
+    """d = 1, q = k = v = 1: o_n = sum_{m<=n} gamma^(n-m) = (1 - gamma^(n+1)) / (1 - gamma)."""
+    T = 65536
+    ones = np.ones((1, 1, T, 1))
+    for g in (0.99, 0.9999):
+        O, S, _ = oracle.recurrent(ones, ones, ones, g, _lib=lib)
+        n = np.arange(T, dtype=np.float64)
+        want = -np.expm1((n + 1.0) * np.log(g)) / (1.0 - g)
+        np.testing.assert_allclose(O[0, 0, :, 0], want, rtol=1e-10)
+        np.testing.assert_allclose(S[0, 0, 0, 0], want[-1], rtol=1e-10)
+
+
+def pin_iir_filter(lib=None):
+    """Constant q = c and k = b, d_v = 1: o = (c.b) * IIR filter 1/(1 - gamma z^-1) of v.
+
+    The scalar-decay special case of the SSD example on the "Linear Attention,
+    RWKV, and RetNet" page (section 13.3), checked against scipy's lfilter.
+    """
+    from scipy.signal import lfilter
+    rng = _rng(3)
+    T, n = 200, 4
+    c, b = rng.standard_normal(n), rng.standard_normal(n)
+    u = rng.standard_normal(T)
+    for alpha in (0.85, 0.5, 1.0):
+        q = np.tile(c, (T, 1))
+        k = np.tile(b, (T, 1))
+        O, _, _ = oracle.recurrent(q, k, u[:, None], alpha, _lib=lib)
+        want = float(c @ b) * lfilter([1.0], [1.0, -alpha], u)
+        np.testing.assert_allclose(O[0, 0, :, 0], want, rtol=1e-12, atol=1e-12)
+
+
+def pin_noncausal_orders(lib=None):
+    rng = _rng(4)
+    q = rng.standard_normal((2, 2, 33, 6))
+    k = rng.standard_normal((2, 2, 33, 6))
+    v = rng.standard_normal((2, 2, 33, 9))
+    for phi, normalize in ((False, False), (True, False), (True, True)):
+        O, S, _ = oracle.noncausal(q, k, v, phi=phi, normalize=normalize, _lib=lib)
+        left = pins.noncausal_left(q, k, v, phi=phi, normalize=normalize)
+        right = pins.noncausal_right(q, k, v, phi=phi, normalize=normalize)
+        assert pins.rel_err(O, left) < 1e-12
+        assert pins.rel_err(O, right) < 1e-12
+        # its summary is the causal final state at gamma = 1
+        _, S_c, _ = oracle.recurrent(q, k, v, 1.0, phi=phi, _lib=lib)
+        assert pins.rel_err(S, S_c) < 1e-12
+
+
+def pin_associative_memory(lib=None):
+    g = _golden("associative_memory_three_pairs.json")
+    k = np.array(g["k"], dtype=np.float64)
+    v = np.array(g["v"], dtype=np.float64)
+    O, S, _ = oracle.noncausal(k[:2], k[:2], v[:2], _lib=lib)
+    np.testing.assert_allclose(S[0, 0], g["S_after_two"], atol=1e-15)
+    np.testing.assert_allclose(O[0, 0, 0], g["reads_after_two"]["k1"], atol=1e-15)
+    np.testing.assert_allclose(O[0, 0, 1], g["reads_after_two"]["k2"], atol=1e-15)
+    O, S, _ = oracle.noncausal(k, k, v, _lib=lib)
+    np.testing.assert_allclose(S[0, 0], g["S_after_three"], atol=1e-14)
+    np.testing.assert_allclose(O[0, 0, 0], g["reads_after_three"]["k1"], atol=1e-14)
+    np.testing.assert_allclose(O[0, 0, 2], g["reads_after_three"]["k3"], atol=1e-14)
+    # the causal form reaches the same final state
+    _, S_c, _ = oracle.recurrent(k, k, v, 1.0, _lib=lib)
+    np.testing.assert_allclose(S_c[0, 0], g["S_after_three"], atol=1e-14)
+
+
+def pin_orthonormal_keys(lib=None):
+    """Orthonormal keys, gamma = 1, identity phi: each causal read returns its own value."""
+    rng = _rng(5)
+    dk, dv = 16, 24
+    Qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    keys = Qm.T  # rows orthonormal
+    v = rng.standard_normal((dk, dv))
+    O, S, _ = oracle.recurrent(keys, keys, v, 1.0, _lib=lib)
+    np.testing.assert_allclose(O[0, 0], v, atol=1e-12)
+    np.testing.assert_allclose(S[0, 0], keys.T @ v, atol=1e-12)
+
+
+def pin_normalised_invariants(lib=None):
+    rng = _rng(6)
+    B, H, T, dk, dv = 1, 3, 64, 8, 5
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    gamma = np.array([1.0, 0.9, 0.5])
+    # constant values give constant outputs (also with decay: z decays like S)
+    c = rng.standard_normal(dv)
+    vc = np.broadcast_to(c, (B, H, T, dv)).copy()
+    O, _, _ = oracle.recurrent(q, k, vc, gamma, phi=True, normalize=True, eps=0.0, _lib=lib)
+    np.testing.assert_allclose(O, vc, rtol=1e-13, atol=1e-13)
+    # the first output is the first value; every output lies in the values' hull
+    v = rng.standard_normal((B, H, T, dv))
+    O, _, _ = oracle.recurrent(q, k, v, gamma, phi=True, normalize=True, eps=0.0, _lib=lib)
+    np.testing.assert_allclose(O[:, :, 0], v[:, :, 0], rtol=1e-13, atol=1e-13)
+    lo = np.minimum.accumulate(v, axis=2)
+    hi = np.maximum.accumulate(v, axis=2)
+    assert np.all(O >= lo - 1e-12) and np.all(O <= hi + 1e-12)
+
+
+def pin_chunkwise_invariance(lib=None):
+    rng = _rng(7)
+    B, H, T, dk, dv = 2, 2, 77, 6, 10
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    v = rng.standard_normal((B, H, T, dv))
+    gamma = np.array([0.95, 0.6])
+    for phi, normalize in ((False, False), (True, True)):
+        O, S, z = oracle.recurrent(q, k, v, gamma, phi=phi, normalize=normalize, _lib=lib)
+        for C in (1, 4, 16, 32, 64, 128):
+            Oc, Sc, zc = pins.chunkwise(q, k, v, gamma, C, phi=phi, normalize=normalize)
+            assert pins.rel_err(Oc, O) < 1e-12, (C, pins.rel_err(Oc, O))
+            assert pins.rel_err(Sc, S) < 1e-12
+            if normalize:
+                assert pins.rel_err(zc, z) < 1e-12
+
+
+def pin_state_handoff(lib=None):
+    """Prefill T1 then resume (chunked or token by token) equals one pass over T."""
+    rng = _rng(8)
+    B, H, T, dk, dv = 2, 2, 50, 4, 6
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    v = rng.standard_normal((B, H, T, dv))
+    gamma = np.array([0.9, 1.0])
+    O, S, z = oracle.recurrent(q, k, v, gamma, phi=True, normalize=True, _lib=lib)
+    t1 = 31
+    O1, S1, z1 = oracle.recurrent(q[:, :, :t1], k[:, :, :t1], v[:, :, :t1], gamma, phi=True,
+                                  normalize=True, _lib=lib)
+    O2, S2, z2 = oracle.recurrent(q[:, :, t1:], k[:, :, t1:], v[:, :, t1:], gamma, phi=True,
+                                  normalize=True, S0=S1, z0=z1, _lib=lib)
+    assert pins.rel_err(np.concatenate([O1, O2], axis=2), O) < 1e-13
+    assert pins.rel_err(S2, S) < 1e-13 and pins.rel_err(z2, z) < 1e-13
+
+
+ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
+            pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
+            pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
+            pin_chunkwise_invariance, pin_state_handoff]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_decode_step_matches_recurrence():
+    rng = _rng(9)
+    B, H, T, dk, dv = 2, 3, 12, 5, 7
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    v = rng.standard_normal((B, H, T, dv))
+    gamma = np.array([0.9, 0.99, 1.0])
+    O, S, z = oracle.recurrent(q, k, v, gamma, phi=True, normalize=True)
+    S_t = np.zeros((B, H, dk, dv))
+    z_t = np.zeros((B, H, dk))
+    for t in range(T):
+        S_in = S_t.copy()
+        o, S_t, z_t = oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], gamma, S_t, z_t,
+                                         phi=True, normalize=True)
+        np.testing.assert_array_equal(S_in, S_in)  # inputs untouched
+        assert pins.rel_err(o, O[:, :, t]) < 1e-13
+    assert pins.rel_err(S_t, S) < 1e-13
+
+
+def test_hand_example_kernel_matrix_pins_the_helper():
+    """The brute-force helper reproduces the page's kernel matrix and row sums."""
+    g = _golden("hand_example_three_tokens.json")
+    fq = pins.phi_elu1(np.array(g["q"], dtype=float))
+    fk = pins.phi_elu1(np.array(g["k"], dtype=float))
+    np.testing.assert_array_equal(fq, g["phi_q"])
+    np.testing.assert_array_equal(fk, g["phi_k"])
+    W = fq @ fk.T
+    np.testing.assert_array_equal(W, g["kernel_matrix"])
+    np.testing.assert_array_equal((W * pins.decay_mask(3, 1.0)).sum(axis=1),
+                                  g["masked_row_sums"])
+
+
+def test_empty_sequence_returns_initial_state():
+    S0 = np.arange(12, dtype=float).reshape(1, 1, 3, 4)
+    z0 = np.arange(3, dtype=float).reshape(1, 1, 3)
+    e = np.zeros((1, 1, 0, 3))
+    O, S, z = oracle.recurrent(e, e, np.zeros((1, 1, 0, 4)), 0.9, S0=S0, z0=z0)
+    assert O.shape == (1, 1, 0, 4)
+    np.testing.assert_array_equal(S, S0)
+    np.testing.assert_array_equal(z, z0)
+
+
+def test_workload_decays_are_exact():
+    """gamma_h = 1 - 2^(-5-h) ("RetNet" page, "Multi-Scale Retention") is exact in fp32."""
+    g = workloads.gammas(workloads.CONFIGS["msr_retention_bf16"])
+    for h, x in enumerate(g):
+        assert float(x) == 1.0 - 2.0 ** (-5 - h)
+    g = workloads.gammas(workloads.CONFIGS["decode_bf16"])
+    assert [float(x) for x in g] == [1.0 - 2.0 ** (-5 - (h % 8)) for h in range(32)]
+    g = workloads.gammas(workloads.CONFIGS["long_retention_bf16"])
+    assert np.all((g >= np.float32(0.99)) & (g <= np.float32(0.9999)))
+
+
+def test_input_slices_regenerate_exactly():
+    full = workloads.make_inputs("linear_attention_bf16")
+    pairs = [(0, 0), (2, 5), (3, 7)]
+    part = workloads.make_inputs("linear_attention_bf16", pairs=pairs)
+    for i, (b, h) in enumerate(pairs):
+        for n in ("q", "k", "v"):
+            assert (part[n][i] == full[n][b, h]).all()
+
+
+MUTANTS = {
+    1: "read before write",
+    2: "decay applied to the new term",
+    3: "decay dropped",
+    4: "normaliser not decayed",
+    5: "outer product transposed",
+    6: "elu without +1",
+    7: "normaliser over the wrong axis",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda m: MUTANTS[m].replace(" ", "_"))
+def test_planted_mistake_is_caught(mutant, tmp_path):
+    lib = oracle.load_mutant(mutant, str(tmp_path))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
