@@ -1,0 +1,484 @@
+"""Benchmark: causal decayed linear attention (retention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  A "step" is one chunkwise forward (la_chunk_fwd)
+over the headline workload: causal linear attention, B=4, H=8, T=4096,
+d_k=d_v=64, bf16 inputs, phi = elu+1, normalised.  The same line carries
+sub-measurements of the other workloads (multi-scale retention prefill,
+long-sequence prefill, the recurrent decode step), each timed the same way.
+
+Timing: CUDA events on the launching stream; W untimed warm-up steps; the K
+timed steps cycle through enough input copies that their footprint exceeds
+3x the L2 cache, so every step reads its inputs from HBM.  N > 1 (torchrun):
+each rank runs its own shard of a batch N times larger (weak scaling, no
+collective on the data path); the time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a
+bounded sample of the same workload (the comparison arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = ("retention fwd tokens/s & TFLOP/s (% bf16 TC peak); decode steps/s & HBM GB/s")
+HEADLINE = "linear_attention_bf16"
+L2_BYTES = 129 * 1024 * 1024
+C_REF = 64  # chunk length fixed for counting useful intra-chunk flops
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def alg_bytes(c: dict) -> int:
+    """Bytes the method must move: read Q, K, V, write O, write S_T (and z_T) in fp32."""
+    es = 2 if c["dtype"] == "bf16" else 4
+    nbh = c["B"] * c["H"]
+    io = nbh * c["T"] * (2 * c["dk"] + 2 * c["dv"]) * es
+    state = nbh * c["dk"] * c["dv"] * 4 + (nbh * c["dk"] * 4 if c["normalize"] else 0)
+    return io + state
+
+
+def alg_flops(c: dict) -> int:
+    """Useful flops: 4 d_k d_v per head-token (state update + read-out, the right
+    order of "Moving the parentheses") plus the causal lower triangle of C_REF-long
+    intra-chunk squares, C_REF (d_k + d_v) per head-token."""
+    nbh = c["B"] * c["H"]
+    return nbh * c["T"] * (4 * c["dk"] * c["dv"] + C_REF * (c["dk"] + c["dv"]))
+
+
+def decode_bytes(c: dict) -> int:
+    """Per decode step: read + write the fp32 state, read q, k, v, write o."""
+    nbh = c["B"] * c["H"]
+    es = 2 if c["dtype"] == "bf16" else 4
+    return nbh * (2 * c["dk"] * c["dv"] * 4 + (2 * c["dk"] + 2 * c["dv"]) * es)
+
+
+def decode_flops(c: dict) -> int:
+    """About 4 d_k d_v flops per head per token ("Decoding, training, ...")."""
+    return c["B"] * c["H"] * 4 * c["dk"] * c["dv"]
+
+
+def describe(name: str, c: dict) -> str:
+    bits = [f"{name}: B={c['B']} H={c['H']} T={c['T']} d_k={c['dk']} d_v={c['dv']}",
+            c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity",
+            "normalised" if c["normalize"] else "no normaliser"]
+    return ", ".join(bits)
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained",
+                                                      d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict | None:
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 0.25 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in busy),
+                    sm_max_mhz=max(r["smax"] for r in rows), reasons=sorted(reasons),
+                    samples=len(rows))
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def time_region(fn, steps: int, stream) -> float:
+    """Device milliseconds for `steps` calls of fn(i), bracketed by events on `stream`."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: int,
+                    e2e: bool = False) -> dict:
+    c = dict(workloads.CONFIGS[name])
+    B = c["B"]
+    pairs = [(rank * B + b, h) for b in range(B) for h in range(c["H"])]
+    cw = dict(c)
+    cw["B"] = B * world
+    x = workloads.make_inputs(cw, pairs=pairs)
+    shape_qk = (B, c["H"], c["T"], c["dk"])
+    shape_v = (B, c["H"], c["T"], c["dv"])
+    q = x["q"].reshape(shape_qk)
+    k = x["k"].reshape(shape_qk)
+    v = x["v"].reshape(shape_v)
+    gamma = x["gamma"]
+    dev = torch.device("cuda")
+    per_set = alg_bytes(c)
+    n_sets = max(1, min(16, (3 * L2_BYTES + per_set - 1) // per_set))
+    sets = []
+    for _ in range(n_sets):
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        O = torch.empty(shape_v, dtype=qd.dtype, device=dev)
+        S = torch.empty(B, c["H"], c["dk"], c["dv"], device=dev)
+        z = torch.empty(B, c["H"], c["dk"], device=dev) if c["normalize"] else None
+        sets.append((qd, kd, vd, O, S, z))
+    ws_n = la.workspace_size(B, c["H"], c["T"], c["dk"], c["dv"], qd.dtype, c["phi"],
+                             c["normalize"])
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        qd, kd, vd, O, S, z = sets[i % n_sets]
+        la.chunk_fwd(qd, kd, vd, gamma, phi=c["phi"], normalize=c["normalize"], out=O,
+                     S_out=S, z_out=z, workspace=ws, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    ms = time_region(step, steps, stream)
+    res = dict(name=name, config=c, ms=ms / steps, tokens=B * c["T"], n_sets=n_sets,
+               alg_bytes=alg_bytes(c), alg_flops=alg_flops(c))
+    if e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        Oh = torch.empty(shape_v, dtype=q.dtype, pin_memory=True)
+        Sh = torch.empty(B, c["H"], c["dk"], c["dv"], pin_memory=True)
+        zh = torch.empty(B, c["H"], c["dk"], pin_memory=True) if c["normalize"] else None
+
+        def step_host(i):
+            qd, kd, vd, O, S, z = sets[i % n_sets]
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            la.chunk_fwd(qd, kd, vd, gamma, phi=c["phi"], normalize=c["normalize"], out=O,
+                         S_out=S, z_out=z, workspace=ws, stream=stream)
+            Oh.copy_(O, non_blocking=True)
+            Sh.copy_(S, non_blocking=True)
+            if zh is not None:
+                zh.copy_(z, non_blocking=True)
+
+        for i in range(warmup):
+            step_host(i)
+        ms_h = time_region(step_host, steps, stream)
+        es = q.element_size()
+        res["e2e_ms"] = ms_h / steps
+        res["h2d"] = (q.numel() + k.numel() + v.numel()) * es
+        res["d2h"] = Oh.numel() * es + Sh.numel() * 4 + (zh.numel() * 4 if zh is not None else 0)
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> dict:
+    name = "decode_bf16"
+    c = dict(workloads.CONFIGS[name])
+    B, H = c["B"], c["H"]
+    pairs = [(rank * B + b, h) for b in range(B) for h in range(H)]
+    cw = dict(c)
+    cw["B"] = B * world
+    x = workloads.make_inputs(cw, pairs=pairs)
+    dev = torch.device("cuda")
+    q = x["q"].reshape(B, H, c["T"], c["dk"]).to(dev)
+    k = x["k"].reshape(B, H, c["T"], c["dk"]).to(dev)
+    v = x["v"].reshape(B, H, c["T"], c["dv"]).to(dev)
+    _, S, _ = la.chunk_fwd(q, k, v, x["gamma"])
+    del q, k, v
+    # every decode step's own inputs, resident before timing
+    d = workloads.decode_inputs_all(cw, steps_total)
+    bsl = slice(rank * B, (rank + 1) * B)
+    dq = d["q"][:, bsl].contiguous().to(dev)
+    dk = d["k"][:, bsl].contiguous().to(dev)
+    dv = d["v"][:, bsl].contiguous().to(dev)
+    o = torch.empty(steps_total, B, H, c["dv"], dtype=dq.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    S_warm = S.clone()
+
+    for i in range(warmup):  # warm-up on a scratch copy of the state
+        la.recurrent_step(dq[i], dk[i], dv[i], x["gamma"], S_warm, out=o[i], stream=stream)
+    del S_warm
+
+    def step(i):
+        la.recurrent_step(dq[i], dk[i], dv[i], x["gamma"], S, out=o[i], stream=stream)
+
+    ms = time_region(step, steps_total, stream)
+    res = dict(name=name, config=c, ms=ms / steps_total, steps=steps_total,
+               bytes=decode_bytes(c), flops=decode_flops(c))
+    del dq, dk, dv, o, S
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_baseline(name: str, budget_s: float = 12.0) -> dict:
+    """The fp64 oracle on the host cores, on whole (b, h) sequences of the workload."""
+    import oracle
+    c = workloads.CONFIGS[name]
+    H = c["H"]
+    pairs = workloads.sample_pairs(c["B"], H, max(1, min(c["B"] * H, oracle.num_threads())))
+    x = workloads.make_inputs(c, pairs=pairs)
+    g = x["gamma_pairs"]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.recurrent(x["q"][None], x["k"][None], x["v"][None], g, phi=c["phi"],
+                         normalize=c["normalize"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    tok = reps * len(pairs) * c["T"] / H  # token = one position of all H heads
+    return dict(value=tok / el, unit="tokens/s", cores=oracle.num_threads(), kind="oracle",
+                sample=(f"{reps} x {len(pairs)} whole (b, h) sequences of T={c['T']} "
+                        f"({describe(name, c)}); tokens counted per position of all {H} heads"),
+                seconds=el)
+
+
+def run_ours(args) -> dict | None:
+    import retnet_retention_gb300 as la
+    from retnet_retention_gb300 import _build
+    _build.build()
+    la.library()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk = peaks()
+    barrier()
+    sampler = ClockSampler(local)
+    with sampler:
+        head = prefill_measure(la, HEADLINE, args.steps, args.warmup, rank, world, e2e=True)
+    barrier()
+    head_ms = max_over_ranks(head["ms"])
+    e2e_ms = max_over_ranks(head["e2e_ms"])
+    others = {}
+    if not args.headline_only:
+        for name in ("msr_retention_bf16", "long_retention_bf16"):
+            r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
+            r["ms"] = max_over_ranks(r["ms"])
+            others[name] = r
+        dec = decode_measure(la, workloads.CONFIGS["decode_bf16"]["decode_steps"],
+                             args.warmup, rank, world)
+        dec["ms"] = max_over_ranks(dec["ms"])
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    c = head["config"]
+    tokens_all = head["tokens"] * world
+    value = tokens_all / (head_ms * 1e-3)
+    achieved_gbs = head["alg_bytes"] / (head["ms"] * 1e-3) / 1e9
+    useful_tflops = head["alg_flops"] / (head["ms"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, see workloads/)",
+        "config": {
+            "workload": describe(HEADLINE, c),
+            "global_batch": c["B"] * world,
+            "seq_len": c["T"],
+            "parallelism": "replicas" if world == 1 else f"batch-sharded x{world}",
+            "l2": f"inputs rotate over {head['n_sets']} copies ({head['n_sets'] * head['alg_bytes'] / 1e6:.0f} MB > L2)",
+        },
+        "tflops_useful": useful_tflops,
+        "pct_bf16_peak": 100.0 * useful_tflops / pk["bf16_tflops"],
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved_gbs,
+            "peak": pk["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved_gbs / pk["hbm_gbs"],
+            "traffic": None,
+            "kernel": "chunk_simt_kernel",
+            "peak_source": pk["source"],
+        },
+        "e2e": {
+            "value": tokens_all / (e2e_ms * 1e-3),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": head["h2d"],
+            "d2h_bytes_per_step": head["d2h"],
+        },
+        "gpu_launches": args.steps,
+    }
+    if not args.headline_only:
+        sub = {}
+        for name, r in others.items():
+            rc = r["config"]
+            gbs = r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9
+            tf = r["alg_flops"] / (r["ms"] * 1e-3) / 1e12
+            sub[name] = dict(workload=describe(name, rc), tokens_per_s=r["tokens"] * world /
+                             (r["ms"] * 1e-3), ms=r["ms"], alg_gbs=gbs,
+                             roofline_frac=gbs / pk["hbm_gbs"], tflops_useful=tf,
+                             pct_bf16_peak=100.0 * tf / pk["bf16_tflops"])
+        dc = dec["config"]
+        gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
+        sub["decode_bf16"] = dict(
+            workload=f"decode_bf16: B={dc['B']} H={dc['H']} d_k={dc['dk']} d_v={dc['dv']} fp32 "
+                     f"state after a {dc['T']}-token prefill, {dec['steps']} steps",
+            steps_per_s=1e3 / dec["ms"], ms_per_step=dec["ms"], hbm_gbs=gbs,
+            roofline_frac=gbs / pk["hbm_gbs"], kernel="decode_step_kernel")
+        line["workloads"] = sub
+    clocks = sampler.summary()
+    if clocks is not None:
+        line["clocks"] = clocks
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(HEADLINE)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def run_reference(args) -> dict | None:
+    """The oracle as it stands, on the host cores, on bounded samples of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    c = workloads.CONFIGS[HEADLINE]
+    H = c["H"]
+    n = max(1, min(c["B"] * H, oracle.num_threads()))
+    pairs = workloads.sample_pairs(c["B"], H, n)
+    x = workloads.make_inputs(c, pairs=pairs)
+    g = x["gamma_pairs"]
+
+    def one():
+        oracle.recurrent(x["q"][None], x["k"][None], x["v"][None], g, phi=c["phi"],
+                         normalize=c["normalize"])
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    tok_per_step = len(pairs) * c["T"] / H
+    value = args.steps * tok_per_step / el
+    sample = (f"each step: {len(pairs)} whole (b, h) sequences of T={c['T']} of "
+              f"{describe(HEADLINE, c)}; tokens counted per position of all {H} heads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(HEADLINE, c), "global_batch": c["B"],
+                   "seq_len": c["T"], "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * linattn.h - C ABI of the GB300 (sm_103a) causal decayed linear attention
+ * library, liblinattn.so.
+ *
+ * The operator (one head, one sequence):
+ *
+ *   S_t = gamma * S_{t-1} + phi(k_t) v_t^T        S: d_k x d_v, fp32
+ *   z_t = gamma * z_{t-1} + phi(k_t)              z: d_k,       fp32
+ *   o_t = phi(q_t)^T S_t  [ / (phi(q_t)^T z_t + eps)  when normalising ]
+ *
+ * which equals the masked parallel form O = (Q K^T . D) V, D_nm = gamma^(n-m)
+ * for n >= m and 0 otherwise.
+ *   - "RetNet" (bembew): "Parallel Representation" (O = (QK^T . D)V and D),
+ *     "Recurrent Representation" (S_n = gamma S_{n-1} + K_n^T V_n,
+ *     O_n = Q_n S_n), "Chunked Recurrent Representation" (chunks computed in
+ *     parallel, the state carried between them), "Multi-Scale Retention"
+ *     (one gamma per head).
+ *   - "Linear attention" (zerotofrontier 21.2): box "Causal linear attention,
+ *     recurrent form" (phi, the normaliser z, eps in the denominator, rows of
+ *     S index features and columns value dimensions) and box "Linear
+ *     attention" (the non-causal form).
+ *   - "Efficient and Sparse Transformers" (temporalbook 12.5), subsection 6:
+ *     linear attention is the gamma = 1 case; phi(x) = elu(x) + 1.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major, caller-owned DEVICE memory (allocated by
+ *     the caller, e.g. PyTorch); the library allocates nothing, keeps no
+ *     state between calls and never synchronises the stream.
+ *   - Layouts: Q, K [B][H][T][d_k]; V, O [B][H][T][d_v]; S [B][H][d_k][d_v]
+ *     (rows = features, columns = value dims); z [B][H][d_k].
+ *   - Q/K/V/O hold `dtype` elements (fp32 or bf16); states are always fp32.
+ *   - Every device pointer must be 16-byte aligned; d_k and d_v must be
+ *     multiples of 16 in [16, 256].
+ *   - `gamma` is a HOST array of H fp32 decays, each in (0, 1]; it is read
+ *     during the call (its values travel in the kernel parameters), so the
+ *     array may be reused as soon as the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  The return code covers host-side argument
+ *     checks and launch errors only.  `dev_status`, if not NULL, is a device
+ *     int the kernels set to a nonzero la_status when they detect a problem
+ *     on the device (a bounded wait that ran out); the caller zeroes it
+ *     beforehand and reads it after synchronising.
+ *   - Arguments are checked before anything is enqueued: a call that returns
+ *     LA_ERR_INVALID_ARG or LA_ERR_UNSUPPORTED has launched nothing and
+ *     written nothing.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library (the library is built with hidden default
+ * visibility; only these are exported). */
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* bad size, pointer, alignment, gamma or workspace */
+    LA_ERR_UNSUPPORTED = 2,  /* a combination the method does not define */
+    LA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    LA_ERR_TIMEOUT = 4       /* device side only: a bounded wait ran out */
+} la_status;
+
+typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
+
+/* flags */
+#define LA_PHI_ELU1  1u  /* apply phi(x) = elu(x) + 1 to q and k (not v) */
+#define LA_NORMALIZE 2u  /* divide by phi(q)^T z + eps */
+#define LA_NONCAUSAL 4u  /* every query reads the whole sequence; gamma must be 1 */
+
+/* Human-readable text of a status code (static storage, never NULL). */
+LA_API const char* la_status_string(int status);
+
+/* ABI version of this header: LA_ABI_VERSION. */
+#define LA_ABI_VERSION 1
+LA_API int la_abi_version(void);
+
+/*
+ * Bytes of device workspace la_chunk_fwd needs for these arguments (0 when
+ * the chosen path needs none).  Pure host arithmetic; never fails (returns
+ * 0 for arguments la_chunk_fwd would reject).  `chunk` as for la_chunk_fwd.
+ */
+LA_API size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
+                         unsigned flags, int chunk);
+
+/*
+ * Zero-fill a state: S[B][H][d_k][d_v] and, if not NULL, z[B][H][d_k].
+ * The empty state S_0 = 0, z_0 = 0 of the "Causal linear attention,
+ * recurrent form" box ("Linear attention", zerotofrontier 21.2).
+ * Errors: LA_ERR_INVALID_ARG for S == NULL, a negative size, or a misaligned
+ * pointer; LA_ERR_CUDA if the launch fails.  B or H == 0 is a no-op.
+ */
+LA_API la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v,
+                        la_stream_t stream);
+
+/*
+ * Chunkwise forward over whole sequences (prefill / training forward):
+ * "Chunked Recurrent Representation" ("RetNet", bembew) - the intra-chunk
+ * part in the parallel form, the inter-chunk part through the carried state.
+ *
+ *   Q, K      [B][H][T][d_k]  dtype      inputs, read only
+ *   V         [B][H][T][d_v]  dtype      input, read only
+ *   gamma     host float[H]              per-head decay in (0, 1]
+ *   flags     LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL
+ *   eps       added to the denominator (used only with LA_NORMALIZE; the
+ *             pages use 1e-6)
+ *   S0, z0    [B][H][d_k][d_v], [B][H][d_k] fp32 initial state, or NULL for
+ *             zero.  S0 may alias S_out and z0 may alias z_out (in-place
+ *             continuation).  The normaliser state z is carried whether or
+ *             not LA_NORMALIZE is set, so z_out is valid either way.
+ *   O         [B][H][T][d_v]  dtype      output; must not overlap Q, K, V
+ *   S_out     [B][H][d_k][d_v] fp32 final state S_T, or NULL
+ *   z_out     [B][H][d_k] fp32 final normaliser z_T, or NULL
+ *   chunk     chunk length C: 0 = let the library choose, else one of
+ *             16, 32, 64, 128 (the result does not depend on it beyond
+ *             rounding)
+ *   workspace device scratch of at least la_workspace_size(...) bytes
+ *             (may be NULL when that size is 0); overwritten by the call
+ *   dev_status  device int or NULL (see the conventions above)
+ *
+ * T == 0 is valid: nothing is written to O and the final state equals the
+ * initial one.  B == 0 or H == 0 is a no-op.
+ * LA_NONCAUSAL ("Linear attention" box, non-causal form): requires every
+ * gamma == 1 and S0 == z0 == NULL, else LA_ERR_UNSUPPORTED; S_out / z_out
+ * then receive phi(K)^T V and phi(K)^T 1.
+ * Errors: LA_ERR_INVALID_ARG (negative size, d_k/d_v not a multiple of 16
+ * in [16, 256], a NULL required pointer, misalignment, gamma outside (0, 1],
+ * non-finite or negative eps, an unknown flag, dtype or chunk, workspace
+ * too small, O overlapping an input); LA_ERR_UNSUPPORTED; LA_ERR_CUDA.
+ */
+LA_API la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
+                       const float* gamma, int B, int H, int T, int d_k, int d_v,
+                       unsigned flags, float eps,
+                       const float* S0, const float* z0,
+                       void* O, float* S_out, float* z_out,
+                       int chunk, void* workspace, size_t workspace_bytes,
+                       int* dev_status, la_stream_t stream);
+
+/*
+ * One recurrent decode step for every (b, h), updating the state in place:
+ * "Recurrent Representation" ("RetNet", bembew) and the decode step of the
+ * "Linear attention" page (zerotofrontier 21.2, "Decoding, training, and
+ * what each costs"; update first, then read, so the token is in its own sum):
+ *
+ *   S = gamma S + phi(k) v^T ;  z = gamma z + phi(k)     (z only if normalising)
+ *   o = phi(q)^T S  [ / (phi(q)^T z + eps) ]
+ *
+ *   q, k   [B][H][d_k] dtype;  v [B][H][d_v] dtype;  o [B][H][d_v] dtype
+ *   S      [B][H][d_k][d_v] fp32, read and written in place
+ *   z      [B][H][d_k] fp32, in place; required with LA_NORMALIZE, else ignored
+ *   flags  LA_PHI_ELU1 | LA_NORMALIZE (LA_NONCAUSAL is LA_ERR_UNSUPPORTED)
+ * Errors: as la_chunk_fwd.
+ */
+LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
+                            const float* gamma, int B, int H, int d_k, int d_v,
+                            unsigned flags, float eps,
+                            float* S, float* z, void* o,
+                            int* dev_status, la_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,218 @@
+"""Python binding of liblinattn.so: causal decayed linear attention on GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels behind the C ABI (include/linattn.h); PyTorch supplies device memory
+and the current stream.  There is no CPU fallback: without the built library
+every call raises.
+
+Names follow the C ABI:
+  state_init(S, z=None)                        zero a state        (la_state_init)
+  chunk_fwd(q, k, v, gamma, ...)               prefill / forward   (la_chunk_fwd)
+  recurrent_step(q, k, v, gamma, S, z, ...)    one decode step     (la_recurrent_step)
+  workspace_size(...)                          scratch bytes       (la_workspace_size)
+  chunk_fwd_host(...)                          la_chunk_fwd on host buffers, copies included
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import _build
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
+LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL = 1, 2, 4
+
+LIBRARY_PATH = _build.LIBRARY
+_LIB = None
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def _load() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIBRARY_PATH):
+        raise RuntimeError(
+            f"{LIBRARY_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`"
+            " (or retnet_retention_gb300/_build.py) first")
+    lib = ctypes.CDLL(LIBRARY_PATH)
+    vp, i, u, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
+    lib.la_status_string.argtypes = [i]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_abi_version.restype = i
+    lib.la_workspace_size.argtypes = [i, i, i, i, i, i, u, i]
+    lib.la_workspace_size.restype = sz
+    lib.la_state_init.argtypes = [vp, vp, i, i, i, i, vp]
+    lib.la_state_init.restype = i
+    lib.la_chunk_fwd.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp, vp, i,
+                                 vp, sz, vp, vp]
+    lib.la_chunk_fwd.restype = i
+    lib.la_recurrent_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, u, f, vp, vp, vp, vp, vp]
+    lib.la_recurrent_step.restype = i
+    _LIB = lib
+    return lib
+
+
+def library() -> ctypes.CDLL:
+    """The loaded liblinattn.so (raises if it is not built)."""
+    return _load()
+
+
+def status_string(status: int) -> str:
+    return _load().la_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_load().la_abi_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return LA_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _flags(phi: bool, normalize: bool, causal: bool) -> int:
+    return (LA_PHI_ELU1 if phi else 0) | (LA_NORMALIZE if normalize else 0) | (
+        0 if causal else LA_NONCAUSAL)
+
+
+def _ptr(t) -> int | None:
+    """Device address of a contiguous CUDA tensor (None passes through)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("liblinattn takes CUDA device tensors (use chunk_fwd_host for host data)")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to liblinattn must be contiguous")
+    return t.data_ptr()
+
+
+def _gamma_host(gamma, H: int) -> np.ndarray:
+    if isinstance(gamma, torch.Tensor):
+        gamma = gamma.detach().to("cpu", torch.float32).numpy()
+    g = np.ascontiguousarray(np.broadcast_to(np.asarray(gamma, dtype=np.float32).reshape(-1),
+                                             (H,)), dtype=np.float32)
+    return g
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _check(status: int, what: str):
+    if status != LA_OK:
+        raise LinAttnError(status, what)
+
+
+def workspace_size(B, H, T, dk, dv, dtype=torch.bfloat16, phi=False, normalize=False,
+                   causal=True, chunk=0) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(_load().la_workspace_size(B, H, T, dk, dv, code, _flags(phi, normalize, causal),
+                                         chunk))
+
+
+def state_init(S: torch.Tensor, z: torch.Tensor | None = None, stream=None):
+    """Zero S [B,H,dk,dv] (and z [B,H,dk]) on the device."""
+    B, H, dk, dv = S.shape
+    _check(_load().la_state_init(_ptr(S), _ptr(z), B, H, dk, dv, _stream(stream)),
+           "la_state_init")
+
+
+def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
+              S0=None, z0=None, chunk=0, out=None, S_out=None, z_out=None, return_state=True,
+              workspace=None, dev_status=None, stream=None):
+    """Chunkwise forward over [B,H,T,d] device tensors.
+
+    Returns (O, S_T, z_T); S_T / z_T are None when return_state is False and
+    no output buffer was given.  z_T is returned when normalising (or when
+    z_out is given).
+    """
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    dt = _dtype_code(q)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    if return_state and normalize and z_out is None:
+        z_out = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+    g = _gamma_host(gamma, H)
+    flags = _flags(phi, normalize, causal)
+    lib = _load()
+    need = int(lib.la_workspace_size(B, H, T, dk, dv, dt, flags, chunk))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), dt, g.ctypes.data, B, H, T, dk, dv, flags,
+                          float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out), _ptr(z_out),
+                          int(chunk), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                          _stream(stream))
+    _check(st, "la_chunk_fwd")
+    return out, S_out, z_out
+
+
+def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps=1e-6,
+                   out=None, dev_status=None, stream=None):
+    """One decode step on [B,H,d] device tensors; S (and z) are updated in place."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    g = _gamma_host(gamma, H)
+    st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
+                                   H, dk, dv, _flags(phi, normalize, True), float(eps), _ptr(S),
+                                   _ptr(z), _ptr(out), _ptr(dev_status), _stream(stream))
+    _check(st, "la_recurrent_step")
+    return out
+
+
+def chunk_fwd_host(q, k, v, gamma, *, device="cuda", stream=None, **kw):
+    """la_chunk_fwd on HOST tensors: copy in, compute, copy the results back.
+
+    q, k, v should be pinned CPU tensors for asynchronous copies.  Returns
+    CPU (O, S_T, z_T).  The stream is synchronised before returning.
+    """
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        qd = q.to(device, non_blocking=True)
+        kd = k.to(device, non_blocking=True)
+        vd = v.to(device, non_blocking=True)
+        O, S_T, z_T = chunk_fwd(qd, kd, vd, gamma, stream=s, **kw)
+        Oh = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        Oh.copy_(O, non_blocking=True)
+        Sh = None
+        if S_T is not None:
+            Sh = torch.empty(S_T.shape, dtype=S_T.dtype, pin_memory=True)
+            Sh.copy_(S_T, non_blocking=True)
+        zh = None
+        if z_T is not None:
+            zh = torch.empty(z_T.shape, dtype=z_T.dtype, pin_memory=True)
+            zh.copy_(z_T, non_blocking=True)
+    s.synchronize()
+    return Oh, Sh, zh
+
+
+__all__ = ["chunk_fwd", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
+           "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
+           "LA_NORMALIZE", "LA_NONCAUSAL"]

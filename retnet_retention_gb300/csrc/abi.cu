@@ -1,0 +1,175 @@
+// The exported C ABI of liblinattn.so (declared in include/linattn.h):
+// argument checks on the host, then asynchronous launches on the caller's
+// stream.  Nothing is launched or written when a check fails.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "launch.h"
+
+using namespace la;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dim(int d) { return d >= 16 && d <= 256 && d % 16 == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Fills the per-head decay block; returns false if any gamma is outside (0, 1].
+bool fill_gammas(const float* gamma, int H, KernelGammas* g, bool* all_one) {
+    std::memset(g, 0, sizeof(*g));
+    *all_one = true;
+    for (int h = 0; h < H; ++h) {
+        float x = gamma[h];
+        if (!(x > 0.f && x <= 1.f)) return false;  // also rejects NaN
+        g->gamma[h] = x;
+        g->log2g[h] = (float)std::log2((double)x);
+        if (x != 1.f) *all_one = false;
+    }
+    return true;
+}
+
+la_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+size_t elem_size(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char* la_status_string(int status) {
+    switch (status) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported combination";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int la_abi_version(void) { return LA_ABI_VERSION; }
+
+size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                         int chunk) {
+    (void)B; (void)H; (void)T; (void)d_k; (void)d_v; (void)dtype; (void)flags; (void)chunk;
+    return 0;
+}
+
+la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_stream_t stream) {
+    if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
+    if ((size_t)B * H == 0) return LA_OK;
+    if (!S || !aligned16(S) || (z && !aligned16(z))) return LA_ERR_INVALID_ARG;
+    const size_t nbh = (size_t)B * H;
+    return cuda_status(launch_state_zero(S, z, nbh * d_k * d_v, z ? nbh * d_k : 0,
+                                         (cudaStream_t)stream));
+}
+
+la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
+                       const float* gamma, int B, int H, int T, int d_k, int d_v,
+                       unsigned flags, float eps, const float* S0, const float* z0, void* O,
+                       float* S_out, float* z_out, int chunk, void* workspace,
+                       size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL)) return LA_ERR_INVALID_ARG;
+    if (!(chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128))
+        return LA_ERR_INVALID_ARG;
+    if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+    const size_t nbh = (size_t)B * H;
+    if (nbh == 0) return LA_OK;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    KernelGammas g;
+    bool all_one = true;
+    if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
+    const bool noncausal = (flags & LA_NONCAUSAL) != 0;
+    const bool normalize = (flags & LA_NORMALIZE) != 0;
+    if (noncausal && (!all_one || S0 || z0)) return LA_ERR_UNSUPPORTED;
+
+    const size_t es = elem_size(dtype);
+    const size_t n_qk = nbh * (size_t)T * d_k * es, n_v = nbh * (size_t)T * d_v * es;
+    if (T > 0) {
+        if (!Q || !K || !V || !O) return LA_ERR_INVALID_ARG;
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+            return LA_ERR_INVALID_ARG;
+        if (overlaps(O, n_v, Q, n_qk) || overlaps(O, n_v, K, n_qk) || overlaps(O, n_v, V, n_v))
+            return LA_ERR_INVALID_ARG;
+    }
+    for (const void* p : {(const void*)S0, (const void*)z0, (const void*)S_out,
+                          (const void*)z_out, (const void*)workspace})
+        if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+    if (workspace_bytes < la_workspace_size(B, H, T, d_k, d_v, dtype, flags, chunk))
+        return LA_ERR_INVALID_ARG;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t nS = nbh * d_k * d_v, nz = nbh * d_k;
+    if (T == 0) {  // empty sequence: the final state is the initial one
+        cudaError_t e = cudaSuccess;
+        if (S_out) e = S0 ? launch_state_copy(S_out, S0, nS, s) : launch_state_zero(S_out, nullptr, nS, 0, s);
+        if (e == cudaSuccess && z_out)
+            e = z0 ? launch_state_copy(z_out, z0, nz, s) : launch_state_zero(z_out, nullptr, nz, 0, s);
+        return cuda_status(e);
+    }
+
+    ChunkArgs a;
+    a.Q = Q; a.K = K; a.V = V; a.O = O;
+    a.S0 = S0; a.z0 = z0; a.S_out = S_out; a.z_out = z_out;
+    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v;
+    a.chunk = chunk;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.normalize = normalize;
+    a.noncausal = noncausal;
+    a.eps = eps;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.dev_status = dev_status;
+    return cuda_status(launch_chunk_simt(a, g, s));
+}
+
+la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
+                            const float* gamma, int B, int H, int d_k, int d_v, unsigned flags,
+                            float eps, float* S, float* z, void* o, int* dev_status,
+                            la_stream_t stream) {
+    (void)dev_status;  // the decode step has no device-side waits
+    if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL)) return LA_ERR_INVALID_ARG;
+    if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
+    if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+    const size_t nbh = (size_t)B * H;
+    if (nbh == 0) return LA_OK;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    KernelGammas g;
+    bool all_one = true;
+    if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
+    const bool normalize = (flags & LA_NORMALIZE) != 0;
+    if (!q || !k || !v || !o || !S || (normalize && !z)) return LA_ERR_INVALID_ARG;
+    for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
+                          (const void*)S, (const void*)z})
+        if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    const size_t n_o = nbh * d_v * es;
+    if (overlaps(o, n_o, q, nbh * d_k * es) || overlaps(o, n_o, k, nbh * d_k * es) ||
+        overlaps(o, n_o, v, n_o) || overlaps(o, n_o, S, nbh * d_k * d_v * 4))
+        return LA_ERR_INVALID_ARG;
+
+    StepArgs a;
+    a.q = q; a.k = k; a.v = v; a.o = o; a.S = S; a.z = normalize ? z : nullptr;
+    a.B = B; a.H = H; a.dk = d_k; a.dv = d_v;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.normalize = normalize;
+    a.eps = eps;
+    return cuda_status(launch_decode_step(a, g, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// Recurrent decode step (one token for every (b, h)), state updated in place:
+//
+//   S = gamma S + phi(k) v^T ;  z = gamma z + phi(k) ;  o = phi(q)^T S [/ (phi(q)^T z + eps)]
+//
+// "RetNet" (bembew), "Recurrent Representation"; "Linear attention"
+// (zerotofrontier 21.2), the decode step: update first, then read.
+//
+// The step is bound by HBM: every call reads and writes the whole fp32 state
+// (d_k * d_v * 8 bytes per head) and does 4 d_k d_v flops per head.  One CTA
+// owns one (b, h) state block.  Each thread owns 4 consecutive value columns
+// (a float4) of a set of rows, so a warp reads whole 512-byte row segments;
+// rows are streamed in batches of 8 float4 loads per thread that are issued
+// before any of them is used, keeping ~32 KB per CTA in flight.  The
+// read-out sum over d_k is a register accumulation followed by a shared-
+// memory reduction across the row slots.
+#include "launch.h"
+
+namespace la {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBatch = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) decode_step_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int H, int dk, int dv,
+    int phi, int normalize, float eps, const __grid_constant__ KernelGammas g) {
+    __shared__ float qf[256];
+    __shared__ float kf[256];
+    __shared__ float red[kThreads * 4];
+    __shared__ float den_part[kThreads / 32];
+
+    const int bh = blockIdx.x;
+    const int h = bh % H;
+    const float gam = g.gamma[h];
+    const int tid = threadIdx.x;
+
+    if (tid < dk) {
+        float qv = load_elem(q, (size_t)bh * dk + tid);
+        float kv = load_elem(k, (size_t)bh * dk + tid);
+        qf[tid] = phi ? phi_elu1(qv) : qv;
+        kf[tid] = phi ? phi_elu1(kv) : kv;
+    }
+
+    const int tpr = dv >> 2;           // threads per state row
+    const int rpi = kThreads / tpr;    // rows per pass over the block
+    const int cg = tid % tpr;          // my float4 column group
+    const int rs = tid / tpr;          // my first row
+    float vv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) vv[c] = load_elem(v, (size_t)bh * dv + cg * 4 + c);
+    __syncthreads();
+
+    float4* Sb = reinterpret_cast<float4*>(S + (size_t)bh * dk * dv);
+    const int row4 = dv >> 2;  // float4 per row
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+
+    for (int i0 = rs; i0 < dk; i0 += rpi * kBatch) {
+        float4 s[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            int i = i0 + u * rpi;
+            if (i < dk) s[u] = __ldcs(Sb + (size_t)i * row4 + cg);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            int i = i0 + u * rpi;
+            if (i < dk) {
+                const float kk = kf[i], qq = qf[i];
+                float4 x = s[u];
+                x.x = fmaf(gam, x.x, kk * vv[0]);
+                x.y = fmaf(gam, x.y, kk * vv[1]);
+                x.z = fmaf(gam, x.z, kk * vv[2]);
+                x.w = fmaf(gam, x.w, kk * vv[3]);
+                __stcs(Sb + (size_t)i * row4 + cg, x);
+                acc[0] = fmaf(qq, x.x, acc[0]);
+                acc[1] = fmaf(qq, x.y, acc[1]);
+                acc[2] = fmaf(qq, x.z, acc[2]);
+                acc[3] = fmaf(qq, x.w, acc[3]);
+            }
+        }
+    }
+    // red[rs][col] for the rpi row slots
+#pragma unroll
+    for (int c = 0; c < 4; ++c) red[rs * dv + cg * 4 + c] = acc[c];
+
+    float den = 1.f;
+    if (normalize) {
+        float part = 0.f;
+        if (tid < dk) {
+            float* zb = z + (size_t)bh * dk;
+            float zi = fmaf(gam, zb[tid], kf[tid]);
+            zb[tid] = zi;
+            part = qf[tid] * zi;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if ((tid & 31) == 0) den_part[tid >> 5] = part;
+    }
+    __syncthreads();
+    if (normalize) {
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) d += den_part[w];
+        den = d + eps;
+    }
+    for (int j = tid; j < dv; j += kThreads) {
+        float sum = 0.f;
+        for (int r = 0; r < rpi; ++r) sum += red[r * dv + j];
+        store_elem(o, (size_t)bh * dv + j, normalize ? sum / den : sum);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStream_t s) {
+    const size_t nbh = (size_t)a.B * a.H;
+    if (nbh == 0) return cudaSuccess;
+    if (nbh > 0x7fffffffu) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)nbh);
+    if (a.bf16) {
+        decode_step_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+            (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+            (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, a.normalize, a.eps, g);
+    } else {
+        decode_step_kernel<float><<<grid, kThreads, 0, s>>>(
+            (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.o, a.S, a.z,
+            a.H, a.dk, a.dv, a.phi, a.normalize, a.eps, g);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace la

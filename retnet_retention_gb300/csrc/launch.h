@@ -1,0 +1,59 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+// Nothing here is exported from liblinattn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace la {
+
+// Arguments of one chunkwise forward, already validated by the ABI layer.
+struct ChunkArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* O;
+    const float* S0;  // may be null
+    const float* z0;  // may be null
+    float* S_out;     // may be null
+    float* z_out;     // may be null
+    int B, H, T, dk, dv;
+    int chunk;        // requested chunk length (0 = auto)
+    bool bf16;
+    bool phi;
+    bool normalize;
+    bool noncausal;
+    float eps;
+    void* workspace;
+    size_t workspace_bytes;
+    int* dev_status;
+};
+
+struct StepArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* S;
+    float* z;  // null unless normalising
+    int B, H, dk, dv;
+    bool bf16;
+    bool phi;
+    bool normalize;
+    float eps;
+};
+
+// state.cu
+cudaError_t launch_state_zero(float* S, float* z, size_t n_S, size_t n_z, cudaStream_t s);
+cudaError_t launch_state_copy(float* dst, const float* src, size_t n, cudaStream_t s);
+
+// decode.cu
+cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStream_t s);
+
+// chunk_simt.cu: the fp32 SIMT chunkwise kernel (any supported shape)
+cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s);
+int simt_chunk_len(int requested, int dk);
+
+}  // namespace la

@@ -1,0 +1,144 @@
+"""The C ABI on the host: the library loads, exports what include/linattn.h
+declares, and rejects bad arguments before launching anything.
+
+These tests make no compute call: every call below fails its host-side
+checks (or is a pure size query), so they run without a GPU.  Device
+pointers are fake, aligned or misaligned integers that are never touched.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import retnet_retention_gb300 as la
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "linattn.h")
+
+FAKE = 0x10000000  # an aligned address that is never dereferenced
+GAM = np.full(8, 0.9, dtype=np.float32)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from retnet_retention_gb300 import _build
+    _build.build()
+    return la.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"LA_API\s+[\w\s\*]+?\b(la_\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    assert set(names) >= {"la_state_init", "la_chunk_fwd", "la_recurrent_step",
+                          "la_workspace_size", "la_status_string", "la_abi_version"}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in linattn.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    assert la.abi_version() == 1
+    for code in range(5):
+        assert la.status_string(code)
+    assert la.status_string(77) == "unknown status"
+
+
+def chunk(lib, **over):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dtype=1, gamma=GAM.ctypes.data, B=2,
+             H=8, T=64, dk=64, dv=64, flags=0, eps=1e-6, S0=None, z0=None, O=FAKE + 0x400000,
+             S_out=None, z_out=None, chunk=0, ws=None, ws_bytes=0, st=None, stream=None)
+    a.update(over)
+    return lib.la_chunk_fwd(a["Q"], a["K"], a["V"], a["dtype"], a["gamma"], a["B"], a["H"],
+                            a["T"], a["dk"], a["dv"], a["flags"], a["eps"], a["S0"], a["z0"],
+                            a["O"], a["S_out"], a["z_out"], a["chunk"], a["ws"], a["ws_bytes"],
+                            a["st"], a["stream"])
+
+
+BAD_CHUNK_ARGS = [
+    dict(B=-1), dict(H=-2), dict(T=-1), dict(dk=0), dict(dk=8), dict(dk=24), dict(dk=272),
+    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=8), dict(chunk=48), dict(chunk=256),
+    dict(eps=float("nan")), dict(eps=-1.0), dict(Q=None), dict(V=None), dict(O=None),
+    dict(Q=FAKE + 8), dict(O=FAKE + 0x400004), dict(S0=FAKE + 0x800004),
+    dict(O=FAKE + 0x100000),  # O overlaps K
+    dict(H=300, gamma=np.full(300, 0.9, dtype=np.float32).ctypes.data),
+]
+
+
+@pytest.mark.parametrize("over", BAD_CHUNK_ARGS, ids=lambda d: ",".join(f"{k}" for k in d))
+def test_chunk_fwd_rejects(lib, over):
+    assert chunk(lib, **over) == la.LA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [0.0, -0.5, 1.0001, float("nan"), float("inf")])
+def test_chunk_fwd_rejects_gamma(lib, bad):
+    g = GAM.copy()
+    g[3] = bad
+    assert chunk(lib, gamma=g.ctypes.data) == la.LA_ERR_INVALID_ARG
+
+
+def test_noncausal_needs_gamma_one_and_no_state(lib):
+    ones = np.ones(8, dtype=np.float32)
+    assert chunk(lib, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED  # gamma 0.9
+    assert chunk(lib, flags=la.LA_NONCAUSAL, gamma=ones.ctypes.data,
+                 S0=FAKE + 0x800000) == la.LA_ERR_UNSUPPORTED
+
+
+def test_empty_batch_is_a_noop(lib):
+    # B == 0: nothing to do, no pointer is needed
+    assert chunk(lib, B=0, Q=None, K=None, V=None, O=None, gamma=None) == la.LA_OK
+
+
+def test_workspace_size_is_a_host_query(lib):
+    for (B, H, T, dk, dv) in [(4, 8, 4096, 64, 64), (8, 16, 8192, 128, 256),
+                              (1, 8, 65536, 128, 128), (0, 1, 1, 16, 16)]:
+        n = lib.la_workspace_size(B, H, T, dk, dv, 1, 0, 0)
+        assert n >= 0 and n % 16 == 0
+
+
+def step(lib, **over):
+    a = dict(q=FAKE, k=FAKE + 0x1000, v=FAKE + 0x2000, dtype=1, gamma=GAM.ctypes.data, B=2, H=8,
+             dk=64, dv=64, flags=0, eps=1e-6, S=FAKE + 0x100000, z=None, o=FAKE + 0x200000,
+             st=None, stream=None)
+    a.update(over)
+    return lib.la_recurrent_step(a["q"], a["k"], a["v"], a["dtype"], a["gamma"], a["B"], a["H"],
+                                 a["dk"], a["dv"], a["flags"], a["eps"], a["S"], a["z"], a["o"],
+                                 a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [dict(B=-1), dict(dk=20), dict(dv=512), dict(S=None),
+                                  dict(o=None), dict(flags=la.LA_NORMALIZE),  # z missing
+                                  dict(q=FAKE + 2), dict(S=FAKE + 0x100008), dict(dtype=5),
+                                  dict(o=FAKE + 0x100000)],  # o overlaps S
+                         ids=lambda d: ",".join(d))
+def test_recurrent_step_rejects(lib, over):
+    assert step(lib, **over) == la.LA_ERR_INVALID_ARG
+
+
+def test_recurrent_step_noncausal_unsupported(lib):
+    assert step(lib, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
+
+
+def test_state_init_rejects(lib):
+    assert lib.la_state_init(None, None, 2, 2, 64, 64, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_state_init(FAKE + 4, None, 2, 2, 64, 64, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_state_init(FAKE, None, 2, 2, 63, 64, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_state_init(None, None, 0, 2, 64, 64, None) == la.LA_OK
+
+
+def test_python_binding_refuses_host_tensors():
+    """Host tensors never reach the library (their addresses are not device memory)."""
+    import torch
+    q = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(ValueError):
+        la.chunk_fwd(q, q, q, [0.5], out=q.clone(), return_state=False)
+    with pytest.raises(ValueError):
+        la.recurrent_step(q[:, :, 0], q[:, :, 0], q[:, :, 0], [0.5], torch.zeros(1, 1, 16, 16),
+                          out=q[:, :, 0].clone())
