@@ -251,7 +251,9 @@ def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> 
     k = x["k"].reshape(B, H, c["T"], c["dk"]).to(dev)
     v = x["v"].reshape(B, H, c["T"], c["dv"]).to(dev)
     _, S, _ = la.chunk_fwd(q, k, v, x["gamma"])
-    del q, k, v
+    torch.cuda.synchronize()
+    del q, k, v, x
+    torch.cuda.empty_cache()
     # every decode step's own inputs, resident before timing
     d = workloads.decode_inputs_all(cw, steps_total)
     bsl = slice(rank * B, (rank + 1) * B)
@@ -328,6 +330,19 @@ def run_ours(args) -> dict | None:
         return float(t.item())
 
     pk = peaks()
+    only = args.only
+    if only == "decode":  # profiling aid: the decode workload alone
+        dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
+        if rank == 0:
+            print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
+                              "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
+        return None
+    if only in ("msr_retention_bf16", "long_retention_bf16"):  # profiling aid
+        r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
+        if rank == 0:
+            print(json.dumps({"only": only, "ms_per_step": r["ms"],
+                              "alg_gbs": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9}))
+        return None
     barrier()
     sampler = ClockSampler(local)
     with sampler:
@@ -336,13 +351,13 @@ def run_ours(args) -> dict | None:
     head_ms = max_over_ranks(head["ms"])
     e2e_ms = max_over_ranks(head["e2e_ms"])
     others = {}
-    if not args.headline_only:
+    headline_only = args.headline_only or only == "headline"
+    if not headline_only:
         for name in ("msr_retention_bf16", "long_retention_bf16"):
             r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             others[name] = r
-        dec = decode_measure(la, workloads.CONFIGS["decode_bf16"]["decode_steps"],
-                             args.warmup, rank, world)
+        dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         dec["ms"] = max_over_ranks(dec["ms"])
     if rank != 0:
         if dist is not None:
@@ -394,7 +409,7 @@ def run_ours(args) -> dict | None:
         },
         "gpu_launches": args.steps,
     }
-    if not args.headline_only:
+    if not headline_only:
         sub = {}
         for name, r in others.items():
             rc = r["config"]
@@ -472,6 +487,12 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
+                                       "decode"), default=None,
+                    help="profiling aid: run one workload only")
+    ap.add_argument("--decode-steps", type=int,
+                    default=workloads.CONFIGS["decode_bf16"]["decode_steps"],
+                    help="decode steps to time (the workload has 1024)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -9,8 +9,9 @@
 // (d_k * d_v * 8 bytes per head) and does 4 d_k d_v flops per head.  One CTA
 // owns one (b, h) state block.  Each thread owns 4 consecutive value columns
 // (a float4) of a set of rows, so a warp reads whole 512-byte row segments;
-// rows are streamed in batches of 8 float4 loads per thread that are issued
-// before any of them is used, keeping ~32 KB per CTA in flight.  The
+// rows are streamed in batches of 16 float4 loads per thread that are issued
+// before any of them is used (the first batch even before q, k, v are read),
+// keeping up to 64 KB per CTA in flight.  The
 // read-out sum over d_k is a register accumulation followed by a shared-
 // memory reduction across the row slots.
 #include "launch.h"
@@ -20,10 +21,10 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 8;
+constexpr int kBatch = 16;
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) decode_step_kernel(
+__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int H, int dk, int dv,
     int phi, int normalize, float eps, const __grid_constant__ KernelGammas g) {
@@ -36,34 +37,34 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(
     const int h = bh % H;
     const float gam = g.gamma[h];
     const int tid = threadIdx.x;
+    const int tpr = dv >> 2;           // threads per state row
+    const int rpi = kThreads / tpr;    // rows per pass over the block
+    const int cg = tid % tpr;          // my float4 column group
+    const int rs = tid / tpr;          // my first row
+    const int row4 = dv >> 2;          // float4 per row
+    float4* Sb = reinterpret_cast<float4*>(S + (size_t)bh * dk * dv);
 
+    // The state block is the only large read: issue the first batch of its
+    // loads before anything else so their latency overlaps the q/k/v loads.
+    float4 s[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+        int i = rs + u * rpi;
+        if (i < dk) s[u] = __ldcs(Sb + (size_t)i * row4 + cg);
+    }
     if (tid < dk) {
         float qv = load_elem(q, (size_t)bh * dk + tid);
         float kv = load_elem(k, (size_t)bh * dk + tid);
         qf[tid] = phi ? phi_elu1(qv) : qv;
         kf[tid] = phi ? phi_elu1(kv) : kv;
     }
-
-    const int tpr = dv >> 2;           // threads per state row
-    const int rpi = kThreads / tpr;    // rows per pass over the block
-    const int cg = tid % tpr;          // my float4 column group
-    const int rs = tid / tpr;          // my first row
     float vv[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) vv[c] = load_elem(v, (size_t)bh * dv + cg * 4 + c);
     __syncthreads();
 
-    float4* Sb = reinterpret_cast<float4*>(S + (size_t)bh * dk * dv);
-    const int row4 = dv >> 2;  // float4 per row
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-
-    for (int i0 = rs; i0 < dk; i0 += rpi * kBatch) {
-        float4 s[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            int i = i0 + u * rpi;
-            if (i < dk) s[u] = __ldcs(Sb + (size_t)i * row4 + cg);
-        }
+    for (int i0 = rs;; ) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             int i = i0 + u * rpi;
@@ -80,6 +81,14 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(
                 acc[2] = fmaf(qq, x.z, acc[2]);
                 acc[3] = fmaf(qq, x.w, acc[3]);
             }
+        }
+        i0 += rpi * kBatch;
+        if (i0 >= dk) break;
+        // next batch (only when d_k * d_v > 1024 * kBatch)
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            int i = i0 + u * rpi;
+            if (i < dk) s[u] = __ldcs(Sb + (size_t)i * row4 + cg);
         }
     }
     // red[rs][col] for the rpi row slots
