@@ -92,7 +92,16 @@ LA_API int la_abi_version(void);
  * 0 for arguments la_chunk_fwd would reject).  `chunk` as for la_chunk_fwd.
  */
 LA_API size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
-                         unsigned flags, int chunk);
+                                unsigned flags, int chunk);
+
+/*
+ * Number of kernels la_chunk_fwd enqueues for these arguments on the current
+ * device (1 for the single-pass paths; 3 when a long sequence is split into
+ * segments: segment states, the scan over them, the outputs).  0 for
+ * arguments la_chunk_fwd would reject or T == 0.  Pure host query.
+ */
+LA_API int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
+                                 unsigned flags, int chunk);
 
 /*
  * Zero-fill a state: S[B][H][d_k][d_v] and, if not NULL, z[B][H][d_k].
@@ -102,7 +111,7 @@ LA_API size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype 
  * pointer; LA_ERR_CUDA if the launch fails.  B or H == 0 is a no-op.
  */
 LA_API la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v,
-                        la_stream_t stream);
+                               la_stream_t stream);
 
 /*
  * Chunkwise forward over whole sequences (prefill / training forward):
@@ -140,12 +149,12 @@ LA_API la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_
  * too small, O overlapping an input); LA_ERR_UNSUPPORTED; LA_ERR_CUDA.
  */
 LA_API la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
-                       const float* gamma, int B, int H, int T, int d_k, int d_v,
-                       unsigned flags, float eps,
-                       const float* S0, const float* z0,
-                       void* O, float* S_out, float* z_out,
-                       int chunk, void* workspace, size_t workspace_bytes,
-                       int* dev_status, la_stream_t stream);
+                              const float* gamma, int B, int H, int T, int d_k, int d_v,
+                              unsigned flags, float eps,
+                              const float* S0, const float* z0,
+                              void* O, float* S_out, float* z_out,
+                              int chunk, void* workspace, size_t workspace_bytes,
+                              int* dev_status, la_stream_t stream);
 
 /*
  * One recurrent decode step for every (b, h), updating the state in place:
@@ -163,10 +172,10 @@ LA_API la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dt
  * Errors: as la_chunk_fwd.
  */
 LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
-                            const float* gamma, int B, int H, int d_k, int d_v,
-                            unsigned flags, float eps,
-                            float* S, float* z, void* o,
-                            int* dev_status, la_stream_t stream);
+                                   const float* gamma, int B, int H, int d_k, int d_v,
+                                   unsigned flags, float eps,
+                                   float* S, float* z, void* o,
+                                   int* dev_status, la_stream_t stream);
 
 #ifdef __cplusplus
 }

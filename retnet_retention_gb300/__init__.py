@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
     lib.la_chunk_fwd.restype = i
     lib.la_recurrent_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, u, f, vp, vp, vp, vp, vp]
     lib.la_recurrent_step.restype = i
+    lib.la_chunk_fwd_launches.argtypes = [i, i, i, i, i, i, u, i]
+    lib.la_chunk_fwd_launches.restype = i
     _LIB = lib
     return lib
 

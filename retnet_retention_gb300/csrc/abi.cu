@@ -3,6 +3,7 @@
 // stream.  Nothing is launched or written when a check fails.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "launch.h"
@@ -56,10 +57,41 @@ const char* la_status_string(int status) {
 
 int la_abi_version(void) { return LA_ABI_VERSION; }
 
+// The arguments la_chunk_fwd's path choice depends on (pointers are irrelevant).
+static ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                           int chunk) {
+    ChunkArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.normalize = (flags & LA_NORMALIZE) != 0;
+    a.noncausal = (flags & LA_NONCAUSAL) != 0;
+    return a;
+}
+
+static bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags) {
+    return B > 0 && H > 0 && T > 0 && valid_dim(d_k) && valid_dim(d_v) && H <= kMaxHeads &&
+           (dtype == LA_DTYPE_F32 || dtype == LA_DTYPE_BF16) &&
+           !(flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL));
+}
+
 size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
                          int chunk) {
-    (void)B; (void)H; (void)T; (void)d_k; (void)d_v; (void)dtype; (void)flags; (void)chunk;
-    return 0;
+    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags)) return 0;
+    ChunkArgs a = plan_args(B, H, T, d_k, d_v, dtype, flags, chunk);
+    const char* pin = std::getenv("LA_CHUNK_PATH");
+    if ((pin && std::strcmp(pin, "simt") == 0) || !tc_supported(a)) return 0;
+    return tc_workspace_bytes(B, H, T, d_k, d_v, a.noncausal);
+}
+
+int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                          int chunk) {
+    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags)) return 0;
+    ChunkArgs a = plan_args(B, H, T, d_k, d_v, dtype, flags, chunk);
+    const char* pin = std::getenv("LA_CHUNK_PATH");
+    if ((pin && std::strcmp(pin, "simt") == 0) || !tc_supported(a)) return 1;
+    return tc_workspace_bytes(B, H, T, d_k, d_v, a.noncausal) > 0 ? 3 : 1;
 }
 
 la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_stream_t stream) {
@@ -131,6 +163,16 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.dev_status = dev_status;
+    // LA_CHUNK_PATH=simt|tc pins the path (tests compare both); default: tensor
+    // cores whenever the shape allows, the fp32 CUDA-core kernel otherwise.
+    const char* pin = std::getenv("LA_CHUNK_PATH");
+    const bool want_simt = pin && std::strcmp(pin, "simt") == 0;
+    const bool want_tc = pin && std::strcmp(pin, "tc") == 0;
+    if (!want_simt && tc_supported(a)) {
+        int launches = 0;
+        return cuda_status(launch_chunk_tc(a, g, s, &launches));
+    }
+    if (want_tc) return LA_ERR_UNSUPPORTED;
     return cuda_status(launch_chunk_simt(a, g, s));
 }
 

@@ -1,0 +1,766 @@
+// Chunkwise forward on the tcgen05 tensor cores (bf16 inputs, fp32
+// accumulation), sm_103a.
+//
+// "Chunked Recurrent Representation" ("RetNet", bembew): chunks of C = 128
+// tokens; inside a chunk the parallel form (Q K^T . D) V, across chunks the
+// carried state S.  Written out from the recurrence (the pages give the
+// chunkwise form only in words), for a chunk of L <= C rows, local indices
+// i (query) and j (key), entry state S_{c-1}:
+//
+//   P_ij = (phi(q_i) . phi(k_j)) gamma^(i-j)   (j <= i, else 0)
+//   O_c  = P V_c + (xi . phi(Q_c)) S_{c-1}                 xi_i   = gamma^(i+1)
+//   S_c  = gamma^L S_{c-1} + (zeta . phi(K_c))^T V_c       zeta_j = gamma^(L-1-j)
+//   normaliser: den_i = sum_j P_ij + xi_i phi(q_i) . z_{c-1} + eps,
+//               z_c = gamma^L z_{c-1} + sum_j zeta_j phi(k_j)
+//
+// One CTA owns one unit: a (b, h) sequence, a block of DVB value columns and
+// a segment of consecutive chunks; it walks the chunks in order with S held
+// in tensor memory (fp32) the whole time.  Per chunk (all four contractions
+// on the tensor cores, M = 128):
+//   MMA1  scores = Q K^T            A = Q (K-major smem)   B = K (K-major smem)
+//   E1    P = bf16(scores . D)      tcgen05.ld -> mask -> tcgen05.st (P stays in TMEM)
+//   E3    S_bf16 = bf16(S) in smem; S = gamma^L S in TMEM
+//   MMA2  O = P V                   A = P (TMEM)           B = V (MN-major smem)
+//   MMA3  O += Q^ S_bf16            A = Q^ (K-major smem)  B = S_bf16 (MN-major smem)
+//   MMA4  S += K^^T V               A = K^ (MN-major smem) B = V (MN-major smem)
+//   E2    O -> bf16 -> global
+// Q, K, V arrive by TMA (128-byte swizzle) into a two-stage ring, so chunk
+// c+1 loads while chunk c computes.  Only non-negative powers of gamma are
+// used: small gamma underflows to 0 instead of overflowing.
+//
+// Unit kinds (one kernel, `mode`):
+//   kFull       outputs and state from an entry state (zero, S0 or a segment entry)
+//   kStateOnly  only the state walk (MMA4), from zero: a segment's own
+//               contribution sum_t gamma^(end-1-t) phi(k_t) v_t^T
+//   kNonCausal  gamma = 1: a state walk over the whole sequence, then every
+//               chunk reads the final summary (MMA3 only)
+//
+// Every wait on an mbarrier is bounded by a time limit; on expiry the CTA
+// records LA_ERR_TIMEOUT in dev_status, stops issuing work, frees its tensor
+// memory and returns.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;         // chunk length (= MMA M)
+constexpr int kThreads = 128;   // 4 warps: warp w owns TMEM lanes 32w .. 32w+31
+constexpr uint32_t kColP = 0;     // scores (fp32, 128 cols) then P (bf16 pairs, 64 cols)
+constexpr uint32_t kColO = 128;   // O accumulator (DVB cols), then the state S (DVB cols)
+constexpr uint32_t kBlk = 16384;  // one [128 rows x 64 bf16] swizzled block
+
+// TMEM columns: scores/P 128 + O DVB + S DVB, rounded up to a power of two
+// (256 for DVB = 64, so two CTAs can share an SM; 512 for DVB = 128).
+template <int DVB>
+struct Tmem {
+    static constexpr uint32_t kColS = kColO + DVB;
+    static constexpr uint32_t kCols = (128 + 2 * DVB) <= 256 ? 256 : 512;
+};
+
+enum Mode { kFull = 0, kStateOnly = 1, kNonCausal = 2 };
+
+struct TcParams {
+    CUtensorMap tmQ, tmK, tmV;  // [BH][T][d] bf16, box {64, 128, 1}, 128B swizzle
+    __nv_bfloat16* O;           // [BH][T][dv]
+    const float* S_in;          // entry states or nullptr (zero)
+    const float* z_in;
+    float* S_out;               // final states or nullptr
+    float* z_out;
+    int in_nseg;                // entry-state index = bh * in_nseg + seg
+    int out_nseg;               // exit-state index = bh * out_nseg + (out_last_only ? 0 : seg)
+    int out_last_only;
+    int H, T, dv;
+    int n_dvb;                  // value-column blocks per sequence
+    int seg_chunks;             // chunks per segment
+    int n_seg;                  // segments per sequence (this launch covers seg0 .. seg0+n_seg-1)
+    int mode;
+    int normalize;
+    int track_z;                // carry the normaliser state z (normalising, or z_out wanted)
+    int phi;
+    float eps;
+    int* dev_status;
+    unsigned long long wait_ns;
+    int force_timeout;
+    KernelGammas g;
+};
+
+template <int DK, int DVB>
+struct Layout {
+    static constexpr uint32_t kQ = (DK / 64) * kBlk;
+    static constexpr uint32_t kK = (DK / 64) * kBlk;
+    static constexpr uint32_t kV = (DVB / 64) * kBlk;
+    static constexpr uint32_t kStage = kQ + kK + kV;
+    static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // S_bf16, MN-major
+    static constexpr uint32_t oSB = 2 * kStage;
+    static constexpr uint32_t oPw = oSB + kSB;            // float pw[kC + 4]
+    static constexpr uint32_t oZ = oPw + (kC + 4) * 4;    // float z[DK]
+    static constexpr uint32_t oBar = oZ + DK * 4;         // 4 mbarriers
+    static constexpr uint32_t oSlot = oBar + 4 * 8;       // TMEM base address
+    static constexpr uint32_t kBytes = oSlot + 16;
+    static constexpr uint32_t kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ void record_status(int* st, int code) {
+    if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+// In-place pass over a [128 x 64*nblk] K-major swizzled tile: apply phi
+// (optional) and multiply row r by fac(r).  Rows are whole 128-byte lines,
+// so the swizzle never moves an element to another row.
+template <typename F>
+__device__ __forceinline__ void row_pass(char* tile, int nblk, bool apply_phi, F fac) {
+    const int n16 = nblk * (kBlk / 16);
+    for (int idx = threadIdx.x; idx < n16; idx += kThreads) {
+        const int r = (idx >> 3) & 127;
+        uint4* p = reinterpret_cast<uint4*>(tile) + idx;
+        uint4 u = *p;
+        const float f = fac(r);
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 x = __bfloat1622float2(h[e]);
+            if (apply_phi) {
+                x.x = phi_f(x.x);
+                x.y = phi_f(x.y);
+            }
+            h[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+        }
+        *p = u;
+    }
+}
+
+template <int DK, int DVB>
+__global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
+    using Lay = Layout<DK, DVB>;
+    constexpr uint32_t kColS = Tmem<DVB>::kColS;
+    constexpr uint32_t kTmemCols = Tmem<DVB>::kCols;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    float* pw = reinterpret_cast<float*>(sm + Lay::oPw);
+    float* zs = reinterpret_cast<float*>(sm + Lay::oZ);
+    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);  // [2]
+    uint64_t* bar_mma = bar_full + 2;
+    uint64_t* bar_never = bar_full + 3;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oSlot);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int unit = blockIdx.x;
+    const int seg = unit % p.n_seg;
+    const int dvb = (unit / p.n_seg) % p.n_dvb;
+    const int bh = unit / (p.n_seg * p.n_dvb);
+    const int h = bh % p.H;
+    const int v0 = dvb * DVB;
+    const float l2g = p.g.log2g[h];
+    const bool unit_gamma = p.g.gamma[h] == 1.0f;
+    const int n_chunks = (p.T + kC - 1) / kC;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = min(n_chunks, c_begin + p.seg_chunks);
+
+    if (tid == 0) {
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_never, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&p.tmQ);
+        prefetch_tensormap(&p.tmK);
+        prefetch_tensormap(&p.tmV);
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, kTmemCols);
+        tmem_relinquish();
+    }
+    for (int n = tid; n <= kC + 1; n += kThreads) pw[n] = gamma_pow(l2g, (float)n);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sbase = smem_addr(sm);
+
+    bool failed = false;
+    if (p.force_timeout) {  // test hook: a wait on a barrier nothing arrives on
+        if (tid == 0 && !mbar_wait(bar_never, 0, p.wait_ns)) record_status(p.dev_status, LA_ERR_TIMEOUT);
+        failed = true;
+    }
+
+    // ---- entry state: S rows d < DK into TMEM lanes, z into shared memory
+    if (!failed) {
+        const int sidx = bh * p.in_nseg + seg;
+        const bool has_in = p.S_in != nullptr && p.mode != kStateOnly && p.mode != kNonCausal;
+        for (int c0 = 0; c0 < DVB; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                float x = 0.f;
+                if (has_in && tid < DK)
+                    x = p.S_in[((size_t)sidx * DK + tid) * p.dv + v0 + c0 + e];
+                r[e] = __float_as_uint(x);
+            }
+            tmem_st32(tbase + lane_off + kColS + c0, r);
+        }
+        tmem_st_wait();
+        for (int d = tid; d < DK; d += kThreads)
+            zs[d] = (has_in && p.z_in) ? p.z_in[(size_t)sidx * DK + d] : 0.f;
+    }
+
+    const uint32_t kBytesQ = Lay::kQ, kBytesK = Lay::kK, kBytesV = Lay::kV;
+    const int z3 = bh;
+    // Issues the TMA loads of chunk c for walk `w` into stage s.
+    auto issue = [&](int c, int s, bool need_q, bool need_kv) {
+        char* st = sm + s * Lay::kStage;
+        uint32_t bytes = (need_q ? kBytesQ : 0) + (need_kv ? kBytesK + kBytesV : 0);
+        mbar_arrive_expect_tx(&bar_full[s], bytes);
+        const int y = c * kC;
+        if (need_q)
+            for (int b = 0; b < DK / 64; ++b) tma_load_3d(st + b * kBlk, &p.tmQ, b * 64, y, z3, &bar_full[s]);
+        if (need_kv) {
+            for (int b = 0; b < DK / 64; ++b)
+                tma_load_3d(st + Lay::kQ + b * kBlk, &p.tmK, b * 64, y, z3, &bar_full[s]);
+            for (int b = 0; b < DVB / 64; ++b)
+                tma_load_3d(st + Lay::kQ + Lay::kK + b * kBlk, &p.tmV, v0 + b * 64, y, z3, &bar_full[s]);
+        }
+    };
+
+    uint32_t full_phase[2] = {0, 0};
+    uint32_t mma_phase = 0;
+    bool inflight[2] = {false, false};  // a TMA fill of the stage not yet waited for
+    bool mma_inflight = false;          // MMAs committed but not yet waited for
+    // walk 0: the causal walk (or the state walk of kStateOnly / kNonCausal);
+    // walk 1: the non-causal read-out walk.
+    const int n_walks = p.mode == kNonCausal ? 2 : 1;
+    for (int walk = 0; walk < n_walks && !failed; ++walk) {
+        const bool do_out = (p.mode == kFull) || (p.mode == kNonCausal && walk == 1);
+        const bool do_intra = p.mode == kFull;
+        const bool do_state = (p.mode == kFull) || (p.mode == kStateOnly) ||
+                              (p.mode == kNonCausal && walk == 0);
+        const bool need_q = do_out;
+        const bool need_kv = do_intra || do_state;
+        const int cb = p.mode == kNonCausal ? 0 : c_begin;
+        const int ce = p.mode == kNonCausal ? n_chunks : c_end;
+
+        if (p.mode == kNonCausal && walk == 1) {
+            // the summary is final: one bf16 copy of S for every read-out MMA
+            if (tid < DK) {
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e8 = 0; e8 < 32; e8 += 8) {
+                        const int v = c0 + e8;
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
+                        w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
+                        w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
+                        w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
+                        *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                  sw128_offset(tid, v & 63)) = w;
+                    }
+                }
+            } else {
+                for (int c0 = 0; c0 < DVB; c0 += 32) {  // keep the warp-wide ld collective
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                    tmem_ld_wait();
+                }
+            }
+            fence_proxy_async_smem();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+        }
+        if (cb >= ce) continue;
+        if (tid == 0) issue(cb, 0, need_q, need_kv);
+        inflight[0] = true;
+
+        for (int c = cb; c < ce; ++c) {
+            const int it = c - cb;
+            const int s = it & 1;
+            char* st = sm + s * Lay::kStage;
+            char* tQ = st;
+            char* tK = st + Lay::kQ;
+            const int L = min(kC, p.T - c * kC);
+            if (c + 1 < ce) {
+                if (tid == 0) issue(c + 1, s ^ 1, need_q, need_kv);
+                inflight[s ^ 1] = true;
+            }
+
+            bool to = !mbar_wait(&bar_full[s], full_phase[s], p.wait_ns);
+            if (__syncthreads_or(to)) {
+                failed = true;
+                break;
+            }
+            full_phase[s] ^= 1;
+            inflight[s] = false;
+            // phi on q and k (rows >= L zeroed: phi(0) = 1 must not leak in)
+            if (p.phi) {
+                if (need_q) row_pass(tQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; });
+                if (need_kv) row_pass(tK, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; });
+                fence_proxy_async_smem();
+            }
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+
+            float r_i = 0.f;  // row sum of P (normaliser)
+            if (do_intra) {
+                if (tid == 0) {
+                    // MMA1: scores[128 x 128] = Q K^T, K = DK
+                    const uint32_t id = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
+                        mma_ss(tbase + kColP, smem_desc_sw128(sbase + (uint32_t)(tQ - sm) + off, 16, 1024),
+                               smem_desc_sw128(sbase + (uint32_t)(tK - sm) + off, 16, 1024), id, kk > 0);
+                    }
+                    mma_commit(bar_mma);
+                }
+                mma_inflight = true;
+                to = !mbar_wait(bar_mma, mma_phase, p.wait_ns);
+                if (__syncthreads_or(to)) {
+                    failed = true;
+                    break;
+                }
+                mma_phase ^= 1;
+                mma_inflight = false;
+                fence_after_sync();
+                // E1: row i = tid: P_ij = s_ij gamma^(i-j) for j <= i, packed bf16 back into TMEM
+                const int i = tid;
+#pragma unroll
+                for (int c0 = 0; c0 < kC; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColP + c0, r);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int j0 = c0 + e, j1 = j0 + 1;
+                        float a0 = (j0 <= i) ? __uint_as_float(r[e]) : 0.f;
+                        float a1 = (j1 <= i) ? __uint_as_float(r[e + 1]) : 0.f;
+                        if (!unit_gamma) {
+                            a0 *= pw[max(i - j0, 0)];
+                            a1 *= pw[max(i - j1, 0)];
+                        }
+                        const uint32_t u = pack_bf16x2(a0, a1);
+                        pk[e >> 1] = u;
+                        const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+                        r_i += back.x + back.y;
+                    }
+                    tmem_st16(tbase + lane_off + kColP + (c0 >> 1), pk);
+                }
+                tmem_st_wait();
+            }
+            // Q^ = xi . Q, K^ = zeta . K (rows >= L of K get 0)
+            const float gL = pw[L];
+            if (!unit_gamma) {
+                if (do_out) row_pass(tQ, DK / 64, false, [&](int r) { return pw[r + 1]; });
+                if (do_state)
+                    row_pass(tK, DK / 64, false, [&](int r) { return r < L ? pw[L - 1 - r] : 0.f; });
+            }
+            __syncthreads();
+            // normaliser: qz_i = q^_i . z_{c-1}
+            float qz = 0.f;
+            if (p.normalize && do_out) {
+                const int i = tid;
+#pragma unroll 4
+                for (int d8 = 0; d8 < DK; d8 += 8) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(tQ + (d8 >> 6) * kBlk + sw128_offset(i, d8 & 63));
+                    const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = __bfloat1622float2(hq[e]);
+                        qz = fmaf(x.x, zs[d8 + 2 * e], qz);
+                        qz = fmaf(x.y, zs[d8 + 2 * e + 1], qz);
+                    }
+                }
+            }
+            // E3: S_bf16 = bf16(S_{c-1}) (for MMA3), S = gamma^L S (before MMA4 accumulates)
+            const bool need_sb = do_out && p.mode == kFull;
+            const bool scale_s = do_state && !unit_gamma;
+            if (need_sb || scale_s) {
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                    tmem_ld_wait();
+                    if (need_sb && tid < DK) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            const int v = c0 + e8;
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
+                            *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                      sw128_offset(tid, v & 63)) = w;
+                        }
+                    }
+                    if (scale_s) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gL);
+                        tmem_st32(tbase + lane_off + kColS + c0, r);
+                    }
+                }
+                if (scale_s) tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+
+            // MMA2..4
+            if (tid == 0) {
+                const uint32_t vbase = sbase + (uint32_t)(tK - sm) + Lay::kK;
+                if (do_intra) {  // MMA2: O = P V, K = 128 tokens
+                    const uint32_t id = idesc_bf16(128, DVB, 0, 1);
+#pragma unroll
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_ts(tbase + kColO, tbase + kColP + kk * 8,
+                               smem_desc_sw128(vbase + kk * 2048, kBlk, 1024), id, kk > 0);
+                }
+                if (do_out) {  // MMA3: O (+)= Q^ S_bf16, K = DK
+                    const uint32_t id = idesc_bf16(128, DVB, 0, 1);
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; ++kk) {
+                        const uint32_t offa = (kk >> 2) * kBlk + (kk & 3) * 32;
+                        mma_ss(tbase + kColO, smem_desc_sw128(sbase + (uint32_t)(tQ - sm) + offa, 16, 1024),
+                               smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id,
+                               (do_intra || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (do_state) {  // MMA4: S += K^^T V, M = 128 (rows >= DK unused), K = 128 tokens
+                    const uint32_t id = idesc_bf16(128, DVB, 1, 1);
+#pragma unroll
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_ss(tbase + kColS, smem_desc_sw128(sbase + (uint32_t)(tK - sm) + kk * 2048, kBlk, 1024),
+                               smem_desc_sw128(vbase + kk * 2048, kBlk, 1024), id, 1u);
+                }
+                mma_commit(bar_mma);
+            }
+            mma_inflight = true;
+            // normaliser state: z_c = gamma^L z + sum_j K^[j]   (z_{c-1} already used above)
+            if (p.track_z && do_state && tid < DK) {
+                const int d = tid;
+                float acc = 0.f;
+                for (int j = 0; j < L; ++j) {
+                    const __nv_bfloat16 x = *reinterpret_cast<const __nv_bfloat16*>(
+                        tK + (d >> 6) * kBlk + sw128_offset(j, d & 63));
+                    acc += __bfloat162float(x);
+                }
+                zs[d] = fmaf(unit_gamma ? 1.f : gL, zs[d], acc);
+            }
+            to = !mbar_wait(bar_mma, mma_phase, p.wait_ns);
+            if (__syncthreads_or(to)) {
+                failed = true;
+                break;
+            }
+            mma_phase ^= 1;
+            mma_inflight = false;
+            fence_after_sync();
+            // E2: O row i = tid -> global (rows < L)
+            if (do_out) {
+                const int i = tid;
+                const float inv = p.normalize ? 1.f / (r_i + qz + p.eps) : 1.f;
+                __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + i) * p.dv + v0;
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColO + c0, r);
+                    tmem_ld_wait();
+                    if (i < L) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c0 + e8) = w;
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            fence_before_sync();
+            __syncthreads();  // stage s may be refilled by the next iteration's TMA
+            fence_after_sync();
+        }
+    }
+
+    // ---- exit state
+    if (!failed && p.S_out) {
+        const bool write = !p.out_last_only || seg == p.n_seg - 1;
+        const int oidx = bh * p.out_nseg + (p.out_last_only ? 0 : seg);
+        for (int c0 = 0; c0 < DVB; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + lane_off + kColS + c0, r);
+            tmem_ld_wait();
+            if (write && tid < DK) {
+                float* srow = p.S_out + ((size_t)oidx * DK + tid) * p.dv + v0 + c0;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(srow + e) =
+                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                    __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+            }
+        }
+        if (write && p.z_out && dvb == 0)
+            for (int d = tid; d < DK; d += kThreads) p.z_out[(size_t)oidx * DK + d] = zs[d];
+    }
+    if (failed) {
+        record_status(p.dev_status, LA_ERR_TIMEOUT);
+        // let our own copies and MMAs land (bounded) before the memory is released
+        if (tid == 0) {
+            for (int q = 0; q < 2; ++q)
+                if (inflight[q]) mbar_wait(&bar_full[q], full_phase[q], p.wait_ns);
+            if (mma_inflight) mbar_wait(bar_mma, mma_phase, p.wait_ns);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int DK, int DVB>
+cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
+    using Lay = Layout<DK, DVB>;
+    auto kern = chunk_tc_kernel<DK, DVB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, Lay::kAlloc, s>>>(prm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, cudaStream_t s) {
+    if (grid <= 0) return cudaSuccess;
+    if (dk == 64 && dvb == 64) return launch_tc<64, 64>(prm, grid, s);
+    if (dk == 64 && dvb == 128) return launch_tc<64, 128>(prm, grid, s);
+    if (dk == 128 && dvb == 64) return launch_tc<128, 64>(prm, grid, s);
+    if (dk == 128 && dvb == 128) return launch_tc<128, 128>(prm, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// Segments per sequence: enough units to cover the SMs once.
+int choose_segments(int units, int n_chunks) {
+    const int sms = sm_count();
+    if (units * 4 >= sms * 3 || n_chunks < 4) return 1;
+    int P = (sms + units - 1) / units;
+    if (P > n_chunks / 2) P = n_chunks / 2;
+    return P < 1 ? 1 : P;
+}
+
+// Entry state of every segment from the segments' own contributions:
+//   entry_0 = S0 (or 0),  entry_{q+1} = gamma^len entry_q + agg_q
+// (len = the common segment length).  One thread per state element; z rides
+// along on the threads of column 0.
+__global__ void segment_scan_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
+                                    const float* __restrict__ agg, const float* __restrict__ zagg,
+                                    float* __restrict__ entry, float* __restrict__ zentry,
+                                    size_t total, int H, int P, int seg_len, int dk, int dv,
+                                    const __grid_constant__ KernelGammas g) {
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const size_t per = (size_t)dk * dv;
+    const size_t bh = idx / per;
+    const size_t e = idx % per;
+    const float gseg = gamma_pow(g.log2g[bh % H], (float)seg_len);
+    float x = S0 ? S0[bh * per + e] : 0.f;
+    const bool do_z = (e % dv) == 0;
+    const size_t d = e / dv;
+    float zz = (do_z && z0) ? z0[bh * dk + d] : 0.f;
+    for (int q = 0; q < P; ++q) {
+        entry[(bh * P + q) * per + e] = x;
+        if (do_z) zentry[(bh * P + q) * dk + d] = zz;
+        if (q + 1 < P) {
+            x = fmaf(gseg, x, agg[(bh * P + q) * per + e]);
+            if (do_z) zz = fmaf(gseg, zz, zagg[(bh * P + q) * dk + d]);
+        }
+    }
+}
+
+}  // namespace
+
+bool tc_supported(const ChunkArgs& a) {
+    if (!a.bf16) return false;
+    if (a.dk != 64 && a.dk != 128) return false;
+    if (a.dv != 64 && a.dv != 128 && a.dv != 256) return false;
+    if (a.chunk != 0 && a.chunk != kC) return false;
+    if (!encode_fn()) return false;
+    int dev = 0, major = 0, minor = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return major == 10 && minor == 3;
+}
+
+static int tc_dvb(int dv) { return dv == 64 ? 64 : 128; }
+
+size_t tc_workspace_bytes(int B, int H, int T, int dk, int dv, bool noncausal) {
+    if (noncausal || T <= 0) return 0;
+    const int n_chunks = (T + kC - 1) / kC;
+    const int units = B * H * (dv / tc_dvb(dv));
+    const int P = choose_segments(units, n_chunks);
+    if (P <= 1) return 0;
+    const size_t nbh = (size_t)B * H;
+    // agg, entry: [BH][P][dk][dv]; zagg, zentry: [BH][P][dk]
+    return (2 * nbh * P * dk * dv + 2 * nbh * P * dk) * sizeof(float);
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
+                            int* launches) {
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int BH = a.B * a.H;
+    if (!make_map(&prm.tmQ, a.Q, BH, a.T, a.dk) || !make_map(&prm.tmK, a.K, BH, a.T, a.dk) ||
+        !make_map(&prm.tmV, a.V, BH, a.T, a.dv))
+        return cudaErrorInvalidValue;
+    const int dvb = tc_dvb(a.dv);
+    prm.O = (__nv_bfloat16*)a.O;
+    prm.H = a.H;
+    prm.T = a.T;
+    prm.dv = a.dv;
+    prm.n_dvb = a.dv / dvb;
+    prm.normalize = a.normalize;
+    prm.track_z = a.normalize || a.z_out != nullptr;
+    prm.phi = a.phi;
+    prm.eps = a.eps;
+    prm.dev_status = a.dev_status;
+    prm.wait_ns = 2000000000ull;
+    const char* ft = std::getenv("LA_DEBUG_FORCE_TIMEOUT");
+    if (ft && ft[0] == '1') {
+        prm.force_timeout = 1;
+        prm.wait_ns = 1000000ull;  // 1 ms
+    }
+    prm.g = g;
+    const int n_chunks = (a.T + kC - 1) / kC;
+    const int units = BH * prm.n_dvb;
+    *launches = 0;
+
+    if (a.noncausal) {
+        prm.mode = kNonCausal;
+        prm.seg_chunks = n_chunks;
+        prm.n_seg = 1;
+        prm.in_nseg = 1;
+        prm.S_out = a.S_out;
+        prm.z_out = a.z_out;
+        prm.out_nseg = 1;
+        prm.out_last_only = 1;
+        *launches = 1;
+        return launch_tc_dispatch(a.dk, dvb, prm, units, s);
+    }
+    const int P = choose_segments(units, n_chunks);
+    if (P <= 1) {
+        prm.mode = kFull;
+        prm.seg_chunks = n_chunks;
+        prm.n_seg = 1;
+        prm.S_in = a.S0;
+        prm.z_in = a.z0;
+        prm.in_nseg = 1;
+        prm.S_out = a.S_out;
+        prm.z_out = a.z_out;
+        prm.out_nseg = 1;
+        prm.out_last_only = 1;
+        *launches = 1;
+        return launch_tc_dispatch(a.dk, dvb, prm, units, s);
+    }
+    // segmented: (1) each segment's own state, (2) scan to entry states, (3) outputs
+    const int seg_chunks = (n_chunks + P - 1) / P;
+    const int Pu = (n_chunks + seg_chunks - 1) / seg_chunks;  // segments actually used
+    const size_t nbh = (size_t)BH;
+    float* agg = (float*)a.workspace;
+    float* entry = agg + nbh * Pu * a.dk * a.dv;
+    float* zagg = entry + nbh * Pu * a.dk * a.dv;
+    float* zentry = zagg + nbh * Pu * a.dk;
+    if (tc_workspace_bytes(a.B, a.H, a.T, a.dk, a.dv, false) <
+        (2 * nbh * Pu * a.dk * a.dv + 2 * nbh * Pu * a.dk) * sizeof(float))
+        return cudaErrorInvalidValue;
+
+    TcParams pa = prm;  // state-only walks of segments 0 .. Pu-2
+    pa.mode = kStateOnly;
+    pa.seg_chunks = seg_chunks;
+    pa.n_seg = Pu;
+    pa.S_out = agg;
+    pa.z_out = zagg;
+    pa.out_nseg = Pu;
+    pa.out_last_only = 0;
+    // launch all Pu segments' state walks (the last one's is unused but keeps the grid simple)
+    cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * Pu, s);
+    if (e != cudaSuccess) return e;
+    const size_t total = nbh * (size_t)a.dk * a.dv;
+    segment_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+        a.S0, a.z0, agg, zagg, entry, zentry, total, a.H, Pu, seg_chunks * kC, a.dk, a.dv, g);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    TcParams pc = prm;
+    pc.mode = kFull;
+    pc.seg_chunks = seg_chunks;
+    pc.n_seg = Pu;
+    pc.S_in = entry;
+    pc.z_in = zentry;
+    pc.in_nseg = Pu;
+    pc.S_out = a.S_out;
+    pc.z_out = a.z_out;
+    pc.out_nseg = 1;
+    pc.out_last_only = 1;
+    *launches = 3;
+    return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s);
+}
+
+}  // namespace la

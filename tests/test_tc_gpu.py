@@ -1,0 +1,150 @@
+"""The tensor-core (tcgen05) chunkwise path against the fp64 oracle.
+
+LA_CHUNK_PATH=tc pins la_chunk_fwd to the tensor-core kernels (an error if
+the shape is outside them), LA_CHUNK_PATH=simt to the fp32 CUDA-core kernel;
+both are compared with the oracle on the same seeded inputs, and with each
+other.  Shapes cover one and several chunks of 128, ragged tails, T = 1,
+d_k != d_v, both value-column block widths, the split of a long sequence into
+segments (few sequences, many chunks), phi/normaliser, and the non-causal form.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+import workloads
+
+la = pytest.importorskip("retnet_retention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from retnet_retention_gb300 import _build
+    _build.build()
+    la.library()
+
+
+@pytest.fixture
+def tc_path(monkeypatch):
+    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+
+
+def run(x, phi, normalize, causal=True, S0=None, z0=None, dev_status=None):
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    B, H, T, dk = q.shape
+    O, S, z = la.chunk_fwd(q, k, v, x["gamma"], phi=phi, normalize=normalize, causal=causal,
+                           S0=S0, z0=z0, z_out=torch.empty(B, H, dk, device=DEV),
+                           dev_status=dev_status)
+    torch.cuda.synchronize()
+    return (O.double().cpu().numpy(), S.double().cpu().numpy(), z.double().cpu().numpy())
+
+
+def check(name, got, want, tol=TOL):
+    assert np.all(np.isfinite(got)), f"{name}: non-finite"
+    err = pins.rel_err(got, want)
+    assert err <= tol, f"{name}: rel err {err:.3e} > {tol:.0e}"
+
+
+TC_SHAPES = [  # B, H, T, dk, dv
+    (1, 2, 1, 64, 64),
+    (2, 2, 128, 64, 64),
+    (1, 3, 300, 128, 128),
+    (2, 1, 129, 128, 256),
+    (1, 2, 517, 64, 128),
+    (1, 1, 384, 128, 64),
+    (1, 2, 4100, 128, 128),   # few sequences, many chunks: segmented
+    (1, 1, 2000, 64, 64),     # segmented with a ragged last segment
+]
+
+
+@pytest.mark.parametrize("flags", [(False, False), (True, True), (True, False)],
+                         ids=lambda f: f"phi{int(f[0])}_norm{int(f[1])}")
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tc_matches_oracle(shape, flags, tc_path):
+    B, H, T, dk, dv = shape
+    phi, normalize = flags
+    seed = zlib.crc32(repr((shape, flags, "tc")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16")
+    O, S, z = run(x, phi, normalize)
+    Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=phi,
+                                  normalize=normalize)
+    check("O", O, Or)
+    check("S_T", S, Sr)
+    check("z_T", z, zr)
+
+
+@pytest.mark.parametrize("gamma", [[0.5, 0.9], [1.0, 0.999], [0.05, 0.99]])
+def test_tc_decay_extremes(gamma, tc_path):
+    """Small decays underflow instead of overflowing; gamma = 1 skips the scaling."""
+    x = workloads.random_case(31, 1, 2, 700, 128, 128, dtype="bf16", gamma=gamma)
+    O, S, _ = run(x, False, False)
+    Or, Sr, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"])
+    check("O", O, Or)
+    check("S_T", S, Sr)
+
+
+def test_tc_resume_from_state(tc_path):
+    x = workloads.random_case(41, 2, 2, 900, 128, 128, dtype="bf16")
+    Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=True, normalize=True)
+    t1 = 389
+    a = {n: x[n][:, :, :t1].contiguous() for n in ("q", "k", "v")}
+    b = {n: x[n][:, :, t1:].contiguous() for n in ("q", "k", "v")}
+    a["gamma"] = b["gamma"] = x["gamma"]
+    O1, S1, z1 = run(a, True, True)
+    O2, S2, z2 = run(b, True, True, S0=torch.from_numpy(S1).float().to(DEV),
+                     z0=torch.from_numpy(z1).float().to(DEV))
+    check("O", np.concatenate([O1, O2], axis=2), Or)
+    check("S_T", S2, Sr)
+    check("z_T", z2, zr)
+
+
+@pytest.mark.parametrize("flags", [(False, False), (True, True)],
+                         ids=lambda f: f"phi{int(f[0])}_norm{int(f[1])}")
+def test_tc_noncausal(flags, tc_path):
+    phi, normalize = flags
+    x = workloads.random_case(51, 1, 3, 333, 128, 128, dtype="bf16", gamma=1.0)
+    O, S, _ = run(x, phi, normalize, causal=False)
+    Or, Sr, _ = oracle.noncausal(x["q"], x["k"], x["v"], phi=phi, normalize=normalize)
+    check("O", O, Or)
+    check("S", S, Sr)
+
+
+def test_tc_and_simt_agree(monkeypatch):
+    x = workloads.random_case(61, 2, 4, 640, 64, 64, dtype="bf16")
+    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    Ot, St, zt = run(x, True, True)
+    monkeypatch.setenv("LA_CHUNK_PATH", "simt")
+    Os, Ss, zs = run(x, True, True)
+    check("O", Ot, Os)
+    check("S", St, Ss)
+    check("z", zt, zs)
+
+
+def test_tc_is_the_default_for_supported_shapes():
+    assert la.library().la_chunk_fwd_launches(4, 8, 4096, 64, 64, 1, 3, 0) in (1, 3)
+    assert la.workspace_size(1, 8, 65536, 128, 128) > 0  # long and few: segmented
+
+
+def test_timeout_is_reported_not_hung(monkeypatch):
+    """A wait that runs out (on a barrier nothing arrives on) sets dev_status; the
+    context stays usable."""
+    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    monkeypatch.setenv("LA_DEBUG_FORCE_TIMEOUT", "1")
+    x = workloads.random_case(71, 1, 2, 256, 64, 64, dtype="bf16")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    run(x, False, False, dev_status=status)
+    assert int(status.item()) == la.LA_ERR_TIMEOUT
+    monkeypatch.delenv("LA_DEBUG_FORCE_TIMEOUT")
+    status.zero_()
+    O, S, _ = run(x, False, False, dev_status=status)
+    assert int(status.item()) == 0
+    Or, Sr, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"])
+    check("O after a reported timeout", O, Or)
