@@ -177,6 +177,24 @@ LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, 
                                    float* S, float* z, void* o,
                                    int* dev_status, la_stream_t stream);
 
+/*
+ * Launch tracing (profiling aid; no counterpart on the pages).  While enabled,
+ * the library records a pair of CUDA events on the launching stream around
+ * every kernel it enqueues, for up to `capacity` launches (capacity <= 0
+ * disables tracing and frees the events).  la_trace_collect waits for the
+ * recorded launches, writes up to max_records {kernel name, device ms}
+ * records (names are static strings) and resets the log; it returns the
+ * number written, or -LA_ERR_CUDA.  Not thread-safe across concurrent
+ * streams' interleaved calls beyond keeping each record's pair consistent.
+ */
+typedef struct {
+    const char* kernel;
+    float ms;
+} la_trace_record;
+
+LA_API int la_trace_enable(int capacity);
+LA_API int la_trace_collect(la_trace_record* out, int max_records);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,6 +30,24 @@ LIBRARY_PATH = _build.LIBRARY
 _LIB = None
 
 
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char_p), ("ms", ctypes.c_float)]
+
+
+def trace_enable(capacity: int = 4096):
+    """Record CUDA events around every library kernel launch (0 disables)."""
+    _check(_load().la_trace_enable(int(capacity)), "la_trace_enable")
+
+
+def trace_collect(max_records: int = 4096) -> list[tuple[str, float]]:
+    """(kernel name, device ms) of every launch traced since the last collect."""
+    buf = (TraceRecord * max_records)()
+    n = _load().la_trace_collect(buf, max_records)
+    if n < 0:
+        raise LinAttnError(-n, "la_trace_collect")
+    return [(buf[i].kernel.decode(), float(buf[i].ms)) for i in range(n)]
+
+
 class LinAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -60,6 +78,10 @@ def _load() -> ctypes.CDLL:
     lib.la_recurrent_step.restype = i
     lib.la_chunk_fwd_launches.argtypes = [i, i, i, i, i, i, u, i]
     lib.la_chunk_fwd_launches.restype = i
+    lib.la_trace_enable.argtypes = [i]
+    lib.la_trace_enable.restype = i
+    lib.la_trace_collect.argtypes = [ctypes.POINTER(TraceRecord), i]
+    lib.la_trace_collect.restype = i
     _LIB = lib
     return lib
 
@@ -216,5 +238,6 @@ def chunk_fwd_host(q, k, v, gamma, *, device="cuda", stream=None, **kw):
 
 
 __all__ = ["chunk_fwd", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
+           "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
            "LA_NORMALIZE", "LA_NONCAUSAL"]

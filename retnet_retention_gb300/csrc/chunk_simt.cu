@@ -22,6 +22,7 @@
 // chunks in order; S (d_k x 64 fp32) stays in shared memory for the whole
 // sequence.  Inputs are read once per column block.
 #include "launch.h"
+#include "trace.h"
 
 namespace la {
 
@@ -205,6 +206,7 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStr
     const size_t smem = (size_t)simt_layout(C, a.dk, dvb).total * sizeof(float);
     dim3 grid((unsigned)((size_t)a.B * a.H), (a.dv + dvb - 1) / dvb);
     cudaError_t e;
+    TraceScope trace("chunk_simt_kernel", s);
     if (a.bf16) {
         auto kern = chunk_simt_kernel<__nv_bfloat16>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -47,6 +47,7 @@
 
 #include "launch.h"
 #include "tc_ptx.cuh"
+#include "trace.h"
 
 namespace la {
 
@@ -577,6 +578,9 @@ cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
+    static const char* const names[3] = {"chunk_tc_kernel/full", "chunk_tc_kernel/state",
+                                         "chunk_tc_kernel/noncausal"};
+    TraceScope trace(names[prm.mode], s);
     kern<<<grid, kThreads, Lay::kAlloc, s>>>(prm);
     return cudaGetLastError();
 }
@@ -744,8 +748,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * Pu, s);
     if (e != cudaSuccess) return e;
     const size_t total = nbh * (size_t)a.dk * a.dv;
+    {
+    TraceScope trace("segment_scan_kernel", s);
     segment_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
         a.S0, a.z0, agg, zagg, entry, zentry, total, a.H, Pu, seg_chunks * kC, a.dk, a.dv, g);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     TcParams pc = prm;

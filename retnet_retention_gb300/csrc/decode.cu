@@ -15,6 +15,7 @@
 // read-out sum over d_k is a register accumulation followed by a shared-
 // memory reduction across the row slots.
 #include "launch.h"
+#include "trace.h"
 
 namespace la {
 
@@ -129,6 +130,7 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
     if (nbh == 0) return cudaSuccess;
     if (nbh > 0x7fffffffu) return cudaErrorInvalidValue;
     dim3 grid((unsigned)nbh);
+    TraceScope trace("decode_step_kernel", s);
     if (a.bf16) {
         decode_step_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
             (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,

@@ -3,6 +3,7 @@
 // linear attention, recurrent form"), and the S_T = S_0 hand-off of an empty
 // sequence.  Plain bandwidth kernels: 16-byte stores, grid-stride loops.
 #include "launch.h"
+#include "trace.h"
 
 namespace la {
 
@@ -38,6 +39,7 @@ static int grid_for(size_t work) {
 cudaError_t launch_state_zero(float* S, float* z, size_t n_S, size_t n_z, cudaStream_t s) {
     if (n_S == 0 && n_z == 0) return cudaSuccess;
     size_t n4 = n_S / 4;
+    TraceScope trace("state_zero_kernel", s);
     state_zero_kernel<<<grid_for(n4 > n_z ? n4 : n_z), 256, 0, s>>>(
         reinterpret_cast<float4*>(S), n4, z, z ? n_z : 0);
     return cudaGetLastError();
@@ -47,6 +49,7 @@ cudaError_t launch_state_zero(float* S, float* z, size_t n_S, size_t n_z, cudaSt
 cudaError_t launch_state_copy(float* dst, const float* src, size_t n, cudaStream_t s) {
     if (n == 0 || dst == src) return cudaSuccess;
     size_t n4 = n / 4;
+    TraceScope trace("state_copy_kernel", s);
     state_copy_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<float4*>(dst),
                                                    reinterpret_cast<const float4*>(src), n4);
     return cudaGetLastError();

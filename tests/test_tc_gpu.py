@@ -148,3 +148,18 @@ def test_timeout_is_reported_not_hung(monkeypatch):
     assert int(status.item()) == 0
     Or, Sr, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"])
     check("O after a reported timeout", O, Or)
+
+
+def test_launch_trace_names_the_kernels():
+    x = workloads.random_case(81, 1, 1, 4096, 64, 64, dtype="bf16")
+    la.trace_enable(64)
+    try:
+        run(x, True, True)
+        recs = la.trace_collect()
+    finally:
+        la.trace_enable(0)
+    names = [n for n, _ in recs]
+    assert "chunk_tc_kernel/full" in names
+    assert all(ms > 0.0 for _, ms in recs)
+    n = la.library().la_chunk_fwd_launches(1, 1, 4096, 64, 64, 1, 3, 0)
+    assert len(names) == n, (names, n)
