@@ -194,7 +194,7 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
                     e2e: bool = False) -> dict:
     c = dict(workloads.CONFIGS[name])
     B = c["B"]
-    pairs = [(rank * B + b, h) for b in range(B) for h in range(c["H"])]
+    pairs = workloads.shard_pairs(rank, world, B, c["H"])
     cw = dict(c)
     cw["B"] = B * world
     x = workloads.make_inputs(cw, pairs=pairs)
@@ -268,7 +268,7 @@ def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> 
     name = "decode_bf16"
     c = dict(workloads.CONFIGS[name])
     B, H = c["B"], c["H"]
-    pairs = [(rank * B + b, h) for b in range(B) for h in range(H)]
+    pairs = workloads.shard_pairs(rank, world, B, H)
     cw = dict(c)
     cw["B"] = B * world
     x = workloads.make_inputs(cw, pairs=pairs)

@@ -196,11 +196,18 @@ def sample_pairs(B: int, H: int, n: int, seed: int = 12345) -> list:
     return [(i // H, i % H) for i in sorted(idx)]
 
 
+def shard_pairs(rank: int, world: int, B: int, H: int) -> list:
+    """The (b, h) sequences rank `rank` of `world` owns when each rank runs its own
+    batch of B sequences out of a global batch of B * world (weak scaling):
+    global batch rows rank*B .. rank*B + B - 1, every head."""
+    return [(rank * B + b, h) for b in range(B) for h in range(H)]
+
+
 def tokens(cfg) -> int:
     c = CONFIGS[cfg] if isinstance(cfg, str) else cfg
     return c["B"] * c["T"]
 
 
 __all__ = ["CONFIGS", "make_inputs", "decode_inputs", "decode_inputs_all", "random_case",
-           "gammas", "sample_pairs", "normal_bhtd", "torch_dtype", "tokens"]
+           "gammas", "sample_pairs", "shard_pairs", "normal_bhtd", "torch_dtype", "tokens"]
 
