@@ -45,21 +45,19 @@
 
 #include <cudaTypedefs.h>
 
+#include "chunk_tc_common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
 #include "trace.h"
 
 namespace la {
 
+using namespace tck;
+
 namespace {
 
-using namespace tc;
-
-constexpr int kC = 128;         // chunk length (= MMA M)
 constexpr int kThreads = 128;   // 4 warps: warp w owns TMEM lanes 32w .. 32w+31
-constexpr uint32_t kColP = 0;     // scores (fp32, 128 cols) then P (bf16 pairs, 64 cols)
 constexpr uint32_t kColO = 128;   // O accumulator (DVB cols), then the state S (DVB cols)
-constexpr uint32_t kBlk = 16384;  // one [128 rows x 64 bf16] swizzled block
 
 // TMEM columns: scores/P 128 + O DVB + S DVB, rounded up to a power of two
 // (256 for DVB = 64, so two CTAs can share an SM; 512 for DVB = 128).
@@ -67,33 +65,6 @@ template <int DVB>
 struct Tmem {
     static constexpr uint32_t kColS = kColO + DVB;
     static constexpr uint32_t kCols = (128 + 2 * DVB) <= 256 ? 256 : 512;
-};
-
-enum Mode { kFull = 0, kStateOnly = 1, kNonCausal = 2 };
-
-struct TcParams {
-    CUtensorMap tmQ, tmK, tmV;  // [BH][T][d] bf16, box {64, 128, 1}, 128B swizzle
-    __nv_bfloat16* O;           // [BH][T][dv]
-    const float* S_in;          // entry states or nullptr (zero)
-    const float* z_in;
-    float* S_out;               // final states or nullptr
-    float* z_out;
-    int in_nseg;                // entry-state index = bh * in_nseg + seg
-    int out_nseg;               // exit-state index = bh * out_nseg + (out_last_only ? 0 : seg)
-    int out_last_only;
-    int H, T, dv;
-    int n_dvb;                  // value-column blocks per sequence
-    int seg_chunks;             // chunks per segment
-    int n_seg;                  // segments per sequence (this launch covers seg0 .. seg0+n_seg-1)
-    int mode;
-    int normalize;
-    int track_z;                // carry the normaliser state z (normalising, or z_out wanted)
-    int phi;
-    float eps;
-    int* dev_status;
-    unsigned long long wait_ns;
-    int force_timeout;
-    KernelGammas g;
 };
 
 template <int DK, int DVB>
@@ -104,49 +75,13 @@ struct Layout {
     static constexpr uint32_t kStage = kQ + kK + kV;
     static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // S_bf16, MN-major
     static constexpr uint32_t oSB = 2 * kStage;
-    static constexpr uint32_t oPw = oSB + kSB;            // float pw[kC + 4]
-    static constexpr uint32_t oZ = oPw + (kC + 4) * 4;    // float z[DK]
-    static constexpr uint32_t oBar = oZ + DK * 4;         // 4 mbarriers
+    static constexpr uint32_t oZ = oSB + kSB;             // float z[DK]
+    static constexpr uint32_t oZP = oZ + DK * 4;          // float colsum partials [256/DK][DK]
+    static constexpr uint32_t oBar = oZP + 256 * 4;       // 4 mbarriers
     static constexpr uint32_t oSlot = oBar + 4 * 8;       // TMEM base address
     static constexpr uint32_t kBytes = oSlot + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
-
-__device__ __forceinline__ void record_status(int* st, int code) {
-    if (st) atomicCAS(st, 0, code);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
-
-// In-place pass over a [128 x 64*nblk] K-major swizzled tile: apply phi
-// (optional) and multiply row r by fac(r).  Rows are whole 128-byte lines,
-// so the swizzle never moves an element to another row.
-template <typename F>
-__device__ __forceinline__ void row_pass(char* tile, int nblk, bool apply_phi, F fac) {
-    const int n16 = nblk * (kBlk / 16);
-    for (int idx = threadIdx.x; idx < n16; idx += kThreads) {
-        const int r = (idx >> 3) & 127;
-        uint4* p = reinterpret_cast<uint4*>(tile) + idx;
-        uint4 u = *p;
-        const float f = fac(r);
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float2 x = __bfloat1622float2(h[e]);
-            if (apply_phi) {
-                x.x = phi_f(x.x);
-                x.y = phi_f(x.y);
-            }
-            h[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
-        }
-        *p = u;
-    }
-}
 
 template <int DK, int DVB>
 __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
@@ -155,7 +90,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     constexpr uint32_t kTmemCols = Tmem<DVB>::kCols;
     extern __shared__ __align__(1024) char smem_raw[];
     char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    float* pw = reinterpret_cast<float*>(sm + Lay::oPw);
     float* zs = reinterpret_cast<float*>(sm + Lay::oZ);
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);  // [2]
     uint64_t* bar_mma = bar_full + 2;
@@ -190,7 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         tmem_alloc(slot, kTmemCols);
         tmem_relinquish();
     }
-    for (int n = tid; n <= kC + 1; n += kThreads) pw[n] = gamma_pow(l2g, (float)n);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -315,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
             inflight[s] = false;
             // phi on q and k (rows >= L zeroed: phi(0) = 1 must not leak in)
             if (p.phi) {
-                if (need_q) row_pass(tQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; });
-                if (need_kv) row_pass(tK, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; });
+                if (need_q) row_pass(tQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, tid, kThreads);
+                if (need_kv) row_pass(tK, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, tid, kThreads);
                 fence_proxy_async_smem();
             }
             fence_before_sync();
@@ -347,22 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                 fence_after_sync();
                 // E1: row i = tid: P_ij = s_ij gamma^(i-j) for j <= i, packed bf16 back into TMEM
                 const int i = tid;
+                const float gam = p.g.gamma[h];
 #pragma unroll
                 for (int c0 = 0; c0 < kC; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tbase + lane_off + kColP + c0, r);
                     tmem_ld_wait();
                     uint32_t pk[16];
+                    // gamma^(i-j) by a running product from the piece's top column down
+                    const int jt = min(i, c0 + 31);
+                    float w = (unit_gamma || jt < c0) ? 1.f : gamma_pow(l2g, (float)(i - jt));
+                    float a[32];
+#pragma unroll
+                    for (int e = 31; e >= 0; --e) {
+                        float x = 0.f;
+                        if (c0 + e <= i) {
+                            x = __uint_as_float(r[e]);
+                            if (!unit_gamma) {
+                                x *= w;
+                                w *= gam;
+                            }
+                        }
+                        a[e] = x;
+                    }
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const int j0 = c0 + e, j1 = j0 + 1;
-                        float a0 = (j0 <= i) ? __uint_as_float(r[e]) : 0.f;
-                        float a1 = (j1 <= i) ? __uint_as_float(r[e + 1]) : 0.f;
-                        if (!unit_gamma) {
-                            a0 *= pw[max(i - j0, 0)];
-                            a1 *= pw[max(i - j1, 0)];
-                        }
-                        const uint32_t u = pack_bf16x2(a0, a1);
+                        const uint32_t u = pack_bf16x2(a[e], a[e + 1]);
                         pk[e >> 1] = u;
                         const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
                         r_i += back.x + back.y;
@@ -372,11 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                 tmem_st_wait();
             }
             // Q^ = xi . Q, K^ = zeta . K (rows >= L of K get 0)
-            const float gL = pw[L];
+            const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
             if (!unit_gamma) {
-                if (do_out) row_pass(tQ, DK / 64, false, [&](int r) { return pw[r + 1]; });
+                if (do_out)
+                    row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); },
+                             tid, kThreads);
                 if (do_state)
-                    row_pass(tK, DK / 64, false, [&](int r) { return r < L ? pw[L - 1 - r] : 0.f; });
+                    row_pass(tK, DK / 64, false,
+                             [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
+                             tid, kThreads);
             }
             __syncthreads();
             // normaliser: qz_i = q^_i . z_{c-1}
@@ -459,16 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                 mma_commit(bar_mma);
             }
             mma_inflight = true;
-            // normaliser state: z_c = gamma^L z + sum_j K^[j]   (z_{c-1} already used above)
-            if (p.track_z && do_state && tid < DK) {
-                const int d = tid;
-                float acc = 0.f;
-                for (int j = 0; j < L; ++j) {
-                    const __nv_bfloat16 x = *reinterpret_cast<const __nv_bfloat16*>(
-                        tK + (d >> 6) * kBlk + sw128_offset(j, d & 63));
-                    acc += __bfloat162float(x);
-                }
-                zs[d] = fmaf(unit_gamma ? 1.f : gL, zs[d], acc);
+            // normaliser state: z_c = gamma^L z + sum_j K^[j]   (z_{c-1} already used above;
+            // rows >= L of K^ are zero)
+            if (p.track_z && do_state) {
+                float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+                colsum_partial<DK>(tK, tid, zpart);
+                __syncthreads();
+                if (tid < DK) zs[tid] = fmaf(unit_gamma ? 1.f : gL, zs[tid], colsum_total<DK>(zpart, tid));
             }
             to = !mbar_wait(bar_mma, mma_phase, p.wait_ns);
             if (__syncthreads_or(to)) {
@@ -558,18 +502,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
 
 template <int DK, int DVB>
 cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
@@ -585,8 +517,18 @@ cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+}  // namespace
+
+bool tc_ws_supported(int dk, int dvb, bool normalize);
+cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
+                               cudaStream_t s);
+
+namespace {
+
 cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
+    if (prm.mode == kFull && tc_ws_supported(dk, dvb, prm.normalize != 0))
+        return launch_chunk_tc_ws(dk, dvb, prm.normalize != 0, prm, grid, s);
     if (dk == 64 && dvb == 64) return launch_tc<64, 64>(prm, grid, s);
     if (dk == 64 && dvb == 128) return launch_tc<64, 128>(prm, grid, s);
     if (dk == 128 && dvb == 64) return launch_tc<128, 64>(prm, grid, s);
@@ -640,6 +582,21 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
 }
 
 }  // namespace
+
+namespace tck {
+bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+}  // namespace tck
 
 bool tc_supported(const ChunkArgs& a) {
     if (!a.bf16) return false;

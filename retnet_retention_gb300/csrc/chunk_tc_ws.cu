@@ -1,0 +1,509 @@
+// Chunkwise forward, warp-specialised tcgen05 pipeline (the output walk of a
+// causal sequence or segment: mode kFull).
+//
+// Same arithmetic as the lockstep kernel in chunk_tc.cu ("Chunked Recurrent
+// Representation", "RetNet" page; equations in chunk_tc.cu's header), but
+// the roles run concurrently and hand work over through mbarriers:
+//
+//   warp 0      TMA producer: Q, K, V of chunk c into a two-stage ring
+//   warp 1      MMA issuer (one thread): MMA1 of chunk c+1 is issued ahead of
+//               MMA2..4 of chunk c, into the other of two TMEM score buffers
+//   warps 2-5   epilogue A: E1 (scores -> decay mask -> bf16 P back into
+//               TMEM, row sums) and E3 (bf16 copy of S for MMA3, S *= gamma^L)
+//   warps 6-9   epilogue B: phi on the next chunk's Q/K tiles, the xi/zeta row
+//               scalings, the normaliser (q^ . z and the z update), and E2
+//               (O of the previous chunk -> global)
+//
+// so that per chunk the tensor pipe waits only for E3 (and E2 frees O) after
+// MMA4 of the previous chunk.  TMEM (512 columns): two score/P buffers at 0
+// and 128, O at 256, S after O, and (DVB = 64) four row-sum columns at 384.
+// Taken for DVB = 64 with any flags and for DVB = 128 without the
+// normaliser; other cases use the lockstep kernel.
+//
+// Every wait is bounded; a role that times out raises a shared abort flag,
+// every other role's waits then give up too, all roles meet at the end, the
+// producer and issuer wait (bounded) for their own copies and MMAs, the CTA
+// records LA_ERR_TIMEOUT and frees its TMEM.
+#include <cstdlib>
+#include <cstring>
+
+#include "chunk_tc_common.cuh"
+#include "launch.h"
+#include "trace.h"
+
+namespace la {
+
+using namespace tck;
+
+namespace {
+
+constexpr int kThreadsWS = 320;
+constexpr int kWgA = 2;   // first warp of epilogue A
+constexpr int kWgB = 6;   // first warp of epilogue B
+constexpr int kBarA = 1;  // named barrier ids
+constexpr int kBarB = 2;
+constexpr uint32_t kColScores = 0;  // + 128 * buffer
+constexpr uint32_t kColO = 256;
+
+template <int DK, int DVB>
+struct LayoutWS {
+    static constexpr uint32_t kQ = (DK / 64) * kBlk;
+    static constexpr uint32_t kK = (DK / 64) * kBlk;
+    static constexpr uint32_t kV = (DVB / 64) * kBlk;
+    static constexpr uint32_t kStage = kQ + kK + kV;
+    static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // bf16 S, MN-major
+    static constexpr uint32_t oSB = 2 * kStage;
+    static constexpr uint32_t oZ = oSB + kSB;           // float z[DK]
+    static constexpr uint32_t oZP = oZ + DK * 4;        // float colsum partials [256/DK][DK]
+    static constexpr uint32_t oBar = oZP + 256 * 4;     // 16 mbarriers
+    static constexpr uint32_t oFlags = oBar + 16 * 8;   // int abort, uint32 tmem slot
+    static constexpr uint32_t kBytes = oFlags + 16;
+    static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
+    static constexpr uint32_t kColS = kColO + DVB;
+    static constexpr uint32_t kColR = 384;              // row sums, 4 rotating columns (DVB = 64)
+};
+
+// Barriers.  Per-chunk hand-overs that one side could otherwise complete twice
+// before the other side waits once are double-buffered by chunk parity
+// (full, empty, qk, sfull, pready); o_full / o_empty cannot run ahead.
+enum Bars {
+    kFull0 = 0, kFull1, kEmpty0, kEmpty1, kQk0, kQk1, kSfull0, kSfull1,
+    kPready0, kPready1, kOfull, kOempty, kNever, kDrain, kNumBars
+};
+
+template <int DK, int DVB, bool NORM>
+__global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    using Lay = LayoutWS<DK, DVB>;
+    static_assert(!NORM || DVB == 64, "row-sum columns exist only for DVB = 64");
+    extern __shared__ __align__(1024) char smem_raw[];
+    char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    float* zs = reinterpret_cast<float*>(sm + Lay::oZ);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::oFlags);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oFlags + 4);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int unit = blockIdx.x;
+    const int seg = unit % p.n_seg;
+    const int dvb = (unit / p.n_seg) % p.n_dvb;
+    const int bh = unit / (p.n_seg * p.n_dvb);
+    const int h = bh % p.H;
+    const int v0 = dvb * DVB;
+    const float l2g = p.g.log2g[h];
+    const float gam = p.g.gamma[h];
+    const bool unit_gamma = gam == 1.0f;
+    const int n_chunks = (p.T + kC - 1) / kC;
+    const int cb = seg * p.seg_chunks;
+    const int ce = min(n_chunks, cb + p.seg_chunks);
+    const int n = ce - cb;  // chunks of this unit
+    const uint64_t lim = p.wait_ns;
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
+        mbar_init(&bar[kEmpty0], 2);  // MMA commit + epilogue B
+        mbar_init(&bar[kEmpty1], 2);
+        mbar_init(&bar[kPready0], 2);  // epilogue A + epilogue B
+        mbar_init(&bar[kPready1], 2);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&p.tmQ);
+        prefetch_tensormap(&p.tmK);
+        prefetch_tensormap(&p.tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(slot, 512);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t sbase = smem_addr(sm);
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane of this thread (epilogue warps)
+
+    bool forced = false;
+    if (p.force_timeout) {  // test hook: a wait on a barrier nothing arrives on
+        if (tid == 0 && !mbar_wait(&bar[kNever], 0, lim)) record_status(p.dev_status, LA_ERR_TIMEOUT);
+        forced = true;
+    }
+
+    // ---- entry state into TMEM (epilogue B owns all 128 lanes), z into smem
+    if (!forced && warp >= kWgB) {
+        const int sidx = bh * p.in_nseg + seg;
+        const bool has_in = p.S_in != nullptr;
+        for (int c0 = 0; c0 < DVB; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                float x = 0.f;
+                if (has_in && row < DK) x = p.S_in[((size_t)sidx * DK + row) * p.dv + v0 + c0 + e];
+                r[e] = __float_as_uint(x);
+            }
+            tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
+        }
+        tmem_st_wait();
+        if (row < DK) zs[row] = (has_in && p.z_in) ? p.z_in[(size_t)sidx * DK + row] : 0.f;
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // per-role bookkeeping that the drain at the end needs
+    int fills[2] = {0, 0};     // producer: TMA fills issued per stage
+    bool mma_issued = false;   // issuer: any MMA issued
+
+    if (!forced && n > 0) {
+        if (warp == 0 && lane == 0) {
+            // ---------------- producer
+            for (int it = 0; it < n; ++it) {
+                const int s = it & 1;
+                if (it >= 2 && !mbar_wait_or_abort(&bar[kEmpty0 + s], ((it - 2) >> 1) & 1, lim, abort_flag))
+                    break;
+                char* st = sm + s * Lay::kStage;
+                const int y = (cb + it) * kC;
+                mbar_arrive_expect_tx(&bar[kFull0 + s], Lay::kStage);
+#pragma unroll
+                for (int b = 0; b < DK / 64; ++b) {
+                    tma_load_3d(st + b * kBlk, &p.tmQ, b * 64, y, bh, &bar[kFull0 + s]);
+                    tma_load_3d(st + Lay::kQ + b * kBlk, &p.tmK, b * 64, y, bh, &bar[kFull0 + s]);
+                }
+#pragma unroll
+                for (int b = 0; b < DVB / 64; ++b)
+                    tma_load_3d(st + Lay::kQ + Lay::kK + b * kBlk, &p.tmV, v0 + b * 64, y, bh,
+                                &bar[kFull0 + s]);
+                ++fills[s];
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
+            const uint32_t id_pv = idesc_bf16(128, DVB, 0, 1);
+            const uint32_t id_kv = idesc_bf16(128, DVB, 1, 1);
+            auto issue_mma1 = [&](int it) -> bool {
+                const int s = it & 1;
+                const uint32_t par = (it >> 1) & 1;
+                if (!mbar_wait_or_abort(&bar[kFull0 + s], par, lim, abort_flag)) return false;
+                if (p.phi && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag)) return false;
+                fence_after_sync();
+                const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ;
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
+                    mma_ss(tbase + kColScores + (it & 1) * 128, smem_desc_sw128(qa + off, 16, 1024),
+                           smem_desc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+                }
+                mma_commit(&bar[kSfull0 + (it & 1)]);
+                mma_issued = true;
+                return true;
+            };
+            bool ok = issue_mma1(0);
+            for (int it = 0; it < n && ok; ++it) {
+                const int s = it & 1;
+                if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag)) break;
+                if (it >= 1 && !mbar_wait_or_abort(&bar[kOempty], (it - 1) & 1, lim, abort_flag)) break;
+                fence_after_sync();
+                const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ, va = ka + Lay::kK;
+                // MMA2: O = P V (A = P from TMEM, K = 128 tokens)
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ts(tbase + kColO, tbase + kColScores + (it & 1) * 128 + kk * 8,
+                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_pv, kk > 0);
+                // MMA3: O += Q^ S_bf16 (K = DK)
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
+                    mma_ss(tbase + kColO, smem_desc_sw128(qa + off, 16, 1024),
+                           smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id_pv, 1u);
+                }
+                // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
+                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
+                mma_commit(&bar[kOfull]);
+                mma_commit(&bar[kEmpty0 + s]);
+            }
+        } else if (warp >= kWgA && warp < kWgB) {
+            // ---------------- epilogue A: E1 (P, row sums) and E3 (S copies)
+            const int t = tid - kWgA * 32;
+            for (int it = 0; it < n; ++it) {
+                const int c = cb + it;
+                const int L = min(kC, p.T - c * kC);
+                bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
+                if (named_bar_or(kBarA, 128, !ok)) break;
+                fence_after_sync();
+                const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
+                const int i = row;
+                float rsum = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < kC; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(sc + c0, r);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+                    // gamma^(i-j) by a running product from the piece's top column down
+                    const int jt = min(i, c0 + 31);
+                    float w = (unit_gamma || jt < c0) ? 1.f : gamma_pow(l2g, (float)(i - jt));
+                    float a[32];
+#pragma unroll
+                    for (int e = 31; e >= 0; --e) {
+                        const int j = c0 + e;
+                        float x = 0.f;
+                        if (j <= i) {
+                            x = __uint_as_float(r[e]);
+                            if (!unit_gamma) {
+                                x *= w;
+                                w *= gam;
+                            }
+                        }
+                        a[e] = x;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint32_t u = pack_bf16x2(a[e], a[e + 1]);
+                        pk[e >> 1] = u;
+                        if (NORM) {
+                            const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+                            rsum += back.x + back.y;
+                        }
+                    }
+                    tmem_st16(sc + (c0 >> 1), pk);
+                }
+                if (NORM) tmem_st1(tbase + lane_off + Lay::kColR + (it & 3), __float_as_uint(rsum));
+                tmem_st_wait();
+                // E3 needs S after MMA4 of the previous chunk
+                if (it >= 1) {
+                    ok = mbar_wait_or_abort(&bar[kOfull], (it - 1) & 1, lim, abort_flag);
+                    if (named_bar_or(kBarA, 128, !ok)) break;
+                    fence_after_sync();
+                }
+                const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
+                    tmem_ld_wait();
+                    if (row < DK) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            const int v = c0 + e8;
+                            uint4 wv;
+                            wv.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
+                            wv.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
+                            wv.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
+                            wv.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
+                            *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                      sw128_offset(row, v & 63)) = wv;
+                        }
+                    }
+                    if (!unit_gamma) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gL);
+                        tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
+                    }
+                }
+                if (!unit_gamma) tmem_st_wait();
+                fence_proxy_async_smem();
+                fence_before_sync();
+                named_bar_sync(kBarA, 128);
+                if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
+            }
+        } else if (warp >= kWgB) {
+            // ---------------- epilogue B: phi, scalings, normaliser, E2
+            const int t = tid - kWgB * 32;
+            float qz_prev = 0.f, qz_cur = 0.f;
+            int L_prev = 0;
+            bool stop = false;
+            // phi on the Q/K tiles of chunk `it` (rows >= L zeroed), then release MMA1
+            auto do_phi = [&](int it) -> bool {
+                const int s = it & 1;
+                const int L = min(kC, p.T - (cb + it) * kC);
+                bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it >> 1) & 1, lim, abort_flag);
+                if (named_bar_or(kBarB, 128, !ok)) return false;
+                char* st = sm + s * Lay::kStage;
+                row_pass(st, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
+                row_pass(st + Lay::kQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
+                fence_proxy_async_smem();
+                named_bar_sync(kBarB, 128);
+                if (t == 0) mbar_arrive(&bar[kQk0 + s]);
+                return true;
+            };
+            // E2 of chunk `it`: O rows -> global, normalised
+            auto do_e2 = [&](int it, float qz, int L) -> bool {
+                bool ok = mbar_wait_or_abort(&bar[kOfull], it & 1, lim, abort_flag);
+                if (named_bar_or(kBarB, 128, !ok)) return false;
+                fence_after_sync();
+                float inv = 1.f;
+                if (NORM) {
+                    const float rs = __uint_as_float(tmem_ld1(tbase + lane_off + Lay::kColR + (it & 3)));
+                    tmem_ld_wait();
+                    inv = 1.f / (rs + qz + p.eps);
+                }
+                const int c = cb + it;
+                __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColO + c0, r);
+                    tmem_ld_wait();
+                    if (row < L) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            uint4 wv;
+                            wv.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
+                            wv.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
+                            wv.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
+                            wv.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c0 + e8) = wv;
+                        }
+                    }
+                }
+                fence_before_sync();
+                named_bar_sync(kBarB, 128);
+                if (t == 0) mbar_arrive(&bar[kOempty]);
+                return true;
+            };
+            if (p.phi && !do_phi(0)) stop = true;
+            for (int it = 0; it < n && !stop; ++it) {
+                const int s = it & 1;
+                const int c = cb + it;
+                const int L = min(kC, p.T - c * kC);
+                char* tQ = sm + s * Lay::kStage;
+                char* tK = tQ + Lay::kQ;
+                if (p.phi && it + 1 < n && !do_phi(it + 1)) break;
+                // MMA1 of this chunk is done with the unscaled tiles
+                bool ok = mbar_wait_or_abort(&bar[kSfull0 + s], (it >> 1) & 1, lim, abort_flag);
+                if (named_bar_or(kBarB, 128, !ok)) break;
+                if (!unit_gamma) {
+                    row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); }, t, 128);
+                    row_pass(tK, DK / 64, false,
+                             [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; }, t, 128);
+                    fence_proxy_async_smem();
+                    named_bar_sync(kBarB, 128);
+                }
+                if (NORM || p.track_z) {
+                    if (NORM) {  // qz_i = q^_i . z_{c-1}
+                        float acc = 0.f;
+#pragma unroll 4
+                        for (int d8 = 0; d8 < DK; d8 += 8) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(tQ + (d8 >> 6) * kBlk +
+                                                                            sw128_offset(row, d8 & 63));
+                            const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 x = __bfloat1622float2(hq[e]);
+                                acc = fmaf(x.x, zs[d8 + 2 * e], acc);
+                                acc = fmaf(x.y, zs[d8 + 2 * e + 1], acc);
+                            }
+                        }
+                        qz_cur = acc;
+                    }
+                    // z_c = gamma^L z_{c-1} + sum_j K^[j] (rows >= L of K^ are zero)
+                    float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+                    colsum_partial<DK>(tK, t, zpart);
+                    named_bar_sync(kBarB, 128);  // partials written; every read of z_{c-1} done
+                    if (t < DK) {
+                        const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
+                        zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
+                    }
+                }
+                fence_before_sync();
+                named_bar_sync(kBarB, 128);
+                if (t == 0) {
+                    mbar_arrive(&bar[kPready0 + (it & 1)]);
+                    mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
+                }
+                if (it >= 1 && !do_e2(it - 1, qz_prev, L_prev)) {
+                    stop = true;
+                    break;
+                }
+                qz_prev = qz_cur;
+                L_prev = L;
+            }
+            if (!stop && !*abort_flag) {
+                if (do_e2(n - 1, qz_prev, L_prev)) {
+                    // exit state: S after MMA4 of the last chunk (waited in do_e2)
+                    if (p.S_out) {
+                        const bool write = !p.out_last_only || seg == p.n_seg - 1;
+                        const int oidx = bh * p.out_nseg + (p.out_last_only ? 0 : seg);
+                        for (int c0 = 0; c0 < DVB; c0 += 32) {
+                            uint32_t r[32];
+                            tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
+                            tmem_ld_wait();
+                            if (write && row < DK) {
+                                float* srow = p.S_out + ((size_t)oidx * DK + row) * p.dv + v0 + c0;
+#pragma unroll
+                                for (int e = 0; e < 32; e += 4)
+                                    *reinterpret_cast<float4*>(srow + e) =
+                                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                                    __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                            }
+                        }
+                        if (write && p.z_out && dvb == 0 && row < DK)
+                            p.z_out[(size_t)oidx * DK + row] = zs[row];
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (*abort_flag || forced) {
+        record_status(p.dev_status, LA_ERR_TIMEOUT);
+        if (warp == 0 && lane == 0) {  // our own TMA fills must land before the smem is released
+            for (int s = 0; s < 2; ++s)
+                if (fills[s] > 0) mbar_wait(&bar[kFull0 + s], (fills[s] - 1) & 1, lim);
+        }
+        if (warp == 1 && lane == 0 && mma_issued) {  // and our MMAs before TMEM is freed
+            mma_commit(&bar[kDrain]);
+            mbar_wait(&bar[kDrain], 0, lim);
+        }
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+    if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int DK, int DVB, bool NORM>
+cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s) {
+    using Lay = LayoutWS<DK, DVB>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    TraceScope trace("chunk_tc_ws_kernel/full", s);
+    kern<<<grid, kThreadsWS, Lay::kAlloc, s>>>(prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_ws_supported(int dk, int dvb, bool normalize) {
+    const char* pin = std::getenv("LA_TC_KERNEL");
+    if (pin && std::strcmp(pin, "lockstep") == 0) return false;
+    if (dk != 64 && dk != 128) return false;
+    if (dvb == 64) return true;
+    return dvb == 128 && !normalize;
+}
+
+cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
+                               cudaStream_t s) {
+    if (grid <= 0) return cudaSuccess;
+    if (normalize) {
+        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true>(prm, grid, s);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true>(prm, grid, s);
+        return cudaErrorInvalidValue;
+    }
+    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false>(prm, grid, s);
+    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false>(prm, grid, s);
+    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false>(prm, grid, s);
+    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false>(prm, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace la

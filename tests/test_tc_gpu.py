@@ -37,6 +37,18 @@ def tc_path(monkeypatch):
     monkeypatch.setenv("LA_CHUNK_PATH", "tc")
 
 
+@pytest.fixture(params=["pipelined", "lockstep"])
+def tc_kernel(request, monkeypatch):
+    """Both tensor-core output kernels: the warp-specialised pipeline (default
+    where it applies) and the lockstep kernel (LA_TC_KERNEL=lockstep)."""
+    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    if request.param == "lockstep":
+        monkeypatch.setenv("LA_TC_KERNEL", "lockstep")
+    else:
+        monkeypatch.delenv("LA_TC_KERNEL", raising=False)
+    return request.param
+
+
 def run(x, phi, normalize, causal=True, S0=None, z0=None, dev_status=None):
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     B, H, T, dk = q.shape
@@ -68,7 +80,7 @@ TC_SHAPES = [  # B, H, T, dk, dv
 @pytest.mark.parametrize("flags", [(False, False), (True, True), (True, False)],
                          ids=lambda f: f"phi{int(f[0])}_norm{int(f[1])}")
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_tc_matches_oracle(shape, flags, tc_path):
+def test_tc_matches_oracle(shape, flags, tc_kernel):
     B, H, T, dk, dv = shape
     phi, normalize = flags
     seed = zlib.crc32(repr((shape, flags, "tc")).encode()) % 100000
@@ -82,7 +94,7 @@ def test_tc_matches_oracle(shape, flags, tc_path):
 
 
 @pytest.mark.parametrize("gamma", [[0.5, 0.9], [1.0, 0.999], [0.05, 0.99]])
-def test_tc_decay_extremes(gamma, tc_path):
+def test_tc_decay_extremes(gamma, tc_kernel):
     """Small decays underflow instead of overflowing; gamma = 1 skips the scaling."""
     x = workloads.random_case(31, 1, 2, 700, 128, 128, dtype="bf16", gamma=gamma)
     O, S, _ = run(x, False, False)
@@ -91,7 +103,7 @@ def test_tc_decay_extremes(gamma, tc_path):
     check("S_T", S, Sr)
 
 
-def test_tc_resume_from_state(tc_path):
+def test_tc_resume_from_state(tc_kernel):
     x = workloads.random_case(41, 2, 2, 900, 128, 128, dtype="bf16")
     Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=True, normalize=True)
     t1 = 389
@@ -133,10 +145,9 @@ def test_tc_is_the_default_for_supported_shapes():
     assert la.workspace_size(1, 8, 65536, 128, 128) > 0  # long and few: segmented
 
 
-def test_timeout_is_reported_not_hung(monkeypatch):
+def test_timeout_is_reported_not_hung(monkeypatch, tc_kernel):
     """A wait that runs out (on a barrier nothing arrives on) sets dev_status; the
     context stays usable."""
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
     monkeypatch.setenv("LA_DEBUG_FORCE_TIMEOUT", "1")
     x = workloads.random_case(71, 1, 2, 256, 64, 64, dtype="bf16")
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -159,7 +170,7 @@ def test_launch_trace_names_the_kernels():
     finally:
         la.trace_enable(0)
     names = [n for n, _ in recs]
-    assert "chunk_tc_kernel/full" in names
+    assert any(n.endswith("/full") for n in names), names
     assert all(ms > 0.0 for _, ms in recs)
     n = la.library().la_chunk_fwd_launches(1, 1, 4096, 64, 64, 1, 3, 0)
     assert len(names) == n, (names, n)
