@@ -519,7 +519,7 @@ cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
 
 }  // namespace
 
-bool tc_ws_supported(int dk, int dvb, bool normalize);
+bool tc_ws_supported(int mode, int dk, int dvb, bool normalize);
 cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
                                cudaStream_t s);
 
@@ -527,7 +527,7 @@ namespace {
 
 cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    if (prm.mode == kFull && tc_ws_supported(dk, dvb, prm.normalize != 0))
+    if (tc_ws_supported(prm.mode, dk, dvb, prm.normalize != 0))
         return launch_chunk_tc_ws(dk, dvb, prm.normalize != 0, prm, grid, s);
     if (dk == 64 && dvb == 64) return launch_tc<64, 64>(prm, grid, s);
     if (dk == 64 && dvb == 128) return launch_tc<64, 128>(prm, grid, s);
@@ -544,12 +544,14 @@ int sm_count() {
 }
 
 // Segments per sequence: enough units to cover the SMs once.
+// Segments per sequence: as many as fit the SMs in one wave (the kernels run
+// one CTA per SM), when that is at least two and each segment keeps two or
+// more chunks.
 int choose_segments(int units, int n_chunks) {
     const int sms = sm_count();
-    if (units * 4 >= sms * 3 || n_chunks < 4) return 1;
-    int P = (sms + units - 1) / units;
+    int P = sms / units;
     if (P > n_chunks / 2) P = n_chunks / 2;
-    return P < 1 ? 1 : P;
+    return P < 2 ? 1 : P;
 }
 
 // Entry state of every segment from the segments' own contributions:

@@ -55,6 +55,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
+// phi = elu + 1 on a bf16 pair in bf16x2 arithmetic: x + 1 for x >= 0, e^x
+// for x < 0 (the two agree at 0).  Each half is selected by its sign bit.
+__device__ __forceinline__ __nv_bfloat162 phi_bf16x2(__nv_bfloat162 x) {
+    const __nv_bfloat162 xp1 = __hadd2(x, __float2bfloat162_rn(1.f));
+    const __nv_bfloat162 e = h2exp(x);
+    const uint32_t xb = *reinterpret_cast<const uint32_t*>(&x);
+    const uint32_t neg = ((xb & 0x80008000u) >> 15) * 0xFFFFu;  // all-ones halves where x < 0
+    const uint32_t r = (*reinterpret_cast<const uint32_t*>(&e) & neg) |
+                       (*reinterpret_cast<const uint32_t*>(&xp1) & ~neg);
+    return *reinterpret_cast<const __nv_bfloat162*>(&r);
+}
+
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`
 // threads (this one is `t`): apply phi (optional) and multiply row r by
 // fac(r).  Rows are whole 128-byte lines, so the swizzle never moves an
@@ -69,14 +81,16 @@ __device__ __forceinline__ void row_pass(char* tile, int nblk, bool apply_phi, F
         uint4 u = *p;
         const float f = fac(r);
         __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+        if (apply_phi) {
+            const __nv_bfloat162 ff = __float2bfloat162_rn(f);  // f is 0 or 1 here
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float2 x = __bfloat1622float2(h[e]);
-            if (apply_phi) {
-                x.x = phi_f(x.x);
-                x.y = phi_f(x.y);
+            for (int e = 0; e < 4; ++e) h[e] = __hmul2(phi_bf16x2(h[e]), ff);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = __bfloat1622float2(h[e]);
+                h[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
             }
-            h[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
         }
         *p = u;
     }

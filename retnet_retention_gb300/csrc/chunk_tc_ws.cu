@@ -5,7 +5,7 @@
 // Representation", "RetNet" page; equations in chunk_tc.cu's header), but
 // the roles run concurrently and hand work over through mbarriers:
 //
-//   warp 0      TMA producer: Q, K, V of chunk c into a two-stage ring
+//   warp 0      TMA producer: Q, K, V of chunk c into a ring of 2-4 stages
 //   warp 1      MMA issuer (one thread): MMA1 of chunk c+1 is issued ahead of
 //               MMA2..4 of chunk c, into the other of two TMEM score buffers
 //   warps 2-5   epilogue A: E1 (scores -> decay mask -> bf16 P back into
@@ -45,6 +45,8 @@ constexpr int kBarB = 2;
 constexpr uint32_t kColScores = 0;  // + 128 * buffer
 constexpr uint32_t kColO = 256;
 
+constexpr uint32_t kSmemLimit = 232448;  // opt-in shared memory per CTA
+
 template <int DK, int DVB>
 struct LayoutWS {
     static constexpr uint32_t kQ = (DK / 64) * kBlk;
@@ -52,26 +54,36 @@ struct LayoutWS {
     static constexpr uint32_t kV = (DVB / 64) * kBlk;
     static constexpr uint32_t kStage = kQ + kK + kV;
     static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // bf16 S, MN-major
-    static constexpr uint32_t oSB = 2 * kStage;
+    static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + 24 * 8 + 16 + 1024;
+    // ring depth: as many stages (up to 4) as shared memory holds
+    static constexpr int NS = (4 * kStage + kSB + kSmall <= kSmemLimit) ? 4
+                            : (3 * kStage + kSB + kSmall <= kSmemLimit) ? 3 : 2;
+    static constexpr uint32_t oSB = NS * kStage;
     static constexpr uint32_t oZ = oSB + kSB;           // float z[DK]
     static constexpr uint32_t oZP = oZ + DK * 4;        // float colsum partials [256/DK][DK]
-    static constexpr uint32_t oBar = oZP + 256 * 4;     // 16 mbarriers
-    static constexpr uint32_t oFlags = oBar + 16 * 8;   // int abort, uint32 tmem slot
+    static constexpr uint32_t oBar = oZP + 256 * 4;     // 24 mbarrier slots
+    static constexpr uint32_t oFlags = oBar + 24 * 8;   // int abort, uint32 tmem slot
     static constexpr uint32_t kBytes = oFlags + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
     static constexpr uint32_t kColS = kColO + DVB;
     static constexpr uint32_t kColR = 384;              // row sums, 4 rotating columns (DVB = 64)
+    static_assert(kAlloc <= kSmemLimit, "shared memory budget");
 };
 
-// Barriers.  Per-chunk hand-overs that one side could otherwise complete twice
-// before the other side waits once are double-buffered by chunk parity
-// (full, empty, qk, sfull, pready); o_full / o_empty cannot run ahead.
+// Barriers.  Stage barriers (full, empty, qk) have one slot per ring stage;
+// hand-overs that one side could otherwise complete twice before the other
+// side waits once are double-buffered by chunk parity (sfull, pready);
+// o_full / o_empty cannot run ahead.
 enum Bars {
-    kFull0 = 0, kFull1, kEmpty0, kEmpty1, kQk0, kQk1, kSfull0, kSfull1,
-    kPready0, kPready1, kOfull, kOempty, kNever, kDrain, kNumBars
+    kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
+    kOfull, kOempty, kNever, kDrain, kNumBars
 };
 
-template <int DK, int DVB, bool NORM>
+// STATE_ONLY: the walk of a segment's own state contribution (mode
+// kStateOnly: K and V only, MMA4 only).  Its per-chunk hand-over to the
+// issuer (kReadyS) has one slot per ring stage, which bounds how far the
+// epilogues may run ahead.
+template <int DK, int DVB, bool NORM, bool STATE_ONLY>
 __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
     using Lay = LayoutWS<DK, DVB>;
     static_assert(!NORM || DVB == 64, "row-sum columns exist only for DVB = 64");
@@ -100,12 +112,14 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     const int n = ce - cb;  // chunks of this unit
     const uint64_t lim = p.wait_ns;
 
+    constexpr int NS = Lay::NS;
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
-        mbar_init(&bar[kEmpty0], 2);  // MMA commit + epilogue B
-        mbar_init(&bar[kEmpty1], 2);
+        for (int q = 0; q < NS; ++q) mbar_init(&bar[kEmpty0 + q], 2);  // MMA commit + epilogue B
         mbar_init(&bar[kPready0], 2);  // epilogue A + epilogue B
         mbar_init(&bar[kPready1], 2);
+        // state walk: epilogue B, plus epilogue A when S must be rescaled (gamma < 1)
+        for (int q = 0; q < NS; ++q) mbar_init(&bar[kReadyS0 + q], unit_gamma ? 1 : 2);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&p.tmQ);
@@ -133,7 +147,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     // ---- entry state into TMEM (epilogue B owns all 128 lanes), z into smem
     if (!forced && warp >= kWgB) {
         const int sidx = bh * p.in_nseg + seg;
-        const bool has_in = p.S_in != nullptr;
+        const bool has_in = p.S_in != nullptr && !STATE_ONLY;
         for (int c0 = 0; c0 < DVB; c0 += 32) {
             uint32_t r[32];
 #pragma unroll
@@ -152,22 +166,23 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     fence_after_sync();
 
     // per-role bookkeeping that the drain at the end needs
-    int fills[2] = {0, 0};     // producer: TMA fills issued per stage
+    int fills[4] = {0, 0, 0, 0};  // producer: TMA fills issued per stage
     bool mma_issued = false;   // issuer: any MMA issued
 
     if (!forced && n > 0) {
         if (warp == 0 && lane == 0) {
             // ---------------- producer
             for (int it = 0; it < n; ++it) {
-                const int s = it & 1;
-                if (it >= 2 && !mbar_wait_or_abort(&bar[kEmpty0 + s], ((it - 2) >> 1) & 1, lim, abort_flag))
+                const int s = it % NS;
+                if (it >= NS &&
+                    !mbar_wait_or_abort(&bar[kEmpty0 + s], ((it - NS) / NS) & 1, lim, abort_flag))
                     break;
                 char* st = sm + s * Lay::kStage;
                 const int y = (cb + it) * kC;
-                mbar_arrive_expect_tx(&bar[kFull0 + s], Lay::kStage);
+                mbar_arrive_expect_tx(&bar[kFull0 + s], STATE_ONLY ? Lay::kK + Lay::kV : Lay::kStage);
 #pragma unroll
                 for (int b = 0; b < DK / 64; ++b) {
-                    tma_load_3d(st + b * kBlk, &p.tmQ, b * 64, y, bh, &bar[kFull0 + s]);
+                    if (!STATE_ONLY) tma_load_3d(st + b * kBlk, &p.tmQ, b * 64, y, bh, &bar[kFull0 + s]);
                     tma_load_3d(st + Lay::kQ + b * kBlk, &p.tmK, b * 64, y, bh, &bar[kFull0 + s]);
                 }
 #pragma unroll
@@ -182,8 +197,8 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
             const uint32_t id_pv = idesc_bf16(128, DVB, 0, 1);
             const uint32_t id_kv = idesc_bf16(128, DVB, 1, 1);
             auto issue_mma1 = [&](int it) -> bool {
-                const int s = it & 1;
-                const uint32_t par = (it >> 1) & 1;
+                const int s = it % NS;
+                const uint32_t par = (it / NS) & 1;
                 if (!mbar_wait_or_abort(&bar[kFull0 + s], par, lim, abort_flag)) return false;
                 if (p.phi && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag)) return false;
                 fence_after_sync();
@@ -198,9 +213,26 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 mma_issued = true;
                 return true;
             };
-            bool ok = issue_mma1(0);
+            if constexpr (STATE_ONLY) {
+                for (int it = 0; it < n; ++it) {
+                    const int s = it % NS;
+                    if (!mbar_wait_or_abort(&bar[kReadyS0 + s], (it / NS) & 1, lim, abort_flag)) break;
+                    fence_after_sync();
+                    const uint32_t ka = sbase + s * Lay::kStage + Lay::kQ, va = ka + Lay::kK;
+#pragma unroll
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
+                               smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
+                    mma_commit(&bar[kOfull]);
+                    mma_commit(&bar[kEmpty0 + s]);
+                    mma_issued = true;
+                }
+                (void)issue_mma1;
+                (void)id_pv;
+            }
+            bool ok = !STATE_ONLY && issue_mma1(0);
             for (int it = 0; it < n && ok; ++it) {
-                const int s = it & 1;
+                const int s = it % NS;
                 if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
                 if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag)) break;
                 if (it >= 1 && !mbar_wait_or_abort(&bar[kOempty], (it - 1) & 1, lim, abort_flag)) break;
@@ -229,7 +261,31 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         } else if (warp >= kWgA && warp < kWgB) {
             // ---------------- epilogue A: E1 (P, row sums) and E3 (S copies)
             const int t = tid - kWgA * 32;
-            for (int it = 0; it < n; ++it) {
+            if constexpr (STATE_ONLY) {
+                // only S = gamma^L S before each MMA4 (nothing to do when gamma == 1)
+                for (int it = 0; it < n && !unit_gamma; ++it) {
+                    const int L = min(kC, p.T - (cb + it) * kC);
+                    if (it >= 1) {
+                        bool ok = mbar_wait_or_abort(&bar[kOfull], (it - 1) & 1, lim, abort_flag);
+                        if (named_bar_or(kBarA, 128, !ok)) break;
+                        fence_after_sync();
+                    }
+                    const float gL = gamma_pow(l2g, (float)L);
+                    for (int c0 = 0; c0 < DVB; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gL);
+                        tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
+                    }
+                    tmem_st_wait();
+                    fence_before_sync();
+                    named_bar_sync(kBarA, 128);
+                    if (t == 0) mbar_arrive(&bar[kReadyS0 + it % NS]);
+                }
+            }
+            for (int it = 0; it < n && !STATE_ONLY; ++it) {
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
@@ -318,9 +374,9 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
             bool stop = false;
             // phi on the Q/K tiles of chunk `it` (rows >= L zeroed), then release MMA1
             auto do_phi = [&](int it) -> bool {
-                const int s = it & 1;
+                const int s = it % NS;
                 const int L = min(kC, p.T - (cb + it) * kC);
-                bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it >> 1) & 1, lim, abort_flag);
+                bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 char* st = sm + s * Lay::kStage;
                 row_pass(st, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
@@ -329,6 +385,26 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 named_bar_sync(kBarB, 128);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
                 return true;
+            };
+            // exit state: S (after the last MMA4, which the caller has waited for) and z
+            auto write_exit_state = [&]() {
+                if (!p.S_out) return;
+                const bool write = !p.out_last_only || seg == p.n_seg - 1;
+                const int oidx = bh * p.out_nseg + (p.out_last_only ? 0 : seg);
+                for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
+                    tmem_ld_wait();
+                    if (write && row < DK) {
+                        float* srow = p.S_out + ((size_t)oidx * DK + row) * p.dv + v0 + c0;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(srow + e) =
+                                make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                            __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                    }
+                }
+                if (write && p.z_out && dvb == 0 && row < DK) p.z_out[(size_t)oidx * DK + row] = zs[row];
             };
             // E2 of chunk `it`: O rows -> global, normalised
             auto do_e2 = [&](int it, float qz, int L) -> bool {
@@ -364,16 +440,61 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 if (t == 0) mbar_arrive(&bar[kOempty]);
                 return true;
             };
-            if (p.phi && !do_phi(0)) stop = true;
+            if constexpr (STATE_ONLY) {
+                for (int it = 0; it < n; ++it) {
+                    const int s = it % NS;
+                    const int L = min(kC, p.T - (cb + it) * kC);
+                    char* tK = sm + s * Lay::kStage + Lay::kQ;
+                    bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
+                    if (named_bar_or(kBarB, 128, !ok)) {
+                        stop = true;
+                        break;
+                    }
+                    // K^ = zeta . phi(K), rows >= L zeroed
+                    if (p.phi || !unit_gamma)
+                        row_pass(tK, DK / 64, p.phi != 0,
+                                 [&](int r) {
+                                     return r < L ? (unit_gamma ? 1.f : gamma_pow(l2g, (float)(L - 1 - r)))
+                                                  : 0.f;
+                                 },
+                                 t, 128);
+                    named_bar_sync(kBarB, 128);
+                    if (p.track_z) {  // z_c = gamma^L z_{c-1} + sum_j K^[j]
+                        float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+                        colsum_partial<DK>(tK, t, zpart);
+                        named_bar_sync(kBarB, 128);
+                        if (t < DK) {
+                            const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
+                            zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    fence_before_sync();
+                    named_bar_sync(kBarB, 128);
+                    if (t == 0) {
+                        mbar_arrive(&bar[kReadyS0 + s]);
+                        mbar_arrive(&bar[kEmpty0 + s]);
+                    }
+                }
+                if (!stop && !*abort_flag) {
+                    bool ok = mbar_wait_or_abort(&bar[kOfull], (n - 1) & 1, lim, abort_flag);
+                    if (!named_bar_or(kBarB, 128, !ok)) {
+                        fence_after_sync();
+                        write_exit_state();
+                    }
+                }
+                stop = true;
+            }
+            if (p.phi && !stop && !do_phi(0)) stop = true;
             for (int it = 0; it < n && !stop; ++it) {
-                const int s = it & 1;
+                const int s = it % NS;
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 char* tQ = sm + s * Lay::kStage;
                 char* tK = tQ + Lay::kQ;
                 if (p.phi && it + 1 < n && !do_phi(it + 1)) break;
                 // MMA1 of this chunk is done with the unscaled tiles
-                bool ok = mbar_wait_or_abort(&bar[kSfull0 + s], (it >> 1) & 1, lim, abort_flag);
+                bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
                 if (!unit_gamma) {
                     row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); }, t, 128);
@@ -421,29 +542,8 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 qz_prev = qz_cur;
                 L_prev = L;
             }
-            if (!stop && !*abort_flag) {
-                if (do_e2(n - 1, qz_prev, L_prev)) {
-                    // exit state: S after MMA4 of the last chunk (waited in do_e2)
-                    if (p.S_out) {
-                        const bool write = !p.out_last_only || seg == p.n_seg - 1;
-                        const int oidx = bh * p.out_nseg + (p.out_last_only ? 0 : seg);
-                        for (int c0 = 0; c0 < DVB; c0 += 32) {
-                            uint32_t r[32];
-                            tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
-                            tmem_ld_wait();
-                            if (write && row < DK) {
-                                float* srow = p.S_out + ((size_t)oidx * DK + row) * p.dv + v0 + c0;
-#pragma unroll
-                                for (int e = 0; e < 32; e += 4)
-                                    *reinterpret_cast<float4*>(srow + e) =
-                                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                                    __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-                            }
-                        }
-                        if (write && p.z_out && dvb == 0 && row < DK)
-                            p.z_out[(size_t)oidx * DK + row] = zs[row];
-                    }
-                }
+            if (!STATE_ONLY && !stop && !*abort_flag) {
+                if (do_e2(n - 1, qz_prev, L_prev)) write_exit_state();  // do_e2 waited for MMA4
             }
         }
     }
@@ -455,7 +555,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     if (*abort_flag || forced) {
         record_status(p.dev_status, LA_ERR_TIMEOUT);
         if (warp == 0 && lane == 0) {  // our own TMA fills must land before the smem is released
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < NS; ++s)
                 if (fills[s] > 0) mbar_wait(&bar[kFull0 + s], (fills[s] - 1) & 1, lim);
         }
         if (warp == 1 && lane == 0 && mma_issued) {  // and our MMAs before TMEM is freed
@@ -469,40 +569,49 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int DK, int DVB, bool NORM>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s) {
     using Lay = LayoutWS<DK, DVB>;
-    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
-    TraceScope trace("chunk_tc_ws_kernel/full", s);
+    TraceScope trace(STATE_ONLY ? "chunk_tc_ws_kernel/state" : "chunk_tc_ws_kernel/full", s);
     kern<<<grid, kThreadsWS, Lay::kAlloc, s>>>(prm);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool tc_ws_supported(int dk, int dvb, bool normalize) {
+bool tc_ws_supported(int mode, int dk, int dvb, bool normalize) {
     const char* pin = std::getenv("LA_TC_KERNEL");
     if (pin && std::strcmp(pin, "lockstep") == 0) return false;
     if (dk != 64 && dk != 128) return false;
-    if (dvb == 64) return true;
-    return dvb == 128 && !normalize;
+    if (dvb != 64 && dvb != 128) return false;
+    if (mode == kStateOnly) return true;
+    if (mode != kFull) return false;
+    return dvb == 64 || !normalize;
 }
 
 cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
                                cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    if (normalize) {
-        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true>(prm, grid, s);
-        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true>(prm, grid, s);
+    if (prm.mode == kStateOnly) {
+        if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, true>(prm, grid, s);
+        if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, true>(prm, grid, s);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true>(prm, grid, s);
+        if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true>(prm, grid, s);
         return cudaErrorInvalidValue;
     }
-    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false>(prm, grid, s);
-    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false>(prm, grid, s);
-    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false>(prm, grid, s);
-    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false>(prm, grid, s);
+    if (normalize) {
+        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true, false>(prm, grid, s);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true, false>(prm, grid, s);
+        return cudaErrorInvalidValue;
+    }
+    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false>(prm, grid, s);
+    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false>(prm, grid, s);
+    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false>(prm, grid, s);
+    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, false>(prm, grid, s);
     return cudaErrorInvalidValue;
 }
 
