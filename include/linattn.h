@@ -178,6 +178,40 @@ LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, 
                                    int* dev_status, la_stream_t stream);
 
 /*
+ * la_chunk_fwd for callers that cannot allocate device memory.  The source
+ * pages have no counterpart to this entry point.
+ *
+ * la_chunk_fwd may need caller-provided scratch (la_workspace_size).  Some
+ * callers cannot call cudaMalloc: a plugin inside a host framework that owns
+ * every device allocation and passes the plugin only its inputs and outputs,
+ * or a serving loop that must not allocate once running (cudaMalloc can
+ * synchronise the device and can fail under memory pressure).  This entry
+ * point takes the same arguments as la_chunk_fwd minus the workspace and
+ * uses instead a fixed scratch array compiled into the library: a file-scope
+ * device array of LA_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the
+ * library holds until the process exits.  It allocates nothing.
+ *
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Calls whose la_workspace_size exceeds LA_NOALLOC_SCRATCH_BYTES return
+ *     LA_ERR_INVALID_ARG without launching anything.
+ *   - Every call shares the one array, and the array keeps whatever the last
+ *     call left in it.  Nothing needs clearing: each call writes every scratch
+ *     byte it later reads.  Calls that overlap on the GPU (different streams,
+ *     or host threads) race on the array and give wrong results; serialise
+ *     them.
+ *   - Errors otherwise as la_chunk_fwd; LA_ERR_CUDA if the address lookup fails.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
+LA_API la_status la_chunk_fwd_noalloc(const void* Q, const void* K, const void* V,
+                                      la_dtype dtype, const float* gamma, int B, int H, int T,
+                                      int d_k, int d_v, unsigned flags, float eps,
+                                      const float* S0, const float* z0,
+                                      void* O, float* S_out, float* z_out, int chunk,
+                                      int* dev_status, la_stream_t stream);
+
+/*
  * Launch tracing (profiling aid; no counterpart on the pages).  While enabled,
  * the library records a pair of CUDA events on the launching stream around
  * every kernel it enqueues, for up to `capacity` launches (capacity <= 0

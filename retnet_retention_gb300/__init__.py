@@ -78,6 +78,9 @@ def _load() -> ctypes.CDLL:
     lib.la_recurrent_step.restype = i
     lib.la_chunk_fwd_launches.argtypes = [i, i, i, i, i, i, u, i]
     lib.la_chunk_fwd_launches.restype = i
+    lib.la_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
+                                         vp, i, vp, vp]
+    lib.la_chunk_fwd_noalloc.restype = i
     lib.la_trace_enable.argtypes = [i]
     lib.la_trace_enable.restype = i
     lib.la_trace_collect.argtypes = [ctypes.POINTER(TraceRecord), i]
@@ -196,6 +199,25 @@ def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e
     return out, S_out, z_out
 
 
+def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
+                      S0=None, z0=None, chunk=0, out=None, S_out=None, z_out=None,
+                      dev_status=None, stream=None):
+    """chunk_fwd through la_chunk_fwd_noalloc: no workspace argument; the library's
+    fixed scratch array is used instead (for callers that cannot allocate device
+    memory).  out / S_out / z_out must be given: this call allocates nothing."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if out is None or S_out is None:
+        raise ValueError("chunk_fwd_noalloc allocates nothing: pass out and S_out")
+    g = _gamma_host(gamma, H)
+    st = _load().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
+                                      H, T, dk, dv, _flags(phi, normalize, causal), float(eps),
+                                      _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out), _ptr(z_out),
+                                      int(chunk), _ptr(dev_status), _stream(stream))
+    _check(st, "la_chunk_fwd_noalloc")
+    return out, S_out, z_out
+
+
 def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps=1e-6,
                    out=None, dev_status=None, stream=None):
     """One decode step on [B,H,d] device tensors; S (and z) are updated in place."""
@@ -237,7 +259,7 @@ def chunk_fwd_host(q, k, v, gamma, *, device="cuda", stream=None, **kw):
     return Oh, Sh, zh
 
 
-__all__ = ["chunk_fwd", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
+__all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
            "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
            "LA_NORMALIZE", "LA_NONCAUSAL"]
