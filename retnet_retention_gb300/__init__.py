@@ -233,30 +233,82 @@ def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps
     return out
 
 
-def chunk_fwd_host(q, k, v, gamma, *, device="cuda", stream=None, **kw):
+_SIDE_STREAMS: dict = {}
+
+
+def _side_streams(device, n: int):
+    key = (str(device), n)
+    if key not in _SIDE_STREAMS:
+        _SIDE_STREAMS[key] = [torch.cuda.Stream(device=device) for _ in range(n)]
+    return _SIDE_STREAMS[key]
+
+
+def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
+                   S0=None, z0=None, chunk=0, pieces=None, out=None, S_out=None, z_out=None,
+                   device="cuda", timing=None):
     """la_chunk_fwd on HOST tensors: copy in, compute, copy the results back.
 
-    q, k, v should be pinned CPU tensors for asynchronous copies.  Returns
-    CPU (O, S_T, z_T).  The stream is synchronised before returning.
+    q, k, v (and S0, z0) are CPU tensors, pinned for asynchronous copies.  The
+    batch is cut into `pieces` groups of whole sequences (default min(B, 4));
+    each group's copy in, la_chunk_fwd and copy out run in order on one of two
+    side streams, so the copies of one group overlap the compute of another.
+    Returns host (O, S_T, z_T) (z_T when normalising or when z_out is given),
+    written into out / S_out / z_out when those pinned buffers are passed.
+    With `timing` (a list), the device milliseconds from before the first copy
+    to after the last are appended to it.  Synchronises before returning.
     """
-    s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        qd = q.to(device, non_blocking=True)
-        kd = k.to(device, non_blocking=True)
-        vd = v.to(device, non_blocking=True)
-        O, S_T, z_T = chunk_fwd(qd, kd, vd, gamma, stream=s, **kw)
-        Oh = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
-        Oh.copy_(O, non_blocking=True)
-        Sh = None
-        if S_T is not None:
-            Sh = torch.empty(S_T.shape, dtype=S_T.dtype, pin_memory=True)
-            Sh.copy_(S_T, non_blocking=True)
-        zh = None
-        if z_T is not None:
-            zh = torch.empty(z_T.shape, dtype=z_T.dtype, pin_memory=True)
-            zh.copy_(z_T, non_blocking=True)
-    s.synchronize()
-    return Oh, Sh, zh
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    n = max(1, min(B, pieces if pieces else 4))
+    bounds = [(i * B) // n for i in range(n + 1)]
+    dev = torch.device(device)
+    pin = dict(pin_memory=True)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, **pin)
+    if S_out is None:
+        S_out = torch.empty((B, H, dk, dv), dtype=torch.float32, **pin)
+    if z_out is None and normalize:
+        z_out = torch.empty((B, H, dk), dtype=torch.float32, **pin)
+    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
+    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    Od = torch.empty(out.shape, dtype=out.dtype, device=dev)
+    Sd = torch.empty(S_out.shape, dtype=torch.float32, device=dev)
+    zd = torch.empty(z_out.shape, dtype=torch.float32, device=dev) if z_out is not None else None
+    S0d = torch.empty(S0.shape, dtype=torch.float32, device=dev) if S0 is not None else None
+    z0d = torch.empty(z0.shape, dtype=torch.float32, device=dev) if z0 is not None else None
+    main = torch.cuda.current_stream(dev)
+    sides = _side_streams(dev, 2)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(main)
+    for st in sides:
+        st.wait_event(start)
+    for i in range(n):
+        b0, b1 = bounds[i], bounds[i + 1]
+        if b0 == b1:
+            continue
+        st = sides[i % 2]
+        with torch.cuda.stream(st):
+            for d, h in ((qd, q), (kd, k), (vd, v), (S0d, S0), (z0d, z0)):
+                if d is not None:
+                    d[b0:b1].copy_(h[b0:b1], non_blocking=True)
+            chunk_fwd(qd[b0:b1], kd[b0:b1], vd[b0:b1], gamma, phi=phi, normalize=normalize,
+                      causal=causal, eps=eps,
+                      S0=None if S0d is None else S0d[b0:b1],
+                      z0=None if z0d is None else z0d[b0:b1], chunk=chunk, out=Od[b0:b1],
+                      S_out=Sd[b0:b1], z_out=None if zd is None else zd[b0:b1], stream=st)
+            out[b0:b1].copy_(Od[b0:b1], non_blocking=True)
+            S_out[b0:b1].copy_(Sd[b0:b1], non_blocking=True)
+            if zd is not None:
+                z_out[b0:b1].copy_(zd[b0:b1], non_blocking=True)
+    for st in sides:
+        main.wait_stream(st)
+    end.record(main)
+    end.synchronize()
+    if timing is not None:
+        timing.append(start.elapsed_time(end))
+    return out, S_out, z_out
 
 
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",

@@ -305,3 +305,23 @@ def test_decode_bf16_sampled():
     Or, Sr, _ = oracle.recurrent(qs[None], ks[None], vs[None], g)
     check("decode outputs", np.stack(outs, axis=1), Or[0, :, c["T"]:], TOL["bf16"])
     check("final state", S[bi, hi].double().cpu().numpy(), Sr[0], TOL["bf16"])
+
+
+@pytest.mark.parametrize("pieces", [1, 3])
+def test_host_entry_point_pipelined(pieces):
+    """chunk_fwd_host: pinned host inputs in, host results out, batch split over
+    two side streams; equals the oracle (initial state included)."""
+    x = workloads.random_case(91, 3, 2, 300, 64, 64, dtype="bf16")
+    rng = np.random.default_rng(5)
+    S0 = torch.from_numpy(rng.standard_normal((3, 2, 64, 64)).astype(np.float32) * 0.1)
+    z0 = torch.from_numpy(np.abs(rng.standard_normal((3, 2, 64))).astype(np.float32))
+    times = []
+    O, S, z = la.chunk_fwd_host(x["q"].pin_memory(), x["k"].pin_memory(), x["v"].pin_memory(),
+                                x["gamma"], phi=True, normalize=True, S0=S0.pin_memory(),
+                                z0=z0.pin_memory(), pieces=pieces, timing=times)
+    assert O.device.type == "cpu" and len(times) == 1 and times[0] > 0
+    Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=True, normalize=True,
+                                  S0=S0, z0=z0)
+    check("O", np64(O), Or, TOL["bf16"])
+    check("S_T", np64(S), Sr, TOL["bf16"])
+    check("z_T", np64(z), zr, TOL["bf16"])
