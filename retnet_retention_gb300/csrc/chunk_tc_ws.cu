@@ -65,8 +65,11 @@ struct LayoutWS {
     static constexpr uint32_t oFlags = oBar + 24 * 8;   // int abort, uint32 tmem slot
     static constexpr uint32_t kBytes = oFlags + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
-    static constexpr uint32_t kColS = kColO + DVB;
-    static constexpr uint32_t kColR = 384;              // row sums, 4 rotating columns (DVB = 64)
+    // O accumulators: two for DVB = 64 (E2 of a chunk overlaps the next chunk's MMAs),
+    // one for DVB = 128; then S; then (DVB = 64) four rotating row-sum columns.
+    static constexpr int NOB = DVB == 64 ? 2 : 1;
+    static constexpr uint32_t kColS = kColO + NOB * DVB;
+    static constexpr uint32_t kColR = kColS + DVB;
     static_assert(kAlloc <= kSmemLimit, "shared memory budget");
 };
 
@@ -76,7 +79,7 @@ struct LayoutWS {
 // o_full / o_empty cannot run ahead.
 enum Bars {
     kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
-    kOfull, kOempty, kNever, kDrain, kNumBars
+    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kNumBars
 };
 
 // STATE_ONLY: the walk of a segment's own state contribution (mode
@@ -113,6 +116,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     const uint64_t lim = p.wait_ns;
 
     constexpr int NS = Lay::NS;
+    constexpr int NOB = Lay::NOB;
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
         for (int q = 0; q < NS; ++q) mbar_init(&bar[kEmpty0 + q], 2);  // MMA commit + epilogue B
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     for (int kk = 0; kk < kC / 16; ++kk)
                         mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
                                smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
-                    mma_commit(&bar[kOfull]);
+                    mma_commit(&bar[kOfull0]);
                     mma_commit(&bar[kEmpty0 + s]);
                     mma_issued = true;
                 }
@@ -235,19 +239,23 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 const int s = it % NS;
                 if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
                 if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag)) break;
-                if (it >= 1 && !mbar_wait_or_abort(&bar[kOempty], (it - 1) & 1, lim, abort_flag)) break;
+                const int ob = it % NOB;  // O buffer of this chunk
+                if (it >= NOB &&
+                    !mbar_wait_or_abort(&bar[kOempty0 + ob], ((it - NOB) / NOB) & 1, lim, abort_flag))
+                    break;
                 fence_after_sync();
+                const uint32_t ocol = tbase + kColO + ob * DVB;
                 const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ, va = ka + Lay::kK;
                 // MMA2: O = P V (A = P from TMEM, K = 128 tokens)
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ts(tbase + kColO, tbase + kColScores + (it & 1) * 128 + kk * 8,
+                    mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8,
                            smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_pv, kk > 0);
                 // MMA3: O += Q^ S_bf16 (K = DK)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
-                    mma_ss(tbase + kColO, smem_desc_sw128(qa + off, 16, 1024),
+                    mma_ss(ocol, smem_desc_sw128(qa + off, 16, 1024),
                            smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id_pv, 1u);
                 }
                 // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 for (int kk = 0; kk < kC / 16; ++kk)
                     mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
                            smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
-                mma_commit(&bar[kOfull]);
+                mma_commit(&bar[kOfull0 + ob]);
                 mma_commit(&bar[kEmpty0 + s]);
             }
         } else if (warp >= kWgA && warp < kWgB) {
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 for (int it = 0; it < n && !unit_gamma; ++it) {
                     const int L = min(kC, p.T - (cb + it) * kC);
                     if (it >= 1) {
-                        bool ok = mbar_wait_or_abort(&bar[kOfull], (it - 1) & 1, lim, abort_flag);
+                        bool ok = mbar_wait_or_abort(&bar[kOfull0], (it - 1) & 1, lim, abort_flag);
                         if (named_bar_or(kBarA, 128, !ok)) break;
                         fence_after_sync();
                     }
@@ -332,7 +340,8 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 tmem_st_wait();
                 // E3 needs S after MMA4 of the previous chunk
                 if (it >= 1) {
-                    ok = mbar_wait_or_abort(&bar[kOfull], (it - 1) & 1, lim, abort_flag);
+                    ok = mbar_wait_or_abort(&bar[kOfull0 + (it - 1) % NOB], ((it - 1) / NOB) & 1, lim,
+                                            abort_flag);
                     if (named_bar_or(kBarA, 128, !ok)) break;
                     fence_after_sync();
                 }
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
             };
             // E2 of chunk `it`: O rows -> global, normalised
             auto do_e2 = [&](int it, float qz, int L) -> bool {
-                bool ok = mbar_wait_or_abort(&bar[kOfull], it & 1, lim, abort_flag);
+                bool ok = mbar_wait_or_abort(&bar[kOfull0 + it % NOB], (it / NOB) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 fence_after_sync();
                 float inv = 1.f;
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
                 for (int c0 = 0; c0 < DVB; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tbase + lane_off + kColO + c0, r);
+                    tmem_ld32(tbase + lane_off + kColO + (it % NOB) * DVB + c0, r);
                     tmem_ld_wait();
                     if (row < L) {
 #pragma unroll
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 fence_before_sync();
                 named_bar_sync(kBarB, 128);
-                if (t == 0) mbar_arrive(&bar[kOempty]);
+                if (t == 0) mbar_arrive(&bar[kOempty0 + it % NOB]);
                 return true;
             };
             if constexpr (STATE_ONLY) {
@@ -477,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     }
                 }
                 if (!stop && !*abort_flag) {
-                    bool ok = mbar_wait_or_abort(&bar[kOfull], (n - 1) & 1, lim, abort_flag);
+                    bool ok = mbar_wait_or_abort(&bar[kOfull0], (n - 1) & 1, lim, abort_flag);
                     if (!named_bar_or(kBarB, 128, !ok)) {
                         fence_after_sync();
                         write_exit_state();
@@ -485,14 +494,16 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 stop = true;
             }
+            // phi runs two chunks ahead, after this chunk's hand-overs and E2 of the
+            // previous chunk, so the issuer finds the next chunk's tiles ready
             if (p.phi && !stop && !do_phi(0)) stop = true;
+            if (p.phi && !stop && n > 1 && !do_phi(1)) stop = true;
             for (int it = 0; it < n && !stop; ++it) {
                 const int s = it % NS;
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 char* tQ = sm + s * Lay::kStage;
                 char* tK = tQ + Lay::kQ;
-                if (p.phi && it + 1 < n && !do_phi(it + 1)) break;
                 // MMA1 of this chunk is done with the unscaled tiles
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
@@ -541,6 +552,10 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 qz_prev = qz_cur;
                 L_prev = L;
+                if (p.phi && it + 2 < n && !do_phi(it + 2)) {
+                    stop = true;
+                    break;
+                }
             }
             if (!STATE_ONLY && !stop && !*abort_flag) {
                 if (do_e2(n - 1, qz_prev, L_prev)) write_exit_state();  // do_e2 waited for MMA4
