@@ -248,10 +248,11 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
                    device="cuda", timing=None):
     """la_chunk_fwd on HOST tensors: copy in, compute, copy the results back.
 
-    q, k, v (and S0, z0) are CPU tensors, pinned for asynchronous copies.  The
-    batch is cut into `pieces` groups of whole sequences (default min(B, 4));
+    q, k, v (and S0, z0) are CPU tensors, pinned for asynchronous copies.  With
+    `pieces` > 1 the batch is cut into that many groups of whole sequences and
     each group's copy in, la_chunk_fwd and copy out run in order on one of two
-    side streams, so the copies of one group overlap the compute of another.
+    side streams, so the copies of one group overlap the compute of another
+    (default 1: one pass on the current stream).
     Returns host (O, S_T, z_T) (z_T when normalising or when z_out is given),
     written into out / S_out / z_out when those pinned buffers are passed.
     With `timing` (a list), the device milliseconds from before the first copy
@@ -259,7 +260,7 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
     """
     B, H, T, dk = q.shape
     dv = v.shape[-1]
-    n = max(1, min(B, pieces if pieces else 4))
+    n = max(1, min(B, pieces if pieces else 1))
     bounds = [(i * B) // n for i in range(n + 1)]
     dev = torch.device(device)
     pin = dict(pin_memory=True)
@@ -278,12 +279,13 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
     S0d = torch.empty(S0.shape, dtype=torch.float32, device=dev) if S0 is not None else None
     z0d = torch.empty(z0.shape, dtype=torch.float32, device=dev) if z0 is not None else None
     main = torch.cuda.current_stream(dev)
-    sides = _side_streams(dev, 2)
+    sides = _side_streams(dev, 2) if n > 1 else [main]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(main)
     for st in sides:
-        st.wait_event(start)
+        if st is not main:
+            st.wait_event(start)
     for i in range(n):
         b0, b1 = bounds[i], bounds[i + 1]
         if b0 == b1:
@@ -303,7 +305,8 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
             if zd is not None:
                 z_out[b0:b1].copy_(zd[b0:b1], non_blocking=True)
     for st in sides:
-        main.wait_stream(st)
+        if st is not main:
+            main.wait_stream(st)
     end.record(main)
     end.synchronize()
     if timing is not None:

@@ -56,9 +56,13 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = ()) -> str:
-    """Compile and link liblinattn.so unless it is already newer than its sources."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = (),
+          out: str | None = None) -> str:
+    """Compile and link liblinattn.so unless it is already newer than its sources.
+
+    `extra_flags` / `out` build a variant (e.g. an instrumented one) elsewhere."""
+    target = out or LIBRARY
+    if not force and out is None and up_to_date():
         return LIBRARY
     nvcc = _nvcc()
     flags = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -85,10 +89,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ..
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp_lib, LIBRARY)
+        os.replace(tmp_lib, target)
     finally:
         shutil.rmtree(objdir, ignore_errors=True)
-    return LIBRARY
+    return target
 
 
 if __name__ == "__main__":

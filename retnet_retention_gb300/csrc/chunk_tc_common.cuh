@@ -128,6 +128,20 @@ __device__ __forceinline__ float colsum_total(const float* part, int d) {
     return s;
 }
 
+// Development timeline (compiled only with -DLA_TIMELINE): CTA 0 stamps the
+// global timer at pipeline events into a device array the host reads back.
+#ifdef LA_TIMELINE
+extern __device__ unsigned long long la_timeline[4096];
+#define LA_TL(slot)                                                    \
+    do {                                                               \
+        if (blockIdx.x == 0 && (slot) < 4096) la_timeline[(slot)] = tc::global_timer_ns(); \
+    } while (0)
+#else
+#define LA_TL(slot) \
+    do {            \
+    } while (0)
+#endif
+
 // Host: 3-D TMA map [BH][T][d] bf16, box {64, 128, 1}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d);
 

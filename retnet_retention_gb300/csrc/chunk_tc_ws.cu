@@ -31,6 +31,15 @@
 #include "launch.h"
 #include "trace.h"
 
+#ifdef LA_TIMELINE
+__device__ unsigned long long la_timeline[4096];
+extern "C" __attribute__((visibility("default"))) int la_timeline_read(unsigned long long* host,
+                                                                          int n) {
+    if (n > 4096) n = 4096;
+    return cudaMemcpyFromSymbol(host, la_timeline, (size_t)n * 8) == cudaSuccess ? n : -1;
+}
+#endif
+
 namespace la {
 
 using namespace tck;
@@ -54,15 +63,15 @@ struct LayoutWS {
     static constexpr uint32_t kV = (DVB / 64) * kBlk;
     static constexpr uint32_t kStage = kQ + kK + kV;
     static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // bf16 S, MN-major
-    static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + 24 * 8 + 16 + 1024;
+    static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + 32 * 8 + 16 + 1024;
     // ring depth: as many stages (up to 4) as shared memory holds
     static constexpr int NS = (4 * kStage + kSB + kSmall <= kSmemLimit) ? 4
                             : (3 * kStage + kSB + kSmall <= kSmemLimit) ? 3 : 2;
     static constexpr uint32_t oSB = NS * kStage;
     static constexpr uint32_t oZ = oSB + kSB;           // float z[DK]
     static constexpr uint32_t oZP = oZ + DK * 4;        // float colsum partials [256/DK][DK]
-    static constexpr uint32_t oBar = oZP + 256 * 4;     // 24 mbarrier slots
-    static constexpr uint32_t oFlags = oBar + 24 * 8;   // int abort, uint32 tmem slot
+    static constexpr uint32_t oBar = oZP + 256 * 4;     // 32 mbarrier slots
+    static constexpr uint32_t oFlags = oBar + 32 * 8;   // int abort, uint32 tmem slot
     static constexpr uint32_t kBytes = oFlags + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
     // O accumulators: two for DVB = 64 (E2 of a chunk overlaps the next chunk's MMAs),
@@ -79,7 +88,7 @@ struct LayoutWS {
 // o_full / o_empty cannot run ahead.
 enum Bars {
     kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
-    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kNumBars
+    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kNumBars
 };
 
 // STATE_ONLY: the walk of a segment's own state contribution (mode
@@ -114,6 +123,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     const int ce = min(n_chunks, cb + p.seg_chunks);
     const int n = ce - cb;  // chunks of this unit
     const uint64_t lim = p.wait_ns;
+    if (tid == 0) LA_TL(4000);
 
     constexpr int NS = Lay::NS;
     constexpr int NOB = Lay::NOB;
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     fence_after_sync();
     const uint32_t tbase = *slot;
     const uint32_t sbase = smem_addr(sm);
+    if (tid == 0) LA_TL(4001);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int row = (warp & 3) * 32 + lane;  // TMEM lane of this thread (epilogue warps)
 
@@ -171,6 +182,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
 
     // per-role bookkeeping that the drain at the end needs
     int fills[4] = {0, 0, 0, 0};  // producer: TMA fills issued per stage
+    if (tid == 0) LA_TL(4002);
     bool mma_issued = false;   // issuer: any MMA issued
 
     if (!forced && n > 0) {
@@ -194,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     tma_load_3d(st + Lay::kQ + Lay::kK + b * kBlk, &p.tmV, v0 + b * 64, y, bh,
                                 &bar[kFull0 + s]);
                 ++fills[s];
+                LA_TL(it * 16 + 0);
             }
         } else if (warp == 1 && lane == 0) {
             // ---------------- MMA issuer
@@ -215,6 +228,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 mma_commit(&bar[kSfull0 + (it & 1)]);
                 mma_issued = true;
+                LA_TL(it * 16 + 1);
                 return true;
             };
             if constexpr (STATE_ONLY) {
@@ -239,6 +253,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 const int s = it % NS;
                 if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
                 if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag)) break;
+                LA_TL(it * 16 + 2);
                 const int ob = it % NOB;  // O buffer of this chunk
                 if (it >= NOB &&
                     !mbar_wait_or_abort(&bar[kOempty0 + ob], ((it - NOB) / NOB) & 1, lim, abort_flag))
@@ -246,25 +261,30 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 fence_after_sync();
                 const uint32_t ocol = tbase + kColO + ob * DVB;
                 const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ, va = ka + Lay::kK;
-                // MMA2: O = P V (A = P from TMEM, K = 128 tokens)
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8,
-                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_pv, kk > 0);
-                // MMA3: O += Q^ S_bf16 (K = DK)
+                // MMA3 and MMA4 first: the next chunk's E3 waits only for them (kSdone),
+                // while MMA2 runs
+                // MMA3: O = Q^ S_bf16 (K = DK)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
                     mma_ss(ocol, smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id_pv, 1u);
+                           smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id_pv,
+                           kk > 0);
                 }
                 // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
                     mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
                            smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
+                mma_commit(&bar[kSdone]);
+                // MMA2: O += P V (A = P from TMEM, K = 128 tokens)
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8,
+                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_pv, 1u);
                 mma_commit(&bar[kOfull0 + ob]);
                 mma_commit(&bar[kEmpty0 + s]);
+                LA_TL(it * 16 + 3);
             }
         } else if (warp >= kWgA && warp < kWgB) {
             // ---------------- epilogue A: E1 (P, row sums) and E3 (S copies)
@@ -299,6 +319,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (named_bar_or(kBarA, 128, !ok)) break;
                 fence_after_sync();
+                if (t == 0) LA_TL(it * 16 + 4);
                 const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
                 const int i = row;
                 float rsum = 0.f;
@@ -338,35 +359,41 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 if (NORM) tmem_st1(tbase + lane_off + Lay::kColR + (it & 3), __float_as_uint(rsum));
                 tmem_st_wait();
-                // E3 needs S after MMA4 of the previous chunk
+                if (t == 0) LA_TL(it * 16 + 5);
+                // E3 needs S after MMA3/MMA4 of the previous chunk (kSdone)
                 if (it >= 1) {
-                    ok = mbar_wait_or_abort(&bar[kOfull0 + (it - 1) % NOB], ((it - 1) / NOB) & 1, lim,
-                                            abort_flag);
+                    ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
                     if (named_bar_or(kBarA, 128, !ok)) break;
                     fence_after_sync();
+                    if (t == 0) LA_TL(it * 16 + 6);
                 }
                 const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
-                for (int c0 = 0; c0 < DVB; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
+                for (int c0 = 0; c0 < DVB; c0 += 64) {  // two TMEM loads in flight per wait
+                    uint32_t r[2][32];
+                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, r[0]);
+                    tmem_ld32(tbase + lane_off + Lay::kColS + c0 + 32, r[1]);
                     tmem_ld_wait();
-                    if (row < DK) {
 #pragma unroll
-                        for (int e8 = 0; e8 < 32; e8 += 8) {
-                            const int v = c0 + e8;
-                            uint4 wv;
-                            wv.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
-                            wv.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
-                            wv.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
-                            wv.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
-                            *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
-                                                      sw128_offset(row, v & 63)) = wv;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (row < DK) {
+#pragma unroll
+                            for (int e8 = 0; e8 < 32; e8 += 8) {
+                                const int v = c0 + hh * 32 + e8;
+                                uint4 wv;
+                                wv.x = pack_bf16x2(__uint_as_float(r[hh][e8 + 0]), __uint_as_float(r[hh][e8 + 1]));
+                                wv.y = pack_bf16x2(__uint_as_float(r[hh][e8 + 2]), __uint_as_float(r[hh][e8 + 3]));
+                                wv.z = pack_bf16x2(__uint_as_float(r[hh][e8 + 4]), __uint_as_float(r[hh][e8 + 5]));
+                                wv.w = pack_bf16x2(__uint_as_float(r[hh][e8 + 6]), __uint_as_float(r[hh][e8 + 7]));
+                                *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                          sw128_offset(row, v & 63)) = wv;
+                            }
                         }
-                    }
-                    if (!unit_gamma) {
+                        if (!unit_gamma) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * gL);
-                        tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
+                            for (int e = 0; e < 32; ++e)
+                                r[hh][e] = __float_as_uint(__uint_as_float(r[hh][e]) * gL);
+                            tmem_st32(tbase + lane_off + Lay::kColS + c0 + hh * 32, r[hh]);
+                        }
                     }
                 }
                 if (!unit_gamma) tmem_st_wait();
@@ -374,6 +401,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 fence_before_sync();
                 named_bar_sync(kBarA, 128);
                 if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
+                if (t == 0) LA_TL(it * 16 + 7);
             }
         } else if (warp >= kWgB) {
             // ---------------- epilogue B: phi, scalings, normaliser, E2
@@ -388,12 +416,14 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 char* st = sm + s * Lay::kStage;
+                if (t == 0) LA_TL(it * 16 + 12);
                 row_pass(st, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
                 row_pass(st + Lay::kQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
                 fence_proxy_async_smem();
                 named_bar_sync(kBarB, 128);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
                 return true;
+                if (t == 0) LA_TL(it * 16 + 13);
             };
             // exit state: S (after the last MMA4, which the caller has waited for) and z
             auto write_exit_state = [&]() {
@@ -420,6 +450,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 bool ok = mbar_wait_or_abort(&bar[kOfull0 + it % NOB], (it / NOB) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 fence_after_sync();
+                if (t == 0) LA_TL(it * 16 + 10);
                 float inv = 1.f;
                 if (NORM) {
                     const float rs = __uint_as_float(tmem_ld1(tbase + lane_off + Lay::kColR + (it & 3)));
@@ -447,6 +478,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 fence_before_sync();
                 named_bar_sync(kBarB, 128);
                 if (t == 0) mbar_arrive(&bar[kOempty0 + it % NOB]);
+                if (t == 0) LA_TL(it * 16 + 11);
                 return true;
             };
             if constexpr (STATE_ONLY) {
@@ -507,6 +539,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 // MMA1 of this chunk is done with the unscaled tiles
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
+                if (t == 0) LA_TL(it * 16 + 8);
                 if (!unit_gamma) {
                     row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); }, t, 128);
                     row_pass(tK, DK / 64, false,
@@ -546,6 +579,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     mbar_arrive(&bar[kPready0 + (it & 1)]);
                     mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
                 }
+                if (t == 0) LA_TL(it * 16 + 9);
                 if (it >= 1 && !do_e2(it - 1, qz_prev, L_prev)) {
                     stop = true;
                     break;
@@ -582,6 +616,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         fence_after_sync();
     }
     if (warp == 1) tmem_dealloc(tbase, 512);
+    if (tid == 0) LA_TL(4003);
 }
 
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
