@@ -59,7 +59,8 @@ __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __e
 // for x < 0 (the two agree at 0).  Each half is selected by its sign bit.
 __device__ __forceinline__ __nv_bfloat162 phi_bf16x2(__nv_bfloat162 x) {
     const __nv_bfloat162 xp1 = __hadd2(x, __float2bfloat162_rn(1.f));
-    const __nv_bfloat162 e = h2exp(x);
+    const float2 xf = __bfloat1622float2(x);
+    const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(xf.x), __expf(xf.y));
     const uint32_t xb = *reinterpret_cast<const uint32_t*>(&x);
     const uint32_t neg = ((xb & 0x80008000u) >> 15) * 0xFFFFu;  // all-ones halves where x < 0
     const uint32_t r = (*reinterpret_cast<const uint32_t*>(&e) & neg) |
@@ -127,20 +128,6 @@ __device__ __forceinline__ float colsum_total(const float* part, int d) {
     for (int g = 0; g < 128 / (DK / 2); ++g) s += part[g * DK + d];
     return s;
 }
-
-// Development timeline (compiled only with -DLA_TIMELINE): CTA 0 stamps the
-// global timer at pipeline events into a device array the host reads back.
-#ifdef LA_TIMELINE
-extern __device__ unsigned long long la_timeline[4096];
-#define LA_TL(slot)                                                    \
-    do {                                                               \
-        if (blockIdx.x == 0 && (slot) < 4096) la_timeline[(slot)] = tc::global_timer_ns(); \
-    } while (0)
-#else
-#define LA_TL(slot) \
-    do {            \
-    } while (0)
-#endif
 
 // Host: 3-D TMA map [BH][T][d] bf16, box {64, 128, 1}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d);

@@ -31,13 +31,23 @@
 #include "launch.h"
 #include "trace.h"
 
+// Development timeline (compiled only with -DLA_TIMELINE): CTA 0 stamps the
+// global timer at pipeline events into a device array the host reads back.
 #ifdef LA_TIMELINE
 __device__ unsigned long long la_timeline[4096];
+#define LA_TL(slot)                                                                      \
+    do {                                                                                 \
+        if (blockIdx.x == 0) la_timeline[(slot) & 4095] = la::tc::global_timer_ns() | 1ull; \
+    } while (0)
 extern "C" __attribute__((visibility("default"))) int la_timeline_read(unsigned long long* host,
                                                                           int n) {
     if (n > 4096) n = 4096;
     return cudaMemcpyFromSymbol(host, la_timeline, (size_t)n * 8) == cudaSuccess ? n : -1;
 }
+#else
+#define LA_TL(slot) \
+    do {            \
+    } while (0)
 #endif
 
 namespace la {
@@ -422,8 +432,8 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 fence_proxy_async_smem();
                 named_bar_sync(kBarB, 128);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
-                return true;
                 if (t == 0) LA_TL(it * 16 + 13);
+                return true;
             };
             // exit state: S (after the last MMA4, which the caller has waited for) and z
             auto write_exit_state = [&]() {

@@ -49,6 +49,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete, for at most
 // `limit_ns` nanoseconds of the global timer.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -67,9 +79,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // Wait for the phase with the given parity, for at most `limit_ns`, giving up
 // early when another role has raised *abort (it then returns false too).
 // On a timeout of its own it raises *abort.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   uint64_t limit_ns, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t* bar, uint32_t parity,
+                                                     uint64_t limit_ns, volatile int* abort) {
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -79,6 +90,11 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   uint64_t limit_ns, volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;  // fast path inline, the loop out of line
+    return mbar_wait_or_abort_slow(bar, parity, limit_ns, abort);
 }
 
 // Named barrier over `nthreads` threads (whole warps), id 1..15.
