@@ -55,17 +55,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
-// phi = elu + 1 on a bf16 pair in bf16x2 arithmetic: x + 1 for x >= 0, e^x
-// for x < 0 (the two agree at 0).  Each half is selected by its sign bit.
+// phi = elu + 1 on a bf16 pair: relu(x) + e^min(x, 0), i.e. x + 1 above zero
+// (rounded once, in bf16) and e^x at or below it (e^x in fp32, then rounded).
 __device__ __forceinline__ __nv_bfloat162 phi_bf16x2(__nv_bfloat162 x) {
-    const __nv_bfloat162 xp1 = __hadd2(x, __float2bfloat162_rn(1.f));
-    const float2 xf = __bfloat1622float2(x);
-    const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(xf.x), __expf(xf.y));
-    const uint32_t xb = *reinterpret_cast<const uint32_t*>(&x);
-    const uint32_t neg = ((xb & 0x80008000u) >> 15) * 0xFFFFu;  // all-ones halves where x < 0
-    const uint32_t r = (*reinterpret_cast<const uint32_t*>(&e) & neg) |
-                       (*reinterpret_cast<const uint32_t*>(&xp1) & ~neg);
-    return *reinterpret_cast<const __nv_bfloat162*>(&r);
+    const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+    const float2 m = __bfloat1622float2(__hmin2(x, zero));
+    return __hadd2(__hmax2(x, zero), __floats2bfloat162_rn(__expf(m.x), __expf(m.y)));
+}
+
+// phi on rows < L of a [128 x 64*nblk] K-major swizzled tile, rows >= L set
+// to zero (phi(0) = 1, so rows past the end of the sequence must be cleared),
+// by `nthr` threads (this one is `t`).
+__device__ __forceinline__ void phi_rows(char* tile, int nblk, int L, int t, int nthr) {
+    const int n16 = nblk * (kBlk / 16);
+    for (int idx = t; idx < n16; idx += nthr) {
+        const int r = (idx >> 3) & 127;
+        uint4* p = reinterpret_cast<uint4*>(tile) + idx;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < L) {
+            u = *p;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = phi_bf16x2(h[e]);
+        }
+        *p = u;
+    }
 }
 
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`

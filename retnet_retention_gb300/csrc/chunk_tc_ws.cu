@@ -9,14 +9,26 @@
 //   warp 1      MMA issuer (one thread): MMA1 of chunk c+1 is issued ahead of
 //               MMA2..4 of chunk c, into the other of two TMEM score buffers
 //   warps 2-5   epilogue A: E1 (scores -> decay mask -> bf16 P back into
-//               TMEM, row sums) and E3 (bf16 copy of S for MMA3, S *= gamma^L)
-//   warps 6-9   epilogue B: phi on the next chunk's Q/K tiles, the xi/zeta row
-//               scalings, the normaliser (q^ . z and the z update), and E2
-//               (O of the previous chunk -> global)
+//               TMEM) and E3 (bf16 copy of S for MMA3, S *= gamma^L)
+//   warps 6-9   epilogue B: the entry state, the xi/zeta row scalings, the
+//               z update, and E2 (O of the previous chunk -> global, divided
+//               by the normaliser)
+//   warps 10-13 phi = elu + 1 on the Q/K tiles as they land, up to a ring's
+//               depth ahead of the tensor work
 //
 // so that per chunk the tensor pipe waits only for E3 (and E2 frees O) after
 // MMA4 of the previous chunk.  TMEM (512 columns): two score/P buffers at 0
-// and 128, O at 256, S after O, and (DVB = 64) four row-sum columns at 384.
+// and 128, O at 256 (two buffers for DVB = 64), S after O.
+//
+// The normaliser runs on the tensor cores.  With z treated as one more value
+// column ("Linear Attention" page, the normalised form; z_c = gamma^L z_{c-1}
+// + sum_j zeta_j k^_j is S's recurrence for an all-ones value column), MMA2
+// and MMA3 are issued with N = DVB + 16: V is followed by a block of ones
+// (so O's column DVB collects sum_j P_ij) and the bf16 copy of S by a block
+// holding z_{c-1} (so it also collects xi_i q^_i . z_{c-1}).  Column DVB of
+// O is then the whole denominator but eps.  z itself stays in fp32 shared
+// memory, updated by column sums of K^.
+//
 // Taken for DVB = 64 with any flags and for DVB = 128 without the
 // normaliser; other cases use the lockstep kernel.
 //
@@ -56,40 +68,50 @@ using namespace tck;
 
 namespace {
 
-constexpr int kThreadsWS = 320;
+constexpr int kThreadsWS = 448;
 constexpr int kWgA = 2;   // first warp of epilogue A
 constexpr int kWgB = 6;   // first warp of epilogue B
+constexpr int kWgC = 10;  // first warp of the feature-map group
 constexpr int kBarA = 1;  // named barrier ids
 constexpr int kBarB = 2;
+constexpr int kBarEntry = 3;  // epilogue B has put the entry state in TMEM (A + B)
+constexpr int kBarC = 4;
 constexpr uint32_t kColScores = 0;  // + 128 * buffer
 constexpr uint32_t kColO = 256;
 
 constexpr uint32_t kSmemLimit = 232448;  // opt-in shared memory per CTA
 
-template <int DK, int DVB>
+template <int DK, int DVB, bool NORM>
 struct LayoutWS {
     static constexpr uint32_t kQ = (DK / 64) * kBlk;
     static constexpr uint32_t kK = (DK / 64) * kBlk;
     static constexpr uint32_t kV = (DVB / 64) * kBlk;
     static constexpr uint32_t kStage = kQ + kK + kV;
-    static constexpr uint32_t kSB = (DVB / 64) * (DK * 128);  // bf16 S, MN-major
+    // bf16 S, MN-major, 64-column blocks DK * 128 bytes apart; with the
+    // normaliser one more block whose first 16 columns hold z
+    static constexpr uint32_t kSB = (DVB / 64 + (NORM ? 1 : 0)) * (DK * 128);
+    static constexpr uint32_t kOnes = NORM ? kBlk : 0;  // [128 x 64] bf16 ones
     static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + 32 * 8 + 16 + 1024;
     // ring depth: as many stages (up to 4) as shared memory holds
-    static constexpr int NS = (4 * kStage + kSB + kSmall <= kSmemLimit) ? 4
-                            : (3 * kStage + kSB + kSmall <= kSmemLimit) ? 3 : 2;
+    static constexpr int NS = (4 * kStage + kSB + kOnes + kSmall <= kSmemLimit) ? 4
+                            : (3 * kStage + kSB + kOnes + kSmall <= kSmemLimit) ? 3 : 2;
     static constexpr uint32_t oSB = NS * kStage;
-    static constexpr uint32_t oZ = oSB + kSB;           // float z[DK]
+    static constexpr uint32_t oOnes = oSB + kSB;        // 1024-byte aligned
+    static constexpr uint32_t oZ = oOnes + kOnes;       // float z[DK]
     static constexpr uint32_t oZP = oZ + DK * 4;        // float colsum partials [256/DK][DK]
     static constexpr uint32_t oBar = oZP + 256 * 4;     // 32 mbarrier slots
     static constexpr uint32_t oFlags = oBar + 32 * 8;   // int abort, uint32 tmem slot
     static constexpr uint32_t kBytes = oFlags + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
     // O accumulators: two for DVB = 64 (E2 of a chunk overlaps the next chunk's MMAs),
-    // one for DVB = 128; then S; then (DVB = 64) four rotating row-sum columns.
+    // one for DVB = 128; then S.  With the normaliser an O accumulator has
+    // DVB + 16 columns (column DVB: the denominator), its slot rounded up to 32.
     static constexpr int NOB = DVB == 64 ? 2 : 1;
-    static constexpr uint32_t kColS = kColO + NOB * DVB;
-    static constexpr uint32_t kColR = kColS + DVB;
+    static constexpr int NO = NORM ? DVB + 16 : DVB;    // MMA2/MMA3 N
+    static constexpr uint32_t kOSlot = (NO + 31) / 32 * 32;
+    static constexpr uint32_t kColS = kColO + NOB * kOSlot;
     static_assert(kAlloc <= kSmemLimit, "shared memory budget");
+    static_assert(kColS + DVB <= 512, "tensor memory budget");
 };
 
 // Barriers.  Stage barriers (full, empty, qk) have one slot per ring stage;
@@ -107,8 +129,8 @@ enum Bars {
 // epilogues may run ahead.
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
 __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
-    using Lay = LayoutWS<DK, DVB>;
-    static_assert(!NORM || DVB == 64, "row-sum columns exist only for DVB = 64");
+    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
+    static_assert(!NORM || DVB == 64, "the normaliser's columns fit tensor memory only for DVB = 64");
     extern __shared__ __align__(1024) char smem_raw[];
     char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* zs = reinterpret_cast<float*>(sm + Lay::oZ);
@@ -154,6 +176,12 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         tmem_alloc(slot, 512);
         tmem_relinquish();
     }
+    if constexpr (NORM) {  // the block of ones after V (read by MMA2 through the async proxy)
+        const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < (int)(kBlk / 16); i += kThreadsWS)
+            reinterpret_cast<uint4*>(sm + Lay::oOnes)[i] = ones;
+        fence_proxy_async_smem();
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -169,26 +197,31 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         forced = true;
     }
 
-    // ---- entry state into TMEM (epilogue B owns all 128 lanes), z into smem
-    if (!forced && warp >= kWgB) {
+    // ---- entry state into TMEM and z into smem: epilogue B (all 128 lanes), at the
+    // start of its role below, while the producer already loads the first chunks;
+    // epilogue A waits for it (kBarEntry) before its first read of S.
+    auto load_entry_state = [&]() {
         const int sidx = bh * p.in_nseg + seg;
         const bool has_in = p.S_in != nullptr && !STATE_ONLY;
+        const float* srow = has_in && row < DK ? p.S_in + ((size_t)sidx * DK + row) * p.dv + v0
+                                               : nullptr;
         for (int c0 = 0; c0 < DVB; c0 += 32) {
             uint32_t r[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                float x = 0.f;
-                if (has_in && row < DK) x = p.S_in[((size_t)sidx * DK + row) * p.dv + v0 + c0 + e];
-                r[e] = __float_as_uint(x);
+            for (int e = 0; e < 32; e += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (srow) x = *reinterpret_cast<const float4*>(srow + c0 + e);
+                r[e] = __float_as_uint(x.x);
+                r[e + 1] = __float_as_uint(x.y);
+                r[e + 2] = __float_as_uint(x.z);
+                r[e + 3] = __float_as_uint(x.w);
             }
             tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
         }
         tmem_st_wait();
         if (row < DK) zs[row] = (has_in && p.z_in) ? p.z_in[(size_t)sidx * DK + row] : 0.f;
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+        fence_before_sync();
+    };
 
     // per-role bookkeeping that the drain at the end needs
     int fills[4] = {0, 0, 0, 0};  // producer: TMA fills issued per stage
@@ -221,7 +254,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         } else if (warp == 1 && lane == 0) {
             // ---------------- MMA issuer
             const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
-            const uint32_t id_pv = idesc_bf16(128, DVB, 0, 1);
+            const uint32_t id_pv = idesc_bf16(128, Lay::NO, 0, 1);  // MMA2, MMA3
             const uint32_t id_kv = idesc_bf16(128, DVB, 1, 1);
             auto issue_mma1 = [&](int it) -> bool {
                 const int s = it % NS;
@@ -269,8 +302,11 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     !mbar_wait_or_abort(&bar[kOempty0 + ob], ((it - NOB) / NOB) & 1, lim, abort_flag))
                     break;
                 fence_after_sync();
-                const uint32_t ocol = tbase + kColO + ob * DVB;
+                const uint32_t ocol = tbase + kColO + ob * Lay::kOSlot;
                 const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ, va = ka + Lay::kK;
+                // V's 64-column blocks are kBlk apart; with the normaliser the block
+                // of ones stands in for the next one (N = DVB + 16)
+                const uint32_t v_lbo = NORM ? sbase + Lay::oOnes - va : kBlk;
                 // MMA3 and MMA4 first: the next chunk's E3 waits only for them (kSdone),
                 // while MMA2 runs
                 // MMA3: O = Q^ S_bf16 (K = DK)
@@ -291,14 +327,16 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
                     mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8,
-                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_pv, 1u);
+                           smem_desc_sw128(va + kk * 2048, v_lbo, 1024), id_pv, 1u);
                 mma_commit(&bar[kOfull0 + ob]);
                 mma_commit(&bar[kEmpty0 + s]);
                 LA_TL(it * 16 + 3);
             }
         } else if (warp >= kWgA && warp < kWgB) {
-            // ---------------- epilogue A: E1 (P, row sums) and E3 (S copies)
+            // ---------------- epilogue A: E1 (P) and E3 (S copies)
             const int t = tid - kWgA * 32;
+            named_bar_sync(kBarEntry, 256);  // the entry state is in TMEM
+            fence_after_sync();
             if constexpr (STATE_ONLY) {
                 // only S = gamma^L S before each MMA4 (nothing to do when gamma == 1)
                 for (int it = 0; it < n && !unit_gamma; ++it) {
@@ -332,7 +370,6 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 if (t == 0) LA_TL(it * 16 + 4);
                 const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
                 const int i = row;
-                float rsum = 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < kC; c0 += 32) {
                     uint32_t r[32];
@@ -357,17 +394,9 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                         a[e] = x;
                     }
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const uint32_t u = pack_bf16x2(a[e], a[e + 1]);
-                        pk[e >> 1] = u;
-                        if (NORM) {
-                            const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-                            rsum += back.x + back.y;
-                        }
-                    }
+                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
                     tmem_st16(sc + (c0 >> 1), pk);
                 }
-                if (NORM) tmem_st1(tbase + lane_off + Lay::kColR + (it & 3), __float_as_uint(rsum));
                 tmem_st_wait();
                 if (t == 0) LA_TL(it * 16 + 5);
                 // E3 needs S after MMA3/MMA4 of the previous chunk (kSdone)
@@ -413,28 +442,31 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
                 if (t == 0) LA_TL(it * 16 + 7);
             }
-        } else if (warp >= kWgB) {
-            // ---------------- epilogue B: phi, scalings, normaliser, E2
-            const int t = tid - kWgB * 32;
-            float qz_prev = 0.f, qz_cur = 0.f;
-            int L_prev = 0;
-            bool stop = false;
-            // phi on the Q/K tiles of chunk `it` (rows >= L zeroed), then release MMA1
-            auto do_phi = [&](int it) -> bool {
+        } else if (warp >= kWgC) {
+            // ---------------- feature map: phi on Q and K (K only for a state walk), rows
+            // past the end zeroed, then release the stage to the issuer (kQk)
+            const int t = tid - kWgC * 32;
+            for (int it = 0; it < n && p.phi; ++it) {
                 const int s = it % NS;
                 const int L = min(kC, p.T - (cb + it) * kC);
                 bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
-                if (named_bar_or(kBarB, 128, !ok)) return false;
+                if (named_bar_or(kBarC, 128, !ok)) break;
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
-                row_pass(st, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
-                row_pass(st + Lay::kQ, DK / 64, true, [&](int r) { return r < L ? 1.f : 0.f; }, t, 128);
+                if (!STATE_ONLY) phi_rows(st, DK / 64, L, t, 128);
+                phi_rows(st + Lay::kQ, DK / 64, L, t, 128);
                 fence_proxy_async_smem();
-                named_bar_sync(kBarB, 128);
+                named_bar_sync(kBarC, 128);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
                 if (t == 0) LA_TL(it * 16 + 13);
-                return true;
-            };
+            }
+        } else if (warp >= kWgB) {
+            // ---------------- epilogue B: entry state, scalings, z, E2
+            const int t = tid - kWgB * 32;
+            load_entry_state();
+            named_bar_arrive(kBarEntry, 256);
+            int L_prev = 0;
+            bool stop = false;
             // exit state: S (after the last MMA4, which the caller has waited for) and z
             auto write_exit_state = [&]() {
                 if (!p.S_out) return;
@@ -455,23 +487,24 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 if (write && p.z_out && dvb == 0 && row < DK) p.z_out[(size_t)oidx * DK + row] = zs[row];
             };
-            // E2 of chunk `it`: O rows -> global, normalised
-            auto do_e2 = [&](int it, float qz, int L) -> bool {
+            // E2 of chunk `it`: O rows -> global, divided by the normaliser
+            auto do_e2 = [&](int it, int L) -> bool {
                 bool ok = mbar_wait_or_abort(&bar[kOfull0 + it % NOB], (it / NOB) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 fence_after_sync();
                 if (t == 0) LA_TL(it * 16 + 10);
+                const uint32_t ocol = tbase + lane_off + kColO + (it % NOB) * Lay::kOSlot;
                 float inv = 1.f;
-                if (NORM) {
-                    const float rs = __uint_as_float(tmem_ld1(tbase + lane_off + Lay::kColR + (it & 3)));
+                if (NORM) {  // column DVB: sum_j P_ij + xi_i q^_i . z_{c-1}
+                    const float den = __uint_as_float(tmem_ld1(ocol + DVB));
                     tmem_ld_wait();
-                    inv = 1.f / (rs + qz + p.eps);
+                    inv = 1.f / (den + p.eps);
                 }
                 const int c = cb + it;
                 __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
                 for (int c0 = 0; c0 < DVB; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tbase + lane_off + kColO + (it % NOB) * DVB + c0, r);
+                    tmem_ld32(ocol + c0, r);
                     tmem_ld_wait();
                     if (row < L) {
 #pragma unroll
@@ -496,18 +529,17 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     const int s = it % NS;
                     const int L = min(kC, p.T - (cb + it) * kC);
                     char* tK = sm + s * Lay::kStage + Lay::kQ;
+                    // the tile, and phi(K) from the feature-map group
                     bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
+                    if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                     if (named_bar_or(kBarB, 128, !ok)) {
                         stop = true;
                         break;
                     }
                     // K^ = zeta . phi(K), rows >= L zeroed
-                    if (p.phi || !unit_gamma)
-                        row_pass(tK, DK / 64, p.phi != 0,
-                                 [&](int r) {
-                                     return r < L ? (unit_gamma ? 1.f : gamma_pow(l2g, (float)(L - 1 - r)))
-                                                  : 0.f;
-                                 },
+                    if (!unit_gamma)
+                        row_pass(tK, DK / 64, false,
+                                 [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
                                  t, 128);
                     named_bar_sync(kBarB, 128);
                     if (p.track_z) {  // z_c = gamma^L z_{c-1} + sum_j K^[j]
@@ -536,18 +568,16 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 }
                 stop = true;
             }
-            // phi runs two chunks ahead, after this chunk's hand-overs and E2 of the
-            // previous chunk, so the issuer finds the next chunk's tiles ready
-            if (p.phi && !stop && !do_phi(0)) stop = true;
-            if (p.phi && !stop && n > 1 && !do_phi(1)) stop = true;
             for (int it = 0; it < n && !stop; ++it) {
                 const int s = it % NS;
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 char* tQ = sm + s * Lay::kStage;
                 char* tK = tQ + Lay::kQ;
-                // MMA1 of this chunk is done with the unscaled tiles
+                // MMA1 of this chunk is done with the unscaled tiles (and phi's writes
+                // to them are visible here through kQk)
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
+                if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
                 if (t == 0) LA_TL(it * 16 + 8);
                 if (!unit_gamma) {
@@ -558,21 +588,23 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     named_bar_sync(kBarB, 128);
                 }
                 if (NORM || p.track_z) {
-                    if (NORM) {  // qz_i = q^_i . z_{c-1}
-                        float acc = 0.f;
-#pragma unroll 4
-                        for (int d8 = 0; d8 < DK; d8 += 8) {
-                            const uint4 u = *reinterpret_cast<const uint4*>(tQ + (d8 >> 6) * kBlk +
-                                                                            sw128_offset(row, d8 & 63));
-                            const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 x = __bfloat1622float2(hq[e]);
-                                acc = fmaf(x.x, zs[d8 + 2 * e], acc);
-                                acc = fmaf(x.y, zs[d8 + 2 * e + 1], acc);
-                            }
+                    if (NORM) {
+                        // z_{c-1} into the block after bf16 S, once MMA3 of the previous
+                        // chunk has read the old one; MMA3 then adds xi_i q^_i . z_{c-1}
+                        // to O's column DVB
+                        if (it >= 1) {
+                            ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
+                            if (named_bar_or(kBarB, 128, !ok)) break;
                         }
-                        qz_cur = acc;
+                        if (t < DK) {
+                            const __nv_bfloat162 z2 = __float2bfloat162_rn(zs[t]);
+                            const uint32_t zw = *reinterpret_cast<const uint32_t*>(&z2);
+                            const uint4 zv = make_uint4(zw, zw, zw, zw);
+                            char* zb = sm + Lay::oSB + (DVB / 64) * (DK * 128);
+                            *reinterpret_cast<uint4*>(zb + sw128_offset(t, 0)) = zv;
+                            *reinterpret_cast<uint4*>(zb + sw128_offset(t, 8)) = zv;
+                        }
+                        fence_proxy_async_smem();
                     }
                     // z_c = gamma^L z_{c-1} + sum_j K^[j] (rows >= L of K^ are zero)
                     float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
@@ -590,19 +622,14 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
                 }
                 if (t == 0) LA_TL(it * 16 + 9);
-                if (it >= 1 && !do_e2(it - 1, qz_prev, L_prev)) {
+                if (it >= 1 && !do_e2(it - 1, L_prev)) {
                     stop = true;
                     break;
                 }
-                qz_prev = qz_cur;
                 L_prev = L;
-                if (p.phi && it + 2 < n && !do_phi(it + 2)) {
-                    stop = true;
-                    break;
-                }
             }
             if (!STATE_ONLY && !stop && !*abort_flag) {
-                if (do_e2(n - 1, qz_prev, L_prev)) write_exit_state();  // do_e2 waited for MMA4
+                if (do_e2(n - 1, L_prev)) write_exit_state();  // do_e2 waited for MMA4
             }
         }
     }
@@ -631,7 +658,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
 
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s) {
-    using Lay = LayoutWS<DK, DVB>;
+    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
     auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);

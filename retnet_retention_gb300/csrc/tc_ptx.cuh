@@ -102,6 +102,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on a named barrier without waiting (the waiting side uses bar.sync
+// with the same thread count).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads.
 __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
     uint32_t out;
