@@ -521,14 +521,18 @@ cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t s) {
 
 bool tc_ws_supported(int mode, int dk, int dvb, bool normalize);
 cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
-                               cudaStream_t s);
+                               cudaStream_t s, bool pdl);
 
 namespace {
 
-cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, cudaStream_t s) {
+// pdl: the pipelined kernel may be launched as a programmatic dependent of the
+// previous kernel (it waits for it before reading entry states); the lockstep
+// kernel is always launched in plain stream order.
+cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, cudaStream_t s,
+                               bool pdl = false) {
     if (grid <= 0) return cudaSuccess;
     if (tc_ws_supported(prm.mode, dk, dvb, prm.normalize != 0))
-        return launch_chunk_tc_ws(dk, dvb, prm.normalize != 0, prm, grid, s);
+        return launch_chunk_tc_ws(dk, dvb, prm.normalize != 0, prm, grid, s, pdl);
     if (dk == 64 && dvb == 64) return launch_tc<64, 64>(prm, grid, s);
     if (dk == 64 && dvb == 128) return launch_tc<64, 128>(prm, grid, s);
     if (dk == 128 && dvb == 64) return launch_tc<128, 64>(prm, grid, s);
@@ -557,12 +561,19 @@ int choose_segments(int units, int n_chunks) {
 // Entry state of every segment from the segments' own contributions:
 //   entry_0 = S0 (or 0),  entry_{q+1} = gamma^len entry_q + agg_q
 // (len = the common segment length).  One thread per state element; z rides
-// along on the threads of column 0.
+// along on the threads of column 0.  The contributions are loaded in batches
+// of kScanBatch before the recurrence runs over them, so a thread waits for
+// memory once per batch rather than once per segment.  Launched as a
+// programmatic dependent of the state walk: it lets the output walk be
+// scheduled at once and waits for the state walk's results.
+constexpr int kScanBatch = 8;
 __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
                                     const float* __restrict__ agg, const float* __restrict__ zagg,
                                     float* __restrict__ entry, float* __restrict__ zentry,
                                     size_t total, int H, int P, int seg_len, int dk, int dv,
                                     const __grid_constant__ KernelGammas g) {
+    tc::griddep_launch_dependents();
+    tc::griddep_wait();
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const size_t per = (size_t)dk * dv;
@@ -573,12 +584,22 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
     const bool do_z = (e % dv) == 0;
     const size_t d = e / dv;
     float zz = (do_z && z0) ? z0[bh * dk + d] : 0.f;
-    for (int q = 0; q < P; ++q) {
-        entry[(bh * P + q) * per + e] = x;
-        if (do_z) zentry[(bh * P + q) * dk + d] = zz;
-        if (q + 1 < P) {
-            x = fmaf(gseg, x, agg[(bh * P + q) * per + e]);
-            if (do_z) zz = fmaf(gseg, zz, zagg[(bh * P + q) * dk + d]);
+    for (int q0 = 0; q0 < P; q0 += kScanBatch) {
+        float a[kScanBatch], za[kScanBatch];
+#pragma unroll
+        for (int b = 0; b < kScanBatch; ++b) {  // the last segment's contribution is not needed
+            const int q = q0 + b;
+            a[b] = q + 1 < P ? agg[(bh * P + q) * per + e] : 0.f;
+            za[b] = (do_z && q + 1 < P) ? zagg[(bh * P + q) * dk + d] : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kScanBatch; ++b) {
+            const int q = q0 + b;
+            if (q >= P) break;
+            entry[(bh * P + q) * per + e] = x;
+            if (do_z) zentry[(bh * P + q) * dk + d] = zz;
+            x = fmaf(gseg, x, a[b]);
+            if (do_z) zz = fmaf(gseg, zz, za[b]);
         }
     }
 }
@@ -708,11 +729,20 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     if (e != cudaSuccess) return e;
     const size_t total = nbh * (size_t)a.dk * a.dv;
     {
-    TraceScope trace("segment_scan_kernel", s);
-    segment_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-        a.S0, a.z0, agg, zagg, entry, zentry, total, a.H, Pu, seg_chunks * kC, a.dk, a.dv, g);
+        TraceScope trace("segment_scan_kernel", s);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((total + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, a.S0, a.z0, (const float*)agg,
+                               (const float*)zagg, entry, zentry, total, a.H, Pu, seg_chunks * kC,
+                               a.dk, a.dv, g);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     TcParams pc = prm;
     pc.mode = kFull;
@@ -726,7 +756,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     pc.out_nseg = 1;
     pc.out_last_only = 1;
     *launches = 3;
-    return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s);
+    return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
 }
 
 }  // namespace la

@@ -8,12 +8,13 @@
 //   warp 0      TMA producer: Q, K, V of chunk c into a ring of 2-4 stages
 //   warp 1      MMA issuer (one thread): MMA1 of chunk c+1 is issued ahead of
 //               MMA2..4 of chunk c, into the other of two TMEM score buffers
-//   warps 2-5   epilogue A: E1 (scores -> decay mask -> bf16 P back into
-//               TMEM) and E3 (bf16 copy of S for MMA3, S *= gamma^L)
-//   warps 6-9   epilogue B: the entry state, the xi/zeta row scalings, the
+//   warps 2-9   epilogue A: E1 (scores -> decay mask -> bf16 P back into
+//               TMEM) and E3 (bf16 copy of S for MMA3, S *= gamma^L); two
+//               warps per TMEM lane quarter, each on half of the columns
+//   warps 10-13 epilogue B: the entry state, the xi/zeta row scalings, the
 //               z update, and E2 (O of the previous chunk -> global, divided
 //               by the normaliser)
-//   warps 10-13 phi = elu + 1 on the Q/K tiles as they land, up to a ring's
+//   warps 14-17 phi = elu + 1 on the Q/K tiles as they land, up to a ring's
 //               depth ahead of the tensor work
 //
 // so that per chunk the tensor pipe waits only for E3 (and E2 frees O) after
@@ -36,6 +37,7 @@
 // every other role's waits then give up too, all roles meet at the end, the
 // producer and issuer wait (bounded) for their own copies and MMAs, the CTA
 // records LA_ERR_TIMEOUT and frees its TMEM.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -47,18 +49,37 @@
 // global timer at pipeline events into a device array the host reads back.
 #ifdef LA_TIMELINE
 __device__ unsigned long long la_timeline[4096];
-#define LA_TL(slot)                                                                      \
-    do {                                                                                 \
-        if (blockIdx.x == 0) la_timeline[(slot) & 4095] = la::tc::global_timer_ns() | 1ull; \
+#define LA_TL(slot)                                                                        \
+    do {                                                                                   \
+        if (blockIdx.x == 0)                                                               \
+            la_timeline[((slot) + (STATE_ONLY ? 2048 : 0)) & 4095] = la::tc::global_timer_ns() | 1ull; \
     } while (0)
 extern "C" __attribute__((visibility("default"))) int la_timeline_read(unsigned long long* host,
                                                                           int n) {
     if (n > 4096) n = 4096;
     return cudaMemcpyFromSymbol(host, la_timeline, (size_t)n * 8) == cudaSuccess ? n : -1;
 }
+__device__ unsigned long long la_cta_times[4 * 1024];  // per CTA: start, end (x2 kernels)
+extern "C" __attribute__((visibility("default"))) int la_cta_times_read(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, la_cta_times, sizeof(la_cta_times)) == cudaSuccess ? 0 : -1;
+}
+extern "C" __attribute__((visibility("default"))) int la_timeline_clear() {
+    static const unsigned long long z2[4 * 1024] = {};
+    cudaMemcpyToSymbol(la_cta_times, z2, sizeof(z2));
+    static const unsigned long long zeros[4096] = {};
+    return cudaMemcpyToSymbol(la_timeline, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#define LA_CTA_T(which)                                                                  \
+    do {                                                                                 \
+        if (threadIdx.x == 0 && blockIdx.x < 1024)                                       \
+            la_cta_times[(STATE_ONLY ? 2048 : 0) + 2 * blockIdx.x + (which)] = la::tc::global_timer_ns(); \
+    } while (0)
 #else
 #define LA_TL(slot) \
     do {            \
+    } while (0)
+#define LA_CTA_T(which) \
+    do {                \
     } while (0)
 #endif
 
@@ -68,14 +89,16 @@ using namespace tck;
 
 namespace {
 
-constexpr int kThreadsWS = 448;
-constexpr int kWgA = 2;   // first warp of epilogue A
-constexpr int kWgB = 6;   // first warp of epilogue B
-constexpr int kWgC = 10;  // first warp of the feature-map group
+constexpr int kThreadsWS = 576;
+constexpr int kWgA = 2;   // first warp of epilogue A (8 warps: two per TMEM lane quarter)
+constexpr int kWgB = 10;  // first warp of epilogue B
+constexpr int kWgC = 14;  // first warp of the feature-map group
 constexpr int kBarA = 1;  // named barrier ids
 constexpr int kBarB = 2;
 constexpr int kBarEntry = 3;  // epilogue B has put the entry state in TMEM (A + B)
 constexpr int kBarC = 4;
+constexpr int kBarP = 5;      // E1: the first column half has read its scores (A)
+constexpr int kThreadsA = 256;
 constexpr uint32_t kColScores = 0;  // + 128 * buffer
 constexpr uint32_t kColO = 256;
 
@@ -156,6 +179,8 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     const int n = ce - cb;  // chunks of this unit
     const uint64_t lim = p.wait_ns;
     if (tid == 0) LA_TL(4000);
+    LA_CTA_T(0);
+    griddep_launch_dependents();  // the next kernel's CTAs may be scheduled (it waits itself)
 
     constexpr int NS = Lay::NS;
     constexpr int NOB = Lay::NOB;
@@ -256,18 +281,22 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
             const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
             const uint32_t id_pv = idesc_bf16(128, Lay::NO, 0, 1);  // MMA2, MMA3
             const uint32_t id_kv = idesc_bf16(128, DVB, 1, 1);
+            // descriptors of stage 0 and of bf16 S; the others are offsets from them
+            const uint64_t dQk0 = smem_desc_sw128(sbase, 16, 1024);          // Q, K: K-major
+            const uint64_t dKmn0 = smem_desc_sw128(sbase + Lay::kQ, kBlk, 1024);  // K: MN-major
+            const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, DK * 128, 1024);
             auto issue_mma1 = [&](int it) -> bool {
                 const int s = it % NS;
                 const uint32_t par = (it / NS) & 1;
                 if (!mbar_wait_or_abort(&bar[kFull0 + s], par, lim, abort_flag)) return false;
                 if (p.phi && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag)) return false;
                 fence_after_sync();
-                const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ;
+                const uint64_t dq = desc_adv(dQk0, s * Lay::kStage), dk = desc_adv(dq, Lay::kQ);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
-                    mma_ss(tbase + kColScores + (it & 1) * 128, smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+                    mma_ss(tbase + kColScores + (it & 1) * 128, desc_adv(dq, off), desc_adv(dk, off),
+                           id_qk, kk > 0);
                 }
                 mma_commit(&bar[kSfull0 + (it & 1)]);
                 mma_issued = true;
@@ -279,14 +308,15 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     const int s = it % NS;
                     if (!mbar_wait_or_abort(&bar[kReadyS0 + s], (it / NS) & 1, lim, abort_flag)) break;
                     fence_after_sync();
-                    const uint32_t ka = sbase + s * Lay::kStage + Lay::kQ, va = ka + Lay::kK;
+                    const uint64_t dk = desc_adv(dKmn0, s * Lay::kStage), dv = desc_adv(dk, Lay::kK);
 #pragma unroll
                     for (int kk = 0; kk < kC / 16; ++kk)
-                        mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
-                               smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
+                        mma_ss(tbase + Lay::kColS, desc_adv(dk, kk * 2048), desc_adv(dv, kk * 2048),
+                               id_kv, 1u);
                     mma_commit(&bar[kOfull0]);
                     mma_commit(&bar[kEmpty0 + s]);
                     mma_issued = true;
+                    LA_TL(it * 16 + 3);
                 }
                 (void)issue_mma1;
                 (void)id_pv;
@@ -303,51 +333,54 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     break;
                 fence_after_sync();
                 const uint32_t ocol = tbase + kColO + ob * Lay::kOSlot;
-                const uint32_t qa = sbase + s * Lay::kStage, ka = qa + Lay::kQ, va = ka + Lay::kK;
-                // V's 64-column blocks are kBlk apart; with the normaliser the block
-                // of ones stands in for the next one (N = DVB + 16)
-                const uint32_t v_lbo = NORM ? sbase + Lay::oOnes - va : kBlk;
+                const uint64_t dq = desc_adv(dQk0, s * Lay::kStage);
+                const uint64_t dk = desc_adv(dKmn0, s * Lay::kStage), dv = desc_adv(dk, Lay::kK);
+                // V for MMA2: its 64-column blocks are kBlk apart; with the normaliser the
+                // block of ones stands in for the next one (N = DVB + 16)
+                const uint32_t va = sbase + s * Lay::kStage + Lay::kQ + Lay::kK;
+                const uint64_t dv2 = NORM ? smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024) : dv;
                 // MMA3 and MMA4 first: the next chunk's E3 waits only for them (kSdone),
                 // while MMA2 runs
                 // MMA3: O = Q^ S_bf16 (K = DK)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
-                    mma_ss(ocol, smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(sbase + Lay::oSB + kk * 2048, DK * 128, 1024), id_pv,
-                           kk > 0);
+                    mma_ss(ocol, desc_adv(dq, off), desc_adv(dSB, kk * 2048), id_pv, kk > 0);
                 }
                 // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ss(tbase + Lay::kColS, smem_desc_sw128(ka + kk * 2048, kBlk, 1024),
-                           smem_desc_sw128(va + kk * 2048, kBlk, 1024), id_kv, 1u);
+                    mma_ss(tbase + Lay::kColS, desc_adv(dk, kk * 2048), desc_adv(dv, kk * 2048), id_kv,
+                           1u);
                 mma_commit(&bar[kSdone]);
                 // MMA2: O += P V (A = P from TMEM, K = 128 tokens)
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8,
-                           smem_desc_sw128(va + kk * 2048, v_lbo, 1024), id_pv, 1u);
+                    mma_ts(ocol, tbase + kColScores + (it & 1) * 128 + kk * 8, desc_adv(dv2, kk * 2048),
+                           id_pv, 1u);
                 mma_commit(&bar[kOfull0 + ob]);
                 mma_commit(&bar[kEmpty0 + s]);
                 LA_TL(it * 16 + 3);
             }
         } else if (warp >= kWgA && warp < kWgB) {
-            // ---------------- epilogue A: E1 (P) and E3 (S copies)
+            // ---------------- epilogue A: E1 (P) and E3 (S copies).  Warps kWgA..+3 take
+            // the first half of the columns (half 0), warps kWgA+4..+7 the second.
             const int t = tid - kWgA * 32;
-            named_bar_sync(kBarEntry, 256);  // the entry state is in TMEM
+            const int half = t >> 7;
+            named_bar_sync(kBarEntry, kThreadsA + 128);  // the entry state is in TMEM
             fence_after_sync();
+            constexpr int kSHalf = DVB / 2;  // S columns per half
             if constexpr (STATE_ONLY) {
                 // only S = gamma^L S before each MMA4 (nothing to do when gamma == 1)
                 for (int it = 0; it < n && !unit_gamma; ++it) {
                     const int L = min(kC, p.T - (cb + it) * kC);
                     if (it >= 1) {
                         bool ok = mbar_wait_or_abort(&bar[kOfull0], (it - 1) & 1, lim, abort_flag);
-                        if (named_bar_or(kBarA, 128, !ok)) break;
+                        if (named_bar_or(kBarA, kThreadsA, !ok)) break;
                         fence_after_sync();
                     }
                     const float gL = gamma_pow(l2g, (float)L);
-                    for (int c0 = 0; c0 < DVB; c0 += 32) {
+                    for (int c0 = half * kSHalf; c0 < (half + 1) * kSHalf; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
                         tmem_ld_wait();
@@ -357,7 +390,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     }
                     tmem_st_wait();
                     fence_before_sync();
-                    named_bar_sync(kBarA, 128);
+                    named_bar_sync(kBarA, kThreadsA);
                     if (t == 0) mbar_arrive(&bar[kReadyS0 + it % NS]);
                 }
             }
@@ -365,16 +398,24 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
-                if (named_bar_or(kBarA, 128, !ok)) break;
+                if (named_bar_or(kBarA, kThreadsA, !ok)) break;
                 fence_after_sync();
                 if (t == 0) LA_TL(it * 16 + 4);
                 const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
                 const int i = row;
+                // this half's two 32-column pieces of scores, one at a time.  P (bf16
+                // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
+                // piece, so half 1 stores only after half 0 has read that piece (kBarP).
 #pragma unroll
-                for (int c0 = 0; c0 < kC; c0 += 32) {
+                for (int q = 0; q < 2; ++q) {
+                    const int c0 = 64 * half + 32 * q;
                     uint32_t r[32];
                     tmem_ld32(sc + c0, r);
                     tmem_ld_wait();
+                    if (half == 0 && q == 1) {
+                        fence_before_sync();
+                        named_bar_arrive(kBarP, kThreadsA);
+                    }
                     uint32_t pk[16];
                     // gamma^(i-j) by a running product from the piece's top column down
                     const int jt = min(i, c0 + 31);
@@ -395,6 +436,10 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                     }
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                    if (half == 1 && q == 0) {
+                        named_bar_sync(kBarP, kThreadsA);
+                        fence_after_sync();
+                    }
                     tmem_st16(sc + (c0 >> 1), pk);
                 }
                 tmem_st_wait();
@@ -402,43 +447,39 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 // E3 needs S after MMA3/MMA4 of the previous chunk (kSdone)
                 if (it >= 1) {
                     ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
-                    if (named_bar_or(kBarA, 128, !ok)) break;
+                    if (named_bar_or(kBarA, kThreadsA, !ok)) break;
                     fence_after_sync();
                     if (t == 0) LA_TL(it * 16 + 6);
                 }
                 const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
-                for (int c0 = 0; c0 < DVB; c0 += 64) {  // two TMEM loads in flight per wait
-                    uint32_t r[2][32];
-                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, r[0]);
-                    tmem_ld32(tbase + lane_off + Lay::kColS + c0 + 32, r[1]);
+#pragma unroll
+                for (int c0 = half * kSHalf; c0 < (half + 1) * kSHalf; c0 += 32) {
+                    uint32_t rs[32];
+                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, rs);
                     tmem_ld_wait();
+                    if (row < DK) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (row < DK) {
-#pragma unroll
-                            for (int e8 = 0; e8 < 32; e8 += 8) {
-                                const int v = c0 + hh * 32 + e8;
-                                uint4 wv;
-                                wv.x = pack_bf16x2(__uint_as_float(r[hh][e8 + 0]), __uint_as_float(r[hh][e8 + 1]));
-                                wv.y = pack_bf16x2(__uint_as_float(r[hh][e8 + 2]), __uint_as_float(r[hh][e8 + 3]));
-                                wv.z = pack_bf16x2(__uint_as_float(r[hh][e8 + 4]), __uint_as_float(r[hh][e8 + 5]));
-                                wv.w = pack_bf16x2(__uint_as_float(r[hh][e8 + 6]), __uint_as_float(r[hh][e8 + 7]));
-                                *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
-                                                          sw128_offset(row, v & 63)) = wv;
-                            }
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            const int v = c0 + e8;
+                            uint4 wv;
+                            wv.x = pack_bf16x2(__uint_as_float(rs[e8 + 0]), __uint_as_float(rs[e8 + 1]));
+                            wv.y = pack_bf16x2(__uint_as_float(rs[e8 + 2]), __uint_as_float(rs[e8 + 3]));
+                            wv.z = pack_bf16x2(__uint_as_float(rs[e8 + 4]), __uint_as_float(rs[e8 + 5]));
+                            wv.w = pack_bf16x2(__uint_as_float(rs[e8 + 6]), __uint_as_float(rs[e8 + 7]));
+                            *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                      sw128_offset(row, v & 63)) = wv;
                         }
-                        if (!unit_gamma) {
+                    }
+                    if (!unit_gamma) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                r[hh][e] = __float_as_uint(__uint_as_float(r[hh][e]) * gL);
-                            tmem_st32(tbase + lane_off + Lay::kColS + c0 + hh * 32, r[hh]);
-                        }
+                        for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                        tmem_st32(tbase + lane_off + Lay::kColS + c0, rs);
                     }
                 }
                 if (!unit_gamma) tmem_st_wait();
                 fence_proxy_async_smem();
                 fence_before_sync();
-                named_bar_sync(kBarA, 128);
+                named_bar_sync(kBarA, kThreadsA);
                 if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
                 if (t == 0) LA_TL(it * 16 + 7);
             }
@@ -453,8 +494,13 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 if (named_bar_or(kBarC, 128, !ok)) break;
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
-                if (!STATE_ONLY) phi_rows(st, DK / 64, L, t, 128);
-                phi_rows(st + Lay::kQ, DK / 64, L, t, 128);
+                if constexpr (STATE_ONLY) {  // alone on the SM's conversion pipe: all loads first
+                    char* const tiles[1] = {st + Lay::kQ};
+                    phi_rows_128<1, DK / 64>(tiles, L, t);
+                } else {  // one piece at a time, leaving the pipe to the epilogues' packs
+                    phi_rows(st, DK / 64, L, t, 128);
+                    phi_rows(st + Lay::kQ, DK / 64, L, t, 128);
+                }
                 fence_proxy_async_smem();
                 named_bar_sync(kBarC, 128);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
@@ -463,8 +509,9 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
         } else if (warp >= kWgB) {
             // ---------------- epilogue B: entry state, scalings, z, E2
             const int t = tid - kWgB * 32;
+            griddep_wait();  // entry states come from the previous kernel in the stream
             load_entry_state();
-            named_bar_arrive(kBarEntry, 256);
+            named_bar_arrive(kBarEntry, kThreadsA + 128);
             int L_prev = 0;
             bool stop = false;
             // exit state: S (after the last MMA4, which the caller has waited for) and z
@@ -558,6 +605,7 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                         mbar_arrive(&bar[kReadyS0 + s]);
                         mbar_arrive(&bar[kEmpty0 + s]);
                     }
+                    if (t == 0) LA_TL(it * 16 + 9);
                 }
                 if (!stop && !*abort_flag) {
                     bool ok = mbar_wait_or_abort(&bar[kOfull0], (n - 1) & 1, lim, abort_flag);
@@ -654,18 +702,44 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
     }
     if (warp == 1) tmem_dealloc(tbase, 512);
     if (tid == 0) LA_TL(4003);
+    LA_CTA_T(1);
 }
 
+// pdl: launch as a programmatic dependent of the previous kernel in the stream
+// (the kernel's entry-state reads wait for that kernel; everything else may
+// start early).
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
-cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s) {
+cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
     auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
     TraceScope trace(STATE_ONLY ? "chunk_tc_ws_kernel/state" : "chunk_tc_ws_kernel/full", s);
-    kern<<<grid, kThreadsWS, Lay::kAlloc, s>>>(prm);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreadsWS);
+    cfg.dynamicSmemBytes = Lay::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, prm);
+#ifdef LA_DEBUG_LAUNCH
+    {  // development aid: the reason a launch was refused, with the kernel's resources
+        cudaFuncAttributes fa;
+        cudaFuncGetAttributes(&fa, kern);
+        std::fprintf(stderr,
+                     "launch_ws<%d,%d,%d,%d>: %s; regs %d, local %zu B, max threads %d, "
+                     "dynamic smem %u B, static smem %zu B, grid %d x %d\n",
+                     DK, DVB, (int)NORM, (int)STATE_ONLY, cudaGetErrorString(e), fa.numRegs,
+                     fa.localSizeBytes, fa.maxThreadsPerBlock, Lay::kAlloc, fa.sharedSizeBytes, grid,
+                     kThreadsWS);
+    }
+#endif
+    return e;
 }
 
 }  // namespace
@@ -681,24 +755,24 @@ bool tc_ws_supported(int mode, int dk, int dvb, bool normalize) {
 }
 
 cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool pdl) {
     if (grid <= 0) return cudaSuccess;
     if (prm.mode == kStateOnly) {
-        if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, true>(prm, grid, s);
-        if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, true>(prm, grid, s);
-        if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true>(prm, grid, s);
-        if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true>(prm, grid, s);
+        if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, true>(prm, grid, s, pdl);
+        if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, true>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true>(prm, grid, s, pdl);
         return cudaErrorInvalidValue;
     }
     if (normalize) {
-        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true, false>(prm, grid, s);
-        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true, false>(prm, grid, s);
+        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true, false>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true, false>(prm, grid, s, pdl);
         return cudaErrorInvalidValue;
     }
-    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false>(prm, grid, s);
-    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false>(prm, grid, s);
-    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false>(prm, grid, s);
-    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, false>(prm, grid, s);
+    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false>(prm, grid, s, pdl);
+    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false>(prm, grid, s, pdl);
+    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false>(prm, grid, s, pdl);
+    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, false>(prm, grid, s, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -97,6 +97,16 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
     return mbar_wait_or_abort_slow(bar, parity, limit_ns, abort);
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel in the
+// stream (when launched with programmatic stream serialization) may be
+// scheduled once every CTA of this grid has issued it or exited.  wait: block
+// until the grids this one depends on have completed and their memory
+// operations are visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (whole warps), id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -178,6 +188,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)2 << 61;
     return d;
 }
+
+// The same descriptor with its start address moved on by `bytes` (a multiple
+// of 16): shared-memory addresses of a CTA stay below 2^18, so the 14-bit
+// field never carries into the next one.
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Instruction descriptor of tcgen05.mma .kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
