@@ -37,6 +37,20 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = ("retention fwd tokens/s & TFLOP/s (% bf16 TC peak); decode steps/s & HBM GB/s")
+
+# DRAM bytes (read + write) per launch of the headline's dominant kernel, from
+# the ncu capture summarised in profiles/chunk_tc_ws_kernel_linear_attention_bf16.md.
+# It holds only for the kernel sources that capture measured (their SHA-256
+# below); any later change to them makes the reported traffic null until the
+# kernel is captured again.
+KERNEL_SOURCES = ("chunk_tc_ws.cu", "chunk_tc_common.cuh", "tc_ptx.cuh", "chunk_tc.cu",
+                  "common.cuh", "launch.h")
+TRAFFIC = {
+    "chunk_tc_ws_kernel/full": {
+        "bytes": 52_533_760 + 240_640,
+        "sources_sha256": "a33eb59e83679c625248929f832c701dac867241424a0bb24275d3a9e6ae24f8",
+    },
+}
 HEADLINE = "linear_attention_bf16"
 L2_BYTES = 129 * 1024 * 1024
 C_REF = 64  # chunk length fixed for counting useful intra-chunk flops
@@ -78,6 +92,22 @@ def describe(name: str, c: dict) -> str:
             c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity",
             "normalised" if c["normalize"] else "no normaliser"]
     return ", ".join(bits)
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "retnet_retention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str) -> int | None:
+    t = TRAFFIC.get(kernel)
+    if t is None or t["sources_sha256"] != kernel_sources_sha256():
+        return None
+    return t["bytes"]
 
 
 def peaks() -> dict:
@@ -424,7 +454,7 @@ def run_ours(args) -> dict | None:
             "peak": pk["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved_gbs / pk["hbm_gbs"],
-            "traffic": None,
+            "traffic": measured_traffic(dom_name),
             "kernel": dom_name,
             "kernel_avg_ms": dom["avg_ms"],
             "peak_source": pk["source"],
