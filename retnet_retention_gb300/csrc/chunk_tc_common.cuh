@@ -82,22 +82,24 @@ __device__ __forceinline__ void phi_rows(char* tile, int nblk, int L, int t, int
     }
 }
 
-// The same over NT tiles of NBLK blocks each by exactly 128 threads, with
-// every load issued before the first exp and every store after the last, so
-// one thread has all its NT * NBLK * 8 16-byte pieces in flight at once.
-template <int NT, int NBLK>
-__device__ __forceinline__ void phi_rows_128(char* const (&tiles)[NT], int L, int t) {
-    constexpr int kPer = NBLK * (kBlk / 16) / 128;  // 16-byte pieces per thread and tile
+// The same over NT tiles of NBLK blocks each by exactly NTHR threads (a
+// multiple of 128 that divides a block's 1024 pieces), with every load issued
+// before the first exp and every store after the last, so one thread has all
+// its pieces in flight at once.
+template <int NT, int NBLK, int NTHR>
+__device__ __forceinline__ void phi_rows_all(char* const (&tiles)[NT], int L, int t) {
+    static_assert(NTHR % 128 == 0 && (kBlk / 16) % NTHR == 0, "thread count");
+    constexpr int kPer = NBLK * (kBlk / 16) / NTHR;  // 16-byte pieces per thread and tile
     uint4 u[NT][kPer];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) u[q][k] = reinterpret_cast<const uint4*>(tiles[q])[t + 128 * k];
+        for (int k = 0; k < kPer; ++k) u[q][k] = reinterpret_cast<const uint4*>(tiles[q])[t + NTHR * k];
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int r = ((t + 128 * k) >> 3) & 127;
+            const int r = ((t + NTHR * k) >> 3) & 127;
             __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[q][k]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) h[e] = phi_bf16x2(h[e]);
@@ -106,7 +108,7 @@ __device__ __forceinline__ void phi_rows_128(char* const (&tiles)[NT], int L, in
 #pragma unroll
     for (int q = 0; q < NT; ++q)
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) reinterpret_cast<uint4*>(tiles[q])[t + 128 * k] = u[q][k];
+        for (int k = 0; k < kPer; ++k) reinterpret_cast<uint4*>(tiles[q])[t + NTHR * k] = u[q][k];
 }
 
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`

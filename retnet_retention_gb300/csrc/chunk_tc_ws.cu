@@ -14,7 +14,8 @@
 //   warps 10-13 epilogue B: the entry state, the xi/zeta row scalings, the
 //               z update, and E2 (O of the previous chunk -> global, divided
 //               by the normaliser)
-//   warps 14-17 phi = elu + 1 on the Q/K tiles as they land, up to a ring's
+//   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for d_k = 64,
+//               4 for d_k = 128), up to a ring's
 //               depth ahead of the tensor work
 //
 // so that per chunk the tensor pipe waits only for E3 (and E2 frees O) after
@@ -89,7 +90,12 @@ using namespace tck;
 
 namespace {
 
-constexpr int kThreadsWS = 576;
+// Feature-map group: 8 warps for d_k = 64, 4 for d_k = 128.  More warps hide
+// the exp latency of phi; at d_k = 128 the register budget of the extra warps
+// (the SM's register file is split over its four schedulers) costs more than
+// they give, and those workloads rarely use phi.
+constexpr int threads_c(int dk) { return dk == 64 ? 256 : 128; }
+constexpr int threads_ws(int dk) { return 448 + threads_c(dk); }
 constexpr int kWgA = 2;   // first warp of epilogue A (8 warps: two per TMEM lane quarter)
 constexpr int kWgB = 10;  // first warp of epilogue B
 constexpr int kWgC = 14;  // first warp of the feature-map group
@@ -151,7 +157,9 @@ enum Bars {
 // issuer (kReadyS) has one slot per ring stage, which bounds how far the
 // epilogues may run ahead.
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
-__global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kThreadsC = threads_c(DK);
+    constexpr int kThreadsWS = threads_ws(DK);
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
     static_assert(!NORM || DVB == 64, "the normaliser's columns fit tensor memory only for DVB = 64");
     extern __shared__ __align__(1024) char smem_raw[];
@@ -491,18 +499,18 @@ __global__ void __launch_bounds__(kThreadsWS, 1) chunk_tc_ws_kernel(const __grid
                 const int s = it % NS;
                 const int L = min(kC, p.T - (cb + it) * kC);
                 bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
-                if (named_bar_or(kBarC, 128, !ok)) break;
+                if (named_bar_or(kBarC, kThreadsC, !ok)) break;
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
                 if constexpr (STATE_ONLY) {  // alone on the SM's conversion pipe: all loads first
                     char* const tiles[1] = {st + Lay::kQ};
-                    phi_rows_128<1, DK / 64>(tiles, L, t);
+                    phi_rows_all<1, DK / 64, kThreadsC>(tiles, L, t);
                 } else {  // one piece at a time, leaving the pipe to the epilogues' packs
-                    phi_rows(st, DK / 64, L, t, 128);
-                    phi_rows(st + Lay::kQ, DK / 64, L, t, 128);
+                    phi_rows(st, DK / 64, L, t, kThreadsC);
+                    phi_rows(st + Lay::kQ, DK / 64, L, t, kThreadsC);
                 }
                 fence_proxy_async_smem();
-                named_bar_sync(kBarC, 128);
+                named_bar_sync(kBarC, kThreadsC);
                 if (t == 0) mbar_arrive(&bar[kQk0 + s]);
                 if (t == 0) LA_TL(it * 16 + 13);
             }
@@ -718,7 +726,7 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     TraceScope trace(STATE_ONLY ? "chunk_tc_ws_kernel/state" : "chunk_tc_ws_kernel/full", s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreadsWS);
+    cfg.blockDim = dim3(threads_ws(DK));
     cfg.dynamicSmemBytes = Lay::kAlloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -736,7 +744,7 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
                      "dynamic smem %u B, static smem %zu B, grid %d x %d\n",
                      DK, DVB, (int)NORM, (int)STATE_ONLY, cudaGetErrorString(e), fa.numRegs,
                      fa.localSizeBytes, fa.maxThreadsPerBlock, Lay::kAlloc, fa.sharedSizeBytes, grid,
-                     kThreadsWS);
+                     threads_ws(DK));
     }
 #endif
     return e;
