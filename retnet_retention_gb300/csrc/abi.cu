@@ -91,7 +91,7 @@ int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
     ChunkArgs a = plan_args(B, H, T, d_k, d_v, dtype, flags, chunk);
     const char* pin = std::getenv("LA_CHUNK_PATH");
     if ((pin && std::strcmp(pin, "simt") == 0) || !tc_supported(a)) return 1;
-    return tc_workspace_bytes(B, H, T, d_k, d_v, a.noncausal) > 0 ? 3 : 1;
+    return tc_launch_count(B, H, T, d_k, d_v, a.noncausal, a.normalize);
 }
 
 la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_stream_t stream) {

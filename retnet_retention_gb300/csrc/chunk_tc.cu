@@ -636,6 +636,23 @@ bool tc_supported(const ChunkArgs& a) {
 
 static int tc_dvb(int dv) { return dv == 64 ? 64 : 128; }
 
+// Whether the output walk folds the segments' contributions into its entry states
+// itself (no scan kernel): few segments per sequence, and the pipelined kernel runs.
+static bool fold_segments(int P, int dk, int dvb, bool normalize) {
+    return P <= kFoldMax && tc_ws_supported(kFull, dk, dvb, normalize);
+}
+
+int tc_launch_count(int B, int H, int T, int dk, int dv, bool noncausal, bool normalize) {
+    if (noncausal || T <= 0) return 1;
+    const int n_chunks = (T + kC - 1) / kC;
+    const int units = B * H * (dv / tc_dvb(dv));
+    const int P = choose_segments(units, n_chunks);
+    if (P <= 1) return 1;
+    const int seg_chunks = (n_chunks + P - 1) / P;
+    const int Pu = (n_chunks + seg_chunks - 1) / seg_chunks;
+    return fold_segments(Pu, dk, tc_dvb(dv), normalize) ? 2 : 3;
+}
+
 size_t tc_workspace_bytes(int B, int H, int T, int dk, int dv, bool noncausal) {
     if (noncausal || T <= 0) return 0;
     const int n_chunks = (T + kC - 1) / kC;
@@ -727,6 +744,25 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     // launch all Pu segments' state walks (the last one's is unused but keeps the grid simple)
     cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * Pu, s);
     if (e != cudaSuccess) return e;
+    TcParams pc = prm;
+    pc.mode = kFull;
+    pc.seg_chunks = seg_chunks;
+    pc.n_seg = Pu;
+    pc.in_nseg = Pu;
+    pc.S_out = a.S_out;
+    pc.z_out = a.z_out;
+    pc.out_nseg = 1;
+    pc.out_last_only = 1;
+    if (fold_segments(Pu, a.dk, dvb, a.normalize != 0)) {
+        // few segments: the output walk folds the contributions into its entry states
+        pc.S_in = agg;
+        pc.z_in = zagg;
+        pc.in_agg = 1;
+        pc.S0 = a.S0;
+        pc.z0 = a.z0;
+        *launches = 2;
+        return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
+    }
     const size_t total = nbh * (size_t)a.dk * a.dv;
     {
         TraceScope trace("segment_scan_kernel", s);
@@ -744,17 +780,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
                                a.dk, a.dv, g);
     }
     if (e != cudaSuccess) return e;
-    TcParams pc = prm;
-    pc.mode = kFull;
-    pc.seg_chunks = seg_chunks;
-    pc.n_seg = Pu;
     pc.S_in = entry;
     pc.z_in = zentry;
-    pc.in_nseg = Pu;
-    pc.S_out = a.S_out;
-    pc.z_out = a.z_out;
-    pc.out_nseg = 1;
-    pc.out_last_only = 1;
     *launches = 3;
     return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
 }

@@ -16,6 +16,7 @@ using namespace tc;
 constexpr int kC = 128;           // chunk length (= MMA M)
 constexpr uint32_t kColP = 0;     // scores (fp32, 128 cols) then P (bf16 pairs, 64 cols)
 constexpr uint32_t kBlk = 16384;  // one [128 rows x 64 bf16] swizzled block
+constexpr int kFoldMax = 4;      // most segments per sequence whose entry states the output walk folds
 
 enum Mode { kFull = 0, kStateOnly = 1, kNonCausal = 2 };
 
@@ -38,6 +39,12 @@ struct TcParams {
     int track_z;                // carry the normaliser state z (normalising, or z_out wanted)
     int phi;
     float eps;
+    // in_agg: S_in / z_in hold the segments' own contributions (state walk), and the
+    // output walk folds them into its entry state itself, starting from S0 / z0
+    // (null = zero): entry_q = gamma^len entry_{q-1} + agg_{q-1}, len = seg_chunks * C
+    int in_agg;
+    const float* S0;
+    const float* z0;
     int* dev_status;
     unsigned long long wait_ns;
     int force_timeout;

@@ -236,6 +236,63 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
     auto load_entry_state = [&]() {
         const int sidx = bh * p.in_nseg + seg;
         const bool has_in = p.S_in != nullptr && !STATE_ONLY;
+        if (has_in && p.in_agg) {
+            // entry state of segment `seg` from S0 and the contributions of segments
+            // 0 .. seg-1 (at most kFoldMax - 1 of them), 8 columns at a time with
+            // every contribution's loads issued before the recurrence runs over them
+            const float gs = gamma_pow(l2g, (float)(p.seg_chunks * kC));
+            const size_t seg_stride = (size_t)DK * p.dv;
+            const int rr = row < DK ? row : 0;  // rows >= DK load nothing
+            const float* arow = p.S_in + ((size_t)(bh * p.in_nseg) * DK + rr) * p.dv + v0;
+            const float* s0row = p.S0 ? p.S0 + ((size_t)bh * DK + rr) * p.dv + v0 : nullptr;
+            for (int c0 = 0; c0 < DVB; c0 += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int h8 = 0; h8 < 32; h8 += 8) {
+                    float4 a[kFoldMax][2];
+#pragma unroll
+                    for (int q = 0; q < kFoldMax; ++q)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            a[q][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (row < DK) {
+                                if (q == 0 && s0row)
+                                    a[q][e] = *reinterpret_cast<const float4*>(s0row + c0 + h8 + 4 * e);
+                                else if (q > 0 && q <= seg)
+                                    a[q][e] = *reinterpret_cast<const float4*>(
+                                        arow + (size_t)(q - 1) * seg_stride + c0 + h8 + 4 * e);
+                            }
+                        }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float4 x = a[0][e];
+#pragma unroll
+                        for (int q = 1; q < kFoldMax; ++q)
+                            if (q <= seg) {
+                                x.x = fmaf(gs, x.x, a[q][e].x);
+                                x.y = fmaf(gs, x.y, a[q][e].y);
+                                x.z = fmaf(gs, x.z, a[q][e].z);
+                                x.w = fmaf(gs, x.w, a[q][e].w);
+                            }
+                        r[h8 + 4 * e] = __float_as_uint(x.x);
+                        r[h8 + 4 * e + 1] = __float_as_uint(x.y);
+                        r[h8 + 4 * e + 2] = __float_as_uint(x.z);
+                        r[h8 + 4 * e + 3] = __float_as_uint(x.w);
+                    }
+                }
+                tmem_st32(tbase + lane_off + Lay::kColS + c0, r);
+            }
+            tmem_st_wait();
+            if (row < DK) {
+                float zz = p.z0 ? p.z0[(size_t)bh * DK + row] : 0.f;
+                if (p.z_in)
+                    for (int q = 0; q < seg; ++q)
+                        zz = fmaf(gs, zz, p.z_in[(size_t)(bh * p.in_nseg + q) * DK + row]);
+                zs[row] = zz;
+            }
+            fence_before_sync();
+            return;
+        }
         const float* srow = has_in && row < DK ? p.S_in + ((size_t)sidx * DK + row) * p.dv + v0
                                                : nullptr;
         for (int c0 = 0; c0 < DVB; c0 += 32) {

@@ -59,6 +59,8 @@ int simt_chunk_len(int requested, int dk);
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);
 size_t tc_workspace_bytes(int B, int H, int T, int dk, int dv, bool noncausal);
+// Kernel launches of one tensor-core chunkwise call (1, 2 or 3).
+int tc_launch_count(int B, int H, int T, int dk, int dv, bool noncausal, bool normalize);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
                             int* launches);
 

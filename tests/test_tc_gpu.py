@@ -74,6 +74,8 @@ TC_SHAPES = [  # B, H, T, dk, dv
     (1, 1, 384, 128, 64),
     (1, 2, 4100, 128, 128),   # few sequences, many chunks: segmented
     (1, 1, 2000, 64, 64),     # segmented with a ragged last segment
+    (2, 16, 1000, 64, 64),    # 4 segments per sequence: entry states folded in the output walk
+    (1, 40, 700, 128, 128),   # 3 segments per sequence, d_k = 128
 ]
 
 
@@ -118,6 +120,30 @@ def test_tc_resume_from_state(tc_kernel):
     check("z_T", z2, zr)
 
 
+def test_tc_resume_from_state_folded_segments(tc_kernel):
+    """A continued prefill whose entry states are folded from the segments'
+    contributions and a nonzero initial state (32 sequences: 2-4 segments each)."""
+    x = workloads.random_case(43, 2, 16, 1000, 64, 64, dtype="bf16")
+    Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=True, normalize=True)
+    t1 = 389
+    a = {n: x[n][:, :, :t1].contiguous() for n in ("q", "k", "v")}
+    b = {n: x[n][:, :, t1:].contiguous() for n in ("q", "k", "v")}
+    a["gamma"] = b["gamma"] = x["gamma"]
+    O1, S1, z1 = run(a, True, True)
+    O2, S2, z2 = run(b, True, True, S0=torch.from_numpy(S1).float().to(DEV),
+                     z0=torch.from_numpy(z1).float().to(DEV))
+    check("O", np.concatenate([O1, O2], axis=2), Or)
+    check("S_T", S2, Sr)
+    check("z_T", z2, zr)
+
+
+def test_launch_count_follows_the_segment_plan():
+    lib = la.library()
+    assert lib.la_chunk_fwd_launches(2, 16, 1000, 64, 64, 1, 3, 0) == 2   # folded entry states
+    assert lib.la_chunk_fwd_launches(1, 8, 65536, 128, 128, 1, 0, 0) == 3  # segment scan
+    assert lib.la_chunk_fwd_launches(8, 16, 8192, 128, 256, 1, 0, 0) == 1  # one wave of units
+
+
 @pytest.mark.parametrize("flags", [(False, False), (True, True)],
                          ids=lambda f: f"phi{int(f[0])}_norm{int(f[1])}")
 def test_tc_noncausal(flags, tc_path):
@@ -141,7 +167,7 @@ def test_tc_and_simt_agree(monkeypatch):
 
 
 def test_tc_is_the_default_for_supported_shapes():
-    assert la.library().la_chunk_fwd_launches(4, 8, 4096, 64, 64, 1, 3, 0) in (1, 3)
+    assert la.library().la_chunk_fwd_launches(4, 8, 4096, 64, 64, 1, 3, 0) in (1, 2, 3)
     assert la.workspace_size(1, 8, 65536, 128, 128) > 0  # long and few: segmented
 
 
