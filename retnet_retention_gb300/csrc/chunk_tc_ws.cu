@@ -6,21 +6,26 @@
 // the roles run concurrently and hand work over through mbarriers:
 //
 //   warp 0      TMA producer: Q, K, V of chunk c into a ring of 2-4 stages
-//   warp 1      MMA issuer (one thread): MMA1 of chunk c+1 is issued ahead of
-//               MMA2..4 of chunk c, into the other of two TMEM score buffers
-//   warps 2-9   epilogue A: E1 (scores -> decay mask -> bf16 P back into
-//               TMEM) and E3 (bf16 copy of S for MMA3, S *= gamma^L); two
-//               warps per TMEM lane quarter, each on half of the columns
+//   warp 1      MMA issuer (one thread): per chunk c, MMA4 and MMA3 as soon as
+//               E3 of c and epilogue B have readied S and the tiles (the state
+//               chain), then MMA1 of c+1 into the other of two TMEM score
+//               buffers, then MMA2 of c once E1 has written P (with a single O
+//               buffer: MMA1 of c+1 first, the rest once S and P are ready)
+//   warps 2-9   epilogue A: per chunk, E3 first (bf16 copy of S for MMA3,
+//               S *= gamma^L), then E1 (scores -> decay mask -> bf16 P back into
+//               TMEM); two warps per TMEM lane quarter, each on half of the
+//               columns
 //   warps 10-13 epilogue B: the entry state, the xi/zeta row scalings, the
 //               z update, and E2 (O of the previous chunk -> global, divided
 //               by the normaliser)
-//   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for d_k = 64,
-//               4 for d_k = 128), up to a ring's
-//               depth ahead of the tensor work
+//   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for
+//               d_k = 64, 4 for d_k = 128), up to a ring's depth ahead of the
+//               tensor work
 //
-// so that per chunk the tensor pipe waits only for E3 (and E2 frees O) after
-// MMA4 of the previous chunk.  TMEM (512 columns): two score/P buffers at 0
-// and 128, O at 256 (two buffers for DVB = 64), S after O.
+// so that the state chain (MMA4 of c -> E3 of c+1 -> MMA4 of c+1) waits for
+// nothing but E3 and epilogue B's per-chunk work, and E1, phi and E2 run beside
+// it.  TMEM (512 columns): two score/P buffers at 0 and 128, O at 256 (two
+// buffers for DVB = 64), S after O.
 //
 // The normaliser runs on the tensor cores.  With z treated as one more value
 // column ("Linear Attention" page, the normalised form; z_c = gamma^L z_{c-1}
@@ -145,11 +150,15 @@ struct LayoutWS {
 
 // Barriers.  Stage barriers (full, empty, qk) have one slot per ring stage;
 // hand-overs that one side could otherwise complete twice before the other
-// side waits once are double-buffered by chunk parity (sfull, pready);
-// o_full / o_empty cannot run ahead.
+// side waits once are double-buffered by chunk parity (sfull, sready, pready);
+// o_full / o_empty cannot run ahead.  Per chunk c with two O buffers:
+// sready(c) = the bf16 copy of S and the scaled S and tiles are in place for
+// MMA3/MMA4 (epilogues A and B); pready(c) = P is in TMEM for MMA2 (epilogue A).
+// With one O buffer pready(c) carries both (epilogues A and B).  sdone(c) =
+// MMA3/MMA4 of c are complete.
 enum Bars {
     kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
-    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kNumBars
+    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kSready0, kSready1, kNumBars
 };
 
 // STATE_ONLY: the walk of a segment's own state contribution (mode
@@ -195,8 +204,12 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
         for (int q = 0; q < NS; ++q) mbar_init(&bar[kEmpty0 + q], 2);  // MMA commit + epilogue B
-        mbar_init(&bar[kPready0], 2);  // epilogue A + epilogue B
-        mbar_init(&bar[kPready1], 2);
+        mbar_init(&bar[kSready0], 2);  // epilogue A + epilogue B (two O buffers)
+        mbar_init(&bar[kSready1], 2);
+        // P ready: epilogue A alone with two O buffers; with one, S and P hand over
+        // together here (epilogue A + epilogue B)
+        mbar_init(&bar[kPready0], NOB == 2 ? 1 : 2);
+        mbar_init(&bar[kPready1], NOB == 2 ? 1 : 2);
         // state walk: epilogue B, plus epilogue A when S must be rescaled (gamma < 1)
         for (int q = 0; q < NS; ++q) mbar_init(&bar[kReadyS0 + q], unit_gamma ? 1 : 2);
         *abort_flag = 0;
@@ -386,11 +399,17 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                 (void)issue_mma1;
                 (void)id_pv;
             }
+            // Per chunk, with two O buffers: MMA4/MMA3 as soon as S is ready (the state
+            // chain), then MMA1 of the next chunk, then MMA2 once P is ready.  With one
+            // O buffer MMA3 must also wait for E2 of the previous chunk, so MMA1 of the
+            // next chunk goes first and MMA4/MMA3/MMA2 follow once S and P are ready.
             bool ok = !STATE_ONLY && issue_mma1(0);
             for (int it = 0; it < n && ok; ++it) {
                 const int s = it % NS;
-                if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
-                if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag)) break;
+                if (NOB == 1 && it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                if (!mbar_wait_or_abort(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)], (it >> 1) & 1,
+                                        lim, abort_flag))
+                    break;
                 LA_TL(it * 16 + 2);
                 const int ob = it % NOB;  // O buffer of this chunk
                 if (it >= NOB &&
@@ -404,8 +423,6 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                 // block of ones stands in for the next one (N = DVB + 16)
                 const uint32_t va = sbase + s * Lay::kStage + Lay::kQ + Lay::kK;
                 const uint64_t dv2 = NORM ? smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024) : dv;
-                // MMA3 and MMA4 first: the next chunk's E3 waits only for them (kSdone),
-                // while MMA2 runs
                 // MMA3: O = Q^ S_bf16 (K = DK)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
@@ -418,6 +435,12 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                     mma_ss(tbase + Lay::kColS, desc_adv(dk, kk * 2048), desc_adv(dv, kk * 2048), id_kv,
                            1u);
                 mma_commit(&bar[kSdone]);
+                if (NOB == 2) {
+                    if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                    if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag))
+                        break;
+                    fence_after_sync();
+                }
                 // MMA2: O += P V (A = P from TMEM, K = 128 tokens)
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
@@ -459,94 +482,112 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                     if (t == 0) mbar_arrive(&bar[kReadyS0 + it % NS]);
                 }
             }
+            // Per chunk, E3 (S after MMA3/MMA4 of the previous chunk -> bf16 copy for
+            // MMA3, S *= gamma^L before MMA4) and E1 (scores -> P for MMA2).  With two O
+            // buffers E3 goes first and hands over on its own (kSready), so the state
+            // chain does not wait for E1 (kPready).  With one, E1 goes first (MMA3 also
+            // waits for E2 of the previous chunk, and E1 overlaps that chunk's MMAs) and
+            // both hand over together (kPready).
             for (int it = 0; it < n && !STATE_ONLY; ++it) {
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
-                bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
-                if (named_bar_or(kBarA, kThreadsA, !ok)) break;
-                fence_after_sync();
-                if (t == 0) LA_TL(it * 16 + 4);
-                const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
-                const int i = row;
-                // this half's two 32-column pieces of scores, one at a time.  P (bf16
-                // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
-                // piece, so half 1 stores only after half 0 has read that piece (kBarP).
+                bool fail = false;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int c0 = 64 * half + 32 * q;
-                    uint32_t r[32];
-                    tmem_ld32(sc + c0, r);
-                    tmem_ld_wait();
-                    if (half == 0 && q == 1) {
-                        fence_before_sync();
-                        named_bar_arrive(kBarP, kThreadsA);
-                    }
-                    uint32_t pk[16];
-                    // gamma^(i-j) by a running product from the piece's top column down
-                    const int jt = min(i, c0 + 31);
-                    float w = (unit_gamma || jt < c0) ? 1.f : gamma_pow(l2g, (float)(i - jt));
-                    float a[32];
+                for (int step = 0; step < 2; ++step) {
+                    if ((NOB == 2) == (step == 0)) {  // ---- E3
+                        if (it >= 1) {
+                            const bool ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
+                            if (named_bar_or(kBarA, kThreadsA, !ok)) { fail = true; break; }
+                            fence_after_sync();
+                            if (t == 0) LA_TL(it * 16 + 6);
+                        }
+                        const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
 #pragma unroll
-                    for (int e = 31; e >= 0; --e) {
-                        const int j = c0 + e;
-                        float x = 0.f;
-                        if (j <= i) {
-                            x = __uint_as_float(r[e]);
+                        for (int c0 = half * kSHalf; c0 < (half + 1) * kSHalf; c0 += 32) {
+                            uint32_t rs[32];
+                            tmem_ld32(tbase + lane_off + Lay::kColS + c0, rs);
+                            tmem_ld_wait();
+                            if (row < DK) {
+#pragma unroll
+                                for (int e8 = 0; e8 < 32; e8 += 8) {
+                                    const int v = c0 + e8;
+                                    uint4 wv;
+                                    wv.x = pack_bf16x2(__uint_as_float(rs[e8 + 0]), __uint_as_float(rs[e8 + 1]));
+                                    wv.y = pack_bf16x2(__uint_as_float(rs[e8 + 2]), __uint_as_float(rs[e8 + 3]));
+                                    wv.z = pack_bf16x2(__uint_as_float(rs[e8 + 4]), __uint_as_float(rs[e8 + 5]));
+                                    wv.w = pack_bf16x2(__uint_as_float(rs[e8 + 6]), __uint_as_float(rs[e8 + 7]));
+                                    *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
+                                                              sw128_offset(row, v & 63)) = wv;
+                                }
+                            }
                             if (!unit_gamma) {
-                                x *= w;
-                                w *= gam;
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                                tmem_st32(tbase + lane_off + Lay::kColS + c0, rs);
                             }
                         }
-                        a[e] = x;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
-                    if (half == 1 && q == 0) {
-                        named_bar_sync(kBarP, kThreadsA);
+                        if (!unit_gamma) tmem_st_wait();
+                        fence_proxy_async_smem();
+                        fence_before_sync();
+                        named_bar_sync(kBarA, kThreadsA);
+                        if (t == 0) mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
+                        if (t == 0) LA_TL(it * 16 + 7);
+                    } else {  // ---- E1
+                        const bool ok1 = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
+                        if (named_bar_or(kBarA, kThreadsA, !ok1)) { fail = true; break; }
                         fence_after_sync();
-                    }
-                    tmem_st16(sc + (c0 >> 1), pk);
-                }
-                tmem_st_wait();
-                if (t == 0) LA_TL(it * 16 + 5);
-                // E3 needs S after MMA3/MMA4 of the previous chunk (kSdone)
-                if (it >= 1) {
-                    ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
-                    if (named_bar_or(kBarA, kThreadsA, !ok)) break;
-                    fence_after_sync();
-                    if (t == 0) LA_TL(it * 16 + 6);
-                }
-                const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
+                        if (t == 0) LA_TL(it * 16 + 4);
+                        const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
+                        const int i = row;
+                        // this half's two 32-column pieces of scores, one at a time.  P (bf16
+                        // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
+                        // piece, so half 1 stores only after half 0 has read that piece (kBarP).
 #pragma unroll
-                for (int c0 = half * kSHalf; c0 < (half + 1) * kSHalf; c0 += 32) {
-                    uint32_t rs[32];
-                    tmem_ld32(tbase + lane_off + Lay::kColS + c0, rs);
-                    tmem_ld_wait();
-                    if (row < DK) {
+                        for (int q = 0; q < 2; ++q) {
+                            const int c0 = 64 * half + 32 * q;
+                            uint32_t r[32];
+                            tmem_ld32(sc + c0, r);
+                            tmem_ld_wait();
+                            if (half == 0 && q == 1) {
+                                fence_before_sync();
+                                named_bar_arrive(kBarP, kThreadsA);
+                            }
+                            uint32_t pk[16];
+                            // gamma^(i-j) by a running product from the piece's top column down
+                            const int jt = min(i, c0 + 31);
+                            float w = (unit_gamma || jt < c0) ? 1.f : gamma_pow(l2g, (float)(i - jt));
+                            float a[32];
 #pragma unroll
-                        for (int e8 = 0; e8 < 32; e8 += 8) {
-                            const int v = c0 + e8;
-                            uint4 wv;
-                            wv.x = pack_bf16x2(__uint_as_float(rs[e8 + 0]), __uint_as_float(rs[e8 + 1]));
-                            wv.y = pack_bf16x2(__uint_as_float(rs[e8 + 2]), __uint_as_float(rs[e8 + 3]));
-                            wv.z = pack_bf16x2(__uint_as_float(rs[e8 + 4]), __uint_as_float(rs[e8 + 5]));
-                            wv.w = pack_bf16x2(__uint_as_float(rs[e8 + 6]), __uint_as_float(rs[e8 + 7]));
-                            *reinterpret_cast<uint4*>(sm + Lay::oSB + (v >> 6) * (DK * 128) +
-                                                      sw128_offset(row, v & 63)) = wv;
+                            for (int e = 31; e >= 0; --e) {
+                                const int j = c0 + e;
+                                float x = 0.f;
+                                if (j <= i) {
+                                    x = __uint_as_float(r[e]);
+                                    if (!unit_gamma) {
+                                        x *= w;
+                                        w *= gam;
+                                    }
+                                }
+                                a[e] = x;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                            if (half == 1 && q == 0) {
+                                named_bar_sync(kBarP, kThreadsA);
+                                fence_after_sync();
+                            }
+                            tmem_st16(sc + (c0 >> 1), pk);
                         }
-                    }
-                    if (!unit_gamma) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
-                        tmem_st32(tbase + lane_off + Lay::kColS + c0, rs);
+                        tmem_st_wait();
+                        if (NOB == 2) {
+                            fence_before_sync();
+                            named_bar_sync(kBarA, kThreadsA);
+                            if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
+                        }
+                        if (t == 0) LA_TL(it * 16 + 5);
                     }
                 }
-                if (!unit_gamma) tmem_st_wait();
-                fence_proxy_async_smem();
-                fence_before_sync();
-                named_bar_sync(kBarA, kThreadsA);
-                if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
-                if (t == 0) LA_TL(it * 16 + 7);
+                if (fail) break;
             }
         } else if (warp >= kWgC) {
             // ---------------- feature map: phi on Q and K (K only for a state walk), rows
@@ -687,9 +728,12 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                 const int L = min(kC, p.T - c * kC);
                 char* tQ = sm + s * Lay::kStage;
                 char* tK = tQ + Lay::kQ;
-                // MMA1 of this chunk is done with the unscaled tiles (and phi's writes
-                // to them are visible here through kQk)
-                bool ok = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
+                // The tiles of this chunk (phi's writes to them are visible through kQk);
+                // with gamma < 1 they are scaled in place, so MMA1 must be done with the
+                // unscaled ones first
+                bool ok = unit_gamma
+                              ? mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag)
+                              : mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
                 if (t == 0) LA_TL(it * 16 + 8);
@@ -701,6 +745,10 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                     named_bar_sync(kBarB, 128);
                 }
                 if (NORM || p.track_z) {
+                    // z_c = gamma^L z_{c-1} + sum_j K^[j] (rows >= L of K^ are zero): the
+                    // column sums first, off the state chain
+                    float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+                    colsum_partial<DK>(tK, t, zpart);
                     if (NORM) {
                         // z_{c-1} into the block after bf16 S, once MMA3 of the previous
                         // chunk has read the old one; MMA3 then adds xi_i q^_i . z_{c-1}
@@ -719,9 +767,6 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                         }
                         fence_proxy_async_smem();
                     }
-                    // z_c = gamma^L z_{c-1} + sum_j K^[j] (rows >= L of K^ are zero)
-                    float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
-                    colsum_partial<DK>(tK, t, zpart);
                     named_bar_sync(kBarB, 128);  // partials written; every read of z_{c-1} done
                     if (t < DK) {
                         const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
@@ -731,7 +776,7 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                 fence_before_sync();
                 named_bar_sync(kBarB, 128);
                 if (t == 0) {
-                    mbar_arrive(&bar[kPready0 + (it & 1)]);
+                    mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
                     mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
                 }
                 if (t == 0) LA_TL(it * 16 + 9);
