@@ -19,8 +19,8 @@
 //               z update, and E2 (O of the previous chunk -> global, divided
 //               by the normaliser)
 //   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for
-//               d_k = 64, 4 for d_k = 128), up to a ring's depth ahead of the
-//               tensor work
+//               64-wide Q/K and value blocks, else 2), up to a ring's depth
+//               ahead of the tensor work
 //
 // so that the state chain (MMA4 of c -> E3 of c+1 -> MMA4 of c+1) waits for
 // nothing but E3 and epilogue B's per-chunk work, and E1, phi and E2 run beside
@@ -95,12 +95,12 @@ using namespace tck;
 
 namespace {
 
-// Feature-map group: 8 warps for d_k = 64, 4 for d_k = 128.  More warps hide
-// the exp latency of phi; at d_k = 128 the register budget of the extra warps
-// (the SM's register file is split over its four schedulers) costs more than
+// Feature-map group: 8 warps for d_k = d_v-block = 64, else 2.  More warps hide
+// the exp latency of phi; for the wider tiles the registers of the extra warps
+// (the SM's register file is split over its four schedulers) cost more than
 // they give, and those workloads rarely use phi.
-constexpr int threads_c(int dk) { return dk == 64 ? 256 : 128; }
-constexpr int threads_ws(int dk) { return 448 + threads_c(dk); }
+constexpr int threads_c(int dk, int dvb) { return dk == 64 && dvb == 64 ? 256 : 64; }
+constexpr int threads_ws(int dk, int dvb) { return 448 + threads_c(dk, dvb); }
 constexpr int kWgA = 2;   // first warp of epilogue A (8 warps: two per TMEM lane quarter)
 constexpr int kWgB = 10;  // first warp of epilogue B
 constexpr int kWgC = 14;  // first warp of the feature-map group
@@ -166,9 +166,9 @@ enum Bars {
 // issuer (kReadyS) has one slot per ring stage, which bounds how far the
 // epilogues may run ahead.
 template <int DK, int DVB, bool NORM, bool STATE_ONLY>
-__global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
-    constexpr int kThreadsC = threads_c(DK);
-    constexpr int kThreadsWS = threads_ws(DK);
+__global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kThreadsC = threads_c(DK, DVB);
+    constexpr int kThreadsWS = threads_ws(DK, DVB);
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
     static_assert(!NORM || DVB == 64, "the normaliser's columns fit tensor memory only for DVB = 64");
     extern __shared__ __align__(1024) char smem_raw[];
@@ -600,9 +600,11 @@ __global__ void __launch_bounds__(threads_ws(DK), 1) chunk_tc_ws_kernel(const __
                 if (named_bar_or(kBarC, kThreadsC, !ok)) break;
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
-                if constexpr (STATE_ONLY) {  // alone on the SM's conversion pipe: all loads first
+                if constexpr (STATE_ONLY && kThreadsC % 128 == 0) {  // all loads first
                     char* const tiles[1] = {st + Lay::kQ};
                     phi_rows_all<1, DK / 64, kThreadsC>(tiles, L, t);
+                } else if constexpr (STATE_ONLY) {
+                    phi_rows(st + Lay::kQ, DK / 64, L, t, kThreadsC);
                 } else {  // one piece at a time, leaving the pipe to the epilogues' packs
                     phi_rows(st, DK / 64, L, t, kThreadsC);
                     phi_rows(st + Lay::kQ, DK / 64, L, t, kThreadsC);
@@ -828,7 +830,7 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     TraceScope trace(STATE_ONLY ? "chunk_tc_ws_kernel/state" : "chunk_tc_ws_kernel/full", s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(threads_ws(DK));
+    cfg.blockDim = dim3(threads_ws(DK, DVB));
     cfg.dynamicSmemBytes = Lay::kAlloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -846,7 +848,7 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
                      "dynamic smem %u B, static smem %zu B, grid %d x %d\n",
                      DK, DVB, (int)NORM, (int)STATE_ONLY, cudaGetErrorString(e), fa.numRegs,
                      fa.localSizeBytes, fa.maxThreadsPerBlock, Lay::kAlloc, fa.sharedSizeBytes, grid,
-                     threads_ws(DK));
+                     threads_ws(DK, DVB));
     }
 #endif
     return e;
