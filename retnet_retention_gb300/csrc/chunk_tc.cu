@@ -733,16 +733,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         (2 * nbh * Pu * a.dk * a.dv + 2 * nbh * Pu * a.dk) * sizeof(float))
         return cudaErrorInvalidValue;
 
-    TcParams pa = prm;  // state-only walks of segments 0 .. Pu-2
+    TcParams pa = prm;  // state-only walks of segments 0 .. Pu-2 (the last one's is not needed)
     pa.mode = kStateOnly;
     pa.seg_chunks = seg_chunks;
-    pa.n_seg = Pu;
+    pa.n_seg = Pu - 1;
     pa.S_out = agg;
     pa.z_out = zagg;
-    pa.out_nseg = Pu;
+    pa.out_nseg = Pu;  // contributions keep the [BH][Pu] layout the scan and the fold read
     pa.out_last_only = 0;
-    // launch all Pu segments' state walks (the last one's is unused but keeps the grid simple)
-    cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * Pu, s);
+    cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * (Pu - 1), s);
     if (e != cudaSuccess) return e;
     TcParams pc = prm;
     pc.mode = kFull;

@@ -118,6 +118,29 @@ __device__ __forceinline__ void phi_rows_all(char* const (&tiles)[NT], int L, in
         for (int k = 0; k < kPer; ++k) reinterpret_cast<uint4*>(tiles[q])[t + NTHR * k] = u[q][k];
 }
 
+// Row r of a [128 x 64*NBLK] K-major swizzled tile times fac(r), by exactly
+// NTHR threads, every load issued before the first multiply.
+template <int NBLK, int NTHR, typename F>
+__device__ __forceinline__ void scale_rows_all(char* tile, F fac, int t) {
+    static_assert(NTHR % 128 == 0 && (kBlk / 16) % NTHR == 0, "thread count");
+    constexpr int kPer = NBLK * (kBlk / 16) / NTHR;
+    uint4 u[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) u[k] = reinterpret_cast<const uint4*>(tile)[t + NTHR * k];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const float f = fac(((t + NTHR * k) >> 3) & 127);
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[k]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(h[e]);
+            h[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) reinterpret_cast<uint4*>(tile)[t + NTHR * k] = u[k];
+}
+
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`
 // threads (this one is `t`): apply phi (optional) and multiply row r by
 // fac(r).  Rows are whole 128-byte lines, so the swizzle never moves an

@@ -691,13 +691,18 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                         stop = true;
                         break;
                     }
-                    // K^ = zeta . phi(K), rows >= L zeroed
+                    // K^ = zeta . phi(K), rows >= L zeroed; then MMA4 may go (kReadyS)
                     if (!unit_gamma)
-                        row_pass(tK, DK / 64, false,
-                                 [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
-                                 t, 128);
+#pragma unroll 1
+                        for (int b = 0; b < DK / 64; ++b)  // one 64-column block at a time
+                            scale_rows_all<1, 128>(
+                                tK + b * kBlk, [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
+                                t);
+                    fence_proxy_async_smem();
+                    fence_before_sync();
                     named_bar_sync(kBarB, 128);
-                    if (p.track_z) {  // z_c = gamma^L z_{c-1} + sum_j K^[j]
+                    if (t == 0) mbar_arrive(&bar[kReadyS0 + s]);
+                    if (p.track_z) {  // z_c = gamma^L z_{c-1} + sum_j K^[j], beside MMA4
                         float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
                         colsum_partial<DK>(tK, t, zpart);
                         named_bar_sync(kBarB, 128);
@@ -705,14 +710,9 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                             const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
                             zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
                         }
+                        named_bar_sync(kBarB, 128);  // every read of the stage and of zpart done
                     }
-                    fence_proxy_async_smem();
-                    fence_before_sync();
-                    named_bar_sync(kBarB, 128);
-                    if (t == 0) {
-                        mbar_arrive(&bar[kReadyS0 + s]);
-                        mbar_arrive(&bar[kEmpty0 + s]);
-                    }
+                    if (t == 0) mbar_arrive(&bar[kEmpty0 + s]);
                     if (t == 0) LA_TL(it * 16 + 9);
                 }
                 if (!stop && !*abort_flag) {
