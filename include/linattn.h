@@ -78,6 +78,12 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
 #define LA_PHI_ELU1  1u  /* apply phi(x) = elu(x) + 1 to q and k (not v) */
 #define LA_NORMALIZE 2u  /* divide by phi(q)^T z + eps */
 #define LA_NONCAUSAL 4u  /* every query reads the whole sequence; gamma must be 1 */
+/* Divide by max(|phi(q)^T z|, 1) instead of phi(q)^T z + eps (implies normalising;
+ * eps unused): the matrix LSTM's floored normaliser, box "An LSTM whose cell is
+ * linear attention" on the "Linear attention" page, which equals RetNet's
+ * division of each score row by the absolute value of its sum clamped below at 1
+ * (same page, "Its normalizer is unstable").  Defined for signed features too. */
+#define LA_NORM_FLOOR 8u
 
 /* Human-readable text of a status code (static storage, never NULL). */
 LA_API const char* la_status_string(int status);
@@ -96,8 +102,9 @@ LA_API size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype 
 
 /*
  * Number of kernels la_chunk_fwd enqueues for these arguments on the current
- * device (1 for the single-pass paths; 3 when a long sequence is split into
- * segments: segment states, the scan over them, the outputs).  0 for
+ * device (1 for the single-pass paths; 2 or 3 when long sequences are split
+ * into segments: segment states, then - for more than four segments per
+ * sequence - the scan over them, then the outputs).  0 for
  * arguments la_chunk_fwd would reject or T == 0.  Pure host query.
  */
 LA_API int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
@@ -121,9 +128,9 @@ LA_API la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_
  *   Q, K      [B][H][T][d_k]  dtype      inputs, read only
  *   V         [B][H][T][d_v]  dtype      input, read only
  *   gamma     host float[H]              per-head decay in (0, 1]
- *   flags     LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL
- *   eps       added to the denominator (used only with LA_NORMALIZE; the
- *             pages use 1e-6)
+ *   flags     LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR
+ *   eps       added to the denominator (used only with LA_NORMALIZE and not
+ *             LA_NORM_FLOOR; the pages use 1e-6)
  *   S0, z0    [B][H][d_k][d_v], [B][H][d_k] fp32 initial state, or NULL for
  *             zero.  S0 may alias S_out and z0 may alias z_out (in-place
  *             continuation).  The normaliser state z is carried whether or
@@ -163,12 +170,14 @@ LA_API la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dt
  * what each costs"; update first, then read, so the token is in its own sum):
  *
  *   S = gamma S + phi(k) v^T ;  z = gamma z + phi(k)     (z only if normalising)
- *   o = phi(q)^T S  [ / (phi(q)^T z + eps) ]
+ *   o = phi(q)^T S  [ / (phi(q)^T z + eps) ]  [ / max(|phi(q)^T z|, 1) ]
  *
  *   q, k   [B][H][d_k] dtype;  v [B][H][d_v] dtype;  o [B][H][d_v] dtype
  *   S      [B][H][d_k][d_v] fp32, read and written in place
- *   z      [B][H][d_k] fp32, in place; required with LA_NORMALIZE, else ignored
- *   flags  LA_PHI_ELU1 | LA_NORMALIZE (LA_NONCAUSAL is LA_ERR_UNSUPPORTED)
+ *   z      [B][H][d_k] fp32, in place; required with LA_NORMALIZE or
+ *          LA_NORM_FLOOR, else ignored
+ *   flags  LA_PHI_ELU1 | LA_NORMALIZE | LA_NORM_FLOOR (LA_NONCAUSAL is
+ *          LA_ERR_UNSUPPORTED)
  * Errors: as la_chunk_fwd.
  */
 LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,

@@ -25,6 +25,12 @@ noncausal(q, k, v, phi, normalize, eps)
     gamma = 1, every query reads the one summary phi(K)^T V: box "Linear
     attention" on the "Linear attention" page.
 
+Each takes ``floor=True`` for the floored normaliser, o / max(|phi(q)^T z|, 1):
+the matrix LSTM of the box "An LSTM whose cell is linear attention" on the
+"Linear attention" page, which equals RetNet's division of each score row by
+the absolute value of its sum, clamped below at 1 (same page, "Its normalizer
+is unstable").
+
 Pins: every function here is checked in ``tests/test_oracle.py`` against the
 pages' worked example, brute-force parallel forms, closed forms, a library
 IIR filter and invariants; see that file for which pin covers which part.
@@ -89,12 +95,17 @@ def _as4(x: np.ndarray, name: str) -> np.ndarray:
     return np.ascontiguousarray(x)
 
 
+def _norm_mode(normalize: bool, floor: bool) -> int:
+    return 2 if floor else (1 if normalize else 0)
+
+
 def recurrent(q, k, v, gamma, phi: bool = False, normalize: bool = False,
-              eps: float = 1e-6, S0=None, z0=None, _lib=None):
+              eps: float = 1e-6, S0=None, z0=None, _lib=None, floor: bool = False):
     """Causal recurrent form in fp64.
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv]; gamma: [H] (or a scalar).
     S0: [B,H,dk,dv] or None; z0: [B,H,dk] or None.
+    floor: divide by max(|q~^T z|, 1) instead (implies normalising; no eps).
     Returns (O [B,H,T,dv], S_T [B,H,dk,dv], z_T [B,H,dk]) as float64 arrays.
     """
     Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
@@ -110,14 +121,14 @@ def recurrent(q, k, v, gamma, phi: bool = False, normalize: bool = False,
     z = np.empty((B, H, dk))
     rc = (_lib or lib()).oracle_recurrent(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(g), B, H, T, dk, dv, int(bool(phi)),
-        int(bool(normalize)), float(eps), _ptr(S0a), _ptr(z0a), _ptr(O), _ptr(S), _ptr(z))
+        _norm_mode(normalize, floor), float(eps), _ptr(S0a), _ptr(z0a), _ptr(O), _ptr(S), _ptr(z))
     if rc != 0:
         raise MemoryError("oracle_recurrent: scratch allocation failed")
     return O, S, z
 
 
 def decode_step(q, k, v, gamma, S, z=None, phi: bool = False, normalize: bool = False,
-                eps: float = 1e-6):
+                eps: float = 1e-6, floor: bool = False):
     """One recurrent decode step for [B,H,dk] q,k and [B,H,dv] v.
 
     Returns (o [B,H,dv], S_new, z_new); the inputs are not modified.
@@ -125,12 +136,12 @@ def decode_step(q, k, v, gamma, S, z=None, phi: bool = False, normalize: bool = 
     q4 = _f64(q)[:, :, None, :]
     k4 = _f64(k)[:, :, None, :]
     v4 = _f64(v)[:, :, None, :]
-    O, S_new, z_new = recurrent(q4, k4, v4, gamma, phi, normalize, eps, S0=S, z0=z)
+    O, S_new, z_new = recurrent(q4, k4, v4, gamma, phi, normalize, eps, S0=S, z0=z, floor=floor)
     return O[:, :, 0, :], S_new, z_new
 
 
 def noncausal(q, k, v, phi: bool = False, normalize: bool = False, eps: float = 1e-6,
-              _lib=None):
+              _lib=None, floor: bool = False):
     """Non-causal (gamma = 1) form in fp64; returns (O, S, z) like ``recurrent``."""
     Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
     B, H, T, dk = Q.shape
@@ -139,7 +150,7 @@ def noncausal(q, k, v, phi: bool = False, normalize: bool = False, eps: float = 
     S = np.empty((B, H, dk, dv))
     z = np.empty((B, H, dk))
     rc = (_lib or lib()).oracle_noncausal(
-        _ptr(Q), _ptr(K), _ptr(V), B, H, T, dk, dv, int(bool(phi)), int(bool(normalize)),
+        _ptr(Q), _ptr(K), _ptr(V), B, H, T, dk, dv, int(bool(phi)), _norm_mode(normalize, floor),
         float(eps), _ptr(O), _ptr(S), _ptr(z))
     if rc != 0:
         raise MemoryError("oracle_noncausal: scratch allocation failed")

@@ -14,7 +14,8 @@
  *       q~ = phi(q_t),  k~ = phi(k_t)                 phi = elu+1 or identity
  *       S  = gamma * S + k~ v_t^T                      (d_k x d_v)
  *       z  = gamma * z + k~                            (d_k)
- *       o_t = q~^T S          [ / (q~^T z + eps) if normalising ]
+ *       o_t = q~^T S          [ / (q~^T z + eps)       if normalising,
+ *                               / max(|q~^T z|, 1)    with the floored normaliser ]
  *
  * Sources (web pages on retention / linear attention):
  *  - "Linear attention" (zerotofrontier, Chapter 21 section 21.2), box
@@ -33,12 +34,18 @@
  *    subsection 4: the generic "decay the old state, add, read out" loop.
  *  - Non-causal form: "Linear attention" (zerotofrontier 21.2), box "Linear
  *    attention": O = diag(phi(Q)(phi(K)^T 1))^-1 phi(Q)(phi(K)^T V).
+ *  - Floored normaliser: same page, section "Its normalizer is unstable" and
+ *    the box "An LSTM whose cell is linear attention": the matrix LSTM divides
+ *    C_t q_t by max(|n_t^T q_t|, 1), n_t the normaliser decayed with the state's
+ *    gate; RetNet divides each row of its scores by the absolute value of the
+ *    row's sum, clamped below at 1 (the same number: that row sum is q^T z).
  *
  * Readings where the pages are silent:
  *  - with gamma < 1 and the normaliser on, z decays with the same gamma as S
  *    (the pages never combine the two; the xLSTM box on the "Linear
  *    attention" page decays its normaliser with the same gate as its state);
- *  - eps is added after the dot product, only when normalising.
+ *  - eps is added after the dot product, only when normalising with eps; the
+ *    floored normaliser has no eps.
  *
  * Compile-time mutants (ORACLE_MUTANT=n) exist only so that the pin tests can
  * show that each plausible mistake is caught; the default build has none.
@@ -72,6 +79,7 @@ static void feature(const double* x, double* out, long n, int phi)
  *   Q, K : [B][H][T][dk]     V : [B][H][T][dv]     gamma : [H]
  *   S0   : [B][H][dk][dv] or NULL (zero state)     z0 : [B][H][dk] or NULL
  *   O    : [B][H][T][dv]     S_out : [B][H][dk][dv] or NULL   z_out : [B][H][dk] or NULL
+ *   normalize: 0 none, 1 divide by q~^T z + eps, 2 divide by max(|q~^T z|, 1)
  *
  * Returns 0, or -1 when a scratch allocation fails.
  */
@@ -149,7 +157,15 @@ int oracle_recurrent(const double* Q, const double* K, const double* V,
 #else
                 for (long i = 0; i < dk; ++i) den += qf[i] * z[i];
 #endif
-                den += eps;
+                if (normalize == 2) {
+#if ORACLE_MUTANT == 8 /* mutant: floor without the absolute value */
+                    den = den > 1.0 ? den : 1.0;
+#else
+                    den = fabs(den) > 1.0 ? fabs(den) : 1.0;
+#endif
+                } else {
+                    den += eps;
+                }
                 for (long j = 0; j < dv; ++j) o[j] /= den;
             }
         }
@@ -163,6 +179,7 @@ int oracle_recurrent(const double* Q, const double* K, const double* V,
 /*
  * Non-causal form (gamma = 1 only): one summary shared by every query.
  *   S = sum_t k~_t v_t^T,  z = sum_t k~_t,  o_t = q~_t^T S [ / (q~_t^T z + eps) ]
+ *   (or / max(|q~_t^T z|, 1) with normalize == 2)
  * Same layouts as oracle_recurrent; S_out/z_out receive S and z.
  */
 int oracle_noncausal(const double* Q, const double* K, const double* V,
@@ -201,8 +218,9 @@ int oracle_noncausal(const double* Q, const double* K, const double* V,
                 o[j] = acc;
             }
             if (normalize) {
-                double den = eps;
+                double den = 0.0;
                 for (long i = 0; i < dk; ++i) den += f[i] * z[i];
+                den = normalize == 2 ? (fabs(den) > 1.0 ? fabs(den) : 1.0) : den + eps;
                 for (long j = 0; j < dv; ++j) o[j] /= den;
             }
         }

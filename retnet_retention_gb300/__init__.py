@@ -24,7 +24,7 @@ from . import _build
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
-LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL = 1, 2, 4
+LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR = 1, 2, 4, 8
 
 LIBRARY_PATH = _build.LIBRARY
 _LIB = None
@@ -110,9 +110,9 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
 
 
-def _flags(phi: bool, normalize: bool, causal: bool) -> int:
+def _flags(phi: bool, normalize: bool, causal: bool, floor: bool = False) -> int:
     return (LA_PHI_ELU1 if phi else 0) | (LA_NORMALIZE if normalize else 0) | (
-        0 if causal else LA_NONCAUSAL)
+        0 if causal else LA_NONCAUSAL) | (LA_NORM_FLOOR if floor else 0)
 
 
 def _ptr(t) -> int | None:
@@ -163,13 +163,15 @@ def state_init(S: torch.Tensor, z: torch.Tensor | None = None, stream=None):
 
 def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
               S0=None, z0=None, chunk=0, out=None, S_out=None, z_out=None, return_state=True,
-              workspace=None, dev_status=None, stream=None):
+              workspace=None, dev_status=None, stream=None, floor=False):
     """Chunkwise forward over [B,H,T,d] device tensors.
 
     Returns (O, S_T, z_T); S_T / z_T are None when return_state is False and
     no output buffer was given.  z_T is returned when normalising (or when
-    z_out is given).
+    z_out is given).  floor=True divides by max(|phi(q)^T z|, 1) (LA_NORM_FLOOR;
+    implies normalising, eps unused).
     """
+    normalize = normalize or floor
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
@@ -185,7 +187,7 @@ def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e
     if return_state and normalize and z_out is None:
         z_out = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
     g = _gamma_host(gamma, H)
-    flags = _flags(phi, normalize, causal)
+    flags = _flags(phi, normalize, causal, floor)
     lib = _load()
     need = int(lib.la_workspace_size(B, H, T, dk, dv, dt, flags, chunk))
     if need and workspace is None:
@@ -201,7 +203,7 @@ def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e
 
 def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
                       S0=None, z0=None, chunk=0, out=None, S_out=None, z_out=None,
-                      dev_status=None, stream=None):
+                      dev_status=None, stream=None, floor=False):
     """chunk_fwd through la_chunk_fwd_noalloc: no workspace argument; the library's
     fixed scratch array is used instead (for callers that cannot allocate device
     memory).  out / S_out / z_out must be given: this call allocates nothing."""
@@ -211,7 +213,7 @@ def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True
         raise ValueError("chunk_fwd_noalloc allocates nothing: pass out and S_out")
     g = _gamma_host(gamma, H)
     st = _load().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
-                                      H, T, dk, dv, _flags(phi, normalize, causal), float(eps),
+                                      H, T, dk, dv, _flags(phi, normalize, causal, floor), float(eps),
                                       _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out), _ptr(z_out),
                                       int(chunk), _ptr(dev_status), _stream(stream))
     _check(st, "la_chunk_fwd_noalloc")
@@ -219,15 +221,16 @@ def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True
 
 
 def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps=1e-6,
-                   out=None, dev_status=None, stream=None):
-    """One decode step on [B,H,d] device tensors; S (and z) are updated in place."""
+                   out=None, dev_status=None, stream=None, floor=False):
+    """One decode step on [B,H,d] device tensors; S (and z) are updated in place.
+    floor=True: divide by max(|phi(q)^T z|, 1) (needs z)."""
     B, H, dk = q.shape
     dv = v.shape[-1]
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     g = _gamma_host(gamma, H)
     st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
-                                   H, dk, dv, _flags(phi, normalize, True), float(eps), _ptr(S),
+                                   H, dk, dv, _flags(phi, normalize, True, floor), float(eps), _ptr(S),
                                    _ptr(z), _ptr(out), _ptr(dev_status), _stream(stream))
     _check(st, "la_recurrent_step")
     return out
@@ -317,4 +320,4 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
            "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
-           "LA_NORMALIZE", "LA_NONCAUSAL"]
+           "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR"]

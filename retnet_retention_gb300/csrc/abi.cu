@@ -65,7 +65,8 @@ static ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype
     a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
     a.bf16 = dtype == LA_DTYPE_BF16;
     a.phi = (flags & LA_PHI_ELU1) != 0;
-    a.normalize = (flags & LA_NORMALIZE) != 0;
+    a.normalize = (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0;
+    a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
     a.noncausal = (flags & LA_NONCAUSAL) != 0;
     return a;
 }
@@ -73,7 +74,7 @@ static ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype
 static bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags) {
     return B > 0 && H > 0 && T > 0 && valid_dim(d_k) && valid_dim(d_v) && H <= kMaxHeads &&
            (dtype == LA_DTYPE_F32 || dtype == LA_DTYPE_BF16) &&
-           !(flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL));
+           !(flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR));
 }
 
 size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
@@ -110,7 +111,7 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
                        size_t workspace_bytes, int* dev_status, la_stream_t stream) {
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR)) return LA_ERR_INVALID_ARG;
     if (!(chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128))
         return LA_ERR_INVALID_ARG;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
@@ -122,7 +123,8 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     bool all_one = true;
     if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
     const bool noncausal = (flags & LA_NONCAUSAL) != 0;
-    const bool normalize = (flags & LA_NORMALIZE) != 0;
+    const bool floor_norm = (flags & LA_NORM_FLOOR) != 0;
+    const bool normalize = (flags & LA_NORMALIZE) != 0 || floor_norm;
     if (noncausal && (!all_one || S0 || z0)) return LA_ERR_UNSUPPORTED;
 
     const size_t es = elem_size(dtype);
@@ -158,6 +160,7 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     a.bf16 = dtype == LA_DTYPE_BF16;
     a.phi = (flags & LA_PHI_ELU1) != 0;
     a.normalize = normalize;
+    a.floor_norm = floor_norm;
     a.noncausal = noncausal;
     a.eps = eps;
     a.workspace = workspace;
@@ -183,7 +186,7 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtyp
     (void)dev_status;  // the decode step has no device-side waits
     if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR)) return LA_ERR_INVALID_ARG;
     if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
@@ -193,7 +196,8 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtyp
     KernelGammas g;
     bool all_one = true;
     if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
-    const bool normalize = (flags & LA_NORMALIZE) != 0;
+    const bool floor_norm = (flags & LA_NORM_FLOOR) != 0;
+    const bool normalize = (flags & LA_NORMALIZE) != 0 || floor_norm;
     if (!q || !k || !v || !o || !S || (normalize && !z)) return LA_ERR_INVALID_ARG;
     for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
                           (const void*)S, (const void*)z})
@@ -210,6 +214,7 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtyp
     a.bf16 = dtype == LA_DTYPE_BF16;
     a.phi = (flags & LA_PHI_ELU1) != 0;
     a.normalize = normalize;
+    a.floor_norm = floor_norm;
     a.eps = eps;
     return cuda_status(launch_decode_step(a, g, (cudaStream_t)stream));
 }

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
                             for (int j = 0; j <= i; ++j) r += As[i * lda + j];
                         float qz = 0.f;
                         for (int d = 0; d < dk; ++d) qz = fmaf(Qs[i * ld + d], zs[d], qz);
-                        den[i] = r + (noncausal ? 1.f : pw[i + 1]) * qz + eps;
+                        den[i] = norm_den(r + (noncausal ? 1.f : pw[i + 1]) * qz, normalize, eps);
                     }
                     __syncthreads();
                 }
@@ -214,7 +214,7 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStr
         kern<<<grid, kThreads, smem, s>>>(
             (const __nv_bfloat16*)a.Q, (const __nv_bfloat16*)a.K, (const __nv_bfloat16*)a.V,
             (__nv_bfloat16*)a.O, a.S0, a.z0, a.S_out, a.z_out, a.H, a.T,
-            a.dk, a.dv, C, dvb, a.phi, a.normalize, a.noncausal, a.eps, g);
+            a.dk, a.dv, C, dvb, a.phi, norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps, g);
     } else {
         auto kern = chunk_simt_kernel<float>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -222,7 +222,7 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStr
         kern<<<grid, kThreads, smem, s>>>(
             (const float*)a.Q, (const float*)a.K, (const float*)a.V, (float*)a.O, a.S0,
             a.z0, a.S_out, a.z_out, a.H, a.T, a.dk, a.dv, C, dvb, a.phi,
-            a.normalize, a.noncausal, a.eps, g);
+            norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps, g);
     }
     return cudaGetLastError();
 }

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
             __syncthreads();
             fence_after_sync();
 
-            float r_i = 0.f;  // row sum of P (normaliser)
+            float r_i = 0.f;  // row sum of the scores (normaliser)
             if (do_intra) {
                 if (tid == 0) {
                     // MMA1: scores[128 x 128] = Q K^T, K = DK
@@ -305,28 +305,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                     }
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const uint32_t u = pack_bf16x2(a[e], a[e + 1]);
-                        pk[e >> 1] = u;
-                        const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-                        r_i += back.x + back.y;
+                        pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                        // the row sum in fp32, before P is rounded: with signed features
+                        // the denominator can be a small difference of large sums
+                        r_i += a[e] + a[e + 1];
                     }
                     tmem_st16(tbase + lane_off + kColP + (c0 >> 1), pk);
                 }
                 tmem_st_wait();
             }
-            // Q^ = xi . Q, K^ = zeta . K (rows >= L of K get 0)
-            const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
-            if (!unit_gamma) {
-                if (do_out)
-                    row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); },
-                             tid, kThreads);
-                if (do_state)
-                    row_pass(tK, DK / 64, false,
-                             [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
-                             tid, kThreads);
+            // the normaliser state's sum_j zeta_j phi(K)[j], in fp32 from the tile before
+            // it is scaled (added to z below, after z_{c-1} has been read)
+            float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+            if (p.track_z && do_state) {
+                if (unit_gamma)
+                    colsum_partial<DK>(tK, tid, zpart);
+                else
+                    colsum_partial_decayed<DK>(tK, tid, zpart, L, l2g, p.g.gamma[h]);
             }
-            __syncthreads();
-            // normaliser: qz_i = q^_i . z_{c-1}
+            // normaliser: qz_i = xi_i (q^_i . z_{c-1}), in fp32 from the unscaled tile (with
+            // signed features q . z can be a small difference of large terms)
             float qz = 0.f;
             if (p.normalize && do_out) {
                 const int i = tid;
@@ -341,7 +339,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                         qz = fmaf(x.y, zs[d8 + 2 * e + 1], qz);
                     }
                 }
+                if (!unit_gamma) qz *= gamma_pow(l2g, (float)(i + 1));
             }
+            // Q^ = xi . Q, K^ = zeta . K (rows >= L of K get 0), once every read above is done
+            const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
+            if (!unit_gamma || (p.track_z && do_state)) __syncthreads();
+            if (!unit_gamma) {
+                if (do_out)
+                    row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); },
+                             tid, kThreads);
+                if (do_state)
+                    row_pass(tK, DK / 64, false,
+                             [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
+                             tid, kThreads);
+            }
+            __syncthreads();
             // E3: S_bf16 = bf16(S_{c-1}) (for MMA3), S = gamma^L S (before MMA4 accumulates)
             const bool need_sb = do_out && p.mode == kFull;
             const bool scale_s = do_state && !unit_gamma;
@@ -406,12 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
                 mma_commit(bar_mma);
             }
             mma_inflight = true;
-            // normaliser state: z_c = gamma^L z + sum_j K^[j]   (z_{c-1} already used above;
-            // rows >= L of K^ are zero)
+            // normaliser state: z_c = gamma^L z + sum_j zeta_j phi(K)[j]   (z_{c-1} already
+            // used above; the partial sums were taken before the scaling)
             if (p.track_z && do_state) {
-                float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
-                colsum_partial<DK>(tK, tid, zpart);
-                __syncthreads();
                 if (tid < DK) zs[tid] = fmaf(unit_gamma ? 1.f : gL, zs[tid], colsum_total<DK>(zpart, tid));
             }
             to = !mbar_wait(bar_mma, mma_phase, p.wait_ns);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
             // E2: O row i = tid -> global (rows < L)
             if (do_out) {
                 const int i = tid;
-                const float inv = p.normalize ? 1.f / (r_i + qz + p.eps) : 1.f;
+                const float inv = p.normalize ? 1.f / norm_den(r_i + qz, p.normalize, p.eps) : 1.f;
                 __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + i) * p.dv + v0;
                 for (int c0 = 0; c0 < DVB; c0 += 32) {
                     uint32_t r[32];
@@ -678,7 +687,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     prm.T = a.T;
     prm.dv = a.dv;
     prm.n_dvb = a.dv / dvb;
-    prm.normalize = a.normalize;
+    prm.normalize = norm_mode(a.normalize, a.floor_norm);
     prm.track_z = a.normalize || a.z_out != nullptr;
     prm.phi = a.phi;
     prm.eps = a.eps;

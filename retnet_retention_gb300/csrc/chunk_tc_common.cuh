@@ -35,7 +35,7 @@ struct TcParams {
     int seg_chunks;             // chunks per segment
     int n_seg;                  // segments per sequence
     int mode;
-    int normalize;
+    int normalize;              // 0 none, 1 divide by q^.z + eps, 2 by max(|q^.z|, 1)
     int track_z;                // carry the normaliser state z (normalising, or z_out wanted)
     int phi;
     float eps;
@@ -141,6 +141,98 @@ __device__ __forceinline__ void scale_rows_all(char* tile, F fac, int t) {
     for (int k = 0; k < kPer; ++k) reinterpret_cast<uint4*>(tile)[t + NTHR * k] = u[k];
 }
 
+// Q^ = xi . Q in place over a [128 x DK] K-major swizzled bf16 tile by 128
+// threads, and per row out[r] = xi_r (q_r . z) in fp32 from the tile before it
+// is rounded: the inter-chunk part of the normaliser without the bf16 rounding
+// of xi_r q_r (with signed features q . z can be a small difference of large
+// terms).  Thread t holds 16-byte piece t & 7 of rows (t >> 3) + 16 m, m < 8,
+// in every 64-column block; the 8 pieces of a row sit in 8 consecutive lanes.
+template <int DK, typename F>
+__device__ __forceinline__ void scale_rows_dot(char* tile, F fac, const float* z, float* out, int t) {
+    const int pc = t & 7;
+#pragma unroll 1
+    for (int m = 0; m < 8; ++m) {
+        const int r = (t >> 3) + 16 * m;
+        const int lc = pc ^ (r & 7);  // logical 8-column group of the physical piece
+        const float f = fac(r);
+        float acc = 0.f;
+#pragma unroll
+        for (int b = 0; b < DK / 64; ++b) {
+            uint4* p = reinterpret_cast<uint4*>(tile + b * kBlk) + (r * 8 + pc);
+            uint4 u = *p;
+            const float4 za = *reinterpret_cast<const float4*>(z + b * 64 + lc * 8);
+            const float4 zb = *reinterpret_cast<const float4*>(z + b * 64 + lc * 8 + 4);
+            __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
+            const float2 x0 = __bfloat1622float2(hv[0]), x1 = __bfloat1622float2(hv[1]);
+            const float2 x2 = __bfloat1622float2(hv[2]), x3 = __bfloat1622float2(hv[3]);
+            acc = fmaf(x0.x, za.x, acc); acc = fmaf(x0.y, za.y, acc);
+            acc = fmaf(x1.x, za.z, acc); acc = fmaf(x1.y, za.w, acc);
+            acc = fmaf(x2.x, zb.x, acc); acc = fmaf(x2.y, zb.y, acc);
+            acc = fmaf(x3.x, zb.z, acc); acc = fmaf(x3.y, zb.w, acc);
+            hv[0] = __floats2bfloat162_rn(x0.x * f, x0.y * f);
+            hv[1] = __floats2bfloat162_rn(x1.x * f, x1.y * f);
+            hv[2] = __floats2bfloat162_rn(x2.x * f, x2.y * f);
+            hv[3] = __floats2bfloat162_rn(x3.x * f, x3.y * f);
+            *p = u;
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (pc == 0) out[r] = f * acc;
+    }
+}
+
+// K^ = zeta . K in place over a [128 x DK] K-major swizzled bf16 tile by 128
+// threads (zeta_r = gamma^(L-1-r), rows >= L zeroed), and the fp32 column sums
+// of zeta_r k_r taken from the unscaled values (the normaliser state's update,
+// without the bf16 rounding of zeta_r k_r).  Each 64-column block has its own
+// NT = 128 / (DK / 64) threads; thread t' of a block holds 16-byte piece t' & 7
+// of rows (t' >> 3) + (NT / 8) m, so it always holds the same logical 8-column
+// group lc = (t' & 7) ^ ((t' >> 3) & 7), and the four lanes of a warp with the
+// same group (lanes l, l ^ 9, l ^ 18, l ^ 27) add their sums.  Lanes 0-7 of
+// each warp then store the warp's sums into part ([256/DK][DK] floats, slot =
+// the warp's index within its block: the layout colsum_total() reads); the
+// caller synchronises the 128 threads before reading them.
+template <int DK>
+__device__ __forceinline__ void scale_rows_zsum(char* tile, int L, float l2g, float* part, int t) {
+    constexpr int NT = 128 / (DK / 64);  // threads per block
+    constexpr int NP = 1024 / NT;        // pieces per thread
+    const int b = t / NT, tb = t % NT;
+    const int pc = tb & 7, rg = tb >> 3;
+    uint4* base = reinterpret_cast<uint4*>(tile + b * kBlk) + rg * 8 + pc;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 2
+    for (int m = 0; m < NP; ++m) {
+        const int r = rg + (NT / 8) * m;
+        const float f = r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f;
+        uint4 u = base[m * NT];  // NT / 8 rows of 8 pieces further on
+        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(hv[e]);
+            const float px = x.x * f, py = x.y * f;
+            acc[2 * e] += px;
+            acc[2 * e + 1] += py;
+            hv[e] = __floats2bfloat162_rn(px, py);
+        }
+        base[m * NT] = u;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 9);
+        acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 18);
+    }
+    const int l = t & 31;
+    if (l < 8) {
+        const int lc = l ^ (rg & 7);  // lane l < 8: piece l of row group rg
+        float4* dst = reinterpret_cast<float4*>(part + (tb >> 5) * DK + b * 64 + lc * 8);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`
 // threads (this one is `t`): apply phi (optional) and multiply row r by
 // fac(r).  Rows are whole 128-byte lines, so the swizzle never moves an
@@ -170,11 +262,45 @@ __device__ __forceinline__ void row_pass(char* tile, int nblk, bool apply_phi, F
     }
 }
 
-// Column sums of a [128 x DK] K-major swizzled bf16 tile (sum over its 128 rows)
-// by 128 threads: thread t sums column pair (2 cp, 2 cp + 1), cp = t mod DK/2, over
-// one of 256/DK row groups; a warp reads whole 128-byte rows (conflict-free).
+// Column sums of a [128 x DK] K-major swizzled bf16 tile (over its rows) by 128
+// threads: thread t sums column pair (2 cp, 2 cp + 1), cp = t mod DK/2, over one
+// of 256/DK row groups; a warp reads whole 128-byte rows (conflict-free).
 // Partials go to `part` ([256/DK][DK] floats); the caller synchronises the 128
 // threads and then reads colsum_total().
+// Each row j < L is weighted by zeta_j = gamma^(L-1-j) in fp32 (rows >= L get
+// weight 0), on the tile before it is scaled: sum_j zeta_j k^_j without the
+// bf16 rounding of zeta_j k^_j, which signed features would otherwise turn into
+// a large error of q^ . z after cancellation.  The weights are a running
+// product from the group's last row upwards (zeta grows by 1/gamma per row
+// towards the top, so the product runs downwards in gamma and never overflows).
+template <int DK>
+__device__ __forceinline__ void colsum_partial_decayed(const char* tile, int t, float* part, int L,
+                                                       float l2g, float gam) {
+    constexpr int kPairs = DK / 2;
+    constexpr int kGroups = 128 / kPairs;
+    constexpr int kRows = 128 / kGroups;
+    const int cp = t % kPairs, grp = t / kPairs;
+    const int col = 2 * cp;
+    const char* base = tile + (col >> 6) * kBlk;
+    const int jtop = grp * kRows + kRows - 1;
+    float w = gamma_pow(l2g, (float)max(L - 1 - jtop, 0));
+    float ax = 0.f, ay = 0.f;
+#pragma unroll 8
+    for (int jj = 0; jj < kRows; ++jj) {
+        const int j = jtop - jj;
+        const float2 f = __bfloat1622float2(
+            *reinterpret_cast<const __nv_bfloat162*>(base + sw128_offset(j, col & 63)));
+        const bool in = j < L;
+        const float wj = in ? w : 0.f;
+        ax = fmaf(wj, f.x, ax);
+        ay = fmaf(wj, f.y, ay);
+        w = in ? w * gam : w;
+    }
+    part[grp * DK + col] = ax;
+    part[grp * DK + col + 1] = ay;
+}
+// The same with gamma = 1: plain column sums over all 128 rows (rows past the
+// end of the sequence hold zeros: the copy's fill, or phi's clearing).
 template <int DK>
 __device__ __forceinline__ void colsum_partial(const char* tile, int t, float* part) {
     constexpr int kPairs = DK / 2;

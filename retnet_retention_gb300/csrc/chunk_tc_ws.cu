@@ -27,14 +27,18 @@
 // it.  TMEM (512 columns): two score/P buffers at 0 and 128, O at 256 (two
 // buffers for DVB = 64), S after O.
 //
-// The normaliser runs on the tensor cores.  With z treated as one more value
-// column ("Linear Attention" page, the normalised form; z_c = gamma^L z_{c-1}
-// + sum_j zeta_j k^_j is S's recurrence for an all-ones value column), MMA2
-// and MMA3 are issued with N = DVB + 16: V is followed by a block of ones
-// (so O's column DVB collects sum_j P_ij) and the bf16 copy of S by a block
-// holding z_{c-1} (so it also collects xi_i q^_i . z_{c-1}).  Column DVB of
-// O is then the whole denominator but eps.  z itself stays in fp32 shared
-// memory, updated by column sums of K^.
+// The normaliser: z is one more value column ("Linear Attention" page, the
+// normalised form; z_c = gamma^L z_{c-1} + sum_j zeta_j k^_j is S's recurrence
+// for an all-ones value column).  With signed features the denominator can
+// be a small difference of large sums, so no term of it is rounded to bf16:
+// E1 takes the row sums of the scores in fp32 before P is rounded; for
+// gamma = 1 MMA3 is issued with N = DVB + 16, the bf16 copy of S followed by a
+// block holding z_{c-1} as a bf16 value and its bf16 residual in two columns,
+// so O's columns DVB and DVB + 1 collect q^_i . z_{c-1} to about 16 bits; for
+// gamma < 1 (where Q is scaled by xi in bf16 for MMA3) epilogue B takes
+// xi_i q^_i . z_{c-1} in fp32 from the unscaled tile as it scales it.  z
+// itself stays in fp32 shared memory, updated by decayed column sums of the
+// unscaled K tile.
 //
 // Taken for DVB = 64 with any flags and for DVB = 128 without the
 // normaliser; other cases use the lockstep kernel.
@@ -95,12 +99,19 @@ using namespace tck;
 
 namespace {
 
-// Feature-map group: 8 warps for d_k = d_v-block = 64, else 2.  More warps hide
-// the exp latency of phi; for the wider tiles the registers of the extra warps
-// (the SM's register file is split over its four schedulers) cost more than
-// they give, and those workloads rarely use phi.
-constexpr int threads_c(int dk, int dvb) { return dk == 64 && dvb == 64 ? 256 : 64; }
-constexpr int threads_ws(int dk, int dvb) { return 448 + threads_c(dk, dvb); }
+// Feature-map group: 8 warps for d_k = d_v-block = 64 with phi, else 2.  More
+// warps hide the exp latency of phi; without phi they would only take registers
+// (the SM's register file is split over its four schedulers: 704 threads get 80
+// registers each, 512 get 128), and for the wider tiles the registers of the
+// extra warps cost more than they give.
+constexpr int threads_c(int dk, int dvb, bool phi) { return phi && dk == 64 && dvb == 64 ? 256 : 64; }
+constexpr int threads_ws(int dk, int dvb, bool phi) { return 448 + threads_c(dk, dvb, phi); }
+// The block size the compiler budgets registers for: for 64-wide tiles without
+// phi the cap of a 640-thread block (96 registers) measured faster than the
+// 128 that 512 threads would allow.
+constexpr int bound_ws(int dk, int dvb, bool phi) {
+    return !phi && dk == 64 && dvb == 64 ? 640 : threads_ws(dk, dvb, phi);
+}
 constexpr int kWgA = 2;   // first warp of epilogue A (8 warps: two per TMEM lane quarter)
 constexpr int kWgB = 10;  // first warp of epilogue B
 constexpr int kWgC = 14;  // first warp of the feature-map group
@@ -115,7 +126,8 @@ constexpr uint32_t kColO = 256;
 
 constexpr uint32_t kSmemLimit = 232448;  // opt-in shared memory per CTA
 
-template <int DK, int DVB, bool NORM>
+// POS: the features are phi(.) > 0, so no term of the normaliser is negative.
+template <int DK, int DVB, bool NORM, bool POS>
 struct LayoutWS {
     static constexpr uint32_t kQ = (DK / 64) * kBlk;
     static constexpr uint32_t kK = (DK / 64) * kBlk;
@@ -124,8 +136,13 @@ struct LayoutWS {
     // bf16 S, MN-major, 64-column blocks DK * 128 bytes apart; with the
     // normaliser one more block whose first 16 columns hold z
     static constexpr uint32_t kSB = (DVB / 64 + (NORM ? 1 : 0)) * (DK * 128);
-    static constexpr uint32_t kOnes = NORM ? kBlk : 0;  // [128 x 64] bf16 ones
-    static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + 32 * 8 + 16 + 1024;
+    // positive features: a [128 x 64] block after V whose column 0 is ones (MMA2's
+    // extra columns collect sum_j P_ij); signed features: fp32 row sums from E1 and,
+    // for gamma < 1, xi_i q^_i . z_{c-1} from epilogue B
+    static constexpr uint32_t kOnes = NORM && POS ? kBlk : 0;
+    static constexpr uint32_t kDQ = NORM && !POS ? 2 * 128 * 4 : 0;      // by chunk parity
+    static constexpr uint32_t kRS = NORM && !POS ? 3 * 2 * 128 * 4 : 0;  // 3 chunks x 2 halves
+    static constexpr uint32_t kSmall = DK * 4 + 256 * 4 + kDQ + kRS + 32 * 8 + 16 + 1024;
     // ring depth: as many stages (up to 4) as shared memory holds
     static constexpr int NS = (4 * kStage + kSB + kOnes + kSmall <= kSmemLimit) ? 4
                             : (3 * kStage + kSB + kOnes + kSmall <= kSmemLimit) ? 3 : 2;
@@ -133,7 +150,9 @@ struct LayoutWS {
     static constexpr uint32_t oOnes = oSB + kSB;        // 1024-byte aligned
     static constexpr uint32_t oZ = oOnes + kOnes;       // float z[DK]
     static constexpr uint32_t oZP = oZ + DK * 4;        // float colsum partials [256/DK][DK]
-    static constexpr uint32_t oBar = oZP + 256 * 4;     // 32 mbarrier slots
+    static constexpr uint32_t oDQ = oZP + 256 * 4;      // float [2][128] (normaliser, gamma < 1)
+    static constexpr uint32_t oRS = oDQ + kDQ;          // float [3][2][128] (normaliser)
+    static constexpr uint32_t oBar = oRS + kRS;         // 32 mbarrier slots
     static constexpr uint32_t oFlags = oBar + 32 * 8;   // int abort, uint32 tmem slot
     static constexpr uint32_t kBytes = oFlags + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
@@ -141,11 +160,12 @@ struct LayoutWS {
     // one for DVB = 128; then S.  With the normaliser an O accumulator has
     // DVB + 16 columns (column DVB: the denominator), its slot rounded up to 32.
     static constexpr int NOB = DVB == 64 ? 2 : 1;
-    static constexpr int NO = NORM ? DVB + 16 : DVB;    // MMA2/MMA3 N
+    static constexpr int NO = NORM ? DVB + 16 : DVB;    // MMA2 (positive features) / MMA3 N
     static constexpr uint32_t kOSlot = (NO + 31) / 32 * 32;
     static constexpr uint32_t kColS = kColO + NOB * kOSlot;
     static_assert(kAlloc <= kSmemLimit, "shared memory budget");
     static_assert(kColS + DVB <= 512, "tensor memory budget");
+    static_assert(!NORM || NOB == 2, "the normaliser's hand-overs assume two O buffers");
 };
 
 // Barriers.  Stage barriers (full, empty, qk) have one slot per ring stage;
@@ -158,22 +178,31 @@ struct LayoutWS {
 // MMA3/MMA4 of c are complete.
 enum Bars {
     kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
-    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kSready0, kSready1, kNumBars
+    kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kSready0, kSready1,
+    kRsum0, kNumBars = kRsum0 + 3
 };
+static_assert(kNumBars <= 32, "mbarrier slots");
 
 // STATE_ONLY: the walk of a segment's own state contribution (mode
 // kStateOnly: K and V only, MMA4 only).  Its per-chunk hand-over to the
 // issuer (kReadyS) has one slot per ring stage, which bounds how far the
 // epilogues may run ahead.
-template <int DK, int DVB, bool NORM, bool STATE_ONLY>
-__global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
-    constexpr int kThreadsC = threads_c(DK, DVB);
-    constexpr int kThreadsWS = threads_ws(DK, DVB);
-    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
+//
+// PHI: the launch applies phi (p.phi), which sizes the feature-map group and
+// makes every term of the normaliser non-negative.
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI>
+__global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kThreadsC = threads_c(DK, DVB, PHI);
+    constexpr int kThreadsWS = threads_ws(DK, DVB, PHI);
+    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI>;
+    constexpr bool kOnesSum = NORM && PHI;   // sum_j P_ij through MMA2 and the ones block
+    constexpr bool kE1Sum = NORM && !PHI;    // sum_j P_ij in fp32 from E1
     static_assert(!NORM || DVB == 64, "the normaliser's columns fit tensor memory only for DVB = 64");
     extern __shared__ __align__(1024) char smem_raw[];
     char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* zs = reinterpret_cast<float*>(sm + Lay::oZ);
+    float* dqz = reinterpret_cast<float*>(sm + Lay::oDQ);
+    float* rsb = reinterpret_cast<float*>(sm + Lay::oRS);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::oFlags);
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oFlags + 4);
@@ -222,10 +251,13 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
         tmem_alloc(slot, 512);
         tmem_relinquish();
     }
-    if constexpr (NORM) {  // the block of ones after V (read by MMA2 through the async proxy)
-        const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = tid; i < (int)(kBlk / 16); i += kThreadsWS)
-            reinterpret_cast<uint4*>(sm + Lay::oOnes)[i] = ones;
+    if constexpr (kOnesSum && !STATE_ONLY) {
+        // the block after V for MMA2's extra columns: ones in column 0, zeros elsewhere
+        // (read through the async proxy)
+        for (int i = tid; i < (int)(kBlk / 16); i += kThreadsWS) {
+            const uint32_t one = (i & 7) == ((i >> 3) & 7) ? 0x3F80u : 0u;  // logical piece 0 of row i >> 3
+            reinterpret_cast<uint4*>(sm + Lay::oOnes)[i] = make_uint4(one, 0u, 0u, 0u);
+        }
         fence_proxy_async_smem();
     }
     fence_before_sync();
@@ -357,7 +389,11 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
         } else if (warp == 1 && lane == 0) {
             // ---------------- MMA issuer
             const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
-            const uint32_t id_pv = idesc_bf16(128, Lay::NO, 0, 1);  // MMA2, MMA3
+            // MMA2, with positive features plus the ones block's columns
+            const uint32_t id_pv = idesc_bf16(128, kOnesSum ? Lay::NO : DVB, 0, 1);
+            // MMA3, with the normaliser plus the z columns (for signed features and
+            // gamma < 1 epilogue B takes xi_i q^_i . z_{c-1} in fp32 instead)
+            const uint32_t id_qs = idesc_bf16(128, NORM && (PHI || unit_gamma) ? Lay::NO : DVB, 0, 1);
             const uint32_t id_kv = idesc_bf16(128, DVB, 1, 1);
             // descriptors of stage 0 and of bf16 S; the others are offsets from them
             const uint64_t dQk0 = smem_desc_sw128(sbase, 16, 1024);          // Q, K: K-major
@@ -398,6 +434,7 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                 }
                 (void)issue_mma1;
                 (void)id_pv;
+                (void)id_qs;
             }
             // Per chunk, with two O buffers: MMA4/MMA3 as soon as S is ready (the state
             // chain), then MMA1 of the next chunk, then MMA2 once P is ready.  With one
@@ -419,15 +456,15 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                 const uint32_t ocol = tbase + kColO + ob * Lay::kOSlot;
                 const uint64_t dq = desc_adv(dQk0, s * Lay::kStage);
                 const uint64_t dk = desc_adv(dKmn0, s * Lay::kStage), dv = desc_adv(dk, Lay::kK);
-                // V for MMA2: its 64-column blocks are kBlk apart; with the normaliser the
-                // block of ones stands in for the next one (N = DVB + 16)
+                // V for MMA2: its 64-column blocks are kBlk apart; with positive features
+                // the ones block stands in for the next one (N = DVB + 16)
                 const uint32_t va = sbase + s * Lay::kStage + Lay::kQ + Lay::kK;
-                const uint64_t dv2 = NORM ? smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024) : dv;
+                const uint64_t dv2 = kOnesSum ? smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024) : dv;
                 // MMA3: O = Q^ S_bf16 (K = DK)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
-                    mma_ss(ocol, desc_adv(dq, off), desc_adv(dSB, kk * 2048), id_pv, kk > 0);
+                    mma_ss(ocol, desc_adv(dq, off), desc_adv(dSB, kk * 2048), id_qs, kk > 0);
                 }
                 // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
 #pragma unroll
@@ -539,50 +576,93 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                         if (t == 0) LA_TL(it * 16 + 4);
                         const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
                         const int i = row;
+                        float rsum = 0.f;  // fp32 row sum of this half's scores (normaliser)
                         // this half's two 32-column pieces of scores, one at a time.  P (bf16
                         // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
                         // piece, so half 1 stores only after half 0 has read that piece (kBarP).
+                        // A warp's 32 rows and a piece's 32 columns are the same 32 x 32 block
+                        // for every lane, so a piece above the diagonal is P = 0 for the whole
+                        // warp (no load; not with phi's 8 warps), and only the piece on the
+                        // diagonal needs the mask j <= i.
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
                             const int c0 = 64 * half + 32 * q;
+                            const int pq = c0 >> 5, lq = warp & 3;
+                            // (the skip costs registers the 80-register build does not have)
+                            const bool zero = !PHI && pq > lq;
                             uint32_t r[32];
-                            tmem_ld32(sc + c0, r);
-                            tmem_ld_wait();
+                            if (!zero) {
+                                tmem_ld32(sc + c0, r);
+                                tmem_ld_wait();
+                            }
                             if (half == 0 && q == 1) {
                                 fence_before_sync();
                                 named_bar_arrive(kBarP, kThreadsA);
                             }
                             uint32_t pk[16];
-                            // gamma^(i-j) by a running product from the piece's top column down
-                            const int jt = min(i, c0 + 31);
-                            float w = (unit_gamma || jt < c0) ? 1.f : gamma_pow(l2g, (float)(i - jt));
-                            float a[32];
+                            if (zero) {
 #pragma unroll
-                            for (int e = 31; e >= 0; --e) {
-                                const int j = c0 + e;
-                                float x = 0.f;
-                                if (j <= i) {
-                                    x = __uint_as_float(r[e]);
-                                    if (!unit_gamma) {
-                                        x *= w;
-                                        w *= gam;
+                                for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                            } else {
+                                // gamma^(i-j) by a running product from the piece's top column down
+                                const int jt = min(i, c0 + 31);
+                                float w = unit_gamma ? 1.f : gamma_pow(l2g, (float)(i - jt));
+                                const bool diag = pq == lq;
+                                if constexpr (!PHI) {  // each pair packed as soon as it is scaled
+#pragma unroll
+                                    for (int e = 30; e >= 0; e -= 2) {
+                                        float x1 = __uint_as_float(r[e + 1]), x0 = __uint_as_float(r[e]);
+                                        if (!unit_gamma) {
+                                            x1 *= w;
+                                            if (!diag || c0 + e + 1 <= i) w *= gam;
+                                            x0 *= w;
+                                            if (!diag || c0 + e <= i) w *= gam;
+                                        }
+                                        if (diag) {
+                                            x1 = c0 + e + 1 <= i ? x1 : 0.f;
+                                            x0 = c0 + e <= i ? x0 : 0.f;
+                                        }
+                                        if (kE1Sum) rsum += x1 + x0;
+                                        pk[e >> 1] = pack_bf16x2(x0, x1);
                                     }
-                                }
-                                a[e] = x;
-                            }
+                                } else {  // (the form that fits 80 registers)
+                                    float a[32];
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                                    for (int e = 31; e >= 0; --e) {
+                                        float x = 0.f;
+                                        if (c0 + e <= i) {
+                                            x = __uint_as_float(r[e]);
+                                            if (!unit_gamma) {
+                                                x *= w;
+                                                w *= gam;
+                                            }
+                                        }
+                                        a[e] = x;
+                                    }
+#pragma unroll
+                                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                                }
+                            }
                             if (half == 1 && q == 0) {
                                 named_bar_sync(kBarP, kThreadsA);
                                 fence_after_sync();
                             }
                             tmem_st16(sc + (c0 >> 1), pk);
                         }
+                        // the row sums before rounding P: with signed features the
+                        // denominator can be a small difference of large sums, which the
+                        // bf16 P would not resolve.  To E2 through shared memory, one slot
+                        // per chunk, three slots (E1 of chunk c + 3 waits for MMA1 of c + 3,
+                        // which the issuer starts only after E2 of c has freed c's O buffer)
+                        if (kE1Sum) rsb[(it % 3) * 256 + half * 128 + row] = rsum;
                         tmem_st_wait();
                         if (NOB == 2) {
                             fence_before_sync();
                             named_bar_sync(kBarA, kThreadsA);
-                            if (t == 0) mbar_arrive(&bar[kPready0 + (it & 1)]);
+                            if (t == 0) {
+                                mbar_arrive(&bar[kPready0 + (it & 1)]);
+                                if (kE1Sum) mbar_arrive(&bar[kRsum0 + it % 3]);
+                            }
                         }
                         if (t == 0) LA_TL(it * 16 + 5);
                     }
@@ -645,15 +725,25 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
             // E2 of chunk `it`: O rows -> global, divided by the normaliser
             auto do_e2 = [&](int it, int L) -> bool {
                 bool ok = mbar_wait_or_abort(&bar[kOfull0 + it % NOB], (it / NOB) & 1, lim, abort_flag);
+                if (kE1Sum && ok) ok = mbar_wait_or_abort(&bar[kRsum0 + it % 3], (it / 3) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
                 fence_after_sync();
                 if (t == 0) LA_TL(it * 16 + 10);
                 const uint32_t ocol = tbase + lane_off + kColO + (it % NOB) * Lay::kOSlot;
                 float inv = 1.f;
-                if (NORM) {  // column DVB: sum_j P_ij + xi_i q^_i . z_{c-1}
-                    const float den = __uint_as_float(tmem_ld1(ocol + DVB));
-                    tmem_ld_wait();
-                    inv = 1.f / (den + p.eps);
+                if (NORM) {  // sum_j P_ij + xi_i q^_i . z_{c-1}
+                    // O's columns DVB and DVB + 1: MMA3's z block (z_{c-1} and its residual)
+                    // and, with positive features, MMA2's ones column (sum_j P_ij)
+                    float den = 0.f;
+                    if (PHI || unit_gamma) {
+                        den = __uint_as_float(tmem_ld1(ocol + DVB)) + __uint_as_float(tmem_ld1(ocol + DVB + 1));
+                        tmem_ld_wait();
+                    }
+                    if (kE1Sum) {
+                        den += rsb[(it % 3) * 256 + row] + rsb[(it % 3) * 256 + 128 + row];
+                        if (!unit_gamma) den += dqz[(it & 1) * 128 + row];
+                    }
+                    inv = 1.f / norm_den(den, p.normalize, p.eps);
                 }
                 const int c = cb + it;
                 __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
@@ -691,27 +781,38 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                         stop = true;
                         break;
                     }
+                    // z_c = gamma^L z_{c-1} + sum_j zeta_j phi(K)[j], the sums in fp32 from the
+                    // unscaled tile: with gamma < 1 in the pass that scales K, with gamma = 1
+                    // (no scaling) beside MMA4
+                    float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
                     // K^ = zeta . phi(K), rows >= L zeroed; then MMA4 may go (kReadyS)
-                    if (!unit_gamma)
+                    if (!unit_gamma) {
+                        if (p.track_z) {
+                            scale_rows_zsum<DK>(tK, L, l2g, zpart, t);
+                        } else {
 #pragma unroll 1
-                        for (int b = 0; b < DK / 64; ++b)  // one 64-column block at a time
-                            scale_rows_all<1, 128>(
-                                tK + b * kBlk, [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; },
-                                t);
+                            for (int b = 0; b < DK / 64; ++b)  // one 64-column block at a time
+                                scale_rows_all<1, 128>(
+                                    tK + b * kBlk,
+                                    [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; }, t);
+                        }
+                    }
                     fence_proxy_async_smem();
                     fence_before_sync();
                     named_bar_sync(kBarB, 128);
                     if (t == 0) mbar_arrive(&bar[kReadyS0 + s]);
-                    if (p.track_z) {  // z_c = gamma^L z_{c-1} + sum_j K^[j], beside MMA4
-                        float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
-                        colsum_partial<DK>(tK, t, zpart);
-                        named_bar_sync(kBarB, 128);
+                    if (p.track_z) {
+                        if (unit_gamma) {
+                            colsum_partial<DK>(tK, t, zpart);
+                            named_bar_sync(kBarB, 128);
+                        }
                         if (t < DK) {
                             const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
                             zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
                         }
-                        named_bar_sync(kBarB, 128);  // every read of the stage and of zpart done
                     }
+                    // every read of the stage was before the last barrier (the next chunk's
+                    // partials are written only after its first barrier)
                     if (t == 0) mbar_arrive(&bar[kEmpty0 + s]);
                     if (t == 0) LA_TL(it * 16 + 9);
                 }
@@ -739,48 +840,58 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
                 if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) break;
                 if (t == 0) LA_TL(it * 16 + 8);
-                if (!unit_gamma) {
-                    row_pass(tQ, DK / 64, false, [&](int r) { return gamma_pow(l2g, (float)(r + 1)); }, t, 128);
-                    row_pass(tK, DK / 64, false,
-                             [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; }, t, 128);
+                // z_c = gamma^L z_{c-1} + sum_j zeta_j phi(K)[j], the sums in fp32 from the
+                // unscaled tile: with gamma = 1 while epilogue B would otherwise wait for
+                // MMA3 of the previous chunk, with gamma < 1 in the pass that scales K
+                float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
+                const bool zsum = NORM || p.track_z;
+                if (unit_gamma) {
+                    if (zsum) colsum_partial<DK>(tK, t, zpart);
+                } else {
+                    auto xi = [&](int r) { return gamma_pow(l2g, (float)(r + 1)); };
+                    if (kE1Sum)  // and xi_i q^_i . z_{c-1} from the unscaled tile, for E2
+                        scale_rows_dot<DK>(tQ, xi, zs, dqz + (it & 1) * 128, t);
+                    else
+                        row_pass(tQ, DK / 64, false, xi, t, 128);
+                    if (zsum)
+                        scale_rows_zsum<DK>(tK, L, l2g, zpart, t);
+                    else
+                        row_pass(tK, DK / 64, false,
+                                 [&](int r) { return r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f; }, t, 128);
                     fence_proxy_async_smem();
-                    named_bar_sync(kBarB, 128);
                 }
-                if (NORM || p.track_z) {
-                    // z_c = gamma^L z_{c-1} + sum_j K^[j] (rows >= L of K^ are zero): the
-                    // column sums first, off the state chain
-                    float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
-                    colsum_partial<DK>(tK, t, zpart);
-                    if (NORM) {
-                        // z_{c-1} into the block after bf16 S, once MMA3 of the previous
-                        // chunk has read the old one; MMA3 then adds xi_i q^_i . z_{c-1}
-                        // to O's column DVB
-                        if (it >= 1) {
-                            ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
-                            if (named_bar_or(kBarB, 128, !ok)) break;
-                        }
-                        if (t < DK) {
-                            const __nv_bfloat162 z2 = __float2bfloat162_rn(zs[t]);
-                            const uint32_t zw = *reinterpret_cast<const uint32_t*>(&z2);
-                            const uint4 zv = make_uint4(zw, zw, zw, zw);
-                            char* zb = sm + Lay::oSB + (DVB / 64) * (DK * 128);
-                            *reinterpret_cast<uint4*>(zb + sw128_offset(t, 0)) = zv;
-                            *reinterpret_cast<uint4*>(zb + sw128_offset(t, 8)) = zv;
-                        }
-                        fence_proxy_async_smem();
+                if (NORM && (PHI || unit_gamma)) {
+                    // z_{c-1} into the block after bf16 S, once MMA3 of the previous chunk
+                    // has read the old one; MMA3 then adds xi_i q^_i . z_{c-1} to O's columns
+                    // DVB and DVB + 1
+                    if (it >= 1) {
+                        ok = mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
+                        if (named_bar_or(kBarB, 128, !ok)) break;
                     }
-                    named_bar_sync(kBarB, 128);  // partials written; every read of z_{c-1} done
+                    if (t < DK) {
+                        // z in two bf16 columns, its rounding and the residual, so q^ . z
+                        // keeps about 16 bits even when its terms cancel
+                        const float zf = zs[t];
+                        const __nv_bfloat16 zh = __float2bfloat16_rn(zf);
+                        const __nv_bfloat16 zl = __float2bfloat16_rn(zf - __bfloat162float(zh));
+                        const uint32_t zw = (uint32_t)__bfloat16_as_ushort(zh) |
+                                            ((uint32_t)__bfloat16_as_ushort(zl) << 16);
+                        char* zb = sm + Lay::oSB + (DVB / 64) * (DK * 128);
+                        *reinterpret_cast<uint4*>(zb + sw128_offset(t, 0)) = make_uint4(zw, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(zb + sw128_offset(t, 8)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                fence_before_sync();
+                named_bar_sync(kBarB, 128);  // tiles scaled, z block written, z sums stored
+                if (t == 0) mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
+                if (zsum) {
                     if (t < DK) {
                         const float gL = unit_gamma ? 1.f : gamma_pow(l2g, (float)L);
                         zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
                     }
                 }
-                fence_before_sync();
-                named_bar_sync(kBarB, 128);
-                if (t == 0) {
-                    mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
-                    mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
-                }
+                if (t == 0) mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
                 if (t == 0) LA_TL(it * 16 + 9);
                 if (it >= 1 && !do_e2(it - 1, L_prev)) {
                     stop = true;
@@ -820,17 +931,17 @@ __global__ void __launch_bounds__(threads_ws(DK, DVB), 1) chunk_tc_ws_kernel(con
 // pdl: launch as a programmatic dependent of the previous kernel in the stream
 // (the kernel's entry-state reads wait for that kernel; everything else may
 // start early).
-template <int DK, int DVB, bool NORM, bool STATE_ONLY>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
-    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY>;
-    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY>;
+    using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
     TraceScope trace(STATE_ONLY ? "chunk_tc_ws_kernel/state" : "chunk_tc_ws_kernel/full", s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(threads_ws(DK, DVB));
+    cfg.blockDim = dim3(threads_ws(DK, DVB, PHI));
     cfg.dynamicSmemBytes = Lay::kAlloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -844,11 +955,11 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
         cudaFuncAttributes fa;
         cudaFuncGetAttributes(&fa, kern);
         std::fprintf(stderr,
-                     "launch_ws<%d,%d,%d,%d>: %s; regs %d, local %zu B, max threads %d, "
+                     "launch_ws<%d,%d,%d,%d,%d>: %s; regs %d, local %zu B, max threads %d, "
                      "dynamic smem %u B, static smem %zu B, grid %d x %d\n",
-                     DK, DVB, (int)NORM, (int)STATE_ONLY, cudaGetErrorString(e), fa.numRegs,
+                     DK, DVB, (int)NORM, (int)STATE_ONLY, (int)PHI, cudaGetErrorString(e), fa.numRegs,
                      fa.localSizeBytes, fa.maxThreadsPerBlock, Lay::kAlloc, fa.sharedSizeBytes, grid,
-                     threads_ws(DK, DVB));
+                     threads_ws(DK, DVB, PHI));
     }
 #endif
     return e;
@@ -866,25 +977,36 @@ bool tc_ws_supported(int mode, int dk, int dvb, bool normalize) {
     return dvb == 64 || !normalize;
 }
 
+// Kernels with phi are instantiated apart where phi changes the kernel: the
+// feature-map group of 64-wide tiles, and the normaliser's row sums.
 cudaError_t launch_chunk_tc_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
                                cudaStream_t s, bool pdl) {
     if (grid <= 0) return cudaSuccess;
+    const bool phi = prm.phi != 0;
     if (prm.mode == kStateOnly) {
-        if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, true>(prm, grid, s, pdl);
-        if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, true>(prm, grid, s, pdl);
-        if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true>(prm, grid, s, pdl);
-        if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true>(prm, grid, s, pdl);
+        if (dk == 64 && dvb == 64)
+            return phi ? launch_ws<64, 64, false, true, true>(prm, grid, s, pdl)
+                       : launch_ws<64, 64, false, true, false>(prm, grid, s, pdl);
+        if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, true, false>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true, false>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true, false>(prm, grid, s, pdl);
         return cudaErrorInvalidValue;
     }
     if (normalize) {
-        if (dk == 64 && dvb == 64) return launch_ws<64, 64, true, false>(prm, grid, s, pdl);
-        if (dk == 128 && dvb == 64) return launch_ws<128, 64, true, false>(prm, grid, s, pdl);
+        if (dk == 64 && dvb == 64)
+            return phi ? launch_ws<64, 64, true, false, true>(prm, grid, s, pdl)
+                       : launch_ws<64, 64, true, false, false>(prm, grid, s, pdl);
+        if (dk == 128 && dvb == 64)
+            return phi ? launch_ws<128, 64, true, false, true>(prm, grid, s, pdl)
+                       : launch_ws<128, 64, true, false, false>(prm, grid, s, pdl);
         return cudaErrorInvalidValue;
     }
-    if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false>(prm, grid, s, pdl);
-    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false>(prm, grid, s, pdl);
-    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false>(prm, grid, s, pdl);
-    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, false>(prm, grid, s, pdl);
+    if (dk == 64 && dvb == 64)
+        return phi ? launch_ws<64, 64, false, false, true>(prm, grid, s, pdl)
+                   : launch_ws<64, 64, false, false, false>(prm, grid, s, pdl);
+    if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false, false>(prm, grid, s, pdl);
+    if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false, false>(prm, grid, s, pdl);
+    if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, false, false>(prm, grid, s, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -31,6 +31,12 @@ __device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float x) 
 }
 
 // phi(x) = elu(x) + 1: x + 1 above zero, e^x at or below it.
+// Normaliser denominator from d = phi(q)^T z: mode 1 adds eps, mode 2 floors
+// |d| at 1 (LA_NORM_FLOOR).
+__device__ __forceinline__ float norm_den(float d, int mode, float eps) {
+    return mode == 2 ? fmaxf(fabsf(d), 1.f) : d + eps;
+}
+
 __device__ __forceinline__ float phi_elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
 // gamma^n for n >= 0 from the host-rounded log2(gamma).

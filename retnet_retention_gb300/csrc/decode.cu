@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
         float d = 0.f;
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) d += den_part[w];
-        den = d + eps;
+        den = norm_den(d, normalize, eps);
     }
     for (int j = tid; j < dv; j += kThreads) {
         float sum = 0.f;
@@ -134,11 +134,11 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
     if (a.bf16) {
         decode_step_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
             (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-            (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, a.normalize, a.eps, g);
+            (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, g);
     } else {
         decode_step_kernel<float><<<grid, kThreads, 0, s>>>(
             (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.o, a.S, a.z,
-            a.H, a.dk, a.dv, a.phi, a.normalize, a.eps, g);
+            a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, g);
     }
     return cudaGetLastError();
 }

@@ -24,6 +24,7 @@ struct ChunkArgs {
     bool bf16;
     bool phi;
     bool normalize;
+    bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     bool noncausal;
     float eps;
     void* workspace;
@@ -42,8 +43,13 @@ struct StepArgs {
     bool bf16;
     bool phi;
     bool normalize;
+    bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     float eps;
 };
+
+// Normaliser mode passed to the kernels: 0 none, 1 divide by phi(q)^T z + eps,
+// 2 divide by max(|phi(q)^T z|, 1).
+inline int norm_mode(bool normalize, bool floor_norm) { return normalize ? (floor_norm ? 2 : 1) : 0; }
 
 // state.cu
 cudaError_t launch_state_zero(float* S, float* z, size_t n_S, size_t n_z, cudaStream_t s);

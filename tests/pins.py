@@ -10,6 +10,10 @@ token-by-token recurrence:
   parallel forms agree" of the "Linear attention" page (zerotofrontier 21.2):
   O = diag(W 1)^-1 W V with W = (phi(Q) phi(K)^T) . L; for gamma < 1 the mask
   L is replaced by D (the reading that z decays with gamma).
+  With ``floor`` each row of W is divided by max(|row sum|, 1) instead: RetNet's
+  row normalisation of its scores ("Its normalizer is unstable" on the "Linear
+  attention" page: each row divided by the absolute value of its sum, clamped
+  below at 1).
 * ``noncausal_left`` / ``noncausal_right``: the two multiplication orders of
   "Moving the parentheses" on the "Linear attention" page.
 * ``chunkwise``: the chunkwise form that the pages describe only in words
@@ -43,7 +47,7 @@ def decay_mask(T: int, gamma: float) -> np.ndarray:
     return np.where(diff >= 0, np.power(float(gamma), np.maximum(diff, 0)), 0.0)
 
 
-def parallel_form(q, k, v, gamma, phi=False, normalize=False, eps=1e-6):
+def parallel_form(q, k, v, gamma, phi=False, normalize=False, eps=1e-6, floor=False):
     """Masked quadratic form for [B,H,T,d] inputs; returns O [B,H,T,dv]."""
     q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
     B, H, T, _ = q.shape
@@ -52,8 +56,10 @@ def parallel_form(q, k, v, gamma, phi=False, normalize=False, eps=1e-6):
     for b in range(B):
         for h in range(H):
             W = (_phi(q[b, h], phi) @ _phi(k[b, h], phi).T) * decay_mask(T, g[h])
+            if floor:  # each score row scaled by 1 / max(|its sum|, 1), then times V
+                W = W / np.maximum(np.abs(W.sum(axis=1, keepdims=True)), 1.0)
             O = W @ v[b, h]
-            if normalize:
+            if normalize and not floor:
                 O = O / (W.sum(axis=1, keepdims=True) + eps)
             out[b, h] = O
     return out

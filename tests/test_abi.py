@@ -64,7 +64,7 @@ def chunk(lib, **over):
 
 BAD_CHUNK_ARGS = [
     dict(B=-1), dict(H=-2), dict(T=-1), dict(dk=0), dict(dk=8), dict(dk=24), dict(dk=272),
-    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=8), dict(chunk=48), dict(chunk=256),
+    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=16), dict(chunk=48), dict(chunk=256),
     dict(eps=float("nan")), dict(eps=-1.0), dict(Q=None), dict(V=None), dict(O=None),
     dict(Q=FAKE + 8), dict(O=FAKE + 0x400004), dict(S0=FAKE + 0x800004),
     dict(O=FAKE + 0x100000),  # O overlaps K
@@ -114,7 +114,7 @@ def step(lib, **over):
 
 
 @pytest.mark.parametrize("over", [dict(B=-1), dict(dk=20), dict(dv=512), dict(S=None),
-                                  dict(o=None), dict(flags=la.LA_NORMALIZE),  # z missing
+                                  dict(o=None), dict(flags=la.LA_NORMALIZE), dict(flags=la.LA_NORM_FLOOR),  # z missing
                                   dict(q=FAKE + 2), dict(S=FAKE + 0x100008), dict(dtype=5),
                                   dict(o=FAKE + 0x100000)],  # o overlaps S
                          ids=lambda d: ",".join(d))

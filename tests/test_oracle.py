@@ -13,6 +13,9 @@ Which pin covers which part of the oracle:
   non-causal form                            -> left/right multiplication orders
   final state                                -> associative-memory example, orthonormal keys
   normalised outputs                         -> constant V, o_1 = v_1, convex hull
+  floored normaliser                         -> RetNet's clamped row sums (parallel form);
+                                                plain normaliser / unnormalised read-out
+                                                where the floor is inactive / active
   chunkwise equations (the CUDA path's form) -> chunk-size invariance
   state hand-off (decode, resume)            -> split prefill / decode == one pass
 """
@@ -225,10 +228,53 @@ def pin_state_handoff(lib=None):
     assert pins.rel_err(S2, S) < 1e-13 and pins.rel_err(z2, z) < 1e-13
 
 
+def pin_floor_clamped_rows(lib=None):
+    """Floored normaliser = RetNet's parallel form with each score row divided by
+    max(|row sum|, 1); identity features of both signs, so rows with sums below
+    -1, between -1 and 1, and above 1 all occur."""
+    rng = _rng(31)
+    B, H, T, dk, dv = 2, 3, 24, 6, 5
+    q = rng.standard_normal((B, H, T, dk)) * 0.8
+    k = rng.standard_normal((B, H, T, dk)) * 0.8
+    v = rng.standard_normal((B, H, T, dv))
+    gamma = np.array([0.9, 0.99, 1.0])
+    O, _, _ = oracle.recurrent(q, k, v, gamma, floor=True, _lib=lib)
+    ref = pins.parallel_form(q, k, v, gamma, floor=True)
+    np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+    sums = np.concatenate([((q[b, h] @ k[b, h].T) * pins.decay_mask(T, gamma[h])).sum(axis=1)
+                           for b in range(B) for h in range(H)])
+    assert (sums < -1).any() and (np.abs(sums) < 1).any() and (sums > 1).any()
+    # the non-causal form, floored, against the left multiplication order
+    On, _, _ = oracle.noncausal(q, k, v, floor=True, _lib=lib)
+    A = np.einsum("bhtd,bhsd->bhts", q, k)
+    A = A / np.maximum(np.abs(A.sum(axis=-1, keepdims=True)), 1.0)
+    np.testing.assert_allclose(On, A @ v, rtol=1e-10, atol=1e-12)
+
+
+def pin_floor_limits(lib=None):
+    """Where every |q~^T z| >= 1 the floor changes nothing (the plain normaliser at
+    eps = 0); where every |q~^T z| < 1 it leaves the read-out undivided."""
+    rng = _rng(32)
+    B, H, T, dk, dv = 1, 2, 20, 4, 3
+    v = rng.standard_normal((B, H, T, dv))
+    q = np.abs(rng.standard_normal((B, H, T, dk))) + 1.0   # elu+1 features >= 2
+    k = np.abs(rng.standard_normal((B, H, T, dk))) + 1.0
+    Of, Sf, zf = oracle.recurrent(q, k, v, 0.95, phi=True, floor=True, _lib=lib)
+    On, Sn, zn = oracle.recurrent(q, k, v, 0.95, phi=True, normalize=True, eps=0.0, _lib=lib)
+    np.testing.assert_allclose(Of, On, rtol=1e-13, atol=0)
+    np.testing.assert_array_equal(Sf, Sn)
+    qs = rng.standard_normal((B, H, T, dk)) * 0.05          # tiny scores: |q^T z| < 1
+    ks = rng.standard_normal((B, H, T, dk)) * 0.05
+    Of, _, _ = oracle.recurrent(qs, ks, v, 0.95, floor=True, _lib=lib)
+    Ou, _, _ = oracle.recurrent(qs, ks, v, 0.95, _lib=lib)
+    np.testing.assert_allclose(Of, Ou, rtol=1e-13, atol=0)
+
+
 ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
             pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
             pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
-            pin_chunkwise_invariance, pin_state_handoff]
+            pin_chunkwise_invariance, pin_state_handoff, pin_floor_clamped_rows,
+            pin_floor_limits]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -306,6 +352,7 @@ MUTANTS = {
     5: "outer product transposed",
     6: "elu without +1",
     7: "normaliser over the wrong axis",
+    8: "floor without the absolute value",
 }
 
 
