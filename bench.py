@@ -47,8 +47,8 @@ KERNEL_SOURCES = ("chunk_tc_ws.cu", "chunk_tc_common.cuh", "tc_ptx.cuh", "chunk_
                   "common.cuh", "launch.h")
 TRAFFIC = {
     "chunk_tc_ws_kernel/full": {
-        "bytes": 52_007_168 + 295_680,
-        "sources_sha256": "f9034b0b31444c09eb6f7a5dfa5bbe478f389a106a794dbb063937a3a0481750",
+        "bytes": 52_005_888 + 293_888,
+        "sources_sha256": "74384df59a64b008c1c2d7aee8f3437e857e174ad78e8b9f832ccaa76d223e63",
     },
 }
 HEADLINE = "linear_attention_bf16"
@@ -90,7 +90,8 @@ def decode_flops(c: dict) -> int:
 def describe(name: str, c: dict) -> str:
     bits = [f"{name}: B={c['B']} H={c['H']} T={c['T']} d_k={c['dk']} d_v={c['dv']}",
             c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity",
-            "normalised" if c["normalize"] else "no normaliser"]
+            ("floored normaliser" if c.get("floor") else "normalised") if c["normalize"]
+            else "no normaliser"]
     return ", ".join(bits)
 
 
@@ -251,14 +252,16 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
 
     def step(i):
         qd, kd, vd, O, S, z = sets[i % n_sets]
-        la.chunk_fwd(qd, kd, vd, gamma, phi=c["phi"], normalize=c["normalize"], out=O,
-                     S_out=S, z_out=z, workspace=ws, stream=stream)
+        la.chunk_fwd(qd, kd, vd, gamma, phi=c["phi"], normalize=c["normalize"],
+                     floor=c.get("floor", False), out=O, S_out=S, z_out=z, workspace=ws,
+                     stream=stream)
 
     for i in range(warmup):
         step(i)
     ms = time_region(step, steps, stream)
     kernels = kernel_breakdown(la, step, steps, stream)
-    flags = (la.LA_PHI_ELU1 if c["phi"] else 0) | (la.LA_NORMALIZE if c["normalize"] else 0)
+    flags = ((la.LA_PHI_ELU1 if c["phi"] else 0) | (la.LA_NORMALIZE if c["normalize"] else 0)
+             | (la.LA_NORM_FLOOR if c.get("floor") else 0))
     launches = la.library().la_chunk_fwd_launches(B, c["H"], c["T"], c["dk"], c["dv"],
                                                   1 if c["dtype"] == "bf16" else 0, flags, 0)
     res = dict(name=name, config=c, ms=ms / steps, tokens=B * c["T"], n_sets=n_sets,
@@ -392,7 +395,7 @@ def run_ours(args) -> dict | None:
             print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
                               "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
         return None
-    if only in ("msr_retention_bf16", "long_retention_bf16"):  # profiling aid
+    if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16"):  # profiling aid
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
         if rank == 0:
             print(json.dumps({"only": only, "ms_per_step": r["ms"],
@@ -408,7 +411,7 @@ def run_ours(args) -> dict | None:
     others = {}
     headline_only = args.headline_only or only == "headline"
     if not headline_only:
-        for name in ("msr_retention_bf16", "long_retention_bf16"):
+        for name in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16"):
             r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             others[name] = r
@@ -552,7 +555,7 @@ def main(argv=None):
                     help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
-                                       "decode"), default=None,
+                                       "retention_floor_bf16", "decode"), default=None,
                     help="profiling aid: run one workload only")
     ap.add_argument("--decode-steps", type=int,
                     default=workloads.CONFIGS["decode_bf16"]["decode_steps"],

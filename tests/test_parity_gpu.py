@@ -233,6 +233,21 @@ def test_linear_attention_bf16_full():
     check("z_T", z, zr, TOL["bf16"])
 
 
+def test_retention_floor_bf16_full():
+    """The bench's floored-normaliser workload in the launch configuration the
+    bench times (identity features, decays per head, every sequence)."""
+    c = workloads.CONFIGS["retention_floor_bf16"]
+    x = workloads.make_inputs(c)
+    O, S, z = la.chunk_fwd(to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), x["gamma"],
+                           phi=False, normalize=True, floor=True,
+                           z_out=torch.empty(c["B"], c["H"], c["dk"], device=DEV))
+    torch.cuda.synchronize()
+    Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], floor=True)
+    check("O", np64(O), Or, TOL["bf16"])
+    check("S_T", np64(S), Sr, TOL["bf16"])
+    check("z_T", np64(z), zr, TOL["bf16"])
+
+
 def _sampled_workload(name, n_pairs, causal=True):
     c = workloads.CONFIGS[name]
     x = workloads.make_inputs(c)

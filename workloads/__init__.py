@@ -29,7 +29,9 @@ Q_ID, K_ID, V_ID = 0, 1, 2
 DQ_ID, DK_ID, DV_ID = 3, 4, 5
 GAMMA_ID = 99
 
-#: The five workloads.  ``scale_q/k/v`` multiply the N(0,1) draws.
+#: The five workloads, then retention with the floored normaliser (xLSTM's
+#: max(|q.z|, 1), RetNet's clamped row sums: signed features, decays per head).
+#: ``scale_q/k/v`` multiply the N(0,1) draws.
 CONFIGS = {
     "tiny_retention_fp32": dict(
         index=0, B=1, H=2, T=256, dk=32, dv=32, dtype="f32", phi=False, normalize=False,
@@ -50,6 +52,10 @@ CONFIGS = {
         index=4, B=256, H=32, T=512, dk=128, dv=128, dtype="bf16", phi=False, normalize=False,
         causal=True, gamma=("msr", 8), scale_q=1.0, scale_k=1.0, scale_v=1.0, seed=4,
         decode_steps=1024),
+    "retention_floor_bf16": dict(
+        index=5, B=4, H=8, T=4096, dk=64, dv=64, dtype="bf16", phi=False, normalize=True,
+        floor=True, causal=True, gamma=("msr", 8), scale_q=64 ** -0.5, scale_k=64 ** -0.5,
+        scale_v=1.0, seed=5),
 }
 
 _THREADS = max(1, min(16, (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
