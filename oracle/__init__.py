@@ -17,6 +17,12 @@ recurrent(q, k, v, gamma, phi, normalize, eps, S0, z0)
     o = phi(q)^T S [/ (phi(q)^T z + eps)], update before read.  Sources:
     "Linear attention" (zerotofrontier 21.2) box "Causal linear attention,
     recurrent form"; "RetNet" (bembew) section "Recurrent Representation".
+recurrent_gated(q, k, v, log_a, phi, normalize, eps, S0, z0)
+    The same recurrence with a per-token decay a_t = exp(log_a[b, h, t]) in
+    place of gamma: the generic "decay the old state, add, read out" loop of
+    "Linear Attention, RWKV, and RetNet" (temporalbook 13.3, subsection 4)
+    with the gate G_t = a_t 1 that depends on the token ("Efficient and Sparse
+    Transformers", temporalbook 12.5, "Gated Linear Attention").
 decode_step(q, k, v, gamma, S, z, phi, normalize, eps)
     One token of the same recurrence: the interview box "Causal linear
     attention, recurrent and parallel, plus the decode step" on the "Linear
@@ -54,6 +60,8 @@ def _load(path: str | None = None):
     lib.oracle_recurrent.argtypes = [dp, dp, dp, dp, L, L, L, L, L, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, dp]
     lib.oracle_recurrent.restype = ctypes.c_int
+    lib.oracle_recurrent_gated.argtypes = lib.oracle_recurrent.argtypes
+    lib.oracle_recurrent_gated.restype = ctypes.c_int
     lib.oracle_noncausal.argtypes = [dp, dp, dp, L, L, L, L, L, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_double, dp, dp, dp]
     lib.oracle_noncausal.restype = ctypes.c_int
@@ -124,6 +132,32 @@ def recurrent(q, k, v, gamma, phi: bool = False, normalize: bool = False,
         _norm_mode(normalize, floor), float(eps), _ptr(S0a), _ptr(z0a), _ptr(O), _ptr(S), _ptr(z))
     if rc != 0:
         raise MemoryError("oracle_recurrent: scratch allocation failed")
+    return O, S, z
+
+
+def recurrent_gated(q, k, v, log_a, phi: bool = False, normalize: bool = False,
+                    eps: float = 1e-6, S0=None, z0=None, _lib=None, floor: bool = False):
+    """Causal recurrent form with a per-token decay, in fp64.
+
+    log_a: [B,H,T] natural log of a_t (the decay applied to the state before
+    token t is added); the other arguments and the results as ``recurrent``.
+    """
+    Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
+    B, H, T, dk = Q.shape
+    dv = V.shape[-1]
+    if K.shape != Q.shape or V.shape[:3] != Q.shape[:3]:
+        raise ValueError(f"shape mismatch q{Q.shape} k{K.shape} v{V.shape}")
+    la = np.ascontiguousarray(_f64(log_a).reshape(B, H, T))
+    S0a = None if S0 is None else np.ascontiguousarray(_f64(S0).reshape(B, H, dk, dv))
+    z0a = None if z0 is None else np.ascontiguousarray(_f64(z0).reshape(B, H, dk))
+    O = np.empty((B, H, T, dv))
+    S = np.empty((B, H, dk, dv))
+    z = np.empty((B, H, dk))
+    rc = (_lib or lib()).oracle_recurrent_gated(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(la), B, H, T, dk, dv, int(bool(phi)),
+        _norm_mode(normalize, floor), float(eps), _ptr(S0a), _ptr(z0a), _ptr(O), _ptr(S), _ptr(z))
+    if rc != 0:
+        raise MemoryError("oracle_recurrent_gated: scratch allocation failed")
     return O, S, z
 
 

@@ -39,8 +39,17 @@
  *    C_t q_t by max(|n_t^T q_t|, 1), n_t the normaliser decayed with the state's
  *    gate; RetNet divides each row of its scores by the absolute value of the
  *    row's sum, clamped below at 1 (the same number: that row sum is q^T z).
+ *  - Per-token decay (oracle_recurrent_gated): "Linear Attention, RWKV, and
+ *    RetNet" (temporalbook section 13.3), subsection 4 "The Unifying Picture":
+ *    decay the old state by G_t, add k_t^T v_t, read out; in the selective
+ *    (input-dependent) case G_t depends on the token.  "Efficient and Sparse
+ *    Transformers" (temporalbook section 12.5), "Gated Linear Attention:
+ *    Toward Input-Dependent Forgetting": RetNet is G_t = gamma 1.  Here G_t is
+ *    a_t 1, one scalar per head and token, given as log a_t.
  *
  * Readings where the pages are silent:
+ *  - a per-token gate a_t multiplies the state of the step before (S_{t-1}) at
+ *    step t, like gamma, and decays z the same way;
  *  - with gamma < 1 and the normaliser on, z decays with the same gamma as S
  *    (the pages never combine the two; the xLSTM box on the "Linear
  *    attention" page decays its normaliser with the same gate as its state);
@@ -76,16 +85,18 @@ static void feature(const double* x, double* out, long n, int phi)
 /*
  * Causal recurrent form over a batch of independent (b, h) sequences.
  *
- *   Q, K : [B][H][T][dk]     V : [B][H][T][dv]     gamma : [H]
+ *   Q, K : [B][H][T][dk]     V : [B][H][T][dv]
+ *   gamma : [H] (per-head decay), or log_a : [B][H][T] (log of a per-token
+ *           decay a_t; exactly one of the two is given)
  *   S0   : [B][H][dk][dv] or NULL (zero state)     z0 : [B][H][dk] or NULL
  *   O    : [B][H][T][dv]     S_out : [B][H][dk][dv] or NULL   z_out : [B][H][dk] or NULL
  *   normalize: 0 none, 1 divide by q~^T z + eps, 2 divide by max(|q~^T z|, 1)
  *
  * Returns 0, or -1 when a scratch allocation fails.
  */
-int oracle_recurrent(const double* Q, const double* K, const double* V,
-                     const double* gamma, long B, long H, long T, long dk, long dv,
-                     int phi, int normalize, double eps,
+static int recurrent(const double* Q, const double* K, const double* V,
+                     const double* gamma, const double* log_a, long B, long H, long T,
+                     long dk, long dv, int phi, int normalize, double eps,
                      const double* S0, const double* z0,
                      double* O, double* S_out, double* z_out)
 {
@@ -94,7 +105,6 @@ int oracle_recurrent(const double* Q, const double* K, const double* V,
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
     for (long bh = 0; bh < BH; ++bh) {
         const long h = bh % H;
-        const double g = gamma[h];
         double* S = (double*)malloc(sizeof(double) * (size_t)(dk * dv));
         double* z = (double*)malloc(sizeof(double) * (size_t)dk);
         double* qf = (double*)malloc(sizeof(double) * (size_t)dk);
@@ -114,6 +124,11 @@ int oracle_recurrent(const double* Q, const double* K, const double* V,
             const double* k = K + (bh * T + t) * dk;
             const double* v = V + (bh * T + t) * dv;
             double* o = O + (bh * T + t) * dv;
+#if ORACLE_MUTANT == 9 /* mutant: a per-token gate applied one token late */
+            const double g = log_a ? (t > 0 ? exp(log_a[bh * T + t - 1]) : 1.0) : gamma[h];
+#else
+            const double g = log_a ? exp(log_a[bh * T + t]) : gamma[h];
+#endif
             feature(q, qf, dk, phi);
             feature(k, kf, dk, phi);
 #if ORACLE_MUTANT == 1 /* mutant: read before write (token left out of its own sum) */
@@ -174,6 +189,27 @@ int oracle_recurrent(const double* Q, const double* K, const double* V,
         free(S); free(z); free(qf); free(kf);
     }
     return failed ? -1 : 0;
+}
+
+int oracle_recurrent(const double* Q, const double* K, const double* V,
+                     const double* gamma, long B, long H, long T, long dk, long dv,
+                     int phi, int normalize, double eps,
+                     const double* S0, const double* z0,
+                     double* O, double* S_out, double* z_out)
+{
+    return recurrent(Q, K, V, gamma, NULL, B, H, T, dk, dv, phi, normalize, eps, S0, z0, O,
+                     S_out, z_out);
+}
+
+/* The same with a per-token decay: a_t = exp(log_a[b][h][t]) in place of gamma. */
+int oracle_recurrent_gated(const double* Q, const double* K, const double* V,
+                           const double* log_a, long B, long H, long T, long dk, long dv,
+                           int phi, int normalize, double eps,
+                           const double* S0, const double* z0,
+                           double* O, double* S_out, double* z_out)
+{
+    return recurrent(Q, K, V, NULL, log_a, B, H, T, dk, dv, phi, normalize, eps, S0, z0, O,
+                     S_out, z_out);
 }
 
 /*

@@ -23,6 +23,15 @@ token-by-token recurrence:
       O_c = ((phi(Q_c) phi(K_c)^T) . D) V_c + (phi(Q_c) . xi) S_{c-1}
       S_c = gamma^L S_{c-1} + (phi(K_c) . zeta)^T V_c
   with xi_i = gamma^(i+1), zeta_j = gamma^(L-1-j), L the chunk's length.
+* ``parallel_form_gated``: the same masked quadratic form with a per-token
+  decay a_t (the gate G_t = a_t 1 of "Gated Linear Attention" in section 12.5
+  and of the generic loop of section 13.3 subsection 4): D[n, m] is the
+  product a_{m+1} ... a_n, formed by explicit products, and the initial state
+  enters as (a_0 ... a_n) q_n S_0.
+* ``chunkwise_gated``: the chunkwise form with that decay, from cumulative
+  log-decays b_i = log a_0 + ... + log a_i inside the chunk:
+  D_ij = e^(b_i - b_j), xi_i = e^(b_i), zeta_j = e^(b_(L-1) - b_j), and the
+  chunk's decay e^(b_(L-1)) in place of gamma^L.
 """
 from __future__ import annotations
 
@@ -63,6 +72,82 @@ def parallel_form(q, k, v, gamma, phi=False, normalize=False, eps=1e-6, floor=Fa
                 O = O / (W.sum(axis=1, keepdims=True) + eps)
             out[b, h] = O
     return out
+
+
+def gated_mask(a) -> np.ndarray:
+    """D[n, m] = a[m+1] * ... * a[n] for n >= m (1 on the diagonal), 0 above it."""
+    a = np.asarray(a, dtype=np.float64)
+    T = a.shape[0]
+    D = np.zeros((T, T))
+    for n in range(T):
+        p = 1.0
+        D[n, n] = 1.0
+        for m in range(n - 1, -1, -1):
+            p *= a[m + 1]
+            D[n, m] = p
+    return D
+
+
+def parallel_form_gated(q, k, v, log_a, phi=False, normalize=False, eps=1e-6, floor=False,
+                        S0=None, z0=None):
+    """Masked quadratic form with per-token decays a = exp(log_a) ([B,H,T]) and an
+    optional initial state; returns O [B,H,T,dv]."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    a = np.exp(np.asarray(log_a, dtype=np.float64))
+    out = np.empty((B, H, T, dv))
+    for b in range(B):
+        for h in range(H):
+            fq, fk = _phi(q[b, h], phi), _phi(k[b, h], phi)
+            W = (fq @ fk.T) * gated_mask(a[b, h])
+            head = np.cumprod(a[b, h])  # a_0 ... a_n: the initial state's decay at n
+            num = W @ v[b, h]
+            den = W.sum(axis=1)
+            if S0 is not None:
+                num = num + head[:, None] * (fq @ np.asarray(S0, dtype=np.float64)[b, h])
+            if z0 is not None:
+                den = den + head * (fq @ np.asarray(z0, dtype=np.float64)[b, h])
+            if floor:
+                num = num / np.maximum(np.abs(den), 1.0)[:, None]
+            elif normalize:
+                num = num / (den[:, None] + eps)
+            out[b, h] = num
+    return out
+
+
+def chunkwise_gated(q, k, v, log_a, C, phi=False, normalize=False, eps=1e-6, S0=None, z0=None):
+    """Chunkwise form with per-token decays (module docstring); returns (O, S_T, z_T)."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    la = np.asarray(log_a, dtype=np.float64)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    O = np.zeros((B, H, T, dv))
+    S_all = np.zeros((B, H, dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    z_all = np.zeros((B, H, dk)) if z0 is None else np.array(z0, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            S, z = S_all[b, h].copy(), z_all[b, h].copy()
+            for c0 in range(0, T, C):
+                L = min(C, T - c0)
+                Qc = _phi(q[b, h, c0:c0 + L], phi)
+                Kc = _phi(k[b, h, c0:c0 + L], phi)
+                Vc = v[b, h, c0:c0 + L]
+                cb = np.cumsum(la[b, h, c0:c0 + L])
+                diff = cb[:, None] - cb[None, :]
+                D = np.where(np.tril(np.ones((L, L))) > 0, np.exp(np.minimum(diff, 0.0)), 0.0)
+                xi = np.exp(cb)[:, None]
+                zeta = np.exp(cb[-1] - cb)[:, None]
+                A = (Qc @ Kc.T) * D
+                num = A @ Vc + (Qc * xi) @ S
+                if normalize:
+                    den = A.sum(axis=1) + (Qc * xi) @ z
+                    num = num / (den[:, None] + eps)
+                O[b, h, c0:c0 + L] = num
+                S = np.exp(cb[-1]) * S + (Kc * zeta).T @ Vc
+                z = np.exp(cb[-1]) * z + (Kc * zeta).sum(axis=0)
+            S_all[b, h], z_all[b, h] = S, z
+    return O, S_all, z_all
 
 
 def noncausal_left(q, k, v, phi=False, normalize=False, eps=1e-6):

@@ -18,6 +18,9 @@ Which pin covers which part of the oracle:
                                                 where the floor is inactive / active
   chunkwise equations (the CUDA path's form) -> chunk-size invariance
   state hand-off (decode, resume)            -> split prefill / decode == one pass
+  per-token decay                            -> masked form with explicit gate products,
+                                                constant gate == gamma, a_t = 0 resets,
+                                                chunkwise equations with cumulative logs
 """
 import json
 import os
@@ -270,11 +273,78 @@ def pin_floor_limits(lib=None):
     np.testing.assert_allclose(Of, Ou, rtol=1e-13, atol=0)
 
 
+def _gated_case(seed, B, H, T, dk, dv):
+    rng = _rng(seed)
+    q = rng.standard_normal((B, H, T, dk)) * 0.7
+    k = rng.standard_normal((B, H, T, dk)) * 0.7
+    v = rng.standard_normal((B, H, T, dv))
+    log_a = -rng.exponential(0.3, (B, H, T))   # a_t in (0, 1], about 0.74 on average
+    S0 = rng.standard_normal((B, H, dk, dv))
+    z0 = np.abs(rng.standard_normal((B, H, dk)))
+    return q, k, v, log_a, S0, z0
+
+
+def pin_gated_parallel_form(lib=None):
+    """Per-token decay = the masked form with D[n, m] = a_{m+1} ... a_n and the
+    initial state decayed by a_0 ... a_n (explicit products), for plain, phi +
+    normaliser and floored read-outs, d_k != d_v."""
+    q, k, v, log_a, S0, z0 = _gated_case(41, 2, 3, 19, 5, 4)
+    for phi, norm, floor in ((False, False, False), (True, True, False), (False, False, True)):
+        O, _, _ = oracle.recurrent_gated(q, k, v, log_a, phi=phi, normalize=norm, floor=floor,
+                                         S0=S0, z0=z0, _lib=lib)
+        ref = pins.parallel_form_gated(q, k, v, log_a, phi=phi, normalize=norm, floor=floor,
+                                       S0=S0, z0=z0)
+        np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_gated_constant_is_gamma(lib=None):
+    """A per-token decay that is the same for every token of a head is gamma."""
+    q, k, v, _, S0, z0 = _gated_case(42, 2, 3, 40, 6, 6)
+    gamma = np.array([0.9, 0.99, 1.0])
+    log_a = np.broadcast_to(np.log(gamma)[None, :, None], (2, 3, 40))
+    Og, Sg, zg = oracle.recurrent_gated(q, k, v, log_a, phi=True, normalize=True, S0=S0, z0=z0,
+                                        _lib=lib)
+    O, S, z = oracle.recurrent(q, k, v, gamma, phi=True, normalize=True, S0=S0, z0=z0, _lib=lib)
+    for got, want in ((Og, O), (Sg, S), (zg, z)):
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def pin_gated_reset(lib=None):
+    """a_t = 0 (log a_t = -1000) forgets everything before t: the rest of the
+    sequence equals a fresh start at t from the zero state."""
+    q, k, v, log_a, S0, z0 = _gated_case(43, 1, 2, 30, 4, 3)
+    t0 = 13
+    log_a = log_a.copy()
+    log_a[:, :, t0] = -1000.0
+    O, S, z = oracle.recurrent_gated(q, k, v, log_a, phi=True, normalize=True, S0=S0, z0=z0,
+                                     _lib=lib)
+    tail = log_a[:, :, t0:].copy()
+    tail[:, :, 0] = 0.0
+    Ot, St, zt = oracle.recurrent_gated(q[:, :, t0:], k[:, :, t0:], v[:, :, t0:], tail,
+                                        phi=True, normalize=True, _lib=lib)
+    np.testing.assert_allclose(O[:, :, t0:], Ot, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S, St, rtol=1e-12, atol=1e-14)
+
+
+def pin_gated_chunkwise(lib=None):
+    """The chunkwise equations with cumulative log-decays equal the recurrence
+    at every chunk length, ragged tails included."""
+    q, k, v, log_a, S0, z0 = _gated_case(44, 1, 2, 45, 5, 3)
+    O, S, z = oracle.recurrent_gated(q, k, v, log_a, phi=True, normalize=True, S0=S0, z0=z0,
+                                     _lib=lib)
+    for C in (1, 4, 16, 45, 64):
+        Oc, Sc, zc = pins.chunkwise_gated(q, k, v, log_a, C, phi=True, normalize=True, S0=S0,
+                                          z0=z0)
+        assert pins.rel_err(Oc, O) < 1e-12 and pins.rel_err(Sc, S) < 1e-12
+        assert pins.rel_err(zc, z) < 1e-12
+
+
 ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
             pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
             pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
             pin_chunkwise_invariance, pin_state_handoff, pin_floor_clamped_rows,
-            pin_floor_limits]
+            pin_floor_limits, pin_gated_parallel_form, pin_gated_constant_is_gamma,
+            pin_gated_reset, pin_gated_chunkwise]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -353,6 +423,7 @@ MUTANTS = {
     6: "elu without +1",
     7: "normaliser over the wrong axis",
     8: "floor without the absolute value",
+    9: "per-token gate one token late",
 }
 
 
