@@ -43,8 +43,8 @@ METRIC = ("retention fwd tokens/s & TFLOP/s (% bf16 TC peak); decode steps/s & H
 # It holds only for the kernel sources that capture measured (their SHA-256
 # below); any later change to them makes the reported traffic null until the
 # kernel is captured again.
-KERNEL_SOURCES = ("chunk_tc_ws.cu", "chunk_tc_common.cuh", "tc_ptx.cuh", "chunk_tc.cu",
-                  "common.cuh", "launch.h")
+KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "tc_ptx.cuh",
+                  "chunk_tc.cu", "common.cuh", "launch.h")
 TRAFFIC = {
     "chunk_tc_ws_kernel/full": {
         "bytes": 52_005_888 + 293_888,
@@ -59,10 +59,11 @@ C_REF = 64  # chunk length fixed for counting useful intra-chunk flops
 # ----------------------------------------------------------------------------- accounting
 
 def alg_bytes(c: dict) -> int:
-    """Bytes the method must move: read Q, K, V, write O, write S_T (and z_T) in fp32."""
+    """Bytes the method must move: read Q, K, V (and the per-token log decays),
+    write O, write S_T (and z_T) in fp32."""
     es = 2 if c["dtype"] == "bf16" else 4
     nbh = c["B"] * c["H"]
-    io = nbh * c["T"] * (2 * c["dk"] + 2 * c["dv"]) * es
+    io = nbh * c["T"] * ((2 * c["dk"] + 2 * c["dv"]) * es + (4 if c.get("gate") else 0))
     state = nbh * c["dk"] * c["dv"] * 4 + (nbh * c["dk"] * 4 if c["normalize"] else 0)
     return io + state
 
@@ -89,7 +90,10 @@ def decode_flops(c: dict) -> int:
 
 def describe(name: str, c: dict) -> str:
     bits = [f"{name}: B={c['B']} H={c['H']} T={c['T']} d_k={c['dk']} d_v={c['dv']}",
-            c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity",
+            c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity"]
+    if c.get("gate"):
+        bits.append("per-token decay")
+    bits += [
             ("floored normaliser" if c.get("floor") else "normalised") if c["normalize"]
             else "no normaliser"]
     return ", ".join(bits)
@@ -235,6 +239,8 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
     k = x["k"].reshape(shape_qk)
     v = x["v"].reshape(shape_v)
     gamma = x["gamma"]
+    gated = bool(c.get("gate"))
+    log_a = x["log_a"].reshape(B, c["H"], c["T"]) if gated else None
     dev = torch.device("cuda")
     per_set = alg_bytes(c)
     n_sets = max(1, min(16, (3 * L2_BYTES + per_set - 1) // per_set))
@@ -244,24 +250,25 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
         O = torch.empty(shape_v, dtype=qd.dtype, device=dev)
         S = torch.empty(B, c["H"], c["dk"], c["dv"], device=dev)
         z = torch.empty(B, c["H"], c["dk"], device=dev) if c["normalize"] else None
-        sets.append((qd, kd, vd, O, S, z))
+        lad = log_a.to(dev) if gated else None
+        sets.append((qd, kd, vd, O, S, z, lad))
     ws_n = la.workspace_size(B, c["H"], c["T"], c["dk"], c["dv"], qd.dtype, c["phi"],
-                             c["normalize"])
+                             c["normalize"], gated=gated, floor=c.get("floor", False))
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(i):
-        qd, kd, vd, O, S, z = sets[i % n_sets]
-        la.chunk_fwd(qd, kd, vd, gamma, phi=c["phi"], normalize=c["normalize"],
-                     floor=c.get("floor", False), out=O, S_out=S, z_out=z, workspace=ws,
-                     stream=stream)
+        qd, kd, vd, O, S, z, lad = sets[i % n_sets]
+        la.chunk_fwd(qd, kd, vd, None if gated else gamma, phi=c["phi"],
+                     normalize=c["normalize"], floor=c.get("floor", False), out=O, S_out=S,
+                     z_out=z, workspace=ws, stream=stream, log_a=lad)
 
     for i in range(warmup):
         step(i)
     ms = time_region(step, steps, stream)
     kernels = kernel_breakdown(la, step, steps, stream)
     flags = ((la.LA_PHI_ELU1 if c["phi"] else 0) | (la.LA_NORMALIZE if c["normalize"] else 0)
-             | (la.LA_NORM_FLOOR if c.get("floor") else 0))
+             | (la.LA_NORM_FLOOR if c.get("floor") else 0) | (la.LA_GATED if gated else 0))
     launches = la.library().la_chunk_fwd_launches(B, c["H"], c["T"], c["dk"], c["dv"],
                                                   1 if c["dtype"] == "bf16" else 0, flags, 0)
     res = dict(name=name, config=c, ms=ms / steps, tokens=B * c["T"], n_sets=n_sets,
@@ -395,7 +402,8 @@ def run_ours(args) -> dict | None:
             print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
                               "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
         return None
-    if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16"):  # profiling aid
+    if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
+                "gated_retention_bf16"):  # profiling aid
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
         if rank == 0:
             print(json.dumps({"only": only, "ms_per_step": r["ms"],
@@ -411,7 +419,8 @@ def run_ours(args) -> dict | None:
     others = {}
     headline_only = args.headline_only or only == "headline"
     if not headline_only:
-        for name in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16"):
+        for name in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
+                     "gated_retention_bf16"):
             r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             others[name] = r
@@ -555,7 +564,8 @@ def main(argv=None):
                     help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
-                                       "retention_floor_bf16", "decode"), default=None,
+                                       "retention_floor_bf16", "gated_retention_bf16", "decode"),
+                    default=None,
                     help="profiling aid: run one workload only")
     ap.add_argument("--decode-steps", type=int,
                     default=workloads.CONFIGS["decode_bf16"]["decode_steps"],

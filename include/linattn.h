@@ -84,6 +84,10 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
  * division of each score row by the absolute value of its sum clamped below at 1
  * (same page, "Its normalizer is unstable").  Defined for signed features too. */
 #define LA_NORM_FLOOR 8u
+/* Per-token decay (la_chunk_fwd_gated): only the planning queries
+ * la_workspace_size and la_chunk_fwd_launches take this flag, to size a
+ * la_chunk_fwd_gated call; la_chunk_fwd rejects it. */
+#define LA_GATED 16u
 
 /* Human-readable text of a status code (static storage, never NULL). */
 LA_API const char* la_status_string(int status);
@@ -185,6 +189,54 @@ LA_API la_status la_recurrent_step(const void* q, const void* k, const void* v, 
                                    unsigned flags, float eps,
                                    float* S, float* z, void* o,
                                    int* dev_status, la_stream_t stream);
+
+/*
+ * Chunkwise forward with a per-token (data-dependent) scalar decay in place
+ * of the per-head gamma:
+ *
+ *   S_t = a_t S_{t-1} + phi(k_t) v_t^T,   z_t = a_t z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t  [ normalised as in la_chunk_fwd ]
+ *
+ * with a_t = exp(log_a[b][h][t]).  The generic "decay the old state, add the
+ * new contribution, read out" recurrence of "Linear Attention, RWKV, and
+ * RetNet" (temporalbook 13.3, subsection 4 "The Unifying Picture"), whose
+ * decay G_t depends on the input in the selective case, with G_t = a_t 1 a
+ * scalar per head and token; "Efficient and Sparse Transformers"
+ * (temporalbook 12.5, "Gated Linear Attention: Toward Input-Dependent
+ * Forgetting") has RetNet as the constant case G_t = gamma 1.  The chunkwise
+ * form uses cumulative log-decays inside each chunk instead of powers of
+ * gamma (the state between chunks decays by the product of the chunk's a_t).
+ *
+ *   log_a  DEVICE fp32 [B][H][T], natural log of each decay, finite and <= 0
+ *          (a_t in (0, 1]); read only; not checked (device memory)
+ *   other arguments as la_chunk_fwd (no gamma); flags as la_chunk_fwd, with
+ *          or without LA_GATED; LA_NONCAUSAL is LA_ERR_UNSUPPORTED
+ *   workspace: at least la_workspace_size(..., flags | LA_GATED, chunk)
+ *          bytes (the tensor-core path always needs some: the per-chunk
+ *          cumulative decays)
+ * Errors: as la_chunk_fwd; LA_ERR_INVALID_ARG also for log_a == NULL or
+ * misaligned when T > 0.
+ */
+LA_API la_status la_chunk_fwd_gated(const void* Q, const void* K, const void* V,
+                                    la_dtype dtype, const float* log_a, int B, int H, int T,
+                                    int d_k, int d_v, unsigned flags, float eps,
+                                    const float* S0, const float* z0,
+                                    void* O, float* S_out, float* z_out,
+                                    int chunk, void* workspace, size_t workspace_bytes,
+                                    int* dev_status, la_stream_t stream);
+
+/*
+ * One decode step with a per-token decay: la_recurrent_step with
+ * S = a S + phi(k) v^T, z = a z + phi(k), a = exp(log_a[b][h]).
+ *   log_a  DEVICE fp32 [B][H] (this step's decays), finite and <= 0
+ * Errors: as la_recurrent_step; LA_ERR_INVALID_ARG also for log_a == NULL or
+ * misaligned.
+ */
+LA_API la_status la_recurrent_step_gated(const void* q, const void* k, const void* v,
+                                         la_dtype dtype, const float* log_a, int B, int H,
+                                         int d_k, int d_v, unsigned flags, float eps,
+                                         float* S, float* z, void* o,
+                                         int* dev_status, la_stream_t stream);
 
 /*
  * la_chunk_fwd for callers that cannot allocate device memory.  The source

@@ -8,7 +8,9 @@ every call raises.
 Names follow the C ABI:
   state_init(S, z=None)                        zero a state        (la_state_init)
   chunk_fwd(q, k, v, gamma, ...)               prefill / forward   (la_chunk_fwd)
+  chunk_fwd(q, k, v, log_a=..., ...)           per-token decay     (la_chunk_fwd_gated)
   recurrent_step(q, k, v, gamma, S, z, ...)    one decode step     (la_recurrent_step)
+  recurrent_step(q, k, v, None, S, z, log_a=)  per-token decay     (la_recurrent_step_gated)
   workspace_size(...)                          scratch bytes       (la_workspace_size)
   chunk_fwd_host(...)                          la_chunk_fwd on host buffers, copies included
 """
@@ -24,7 +26,7 @@ from . import _build
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
-LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR = 1, 2, 4, 8
+LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR, LA_GATED = 1, 2, 4, 8, 16
 
 LIBRARY_PATH = _build.LIBRARY
 _LIB = None
@@ -76,6 +78,10 @@ def _load() -> ctypes.CDLL:
     lib.la_chunk_fwd.restype = i
     lib.la_recurrent_step.argtypes = [vp, vp, vp, i, vp, i, i, i, i, u, f, vp, vp, vp, vp, vp]
     lib.la_recurrent_step.restype = i
+    lib.la_chunk_fwd_gated.argtypes = lib.la_chunk_fwd.argtypes
+    lib.la_chunk_fwd_gated.restype = i
+    lib.la_recurrent_step_gated.argtypes = lib.la_recurrent_step.argtypes
+    lib.la_recurrent_step_gated.restype = i
     lib.la_chunk_fwd_launches.argtypes = [i, i, i, i, i, i, u, i]
     lib.la_chunk_fwd_launches.restype = i
     lib.la_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
@@ -148,10 +154,10 @@ def _check(status: int, what: str):
 
 
 def workspace_size(B, H, T, dk, dv, dtype=torch.bfloat16, phi=False, normalize=False,
-                   causal=True, chunk=0) -> int:
+                   causal=True, chunk=0, gated=False, floor=False) -> int:
     code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
-    return int(_load().la_workspace_size(B, H, T, dk, dv, code, _flags(phi, normalize, causal),
-                                         chunk))
+    flags = _flags(phi, normalize, causal, floor) | (LA_GATED if gated else 0)
+    return int(_load().la_workspace_size(B, H, T, dk, dv, code, flags, chunk))
 
 
 def state_init(S: torch.Tensor, z: torch.Tensor | None = None, stream=None):
@@ -161,15 +167,16 @@ def state_init(S: torch.Tensor, z: torch.Tensor | None = None, stream=None):
            "la_state_init")
 
 
-def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
+def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, eps=1e-6,
               S0=None, z0=None, chunk=0, out=None, S_out=None, z_out=None, return_state=True,
-              workspace=None, dev_status=None, stream=None, floor=False):
+              workspace=None, dev_status=None, stream=None, floor=False, log_a=None):
     """Chunkwise forward over [B,H,T,d] device tensors.
 
     Returns (O, S_T, z_T); S_T / z_T are None when return_state is False and
     no output buffer was given.  z_T is returned when normalising (or when
     z_out is given).  floor=True divides by max(|phi(q)^T z|, 1) (LA_NORM_FLOOR;
-    implies normalising, eps unused).
+    implies normalising, eps unused).  log_a: a [B,H,T] fp32 device tensor of
+    per-token log decays used instead of gamma (la_chunk_fwd_gated).
     """
     normalize = normalize or floor
     B, H, T, dk = q.shape
@@ -186,18 +193,30 @@ def chunk_fwd(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e
         S_out = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
     if return_state and normalize and z_out is None:
         z_out = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
-    g = _gamma_host(gamma, H)
+    if (gamma is None) == (log_a is None):
+        raise ValueError("pass exactly one of gamma and log_a")
+    if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
+        raise ValueError(f"log_a must be float32 [B,H,T] = {(B, H, T)}")
     flags = _flags(phi, normalize, causal, floor)
     lib = _load()
-    need = int(lib.la_workspace_size(B, H, T, dk, dv, dt, flags, chunk))
+    need = int(lib.la_workspace_size(B, H, T, dk, dv, dt,
+                                     flags | (LA_GATED if log_a is not None else 0), chunk))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), dt, g.ctypes.data, B, H, T, dk, dv, flags,
-                          float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out), _ptr(z_out),
-                          int(chunk), _ptr(workspace), ws_bytes, _ptr(dev_status),
-                          _stream(stream))
-    _check(st, "la_chunk_fwd")
+    if log_a is None:
+        g = _gamma_host(gamma, H)
+        st = lib.la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), dt, g.ctypes.data, B, H, T, dk, dv,
+                              flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out),
+                              _ptr(z_out), int(chunk), _ptr(workspace), ws_bytes,
+                              _ptr(dev_status), _stream(stream))
+        _check(st, "la_chunk_fwd")
+    else:
+        st = lib.la_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(log_a), B, H, T, dk, dv,
+                                    flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out),
+                                    _ptr(S_out), _ptr(z_out), int(chunk), _ptr(workspace),
+                                    ws_bytes, _ptr(dev_status), _stream(stream))
+        _check(st, "la_chunk_fwd_gated")
     return out, S_out, z_out
 
 
@@ -221,18 +240,31 @@ def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True
 
 
 def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps=1e-6,
-                   out=None, dev_status=None, stream=None, floor=False):
+                   out=None, dev_status=None, stream=None, floor=False, log_a=None):
     """One decode step on [B,H,d] device tensors; S (and z) are updated in place.
-    floor=True: divide by max(|phi(q)^T z|, 1) (needs z)."""
+    floor=True: divide by max(|phi(q)^T z|, 1) (needs z).  log_a: this step's
+    per-token log decays, a [B,H] fp32 device tensor, instead of gamma."""
     B, H, dk = q.shape
     dv = v.shape[-1]
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
-    g = _gamma_host(gamma, H)
-    st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
-                                   H, dk, dv, _flags(phi, normalize, True, floor), float(eps), _ptr(S),
-                                   _ptr(z), _ptr(out), _ptr(dev_status), _stream(stream))
-    _check(st, "la_recurrent_step")
+    if (gamma is None) == (log_a is None):
+        raise ValueError("pass exactly one of gamma and log_a")
+    flags = _flags(phi, normalize, True, floor)
+    if log_a is None:
+        g = _gamma_host(gamma, H)
+        st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data,
+                                       B, H, dk, dv, flags, float(eps), _ptr(S), _ptr(z),
+                                       _ptr(out), _ptr(dev_status), _stream(stream))
+        _check(st, "la_recurrent_step")
+    else:
+        if log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H):
+            raise ValueError(f"log_a must be float32 [B,H] = {(B, H)}")
+        st = _load().la_recurrent_step_gated(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
+                                             _ptr(log_a), B, H, dk, dv, flags, float(eps),
+                                             _ptr(S), _ptr(z), _ptr(out), _ptr(dev_status),
+                                             _stream(stream))
+        _check(st, "la_recurrent_step_gated")
     return out
 
 
@@ -320,4 +352,4 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
            "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
-           "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR"]
+           "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED"]

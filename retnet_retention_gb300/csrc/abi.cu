@@ -36,9 +36,41 @@ bool fill_gammas(const float* gamma, int H, KernelGammas* g, bool* all_one) {
     return true;
 }
 
+const float kOneGamma = 1.f;  // stands in for an absent gamma array when B * H == 0
+
 la_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
 size_t elem_size(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
+
+constexpr unsigned kCallFlags = LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR;
+
+// The arguments la_chunk_fwd's path choice depends on (pointers are irrelevant;
+// a per-token decay is marked by a non-null log_a).
+ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                    int chunk) {
+    static const float kMarker = 0.f;
+    ChunkArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.normalize = (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0;
+    a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
+    a.noncausal = (flags & LA_NONCAUSAL) != 0;
+    a.log_a = (flags & LA_GATED) ? &kMarker : nullptr;
+    return a;
+}
+
+bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags) {
+    return B > 0 && H > 0 && T > 0 && valid_dim(d_k) && valid_dim(d_v) && H <= kMaxHeads &&
+           (dtype == LA_DTYPE_F32 || dtype == LA_DTYPE_BF16) &&
+           !(flags & ~(kCallFlags | LA_GATED));
+}
+
+bool simt_pinned() {
+    const char* pin = std::getenv("LA_CHUNK_PATH");
+    return pin && std::strcmp(pin, "simt") == 0;
+}
 
 }  // namespace
 
@@ -57,42 +89,20 @@ const char* la_status_string(int status) {
 
 int la_abi_version(void) { return LA_ABI_VERSION; }
 
-// The arguments la_chunk_fwd's path choice depends on (pointers are irrelevant).
-static ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
-                           int chunk) {
-    ChunkArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
-    a.bf16 = dtype == LA_DTYPE_BF16;
-    a.phi = (flags & LA_PHI_ELU1) != 0;
-    a.normalize = (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0;
-    a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
-    a.noncausal = (flags & LA_NONCAUSAL) != 0;
-    return a;
-}
-
-static bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags) {
-    return B > 0 && H > 0 && T > 0 && valid_dim(d_k) && valid_dim(d_v) && H <= kMaxHeads &&
-           (dtype == LA_DTYPE_F32 || dtype == LA_DTYPE_BF16) &&
-           !(flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR));
-}
-
 size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
                          int chunk) {
     if (!plan_ok(B, H, T, d_k, d_v, dtype, flags)) return 0;
     ChunkArgs a = plan_args(B, H, T, d_k, d_v, dtype, flags, chunk);
-    const char* pin = std::getenv("LA_CHUNK_PATH");
-    if ((pin && std::strcmp(pin, "simt") == 0) || !tc_supported(a)) return 0;
-    return tc_workspace_bytes(B, H, T, d_k, d_v, a.noncausal);
+    if (simt_pinned() || !tc_supported(a)) return 0;
+    return tc_workspace_bytes(a);
 }
 
 int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
                           int chunk) {
     if (!plan_ok(B, H, T, d_k, d_v, dtype, flags)) return 0;
     ChunkArgs a = plan_args(B, H, T, d_k, d_v, dtype, flags, chunk);
-    const char* pin = std::getenv("LA_CHUNK_PATH");
-    if ((pin && std::strcmp(pin, "simt") == 0) || !tc_supported(a)) return 1;
-    return tc_launch_count(B, H, T, d_k, d_v, a.noncausal, a.normalize);
+    if (simt_pinned() || !tc_supported(a)) return 1;
+    return tc_launch_count(a);
 }
 
 la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_stream_t stream) {
@@ -104,28 +114,39 @@ la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_s
                                          (cudaStream_t)stream));
 }
 
-la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
-                       const float* gamma, int B, int H, int T, int d_k, int d_v,
-                       unsigned flags, float eps, const float* S0, const float* z0, void* O,
-                       float* S_out, float* z_out, int chunk, void* workspace,
-                       size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// la_chunk_fwd and la_chunk_fwd_gated: exactly one of gamma (host [H]) and log_a
+// (device [B][H][T]) is given.
+la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
+                    const float* gamma, const float* log_a, int B, int H, int T, int d_k,
+                    int d_v, unsigned flags, float eps, const float* S0, const float* z0,
+                    void* O, float* S_out, float* z_out, int chunk, void* workspace,
+                    size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+    const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
     if (!(chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128))
         return LA_ERR_INVALID_ARG;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
     const size_t nbh = (size_t)B * H;
     if (nbh == 0) return LA_OK;
-    if (!gamma) return LA_ERR_INVALID_ARG;
     KernelGammas g;
     bool all_one = true;
-    if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
+    if (gated) {
+        std::memset(&g, 0, sizeof(g));
+        all_one = false;
+    } else if (!fill_gammas(gamma, H, &g, &all_one)) {
+        return LA_ERR_INVALID_ARG;
+    }
     const bool noncausal = (flags & LA_NONCAUSAL) != 0;
     const bool floor_norm = (flags & LA_NORM_FLOOR) != 0;
     const bool normalize = (flags & LA_NORMALIZE) != 0 || floor_norm;
-    if (noncausal && (!all_one || S0 || z0)) return LA_ERR_UNSUPPORTED;
+    if (noncausal && (gated || !all_one || S0 || z0)) return LA_ERR_UNSUPPORTED;
 
     const size_t es = elem_size(dtype);
     const size_t n_qk = nbh * (size_t)T * d_k * es, n_v = nbh * (size_t)T * d_v * es;
@@ -135,11 +156,14 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
             return LA_ERR_INVALID_ARG;
         if (overlaps(O, n_v, Q, n_qk) || overlaps(O, n_v, K, n_qk) || overlaps(O, n_v, V, n_v))
             return LA_ERR_INVALID_ARG;
+        if (gated && (!log_a || !aligned16(log_a) || overlaps(O, n_v, log_a, nbh * T * 4)))
+            return LA_ERR_INVALID_ARG;
     }
     for (const void* p : {(const void*)S0, (const void*)z0, (const void*)S_out,
                           (const void*)z_out, (const void*)workspace})
         if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
-    if (workspace_bytes < la_workspace_size(B, H, T, d_k, d_v, dtype, flags, chunk))
+    if (workspace_bytes <
+        la_workspace_size(B, H, T, d_k, d_v, dtype, flags | (gated ? LA_GATED : 0u), chunk))
         return LA_ERR_INVALID_ARG;
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -163,6 +187,7 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     a.floor_norm = floor_norm;
     a.noncausal = noncausal;
     a.eps = eps;
+    a.log_a = gated ? log_a : nullptr;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.dev_status = dev_status;
@@ -179,28 +204,32 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     return cuda_status(launch_chunk_simt(a, g, s));
 }
 
-la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
-                            const float* gamma, int B, int H, int d_k, int d_v, unsigned flags,
-                            float eps, float* S, float* z, void* o, int* dev_status,
-                            la_stream_t stream) {
-    (void)dev_status;  // the decode step has no device-side waits
+la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
+                         const float* gamma, const float* log_a, int B, int H, int d_k, int d_v,
+                         unsigned flags, float eps, float* S, float* z, void* o,
+                         la_stream_t stream) {
+    const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_PHI_ELU1 | LA_NORMALIZE | LA_NONCAUSAL | LA_NORM_FLOOR)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
     if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
     const size_t nbh = (size_t)B * H;
     if (nbh == 0) return LA_OK;
-    if (!gamma) return LA_ERR_INVALID_ARG;
     KernelGammas g;
     bool all_one = true;
-    if (!fill_gammas(gamma, H, &g, &all_one)) return LA_ERR_INVALID_ARG;
+    if (gated) {
+        std::memset(&g, 0, sizeof(g));
+    } else if (!fill_gammas(gamma, H, &g, &all_one)) {
+        return LA_ERR_INVALID_ARG;
+    }
     const bool floor_norm = (flags & LA_NORM_FLOOR) != 0;
     const bool normalize = (flags & LA_NORMALIZE) != 0 || floor_norm;
-    if (!q || !k || !v || !o || !S || (normalize && !z)) return LA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !S || (normalize && !z) || (gated && !log_a))
+        return LA_ERR_INVALID_ARG;
     for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
-                          (const void*)S, (const void*)z})
+                          (const void*)S, (const void*)z, (const void*)log_a})
         if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     const size_t n_o = nbh * d_v * es;
@@ -216,7 +245,52 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtyp
     a.normalize = normalize;
     a.floor_norm = floor_norm;
     a.eps = eps;
+    a.log_a = gated ? log_a : nullptr;
     return cuda_status(launch_decode_step(a, g, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
+                       const float* gamma, int B, int H, int T, int d_k, int d_v,
+                       unsigned flags, float eps, const float* S0, const float* z0, void* O,
+                       float* S_out, float* z_out, int chunk, void* workspace,
+                       size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+    if (!gamma && (size_t)B * H > 0 && B > 0 && H > 0) return LA_ERR_INVALID_ARG;
+    if (!gamma) gamma = &kOneGamma;  // B or H == 0 (or negative: rejected below)
+    return chunk_fwd(Q, K, V, dtype, gamma, nullptr, B, H, T, d_k, d_v, flags, eps, S0, z0, O,
+                     S_out, z_out, chunk, workspace, workspace_bytes, dev_status, stream);
+}
+
+la_status la_chunk_fwd_gated(const void* Q, const void* K, const void* V, la_dtype dtype,
+                             const float* log_a, int B, int H, int T, int d_k, int d_v,
+                             unsigned flags, float eps, const float* S0, const float* z0,
+                             void* O, float* S_out, float* z_out, int chunk, void* workspace,
+                             size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+    return chunk_fwd(Q, K, V, dtype, nullptr, log_a, B, H, T, d_k, d_v, flags, eps, S0, z0, O,
+                     S_out, z_out, chunk, workspace, workspace_bytes, dev_status, stream);
+}
+
+la_status la_recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
+                            const float* gamma, int B, int H, int d_k, int d_v, unsigned flags,
+                            float eps, float* S, float* z, void* o, int* dev_status,
+                            la_stream_t stream) {
+    (void)dev_status;  // the decode step has no device-side waits
+    if (!gamma && (size_t)B * H > 0 && B > 0 && H > 0) return LA_ERR_INVALID_ARG;
+    if (!gamma) gamma = &kOneGamma;
+    return recurrent_step(q, k, v, dtype, gamma, nullptr, B, H, d_k, d_v, flags, eps, S, z, o,
+                          stream);
+}
+
+la_status la_recurrent_step_gated(const void* q, const void* k, const void* v, la_dtype dtype,
+                                  const float* log_a, int B, int H, int d_k, int d_v,
+                                  unsigned flags, float eps, float* S, float* z, void* o,
+                                  int* dev_status, la_stream_t stream) {
+    (void)dev_status;
+    return recurrent_step(q, k, v, dtype, nullptr, log_a, B, H, d_k, d_v, flags, eps, S, z, o,
+                          stream);
 }
 
 }  // extern "C"

@@ -14,7 +14,10 @@
 //   z_c  = gamma^L z_{c-1} + sum_j gamma^(L-1-j) phi(k_j)
 //
 // Only non-negative powers of gamma appear, so small gamma underflows to 0
-// instead of overflowing.  The non-causal form (gamma = 1, "Linear
+// instead of overflowing.  With a per-token decay a_t (log a_t given) the
+// powers become cumulative log-decays inside the chunk, b_i = sum_{s<=i} log a_s:
+// gamma^(i-j) -> e^(b_i - b_j), gamma^(i+1) -> e^(b_i), gamma^(L-1-j) ->
+// e^(b_(L-1) - b_j), gamma^L -> e^(b_(L-1)) (exponents again never positive).  The non-causal form (gamma = 1, "Linear
 // attention" box) is two passes: the summary S = sum_t phi(k_t) v_t^T, then
 // o_t = phi(q_t)^T S.
 //
@@ -33,7 +36,7 @@ constexpr int kMaxDvBlock = 64;
 
 struct SimtSmem {
     // offsets (in floats) into dynamic shared memory
-    int q, k, v, a, s, z, den, pw, total;
+    int q, k, v, a, s, z, den, pw, cum, xw, total;
 };
 
 __host__ __device__ inline SimtSmem simt_layout(int C, int dk, int dvb) {
@@ -47,7 +50,9 @@ __host__ __device__ inline SimtSmem simt_layout(int C, int dk, int dvb) {
     L.z = L.s + dk * dvb;
     L.den = L.z + dk;
     L.pw = L.den + C;
-    L.total = L.pw + C + 2;
+    L.cum = L.pw + C + 2;
+    L.xw = L.cum + C;
+    L.total = L.xw + C;
     return L;
 }
 
@@ -57,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
     T* __restrict__ O, const float* __restrict__ S0, const float* __restrict__ z0,
     float* __restrict__ S_out, float* __restrict__ z_out, int H, int T_len, int dk, int dv,
     int C, int dvb, int phi, int normalize, int noncausal, float eps,
-    const __grid_constant__ KernelGammas g) {
+    const float* __restrict__ log_a, const __grid_constant__ KernelGammas g) {
     extern __shared__ float smem[];
     const SimtSmem lay = simt_layout(C, dk, dvb);
     float* Qs = smem + lay.q;
@@ -68,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
     float* zs = smem + lay.z;
     float* den = smem + lay.den;
     float* pw = smem + lay.pw;
+    float* cum = smem + lay.cum;  // per-token decay: log2 of the cumulative decay in the chunk
+    float* xw = smem + lay.xw;    // per-token decay: e^(b_i) (pw then holds e^(b_(L-1) - b_j))
     const int ld = dk + 1;
     const int lda = C + 1;
 
@@ -114,7 +121,25 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
                 int i = idx / dvb, cc = idx % dvb;
                 Vs[idx] = cc < nv ? load_elem(V, v_base + (size_t)(t0 + i) * dv + v0 + cc) : 0.f;
             }
+            if (log_a && tid == 0) {  // b_i = sum_{s<=i} log a_s, in log2 units
+                float acc = 0.f;
+                for (int i = 0; i < L; ++i) {
+                    acc += log_a[(size_t)bh * T_len + t0 + i] * 1.44269504088896341f;
+                    cum[i] = acc;
+                }
+            }
             __syncthreads();
+            if (log_a) {
+                for (int i = tid; i < L; i += kThreads) {
+                    xw[i] = exp2f(cum[i]);
+                    pw[i] = exp2f(cum[L - 1] - cum[i]);
+                }
+                __syncthreads();
+            }
+            // decay factors of this chunk (see the header)
+            auto dmask = [&](int i, int j) { return log_a ? exp2f(cum[i] - cum[j]) : pw[i - j]; };
+            auto xi = [&](int i) { return log_a ? xw[i] : pw[i + 1]; };
+            auto zeta = [&](int j) { return log_a ? pw[j] : pw[L - 1 - j]; };
 
             if (do_out) {
                 if (!noncausal) {
@@ -127,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
                             const float* kj = Ks + j * ld;
                             float dot = 0.f;
                             for (int d = 0; d < dk; ++d) dot = fmaf(qi[d], kj[d], dot);
-                            a = dot * pw[i - j];
+                            a = dot * dmask(i, j);
                         }
                         As[i * lda + j] = a;
                     }
@@ -140,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
                             for (int j = 0; j <= i; ++j) r += As[i * lda + j];
                         float qz = 0.f;
                         for (int d = 0; d < dk; ++d) qz = fmaf(Qs[i * ld + d], zs[d], qz);
-                        den[i] = norm_den(r + (noncausal ? 1.f : pw[i + 1]) * qz, normalize, eps);
+                        den[i] = norm_den(r + (noncausal ? 1.f : xi(i)) * qz, normalize, eps);
                     }
                     __syncthreads();
                 }
@@ -152,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
                     float inter = 0.f;
                     const float* qi = Qs + i * ld;
                     for (int d = 0; d < dk; ++d) inter = fmaf(qi[d], Ss[d * dvb + cc], inter);
-                    float o = intra + (noncausal ? 1.f : pw[i + 1]) * inter;
+                    float o = intra + (noncausal ? 1.f : xi(i)) * inter;
                     if (normalize) o = o / den[i];
                     store_elem(O, v_base + (size_t)(t0 + i) * dv + v0 + cc, o);
                 }
@@ -160,19 +185,19 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(
             }
             if (do_state) {
                 // S_c = gamma^L S_{c-1} + sum_j gamma^(L-1-j) phi(k_j) v_j^T
-                const float gL = noncausal ? 1.f : pw[L];
+                const float gL = noncausal ? 1.f : (log_a ? exp2f(cum[L - 1]) : pw[L]);
                 for (int idx = tid; idx < dk * dvb; idx += kThreads) {
                     int d = idx / dvb, cc = idx % dvb;
                     float u = 0.f;
                     for (int j = 0; j < L; ++j) {
-                        float w = noncausal ? 1.f : pw[L - 1 - j];
+                        float w = noncausal ? 1.f : zeta(j);
                         u = fmaf(w * Ks[j * ld + d], Vs[j * dvb + cc], u);
                     }
                     Ss[idx] = fmaf(gL, Ss[idx], u);
                 }
                 for (int d = tid; d < dk; d += kThreads) {
                     float u = 0.f;
-                    for (int j = 0; j < L; ++j) u = fmaf(noncausal ? 1.f : pw[L - 1 - j], Ks[j * ld + d], u);
+                    for (int j = 0; j < L; ++j) u = fmaf(noncausal ? 1.f : zeta(j), Ks[j * ld + d], u);
                     zs[d] = fmaf(gL, zs[d], u);
                 }
                 __syncthreads();
@@ -214,7 +239,8 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStr
         kern<<<grid, kThreads, smem, s>>>(
             (const __nv_bfloat16*)a.Q, (const __nv_bfloat16*)a.K, (const __nv_bfloat16*)a.V,
             (__nv_bfloat16*)a.O, a.S0, a.z0, a.S_out, a.z_out, a.H, a.T,
-            a.dk, a.dv, C, dvb, a.phi, norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps, g);
+            a.dk, a.dv, C, dvb, a.phi, norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps,
+            a.log_a, g);
     } else {
         auto kern = chunk_simt_kernel<float>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -222,7 +248,7 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStr
         kern<<<grid, kThreads, smem, s>>>(
             (const float*)a.Q, (const float*)a.K, (const float*)a.V, (float*)a.O, a.S0,
             a.z0, a.S_out, a.z_out, a.H, a.T, a.dk, a.dv, C, dvb, a.phi,
-            norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps, g);
+            norm_mode(a.normalize, a.floor_norm), a.noncausal, a.eps, a.log_a, g);
     }
     return cudaGetLastError();
 }

@@ -542,6 +542,7 @@ cudaError_t launch_tc_dispatch(int dk, int dvb, const TcParams& prm, int grid, c
     if (grid <= 0) return cudaSuccess;
     if (tc_ws_supported(prm.mode, dk, dvb, prm.normalize != 0))
         return launch_chunk_tc_ws(dk, dvb, prm.normalize != 0, prm, grid, s, pdl);
+    if (prm.gate) return cudaErrorInvalidValue;  // the per-token decay runs in the pipelined kernel only
     if (dk == 64 && dvb == 64) return launch_tc<64, 64>(prm, grid, s);
     if (dk == 64 && dvb == 128) return launch_tc<64, 128>(prm, grid, s);
     if (dk == 128 && dvb == 64) return launch_tc<128, 64>(prm, grid, s);
@@ -575,11 +576,14 @@ int choose_segments(int units, int n_chunks) {
 // memory once per batch rather than once per segment.  Launched as a
 // programmatic dependent of the state walk: it lets the output walk be
 // scheduled at once and waits for the state walk's results.
+// With the per-token decay the decay over segment q is 2^(seg_l2[bh][q]), the
+// segment's total log2 decay that the state walk wrote.
 constexpr int kScanBatch = 8;
 __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
                                     const float* __restrict__ agg, const float* __restrict__ zagg,
                                     float* __restrict__ entry, float* __restrict__ zentry,
                                     size_t total, int H, int P, int seg_len, int dk, int dv,
+                                    const float* __restrict__ seg_l2,
                                     const __grid_constant__ KernelGammas g) {
     tc::griddep_launch_dependents();
     tc::griddep_wait();
@@ -588,18 +592,19 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
     const size_t per = (size_t)dk * dv;
     const size_t bh = idx / per;
     const size_t e = idx % per;
-    const float gseg = gamma_pow(g.log2g[bh % H], (float)seg_len);
+    const float gseg = seg_l2 ? 0.f : gamma_pow(g.log2g[bh % H], (float)seg_len);
     float x = S0 ? S0[bh * per + e] : 0.f;
     const bool do_z = (e % dv) == 0;
     const size_t d = e / dv;
     float zz = (do_z && z0) ? z0[bh * dk + d] : 0.f;
     for (int q0 = 0; q0 < P; q0 += kScanBatch) {
-        float a[kScanBatch], za[kScanBatch];
+        float a[kScanBatch], za[kScanBatch], gq[kScanBatch];
 #pragma unroll
         for (int b = 0; b < kScanBatch; ++b) {  // the last segment's contribution is not needed
             const int q = q0 + b;
             a[b] = q + 1 < P ? agg[(bh * P + q) * per + e] : 0.f;
             za[b] = (do_z && q + 1 < P) ? zagg[(bh * P + q) * dk + d] : 0.f;
+            gq[b] = seg_l2 ? (q + 1 < P ? exp2f(seg_l2[bh * P + q]) : 0.f) : gseg;
         }
 #pragma unroll
         for (int b = 0; b < kScanBatch; ++b) {
@@ -607,10 +612,44 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
             if (q >= P) break;
             entry[(bh * P + q) * per + e] = x;
             if (do_z) zentry[(bh * P + q) * dk + d] = zz;
-            x = fmaf(gseg, x, a[b]);
-            if (do_z) zz = fmaf(gseg, zz, za[b]);
+            x = fmaf(gq[b], x, a[b]);
+            if (do_z) zz = fmaf(gq[b], zz, za[b]);
         }
     }
+}
+
+// Per chunk of every sequence, for the per-token decay: the cumulative log2
+// decays b_i = sum_{s<=i} log2 a_s inside the chunk (flat past the end of the
+// sequence) and the decays a_i themselves, into gate[bh][c][0..127] and
+// [128..255].  One warp per chunk: each lane scans four tokens, then the lanes'
+// totals are scanned with shuffles.
+__global__ void gate_prep_kernel(const float* __restrict__ log_a, float* __restrict__ gate, int T,
+                                 int n_chunks, size_t total_chunks) {
+    const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= total_chunks) return;  // whole warps only: the block size is a multiple of 32
+    const size_t bh = wid / (size_t)n_chunks;
+    const int c = (int)(wid % (size_t)n_chunks);
+    float l[4], a[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int t = c * kC + lane * 4 + e;
+        l[e] = t < T ? log_a[bh * T + t] * 1.44269504088896341f : 0.f;
+        a[e] = exp2f(l[e]);
+    }
+    l[1] += l[0];
+    l[2] += l[1];
+    l[3] += l[2];
+    float inc = l[3];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    const float ex = inc - l[3];  // the lanes before this one
+    float* gp = gate + wid * 256;
+    reinterpret_cast<float4*>(gp)[lane] = make_float4(l[0] + ex, l[1] + ex, l[2] + ex, l[3] + ex);
+    reinterpret_cast<float4*>(gp + 128)[lane] = make_float4(a[0], a[1], a[2], a[3]);
 }
 
 }  // namespace
@@ -630,11 +669,16 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
 }
 }  // namespace tck
 
+static int tc_dvb(const ChunkArgs& a);
+
 bool tc_supported(const ChunkArgs& a) {
     if (!a.bf16) return false;
     if (a.dk != 64 && a.dk != 128) return false;
     if (a.dv != 64 && a.dv != 128 && a.dv != 256) return false;
     if (a.chunk != 0 && a.chunk != kC) return false;
+    // the per-token decay: causal, in the pipelined kernel only
+    if (a.log_a && (a.noncausal || !tc_ws_supported(kFull, a.dk, tc_dvb(a), a.normalize)))
+        return false;
     if (!encode_fn()) return false;
     int dev = 0, major = 0, minor = 0;
     cudaGetDevice(&dev);
@@ -643,7 +687,13 @@ bool tc_supported(const ChunkArgs& a) {
     return major == 10 && minor == 3;
 }
 
-static int tc_dvb(int dv) { return dv == 64 ? 64 : 128; }
+// Value columns per CTA: 64 or 128.  With the per-token decay 64 when
+// normalising (the pipelined kernel's normalising width) or for d_k = 128 (a
+// 128 x 128 stage leaves no shared memory for the chunk's decays).
+static int tc_dvb(const ChunkArgs& a) {
+    if (a.log_a && (a.normalize || a.dk == 128)) return 64;
+    return a.dv == 64 ? 64 : 128;
+}
 
 // Whether the output walk folds the segments' contributions into its entry states
 // itself (no scan kernel): few segments per sequence, and the pipelined kernel runs.
@@ -651,27 +701,59 @@ static bool fold_segments(int P, int dk, int dvb, bool normalize) {
     return P <= kFoldMax && tc_ws_supported(kFull, dk, dvb, normalize);
 }
 
-int tc_launch_count(int B, int H, int T, int dk, int dv, bool noncausal, bool normalize) {
-    if (noncausal || T <= 0) return 1;
-    const int n_chunks = (T + kC - 1) / kC;
-    const int units = B * H * (dv / tc_dvb(dv));
-    const int P = choose_segments(units, n_chunks);
-    if (P <= 1) return 1;
-    const int seg_chunks = (n_chunks + P - 1) / P;
-    const int Pu = (n_chunks + seg_chunks - 1) / seg_chunks;
-    return fold_segments(Pu, dk, tc_dvb(dv), normalize) ? 2 : 3;
+namespace {
+
+// The segment plan and the workspace layout of one tensor-core call.
+struct TcPlan {
+    int n_chunks, units, dvb;
+    int P;           // segments per sequence chosen (1: no segments)
+    int seg_chunks;  // chunks per segment
+    int Pu;          // segments actually used
+    // workspace byte offsets: per-token decays per chunk, segment decays, then the
+    // segment states (agg, entry: [BH][Pu][dk][dv]; zagg, zentry: [BH][Pu][dk])
+    size_t o_gate, o_segl2, o_agg, o_entry, o_zagg, o_zentry, bytes;
+};
+
+TcPlan tc_plan(const ChunkArgs& a) {
+    TcPlan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    pl.n_chunks = (a.T + kC - 1) / kC;
+    pl.dvb = tc_dvb(a);
+    pl.units = a.B * a.H * (a.dv / pl.dvb);
+    pl.P = a.noncausal || a.T <= 0 ? 1 : choose_segments(pl.units, pl.n_chunks);
+    pl.seg_chunks = pl.P > 1 ? (pl.n_chunks + pl.P - 1) / pl.P : pl.n_chunks;
+    pl.Pu = pl.P > 1 ? (pl.n_chunks + pl.seg_chunks - 1) / pl.seg_chunks : 1;
+    const size_t nbh = (size_t)a.B * a.H;
+    size_t off = 0;
+    if (a.log_a && !a.noncausal && a.T > 0) {
+        pl.o_gate = off;
+        off += nbh * pl.n_chunks * 256 * sizeof(float);
+        pl.o_segl2 = off;
+        if (pl.P > 1) off += (nbh * pl.P * sizeof(float) + 15) / 16 * 16;
+    }
+    if (pl.P > 1) {
+        const size_t st = nbh * pl.P * a.dk * a.dv * sizeof(float), zt = nbh * pl.P * a.dk * sizeof(float);
+        pl.o_agg = off;
+        pl.o_entry = off + st;
+        pl.o_zagg = off + 2 * st;
+        pl.o_zentry = off + 2 * st + zt;
+        off += 2 * st + 2 * zt;
+    }
+    pl.bytes = off;
+    return pl;
 }
 
-size_t tc_workspace_bytes(int B, int H, int T, int dk, int dv, bool noncausal) {
-    if (noncausal || T <= 0) return 0;
-    const int n_chunks = (T + kC - 1) / kC;
-    const int units = B * H * (dv / tc_dvb(dv));
-    const int P = choose_segments(units, n_chunks);
-    if (P <= 1) return 0;
-    const size_t nbh = (size_t)B * H;
-    // agg, entry: [BH][P][dk][dv]; zagg, zentry: [BH][P][dk]
-    return (2 * nbh * P * dk * dv + 2 * nbh * P * dk) * sizeof(float);
+}  // namespace
+
+int tc_launch_count(const ChunkArgs& a) {
+    if (a.noncausal || a.T <= 0) return 1;
+    const TcPlan pl = tc_plan(a);
+    const int prep = a.log_a ? 1 : 0;
+    if (pl.P <= 1) return 1 + prep;
+    return (fold_segments(pl.Pu, a.dk, pl.dvb, a.normalize) ? 2 : 3) + prep;
 }
+
+size_t tc_workspace_bytes(const ChunkArgs& a) { return tc_plan(a).bytes; }
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
                             int* launches) {
@@ -681,7 +763,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     if (!make_map(&prm.tmQ, a.Q, BH, a.T, a.dk) || !make_map(&prm.tmK, a.K, BH, a.T, a.dk) ||
         !make_map(&prm.tmV, a.V, BH, a.T, a.dv))
         return cudaErrorInvalidValue;
-    const int dvb = tc_dvb(a.dv);
+    const TcPlan pl = tc_plan(a);
+    if (a.workspace_bytes < pl.bytes || (pl.bytes > 0 && !a.workspace)) return cudaErrorInvalidValue;
+    char* ws = static_cast<char*>(a.workspace);
+    const int dvb = pl.dvb;
     prm.O = (__nv_bfloat16*)a.O;
     prm.H = a.H;
     prm.T = a.T;
@@ -699,8 +784,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         prm.wait_ns = 1000000ull;  // 1 ms
     }
     prm.g = g;
-    const int n_chunks = (a.T + kC - 1) / kC;
-    const int units = BH * prm.n_dvb;
+    const int n_chunks = pl.n_chunks;
+    const int units = pl.units;
     *launches = 0;
 
     if (a.noncausal) {
@@ -715,8 +800,23 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         *launches = 1;
         return launch_tc_dispatch(a.dk, dvb, prm, units, s);
     }
-    const int P = choose_segments(units, n_chunks);
-    if (P <= 1) {
+    if (a.log_a) {
+        // per-token decay: the chunks' cumulative decays first (plain stream order:
+        // every later kernel's producer reads them from its first chunk on)
+        float* gate = reinterpret_cast<float*>(ws + pl.o_gate);
+        const size_t total_chunks = (size_t)BH * n_chunks;
+        {
+            TraceScope trace("gate_prep_kernel", s);
+            gate_prep_kernel<<<(unsigned)((total_chunks * 32 + 255) / 256), 256, 0, s>>>(
+                a.log_a, gate, a.T, n_chunks, total_chunks);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        prm.gate = gate;
+        prm.seg_l2 = pl.P > 1 ? reinterpret_cast<float*>(ws + pl.o_segl2) : nullptr;
+        *launches = 1;
+    }
+    if (pl.P <= 1) {
         prm.mode = kFull;
         prm.seg_chunks = n_chunks;
         prm.n_seg = 1;
@@ -727,20 +827,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         prm.z_out = a.z_out;
         prm.out_nseg = 1;
         prm.out_last_only = 1;
-        *launches = 1;
+        *launches += 1;
         return launch_tc_dispatch(a.dk, dvb, prm, units, s);
     }
     // segmented: (1) each segment's own state, (2) scan to entry states, (3) outputs
-    const int seg_chunks = (n_chunks + P - 1) / P;
-    const int Pu = (n_chunks + seg_chunks - 1) / seg_chunks;  // segments actually used
+    const int seg_chunks = pl.seg_chunks;
+    const int Pu = pl.Pu;  // segments actually used
     const size_t nbh = (size_t)BH;
-    float* agg = (float*)a.workspace;
-    float* entry = agg + nbh * Pu * a.dk * a.dv;
-    float* zagg = entry + nbh * Pu * a.dk * a.dv;
-    float* zentry = zagg + nbh * Pu * a.dk;
-    if (tc_workspace_bytes(a.B, a.H, a.T, a.dk, a.dv, false) <
-        (2 * nbh * Pu * a.dk * a.dv + 2 * nbh * Pu * a.dk) * sizeof(float))
-        return cudaErrorInvalidValue;
+    float* agg = reinterpret_cast<float*>(ws + pl.o_agg);
+    float* entry = reinterpret_cast<float*>(ws + pl.o_entry);
+    float* zagg = reinterpret_cast<float*>(ws + pl.o_zagg);
+    float* zentry = reinterpret_cast<float*>(ws + pl.o_zentry);
 
     TcParams pa = prm;  // state-only walks of segments 0 .. Pu-2 (the last one's is not needed)
     pa.mode = kStateOnly;
@@ -768,7 +865,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         pc.in_agg = 1;
         pc.S0 = a.S0;
         pc.z0 = a.z0;
-        *launches = 2;
+        *launches += 2;
         return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
     }
     const size_t total = nbh * (size_t)a.dk * a.dv;
@@ -785,12 +882,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, segment_scan_kernel, a.S0, a.z0, (const float*)agg,
                                (const float*)zagg, entry, zentry, total, a.H, Pu, seg_chunks * kC,
-                               a.dk, a.dv, g);
+                               a.dk, a.dv, (const float*)prm.seg_l2, g);
     }
     if (e != cudaSuccess) return e;
     pc.S_in = entry;
     pc.z_in = zentry;
-    *launches = 3;
+    *launches += 3;
     return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
 }
 

@@ -45,6 +45,12 @@ struct TcParams {
     int in_agg;
     const float* S0;
     const float* z0;
+    // per-token decay (null: the per-head gammas): per chunk of every sequence,
+    // 128 cumulative log2 decays then 128 decays ([BH][n_chunks][2][128] fp32,
+    // written by gate_prep_kernel), and each segment's total log2 decay
+    // ([BH][n_seg]: written by the state walk, read by the fold and the scan)
+    const float* gate;
+    float* seg_l2;
     int* dev_status;
     unsigned long long wait_ns;
     int force_timeout;
@@ -183,7 +189,7 @@ __device__ __forceinline__ void scale_rows_dot(char* tile, F fac, const float* z
 }
 
 // K^ = zeta . K in place over a [128 x DK] K-major swizzled bf16 tile by 128
-// threads (zeta_r = gamma^(L-1-r), rows >= L zeroed), and the fp32 column sums
+// threads (row r times fac(r) = zeta_r, 0 for rows >= L), and the fp32 column sums
 // of zeta_r k_r taken from the unscaled values (the normaliser state's update,
 // without the bf16 rounding of zeta_r k_r).  Each 64-column block has its own
 // NT = 128 / (DK / 64) threads; thread t' of a block holds 16-byte piece t' & 7
@@ -193,8 +199,8 @@ __device__ __forceinline__ void scale_rows_dot(char* tile, F fac, const float* z
 // each warp then store the warp's sums into part ([256/DK][DK] floats, slot =
 // the warp's index within its block: the layout colsum_total() reads); the
 // caller synchronises the 128 threads before reading them.
-template <int DK>
-__device__ __forceinline__ void scale_rows_zsum(char* tile, int L, float l2g, float* part, int t) {
+template <int DK, typename F>
+__device__ __forceinline__ void scale_rows_zsum(char* tile, F fac, float* part, int t) {
     constexpr int NT = 128 / (DK / 64);  // threads per block
     constexpr int NP = 1024 / NT;        // pieces per thread
     const int b = t / NT, tb = t % NT;
@@ -206,7 +212,7 @@ __device__ __forceinline__ void scale_rows_zsum(char* tile, int L, float l2g, fl
 #pragma unroll 2
     for (int m = 0; m < NP; ++m) {
         const int r = rg + (NT / 8) * m;
-        const float f = r < L ? gamma_pow(l2g, (float)(L - 1 - r)) : 0.f;
+        const float f = fac(r);
         uint4 u = base[m * NT];  // NT / 8 rows of 8 pieces further on
         __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll

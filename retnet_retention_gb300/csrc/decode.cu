@@ -3,7 +3,9 @@
 //   S = gamma S + phi(k) v^T ;  z = gamma z + phi(k) ;  o = phi(q)^T S [/ (phi(q)^T z + eps)]
 //
 // "RetNet" (bembew), "Recurrent Representation"; "Linear attention"
-// (zerotofrontier 21.2), the decode step: update first, then read.
+// (zerotofrontier 21.2), the decode step: update first, then read.  With a
+// per-token decay, gamma is this step's a = e^(log a) of the (b, h) ("Linear
+// Attention, RWKV, and RetNet" 13.3, subsection 4: the gated decay G_t).
 //
 // The step is bound by HBM: every call reads and writes the whole fp32 state
 // (d_k * d_v * 8 bytes per head) and does 4 d_k d_v flops per head.  One CTA
@@ -28,7 +30,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int H, int dk, int dv,
-    int phi, int normalize, float eps, const __grid_constant__ KernelGammas g) {
+    int phi, int normalize, float eps, const float* __restrict__ log_a,
+    const __grid_constant__ KernelGammas g) {
     __shared__ float qf[256];
     __shared__ float kf[256];
     __shared__ float red[kThreads * 4];
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 
     const int bh = blockIdx.x;
     const int h = bh % H;
-    const float gam = g.gamma[h];
+    const float gam = log_a ? exp2f(log_a[bh] * 1.44269504088896341f) : g.gamma[h];
     const int tid = threadIdx.x;
     const int tpr = dv >> 2;           // threads per state row
     const int rpi = kThreads / tpr;    // rows per pass over the block
@@ -134,11 +137,12 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
     if (a.bf16) {
         decode_step_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
             (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
-            (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, g);
+            (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps,
+            a.log_a, g);
     } else {
         decode_step_kernel<float><<<grid, kThreads, 0, s>>>(
             (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.o, a.S, a.z,
-            a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, g);
+            a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, a.log_a, g);
     }
     return cudaGetLastError();
 }

@@ -27,6 +27,9 @@ struct ChunkArgs {
     bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     bool noncausal;
     float eps;
+    // per-token decay: device fp32 [B][H][T] natural logs, in place of the per-head
+    // gammas (null: the gammas)
+    const float* log_a;
     void* workspace;
     size_t workspace_bytes;
     int* dev_status;
@@ -45,6 +48,7 @@ struct StepArgs {
     bool normalize;
     bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     float eps;
+    const float* log_a;  // per-token decay: device fp32 [B][H] natural logs, or null
 };
 
 // Normaliser mode passed to the kernels: 0 none, 1 divide by phi(q)^T z + eps,
@@ -64,9 +68,9 @@ int simt_chunk_len(int requested, int dk);
 
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);
-size_t tc_workspace_bytes(int B, int H, int T, int dk, int dv, bool noncausal);
-// Kernel launches of one tensor-core chunkwise call (1, 2 or 3).
-int tc_launch_count(int B, int H, int T, int dk, int dv, bool noncausal, bool normalize);
+size_t tc_workspace_bytes(const ChunkArgs& a);
+// Kernel launches of one tensor-core chunkwise call (1 to 4).
+int tc_launch_count(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
                             int* launches);
 

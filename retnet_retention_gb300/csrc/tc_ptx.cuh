@@ -97,6 +97,17 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
     return mbar_wait_or_abort_slow(bar, parity, limit_ns, abort);
 }
 
+// A plain (untiled) bulk copy global -> shared of `bytes` bytes (both addresses
+// 16-byte aligned, bytes a multiple of 16), completing on `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :
+        : "r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents: the next kernel in the
 // stream (when launched with programmatic stream serialization) may be
 // scheduled once every CTA of this grid has issued it or exited.  wait: block

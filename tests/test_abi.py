@@ -64,7 +64,8 @@ def chunk(lib, **over):
 
 BAD_CHUNK_ARGS = [
     dict(B=-1), dict(H=-2), dict(T=-1), dict(dk=0), dict(dk=8), dict(dk=24), dict(dk=272),
-    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=16), dict(chunk=48), dict(chunk=256),
+    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=32), dict(chunk=48), dict(chunk=256),
+    dict(flags=la.LA_GATED),  # the per-token decay's planning flag: not a la_chunk_fwd flag
     dict(eps=float("nan")), dict(eps=-1.0), dict(Q=None), dict(V=None), dict(O=None),
     dict(Q=FAKE + 8), dict(O=FAKE + 0x400004), dict(S0=FAKE + 0x800004),
     dict(O=FAKE + 0x100000),  # O overlaps K
@@ -103,6 +104,37 @@ def test_workspace_size_is_a_host_query(lib):
         assert n >= 0 and n % 16 == 0
 
 
+def chunk_gated(lib, **over):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dtype=1, log_a=FAKE + 0x300000, B=2,
+             H=8, T=64, dk=64, dv=64, flags=0, eps=1e-6, S0=None, z0=None, O=FAKE + 0x400000,
+             S_out=None, z_out=None, chunk=0, ws=None, ws_bytes=0, st=None, stream=None)
+    a.update(over)
+    return lib.la_chunk_fwd_gated(a["Q"], a["K"], a["V"], a["dtype"], a["log_a"], a["B"],
+                                  a["H"], a["T"], a["dk"], a["dv"], a["flags"], a["eps"], a["S0"],
+                                  a["z0"], a["O"], a["S_out"], a["z_out"], a["chunk"], a["ws"],
+                                  a["ws_bytes"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [dict(log_a=None), dict(log_a=FAKE + 0x300004), dict(B=-1),
+                                  dict(dk=24), dict(flags=32), dict(Q=None), dict(eps=-1.0),
+                                  dict(log_a=FAKE + 0x400000)],  # O overlaps log_a
+                         ids=lambda d: ",".join(d))
+def test_chunk_fwd_gated_rejects(lib, over):
+    assert chunk_gated(lib, **over) == la.LA_ERR_INVALID_ARG
+
+
+def test_chunk_fwd_gated_noncausal_unsupported_and_empty_batch(lib):
+    assert chunk_gated(lib, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
+    assert chunk_gated(lib, B=0, Q=None, K=None, V=None, O=None, log_a=None) == la.LA_OK
+
+
+def test_workspace_size_takes_the_gated_flag(lib):
+    for (B, H, T, dk, dv) in [(4, 8, 4096, 64, 64), (1, 8, 65536, 128, 128)]:
+        n = lib.la_workspace_size(B, H, T, dk, dv, 1, la.LA_GATED, 0)
+        assert n >= 0 and n % 16 == 0
+    assert lib.la_workspace_size(4, 8, 4096, 64, 64, 1, 32, 0) == 0  # unknown flag
+
+
 def step(lib, **over):
     a = dict(q=FAKE, k=FAKE + 0x1000, v=FAKE + 0x2000, dtype=1, gamma=GAM.ctypes.data, B=2, H=8,
              dk=64, dv=64, flags=0, eps=1e-6, S=FAKE + 0x100000, z=None, o=FAKE + 0x200000,
@@ -124,6 +156,16 @@ def test_recurrent_step_rejects(lib, over):
 
 def test_recurrent_step_noncausal_unsupported(lib):
     assert step(lib, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
+
+
+def test_recurrent_step_gated_rejects(lib):
+    def call(log_a, flags=0):
+        return lib.la_recurrent_step_gated(FAKE, FAKE + 0x1000, FAKE + 0x2000, 1, log_a, 2, 8, 64,
+                                           64, flags, 1e-6, FAKE + 0x100000, None,
+                                           FAKE + 0x200000, None, None)
+    assert call(None) == la.LA_ERR_INVALID_ARG
+    assert call(FAKE + 0x300004) == la.LA_ERR_INVALID_ARG
+    assert call(FAKE + 0x300000, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
 
 
 def test_state_init_rejects(lib):

@@ -14,7 +14,12 @@ Recipe (the same for every workload):
     round-to-nearest-even ``.to(bfloat16)`` (fp32 workloads keep them);
   * per-head decays are fp32 numbers: fixed lists, the multi-scale schedule
     gamma_h = 1 - 2^(-5-h) (exact in fp32), or uniform draws from stream
-    [seed, 99].
+    [seed, 99];
+  * per-token log decays (workloads with a ``gate``): for each (b, h) a stream
+    [seed, 6, b, h] draws u ~ U[0, 2) per token, log a_t = u * log(gamma_h) in
+    fp32 (so the mean log decay is the head's log gamma), and one token in 64,
+    chosen by a second draw from the same stream, gets log a_t = -8 (a gate that
+    nearly resets the state).
 """
 from __future__ import annotations
 
@@ -27,6 +32,7 @@ import torch
 # tensor ids of the keyed streams
 Q_ID, K_ID, V_ID = 0, 1, 2
 DQ_ID, DK_ID, DV_ID = 3, 4, 5
+LOGA_ID = 6
 GAMMA_ID = 99
 
 #: The five workloads, then retention with the floored normaliser (xLSTM's
@@ -56,6 +62,11 @@ CONFIGS = {
         index=5, B=4, H=8, T=4096, dk=64, dv=64, dtype="bf16", phi=False, normalize=True,
         floor=True, causal=True, gamma=("msr", 8), scale_q=64 ** -0.5, scale_k=64 ** -0.5,
         scale_v=1.0, seed=5),
+    # per-token (gated) decay: the heads' gammas set the mean of the log decays
+    "gated_retention_bf16": dict(
+        index=6, B=4, H=16, T=4096, dk=128, dv=128, dtype="bf16", phi=False, normalize=False,
+        causal=True, gamma=("msr", 8), gate=True, scale_q=128 ** -0.5, scale_k=128 ** -0.5,
+        scale_v=1.0, seed=6),
 }
 
 _THREADS = max(1, min(16, (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
@@ -115,6 +126,22 @@ def gammas(cfg: dict) -> np.ndarray:
     return g
 
 
+def log_decays(seed: int, gamma: np.ndarray, B: int, T: int, pairs=None) -> np.ndarray:
+    """Per-token log decays [B,H,T] fp32 (or [len(pairs), T]) around the heads'
+    gammas; see the module docstring."""
+    H = gamma.shape[0]
+    keys = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    out = np.empty((len(keys), T), dtype=np.float32)
+    lg = np.log(gamma.astype(np.float64)).astype(np.float32)
+    for i, (b, h) in enumerate(keys):
+        rng = np.random.default_rng([seed, LOGA_ID, b, h])
+        u = rng.uniform(0.0, 2.0, T).astype(np.float32)
+        x = u * lg[h]
+        x[rng.integers(0, 64, T) == 0] = np.float32(-8.0)
+        out[i] = x
+    return out if pairs is not None else out.reshape(B, H, T)
+
+
 def _to(x: np.ndarray, dtype: str) -> torch.Tensor:
     t = torch.from_numpy(x)
     return t if dtype == "f32" else t.to(torch_dtype(dtype))
@@ -138,6 +165,8 @@ def make_inputs(cfg, pairs=None, T=None) -> dict:
     out = dict(q=_to(q, c["dtype"]), k=_to(k, c["dtype"]), v=_to(v, c["dtype"]), gamma=g)
     if pairs is not None:
         out["gamma_pairs"] = np.asarray([g[h] for (_, h) in pairs], dtype=np.float32)
+    if c.get("gate"):
+        out["log_a"] = torch.from_numpy(log_decays(s, g, B, T, pairs))
     return out
 
 
@@ -170,11 +199,12 @@ def decode_inputs_all(cfg, steps: int) -> dict:
 
 def random_case(seed: int, B: int, H: int, T: int, dk: int, dv: int, dtype: str = "f32",
                 gamma=None, phi: bool = False, normalize: bool = False, causal: bool = True,
-                scale: float | None = None) -> dict:
+                scale: float | None = None, gate: bool = False) -> dict:
     """A small seeded case in the same recipe, for parity and edge-case tests.
 
     gamma: None -> H draws from U[0.8, 1.0) (fp32); a float -> that value for
     every head; a list -> those values.  scale defaults to d_k^-1/2 for q, k.
+    gate: also draw per-token log decays around those gammas (``log_a``).
     """
     sc = dk ** -0.5 if scale is None else scale
     if gamma is None:
@@ -185,7 +215,7 @@ def random_case(seed: int, B: int, H: int, T: int, dk: int, dv: int, dtype: str 
     else:
         g = ("list", list(gamma))
     cfg = dict(B=B, H=H, T=T, dk=dk, dv=dv, dtype=dtype, phi=phi, normalize=normalize,
-               causal=causal, gamma=g, scale_q=sc, scale_k=sc, scale_v=1.0, seed=seed)
+               causal=causal, gamma=g, scale_q=sc, scale_k=sc, scale_v=1.0, seed=seed, gate=gate)
     out = make_inputs(cfg)
     out["cfg"] = cfg
     return out
@@ -215,5 +245,5 @@ def tokens(cfg) -> int:
 
 
 __all__ = ["CONFIGS", "make_inputs", "decode_inputs", "decode_inputs_all", "random_case",
-           "gammas", "sample_pairs", "shard_pairs", "normal_bhtd", "torch_dtype", "tokens"]
+           "gammas", "log_decays", "sample_pairs", "shard_pairs", "normal_bhtd", "torch_dtype", "tokens"]
 
