@@ -23,6 +23,12 @@ recurrent_gated(q, k, v, log_a, phi, normalize, eps, S0, z0)
     "Linear Attention, RWKV, and RetNet" (temporalbook 13.3, subsection 4)
     with the gate G_t = a_t 1 that depends on the token ("Efficient and Sparse
     Transformers", temporalbook 12.5, "Gated Linear Attention").
+recurrent_bwd(q, k, v, gamma, dO, ..., log_a, dS_T, dz_T)
+    Gradients of ``recurrent`` (dq, dk, dv and those of the initial state) for
+    the loss sum(dO * O) + <dS_T, S_T> + <dz_T, z_T>, as two sweeps of
+    cumulative sums, forward in time for the queries and backward for the keys
+    and values ("Linear attention" page, "Decoding, training, and what each
+    costs"); no state is stored.
 decode_step(q, k, v, gamma, S, z, phi, normalize, eps)
     One token of the same recurrence: the interview box "Causal linear
     attention, recurrent and parallel, plus the decode step" on the "Linear
@@ -62,6 +68,10 @@ def _load(path: str | None = None):
     lib.oracle_recurrent.restype = ctypes.c_int
     lib.oracle_recurrent_gated.argtypes = lib.oracle_recurrent.argtypes
     lib.oracle_recurrent_gated.restype = ctypes.c_int
+    lib.oracle_recurrent_bwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, dp,
+                                         dp, dp, dp, dp, dp]
+    lib.oracle_recurrent_bwd.restype = ctypes.c_int
     lib.oracle_noncausal.argtypes = [dp, dp, dp, L, L, L, L, L, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_double, dp, dp, dp]
     lib.oracle_noncausal.restype = ctypes.c_int
@@ -159,6 +169,41 @@ def recurrent_gated(q, k, v, log_a, phi: bool = False, normalize: bool = False,
     if rc != 0:
         raise MemoryError("oracle_recurrent_gated: scratch allocation failed")
     return O, S, z
+
+
+def recurrent_bwd(q, k, v, gamma, dO, phi: bool = False, normalize: bool = False,
+                  eps: float = 1e-6, S0=None, z0=None, dS_T=None, dz_T=None, _lib=None,
+                  floor: bool = False, log_a=None):
+    """Gradients of ``recurrent`` (or ``recurrent_gated`` with ``log_a``; then
+    gamma is ignored) for the loss sum(dO * O) + <dS_T, S_T> + <dz_T, z_T>.
+
+    Returns (dq, dk, dv, dS0, dz0) as float64 arrays of the inputs' shapes.
+    """
+    Q, K, V = _as4(_f64(q), "q"), _as4(_f64(k), "k"), _as4(_f64(v), "v")
+    B, H, T, dk = Q.shape
+    dv = V.shape[-1]
+    if K.shape != Q.shape or V.shape[:3] != Q.shape[:3]:
+        raise ValueError(f"shape mismatch q{Q.shape} k{K.shape} v{V.shape}")
+    G = np.ascontiguousarray(_f64(dO).reshape(B, H, T, dv))
+    g = None if log_a is not None else np.ascontiguousarray(
+        np.broadcast_to(_f64(gamma).reshape(-1), (H,)).astype(np.float64))
+    la = None if log_a is None else np.ascontiguousarray(_f64(log_a).reshape(B, H, T))
+    S0a = None if S0 is None else np.ascontiguousarray(_f64(S0).reshape(B, H, dk, dv))
+    z0a = None if z0 is None else np.ascontiguousarray(_f64(z0).reshape(B, H, dk))
+    dSa = None if dS_T is None else np.ascontiguousarray(_f64(dS_T).reshape(B, H, dk, dv))
+    dza = None if dz_T is None else np.ascontiguousarray(_f64(dz_T).reshape(B, H, dk))
+    dq = np.empty((B, H, T, dk))
+    dkk = np.empty((B, H, T, dk))
+    dvv = np.empty((B, H, T, dv))
+    dS0 = np.empty((B, H, dk, dv))
+    dz0 = np.empty((B, H, dk))
+    rc = (_lib or lib()).oracle_recurrent_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(la), B, H, T, dk, dv, int(bool(phi)),
+        _norm_mode(normalize, floor), float(eps), _ptr(S0a), _ptr(z0a), _ptr(G), _ptr(dSa),
+        _ptr(dza), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dS0), _ptr(dz0))
+    if rc != 0:
+        raise MemoryError("oracle_recurrent_bwd: scratch allocation failed")
+    return dq, dkk, dvv, dS0, dz0
 
 
 def decode_step(q, k, v, gamma, S, z=None, phi: bool = False, normalize: bool = False,

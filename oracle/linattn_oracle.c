@@ -213,6 +213,164 @@ int oracle_recurrent_gated(const double* Q, const double* K, const double* V,
 }
 
 /*
+ * Gradients of the causal recurrent form (the backward pass), for the loss
+ * L = sum_t do_t . o_t + <dS_T, S_T> + <dz_T, z_T>, in two sweeps and without
+ * storing the states: "Linear attention" (zerotofrontier 21.2), section
+ * "Decoding, training, and what each costs": the gradients are cumulative
+ * sums too, forward in time for the queries and backward in time for the keys
+ * and values (Katharopoulos et al.).  Written out from the recurrence by the
+ * chain rule:
+ *
+ *   forward sweep (t = 0 .. T-1), with S_t, z_t as in the forward pass:
+ *       n_t = q~_t S_t,  u_t = q~_t . z_t,  den_t = u_t + eps or max(|u_t|, 1)
+ *       dn_t = do_t / den_t            (do_t without the normaliser)
+ *       du_t = -(do_t . n_t) / den_t^2 * dden/du   (dden/du = 1, or sign(u_t)
+ *              where |u_t| > 1 and 0 elsewhere for the floor)
+ *       dq~_t = S_t dn_t + du_t z_t   (a d_k vector: row i of S_t times dn_t)
+ *   backward sweep (t = T-1 .. 0), G = dL/dS_t and Gz = dL/dz_t:
+ *       G += q~_t^T dn_t,  Gz += du_t q~_t
+ *       dv_t = k~_t^T G (a d_v vector),  dk~_t = G v_t + Gz
+ *       G = a_t G,  Gz = a_t Gz      (a_t = gamma, or the per-token decay)
+ *   and dS_0 = G, dz_0 = Gz after the sweep (gradients of the initial state).
+ *   phi: dq = dq~ * phi'(q), phi'(x) = 1 for x > 0, e^x otherwise.
+ *
+ *   dO : [B][H][T][dv];  dS_T : [B][H][dk][dv] or NULL;  dz_T : [B][H][dk] or NULL
+ *   dQ, dK : [B][H][T][dk];  dV : [B][H][T][dv];  dS0 : [B][H][dk][dv] or NULL;
+ *   dz0 : [B][H][dk] or NULL.  gamma / log_a, S0, z0 and the flags as in the
+ *   forward pass.  Returns 0, or -1 when a scratch allocation fails.
+ */
+static double phi_grad(double x) { return x > 0.0 ? 1.0 : exp(x); }
+
+static int recurrent_bwd(const double* Q, const double* K, const double* V,
+                         const double* gamma, const double* log_a, long B, long H, long T,
+                         long dk, long dv, int phi, int normalize, double eps,
+                         const double* S0, const double* z0, const double* dO,
+                         const double* dS_T, const double* dz_T,
+                         double* dQ, double* dK, double* dV, double* dS0, double* dz0)
+{
+    int failed = 0;
+    long BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (long bh = 0; bh < BH; ++bh) {
+        const long h = bh % H;
+        double* S = (double*)malloc(sizeof(double) * (size_t)(dk * dv));
+        double* z = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* qf = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* kf = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* n = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* den = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double* du = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        if (!S || !z || !qf || !kf || !n || !den || !du) {
+            failed = 1;
+            free(S); free(z); free(qf); free(kf); free(n); free(den); free(du);
+            continue;
+        }
+        /* ---- forward sweep: the states, the denominators, dq */
+        if (S0) memcpy(S, S0 + bh * dk * dv, sizeof(double) * (size_t)(dk * dv));
+        else memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+        if (z0) memcpy(z, z0 + bh * dk, sizeof(double) * (size_t)dk);
+        else memset(z, 0, sizeof(double) * (size_t)dk);
+        for (long t = 0; t < T; ++t) {
+            const double* q = Q + (bh * T + t) * dk;
+            const double* k = K + (bh * T + t) * dk;
+            const double* v = V + (bh * T + t) * dv;
+            const double* g_o = dO + (bh * T + t) * dv;
+            const double g = log_a ? exp(log_a[bh * T + t]) : gamma[h];
+            feature(q, qf, dk, phi);
+            feature(k, kf, dk, phi);
+            for (long i = 0; i < dk; ++i) {
+                for (long j = 0; j < dv; ++j) S[i * dv + j] = g * S[i * dv + j] + kf[i] * v[j];
+                z[i] = g * z[i] + kf[i];
+            }
+            double u = 0.0;
+            for (long i = 0; i < dk; ++i) u += qf[i] * z[i];
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += qf[i] * S[i * dv + j];
+                n[j] = acc;
+            }
+            double d = 1.0, dd_du = 0.0;
+            if (normalize == 1) {
+                d = u + eps;
+                dd_du = 1.0;
+            } else if (normalize == 2) {
+                d = fabs(u) > 1.0 ? fabs(u) : 1.0;
+                dd_du = fabs(u) > 1.0 ? (u > 0.0 ? 1.0 : -1.0) : 0.0;
+            }
+            double don = 0.0;
+            for (long j = 0; j < dv; ++j) don += g_o[j] * n[j];
+            den[t] = d;
+            du[t] = normalize ? -don / (d * d) * dd_du : 0.0;
+            double* gq = dQ + (bh * T + t) * dk;
+            for (long i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; ++j) acc += S[i * dv + j] * g_o[j];
+#if ORACLE_MUTANT == 11 /* mutant: dq without the normaliser's term */
+                gq[i] = acc / d;
+#else
+                gq[i] = acc / d + du[t] * z[i];
+#endif
+                if (phi) gq[i] *= phi_grad(q[i]);
+            }
+        }
+        /* ---- backward sweep: G = dL/dS_t, Gz = dL/dz_t */
+        double* G = S;  /* the forward states are no longer needed */
+        double* Gz = z;
+        if (dS_T) memcpy(G, dS_T + bh * dk * dv, sizeof(double) * (size_t)(dk * dv));
+        else memset(G, 0, sizeof(double) * (size_t)(dk * dv));
+        if (dz_T) memcpy(Gz, dz_T + bh * dk, sizeof(double) * (size_t)dk);
+        else memset(Gz, 0, sizeof(double) * (size_t)dk);
+        for (long t = T - 1; t >= 0; --t) {
+            const double* q = Q + (bh * T + t) * dk;
+            const double* k = K + (bh * T + t) * dk;
+            const double* v = V + (bh * T + t) * dv;
+            const double* g_o = dO + (bh * T + t) * dv;
+            const double g = log_a ? exp(log_a[bh * T + t]) : gamma[h];
+            feature(q, qf, dk, phi);
+            feature(k, kf, dk, phi);
+            for (long i = 0; i < dk; ++i) {
+                for (long j = 0; j < dv; ++j) G[i * dv + j] += qf[i] * g_o[j] / den[t];
+                Gz[i] += du[t] * qf[i];
+            }
+            double* gv = dV + (bh * T + t) * dv;
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += kf[i] * G[i * dv + j];
+                gv[j] = acc;
+            }
+            double* gk = dK + (bh * T + t) * dk;
+            for (long i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; ++j) acc += G[i * dv + j] * v[j];
+                gk[i] = acc + Gz[i];
+                if (phi) gk[i] *= phi_grad(k[i]);
+            }
+#if ORACLE_MUTANT != 10 /* mutant 10: the reverse sweep forgets the decay */
+            for (long i = 0; i < dk; ++i) {
+                for (long j = 0; j < dv; ++j) G[i * dv + j] *= g;
+                Gz[i] *= g;
+            }
+#endif
+        }
+        if (dS0) memcpy(dS0 + bh * dk * dv, G, sizeof(double) * (size_t)(dk * dv));
+        if (dz0) memcpy(dz0 + bh * dk, Gz, sizeof(double) * (size_t)dk);
+        free(S); free(z); free(qf); free(kf); free(n); free(den); free(du);
+    }
+    return failed ? -1 : 0;
+}
+
+int oracle_recurrent_bwd(const double* Q, const double* K, const double* V,
+                         const double* gamma, const double* log_a, long B, long H, long T,
+                         long dk, long dv, int phi, int normalize, double eps,
+                         const double* S0, const double* z0, const double* dO,
+                         const double* dS_T, const double* dz_T,
+                         double* dQ, double* dK, double* dV, double* dS0, double* dz0)
+{
+    return recurrent_bwd(Q, K, V, gamma, log_a, B, H, T, dk, dv, phi, normalize, eps, S0, z0,
+                         dO, dS_T, dz_T, dQ, dK, dV, dS0, dz0);
+}
+
+/*
  * Non-causal form (gamma = 1 only): one summary shared by every query.
  *   S = sum_t k~_t v_t^T,  z = sum_t k~_t,  o_t = q~_t^T S [ / (q~_t^T z + eps) ]
  *   (or / max(|q~_t^T z|, 1) with normalize == 2)

@@ -339,12 +339,79 @@ def pin_gated_chunkwise(lib=None):
         assert pins.rel_err(zc, z) < 1e-12
 
 
+def _loss_and_grads(q, k, v, gamma, W, WS, Wz, phi, normalize, floor, S0, z0, log_a, lib):
+    """L = sum(W * O) + <WS, S_T> + <Wz, z_T> by the forward oracle, and its gradients
+    by the backward oracle (dO = W, dS_T = WS, dz_T = Wz)."""
+    def loss(q_, k_, v_, S0_, z0_):
+        if log_a is None:
+            O, S, z = oracle.recurrent(q_, k_, v_, gamma, phi=phi, normalize=normalize,
+                                       floor=floor, S0=S0_, z0=z0_, _lib=lib)
+        else:
+            O, S, z = oracle.recurrent_gated(q_, k_, v_, log_a, phi=phi, normalize=normalize,
+                                             floor=floor, S0=S0_, z0=z0_, _lib=lib)
+        return float((W * O).sum() + (WS * S).sum() + (Wz * z).sum())
+    grads = oracle.recurrent_bwd(q, k, v, gamma, W, phi=phi, normalize=normalize, floor=floor,
+                                 S0=S0, z0=z0, dS_T=WS, dz_T=Wz, _lib=lib, log_a=log_a)
+    return loss, grads
+
+
+def _check_by_differences(loss, args, grads, h=1e-6, rtol=2e-6):
+    """Central differences of the loss in every element of every argument."""
+    for a, g in zip(args, grads):
+        num = np.zeros_like(a)
+        it = np.nditer(a, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = a[idx]
+            a[idx] = old + h
+            lp = loss(*args)
+            a[idx] = old - h
+            lm = loss(*args)
+            a[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(num - g)) / max(np.max(np.abs(num)), 1e-30)
+        assert err < rtol, f"gradient differs from the central differences: {err:.2e}"
+
+
+def pin_backward_by_differences(lib=None):
+    """The backward sweeps against central differences of the forward oracle, for
+    plain, phi + normaliser and floored read-outs, an initial state and a final-state
+    gradient, and a per-token decay."""
+    rng = _rng(51)
+    B, H, T, dk, dv = 1, 2, 7, 3, 4
+    for phi, norm, floor, gated in ((False, False, False, False), (True, True, False, False),
+                                    (False, False, True, False), (True, True, False, True)):
+        q = rng.standard_normal((B, H, T, dk)) * (0.6 if floor else 0.8)
+        k = rng.standard_normal((B, H, T, dk)) * (0.6 if floor else 0.8)
+        v = rng.standard_normal((B, H, T, dv))
+        S0 = rng.standard_normal((B, H, dk, dv)) * 0.5
+        z0 = np.abs(rng.standard_normal((B, H, dk))) * (0.3 if floor else 1.0) + (0.0 if floor else 0.5)
+        W = rng.standard_normal((B, H, T, dv))
+        WS = rng.standard_normal((B, H, dk, dv))
+        Wz = rng.standard_normal((B, H, dk))
+        gamma = np.array([0.9, 0.97])
+        log_a = -rng.exponential(0.2, (B, H, T)) if gated else None
+        loss, (dq, dk_, dv_, dS0, dz0) = _loss_and_grads(q, k, v, gamma, W, WS, Wz, phi, norm,
+                                                         floor, S0, z0, log_a, lib)
+        if floor:  # the differences must not straddle the floor's kink |q~^T z| = 1
+            us = []
+            for h in range(H):
+                zz = z0[0, h].copy()
+                for t in range(T):
+                    zz = gamma[h] * zz + k[0, h, t]
+                    us.append(abs(q[0, h, t] @ zz))
+            us = np.array(us)
+            assert np.all(np.abs(us - 1.0) > 1e-3)
+            assert (us < 1).any() and (us > 1).any()  # both sides of the floor
+        _check_by_differences(loss, [q, k, v, S0, z0], [dq, dk_, dv_, dS0, dz0])
+
+
 ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
             pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
             pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
             pin_chunkwise_invariance, pin_state_handoff, pin_floor_clamped_rows,
             pin_floor_limits, pin_gated_parallel_form, pin_gated_constant_is_gamma,
-            pin_gated_reset, pin_gated_chunkwise]
+            pin_gated_reset, pin_gated_chunkwise, pin_backward_by_differences]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -424,6 +491,8 @@ MUTANTS = {
     7: "normaliser over the wrong axis",
     8: "floor without the absolute value",
     9: "per-token gate one token late",
+    10: "backward sweep without the decay",
+    11: "dq without the normaliser's term",
 }
 
 
