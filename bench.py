@@ -300,6 +300,53 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
     return res
 
 
+def bwd_bytes(c: dict) -> int:
+    """Backward pass: read Q, K, V, dO, write dQ, dK, dV, and the initial state's
+    gradient; with the normaliser the per-token denominators are written and
+    read once (8 + 8 bytes per head-token)."""
+    es = 2 if c["dtype"] == "bf16" else 4
+    nbh = c["B"] * c["H"]
+    per_tok = (2 * c["dk"] + 2 * c["dv"]) * es + (2 * c["dk"] + c["dv"]) * es
+    if c["normalize"]:
+        per_tok += 16
+    return nbh * c["T"] * per_tok + nbh * c["dk"] * c["dv"] * 4
+
+
+def bwd_measure(la, name: str, steps: int, warmup: int, rank: int, world: int) -> dict:
+    """The backward pass (la_chunk_bwd) of a workload, with a seeded N(0,1) dO."""
+    c = dict(workloads.CONFIGS[name])
+    B, H, T = c["B"], c["H"], c["T"]
+    pairs = workloads.shard_pairs(rank, world, B, H)
+    cw = dict(c)
+    cw["B"] = B * world
+    x = workloads.make_inputs(cw, pairs=pairs)
+    dev = torch.device("cuda")
+    q = x["q"].reshape(B, H, T, c["dk"]).to(dev)
+    k = x["k"].reshape(B, H, T, c["dk"]).to(dev)
+    v = x["v"].reshape(B, H, T, c["dv"]).to(dev)
+    dO = torch.from_numpy(workloads.normal_bhtd(c["seed"] + 100, workloads.V_ID, B, H, T, c["dv"],
+                                                1.0)).to(q.dtype).to(dev)
+    gamma = x["gamma"]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(16, la.library().la_bwd_workspace_size(
+        B, H, T, c["dk"], c["dv"], 1 if c["dtype"] == "bf16" else 0,
+        la.LA_NORMALIZE if c["normalize"] else 0)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        la.chunk_bwd(q, k, v, dO, gamma, phi=c["phi"], normalize=c["normalize"], dq=dq, dk=dk,
+                     dv=dv, workspace=ws, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    ms = time_region(step, steps, stream)
+    res = dict(name=name, config=c, ms=ms / steps, tokens=B * T, bytes=bwd_bytes(c),
+               kernels=kernel_breakdown(la, step, steps, stream))
+    del q, k, v, dO, dq, dk, dv
+    torch.cuda.empty_cache()
+    return res
+
+
 def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> dict:
     name = "decode_bf16"
     c = dict(workloads.CONFIGS[name])
@@ -402,6 +449,12 @@ def run_ours(args) -> dict | None:
             print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
                               "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
         return None
+    if only == "backward":  # profiling aid: the headline's backward pass alone
+        r = bwd_measure(la, HEADLINE, args.steps, args.warmup, rank, world)
+        if rank == 0:
+            print(json.dumps({"only": "backward", "ms": r["ms"],
+                              "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
+        return None
     if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
                 "gated_retention_bf16"):  # profiling aid
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
@@ -426,6 +479,8 @@ def run_ours(args) -> dict | None:
             others[name] = r
         dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         dec["ms"] = max_over_ranks(dec["ms"])
+        bwd = bwd_measure(la, HEADLINE, 3, 1, rank, world)
+        bwd["ms"] = max_over_ranks(bwd["ms"])
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -496,6 +551,13 @@ def run_ours(args) -> dict | None:
                              roofline_frac=kgbs / pk["hbm_gbs"], kernels=r["kernels"])
         dc = dec["config"]
         gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
+        bc = bwd["config"]
+        gbs = bwd["bytes"] / (bwd["ms"] * 1e-3) / 1e9
+        sub["backward_" + HEADLINE] = dict(
+            workload="backward of " + describe(HEADLINE, bc) + " (gradients of Q, K, V and of "
+                     "the initial state for a seeded N(0,1) dO)",
+            tokens_per_s=bwd["tokens"] * world / (bwd["ms"] * 1e-3), ms=bwd["ms"], alg_gbs=gbs,
+            roofline_frac=gbs / pk["hbm_gbs"], kernels=bwd["kernels"])
         sub["decode_bf16"] = dict(
             workload=f"decode_bf16: B={dc['B']} H={dc['H']} d_k={dc['dk']} d_v={dc['dv']} fp32 "
                      f"state after a {dc['T']}-token prefill, {dec['steps']} steps",
@@ -564,7 +626,8 @@ def main(argv=None):
                     help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
-                                       "retention_floor_bf16", "gated_retention_bf16", "decode"),
+                                       "retention_floor_bf16", "gated_retention_bf16", "decode",
+                                       "backward"),
                     default=None,
                     help="profiling aid: run one workload only")
     ap.add_argument("--decode-steps", type=int,

@@ -239,6 +239,51 @@ LA_API la_status la_recurrent_step_gated(const void* q, const void* k, const voi
                                          int* dev_status, la_stream_t stream);
 
 /*
+ * Backward pass: the gradients of la_chunk_fwd's outputs, for the loss
+ *   L = sum_t dO_t . o_t + <dS_T, S_T> + <dz_T, z_T>
+ * with respect to Q, K, V and the initial state.  "Linear attention"
+ * (zerotofrontier 21.2), "Decoding, training, and what each costs": the
+ * gradients are cumulative sums too, forward in time for the queries and
+ * backward in time for the keys and values, so no intermediate state is
+ * stored (the states are recomputed, chunk by chunk).
+ *
+ *   Q, K, V, gamma, flags, eps, S0, z0   as the forward call that made O (flags:
+ *          LA_PHI_ELU1, LA_NORMALIZE, LA_NORM_FLOOR; LA_NONCAUSAL is
+ *          LA_ERR_UNSUPPORTED)
+ *   dO     [B][H][T][d_v] dtype: the loss's gradient with respect to O
+ *   dS_T   [B][H][d_k][d_v] fp32 or NULL (zero); dz_T [B][H][d_k] fp32 or NULL
+ *   dQ, dK [B][H][T][d_k] dtype, dV [B][H][T][d_v] dtype: outputs (may not
+ *          overlap any input)
+ *   dS0    [B][H][d_k][d_v] fp32 or NULL, dz0 [B][H][d_k] fp32 or NULL: the
+ *          initial state's gradients
+ *   workspace: at least la_bwd_workspace_size(...) bytes (per-token
+ *          denominators when normalising; 0 otherwise)
+ * d_k and d_v must be at most 128 (LA_ERR_UNSUPPORTED otherwise).  The
+ * computation runs in fp32 on the CUDA cores.  Errors as la_chunk_fwd.
+ */
+LA_API la_status la_chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                              la_dtype dtype, const float* gamma, int B, int H, int T, int d_k,
+                              int d_v, unsigned flags, float eps, const float* S0,
+                              const float* z0, const float* dS_T, const float* dz_T, void* dQ,
+                              void* dK, void* dV, float* dS0, float* dz0, void* workspace,
+                              size_t workspace_bytes, int* dev_status, la_stream_t stream);
+
+/* la_chunk_bwd with the per-token decay of la_chunk_fwd_gated (log_a: DEVICE
+ * fp32 [B][H][T]) in place of gamma.  The decays themselves get no gradient. */
+LA_API la_status la_chunk_bwd_gated(const void* Q, const void* K, const void* V, const void* dO,
+                                    la_dtype dtype, const float* log_a, int B, int H, int T,
+                                    int d_k, int d_v, unsigned flags, float eps,
+                                    const float* S0, const float* z0, const float* dS_T,
+                                    const float* dz_T, void* dQ, void* dK, void* dV,
+                                    float* dS0, float* dz0, void* workspace,
+                                    size_t workspace_bytes, int* dev_status, la_stream_t stream);
+
+/* Bytes of workspace la_chunk_bwd needs (pure host arithmetic; 0 for arguments
+ * it would reject). */
+LA_API size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
+                                    unsigned flags);
+
+/*
  * la_chunk_fwd for callers that cannot allocate device memory.  The source
  * pages have no counterpart to this entry point.
  *

@@ -9,6 +9,7 @@ Names follow the C ABI:
   state_init(S, z=None)                        zero a state        (la_state_init)
   chunk_fwd(q, k, v, gamma, ...)               prefill / forward   (la_chunk_fwd)
   chunk_fwd(q, k, v, log_a=..., ...)           per-token decay     (la_chunk_fwd_gated)
+  chunk_bwd(q, k, v, dO, gamma, ...)           gradients           (la_chunk_bwd[_gated])
   recurrent_step(q, k, v, gamma, S, z, ...)    one decode step     (la_recurrent_step)
   recurrent_step(q, k, v, None, S, z, log_a=)  per-token decay     (la_recurrent_step_gated)
   workspace_size(...)                          scratch bytes       (la_workspace_size)
@@ -82,6 +83,13 @@ def _load() -> ctypes.CDLL:
     lib.la_chunk_fwd_gated.restype = i
     lib.la_recurrent_step_gated.argtypes = lib.la_recurrent_step.argtypes
     lib.la_recurrent_step_gated.restype = i
+    lib.la_chunk_bwd.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
+                                 vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.la_chunk_bwd.restype = i
+    lib.la_chunk_bwd_gated.argtypes = lib.la_chunk_bwd.argtypes
+    lib.la_chunk_bwd_gated.restype = i
+    lib.la_bwd_workspace_size.argtypes = [i, i, i, i, i, i, u]
+    lib.la_bwd_workspace_size.restype = sz
     lib.la_chunk_fwd_launches.argtypes = [i, i, i, i, i, i, u, i]
     lib.la_chunk_fwd_launches.restype = i
     lib.la_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
@@ -268,6 +276,49 @@ def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps
     return out
 
 
+def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, S0=None,
+              z0=None, dS_T=None, dz_T=None, dq=None, dk=None, dv=None, state_grads=True,
+              workspace=None, stream=None, floor=False, log_a=None):
+    """Gradients of chunk_fwd for the loss sum(dO * O) + <dS_T, S_T> + <dz_T, z_T>.
+
+    q, k, v, gamma (or log_a), the flags and S0, z0 as in the forward call; dO
+    [B,H,T,dv] like v.  Returns (dq, dk, dv, dS0, dz0); dS0 / dz0 are None when
+    state_grads is False (dz0 also without the normaliser)."""
+    normalize = normalize or floor
+    B, H, T, dk_ = q.shape
+    dv_ = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or dO.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, dO")
+    if not (q.dtype == k.dtype == v.dtype == dO.dtype):
+        raise TypeError("q, k, v, dO must share one dtype")
+    if (gamma is None) == (log_a is None):
+        raise ValueError("pass exactly one of gamma and log_a")
+    dt = _dtype_code(q)
+    dev = q.device
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dS0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=dev) if state_grads else None
+    dz0 = (torch.empty((B, H, dk_), dtype=torch.float32, device=dev)
+           if state_grads and normalize else None)
+    flags = _flags(phi, normalize, True, floor)
+    lib = _load()
+    need = int(lib.la_bwd_workspace_size(B, H, T, dk_, dv_, dt, flags))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(dO), dt)
+    rest = (B, H, T, dk_, dv_, flags, float(eps), _ptr(S0), _ptr(z0), _ptr(dS_T), _ptr(dz_T),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes,
+            None, _stream(stream))
+    if log_a is None:
+        g = _gamma_host(gamma, H)
+        _check(lib.la_chunk_bwd(*args, g.ctypes.data, *rest), "la_chunk_bwd")
+    else:
+        _check(lib.la_chunk_bwd_gated(*args, _ptr(log_a), *rest), "la_chunk_bwd_gated")
+    return dq, dk, dv, dS0, dz0
+
+
 _SIDE_STREAMS: dict = {}
 
 
@@ -349,7 +400,7 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
     return out, S_out, z_out
 
 
-__all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
+__all__ = ["chunk_fwd", "chunk_bwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
            "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
            "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED"]

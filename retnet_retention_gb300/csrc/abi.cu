@@ -249,9 +249,104 @@ la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype d
     return cuda_status(launch_decode_step(a, g, (cudaStream_t)stream));
 }
 
+la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO, la_dtype dtype,
+                    const float* gamma, const float* log_a, int B, int H, int T, int d_k,
+                    int d_v, unsigned flags, float eps, const float* S0, const float* z0,
+                    const float* dS_T, const float* dz_T, void* dQ, void* dK, void* dV,
+                    float* dS0, float* dz0, void* workspace, size_t workspace_bytes,
+                    la_stream_t stream) {
+    const bool gated = gamma == nullptr;
+    if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+    const size_t nbh = (size_t)B * H;
+    if (nbh == 0) return LA_OK;
+    KernelGammas g;
+    bool all_one = true;
+    if (gated) {
+        std::memset(&g, 0, sizeof(g));
+    } else if (!fill_gammas(gamma, H, &g, &all_one)) {
+        return LA_ERR_INVALID_ARG;
+    }
+    if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
+    if (d_k > 128 || d_v > 128) return LA_ERR_UNSUPPORTED;
+    const bool floor_norm = (flags & LA_NORM_FLOOR) != 0;
+    const bool normalize = (flags & LA_NORMALIZE) != 0 || floor_norm;
+    const size_t es = elem_size(dtype);
+    const size_t n_qk = nbh * (size_t)T * d_k * es, n_v = nbh * (size_t)T * d_v * es;
+    if (T > 0) {
+        if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return LA_ERR_INVALID_ARG;
+        for (const void* p : {Q, K, V, dO, (const void*)dQ, (const void*)dK, (const void*)dV})
+            if (!aligned16(p)) return LA_ERR_INVALID_ARG;
+        if (gated && (!log_a || !aligned16(log_a))) return LA_ERR_INVALID_ARG;
+        const void* ins[5] = {Q, K, V, dO, log_a};
+        const size_t nin[5] = {n_qk, n_qk, n_v, n_v, gated ? nbh * T * 4 : 0};
+        const void* outs[3] = {dQ, dK, dV};
+        const size_t nout[3] = {n_qk, n_qk, n_v};
+        for (int o = 0; o < 3; ++o) {
+            for (int i = 0; i < 5; ++i)
+                if (overlaps(outs[o], nout[o], ins[i], nin[i])) return LA_ERR_INVALID_ARG;
+            for (int o2 = o + 1; o2 < 3; ++o2)
+                if (overlaps(outs[o], nout[o], outs[o2], nout[o2])) return LA_ERR_INVALID_ARG;
+        }
+    }
+    for (const void* p : {(const void*)S0, (const void*)z0, (const void*)dS_T, (const void*)dz_T,
+                          (const void*)dS0, (const void*)dz0, (const void*)workspace})
+        if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+    if (workspace_bytes < bwd_workspace_bytes(B, H, T, normalize)) return LA_ERR_INVALID_ARG;
+    if (normalize && T > 0 && !workspace) return LA_ERR_INVALID_ARG;
+
+    BwdArgs a;
+    a.Q = Q; a.K = K; a.V = V; a.dO = dO;
+    a.S0 = S0; a.z0 = z0; a.dS_T = dS_T; a.dz_T = dz_T;
+    a.dQ = dQ; a.dK = dK; a.dV = dV; a.dS0 = dS0; a.dz0 = dz0;
+    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.normalize = normalize;
+    a.floor_norm = floor_norm;
+    a.eps = eps;
+    a.log_a = gated ? log_a : nullptr;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return cuda_status(launch_chunk_bwd_simt(a, g, (cudaStream_t)stream));
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
+                             unsigned flags) {
+    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || d_k > 128 || d_v > 128) return 0;
+    return bwd_workspace_bytes(B, H, T, (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0);
+}
+
+la_status la_chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                       la_dtype dtype, const float* gamma, int B, int H, int T, int d_k, int d_v,
+                       unsigned flags, float eps, const float* S0, const float* z0,
+                       const float* dS_T, const float* dz_T, void* dQ, void* dK, void* dV,
+                       float* dS0, float* dz0, void* workspace, size_t workspace_bytes,
+                       int* dev_status, la_stream_t stream) {
+    (void)dev_status;  // the backward kernels have no device-side waits
+    if (!gamma && (size_t)B * H > 0 && B > 0 && H > 0) return LA_ERR_INVALID_ARG;
+    if (!gamma) gamma = &kOneGamma;
+    return chunk_bwd(Q, K, V, dO, dtype, gamma, nullptr, B, H, T, d_k, d_v, flags, eps, S0, z0,
+                     dS_T, dz_T, dQ, dK, dV, dS0, dz0, workspace, workspace_bytes, stream);
+}
+
+la_status la_chunk_bwd_gated(const void* Q, const void* K, const void* V, const void* dO,
+                             la_dtype dtype, const float* log_a, int B, int H, int T, int d_k,
+                             int d_v, unsigned flags, float eps, const float* S0, const float* z0,
+                             const float* dS_T, const float* dz_T, void* dQ, void* dK, void* dV,
+                             float* dS0, float* dz0, void* workspace, size_t workspace_bytes,
+                             int* dev_status, la_stream_t stream) {
+    (void)dev_status;
+    return chunk_bwd(Q, K, V, dO, dtype, nullptr, log_a, B, H, T, d_k, d_v, flags, eps, S0, z0,
+                     dS_T, dz_T, dQ, dK, dV, dS0, dz0, workspace, workspace_bytes, stream);
+}
 
 la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
                        const float* gamma, int B, int H, int T, int d_k, int d_v,

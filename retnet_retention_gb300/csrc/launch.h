@@ -51,6 +51,32 @@ struct StepArgs {
     const float* log_a;  // per-token decay: device fp32 [B][H] natural logs, or null
 };
 
+// Arguments of one backward pass (gradients), validated by the ABI layer.
+struct BwdArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const void* dO;
+    const float* S0;    // may be null
+    const float* z0;    // may be null
+    const float* dS_T;  // may be null (zero)
+    const float* dz_T;  // may be null (zero)
+    void* dQ;
+    void* dK;
+    void* dV;
+    float* dS0;         // may be null
+    float* dz0;         // may be null
+    int B, H, T, dk, dv;
+    bool bf16;
+    bool phi;
+    bool normalize;
+    bool floor_norm;
+    float eps;
+    const float* log_a;  // per-token decay, or null
+    void* workspace;     // the forward sweep's per-token den, du (normalising)
+    size_t workspace_bytes;
+};
+
 // Normaliser mode passed to the kernels: 0 none, 1 divide by phi(q)^T z + eps,
 // 2 divide by max(|phi(q)^T z|, 1).
 inline int norm_mode(bool normalize, bool floor_norm) { return normalize ? (floor_norm ? 2 : 1) : 0; }
@@ -65,6 +91,10 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
 // chunk_simt.cu: the fp32 SIMT chunkwise kernel (any supported shape)
 cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s);
 int simt_chunk_len(int requested, int dk);
+
+// chunk_bwd_simt.cu: the backward pass on the CUDA cores (d_k, d_v <= 128)
+cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s);
+size_t bwd_workspace_bytes(int B, int H, int T, bool normalize);
 
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);

@@ -135,6 +135,42 @@ def test_workspace_size_takes_the_gated_flag(lib):
     assert lib.la_workspace_size(4, 8, 4096, 64, 64, 1, 32, 0) == 0  # unknown flag
 
 
+def bwd(lib, gated=False, **over):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dO=FAKE + 0x300000, dtype=1,
+             gamma=GAM.ctypes.data, log_a=FAKE + 0x900000, B=2, H=8, T=64, dk=64, dv=64, flags=0,
+             eps=1e-6, S0=None, z0=None, dST=None, dzT=None, dQ=FAKE + 0x400000,
+             dK=FAKE + 0x500000, dV=FAKE + 0x600000, dS0=None, dz0=None, ws=None, ws_bytes=0,
+             st=None, stream=None)
+    a.update(over)
+    fn = lib.la_chunk_bwd_gated if gated else lib.la_chunk_bwd
+    return fn(a["Q"], a["K"], a["V"], a["dO"], a["dtype"], a["log_a"] if gated else a["gamma"],
+              a["B"], a["H"], a["T"], a["dk"], a["dv"], a["flags"], a["eps"], a["S0"], a["z0"],
+              a["dST"], a["dzT"], a["dQ"], a["dK"], a["dV"], a["dS0"], a["dz0"], a["ws"],
+              a["ws_bytes"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [dict(B=-1), dict(dk=24), dict(dtype=3), dict(flags=32),
+                                  dict(dO=None), dict(dQ=None), dict(dK=FAKE + 0x500008),
+                                  dict(dQ=FAKE + 0x300000),   # dQ overlaps dO
+                                  dict(dV=FAKE + 0x400000),   # dV overlaps dQ
+                                  dict(flags=la.LA_NORMALIZE),  # no workspace for the denominators
+                                  dict(eps=-1.0)],
+                         ids=lambda d: ",".join(d))
+def test_chunk_bwd_rejects(lib, over):
+    assert bwd(lib, **over) == la.LA_ERR_INVALID_ARG
+
+
+def test_chunk_bwd_unsupported_and_sizes(lib):
+    assert bwd(lib, flags=la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
+    assert bwd(lib, dk=256) == la.LA_ERR_UNSUPPORTED
+    assert bwd(lib, gated=True, log_a=None) == la.LA_ERR_INVALID_ARG
+    assert bwd(lib, B=0, Q=None, K=None, V=None, dO=None, dQ=None, dK=None, dV=None) == la.LA_OK
+    n = lib.la_bwd_workspace_size(2, 8, 64, 64, 64, 1, la.LA_NORMALIZE)
+    assert n == 2 * 8 * 64 * 2 * 4
+    assert lib.la_bwd_workspace_size(2, 8, 64, 64, 64, 1, 0) == 0
+    assert lib.la_bwd_workspace_size(2, 8, 64, 256, 64, 1, 0) == 0  # unsupported
+
+
 def step(lib, **over):
     a = dict(q=FAKE, k=FAKE + 0x1000, v=FAKE + 0x2000, dtype=1, gamma=GAM.ctypes.data, B=2, H=8,
              dk=64, dv=64, flags=0, eps=1e-6, S=FAKE + 0x100000, z=None, o=FAKE + 0x200000,

@@ -1,0 +1,132 @@
+"""The backward pass (la_chunk_bwd) on the GPU against the fp64 oracle.
+
+The loss is L = sum(dO * O) + <dS_T, S_T> + <dz_T, z_T>; the gradients of Q,
+K, V and of the initial state are compared with the oracle's two sweeps of
+cumulative sums ("Linear attention" page, "Decoding, training, and what each
+costs"), which are themselves pinned by central differences.  Shapes cover one
+and several chunks, ragged tails, d_k != d_v, the widest supported state (128 x
+128), phi with the normaliser, the floored normaliser, per-head and per-token
+decays, and an initial state with a final-state gradient.  Same metric and
+tolerances as the forward parity tests.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+import workloads
+
+la = pytest.importorskip("retnet_retention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from retnet_retention_gb300 import _build
+    _build.build()
+    la.library()
+
+
+def check(name, got, want, tol):
+    assert np.all(np.isfinite(got)), f"{name}: non-finite output"
+    err = pins.rel_err(got, want)
+    assert err <= tol, f"{name}: rel err {err:.3e} > {tol:.0e}"
+
+
+def to_np(t):
+    return t.double().cpu().numpy()
+
+
+SHAPES = [  # B, H, T, dk, dv, dtype
+    (1, 2, 1, 16, 16, "f32"),
+    (2, 3, 77, 32, 48, "f32"),
+    (1, 2, 300, 64, 64, "f32"),
+    (2, 2, 260, 64, 64, "bf16"),
+    (1, 2, 130, 128, 128, "bf16"),
+    (2, 1, 97, 64, 128, "bf16"),
+]
+FLAGS = [(False, False, False), (True, True, False), (False, False, True)]
+
+
+@pytest.mark.parametrize("gated", [False, True], ids=["gamma", "gated"])
+@pytest.mark.parametrize("flags", FLAGS, ids=["plain", "phi_norm", "floor"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_matches_oracle(shape, flags, gated):
+    B, H, T, dk, dv, dtype = shape
+    phi, normalize, floor = flags
+    seed = zlib.crc32(repr((shape, flags, gated, "bwd")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype=dtype, gate=gated,
+                              scale=0.5 if floor else None)
+    rng = np.random.default_rng(seed)
+    tdt = workloads.torch_dtype(dtype)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(tdt)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.3)
+    z0 = torch.from_numpy(np.abs(rng.standard_normal((B, H, dk))).astype(np.float32))
+    dST = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.1)
+    dzT = torch.from_numpy(rng.standard_normal((B, H, dk)).astype(np.float32) * 0.1)
+    norm_any = normalize or floor
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    kw = dict(log_a=x["log_a"].to(DEV)) if gated else dict(gamma=x["gamma"])
+    dq, dk_, dv_, dS0, dz0 = la.chunk_bwd(
+        q, k, v, g_o, phi=phi, normalize=normalize, floor=floor, S0=S0.to(DEV),
+        z0=z0.to(DEV) if norm_any else None, dS_T=dST.to(DEV), dz_T=dzT.to(DEV) if norm_any else None,
+        **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, rS0, rz0 = oracle.recurrent_bwd(
+        x["q"], x["k"], x["v"], x["gamma"], dO, phi=phi, normalize=normalize, floor=floor,
+        S0=S0, z0=z0 if norm_any else None, dS_T=dST, dz_T=dzT if norm_any else None,
+        log_a=x["log_a"] if gated else None)
+    tol = TOL[dtype]
+    check("dq", to_np(dq), rq, tol)
+    check("dk", to_np(dk_), rk, tol)
+    check("dv", to_np(dv_), rv, tol)
+    check("dS0", to_np(dS0), rS0, tol)
+    if norm_any:
+        check("dz0", to_np(dz0), rz0, tol)
+
+
+def test_bwd_matches_autograd_of_the_forward_kernel_inputs_on_fp32():
+    """An fp32 case checked against torch autograd through the masked parallel form
+    (an independent route to the same gradients, on the host)."""
+    B, H, T, dk, dv = 1, 2, 40, 16, 16
+    x = workloads.random_case(3, B, H, T, dk, dv, dtype="f32")
+    q, k, v = (x[n].double().requires_grad_(True) for n in ("q", "k", "v"))
+    g = torch.tensor(np.asarray(x["gamma"], np.float64))
+    n = torch.arange(T, dtype=torch.float64)
+    diff = n[:, None] - n[None, :]
+    D = torch.where(diff >= 0, g[:, None, None] ** diff.clamp(min=0), torch.zeros(()))
+    O = ((q @ k.transpose(-1, -2)) * D) @ v
+    dO = torch.randn(B, H, T, dv, dtype=torch.float64, generator=torch.Generator().manual_seed(5))
+    (O * dO).sum().backward()
+    gq, gk, gv, _, _ = la.chunk_bwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV),
+                                     dO.float().to(DEV), x["gamma"])
+    torch.cuda.synchronize()
+    check("dq", to_np(gq), q.grad.numpy(), TOL["f32"])
+    check("dk", to_np(gk), k.grad.numpy(), TOL["f32"])
+    check("dv", to_np(gv), v.grad.numpy(), TOL["f32"])
+
+
+def test_bwd_linear_attention_bf16_sampled():
+    """The headline workload's shape, gradients checked on a sample of sequences."""
+    c = workloads.CONFIGS["linear_attention_bf16"]
+    x = workloads.make_inputs(c)
+    B, H, T, dv = c["B"], c["H"], c["T"], c["dv"]
+    rng = np.random.default_rng(77)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    q, k, v, g_o = (t.to(DEV) for t in (x["q"], x["k"], x["v"], dO))
+    dq, dk, dv_, _, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], phi=True, normalize=True)
+    torch.cuda.synchronize()
+    for (b, h) in workloads.sample_pairs(B, H, 3):
+        rq, rk, rv, _, _ = oracle.recurrent_bwd(x["q"][b, h][None, None], x["k"][b, h][None, None],
+                                                x["v"][b, h][None, None], [x["gamma"][h]],
+                                                dO[b, h][None, None], phi=True, normalize=True)
+        check(f"dq[{b},{h}]", to_np(dq[b, h]), rq[0, 0], TOL["bf16"])
+        check(f"dk[{b},{h}]", to_np(dk[b, h]), rk[0, 0], TOL["bf16"])
+        check(f"dv[{b},{h}]", to_np(dv_[b, h]), rv[0, 0], TOL["bf16"])
