@@ -184,7 +184,9 @@ struct LayoutWS {
 // sready(c) = the bf16 copy of S and the scaled S and tiles are in place for
 // MMA3/MMA4 (epilogues A and B); pready(c) = P is in TMEM for MMA2 (epilogue A).
 // With one O buffer pready(c) carries both (epilogues A and B).  sdone(c) =
-// MMA3/MMA4 of c are complete.
+// MMA3/MMA4 of c are complete; in a state walk sdone completes once, after the
+// last MMA4.  A parity wait is sound only while its barrier is at most one phase
+// behind the phase awaited: every wait here is placed so that it is.
 enum Bars {
     kFull0 = 0, kEmpty0 = 4, kQk0 = 8, kReadyS0 = 12, kSfull0 = 16, kSfull1, kPready0, kPready1,
     kOfull0, kOfull1, kOempty0, kOempty1, kNever, kDrain, kSdone, kSready0, kSready1,
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                                id_kv, 1u);
                     mma_commit(&bar[kOfull0]);
                     mma_commit(&bar[kEmpty0 + s]);
+                    if (it == n - 1) mma_commit(&bar[kSdone]);  // the exit state is complete
                     mma_issued = true;
                     LA_TL(it * 16 + 3);
                 }
@@ -882,7 +885,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                     if (t == 0) LA_TL(it * 16 + 9);
                 }
                 if (!stop && !*abort_flag) {
-                    bool ok = mbar_wait_or_abort(&bar[kOfull0], (n - 1) & 1, lim, abort_flag);
+                    // the last MMA4 on a barrier of its own: this role runs up to a ring of
+                    // stages ahead of the MMAs, so o_full may be two or more phases behind
+                    // here, and a parity wait would then return for an earlier phase
+                    bool ok = mbar_wait_or_abort(&bar[kSdone], 0, lim, abort_flag);
                     if (!named_bar_or(kBarB, 128, !ok)) {
                         fence_after_sync();
                         write_exit_state();

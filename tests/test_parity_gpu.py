@@ -143,6 +143,23 @@ def test_noncausal(flags, dtype):
                                                phi=phi, normalize=normalize), TOL[dtype])
 
 
+@pytest.mark.parametrize("H", [1, 2])
+def test_state_walk_with_inputs_just_written(H):
+    """Inputs written by a kernel right before each call (still in L2, so the tile
+    loads run ahead of the MMAs), segments of two chunks, twelve repeats: the state
+    walk's exit state must be read after its last MMA, not an earlier one."""
+    B, T, dk, dv = 1, 3000, 64, 64
+    x = workloads.random_case(4242 + H, B, H, T, dk, dv, dtype="bf16")
+    want_O, want_S, _ = oracle.recurrent(x["q"].flip(2), x["k"].flip(2), x["v"].flip(2), x["gamma"])
+    q, k, v = (to_dev(x[n]) for n in ("q", "k", "v"))
+    for rep in range(12):
+        qf, kf, vf = (t.flip(2).contiguous() for t in (q, k, v))
+        O, S, _ = la.chunk_fwd(qf, kf, vf, x["gamma"])
+        torch.cuda.synchronize()
+        check(f"O (repeat {rep})", np64(O), want_O, TOL["bf16"])
+        check(f"S (repeat {rep})", np64(S), want_S, TOL["bf16"])
+
+
 def test_closed_form_geometric_series():
     """One nonzero feature and value column, q = k = v = 1: o_n = (1 - g^(n+1)) / (1 - g)."""
     T = 65536
