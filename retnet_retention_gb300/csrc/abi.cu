@@ -72,6 +72,27 @@ bool simt_pinned() {
     return pin && std::strcmp(pin, "simt") == 0;
 }
 
+// The backward pass's path: the tensor cores (three forward passes) where they
+// apply, unless LA_CHUNK_PATH=simt pins the CUDA-core kernel.
+BwdArgs bwd_plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                      bool gated) {
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    static const float kMarker = 0.f;
+    a.B = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    a.phi = (flags & LA_PHI_ELU1) != 0;
+    a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
+    a.normalize = (flags & LA_NORMALIZE) != 0 || a.floor_norm;
+    a.log_a = gated ? &kMarker : nullptr;
+    return a;
+}
+
+size_t bwd_bytes_for(const BwdArgs& a) {
+    if (!simt_pinned() && bwd_tc_supported(a)) return bwd_tc_workspace_bytes(a);
+    return bwd_workspace_bytes(a.B, a.H, a.T, a.normalize);
+}
+
 }  // namespace
 
 extern "C" {
@@ -295,8 +316,8 @@ la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
     for (const void* p : {(const void*)S0, (const void*)z0, (const void*)dS_T, (const void*)dz_T,
                           (const void*)dS0, (const void*)dz0, (const void*)workspace})
         if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
-    if (workspace_bytes < bwd_workspace_bytes(B, H, T, normalize)) return LA_ERR_INVALID_ARG;
-    if (normalize && T > 0 && !workspace) return LA_ERR_INVALID_ARG;
+    const size_t need = T > 0 ? bwd_bytes_for(bwd_plan_args(B, H, T, d_k, d_v, dtype, flags, gated)) : 0;
+    if (workspace_bytes < need || (need > 0 && !workspace)) return LA_ERR_INVALID_ARG;
 
     BwdArgs a;
     a.Q = Q; a.K = K; a.V = V; a.dO = dO;
@@ -311,6 +332,8 @@ la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
     a.log_a = gated ? log_a : nullptr;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
+    if (T > 0 && !simt_pinned() && bwd_tc_supported(a))
+        return cuda_status(launch_chunk_bwd_tc(a, g, (cudaStream_t)stream));
     return cuda_status(launch_chunk_bwd_simt(a, g, (cudaStream_t)stream));
 }
 
@@ -321,7 +344,7 @@ extern "C" {
 size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
                              unsigned flags) {
     if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || d_k > 128 || d_v > 128) return 0;
-    return bwd_workspace_bytes(B, H, T, (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0);
+    return bwd_bytes_for(bwd_plan_args(B, H, T, d_k, d_v, dtype, flags, (flags & LA_GATED) != 0));
 }
 
 la_status la_chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,

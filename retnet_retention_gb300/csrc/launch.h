@@ -96,6 +96,12 @@ int simt_chunk_len(int requested, int dk);
 cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s);
 size_t bwd_workspace_bytes(int B, int H, int T, bool normalize);
 
+// chunk_bwd_tc.cu: the backward pass as three forward passes on the tensor cores
+// (bf16, no feature map, no normaliser, per-head decay, d_k, d_v in {64, 128})
+bool bwd_tc_supported(const BwdArgs& a);
+size_t bwd_tc_workspace_bytes(const BwdArgs& a);
+cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStream_t s);
+
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);
 size_t tc_workspace_bytes(const ChunkArgs& a);

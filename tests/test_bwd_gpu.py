@@ -92,6 +92,67 @@ def test_bwd_matches_oracle(shape, flags, gated):
         check("dz0", to_np(dz0), rz0, tol)
 
 
+TC_SHAPES = [  # B, H, T, dk, dv: bf16, per-head decay, no phi, no normaliser
+    (2, 2, 260, 64, 64),
+    (1, 2, 130, 128, 128),
+    (2, 1, 97, 64, 128),
+    (1, 3, 300, 128, 64),
+    (1, 2, 3000, 64, 64),     # the forward passes split into segments (scan)
+    (2, 16, 1000, 64, 64),    # segments folded in the output walk
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_tensor_core_path(shape, monkeypatch):
+    """The three forward passes on the tensor cores (dQ; dV and dK over the reversed
+    sequences) against the oracle, with an initial state and a final-state gradient."""
+    monkeypatch.delenv("LA_CHUNK_PATH", raising=False)
+    B, H, T, dk, dv = shape
+    seed = zlib.crc32(repr((shape, "bwd-tc")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16")
+    rng = np.random.default_rng(seed)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.3)
+    dST = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.1)
+    lib = la.library()
+    need = lib.la_bwd_workspace_size(B, H, T, dk, dv, 1, 0)
+    assert need > B * H * T * (dk + dv) * 2  # the reversed copies: the tensor-core path
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    dq, dk_, dv_, dS0, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], S0=S0.to(DEV), dS_T=dST.to(DEV))
+    torch.cuda.synchronize()
+    rq, rk, rv, rS0, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, S0=S0,
+                                              dS_T=dST)
+    check("dq", to_np(dq), rq, TOL["bf16"])
+    check("dk", to_np(dk_), rk, TOL["bf16"])
+    check("dv", to_np(dv_), rv, TOL["bf16"])
+    check("dS0", to_np(dS0), rS0, TOL["bf16"])
+    # the same through the CUDA-core kernel
+    monkeypatch.setenv("LA_CHUNK_PATH", "simt")
+    sq, sk, sv, sS0, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], S0=S0.to(DEV), dS_T=dST.to(DEV))
+    torch.cuda.synchronize()
+    check("dq tc vs simt", to_np(dq), to_np(sq), TOL["bf16"])
+    check("dS0 tc vs simt", to_np(dS0), to_np(sS0), TOL["bf16"])
+
+
+def test_bwd_tensor_core_path_repeated(monkeypatch):
+    """The tensor-core composite twelve times over: its dV pass reads reversed copies
+    written just before it (hot in L2), the case that once exposed an exit state read
+    before the state walk's last MMA."""
+    monkeypatch.delenv("LA_CHUNK_PATH", raising=False)
+    B, H, T, dk, dv = 1, 2, 3000, 64, 64
+    x = workloads.random_case(9090, B, H, T, dk, dv, dtype="bf16")
+    rng = np.random.default_rng(9090)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    rq, rk, rv, _, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO)
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    for rep in range(12):
+        dq, dk_, dv_, _, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], state_grads=False)
+        torch.cuda.synchronize()
+        check(f"dq (repeat {rep})", to_np(dq), rq, TOL["bf16"])
+        check(f"dk (repeat {rep})", to_np(dk_), rk, TOL["bf16"])
+        check(f"dv (repeat {rep})", to_np(dv_), rv, TOL["bf16"])
+
+
 def test_bwd_matches_autograd_of_the_forward_kernel_inputs_on_fp32():
     """An fp32 case checked against torch autograd through the masked parallel form
     (an independent route to the same gradients, on the host)."""
