@@ -47,11 +47,13 @@ KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "t
                   "chunk_tc.cu", "common.cuh", "launch.h")
 TRAFFIC = {
     "chunk_tc_ws_kernel/full": {
-        "bytes": 52_005_376 + 297_728,
-        "sources_sha256": "8c2957193942ff1a268aa07660f44a1245ed98235c4030109f81b8c606f87500",
+        "bytes": 52_006_656 + 270_080,
+        "sources_sha256": "c4e34d45d4d377febdf0e57cd9704534c7315dcc17b17cd5ce85f06d246735ef",
     },
 }
 HEADLINE = "linear_attention_bf16"
+# the backward pass on the tensor cores: plain retention, d_k = d_v = 128
+BWD_TC = "long_retention_bf16"
 L2_BYTES = 129 * 1024 * 1024
 C_REF = 64  # chunk length fixed for counting useful intra-chunk flops
 
@@ -449,10 +451,11 @@ def run_ours(args) -> dict | None:
             print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
                               "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
         return None
-    if only == "backward":  # profiling aid: the headline's backward pass alone
-        r = bwd_measure(la, HEADLINE, args.steps, args.warmup, rank, world)
+    if only in ("backward", "backward_" + BWD_TC):  # profiling aid: one backward pass alone
+        r = bwd_measure(la, HEADLINE if only == "backward" else BWD_TC, args.steps, args.warmup,
+                        rank, world)
         if rank == 0:
-            print(json.dumps({"only": "backward", "ms": r["ms"],
+            print(json.dumps({"only": only, "ms": r["ms"],
                               "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
         return None
     if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
@@ -479,8 +482,11 @@ def run_ours(args) -> dict | None:
             others[name] = r
         dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         dec["ms"] = max_over_ranks(dec["ms"])
-        bwd = bwd_measure(la, HEADLINE, 3, 1, rank, world)
-        bwd["ms"] = max_over_ranks(bwd["ms"])
+        bwds = {}
+        for name in (HEADLINE, BWD_TC):
+            r = bwd_measure(la, name, 3, args.warmup, rank, world)
+            r["ms"] = max_over_ranks(r["ms"])
+            bwds[name] = r
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -551,13 +557,15 @@ def run_ours(args) -> dict | None:
                              roofline_frac=kgbs / pk["hbm_gbs"], kernels=r["kernels"])
         dc = dec["config"]
         gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
-        bc = bwd["config"]
-        gbs = bwd["bytes"] / (bwd["ms"] * 1e-3) / 1e9
-        sub["backward_" + HEADLINE] = dict(
-            workload="backward of " + describe(HEADLINE, bc) + " (gradients of Q, K, V and of "
-                     "the initial state for a seeded N(0,1) dO)",
-            tokens_per_s=bwd["tokens"] * world / (bwd["ms"] * 1e-3), ms=bwd["ms"], alg_gbs=gbs,
-            roofline_frac=gbs / pk["hbm_gbs"], kernels=bwd["kernels"])
+        for name, bwd in bwds.items():
+            bc = bwd["config"]
+            bgbs = bwd["bytes"] / (bwd["ms"] * 1e-3) / 1e9
+            sub["backward_" + name] = dict(
+                workload="backward of " + describe(name, bc) + " (gradients of Q, K, V and of "
+                         "the initial state for a seeded N(0,1) dO)",
+                path="tensor cores (three forward passes)" if name == BWD_TC else "CUDA cores",
+                tokens_per_s=bwd["tokens"] * world / (bwd["ms"] * 1e-3), ms=bwd["ms"],
+                alg_gbs=bgbs, roofline_frac=bgbs / pk["hbm_gbs"], kernels=bwd["kernels"])
         sub["decode_bf16"] = dict(
             workload=f"decode_bf16: B={dc['B']} H={dc['H']} d_k={dc['dk']} d_v={dc['dv']} fp32 "
                      f"state after a {dc['T']}-token prefill, {dec['steps']} steps",
@@ -627,7 +635,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
                                        "retention_floor_bf16", "gated_retention_bf16", "decode",
-                                       "backward"),
+                                       "backward", "backward_long_retention_bf16"),
                     default=None,
                     help="profiling aid: run one workload only")
     ap.add_argument("--decode-steps", type=int,
