@@ -33,6 +33,10 @@ decode_step(q, k, v, gamma, S, z, phi, normalize, eps)
     One token of the same recurrence: the interview box "Causal linear
     attention, recurrent and parallel, plus the decode step" on the "Linear
     attention" page.  It is ``recurrent`` with T = 1 and the state passed in.
+taylor_features(x), recurrent_taylor(q, k, v, gamma, normalize, ...)
+    The second-order Taylor feature map phi(x) = (1, x, vec(x x^T)/sqrt(2)) of
+    the "Linear attention" page (box "Taylor features"), and ``recurrent`` on
+    the features it gives (d_phi = 1 + d + d^2; d = 16 gives 273).
 noncausal(q, k, v, phi, normalize, eps)
     gamma = 1, every query reads the one summary phi(K)^T V: box "Linear
     attention" on the "Linear attention" page.
@@ -75,6 +79,8 @@ def _load(path: str | None = None):
     lib.oracle_noncausal.argtypes = [dp, dp, dp, L, L, L, L, L, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_double, dp, dp, dp]
     lib.oracle_noncausal.restype = ctypes.c_int
+    lib.oracle_taylor_features.argtypes = [dp, L, L, dp]
+    lib.oracle_taylor_features.restype = None
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
@@ -236,9 +242,33 @@ def noncausal(q, k, v, phi: bool = False, normalize: bool = False, eps: float = 
     return O, S, z
 
 
+def taylor_features(x, _lib=None):
+    """Second-order Taylor features of every row, in fp64: [..., d] -> [..., 1 + d + d^2],
+    ordered (1, x, vec(x x^T) / sqrt(2)) with vec row-major ("Linear attention" page,
+    box "Taylor features")."""
+    X = np.ascontiguousarray(_f64(x))
+    d = X.shape[-1]
+    n = int(np.prod(X.shape[:-1]))
+    out = np.empty(X.shape[:-1] + (1 + d + d * d,))
+    (_lib or lib()).oracle_taylor_features(_ptr(X), n, d, _ptr(out))
+    return out
+
+
+def recurrent_taylor(q, k, v, gamma, normalize: bool = False, eps: float = 1e-6, S0=None,
+                     z0=None, _lib=None, floor: bool = False):
+    """The causal recurrence with the Taylor feature map: ``recurrent`` on the
+    features of q and k (d_phi = 1 + d + d^2 rows of S and z, in the order of
+    ``taylor_features``).  The page pairs the map with the normaliser, which it
+    keeps positive: phi(q)^T phi(k) = ((s + 1)^2 + 1) / 2 >= 1/2."""
+    fq, fk = taylor_features(q, _lib), taylor_features(k, _lib)
+    return recurrent(fq, fk, v, gamma, phi=False, normalize=normalize, eps=eps, S0=S0, z0=z0,
+                     _lib=_lib, floor=floor)
+
+
 def load_mutant(mutant: int, out_dir: str):
     """Load a build of the oracle with a planted mistake (for pin tests only)."""
     return _load(_build.build_mutant(mutant, out_dir))
 
 
-__all__ = ["recurrent", "decode_step", "noncausal", "num_threads", "load_mutant", "lib"]
+__all__ = ["recurrent", "recurrent_taylor", "taylor_features", "decode_step", "noncausal",
+           "num_threads", "load_mutant", "lib"]

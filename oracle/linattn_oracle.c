@@ -426,6 +426,37 @@ int oracle_noncausal(const double* Q, const double* K, const double* V,
 }
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
+/*
+ * Second-order Taylor features ("Linear attention" page, section "A Taylor
+ * feature map", box "Taylor features"): for x in R^d
+ *
+ *   phi(x) = (1, x_1 .. x_d, vec(x x^T) / sqrt(2))        (1 + d + d^2 entries),
+ *
+ * the constant first, then the d linear features, then the d^2 entries of the
+ * outer product in row-major order, so that phi(q)^T phi(k) = 1 + s + s^2 / 2
+ * with s = q^T k (the page's theorem).
+ *
+ *   X : [n][d]     out : [n][1 + d + d*d]
+ */
+void oracle_taylor_features(const double* X, long n, long d, double* out)
+{
+    const long df = 1 + d + d * d;
+    const double r = 1.0 / sqrt(2.0);
+    for (long t = 0; t < n; ++t) {
+        const double* x = X + t * d;
+        double* f = out + t * df;
+        f[0] = 1.0;
+        for (long i = 0; i < d; ++i) f[1 + i] = x[i];
+        for (long i = 0; i < d; ++i)
+            for (long j = 0; j < d; ++j)
+#if ORACLE_MUTANT == 12 /* mutant: the outer product without the 1 / sqrt(2) */
+                f[1 + d + i * d + j] = x[i] * x[j];
+#else
+                f[1 + d + i * d + j] = x[i] * x[j] * r;
+#endif
+    }
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

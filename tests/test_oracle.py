@@ -21,6 +21,11 @@ Which pin covers which part of the oracle:
   per-token decay                            -> masked form with explicit gate products,
                                                 constant gate == gamma, a_t = 0 resets,
                                                 chunkwise equations with cumulative logs
+  Taylor feature map                         -> the page's worked pair (features and kernel),
+                                                the theorem 1 + s + s^2/2 and its minimum,
+                                                normalised outputs as the kernel-weighted
+                                                average computed from s alone, state rows
+                                                as explicit sums
 """
 import json
 import os
@@ -406,12 +411,67 @@ def pin_backward_by_differences(lib=None):
         _check_by_differences(loss, [q, k, v, S0, z0], [dq, dk_, dv_, dS0, dz0])
 
 
+def pin_taylor_pair(lib=None):
+    """The page's worked pair q = (1, 2), k = (3, 1): the features in the box's order
+    (constant, linear, the outer product row-major over sqrt 2) and the kernel value."""
+    g = _golden("taylor_features_pair.json")
+    f = oracle.taylor_features(np.array([g["q"], g["k"]], float), _lib=lib)
+    r2 = np.sqrt(2.0)
+    np.testing.assert_allclose(f[0], [1.0, *g["q"], *(np.array(g["vec_qq"]) / r2)], rtol=1e-15)
+    np.testing.assert_allclose(f[1], [1.0, *g["k"], *(np.array(g["vec_kk"]) / r2)], rtol=1e-15)
+    assert abs(f[0] @ f[1] - g["kernel"]) < 1e-12
+    assert g["kernel"] == 1 + g["s"] + g["s_squared"] / 2 and g["vec_dot"] == g["s_squared"]
+
+
+def pin_taylor_kernel_theorem(lib=None):
+    """phi(q)^T phi(k) = 1 + s + s^2/2 = ((s + 1)^2 + 1)/2 for random pairs (the page's
+    theorem), and the minimum 1/2 at s = -1."""
+    rng = _rng(61)
+    for d in (1, 3, 16):
+        q, k = rng.standard_normal((2, 50, d))
+        s = np.einsum("nd,nd->n", q, k)
+        fq, fk = oracle.taylor_features(q, _lib=lib), oracle.taylor_features(k, _lib=lib)
+        assert fq.shape == (50, 1 + d + d * d)
+        np.testing.assert_allclose(np.einsum("nf,nf->n", fq, fk), 1 + s + s * s / 2, rtol=1e-12)
+    x = np.array([[1.0, 0.0]])
+    fm = oracle.taylor_features(-x, _lib=lib)[0] @ oracle.taylor_features(x, _lib=lib)[0]
+    assert abs(fm - 0.5) < 1e-15
+
+
+def pin_taylor_attention(lib=None):
+    """Causal normalised attention with the Taylor features and a per-head decay equals
+    the kernel-weighted average sum_s g^(t-s) kappa(q_t, k_s) v_s / sum_s g^(t-s)
+    kappa(q_t, k_s), kappa = 1 + s + s^2/2 taken from the dot products alone; the final
+    state's rows are the explicit decayed sums of 1, k_i and k_i k_j / sqrt 2 times v."""
+    rng = _rng(62)
+    B, H, T, d, dv = 1, 2, 23, 4, 3
+    q, k = rng.standard_normal((2, B, H, T, d)) * 0.7
+    v = rng.standard_normal((B, H, T, dv))
+    gamma = np.array([1.0, 0.9])
+    O, S, z = oracle.recurrent_taylor(q, k, v, gamma, normalize=True, eps=0.0, _lib=lib)
+    for h in range(H):
+        sc = q[0, h] @ k[0, h].T
+        kap = 1 + sc + sc * sc / 2
+        n = np.arange(T)
+        D = np.where(n[:, None] >= n[None, :], gamma[h] ** (n[:, None] - n[None, :]), 0.0)
+        W = kap * D
+        np.testing.assert_allclose(O[0, h], (W @ v[0, h]) / W.sum(1, keepdims=True), rtol=1e-11)
+        w = gamma[h] ** (T - 1 - n)
+        kk = k[0, h]
+        np.testing.assert_allclose(S[0, h, 0], w @ v[0, h], rtol=1e-11)
+        np.testing.assert_allclose(S[0, h, 1:1 + d], (kk * w[:, None]).T @ v[0, h], rtol=1e-11)
+        quad = np.einsum("t,ti,tj,tv->ijv", w, kk, kk, v[0, h]) / np.sqrt(2.0)
+        np.testing.assert_allclose(S[0, h, 1 + d:].reshape(d, d, dv), quad, rtol=1e-11)
+        np.testing.assert_allclose(z[0, h, 0], w.sum(), rtol=1e-12)
+
+
 ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
             pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
             pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
             pin_chunkwise_invariance, pin_state_handoff, pin_floor_clamped_rows,
             pin_floor_limits, pin_gated_parallel_form, pin_gated_constant_is_gamma,
-            pin_gated_reset, pin_gated_chunkwise, pin_backward_by_differences]
+            pin_gated_reset, pin_gated_chunkwise, pin_backward_by_differences,
+            pin_taylor_pair, pin_taylor_kernel_theorem, pin_taylor_attention]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -493,6 +553,7 @@ MUTANTS = {
     9: "per-token gate one token late",
     10: "backward sweep without the decay",
     11: "dq without the normaliser's term",
+    12: "Taylor features without the 1/sqrt(2)",
 }
 
 
