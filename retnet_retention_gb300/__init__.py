@@ -27,7 +27,7 @@ from . import _build
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
-LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR, LA_GATED = 1, 2, 4, 8, 16
+LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR, LA_GATED, LA_PHI_TAYLOR = 1, 2, 4, 8, 16, 32
 
 LIBRARY_PATH = _build.LIBRARY
 _LIB = None
@@ -124,9 +124,22 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
 
 
-def _flags(phi: bool, normalize: bool, causal: bool, floor: bool = False) -> int:
-    return (LA_PHI_ELU1 if phi else 0) | (LA_NORMALIZE if normalize else 0) | (
-        0 if causal else LA_NONCAUSAL) | (LA_NORM_FLOOR if floor else 0)
+def _flags(phi, normalize: bool, causal: bool, floor: bool = False) -> int:
+    """phi: False (identity), True (elu + 1) or "taylor" (the second-order Taylor map)."""
+    if phi == "taylor":
+        fm = LA_PHI_TAYLOR
+    elif phi is True or phi is False:
+        fm = LA_PHI_ELU1 if phi else 0
+    else:
+        raise ValueError(f"phi must be False, True or 'taylor', not {phi!r}")
+    return fm | (LA_NORMALIZE if normalize else 0) | (0 if causal else LA_NONCAUSAL) | (
+        LA_NORM_FLOOR if floor else 0)
+
+
+def state_rows(dk: int, phi=False) -> int:
+    """Rows of the state S (and entries of z) for queries and keys of width dk:
+    dk, or 1 + dk + dk^2 with the Taylor feature map."""
+    return 1 + dk + dk * dk if phi == "taylor" else dk
 
 
 def _ptr(t) -> int | None:
@@ -185,6 +198,8 @@ def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, e
     z_out is given).  floor=True divides by max(|phi(q)^T z|, 1) (LA_NORM_FLOOR;
     implies normalising, eps unused).  log_a: a [B,H,T] fp32 device tensor of
     per-token log decays used instead of gamma (la_chunk_fwd_gated).
+    phi="taylor": the second-order Taylor feature map (LA_PHI_TAYLOR; bf16,
+    d = 16); the states then have state_rows(d, "taylor") = 273 rows.
     """
     normalize = normalize or floor
     B, H, T, dk = q.shape
@@ -197,10 +212,11 @@ def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, e
     dev = q.device
     if out is None:
         out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    ds = state_rows(dk, phi)
     if return_state and S_out is None:
-        S_out = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+        S_out = torch.empty((B, H, ds, dv), dtype=torch.float32, device=dev)
     if return_state and normalize and z_out is None:
-        z_out = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+        z_out = torch.empty((B, H, ds), dtype=torch.float32, device=dev)
     if (gamma is None) == (log_a is None):
         raise ValueError("pass exactly one of gamma and log_a")
     if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
@@ -352,10 +368,11 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
     pin = dict(pin_memory=True)
     if out is None:
         out = torch.empty((B, H, T, dv), dtype=q.dtype, **pin)
+    ds = state_rows(dk, phi)
     if S_out is None:
-        S_out = torch.empty((B, H, dk, dv), dtype=torch.float32, **pin)
+        S_out = torch.empty((B, H, ds, dv), dtype=torch.float32, **pin)
     if z_out is None and normalize:
-        z_out = torch.empty((B, H, dk), dtype=torch.float32, **pin)
+        z_out = torch.empty((B, H, ds), dtype=torch.float32, **pin)
     qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
     kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
     vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
@@ -403,4 +420,4 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
 __all__ = ["chunk_fwd", "chunk_bwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
            "trace_enable", "trace_collect",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
-           "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED"]
+           "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR", "state_rows"]

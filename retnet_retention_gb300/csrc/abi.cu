@@ -57,6 +57,7 @@ ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsig
     a.normalize = (flags & (LA_NORMALIZE | LA_NORM_FLOOR)) != 0;
     a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
     a.noncausal = (flags & LA_NONCAUSAL) != 0;
+    a.taylor = (flags & LA_PHI_TAYLOR) != 0;
     a.log_a = (flags & LA_GATED) ? &kMarker : nullptr;
     return a;
 }
@@ -64,7 +65,7 @@ ChunkArgs plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsig
 bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags) {
     return B > 0 && H > 0 && T > 0 && valid_dim(d_k) && valid_dim(d_v) && H <= kMaxHeads &&
            (dtype == LA_DTYPE_F32 || dtype == LA_DTYPE_BF16) &&
-           !(flags & ~(kCallFlags | LA_GATED));
+           !(flags & ~(kCallFlags | LA_GATED | LA_PHI_TAYLOR));
 }
 
 bool simt_pinned() {
@@ -149,7 +150,11 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | LA_PHI_TAYLOR | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    const bool taylor = (flags & LA_PHI_TAYLOR) != 0;
+    if (taylor && (gated || dtype != LA_DTYPE_BF16 || d_k != 16 || d_v % 64 != 0 ||
+                   (flags & (LA_PHI_ELU1 | LA_NONCAUSAL)) || !(chunk == 0 || chunk == 128)))
+        return LA_ERR_UNSUPPORTED;
     if (!(chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128))
         return LA_ERR_INVALID_ARG;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
@@ -188,7 +193,8 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
         return LA_ERR_INVALID_ARG;
 
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t nS = nbh * d_k * d_v, nz = nbh * d_k;
+    const size_t ds = taylor ? (size_t)taylor_feature_dim(d_k) : (size_t)d_k;  // state rows
+    const size_t nS = nbh * ds * d_v, nz = nbh * ds;
     if (T == 0) {  // empty sequence: the final state is the initial one
         cudaError_t e = cudaSuccess;
         if (S_out) e = S0 ? launch_state_copy(S_out, S0, nS, s) : launch_state_zero(S_out, nullptr, nS, 0, s);
@@ -207,6 +213,7 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     a.normalize = normalize;
     a.floor_norm = floor_norm;
     a.noncausal = noncausal;
+    a.taylor = taylor;
     a.eps = eps;
     a.log_a = gated ? log_a : nullptr;
     a.workspace = workspace;
@@ -217,6 +224,10 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     const char* pin = std::getenv("LA_CHUNK_PATH");
     const bool want_simt = pin && std::strcmp(pin, "simt") == 0;
     const bool want_tc = pin && std::strcmp(pin, "tc") == 0;
+    if (taylor) {  // its own tensor-core kernel; no CUDA-core version
+        if (want_simt || !taylor_supported(a)) return LA_ERR_UNSUPPORTED;
+        return cuda_status(launch_chunk_taylor(a, g, s));
+    }
     if (!want_simt && tc_supported(a)) {
         int launches = 0;
         return cuda_status(launch_chunk_tc(a, g, s, &launches));
@@ -232,6 +243,7 @@ la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype d
     const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
+    if (flags & LA_PHI_TAYLOR) return LA_ERR_UNSUPPORTED;
     if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
     if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
@@ -277,6 +289,7 @@ la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
                     float* dS0, float* dz0, void* workspace, size_t workspace_bytes,
                     la_stream_t stream) {
     const bool gated = gamma == nullptr;
+    if (flags & LA_PHI_TAYLOR) return LA_ERR_UNSUPPORTED;
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
     if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
@@ -343,7 +356,9 @@ extern "C" {
 
 size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
                              unsigned flags) {
-    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || d_k > 128 || d_v > 128) return 0;
+    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || (flags & LA_PHI_TAYLOR) || d_k > 128 ||
+        d_v > 128)
+        return 0;
     return bwd_bytes_for(bwd_plan_args(B, H, T, d_k, d_v, dtype, flags, (flags & LA_GATED) != 0));
 }
 

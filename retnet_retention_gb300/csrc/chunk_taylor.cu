@@ -1,0 +1,560 @@
+// Causal linear attention with the second-order Taylor feature map on the
+// tensor cores.
+//
+// "Linear attention" (zerotofrontier 21.2), section "A Taylor feature map":
+// phi(x) = (1, x, vec(x x^T)/sqrt 2) has 1 + d + d^2 entries and
+// phi(q)^T phi(k) = 1 + s + s^2/2 with s = q^T k; Based projects q and k to
+// d = 16 first, so d_phi = 273.  The queries and keys enter here at their width
+// of 16 (32 bytes a token, not 546): the CTA builds the features on chip.
+//
+// Per chunk of 128 tokens and block of 64 value columns, with xi_i = gamma^(i+1),
+// zeta_j = gamma^(L-1-j) (the forms of the per-head kernels):
+//   MMA1  s = q k^T                         (K = 16, the raw q and k)
+//   E1    P_ij = (1 + s + s^2/2) gamma^(i-j) for j <= i        (bf16, in TMEM)
+//   MMA3  O  = (xi . phi(Q)) S_bf16                            (K = 288 feature columns)
+//   MMA2  O += P [V | 1]                                       (row sums in column 64)
+//   MMA4  S^T += [V | 1]^T (zeta . phi(K))                     (z rides as the row of the 1)
+//   E2    o_i = O_i / (O_i,64 + O_i,65) with the normaliser, else O_i
+//   E3    S_bf16 <- S (z as a bf16 value and its residual), S^T *= gamma^L(next chunk)
+// The state is held transposed in TMEM (lanes 0..63 the value columns, lane 64
+// z, 288 columns of features), so each TMEM lane is one row of MMA3's K-major
+// B operand and z needs no reduction of its own: it is S's column for an
+// all-ones value, the reading of z on the same page.
+//
+// The CTA runs its phases in lockstep (256 threads; thread 0 issues the TMA
+// loads and the MMAs); the loads of chunk c + 1 overlap chunk c.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <cstring>
+
+#include "chunk_tc_common.cuh"
+#include "trace.h"
+
+namespace la {
+
+namespace {
+
+using namespace tck;
+
+constexpr int kD = 16;                  // width of q and k
+constexpr int kDF = 1 + kD + kD * kD;   // 273 features
+constexpr int kDVB = 64;                // value columns per CTA
+constexpr int kNV = kDVB + 16;          // O and S_bf16 width: values, normaliser (2), zeros
+constexpr int kThreads = 256;
+// Feature columns on chip, a fixed permutation of the page's order:
+//   [0, 256)    x_a x_b / sqrt 2 at column 16 a + b    (page index 17 + column)
+//   [256, 272)  x_a                                    (page index 1 + a)
+//   272         the constant 1                         (page index 0)
+//   [273, 288)  zero
+// and, in the query phase only, the raw q at [288, 304) and the raw k at
+// [304, 320) (MMA1's operands; MMA3 and MMA4 never read them).
+constexpr int kFB = 5;                  // 64-column blocks of the feature tile
+constexpr int kFCols = 288;             // feature columns the MMAs contract over
+// TMEM columns
+constexpr uint32_t kColS = 0;           // S^T, 288 columns
+constexpr uint32_t kColSc = 288;        // scores, then P (bf16 pairs)
+constexpr uint32_t kColO = 416;         // O, 80 columns
+constexpr uint32_t kTmemCols = 512;
+
+struct Lay {
+    static constexpr uint32_t kRaw = kC * kD * 2;                   // one raw q or k tile
+    static constexpr uint32_t kSBBlk = kNV * 128;                   // one 64-column block of S_bf16
+    static constexpr uint32_t oPhi = 0;                             // feature tile, 5 x 16 KB
+    static constexpr uint32_t oSB = oPhi + kFB * kBlk;              // S_bf16, 5 x 10 KB
+    static constexpr uint32_t oV = oSB + kFB * kSBBlk;              // V, two stages
+    static constexpr uint32_t oOnes = oV + 2 * kBlk;                // the block after V: ones in column 0
+    static constexpr uint32_t oQr = oOnes + kBlk;                   // raw q, two stages
+    static constexpr uint32_t oKr = oQr + 2 * kRaw;                 // raw k, two stages
+    static constexpr uint32_t oBar = oKr + 2 * kRaw;
+    static constexpr uint32_t kBytes = oBar + 128;
+    static constexpr uint32_t kAlloc = kBytes + 1024;               // + alignment of the base
+};
+static_assert(Lay::oSB % 1024 == 0 && Lay::kSBBlk % 1024 == 0 && Lay::oV % 1024 == 0 &&
+                  Lay::oOnes % 1024 == 0,
+              "swizzled blocks need 1024-byte alignment");
+static_assert(Lay::kAlloc <= 227 * 1024, "shared memory budget");
+
+enum Bars { kFull0 = 0, kFull1 = 1, kMma = 2, kDrain = 3, kNever = 4, kNumBars = 5 };
+
+struct TaylorParams {
+    CUtensorMap tmQ, tmK;   // [BH][T][16] bf16, box {16, 128, 1}, no swizzle
+    CUtensorMap tmV;        // [BH][T][dv] bf16, box {64, 128, 1}, 128-byte swizzle
+    __nv_bfloat16* O;       // [BH][T][dv]
+    const float* S0;        // [BH][273][dv] in the page's feature order, or null (zero)
+    const float* z0;        // [BH][273] or null
+    float* S_out;           // final states (same layouts) or null
+    float* z_out;
+    int H, T, dv, n_dvb;
+    int normalize;          // 0 none, 1 divide by the denominator + eps, 2 by max(|.|, 1)
+    float eps;
+    int* dev_status;
+    unsigned long long wait_ns;
+    int force_timeout;
+    KernelGammas g;
+};
+
+// The page's feature index of on-chip column c, or -1 for a padding column.
+__device__ __forceinline__ int page_row(int c) {
+    return c < 256 ? 17 + c : (c < 272 ? c - 255 : (c == 272 ? 0 : -1));
+}
+
+__device__ __forceinline__ void unpack16(const char* src, float (&x)[kD]) {
+    const uint4 u0 = reinterpret_cast<const uint4*>(src)[0];
+    const uint4 u1 = reinterpret_cast<const uint4*>(src)[1];
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+
+// The outer-product columns of rows a = A0 .. A0 + 7 of one token: x_a x_b sq at
+// column 16 a + b of the 128-byte-swizzled feature tile (row r).
+template <int A0>
+__device__ __forceinline__ void quad_rows(char* phi, int r, const float (&x)[kD], float sq) {
+#pragma unroll
+    for (int a = A0; a < A0 + 8; ++a) {
+        const float xa = x[a] * sq;
+#pragma unroll
+        for (int b0 = 0; b0 < kD; b0 += 8) {
+            const int col = kD * a + b0;
+            uint4 w;
+            w.x = pack_bf16x2(xa * x[b0 + 0], xa * x[b0 + 1]);
+            w.y = pack_bf16x2(xa * x[b0 + 2], xa * x[b0 + 3]);
+            w.z = pack_bf16x2(xa * x[b0 + 4], xa * x[b0 + 5]);
+            w.w = pack_bf16x2(xa * x[b0 + 6], xa * x[b0 + 7]);
+            *reinterpret_cast<uint4*>(phi + (col >> 6) * kBlk + sw128_offset(r, col & 63)) = w;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_constant__ TaylorParams p) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char* sm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oBar + 64);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x;
+    const int bh = unit / p.n_dvb, vb = unit % p.n_dvb, v0 = vb * kDVB;
+    const int h = bh % p.H;
+    const float l2g = p.g.log2g[h];
+    const float gam = p.g.gamma[h];
+    const bool unit_gamma = gam == 1.f;
+    const int n = (p.T + kC - 1) / kC;
+    const uint64_t lim = p.wait_ns;
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&p.tmQ);
+        prefetch_tensormap(&p.tmK);
+        prefetch_tensormap(&p.tmV);
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, kTmemCols);
+        tmem_relinquish();
+    }
+    // the block after V: a one in column 0 of every token row (MMA2's row sums,
+    // MMA4's z row), read through the async proxy; S_bf16 starts at zero (its
+    // rows 66..79 stay zero)
+    for (int i = tid; i < (int)(kBlk / 16); i += kThreads) {
+        const uint32_t one = (i & 7) == ((i >> 3) & 7) ? 0x3F80u : 0u;  // logical piece 0 of row i >> 3
+        reinterpret_cast<uint4*>(sm + Lay::oOnes)[i] = make_uint4(one, 0u, 0u, 0u);
+    }
+    for (int i = tid; i < (int)(kFB * Lay::kSBBlk / 16); i += kThreads)
+        reinterpret_cast<uint4*>(sm + Lay::oSB)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t sbase = smem_addr(sm);
+    const int q4 = warp & 3;                  // TMEM lane quarter of this warp
+    const int half = warp >> 2;               // two warps per quarter split the columns
+    const int row = q4 * 32 + lane;           // TMEM lane of this thread
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    // the state's columns each thread copies: 160 and 128
+    const int sc_begin = half == 0 ? 0 : 160, sc_end = half == 0 ? 160 : kFCols;
+
+    int fills[2] = {0, 0};  // thread 0: TMA fills issued per stage
+    auto issue_fill = [&](int it) {
+        const int s = it & 1;
+        const int y = it * kC;
+        mbar_arrive_expect_tx(&bar[kFull0 + s], 2 * Lay::kRaw + kBlk);
+        tma_load_3d(sm + Lay::oQr + s * Lay::kRaw, &p.tmQ, 0, y, bh, &bar[kFull0 + s]);
+        tma_load_3d(sm + Lay::oKr + s * Lay::kRaw, &p.tmK, 0, y, bh, &bar[kFull0 + s]);
+        tma_load_3d(sm + Lay::oV + s * kBlk, &p.tmV, v0, y, bh, &bar[kFull0 + s]);
+        ++fills[s];
+    };
+    bool fail = false;
+    if (p.force_timeout) {  // test hook: a wait on a barrier nothing arrives on
+        if (tid == 0 && !mbar_wait(&bar[kNever], 0, lim)) record_status(p.dev_status, LA_ERR_TIMEOUT);
+        fail = true;
+    }
+    if (tid == 0 && !fail) {
+        issue_fill(0);
+        if (n > 1) issue_fill(1);
+    }
+
+    // ---- S^T <- the initial state (lanes 0..63: value columns v0 + lane, lane 64: z)
+    if (!fail) {
+        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int f = page_row(c0 + e);
+                float x = 0.f;
+                if (f >= 0) {
+                    if (row < kDVB) {
+                        if (p.S0) x = p.S0[((size_t)bh * kDF + f) * p.dv + v0 + row];
+                    } else if (row == kDVB) {
+                        if (p.z0) x = p.z0[(size_t)bh * kDF + f];
+                    }
+                }
+                r[e] = __float_as_uint(x);
+            }
+            tmem_st32(tbase + lane_off + kColS + c0, r);
+        }
+        tmem_st_wait();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // E3: S^T -> the bf16 B operand of MMA3 (K-major: row n = value column n; rows
+    // 64 and 65 = z's bf16 value and its residual), then S^T *= decay (skipped when
+    // `scale` is false).  Lanes 65..127 hold nothing.
+    auto e3 = [&](float decay, bool scale) {
+        if (q4 > 2) return;  // warp-uniform
+        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + lane_off + kColS + c0, r);
+            tmem_ld_wait();
+            char* base = sm + Lay::oSB + (c0 >> 6) * Lay::kSBBlk;
+            const int cb = c0 & 63;
+            if (row < kDVB) {
+#pragma unroll
+                for (int e8 = 0; e8 < 32; e8 += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
+                    *reinterpret_cast<uint4*>(base + sw128_offset(row, cb + e8)) = w;
+                }
+            } else if (row == kDVB) {
+#pragma unroll
+                for (int e8 = 0; e8 < 32; e8 += 8) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float x0 = __uint_as_float(r[e8 + e]), x1 = __uint_as_float(r[e8 + e + 1]);
+                        const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                        hw[e >> 1] = (uint32_t)__bfloat16_as_ushort(h0) |
+                                     ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                        lw[e >> 1] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    }
+                    *reinterpret_cast<uint4*>(base + sw128_offset(kDVB, cb + e8)) =
+                        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(base + sw128_offset(kDVB + 1, cb + e8)) =
+                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            if (scale) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * decay);
+                tmem_st32(tbase + lane_off + kColS + c0, r);
+            }
+        }
+        if (scale) tmem_st_wait();
+    };
+
+    // The feature tile of the chunk's queries (query = true: xi-scaled, with the
+    // raw q and k for MMA1) or keys (zeta-scaled); rows past the end are zero.
+    // Thread t builds row t mod 128: half 0 the outer-product rows a < 8, half 1
+    // the rows a >= 8 and the fifth block.
+    auto build_phi = [&](bool query, int s, int L) {
+        const int r = tid & (kC - 1), hh = tid >> 7;
+        const char* qsrc = sm + Lay::oQr + s * Lay::kRaw + r * (kD * 2);
+        const char* ksrc = sm + Lay::oKr + s * Lay::kRaw + r * (kD * 2);
+        float x[kD];
+        unpack16(query ? qsrc : ksrc, x);
+        float sc = 0.f;  // xi_r or zeta_r, zero past the end
+        if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(query ? r + 1 : L - 1 - r));
+        const float sq = sc * 0.70710678118654752f;  // and the outer product's 1 / sqrt 2
+        char* phi = sm + Lay::oPhi;
+        if (hh == 0) {
+            quad_rows<0>(phi, r, x, sq);
+        } else {
+            quad_rows<8>(phi, r, x, sq);
+            char* b4 = phi + 4 * kBlk;
+            uint4 w;
+            w.x = pack_bf16x2(x[0] * sc, x[1] * sc);
+            w.y = pack_bf16x2(x[2] * sc, x[3] * sc);
+            w.z = pack_bf16x2(x[4] * sc, x[5] * sc);
+            w.w = pack_bf16x2(x[6] * sc, x[7] * sc);
+            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 0)) = w;
+            w.x = pack_bf16x2(x[8] * sc, x[9] * sc);
+            w.y = pack_bf16x2(x[10] * sc, x[11] * sc);
+            w.z = pack_bf16x2(x[12] * sc, x[13] * sc);
+            w.w = pack_bf16x2(x[14] * sc, x[15] * sc);
+            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 8)) = w;
+            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 16)) = make_uint4(pack_bf16x2(sc, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 24)) = make_uint4(0u, 0u, 0u, 0u);
+            if (query) {  // the raw rows (the tile loads zero past the end of the sequence)
+                const uint4* qr = reinterpret_cast<const uint4*>(qsrc);
+                const uint4* kr = reinterpret_cast<const uint4*>(ksrc);
+                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 32)) = qr[0];
+                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 40)) = qr[1];
+                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 48)) = kr[0];
+                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 56)) = kr[1];
+            }
+        }
+    };
+
+    // E1 on 32 score columns j = cc .. cc + 31 of query row i: the Taylor kernel times
+    // gamma^(i - j) for j <= i < L, else 0, as 16 bf16 pairs
+    auto e1_piece = [&](const uint32_t (&r)[32], int cc, int i, int L, uint32_t (&out)[16]) {
+        const int jt = min(i, cc + 31);
+        float w = unit_gamma ? 1.f : gamma_pow(l2g, (float)max(i - jt, 0));
+        float xv[32];
+#pragma unroll
+        for (int e = 31; e >= 0; --e) {
+            const int j = cc + e;
+            const float s = __uint_as_float(r[e]);
+            float v = 0.f;
+            if (j <= i && i < L) {
+                v = fmaf(s, fmaf(0.5f, s, 1.f), 1.f) * w;
+                if (!unit_gamma) w *= gam;
+            }
+            xv[e] = v;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) out[e >> 1] = pack_bf16x2(xv[e], xv[e + 1]);
+    };
+
+    // E2: O rows -> global, divided by the normaliser
+    auto e2 = [&](int it, int L) {
+        const uint32_t ocol = tbase + lane_off + kColO;
+        float inv = 1.f;
+        if (p.normalize) {
+            const float den = __uint_as_float(tmem_ld1(ocol + kDVB)) + __uint_as_float(tmem_ld1(ocol + kDVB + 1));
+            tmem_ld_wait();
+            inv = 1.f / norm_den(den, p.normalize, p.eps);
+        }
+        uint32_t r[32];
+        tmem_ld32(ocol + 32 * half, r);
+        tmem_ld_wait();
+        if (row < L) {
+            __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 32 * half;
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + e8) = w;
+            }
+        }
+    };
+
+    // the final state in the page's feature order (z from the first value block only)
+    auto write_exit_state = [&]() {
+        if (q4 > 2 || (!p.S_out && !p.z_out)) return;  // warp-uniform
+        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + lane_off + kColS + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int f = page_row(c0 + e);
+                if (f < 0) continue;
+                if (row < kDVB) {
+                    if (p.S_out) p.S_out[((size_t)bh * kDF + f) * p.dv + v0 + row] = __uint_as_float(r[e]);
+                } else if (row == kDVB && vb == 0 && p.z_out) {
+                    p.z_out[(size_t)bh * kDF + f] = __uint_as_float(r[e]);
+                }
+            }
+        }
+    };
+
+    if (!fail) e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)min(kC, p.T)), !unit_gamma);
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // MMA descriptors and instruction descriptors (thread 0)
+    const uint64_t dPhiK = smem_desc_sw128(sbase + Lay::oPhi, 16, 1024);          // K-major
+    const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, 16, 1024);             // K-major
+    const uint64_t dPhiMN = smem_desc_sw128(sbase + Lay::oPhi, kBlk, 1024);       // MN-major, blocks 0..3
+    const uint64_t dPhiMN4 = smem_desc_sw128(sbase + Lay::oPhi + 4 * kBlk, kBlk, 1024);
+    constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t id_qs = idesc_bf16(128, kNV, 0, 0);
+    constexpr uint32_t id_pv = idesc_bf16(128, kNV, 0, 1);
+    constexpr uint32_t id_s256 = idesc_bf16(128, 256, 1, 1);
+    constexpr uint32_t id_s32 = idesc_bf16(128, 32, 1, 1);
+    bool mma_issued = false;
+    uint32_t mma_phase = 0;
+
+    for (int it = 0; it < n && !fail; ++it) {
+        const int s = it & 1;
+        const int L = min(kC, p.T - it * kC);
+        // the chunk's raw q, k and V
+        bool ok = mbar_wait(&bar[kFull0 + s], (it >> 1) & 1, lim);
+        if (__syncthreads_or(!ok)) {
+            fail = true;
+            break;
+        }
+        // ---- queries: features, then MMA1 (scores) and MMA3 (O = phi(Q) S)
+        build_phi(true, s, L);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            mma_ss(tbase + kColSc, desc_adv(dPhiK, 4 * kBlk + 64), desc_adv(dPhiK, 4 * kBlk + 96), id_qk, 0u);
+#pragma unroll
+            for (int kk = 0; kk < kFCols / 16; ++kk)
+                mma_ss(tbase + kColO, desc_adv(dPhiK, (kk >> 2) * kBlk + (kk & 3) * 32),
+                       desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
+            mma_commit(&bar[kMma]);
+            mma_issued = true;
+        }
+        ok = mbar_wait(&bar[kMma], mma_phase, lim);
+        mma_phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            fail = true;
+            break;
+        }
+        fence_after_sync();
+        // ---- E1: scores -> P (every score read before any P lands on them)
+        {
+            const int c0 = 64 * half;
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tbase + lane_off + kColSc + c0, ra);
+            tmem_ld32(tbase + lane_off + kColSc + c0 + 32, rb);
+            tmem_ld_wait();
+            __syncthreads();
+            uint32_t pa[16], pb[16];
+            e1_piece(ra, c0, row, L, pa);
+            e1_piece(rb, c0 + 32, row, L, pb);
+            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1), pa);
+            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1) + 16, pb);
+            tmem_st_wait();
+        }
+        // ---- keys: features (MMA1 and MMA3 are done with the query tile), then MMA2
+        // (O += P [V | 1]) and MMA4 (S^T += [V | 1]^T phi(K))
+        build_phi(false, s, L);
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t va = sbase + Lay::oV + s * kBlk;
+            const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk)
+                mma_ts(tbase + kColO, tbase + kColSc + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                mma_ss(tbase + kColS, desc_adv(dVo, kk * 2048), desc_adv(dPhiMN, kk * 2048), id_s256, 1u);
+                mma_ss(tbase + kColS + 256, desc_adv(dVo, kk * 2048), desc_adv(dPhiMN4, kk * 2048), id_s32,
+                       1u);
+            }
+            mma_commit(&bar[kMma]);
+        }
+        ok = mbar_wait(&bar[kMma], mma_phase, lim);
+        mma_phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            fail = true;
+            break;
+        }
+        fence_after_sync();
+        // the stage is free: the loads of chunk it + 2
+        if (tid == 0 && it + 2 < n) issue_fill(it + 2);
+        // ---- E2 (outputs) and E3 (the state for the next chunk) or the final state
+        e2(it, L);
+        if (it + 1 < n) {
+            const int Ln = min(kC, p.T - (it + 1) * kC);
+            e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)Ln), !unit_gamma);
+        } else {
+            write_exit_state();
+        }
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (fail) {
+        record_status(p.dev_status, LA_ERR_TIMEOUT);
+        if (tid == 0) {  // our own TMA fills and MMAs must land before smem and TMEM are released
+            for (int s = 0; s < 2; ++s)
+                if (fills[s] > 0) mbar_wait(&bar[kFull0 + s], (fills[s] - 1) & 1, lim);
+            if (mma_issued) {
+                mma_commit(&bar[kDrain]);
+                mbar_wait(&bar[kDrain], 0, lim);
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace
+
+bool taylor_supported(const ChunkArgs& a) {
+    return a.taylor && a.bf16 && a.dk == kD && a.dv > 0 && a.dv % kDVB == 0 && !a.noncausal &&
+           !a.phi && !a.log_a && (a.chunk == 0 || a.chunk == kC) && tck::tc_arch_ok();
+}
+
+int taylor_feature_dim(int d) { return 1 + d + d * d; }
+
+cudaError_t launch_chunk_taylor(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s) {
+    if (!taylor_supported(a)) return cudaErrorInvalidValue;
+    TaylorParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int BH = a.B * a.H;
+    if (!tck::make_map_box(&prm.tmQ, a.Q, BH, a.T, kD, kD, false) ||
+        !tck::make_map_box(&prm.tmK, a.K, BH, a.T, kD, kD, false) ||
+        !tck::make_map(&prm.tmV, a.V, BH, a.T, a.dv))
+        return cudaErrorInvalidValue;
+    prm.O = static_cast<__nv_bfloat16*>(a.O);
+    prm.S0 = a.S0;
+    prm.z0 = a.z0;
+    prm.S_out = a.S_out;
+    prm.z_out = a.z_out;
+    prm.H = a.H;
+    prm.T = a.T;
+    prm.dv = a.dv;
+    prm.n_dvb = a.dv / kDVB;
+    prm.normalize = norm_mode(a.normalize, a.floor_norm);
+    prm.eps = a.eps;
+    prm.dev_status = a.dev_status;
+    prm.wait_ns = 2000000000ull;
+    const char* ft = std::getenv("LA_DEBUG_FORCE_TIMEOUT");
+    if (ft && ft[0] == '1') {
+        prm.force_timeout = 1;
+        prm.wait_ns = 1000000ull;  // 1 ms
+    }
+    prm.g = g;
+    cudaError_t e = cudaFuncSetAttribute(chunk_taylor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    TraceScope trace("chunk_taylor_kernel", s);
+    chunk_taylor_kernel<<<BH * prm.n_dvb, kThreads, Lay::kAlloc, s>>>(prm);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -655,17 +655,29 @@ __global__ void gate_prep_kernel(const float* __restrict__ log_a, float* __restr
 }  // namespace
 
 namespace tck {
-bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
+bool make_map_box(CUtensorMap* m, const void* base, int BH, int T, int d, int box_x, bool swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)kC, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
+    return make_map_box(m, base, BH, T, d, 64, true);
+}
+bool tc_arch_ok() {
+    if (!encode_fn()) return false;
+    int dev = 0, major = 0, minor = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return major == 10 && minor == 3;
 }
 }  // namespace tck
 
@@ -679,12 +691,8 @@ bool tc_supported(const ChunkArgs& a) {
     // the per-token decay: causal, in the pipelined kernel only
     if (a.log_a && (a.noncausal || !tc_ws_supported(kFull, a.dk, tc_dvb(a), a.normalize)))
         return false;
-    if (!encode_fn()) return false;
-    int dev = 0, major = 0, minor = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    return major == 10 && minor == 3;
+    if (a.taylor) return false;  // the Taylor feature map has a kernel of its own
+    return tck::tc_arch_ok();
 }
 
 // Value columns per CTA: 64 or 128.  With the per-token decay 64 when

@@ -336,6 +336,10 @@ __device__ __forceinline__ float colsum_total(const float* part, int d) {
 
 // Host: 3-D TMA map [BH][T][d] bf16, box {64, 128, 1}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d);
+// [BH][T][d] bf16 with a box of box_x x 128 rows, 128-byte swizzle or none.
+bool make_map_box(CUtensorMap* m, const void* base, int BH, int T, int d, int box_x, bool swizzle);
+// The tensor-map encoder is reachable and the device is sm_103.
+bool tc_arch_ok();
 
 }  // namespace tck
 }  // namespace la

@@ -26,6 +26,9 @@ struct ChunkArgs {
     bool normalize;
     bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     bool noncausal;
+    // second-order Taylor feature map: q, k of width dk = 16, states of
+    // 1 + dk + dk^2 rows in the page's feature order
+    bool taylor;
     float eps;
     // per-token decay: device fp32 [B][H][T] natural logs, in place of the per-head
     // gammas (null: the gammas)
@@ -109,5 +112,11 @@ size_t tc_workspace_bytes(const ChunkArgs& a);
 int tc_launch_count(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
                             int* launches);
+
+// chunk_taylor.cu: causal attention with the Taylor feature map (bf16, d_k = 16,
+// d_v a multiple of 64), features built on chip
+bool taylor_supported(const ChunkArgs& a);
+int taylor_feature_dim(int d);
+cudaError_t launch_chunk_taylor(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s);
 
 }  // namespace la

@@ -64,7 +64,7 @@ def chunk(lib, **over):
 
 BAD_CHUNK_ARGS = [
     dict(B=-1), dict(H=-2), dict(T=-1), dict(dk=0), dict(dk=8), dict(dk=24), dict(dk=272),
-    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=32), dict(chunk=48), dict(chunk=256),
+    dict(dv=300), dict(dv=17), dict(dtype=2), dict(flags=64), dict(chunk=48), dict(chunk=256),
     dict(flags=la.LA_GATED),  # the per-token decay's planning flag: not a la_chunk_fwd flag
     dict(eps=float("nan")), dict(eps=-1.0), dict(Q=None), dict(V=None), dict(O=None),
     dict(Q=FAKE + 8), dict(O=FAKE + 0x400004), dict(S0=FAKE + 0x800004),
@@ -116,7 +116,7 @@ def chunk_gated(lib, **over):
 
 
 @pytest.mark.parametrize("over", [dict(log_a=None), dict(log_a=FAKE + 0x300004), dict(B=-1),
-                                  dict(dk=24), dict(flags=32), dict(Q=None), dict(eps=-1.0),
+                                  dict(dk=24), dict(flags=64), dict(Q=None), dict(eps=-1.0),
                                   dict(log_a=FAKE + 0x400000)],  # O overlaps log_a
                          ids=lambda d: ",".join(d))
 def test_chunk_fwd_gated_rejects(lib, over):
@@ -132,7 +132,7 @@ def test_workspace_size_takes_the_gated_flag(lib):
     for (B, H, T, dk, dv) in [(4, 8, 4096, 64, 64), (1, 8, 65536, 128, 128)]:
         n = lib.la_workspace_size(B, H, T, dk, dv, 1, la.LA_GATED, 0)
         assert n >= 0 and n % 16 == 0
-    assert lib.la_workspace_size(4, 8, 4096, 64, 64, 1, 32, 0) == 0  # unknown flag
+    assert lib.la_workspace_size(4, 8, 4096, 64, 64, 1, 64, 0) == 0  # unknown flag
 
 
 def bwd(lib, gated=False, **over):
@@ -149,7 +149,7 @@ def bwd(lib, gated=False, **over):
               a["ws_bytes"], a["st"], a["stream"])
 
 
-@pytest.mark.parametrize("over", [dict(B=-1), dict(dk=24), dict(dtype=3), dict(flags=32),
+@pytest.mark.parametrize("over", [dict(B=-1), dict(dk=24), dict(dtype=3), dict(flags=64),
                                   dict(dO=None), dict(dQ=None), dict(dK=FAKE + 0x500008),
                                   dict(dQ=FAKE + 0x300000),   # dQ overlaps dO
                                   dict(dV=FAKE + 0x400000),   # dV overlaps dQ
@@ -220,3 +220,36 @@ def test_python_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         la.recurrent_step(q[:, :, 0], q[:, :, 0], q[:, :, 0], [0.5], torch.zeros(1, 1, 16, 16),
                           out=q[:, :, 0].clone())
+
+
+TAYLOR_UNSUPPORTED = [
+    dict(dk=64), dict(dk=32), dict(dtype=0), dict(dv=48), dict(dv=16), dict(chunk=64),
+    dict(flags=la.LA_PHI_TAYLOR | la.LA_PHI_ELU1), dict(flags=la.LA_PHI_TAYLOR | la.LA_NONCAUSAL),
+]
+
+
+@pytest.mark.parametrize("over", TAYLOR_UNSUPPORTED, ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_taylor_outside_its_kernel_is_unsupported(lib, over):
+    """The Taylor feature map runs for bf16, d_k = 16, d_v a multiple of 64, causal,
+    without elu + 1 and with chunk 0 or 128; other combinations are refused before
+    any launch."""
+    a = dict(dk=16, dv=64, flags=la.LA_PHI_TAYLOR)
+    a.update(over)
+    assert chunk(lib, **a) == la.LA_ERR_UNSUPPORTED
+
+
+def test_taylor_is_refused_by_the_decode_step_and_the_backward_pass(lib):
+    assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert bwd(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert chunk_gated(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert lib.la_bwd_workspace_size(2, 8, 64, 16, 64, 1, la.LA_PHI_TAYLOR) == 0
+
+
+def test_taylor_plan_queries(lib):
+    """No workspace and one launch: the feature map's kernel has no segment plan."""
+    f = la.LA_PHI_TAYLOR | la.LA_NORMALIZE
+    assert lib.la_workspace_size(8, 16, 4096, 16, 64, 1, f, 0) == 0
+    assert lib.la_chunk_fwd_launches(8, 16, 4096, 16, 64, 1, f, 0) == 1
+    assert la.state_rows(16, "taylor") == 273 and la.state_rows(16) == 16
+    with pytest.raises(ValueError):
+        la._flags("softmax", False, True)

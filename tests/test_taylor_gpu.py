@@ -1,0 +1,170 @@
+"""The Taylor feature map (LA_PHI_TAYLOR) on the GPU against the fp64 oracle.
+
+The kernel builds phi(x) = (1, x, vec(x x^T)/sqrt 2) of the 16-wide queries and
+keys on chip (273 features); the oracle expands them in fp64 ("Linear attention"
+page, box "Taylor features") and runs the plain recurrence.  Shapes span one
+chunk and several, ragged tails, two value blocks, per-head decays and gamma = 1,
+with and without the normaliser, with an initial state, and the final state in
+the page's feature order.  Same metric and bf16 tolerance as the other parity
+tests: max|gpu - oracle| / max|oracle| <= 2e-2.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+import workloads
+
+la = pytest.importorskip("retnet_retention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+DEV = "cuda"
+DF = 273
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from retnet_retention_gb300 import _build
+    _build.build()
+    la.library()
+
+
+def check(name, got, want, tol=TOL):
+    assert np.all(np.isfinite(got)), f"{name}: non-finite output"
+    err = pins.rel_err(got, want)
+    assert err <= tol, f"{name}: rel err {err:.3e} > {tol:.0e}"
+
+
+def np64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def case(shape, gamma, seed_tag):
+    B, H, T, dv = shape
+    seed = zlib.crc32(repr((shape, gamma, seed_tag)).encode()) % 100000
+    return workloads.random_case(seed, B, H, T, 16, dv, dtype="bf16", gamma=gamma, scale=0.5)
+
+
+SHAPES = [  # B, H, T, d_v
+    (1, 2, 1, 64),
+    (1, 2, 77, 64),
+    (2, 2, 128, 64),
+    (2, 3, 300, 64),
+    (1, 2, 260, 128),
+    (1, 1, 1000, 64),
+]
+
+
+@pytest.mark.parametrize("normalize", [True, False], ids=["normalised", "plain"])
+@pytest.mark.parametrize("gamma", [None, 1.0], ids=["decayed", "gamma1"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_taylor_matches_oracle(shape, gamma, normalize):
+    x = case(shape, gamma, "taylor")
+    B, H, T, dv = shape
+    O, S, z = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
+                           phi="taylor", normalize=normalize,
+                           z_out=torch.empty((B, H, DF), device=DEV))
+    torch.cuda.synchronize()
+    assert S.shape == (B, H, DF, dv) and z.shape == (B, H, DF)
+    Or, Sr, zr = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"], normalize=normalize)
+    check("O", np64(O), Or)
+    check("S_T", np64(S), Sr)
+    check("z_T", np64(z), zr)
+
+
+@pytest.mark.parametrize("normalize", [True, False], ids=["normalised", "plain"])
+def test_taylor_from_an_initial_state(normalize):
+    """A chunked call resumed from the state of the first part equals one pass; the
+    initial state enters in the page's feature order."""
+    B, H, T, dv = 2, 2, 400, 64
+    x = case((B, H, T, dv), None, "resume")
+    rng = np.random.default_rng(5)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, DF, dv)).astype(np.float32) * 0.1)
+    z0 = torch.from_numpy(np.abs(rng.standard_normal((B, H, DF))).astype(np.float32) + 1.0)
+    O, S, z = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
+                           phi="taylor", normalize=normalize, S0=S0.to(DEV), z0=z0.to(DEV),
+                           z_out=torch.empty((B, H, DF), device=DEV))
+    torch.cuda.synchronize()
+    Or, Sr, zr = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"], normalize=normalize,
+                                         S0=S0, z0=z0)
+    check("O", np64(O), Or)
+    check("S_T", np64(S), Sr)
+    check("z_T", np64(z), zr)
+    # split at a chunk boundary and at a ragged point: the second part starts from the first's state
+    for cut in (128, 201):
+        q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+        O1, S1, z1 = la.chunk_fwd(q[:, :, :cut].contiguous(), k[:, :, :cut].contiguous(),
+                                  v[:, :, :cut].contiguous(), x["gamma"], phi="taylor",
+                                  normalize=normalize, S0=S0.to(DEV), z0=z0.to(DEV),
+                                  z_out=torch.empty((B, H, DF), device=DEV))
+        O2, S2, _ = la.chunk_fwd(q[:, :, cut:].contiguous(), k[:, :, cut:].contiguous(),
+                                 v[:, :, cut:].contiguous(), x["gamma"], phi="taylor",
+                                 normalize=normalize, S0=S1, z0=z1)
+        torch.cuda.synchronize()
+        check(f"O split at {cut}", np.concatenate([np64(O1), np64(O2)], axis=2), Or)
+        check(f"S_T split at {cut}", np64(S2), Sr)
+
+
+def test_taylor_empty_sequence_copies_the_state():
+    B, H, dv = 1, 2, 64
+    S0 = torch.randn(B, H, DF, dv, device=DEV)
+    q = torch.empty((B, H, 0, 16), dtype=torch.bfloat16, device=DEV)
+    v = torch.empty((B, H, 0, dv), dtype=torch.bfloat16, device=DEV)
+    _, S, _ = la.chunk_fwd(q, q, v, [0.9, 0.95], phi="taylor", S0=S0)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S0)
+
+
+def test_taylor_normalised_constant_values_return_unchanged():
+    """With the normaliser the outputs are convex combinations of the v rows (the
+    kernel is >= 1/2 > 0), so a constant V comes back unchanged."""
+    B, H, T, dv = 1, 2, 700, 64
+    x = case((B, H, T, dv), None, "const")
+    v = torch.full((B, H, T, dv), 0.375, dtype=torch.bfloat16)
+    O, _, _ = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), v.to(DEV), x["gamma"], phi="taylor",
+                           normalize=True)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(np64(O), 0.375, rtol=1e-2)
+
+
+def test_taylor_timeout_is_reported_not_hung(monkeypatch):
+    monkeypatch.setenv("LA_DEBUG_FORCE_TIMEOUT", "1")
+    x = case((1, 2, 256, 64), None, "timeout")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"], phi="taylor",
+                 dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == la.LA_ERR_TIMEOUT
+    monkeypatch.delenv("LA_DEBUG_FORCE_TIMEOUT")
+    status.zero_()
+    O, _, _ = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
+                           phi="taylor", dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    Or, _, _ = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"])
+    check("O after a reported timeout", np64(O), Or)
+
+
+def test_taylor_linear_attention_bf16_sampled():
+    """The Taylor workload at full size (B=8 H=16 T=4096, d=16 -> 273 features,
+    d_v=64, normalised, gamma = 1) in the launch the benchmark times; sampled
+    sequences checked against the oracle one by one, every output finite."""
+    c = workloads.CONFIGS["taylor_linear_attention_bf16"]
+    x = workloads.make_inputs(c)
+    B, H, T = c["B"], c["H"], c["T"]
+    O, S, z = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
+                           phi="taylor", normalize=True)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(O).all())
+    for (b, h) in workloads.sample_pairs(B, H, 4):
+        sl = lambda t: t[b, h][None, None]
+        Or, Sr, zr = oracle.recurrent_taylor(sl(x["q"]), sl(x["k"]), sl(x["v"]), [x["gamma"][h]],
+                                             normalize=True)
+        check(f"O[{b},{h}]", np64(O[b, h]), Or[0, 0])
+        check(f"S_T[{b},{h}]", np64(S[b, h]), Sr[0, 0])
+        check(f"z_T[{b},{h}]", np64(z[b, h]), zr[0, 0])

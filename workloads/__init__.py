@@ -67,6 +67,11 @@ CONFIGS = {
         index=6, B=4, H=16, T=4096, dk=128, dv=128, dtype="bf16", phi=False, normalize=False,
         causal=True, gamma=("msr", 8), gate=True, scale_q=128 ** -0.5, scale_k=128 ** -0.5,
         scale_v=1.0, seed=6),
+    # the second-order Taylor feature map (Based: q, k projected to d = 16, 1 + 16 + 256 =
+    # 273 features), normalised linear attention; q, k ~ N(0, 1/4) so that s = q.k ~ N(0, 1)
+    "taylor_linear_attention_bf16": dict(
+        index=7, B=8, H=16, T=4096, dk=16, dv=64, dtype="bf16", phi="taylor", normalize=True,
+        causal=True, gamma=("list", [1.0] * 16), scale_q=0.5, scale_k=0.5, scale_v=1.0, seed=7),
 }
 
 _THREADS = max(1, min(16, (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
