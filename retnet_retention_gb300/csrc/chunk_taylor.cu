@@ -7,22 +7,32 @@
 // d = 16 first, so d_phi = 273.  The queries and keys enter here at their width
 // of 16 (32 bytes a token, not 546): the CTA builds the features on chip.
 //
+// vec(x x^T) is symmetric, so the kernel keeps one feature per unordered pair:
+// x_a x_b for a < b and x_a^2 / sqrt 2 for a = b (136 features), then x and 1 —
+// 153 features whose dot products are the same 1 + s + s^2/2.  The state in
+// these coordinates is the symmetric part of the page's state (rows (a, b) and
+// (b, a) summed over sqrt 2); the antisymmetric part of an initial state never
+// changes but by the decay (every update k k^T is symmetric), so the final state
+// in the page's order is rebuilt exactly from the two.
+//
 // Per chunk of 128 tokens and block of 64 value columns, with xi_i = gamma^(i+1),
 // zeta_j = gamma^(L-1-j) (the forms of the per-head kernels):
 //   MMA1  s = q k^T                         (K = 16, the raw q and k)
 //   E1    P_ij = (1 + s + s^2/2) gamma^(i-j) for j <= i        (bf16, in TMEM)
-//   MMA3  O  = (xi . phi(Q)) S_bf16                            (K = 288 feature columns)
-//   MMA2  O += P [V | 1]                                       (row sums in column 64)
+//   MMA3  O  = (xi . phi(Q)) S_bf16                            (K = 160 feature columns)
 //   MMA4  S^T += [V | 1]^T (zeta . phi(K))                     (z rides as the row of the 1)
+//   MMA2  O += P [V | 1]                                       (row sums in column 64)
 //   E2    o_i = O_i / (O_i,64 + O_i,65) with the normaliser, else O_i
 //   E3    S_bf16 <- S (z as a bf16 value and its residual), S^T *= gamma^L(next chunk)
 // The state is held transposed in TMEM (lanes 0..63 the value columns, lane 64
-// z, 288 columns of features), so each TMEM lane is one row of MMA3's K-major
-// B operand and z needs no reduction of its own: it is S's column for an
-// all-ones value, the reading of z on the same page.
+// z, 160 feature columns), so each TMEM lane is one row of MMA3's K-major B
+// operand and z needs no reduction of its own: it is S's column for an all-ones
+// value, the reading of z on the same page.
 //
-// The CTA runs its phases in lockstep (256 threads; thread 0 issues the TMA
-// loads and the MMAs); the loads of chunk c + 1 overlap chunk c.
+// The CTA runs in lockstep (512 threads, four warps on each TMEM lane quarter;
+// thread 0 issues the TMA loads and the MMAs): both feature tiles and E2 of the
+// previous chunk, then MMA1, MMA3 and MMA4 at once; E1 runs beside MMA3/MMA4, E3
+// beside MMA2, and the loads of chunk c + 1 beside chunk c.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -39,30 +49,33 @@ namespace {
 using namespace tck;
 
 constexpr int kD = 16;                  // width of q and k
-constexpr int kDF = 1 + kD + kD * kD;   // 273 features
+constexpr int kDF = 1 + kD + kD * kD;   // 273 features in the page's order
+constexpr int kNP = kD * (kD + 1) / 2;  // 136 unordered pairs
 constexpr int kDVB = 64;                // value columns per CTA
 constexpr int kNV = kDVB + 16;          // O and S_bf16 width: values, normaliser (2), zeros
-constexpr int kThreads = 256;
-// Feature columns on chip, a fixed permutation of the page's order:
-//   [0, 256)    x_a x_b / sqrt 2 at column 16 a + b    (page index 17 + column)
-//   [256, 272)  x_a                                    (page index 1 + a)
-//   272         the constant 1                         (page index 0)
-//   [273, 288)  zero
-// and, in the query phase only, the raw q at [288, 304) and the raw k at
-// [304, 320) (MMA1's operands; MMA3 and MMA4 never read them).
-constexpr int kFB = 5;                  // 64-column blocks of the feature tile
-constexpr int kFCols = 288;             // feature columns the MMAs contract over
+constexpr int kThreads = 512;
+// Feature columns on chip:
+//   [0, 136)    pair p = (a, b), a <= b, a-major: x_a x_b, or x_a^2 / sqrt 2 for a = b
+//   [136, 152)  x_a
+//   152         the constant 1
+//   [153, 160)  zero
+// and, in the query tile only, the raw q at [160, 176) and the raw k at
+// [176, 192) (MMA1's operands; MMA3 never reads them).  16-byte pieces of 8
+// columns: pieces 0..16 the pairs, 17..18 x, 19 the constant, 20..23 raw.
+constexpr int kFB = 3;                  // 64-column blocks of a feature tile
+constexpr int kFCols = 160;             // feature columns the MMAs contract over
 // TMEM columns
-constexpr uint32_t kColS = 0;           // S^T, 288 columns
-constexpr uint32_t kColSc = 288;        // scores, then P (bf16 pairs)
-constexpr uint32_t kColO = 416;         // O, 80 columns
+constexpr uint32_t kColS = 0;           // S^T, 160 columns
+constexpr uint32_t kColSc = 160;        // scores, then P (bf16 pairs)
+constexpr uint32_t kColO = 288;         // O, 80 columns
 constexpr uint32_t kTmemCols = 512;
 
 struct Lay {
     static constexpr uint32_t kRaw = kC * kD * 2;                   // one raw q or k tile
     static constexpr uint32_t kSBBlk = kNV * 128;                   // one 64-column block of S_bf16
-    static constexpr uint32_t oPhi = 0;                             // feature tile, 5 x 16 KB
-    static constexpr uint32_t oSB = oPhi + kFB * kBlk;              // S_bf16, 5 x 10 KB
+    static constexpr uint32_t oPhiQ = 0;                            // query feature tile, 3 x 16 KB
+    static constexpr uint32_t oPhiK = oPhiQ + kFB * kBlk;           // key feature tile
+    static constexpr uint32_t oSB = oPhiK + kFB * kBlk;             // S_bf16, 3 x 10 KB
     static constexpr uint32_t oV = oSB + kFB * kSBBlk;              // V, two stages
     static constexpr uint32_t oOnes = oV + 2 * kBlk;                // the block after V: ones in column 0
     static constexpr uint32_t oQr = oOnes + kBlk;                   // raw q, two stages
@@ -71,12 +84,18 @@ struct Lay {
     static constexpr uint32_t kBytes = oBar + 128;
     static constexpr uint32_t kAlloc = kBytes + 1024;               // + alignment of the base
 };
-static_assert(Lay::oSB % 1024 == 0 && Lay::kSBBlk % 1024 == 0 && Lay::oV % 1024 == 0 &&
-                  Lay::oOnes % 1024 == 0,
+static_assert(Lay::oPhiK % 1024 == 0 && Lay::oSB % 1024 == 0 && Lay::kSBBlk % 1024 == 0 &&
+                  Lay::oV % 1024 == 0 && Lay::oOnes % 1024 == 0,
               "swizzled blocks need 1024-byte alignment");
 static_assert(Lay::kAlloc <= 227 * 1024, "shared memory budget");
 
-enum Bars { kFull0 = 0, kFull1 = 1, kMma = 2, kDrain = 3, kNever = 4, kNumBars = 5 };
+enum Bars {
+    kFull0 = 0, kFull1 = 1,
+    kScores = 2,  // MMA1 done
+    kState = 3,   // MMA1, MMA3, MMA4 done
+    kOut = 4,     // MMA2 (and everything before it) done
+    kDrain = 5, kNever = 6, kNumBars = 7
+};
 
 struct TaylorParams {
     CUtensorMap tmQ, tmK;   // [BH][T][16] bf16, box {16, 128, 1}, no swizzle
@@ -95,9 +114,26 @@ struct TaylorParams {
     KernelGammas g;
 };
 
-// The page's feature index of on-chip column c, or -1 for a padding column.
-__device__ __forceinline__ int page_row(int c) {
-    return c < 256 ? 17 + c : (c < 272 ? c - 255 : (c == 272 ? 0 : -1));
+// Pair index of (a, b), a <= b, a-major.
+__host__ __device__ constexpr int pair_index(int a, int b) { return a * kD - a * (a - 1) / 2 + (b - a); }
+static_assert(pair_index(kD - 1, kD - 1) == kNP - 1, "pair count");
+
+// The page rows an on-chip column stands for: (r1, r2) for a pair a < b (the state
+// value there is sqrt 2 times the symmetric part of rows r1 = (a, b), r2 = (b, a)),
+// (r1, -1) for the rest, (-1, -1) for padding.
+__device__ __forceinline__ int2 page_rows(int c) {
+    if (c < kNP) {
+        int a = 0, p = c;
+        while (p >= kD - a) {
+            p -= kD - a;
+            ++a;
+        }
+        const int b = a + p;
+        return a == b ? make_int2(17 + 17 * a, -1) : make_int2(17 + kD * a + b, 17 + kD * b + a);
+    }
+    if (c < kNP + kD) return make_int2(1 + c - kNP, -1);
+    if (c == kNP + kD) return make_int2(0, -1);
+    return make_int2(-1, -1);
 }
 
 __device__ __forceinline__ void unpack16(const char* src, float (&x)[kD]) {
@@ -112,24 +148,43 @@ __device__ __forceinline__ void unpack16(const char* src, float (&x)[kD]) {
     }
 }
 
-// The outer-product columns of rows a = A0 .. A0 + 7 of one token: x_a x_b sq at
-// column 16 a + b of the 128-byte-swizzled feature tile (row r).
-template <int A0>
-__device__ __forceinline__ void quad_rows(char* phi, int r, const float (&x)[kD], float sq) {
+__device__ __forceinline__ void store_piece(char* tile, int r, int piece, const float (&f)[8]) {
+    uint4 w;
+    w.x = pack_bf16x2(f[0], f[1]);
+    w.y = pack_bf16x2(f[2], f[3]);
+    w.z = pack_bf16x2(f[4], f[5]);
+    w.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(tile + (piece >> 3) * kBlk + sw128_offset(r, (piece & 7) * 8)) = w;
+}
+
+// Pieces [P0, P1) of the pair features of one token (row r of a 128-byte-swizzled
+// tile) from x and y = sc x: y_a x_b for a < b, y_a x_a / sqrt 2 for a = b.  The
+// pair index is a compile-time constant in every unrolled step.
+template <int P0, int P1>
+__device__ __forceinline__ void pair_pieces(char* tile, int r, const float (&x)[kD], const float (&y)[kD]) {
+    float buf[8];
 #pragma unroll
-    for (int a = A0; a < A0 + 8; ++a) {
-        const float xa = x[a] * sq;
+    for (int a = 0; a < kD; ++a)
 #pragma unroll
-        for (int b0 = 0; b0 < kD; b0 += 8) {
-            const int col = kD * a + b0;
-            uint4 w;
-            w.x = pack_bf16x2(xa * x[b0 + 0], xa * x[b0 + 1]);
-            w.y = pack_bf16x2(xa * x[b0 + 2], xa * x[b0 + 3]);
-            w.z = pack_bf16x2(xa * x[b0 + 4], xa * x[b0 + 5]);
-            w.w = pack_bf16x2(xa * x[b0 + 6], xa * x[b0 + 7]);
-            *reinterpret_cast<uint4*>(phi + (col >> 6) * kBlk + sw128_offset(r, col & 63)) = w;
+        for (int b = a; b < kD; ++b) {
+            const int p = pair_index(a, b);
+            if ((p >> 3) >= P0 && (p >> 3) < P1) {
+                buf[p & 7] = a == b ? y[a] * x[a] * 0.70710678118654752f : y[a] * x[b];
+                if ((p & 7) == 7) store_piece(tile, r, p >> 3, buf);
+            }
         }
-    }
+}
+
+// Pieces 17..19: y = sc x and the constant sc, zeros after it.
+__device__ __forceinline__ void linear_pieces(char* tile, int r, const float (&y)[kD], float sc) {
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = y[e];
+    store_piece(tile, r, 17, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = y[8 + e];
+    store_piece(tile, r, 18, f);
+    *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 24)) = make_uint4(pack_bf16x2(sc, 0.f), 0u, 0u, 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_constant__ TaylorParams p) {
@@ -147,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     const bool unit_gamma = gam == 1.f;
     const int n = (p.T + kC - 1) / kC;
     const uint64_t lim = p.wait_ns;
+    constexpr float kRs2 = 0.70710678118654752f;  // 1 / sqrt 2
+    constexpr int kPieces = kFCols / 32;          // 32-column pieces of the state
 
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
@@ -175,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     const uint32_t tbase = *slot;
     const uint32_t sbase = smem_addr(sm);
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
-    const int half = warp >> 2;               // two warps per quarter split the columns
+    const int grp = warp >> 2;                // four warps per quarter split the columns
     const int row = q4 * 32 + lane;           // TMEM lane of this thread
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // the state's columns each thread copies: 160 and 128
-    const int sc_begin = half == 0 ? 0 : 160, sc_end = half == 0 ? 160 : kFCols;
+    // this warp's 32-column pieces of the state: grp and grp + 4
+    const int n_own = grp + 4 < kPieces ? 2 : 1;
 
     int fills[2] = {0, 0};  // thread 0: TMA fills issued per stage
     auto issue_fill = [&](int it) {
@@ -201,20 +258,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
         if (n > 1) issue_fill(1);
     }
 
-    // ---- S^T <- the initial state (lanes 0..63: value columns v0 + lane, lane 64: z)
+    // ---- S^T <- the initial state in the kernel's coordinates (lanes 0..63: value
+    // columns v0 + lane, lane 64: z; a pair column takes the two page rows' sum over
+    // sqrt 2; other lanes zero)
     if (!fail) {
-        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+        const float* src = nullptr;
+        size_t stride = 0;
+        if (row < kDVB && p.S0) {
+            src = p.S0 + (size_t)bh * kDF * p.dv + v0 + row;
+            stride = p.dv;
+        } else if (row == kDVB && p.z0) {
+            src = p.z0 + (size_t)bh * kDF;
+            stride = 1;
+        }
+        for (int k = 0; k < n_own; ++k) {
+            const int c0 = (grp + 4 * k) * 32;
             uint32_t r[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int f = page_row(c0 + e);
+                const int2 pr = page_rows(c0 + e);
                 float x = 0.f;
-                if (f >= 0) {
-                    if (row < kDVB) {
-                        if (p.S0) x = p.S0[((size_t)bh * kDF + f) * p.dv + v0 + row];
-                    } else if (row == kDVB) {
-                        if (p.z0) x = p.z0[(size_t)bh * kDF + f];
-                    }
+                if (src && pr.x >= 0) {
+                    x = src[pr.x * stride];
+                    if (pr.y >= 0) x = (x + src[pr.y * stride]) * kRs2;
                 }
                 r[e] = __float_as_uint(x);
             }
@@ -231,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     // `scale` is false).  Lanes 65..127 hold nothing.
     auto e3 = [&](float decay, bool scale) {
         if (q4 > 2) return;  // warp-uniform
-        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+        for (int k = 0; k < n_own; ++k) {
+            const int c0 = (grp + 4 * k) * 32;
             uint32_t r[32];
             tmem_ld32(tbase + lane_off + kColS + c0, r);
             tmem_ld_wait();
@@ -274,45 +341,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
         if (scale) tmem_st_wait();
     };
 
-    // The feature tile of the chunk's queries (query = true: xi-scaled, with the
-    // raw q and k for MMA1) or keys (zeta-scaled); rows past the end are zero.
-    // Thread t builds row t mod 128: half 0 the outer-product rows a < 8, half 1
-    // the rows a >= 8 and the fifth block.
-    auto build_phi = [&](bool query, int s, int L) {
-        const int r = tid & (kC - 1), hh = tid >> 7;
-        const char* qsrc = sm + Lay::oQr + s * Lay::kRaw + r * (kD * 2);
-        const char* ksrc = sm + Lay::oKr + s * Lay::kRaw + r * (kD * 2);
-        float x[kD];
-        unpack16(query ? qsrc : ksrc, x);
+    // Both feature tiles of the chunk: queries xi-scaled (with the raw q and k for
+    // MMA1), keys zeta-scaled; rows past the end are zero.  Thread t builds row
+    // t mod 128 of one tile: quarters 0 / 1 the queries' pair pieces 0..10 / the
+    // rest with x, the constant and the raw rows; quarters 2 / 3 the same of the keys.
+    auto build_phi = [&](int s, int L) {
+        const int r = tid & (kC - 1), qq = tid >> 7;  // qq is warp-uniform
+        const bool is_q = qq < 2;
+        const char* src = sm + (is_q ? Lay::oQr : Lay::oKr) + s * Lay::kRaw + r * (kD * 2);
+        char* tile = sm + (is_q ? Lay::oPhiQ : Lay::oPhiK);
         float sc = 0.f;  // xi_r or zeta_r, zero past the end
-        if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(query ? r + 1 : L - 1 - r));
-        const float sq = sc * 0.70710678118654752f;  // and the outer product's 1 / sqrt 2
-        char* phi = sm + Lay::oPhi;
-        if (hh == 0) {
-            quad_rows<0>(phi, r, x, sq);
+        if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(is_q ? r + 1 : L - 1 - r));
+        float x[kD], y[kD];
+        unpack16(src, x);
+#pragma unroll
+        for (int a = 0; a < kD; ++a) y[a] = x[a] * sc;
+        if ((qq & 1) == 0) {
+            pair_pieces<0, 11>(tile, r, x, y);
         } else {
-            quad_rows<8>(phi, r, x, sq);
-            char* b4 = phi + 4 * kBlk;
-            uint4 w;
-            w.x = pack_bf16x2(x[0] * sc, x[1] * sc);
-            w.y = pack_bf16x2(x[2] * sc, x[3] * sc);
-            w.z = pack_bf16x2(x[4] * sc, x[5] * sc);
-            w.w = pack_bf16x2(x[6] * sc, x[7] * sc);
-            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 0)) = w;
-            w.x = pack_bf16x2(x[8] * sc, x[9] * sc);
-            w.y = pack_bf16x2(x[10] * sc, x[11] * sc);
-            w.z = pack_bf16x2(x[12] * sc, x[13] * sc);
-            w.w = pack_bf16x2(x[14] * sc, x[15] * sc);
-            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 8)) = w;
-            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 16)) = make_uint4(pack_bf16x2(sc, 0.f), 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 24)) = make_uint4(0u, 0u, 0u, 0u);
-            if (query) {  // the raw rows (the tile loads zero past the end of the sequence)
-                const uint4* qr = reinterpret_cast<const uint4*>(qsrc);
-                const uint4* kr = reinterpret_cast<const uint4*>(ksrc);
-                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 32)) = qr[0];
-                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 40)) = qr[1];
-                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 48)) = kr[0];
-                *reinterpret_cast<uint4*>(b4 + sw128_offset(r, 56)) = kr[1];
+            pair_pieces<11, 17>(tile, r, x, y);
+            linear_pieces(tile, r, y, sc);
+            if (is_q) {  // the raw rows (the tile loads zero past the end of the sequence)
+                const uint4* qr = reinterpret_cast<const uint4*>(src);
+                const uint4* kr = reinterpret_cast<const uint4*>(sm + Lay::oKr + s * Lay::kRaw + r * (kD * 2));
+                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 32)) = qr[0];
+                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 40)) = qr[1];
+                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 48)) = kr[0];
+                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 56)) = kr[1];
             }
         }
     };
@@ -326,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
 #pragma unroll
         for (int e = 31; e >= 0; --e) {
             const int j = cc + e;
-            const float s = __uint_as_float(r[e]);
+            const float sv = __uint_as_float(r[e]);
             float v = 0.f;
             if (j <= i && i < L) {
-                v = fmaf(s, fmaf(0.5f, s, 1.f), 1.f) * w;
+                v = fmaf(sv, fmaf(0.5f, sv, 1.f), 1.f) * w;
                 if (!unit_gamma) w *= gam;
             }
             xv[e] = v;
@@ -338,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
         for (int e = 0; e < 32; e += 2) out[e >> 1] = pack_bf16x2(xv[e], xv[e + 1]);
     };
 
-    // E2: O rows -> global, divided by the normaliser
+    // E2: O rows -> global, divided by the normaliser (16 value columns a warp)
     auto e2 = [&](int it, int L) {
         const uint32_t ocol = tbase + lane_off + kColO;
         float inv = 1.f;
@@ -347,13 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
             tmem_ld_wait();
             inv = 1.f / norm_den(den, p.normalize, p.eps);
         }
-        uint32_t r[32];
-        tmem_ld32(ocol + 32 * half, r);
+        uint32_t r[16];
+        tmem_ld16(ocol + 16 * grp, r);
         tmem_ld_wait();
         if (row < L) {
-            __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 32 * half;
+            __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 16 * grp;
 #pragma unroll
-            for (int e8 = 0; e8 < 32; e8 += 8) {
+            for (int e8 = 0; e8 < 16; e8 += 8) {
                 uint4 w;
                 w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
                 w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
@@ -364,21 +419,41 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
         }
     };
 
-    // the final state in the page's feature order (z from the first value block only)
+    // The final state in the page's feature order (z from the first value block
+    // only): a pair column gives rows (a, b) and (b, a) its value over sqrt 2, plus
+    // the decayed antisymmetric part of the initial state.
     auto write_exit_state = [&]() {
         if (q4 > 2 || (!p.S_out && !p.z_out)) return;  // warp-uniform
-        for (int c0 = sc_begin; c0 < sc_end; c0 += 32) {
+        float* dst = nullptr;
+        const float* src0 = nullptr;
+        size_t stride = 0;
+        if (row < kDVB && p.S_out) {
+            dst = p.S_out + (size_t)bh * kDF * p.dv + v0 + row;
+            src0 = p.S0 ? p.S0 + (size_t)bh * kDF * p.dv + v0 + row : nullptr;
+            stride = p.dv;
+        } else if (row == kDVB && vb == 0 && p.z_out) {
+            dst = p.z_out + (size_t)bh * kDF;
+            src0 = p.z0 ? p.z0 + (size_t)bh * kDF : nullptr;
+            stride = 1;
+        }
+        const float gT = unit_gamma ? 1.f : gamma_pow(l2g, (float)p.T);
+        for (int k = 0; k < n_own; ++k) {
+            const int c0 = (grp + 4 * k) * 32;
             uint32_t r[32];
             tmem_ld32(tbase + lane_off + kColS + c0, r);
             tmem_ld_wait();
+            if (!dst) continue;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int f = page_row(c0 + e);
-                if (f < 0) continue;
-                if (row < kDVB) {
-                    if (p.S_out) p.S_out[((size_t)bh * kDF + f) * p.dv + v0 + row] = __uint_as_float(r[e]);
-                } else if (row == kDVB && vb == 0 && p.z_out) {
-                    p.z_out[(size_t)bh * kDF + f] = __uint_as_float(r[e]);
+                const int2 pr = page_rows(c0 + e);
+                if (pr.x < 0) continue;
+                const float x = __uint_as_float(r[e]);
+                if (pr.y < 0) {
+                    dst[pr.x * stride] = x;
+                } else {
+                    const float anti = src0 ? 0.5f * gT * (src0[pr.x * stride] - src0[pr.y * stride]) : 0.f;
+                    dst[pr.x * stride] = x * kRs2 + anti;
+                    dst[pr.y * stride] = x * kRs2 - anti;
                 }
             }
         }
@@ -391,105 +466,110 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     fence_after_sync();
 
     // MMA descriptors and instruction descriptors (thread 0)
-    const uint64_t dPhiK = smem_desc_sw128(sbase + Lay::oPhi, 16, 1024);          // K-major
-    const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, 16, 1024);             // K-major
-    const uint64_t dPhiMN = smem_desc_sw128(sbase + Lay::oPhi, kBlk, 1024);       // MN-major, blocks 0..3
-    const uint64_t dPhiMN4 = smem_desc_sw128(sbase + Lay::oPhi + 4 * kBlk, kBlk, 1024);
+    const uint64_t dPhiQ = smem_desc_sw128(sbase + Lay::oPhiQ, 16, 1024);        // K-major
+    const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, 16, 1024);            // K-major
+    const uint64_t dPhiK = smem_desc_sw128(sbase + Lay::oPhiK, kBlk, 1024);      // MN-major
     constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t id_qs = idesc_bf16(128, kNV, 0, 0);
     constexpr uint32_t id_pv = idesc_bf16(128, kNV, 0, 1);
-    constexpr uint32_t id_s256 = idesc_bf16(128, 256, 1, 1);
-    constexpr uint32_t id_s32 = idesc_bf16(128, 32, 1, 1);
+    constexpr uint32_t id_st = idesc_bf16(128, kFCols, 1, 1);
     bool mma_issued = false;
-    uint32_t mma_phase = 0;
 
+    // every thread waits; false on a timeout anywhere
+    auto wait_all = [&](int b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(&bar[b], parity, lim);
+        const bool bad = __syncthreads_or(!ok);
+        fence_after_sync();
+        return !bad;
+    };
+
+    int L_prev = 0;
     for (int it = 0; it < n && !fail; ++it) {
         const int s = it & 1;
         const int L = min(kC, p.T - it * kC);
         // the chunk's raw q, k and V
-        bool ok = mbar_wait(&bar[kFull0 + s], (it >> 1) & 1, lim);
-        if (__syncthreads_or(!ok)) {
+        if (!wait_all(kFull0 + s, (it >> 1) & 1)) {
             fail = true;
             break;
         }
-        // ---- queries: features, then MMA1 (scores) and MMA3 (O = phi(Q) S)
-        build_phi(true, s, L);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after_sync();
-            mma_ss(tbase + kColSc, desc_adv(dPhiK, 4 * kBlk + 64), desc_adv(dPhiK, 4 * kBlk + 96), id_qk, 0u);
-#pragma unroll
-            for (int kk = 0; kk < kFCols / 16; ++kk)
-                mma_ss(tbase + kColO, desc_adv(dPhiK, (kk >> 2) * kBlk + (kk & 3) * 32),
-                       desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
-            mma_commit(&bar[kMma]);
-            mma_issued = true;
+        // ---- both feature tiles (MMA1, MMA3 and MMA4 of the previous chunk are done
+        // with them), and E2 of the previous chunk once its MMA2 is done: then its
+        // stage is free for the loads of chunk it + 1
+        build_phi(s, L);
+        if (it > 0) {
+            if (!wait_all(kOut, (it - 1) & 1)) {
+                fail = true;
+                break;
+            }
+            if (tid == 0 && it + 1 < n) issue_fill(it + 1);
+            e2(it - 1, L_prev);
         }
-        ok = mbar_wait(&bar[kMma], mma_phase, lim);
-        mma_phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
-            fail = true;
-            break;
-        }
-        fence_after_sync();
-        // ---- E1: scores -> P (every score read before any P lands on them)
-        {
-            const int c0 = 64 * half;
-            uint32_t ra[32], rb[32];
-            tmem_ld32(tbase + lane_off + kColSc + c0, ra);
-            tmem_ld32(tbase + lane_off + kColSc + c0 + 32, rb);
-            tmem_ld_wait();
-            __syncthreads();
-            uint32_t pa[16], pb[16];
-            e1_piece(ra, c0, row, L, pa);
-            e1_piece(rb, c0 + 32, row, L, pb);
-            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1), pa);
-            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1) + 16, pb);
-            tmem_st_wait();
-        }
-        // ---- keys: features (MMA1 and MMA3 are done with the query tile), then MMA2
-        // (O += P [V | 1]) and MMA4 (S^T += [V | 1]^T phi(K))
-        build_phi(false, s, L);
         fence_proxy_async_smem();
         fence_before_sync();
         __syncthreads();
+        // ---- MMA1 (scores), MMA3 (O = phi(Q) S), MMA4 (S^T += [V | 1]^T phi(K)):
+        // MMA3 reads S_bf16 and MMA4 the scaled S^T, both written by E3 before
+        const uint32_t va = sbase + Lay::oV + s * kBlk;
+        const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major [V | 1]
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t va = sbase + Lay::oV + s * kBlk;
-            const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major
+            mma_ss(tbase + kColSc, desc_adv(dPhiQ, 2 * kBlk + 64), desc_adv(dPhiQ, 2 * kBlk + 96), id_qk, 0u);
+            mma_commit(&bar[kScores]);
+#pragma unroll
+            for (int kk = 0; kk < kFCols / 16; ++kk)
+                mma_ss(tbase + kColO, desc_adv(dPhiQ, (kk >> 2) * kBlk + (kk & 3) * 32),
+                       desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < kC / 16; ++kk)
-                mma_ts(tbase + kColO, tbase + kColSc + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
-#pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                mma_ss(tbase + kColS, desc_adv(dVo, kk * 2048), desc_adv(dPhiMN, kk * 2048), id_s256, 1u);
-                mma_ss(tbase + kColS + 256, desc_adv(dVo, kk * 2048), desc_adv(dPhiMN4, kk * 2048), id_s32,
-                       1u);
-            }
-            mma_commit(&bar[kMma]);
+                mma_ss(tbase + kColS, desc_adv(dVo, kk * 2048), desc_adv(dPhiK, kk * 2048), id_st, 1u);
+            mma_commit(&bar[kState]);
+            mma_issued = true;
         }
-        ok = mbar_wait(&bar[kMma], mma_phase, lim);
-        mma_phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
+        // ---- E1 beside MMA3 / MMA4: scores -> P (every score read before any P lands)
+        if (!wait_all(kScores, it & 1)) {
             fail = true;
             break;
         }
-        fence_after_sync();
-        // the stage is free: the loads of chunk it + 2
-        if (tid == 0 && it + 2 < n) issue_fill(it + 2);
-        // ---- E2 (outputs) and E3 (the state for the next chunk) or the final state
-        e2(it, L);
+        {
+            const int c0 = 32 * grp;
+            uint32_t ra[32];
+            tmem_ld32(tbase + lane_off + kColSc + c0, ra);
+            tmem_ld_wait();
+            __syncthreads();
+            uint32_t pa[16];
+            e1_piece(ra, c0, row, L, pa);
+            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1), pa);
+            tmem_st_wait();
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {  // MMA2: O += P [V | 1]
+            fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk)
+                mma_ts(tbase + kColO, tbase + kColSc + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
+            mma_commit(&bar[kOut]);
+        }
+        // ---- E3 beside MMA2, once MMA3 and MMA4 are done: the state for the next
+        // chunk, or the final state
+        if (!wait_all(kState, it & 1)) {
+            fail = true;
+            break;
+        }
         if (it + 1 < n) {
             const int Ln = min(kC, p.T - (it + 1) * kC);
             e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)Ln), !unit_gamma);
         } else {
             write_exit_state();
         }
-        fence_proxy_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+        L_prev = L;
+    }
+    // E2 of the last chunk
+    if (!fail && n > 0) {
+        if (wait_all(kOut, (n - 1) & 1))
+            e2(n - 1, L_prev);
+        else
+            fail = true;
     }
 
     fence_before_sync();
