@@ -54,28 +54,38 @@ TRAFFIC = {
 HEADLINE = "linear_attention_bf16"
 # the backward pass on the tensor cores: plain retention, d_k = d_v = 128
 BWD_TC = "long_retention_bf16"
+# the second-order Taylor feature map (273 features from d = 16)
+TAYLOR = "taylor_linear_attention_bf16"
 L2_BYTES = 129 * 1024 * 1024
 C_REF = 64  # chunk length fixed for counting useful intra-chunk flops
 
 
 # ----------------------------------------------------------------------------- accounting
 
+def feature_dim(c: dict) -> int:
+    """Rows of the state: d_k, or 1 + d_k + d_k^2 with the Taylor feature map."""
+    return 1 + c["dk"] + c["dk"] ** 2 if c["phi"] == "taylor" else c["dk"]
+
+
 def alg_bytes(c: dict) -> int:
     """Bytes the method must move: read Q, K, V (and the per-token log decays),
     write O, write S_T (and z_T) in fp32."""
     es = 2 if c["dtype"] == "bf16" else 4
     nbh = c["B"] * c["H"]
+    df = feature_dim(c)
     io = nbh * c["T"] * ((2 * c["dk"] + 2 * c["dv"]) * es + (4 if c.get("gate") else 0))
-    state = nbh * c["dk"] * c["dv"] * 4 + (nbh * c["dk"] * 4 if c["normalize"] else 0)
+    state = nbh * df * c["dv"] * 4 + (nbh * df * 4 if c["normalize"] else 0)
     return io + state
 
 
 def alg_flops(c: dict) -> int:
-    """Useful flops: 4 d_k d_v per head-token (state update + read-out, the right
+    """Useful flops: 4 d_phi d_v per head-token (state update + read-out, the right
     order of "Moving the parentheses") plus the causal lower triangle of C_REF-long
-    intra-chunk squares, C_REF (d_k + d_v) per head-token."""
+    intra-chunk squares, C_REF (d_phi + d_v) per head-token; d_phi = d_k, or 273
+    features with the Taylor map."""
     nbh = c["B"] * c["H"]
-    return nbh * c["T"] * (4 * c["dk"] * c["dv"] + C_REF * (c["dk"] + c["dv"]))
+    df = feature_dim(c)
+    return nbh * c["T"] * (4 * df * c["dv"] + C_REF * (df + c["dv"]))
 
 
 def decode_bytes(c: dict) -> int:
@@ -92,7 +102,8 @@ def decode_flops(c: dict) -> int:
 
 def describe(name: str, c: dict) -> str:
     bits = [f"{name}: B={c['B']} H={c['H']} T={c['T']} d_k={c['dk']} d_v={c['dv']}",
-            c["dtype"], "phi=elu+1" if c["phi"] else "phi=identity"]
+            c["dtype"], {True: "phi=elu+1", False: "phi=identity",
+                         "taylor": f"phi=Taylor (2nd order, {feature_dim(c)} features)"}[c["phi"]]]
     if c.get("gate"):
         bits.append("per-token decay")
     bits += [
@@ -250,8 +261,8 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
     for _ in range(n_sets):
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         O = torch.empty(shape_v, dtype=qd.dtype, device=dev)
-        S = torch.empty(B, c["H"], c["dk"], c["dv"], device=dev)
-        z = torch.empty(B, c["H"], c["dk"], device=dev) if c["normalize"] else None
+        S = torch.empty(B, c["H"], feature_dim(c), c["dv"], device=dev)
+        z = torch.empty(B, c["H"], feature_dim(c), device=dev) if c["normalize"] else None
         lad = log_a.to(dev) if gated else None
         sets.append((qd, kd, vd, O, S, z, lad))
     ws_n = la.workspace_size(B, c["H"], c["T"], c["dk"], c["dv"], qd.dtype, c["phi"],
@@ -269,7 +280,8 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
         step(i)
     ms = time_region(step, steps, stream)
     kernels = kernel_breakdown(la, step, steps, stream)
-    flags = ((la.LA_PHI_ELU1 if c["phi"] else 0) | (la.LA_NORMALIZE if c["normalize"] else 0)
+    flags = ((la.LA_PHI_TAYLOR if c["phi"] == "taylor" else la.LA_PHI_ELU1 if c["phi"] else 0)
+             | (la.LA_NORMALIZE if c["normalize"] else 0)
              | (la.LA_NORM_FLOOR if c.get("floor") else 0) | (la.LA_GATED if gated else 0))
     launches = la.library().la_chunk_fwd_launches(B, c["H"], c["T"], c["dk"], c["dv"],
                                                   1 if c["dtype"] == "bf16" else 0, flags, 0)
@@ -459,7 +471,7 @@ def run_ours(args) -> dict | None:
                               "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
         return None
     if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
-                "gated_retention_bf16"):  # profiling aid
+                "gated_retention_bf16", TAYLOR):  # profiling aid
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
         if rank == 0:
             print(json.dumps({"only": only, "ms_per_step": r["ms"],
@@ -476,7 +488,7 @@ def run_ours(args) -> dict | None:
     headline_only = args.headline_only or only == "headline"
     if not headline_only:
         for name in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
-                     "gated_retention_bf16"):
+                     "gated_retention_bf16", TAYLOR):
             r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             others[name] = r
@@ -549,12 +561,17 @@ def run_ours(args) -> dict | None:
             tf = r["alg_flops"] / (r["ms"] * 1e-3) / 1e12
             dn, dk_ = max(r["kernels"].items(), key=lambda kv: kv[1]["total_ms"])
             kgbs = r["alg_bytes"] / (dk_["avg_ms"] * 1e-3) / 1e9
+            ktf = r["alg_flops"] / (dk_["avg_ms"] * 1e-3) / 1e12
+            # the bound: whichever of the algorithmic bytes and flops takes longer at peak
+            tensor = r["alg_flops"] / (pk["bf16_tflops"] * 1e12) > r["alg_bytes"] / (pk["hbm_gbs"] * 1e9)
             sub[name] = dict(workload=describe(name, rc), tokens_per_s=r["tokens"] * world /
                              (r["ms"] * 1e-3), ms=r["ms"], alg_gbs=gbs,
                              step_roofline_frac=gbs / pk["hbm_gbs"], tflops_useful=tf,
                              pct_bf16_peak=100.0 * tf / pk["bf16_tflops"],
-                             dominant_kernel=dn, kernel_gbs=kgbs,
-                             roofline_frac=kgbs / pk["hbm_gbs"], kernels=r["kernels"])
+                             dominant_kernel=dn, kernel_gbs=kgbs, kernel_tflops=ktf,
+                             bound="tensor" if tensor else "hbm",
+                             roofline_frac=(ktf / pk["bf16_tflops"]) if tensor else kgbs / pk["hbm_gbs"],
+                             kernels=r["kernels"])
         dc = dec["config"]
         gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
         for name, bwd in bwds.items():
@@ -635,7 +652,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
                                        "retention_floor_bf16", "gated_retention_bf16", "decode",
-                                       "backward", "backward_long_retention_bf16"),
+                                       "backward", "backward_long_retention_bf16", TAYLOR),
                     default=None,
                     help="profiling aid: run one workload only")
     ap.add_argument("--decode-steps", type=int,
