@@ -29,10 +29,11 @@
 // operand and z needs no reduction of its own: it is S's column for an all-ones
 // value, the reading of z on the same page.
 //
-// The CTA runs in lockstep (512 threads, four warps on each TMEM lane quarter;
-// thread 0 issues the TMA loads and the MMAs): both feature tiles and E2 of the
-// previous chunk, then MMA1, MMA3 and MMA4 at once; E1 runs beside MMA3/MMA4, E3
-// beside MMA2, and the loads of chunk c + 1 beside chunk c.
+// Warp roles: a TMA warp, an MMA warp and sixteen worker warps (four on each TMEM
+// lane quarter) that run E1, then E3 together with the feature tiles of the next
+// chunk as soon as MMA3 / MMA4 are done, then E2; mbarriers hand over between the
+// roles, every wait bounded in time.  E1 touches only the score pieces on or
+// below the diagonal.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -53,7 +54,10 @@ constexpr int kDF = 1 + kD + kD * kD;   // 273 features in the page's order
 constexpr int kNP = kD * (kD + 1) / 2;  // 136 unordered pairs
 constexpr int kDVB = 64;                // value columns per CTA
 constexpr int kNV = kDVB + 16;          // O and S_bf16 width: values, normaliser (2), zeros
-constexpr int kThreads = 512;
+constexpr int kWarpW = 2;               // first worker warp
+constexpr int kThreadsW = 512;          // sixteen worker warps
+constexpr int kThreads = 32 * kWarpW + kThreadsW;  // 576
+constexpr int kBarW = 1;                // the workers' named barrier
 // Feature columns on chip:
 //   [0, 136)    pair p = (a, b), a <= b, a-major: x_a x_b, or x_a^2 / sqrt 2 for a = b
 //   [136, 152)  x_a
@@ -66,8 +70,9 @@ constexpr int kFB = 3;                  // 64-column blocks of a feature tile
 constexpr int kFCols = 160;             // feature columns the MMAs contract over
 // TMEM columns
 constexpr uint32_t kColS = 0;           // S^T, 160 columns
-constexpr uint32_t kColSc = 160;        // scores, then P (bf16 pairs)
-constexpr uint32_t kColO = 288;         // O, 80 columns
+constexpr uint32_t kColSc = 160;        // scores (fp32)
+constexpr uint32_t kColP = 288;         // P (bf16 pairs), 64 columns
+constexpr uint32_t kColO = 352;         // O, 80 columns
 constexpr uint32_t kTmemCols = 512;
 
 struct Lay {
@@ -81,7 +86,8 @@ struct Lay {
     static constexpr uint32_t oQr = oOnes + kBlk;                   // raw q, two stages
     static constexpr uint32_t oKr = oQr + 2 * kRaw;                 // raw k, two stages
     static constexpr uint32_t oBar = oKr + 2 * kRaw;
-    static constexpr uint32_t kBytes = oBar + 128;
+    static constexpr uint32_t oSlot = oBar + 192;                  // TMEM base, abort flag
+    static constexpr uint32_t kBytes = oBar + 256;
     static constexpr uint32_t kAlloc = kBytes + 1024;               // + alignment of the base
 };
 static_assert(Lay::oPhiK % 1024 == 0 && Lay::oSB % 1024 == 0 && Lay::kSBBlk % 1024 == 0 &&
@@ -90,12 +96,18 @@ static_assert(Lay::oPhiK % 1024 == 0 && Lay::oSB % 1024 == 0 && Lay::kSBBlk % 10
 static_assert(Lay::kAlloc <= 227 * 1024, "shared memory budget");
 
 enum Bars {
-    kFull0 = 0, kFull1 = 1,
-    kScores = 2,  // MMA1 done
-    kState = 3,   // MMA1, MMA3, MMA4 done
-    kOut = 4,     // MMA2 (and everything before it) done
-    kDrain = 5, kNever = 6, kNumBars = 7
+    kFull0 = 0, kFull1 = 1,    // a stage's raw q, k and V landed (TMA)
+    kEmpty0 = 2, kEmpty1 = 3,  // a stage read: the workers (raw q, k) and MMA2 / MMA4 (V)
+    kPhiReady = 4,             // both feature tiles built
+    kSready = 5,               // S_bf16 and the scaled S^T in place (E3, or the initial state)
+    kOfree = 6,                // E2 has read O
+    kPready = 7,               // P in TMEM (E1)
+    kScores = 8,               // MMA1 done
+    kState = 9,                // MMA1, MMA3, MMA4 done: the feature tiles are free again
+    kOut = 10,                 // MMA2 done
+    kDrain = 11, kNever = 12, kNumBars = 13
 };
+static_assert(kNumBars * 8 <= 192, "mbarrier slots");
 
 struct TaylorParams {
     CUtensorMap tmQ, tmK;   // [BH][T][16] bf16, box {16, 128, 1}, no swizzle
@@ -191,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     extern __shared__ __align__(1024) char smem_raw[];
     char* sm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oBar + 64);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Lay::oSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::oSlot + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
@@ -207,12 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
 
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
+        mbar_init(&bar[kEmpty0], 2);
+        mbar_init(&bar[kEmpty1], 2);
+        *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&p.tmQ);
         prefetch_tensormap(&p.tmK);
         prefetch_tensormap(&p.tmV);
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(slot, kTmemCols);
         tmem_relinquish();
     }
@@ -231,365 +247,383 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
     fence_after_sync();
     const uint32_t tbase = *slot;
     const uint32_t sbase = smem_addr(sm);
-    const int q4 = warp & 3;                  // TMEM lane quarter of this warp
-    const int grp = warp >> 2;                // four warps per quarter split the columns
-    const int row = q4 * 32 + lane;           // TMEM lane of this thread
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // this warp's 32-column pieces of the state: grp and grp + 4
-    const int n_own = grp + 4 < kPieces ? 2 : 1;
 
-    int fills[2] = {0, 0};  // thread 0: TMA fills issued per stage
-    auto issue_fill = [&](int it) {
-        const int s = it & 1;
-        const int y = it * kC;
-        mbar_arrive_expect_tx(&bar[kFull0 + s], 2 * Lay::kRaw + kBlk);
-        tma_load_3d(sm + Lay::oQr + s * Lay::kRaw, &p.tmQ, 0, y, bh, &bar[kFull0 + s]);
-        tma_load_3d(sm + Lay::oKr + s * Lay::kRaw, &p.tmK, 0, y, bh, &bar[kFull0 + s]);
-        tma_load_3d(sm + Lay::oV + s * kBlk, &p.tmV, v0, y, bh, &bar[kFull0 + s]);
-        ++fills[s];
-    };
-    bool fail = false;
+    bool forced = false;
     if (p.force_timeout) {  // test hook: a wait on a barrier nothing arrives on
         if (tid == 0 && !mbar_wait(&bar[kNever], 0, lim)) record_status(p.dev_status, LA_ERR_TIMEOUT);
-        fail = true;
+        forced = true;
     }
-    if (tid == 0 && !fail) {
-        issue_fill(0);
-        if (n > 1) issue_fill(1);
-    }
+    int fills[2] = {0, 0};    // producer: TMA fills issued per stage
+    bool mma_issued = false;  // issuer: any MMA issued
 
-    // ---- S^T <- the initial state in the kernel's coordinates (lanes 0..63: value
-    // columns v0 + lane, lane 64: z; a pair column takes the two page rows' sum over
-    // sqrt 2; other lanes zero)
-    if (!fail) {
-        const float* src = nullptr;
-        size_t stride = 0;
-        if (row < kDVB && p.S0) {
-            src = p.S0 + (size_t)bh * kDF * p.dv + v0 + row;
-            stride = p.dv;
-        } else if (row == kDVB && p.z0) {
-            src = p.z0 + (size_t)bh * kDF;
-            stride = 1;
-        }
-        for (int k = 0; k < n_own; ++k) {
-            const int c0 = (grp + 4 * k) * 32;
-            uint32_t r[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int2 pr = page_rows(c0 + e);
-                float x = 0.f;
-                if (src && pr.x >= 0) {
-                    x = src[pr.x * stride];
-                    if (pr.y >= 0) x = (x + src[pr.y * stride]) * kRs2;
-                }
-                r[e] = __float_as_uint(x);
+    if (!forced && n > 0) {
+        if (warp == 0 && lane == 0) {
+            // ---------------- producer: raw q, k and V of each chunk, two stages
+            for (int it = 0; it < n; ++it) {
+                const int s = it & 1;
+                if (it >= 2 && !mbar_wait_or_abort(&bar[kEmpty0 + s], ((it - 2) >> 1) & 1, lim, abort_flag))
+                    break;
+                const int y = it * kC;
+                mbar_arrive_expect_tx(&bar[kFull0 + s], 2 * Lay::kRaw + kBlk);
+                tma_load_3d(sm + Lay::oQr + s * Lay::kRaw, &p.tmQ, 0, y, bh, &bar[kFull0 + s]);
+                tma_load_3d(sm + Lay::oKr + s * Lay::kRaw, &p.tmK, 0, y, bh, &bar[kFull0 + s]);
+                tma_load_3d(sm + Lay::oV + s * kBlk, &p.tmV, v0, y, bh, &bar[kFull0 + s]);
+                ++fills[s];
             }
-            tmem_st32(tbase + lane_off + kColS + c0, r);
-        }
-        tmem_st_wait();
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer
+            const uint64_t dPhiQ = smem_desc_sw128(sbase + Lay::oPhiQ, 16, 1024);        // K-major
+            const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, 16, 1024);            // K-major
+            const uint64_t dPhiK = smem_desc_sw128(sbase + Lay::oPhiK, kBlk, 1024);      // MN-major
+            constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_qs = idesc_bf16(128, kNV, 0, 0);
+            constexpr uint32_t id_pv = idesc_bf16(128, kNV, 0, 1);
+            constexpr uint32_t id_st = idesc_bf16(128, kFCols, 1, 1);
+            for (int it = 0; it < n; ++it) {
+                const int s = it & 1;
+                // the chunk's feature tiles, the state from E3 of the previous chunk, and
+                // O read out by E2 of the previous chunk
+                if (!mbar_wait_or_abort(&bar[kPhiReady], it & 1, lim, abort_flag)) break;
+                if (!mbar_wait_or_abort(&bar[kSready], it & 1, lim, abort_flag)) break;
+                if (it >= 1 && !mbar_wait_or_abort(&bar[kOfree], (it - 1) & 1, lim, abort_flag)) break;
+                fence_after_sync();
+                const uint32_t va = sbase + Lay::oV + s * kBlk;
+                const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major [V | 1]
+                // MMA1: scores = q k^T (the raw rows of the query tile)
+                mma_ss(tbase + kColSc, desc_adv(dPhiQ, 2 * kBlk + 64), desc_adv(dPhiQ, 2 * kBlk + 96), id_qk, 0u);
+                mma_commit(&bar[kScores]);
+                mma_issued = true;
+                // MMA3: O = phi(Q) S_bf16;  MMA4: S^T += [V | 1]^T phi(K)
+#pragma unroll
+                for (int kk = 0; kk < kFCols / 16; ++kk)
+                    mma_ss(tbase + kColO, desc_adv(dPhiQ, (kk >> 2) * kBlk + (kk & 3) * 32),
+                           desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ss(tbase + kColS, desc_adv(dVo, kk * 2048), desc_adv(dPhiK, kk * 2048), id_st, 1u);
+                mma_commit(&bar[kState]);
+                // MMA2: O += P [V | 1] once E1 has P in TMEM
+                if (!mbar_wait_or_abort(&bar[kPready], it & 1, lim, abort_flag)) break;
+                fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_ts(tbase + kColO, tbase + kColP + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
+                mma_commit(&bar[kOut]);
+                mma_commit(&bar[kEmpty0 + s]);
+            }
+        } else if (warp >= kWarpW) {
+            // ---------------- workers: four warps on each TMEM lane quarter
+            const int t = tid - 32 * kWarpW;          // 0 .. 511
+            const int q4 = warp & 3;                  // TMEM lane quarter of this warp
+            const int sub = t >> 7;                   // which of the quarter's four warps (warp-uniform)
+            const int row = q4 * 32 + lane;           // TMEM lane of this thread
+            const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+            // this warp's 32-column pieces of the state: sub and sub + 4
+            const int n_own = sub + 4 < kPieces ? 2 : 1;
 
-    // E3: S^T -> the bf16 B operand of MMA3 (K-major: row n = value column n; rows
-    // 64 and 65 = z's bf16 value and its residual), then S^T *= decay (skipped when
-    // `scale` is false).  Lanes 65..127 hold nothing.
-    auto e3 = [&](float decay, bool scale) {
-        if (q4 > 2) return;  // warp-uniform
-        for (int k = 0; k < n_own; ++k) {
-            const int c0 = (grp + 4 * k) * 32;
-            uint32_t r[32];
-            tmem_ld32(tbase + lane_off + kColS + c0, r);
-            tmem_ld_wait();
-            char* base = sm + Lay::oSB + (c0 >> 6) * Lay::kSBBlk;
-            const int cb = c0 & 63;
-            if (row < kDVB) {
-#pragma unroll
-                for (int e8 = 0; e8 < 32; e8 += 8) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
-                    w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
-                    w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
-                    w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
-                    *reinterpret_cast<uint4*>(base + sw128_offset(row, cb + e8)) = w;
+            // S^T <- the initial state in the kernel's coordinates (lanes 0..63: value
+            // columns v0 + lane, lane 64: z; a pair column takes the two page rows'
+            // sum over sqrt 2; other lanes zero)
+            {
+                const float* src = nullptr;
+                size_t stride = 0;
+                if (row < kDVB && p.S0) {
+                    src = p.S0 + (size_t)bh * kDF * p.dv + v0 + row;
+                    stride = p.dv;
+                } else if (row == kDVB && p.z0) {
+                    src = p.z0 + (size_t)bh * kDF;
+                    stride = 1;
                 }
-            } else if (row == kDVB) {
+                for (int k = 0; k < n_own; ++k) {
+                    const int c0 = (sub + 4 * k) * 32;
+                    uint32_t r[32];
 #pragma unroll
-                for (int e8 = 0; e8 < 32; e8 += 8) {
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const float x0 = __uint_as_float(r[e8 + e]), x1 = __uint_as_float(r[e8 + e + 1]);
-                        const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                        hw[e >> 1] = (uint32_t)__bfloat16_as_ushort(h0) |
-                                     ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                        lw[e >> 1] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    for (int e = 0; e < 32; ++e) {
+                        const int2 pr = page_rows(c0 + e);
+                        float x = 0.f;
+                        if (src && pr.x >= 0) {
+                            x = src[pr.x * stride];
+                            if (pr.y >= 0) x = (x + src[pr.y * stride]) * kRs2;
+                        }
+                        r[e] = __float_as_uint(x);
                     }
-                    *reinterpret_cast<uint4*>(base + sw128_offset(kDVB, cb + e8)) =
-                        make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(base + sw128_offset(kDVB + 1, cb + e8)) =
-                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    tmem_st32(tbase + lane_off + kColS + c0, r);
                 }
+                tmem_st_wait();
+                fence_before_sync();
+                named_bar_sync(kBarW, kThreadsW);
+                fence_after_sync();
             }
-            if (scale) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * decay);
-                tmem_st32(tbase + lane_off + kColS + c0, r);
-            }
-        }
-        if (scale) tmem_st_wait();
-    };
 
-    // Both feature tiles of the chunk: queries xi-scaled (with the raw q and k for
-    // MMA1), keys zeta-scaled; rows past the end are zero.  Thread t builds row
-    // t mod 128 of one tile: quarters 0 / 1 the queries' pair pieces 0..10 / the
-    // rest with x, the constant and the raw rows; quarters 2 / 3 the same of the keys.
-    auto build_phi = [&](int s, int L) {
-        const int r = tid & (kC - 1), qq = tid >> 7;  // qq is warp-uniform
-        const bool is_q = qq < 2;
-        const char* src = sm + (is_q ? Lay::oQr : Lay::oKr) + s * Lay::kRaw + r * (kD * 2);
-        char* tile = sm + (is_q ? Lay::oPhiQ : Lay::oPhiK);
-        float sc = 0.f;  // xi_r or zeta_r, zero past the end
-        if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(is_q ? r + 1 : L - 1 - r));
-        float x[kD], y[kD];
-        unpack16(src, x);
+            // E3: S^T -> the bf16 B operand of MMA3 (K-major: row n = value column n;
+            // rows 64 and 65 = z's bf16 value and its residual), then S^T *= decay
+            // (skipped when `scale` is false).  Lanes 65..127 hold nothing.
+            auto e3 = [&](float decay, bool scale) {
+                if (q4 == 3) return;  // warp-uniform
+                for (int k = 0; k < n_own; ++k) {
+                    const int c0 = (sub + 4 * k) * 32;
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                    tmem_ld_wait();
+                    char* base = sm + Lay::oSB + (c0 >> 6) * Lay::kSBBlk;
+                    const int cb = c0 & 63;
+                    if (row < kDVB) {
 #pragma unroll
-        for (int a = 0; a < kD; ++a) y[a] = x[a] * sc;
-        if ((qq & 1) == 0) {
-            pair_pieces<0, 11>(tile, r, x, y);
-        } else {
-            pair_pieces<11, 17>(tile, r, x, y);
-            linear_pieces(tile, r, y, sc);
-            if (is_q) {  // the raw rows (the tile loads zero past the end of the sequence)
-                const uint4* qr = reinterpret_cast<const uint4*>(src);
-                const uint4* kr = reinterpret_cast<const uint4*>(sm + Lay::oKr + s * Lay::kRaw + r * (kD * 2));
-                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 32)) = qr[0];
-                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 40)) = qr[1];
-                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 48)) = kr[0];
-                *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 56)) = kr[1];
-            }
-        }
-    };
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]), __uint_as_float(r[e8 + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]), __uint_as_float(r[e8 + 7]));
+                            *reinterpret_cast<uint4*>(base + sw128_offset(row, cb + e8)) = w;
+                        }
+                    } else if (row == kDVB) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                            uint32_t hw[4], lw[4];
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const float x0 = __uint_as_float(r[e8 + e]), x1 = __uint_as_float(r[e8 + e + 1]);
+                                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                                hw[e >> 1] = (uint32_t)__bfloat16_as_ushort(h0) |
+                                             ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                                lw[e >> 1] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                            }
+                            *reinterpret_cast<uint4*>(base + sw128_offset(kDVB, cb + e8)) =
+                                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4*>(base + sw128_offset(kDVB + 1, cb + e8)) =
+                                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        }
+                    }
+                    if (scale) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * decay);
+                        tmem_st32(tbase + lane_off + kColS + c0, r);
+                    }
+                }
+                if (scale) tmem_st_wait();
+            };
 
-    // E1 on 32 score columns j = cc .. cc + 31 of query row i: the Taylor kernel times
-    // gamma^(i - j) for j <= i < L, else 0, as 16 bf16 pairs
-    auto e1_piece = [&](const uint32_t (&r)[32], int cc, int i, int L, uint32_t (&out)[16]) {
-        const int jt = min(i, cc + 31);
-        float w = unit_gamma ? 1.f : gamma_pow(l2g, (float)max(i - jt, 0));
-        float xv[32];
+            // The feature tiles of chunk `it` (stage s): queries xi-scaled (with the raw q
+            // and k for MMA1), keys zeta-scaled; rows past the end are zero.  Worker t
+            // builds row t mod 128: sub 0 / 1 the queries' pair pieces 0..10 / the rest
+            // with x, the constant and the raw rows; sub 2 / 3 the same of the keys.
+            auto build_phi = [&](int s, int L) {
+                const int r = t & (kC - 1);
+                const bool is_q = sub < 2;
+                const char* src = sm + (is_q ? Lay::oQr : Lay::oKr) + s * Lay::kRaw + r * (kD * 2);
+                char* tile = sm + (is_q ? Lay::oPhiQ : Lay::oPhiK);
+                float sc = 0.f;  // xi_r or zeta_r, zero past the end
+                if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(is_q ? r + 1 : L - 1 - r));
+                float x[kD], y[kD];
+                unpack16(src, x);
 #pragma unroll
-        for (int e = 31; e >= 0; --e) {
-            const int j = cc + e;
-            const float sv = __uint_as_float(r[e]);
-            float v = 0.f;
-            if (j <= i && i < L) {
-                v = fmaf(sv, fmaf(0.5f, sv, 1.f), 1.f) * w;
-                if (!unit_gamma) w *= gam;
-            }
-            xv[e] = v;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) out[e >> 1] = pack_bf16x2(xv[e], xv[e + 1]);
-    };
-
-    // E2: O rows -> global, divided by the normaliser (16 value columns a warp)
-    auto e2 = [&](int it, int L) {
-        const uint32_t ocol = tbase + lane_off + kColO;
-        float inv = 1.f;
-        if (p.normalize) {
-            const float den = __uint_as_float(tmem_ld1(ocol + kDVB)) + __uint_as_float(tmem_ld1(ocol + kDVB + 1));
-            tmem_ld_wait();
-            inv = 1.f / norm_den(den, p.normalize, p.eps);
-        }
-        uint32_t r[16];
-        tmem_ld16(ocol + 16 * grp, r);
-        tmem_ld_wait();
-        if (row < L) {
-            __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 16 * grp;
-#pragma unroll
-            for (int e8 = 0; e8 < 16; e8 += 8) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
-                w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
-                w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
-                w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
-                *reinterpret_cast<uint4*>(orow + e8) = w;
-            }
-        }
-    };
-
-    // The final state in the page's feature order (z from the first value block
-    // only): a pair column gives rows (a, b) and (b, a) its value over sqrt 2, plus
-    // the decayed antisymmetric part of the initial state.
-    auto write_exit_state = [&]() {
-        if (q4 > 2 || (!p.S_out && !p.z_out)) return;  // warp-uniform
-        float* dst = nullptr;
-        const float* src0 = nullptr;
-        size_t stride = 0;
-        if (row < kDVB && p.S_out) {
-            dst = p.S_out + (size_t)bh * kDF * p.dv + v0 + row;
-            src0 = p.S0 ? p.S0 + (size_t)bh * kDF * p.dv + v0 + row : nullptr;
-            stride = p.dv;
-        } else if (row == kDVB && vb == 0 && p.z_out) {
-            dst = p.z_out + (size_t)bh * kDF;
-            src0 = p.z0 ? p.z0 + (size_t)bh * kDF : nullptr;
-            stride = 1;
-        }
-        const float gT = unit_gamma ? 1.f : gamma_pow(l2g, (float)p.T);
-        for (int k = 0; k < n_own; ++k) {
-            const int c0 = (grp + 4 * k) * 32;
-            uint32_t r[32];
-            tmem_ld32(tbase + lane_off + kColS + c0, r);
-            tmem_ld_wait();
-            if (!dst) continue;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int2 pr = page_rows(c0 + e);
-                if (pr.x < 0) continue;
-                const float x = __uint_as_float(r[e]);
-                if (pr.y < 0) {
-                    dst[pr.x * stride] = x;
+                for (int a = 0; a < kD; ++a) y[a] = x[a] * sc;
+                if ((sub & 1) == 0) {
+                    pair_pieces<0, 11>(tile, r, x, y);
                 } else {
-                    const float anti = src0 ? 0.5f * gT * (src0[pr.x * stride] - src0[pr.y * stride]) : 0.f;
-                    dst[pr.x * stride] = x * kRs2 + anti;
-                    dst[pr.y * stride] = x * kRs2 - anti;
+                    pair_pieces<11, 17>(tile, r, x, y);
+                    linear_pieces(tile, r, y, sc);
+                    if (is_q) {  // the raw rows (the tile loads zero past the end of the sequence)
+                        const uint4* qr = reinterpret_cast<const uint4*>(src);
+                        const uint4* kr = reinterpret_cast<const uint4*>(sm + Lay::oKr + s * Lay::kRaw + r * (kD * 2));
+                        *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 32)) = qr[0];
+                        *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 40)) = qr[1];
+                        *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 48)) = kr[0];
+                        *reinterpret_cast<uint4*>(tile + 2 * kBlk + sw128_offset(r, 56)) = kr[1];
+                    }
+                }
+            };
+
+            // E1 on score piece sub (columns j = 32 sub ..) of query row i: the Taylor
+            // kernel times gamma^(i - j) for j <= i < L, else 0, as 16 bf16 pairs in P.
+            // A warp's 32 rows and a piece's 32 columns are one 32 x 32 block for every
+            // lane: above the diagonal the piece is zero (no load), below it no column
+            // needs the mask.
+            auto e1 = [&](int L) {
+                const int cc = 32 * sub;
+                const int i = row;
+                uint32_t out[16];
+                if (sub > q4) {  // warp-uniform: above the diagonal
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) out[e] = 0u;
+                } else {
+                    const bool diag = sub == q4;
+                    const bool live = i < L;
+                    const int jt = min(i, cc + 31);
+                    float w = unit_gamma ? 1.f : gamma_pow(l2g, (float)(i - jt));
+#pragma unroll
+                    for (int h16 = 16; h16 >= 0; h16 -= 16) {  // the upper 16 columns first (the decay runs down)
+                        uint32_t r[16];
+                        tmem_ld16(tbase + lane_off + kColSc + cc + h16, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 14; e >= 0; e -= 2) {  // each pair packed at once
+                            const int j = cc + h16 + e;
+                            const float s1 = __uint_as_float(r[e + 1]), s0 = __uint_as_float(r[e]);
+                            float v1 = fmaf(s1, fmaf(0.5f, s1, 1.f), 1.f);
+                            float v0 = fmaf(s0, fmaf(0.5f, s0, 1.f), 1.f);
+                            const bool in1 = live && (!diag || j + 1 <= i), in0 = live && (!diag || j <= i);
+                            if (!unit_gamma) {
+                                v1 *= w;
+                                if (in1) w *= gam;
+                                v0 *= w;
+                                if (in0) w *= gam;
+                            }
+                            out[(h16 + e) >> 1] = pack_bf16x2(in0 ? v0 : 0.f, in1 ? v1 : 0.f);
+                        }
+                    }
+                }
+                tmem_st16(tbase + lane_off + kColP + (cc >> 1), out);
+                tmem_st_wait();
+            };
+
+            // E2: O rows -> global, divided by the normaliser (16 value columns a warp)
+            auto e2 = [&](int it, int L) {
+                const uint32_t ocol = tbase + lane_off + kColO;
+                uint32_t r[16];
+                tmem_ld16(ocol + 16 * sub, r);
+                float inv = 1.f;
+                if (p.normalize) {
+                    const float den = __uint_as_float(tmem_ld1(ocol + kDVB)) +
+                                      __uint_as_float(tmem_ld1(ocol + kDVB + 1));
+                    tmem_ld_wait();
+                    inv = 1.f / norm_den(den, p.normalize, p.eps);
+                } else {
+                    tmem_ld_wait();
+                }
+                if (row < L) {
+                    __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 16 * sub;
+#pragma unroll
+                    for (int e8 = 0; e8 < 16; e8 += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + e8) = w;
+                    }
+                }
+            };
+
+            // The final state in the page's feature order (z from the first value block
+            // only): a pair column gives rows (a, b) and (b, a) its value over sqrt 2,
+            // plus the decayed antisymmetric part of the initial state.
+            auto write_exit_state = [&]() {
+                if (q4 == 3 || (!p.S_out && !p.z_out)) return;  // warp-uniform
+                float* dst = nullptr;
+                const float* src0 = nullptr;
+                size_t stride = 0;
+                if (row < kDVB && p.S_out) {
+                    dst = p.S_out + (size_t)bh * kDF * p.dv + v0 + row;
+                    src0 = p.S0 ? p.S0 + (size_t)bh * kDF * p.dv + v0 + row : nullptr;
+                    stride = p.dv;
+                } else if (row == kDVB && vb == 0 && p.z_out) {
+                    dst = p.z_out + (size_t)bh * kDF;
+                    src0 = p.z0 ? p.z0 + (size_t)bh * kDF : nullptr;
+                    stride = 1;
+                }
+                const float gT = unit_gamma ? 1.f : gamma_pow(l2g, (float)p.T);
+                for (int k = 0; k < n_own; ++k) {
+                    const int c0 = (sub + 4 * k) * 32;
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                    tmem_ld_wait();
+                    if (!dst) continue;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int2 pr = page_rows(c0 + e);
+                        if (pr.x < 0) continue;
+                        const float x = __uint_as_float(r[e]);
+                        if (pr.y < 0) {
+                            dst[pr.x * stride] = x;
+                        } else {
+                            const float anti = src0 ? 0.5f * gT * (src0[pr.x * stride] - src0[pr.y * stride]) : 0.f;
+                            dst[pr.x * stride] = x * kRs2 + anti;
+                            dst[pr.y * stride] = x * kRs2 - anti;
+                        }
+                    }
+                }
+            };
+
+            // E3 for chunk `it` (or the initial state, it = -1) and the feature tiles
+            // of chunk it + 1, then hand both over to the MMA warp
+            auto state_and_features = [&](int it) -> bool {
+                const int nx = it + 1;
+                const int Ln = min(kC, p.T - nx * kC);
+                e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)Ln), !unit_gamma);
+                const int s = nx & 1;
+                const bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (nx >> 1) & 1, lim, abort_flag);
+                if (named_bar_or(kBarW, kThreadsW, !ok)) return false;
+                build_phi(s, Ln);
+                fence_proxy_async_smem();
+                fence_before_sync();
+                named_bar_sync(kBarW, kThreadsW);
+                if (t == 0) {
+                    mbar_arrive(&bar[kSready]);
+                    mbar_arrive(&bar[kPhiReady]);
+                    mbar_arrive(&bar[kEmpty0 + s]);  // the stage's raw rows are read
+                }
+                return true;
+            };
+
+            // it = -1 hands over the initial state and the first chunk's features
+            for (int it = -1; it < n; ++it) {
+                const int L = it >= 0 ? min(kC, p.T - it * kC) : 0;
+                bool ok = true;
+                if (it >= 0) {
+                    // ---- E1 once MMA1 is done (MMA3 / MMA4 run beside it)
+                    ok = mbar_wait_or_abort(&bar[kScores], it & 1, lim, abort_flag);
+                    if (named_bar_or(kBarW, kThreadsW, !ok)) break;
+                    fence_after_sync();
+                    e1(L);
+                    fence_before_sync();
+                    named_bar_sync(kBarW, kThreadsW);
+                    if (t == 0) mbar_arrive(&bar[kPready]);
+                    // ---- once MMA3 and MMA4 are done (MMA2 runs beside it)
+                    ok = mbar_wait_or_abort(&bar[kState], it & 1, lim, abort_flag);
+                    if (named_bar_or(kBarW, kThreadsW, !ok)) break;
+                    fence_after_sync();
+                }
+                // ---- E3 and the next chunk's feature tiles, or the final state
+                if (it + 1 < n) {
+                    if (!state_and_features(it)) break;
+                } else {
+                    write_exit_state();
+                }
+                if (it >= 0) {
+                    // ---- E2 once MMA2 is done, then O is free for the next chunk's MMA3
+                    ok = mbar_wait_or_abort(&bar[kOut], it & 1, lim, abort_flag);
+                    if (named_bar_or(kBarW, kThreadsW, !ok)) break;
+                    fence_after_sync();
+                    e2(it, L);
+                    fence_before_sync();
+                    named_bar_sync(kBarW, kThreadsW);
+                    if (t == 0) mbar_arrive(&bar[kOfree]);
                 }
             }
         }
-    };
+    }
 
-    if (!fail) e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)min(kC, p.T)), !unit_gamma);
-    fence_proxy_async_smem();
+    __syncwarp();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-
-    // MMA descriptors and instruction descriptors (thread 0)
-    const uint64_t dPhiQ = smem_desc_sw128(sbase + Lay::oPhiQ, 16, 1024);        // K-major
-    const uint64_t dSB = smem_desc_sw128(sbase + Lay::oSB, 16, 1024);            // K-major
-    const uint64_t dPhiK = smem_desc_sw128(sbase + Lay::oPhiK, kBlk, 1024);      // MN-major
-    constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t id_qs = idesc_bf16(128, kNV, 0, 0);
-    constexpr uint32_t id_pv = idesc_bf16(128, kNV, 0, 1);
-    constexpr uint32_t id_st = idesc_bf16(128, kFCols, 1, 1);
-    bool mma_issued = false;
-
-    // every thread waits; false on a timeout anywhere
-    auto wait_all = [&](int b, uint32_t parity) -> bool {
-        const bool ok = mbar_wait(&bar[b], parity, lim);
-        const bool bad = __syncthreads_or(!ok);
-        fence_after_sync();
-        return !bad;
-    };
-
-    int L_prev = 0;
-    for (int it = 0; it < n && !fail; ++it) {
-        const int s = it & 1;
-        const int L = min(kC, p.T - it * kC);
-        // the chunk's raw q, k and V
-        if (!wait_all(kFull0 + s, (it >> 1) & 1)) {
-            fail = true;
-            break;
-        }
-        // ---- both feature tiles (MMA1, MMA3 and MMA4 of the previous chunk are done
-        // with them), and E2 of the previous chunk once its MMA2 is done: then its
-        // stage is free for the loads of chunk it + 1
-        build_phi(s, L);
-        if (it > 0) {
-            if (!wait_all(kOut, (it - 1) & 1)) {
-                fail = true;
-                break;
-            }
-            if (tid == 0 && it + 1 < n) issue_fill(it + 1);
-            e2(it - 1, L_prev);
-        }
-        fence_proxy_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        // ---- MMA1 (scores), MMA3 (O = phi(Q) S), MMA4 (S^T += [V | 1]^T phi(K)):
-        // MMA3 reads S_bf16 and MMA4 the scaled S^T, both written by E3 before
-        const uint32_t va = sbase + Lay::oV + s * kBlk;
-        const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major [V | 1]
-        if (tid == 0) {
-            fence_after_sync();
-            mma_ss(tbase + kColSc, desc_adv(dPhiQ, 2 * kBlk + 64), desc_adv(dPhiQ, 2 * kBlk + 96), id_qk, 0u);
-            mma_commit(&bar[kScores]);
-#pragma unroll
-            for (int kk = 0; kk < kFCols / 16; ++kk)
-                mma_ss(tbase + kColO, desc_adv(dPhiQ, (kk >> 2) * kBlk + (kk & 3) * 32),
-                       desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk)
-                mma_ss(tbase + kColS, desc_adv(dVo, kk * 2048), desc_adv(dPhiK, kk * 2048), id_st, 1u);
-            mma_commit(&bar[kState]);
-            mma_issued = true;
-        }
-        // ---- E1 beside MMA3 / MMA4: scores -> P (every score read before any P lands)
-        if (!wait_all(kScores, it & 1)) {
-            fail = true;
-            break;
-        }
-        {
-            const int c0 = 32 * grp;
-            uint32_t ra[32];
-            tmem_ld32(tbase + lane_off + kColSc + c0, ra);
-            tmem_ld_wait();
-            __syncthreads();
-            uint32_t pa[16];
-            e1_piece(ra, c0, row, L, pa);
-            tmem_st16(tbase + lane_off + kColSc + (c0 >> 1), pa);
-            tmem_st_wait();
-        }
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {  // MMA2: O += P [V | 1]
-            fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk)
-                mma_ts(tbase + kColO, tbase + kColSc + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
-            mma_commit(&bar[kOut]);
-        }
-        // ---- E3 beside MMA2, once MMA3 and MMA4 are done: the state for the next
-        // chunk, or the final state
-        if (!wait_all(kState, it & 1)) {
-            fail = true;
-            break;
-        }
-        if (it + 1 < n) {
-            const int Ln = min(kC, p.T - (it + 1) * kC);
-            e3(unit_gamma ? 1.f : gamma_pow(l2g, (float)Ln), !unit_gamma);
-        } else {
-            write_exit_state();
-        }
-        L_prev = L;
-    }
-    // E2 of the last chunk
-    if (!fail && n > 0) {
-        if (wait_all(kOut, (n - 1) & 1))
-            e2(n - 1, L_prev);
-        else
-            fail = true;
-    }
-
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (fail) {
+    if (*abort_flag || forced) {
         record_status(p.dev_status, LA_ERR_TIMEOUT);
-        if (tid == 0) {  // our own TMA fills and MMAs must land before smem and TMEM are released
+        if (warp == 0 && lane == 0) {  // our own TMA fills must land before the smem is released
             for (int s = 0; s < 2; ++s)
                 if (fills[s] > 0) mbar_wait(&bar[kFull0 + s], (fills[s] - 1) & 1, lim);
-            if (mma_issued) {
-                mma_commit(&bar[kDrain]);
-                mbar_wait(&bar[kDrain], 0, lim);
-            }
+        }
+        if (warp == 1 && lane == 0 && mma_issued) {  // and our MMAs before TMEM is freed
+            mma_commit(&bar[kDrain]);
+            mbar_wait(&bar[kDrain], 0, lim);
         }
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
     }
-    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+    if (warp == 1) tmem_dealloc(tbase, kTmemCols);
 }
 
 }  // namespace
