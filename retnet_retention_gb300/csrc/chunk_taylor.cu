@@ -72,7 +72,7 @@ constexpr int kFCols = 160;             // feature columns the MMAs contract ove
 constexpr uint32_t kColS = 0;           // S^T, 160 columns
 constexpr uint32_t kColSc = 160;        // scores (fp32)
 constexpr uint32_t kColP = 288;         // P (bf16 pairs), 64 columns
-constexpr uint32_t kColO = 352;         // O, 80 columns
+constexpr uint32_t kColO = 352;         // O, two buffers of 80 columns (chunk c uses c mod 2)
 constexpr uint32_t kTmemCols = 512;
 
 struct Lay {
@@ -83,7 +83,8 @@ struct Lay {
     static constexpr uint32_t oSB = oPhiK + kFB * kBlk;             // S_bf16, 3 x 10 KB
     static constexpr uint32_t oV = oSB + kFB * kSBBlk;              // V, two stages
     static constexpr uint32_t oOnes = oV + 2 * kBlk;                // the block after V: ones in column 0
-    static constexpr uint32_t oQr = oOnes + kBlk;                   // raw q, two stages
+    static constexpr uint32_t oOst = oOnes + kBlk;                  // O staging tile (bf16, swizzled)
+    static constexpr uint32_t oQr = oOst + kBlk;                    // raw q, two stages
     static constexpr uint32_t oKr = oQr + 2 * kRaw;                 // raw k, two stages
     static constexpr uint32_t oBar = oKr + 2 * kRaw;
     static constexpr uint32_t oSlot = oBar + 192;                  // TMEM base, abort flag
@@ -91,7 +92,7 @@ struct Lay {
     static constexpr uint32_t kAlloc = kBytes + 1024;               // + alignment of the base
 };
 static_assert(Lay::oPhiK % 1024 == 0 && Lay::oSB % 1024 == 0 && Lay::kSBBlk % 1024 == 0 &&
-                  Lay::oV % 1024 == 0 && Lay::oOnes % 1024 == 0,
+                  Lay::oV % 1024 == 0 && Lay::oOnes % 1024 == 0 && Lay::oOst % 1024 == 0,
               "swizzled blocks need 1024-byte alignment");
 static_assert(Lay::kAlloc <= 227 * 1024, "shared memory budget");
 
@@ -100,18 +101,20 @@ enum Bars {
     kEmpty0 = 2, kEmpty1 = 3,  // a stage read: the workers (raw q, k) and MMA2 / MMA4 (V)
     kPhiReady = 4,             // both feature tiles built
     kSready = 5,               // S_bf16 and the scaled S^T in place (E3, or the initial state)
-    kOfree = 6,                // E2 has read O
-    kPready = 7,               // P in TMEM (E1)
-    kScores = 8,               // MMA1 done
-    kState = 9,                // MMA1, MMA3, MMA4 done: the feature tiles are free again
-    kOut = 10,                 // MMA2 done
-    kDrain = 11, kNever = 12, kNumBars = 13
+    kOfree0 = 6,               // E2 has read O buffer 0
+    kOfree1 = 7,               // ... and buffer 1
+    kPready = 8,               // P in TMEM (E1)
+    kScores = 9,               // MMA1 done
+    kState = 10,               // MMA1, MMA3, MMA4 done: the feature tiles are free again
+    kOut = 11,                 // MMA2 done
+    kDrain = 12, kNever = 13, kNumBars = 14
 };
 static_assert(kNumBars * 8 <= 192, "mbarrier slots");
 
 struct TaylorParams {
     CUtensorMap tmQ, tmK;   // [BH][T][16] bf16, box {16, 128, 1}, no swizzle
     CUtensorMap tmV;        // [BH][T][dv] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmO;        // O, the same layout (stored from the staging tile)
     __nv_bfloat16* O;       // [BH][T][dv]
     const float* S0;        // [BH][273][dv] in the page's feature order, or null (zero)
     const float* z0;        // [BH][273] or null
@@ -282,10 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
             for (int it = 0; it < n; ++it) {
                 const int s = it & 1;
                 // the chunk's feature tiles, the state from E3 of the previous chunk, and
-                // O read out by E2 of the previous chunk
+                // this chunk's O buffer read out by E2 two chunks back
+                const int ob = it & 1;
                 if (!mbar_wait_or_abort(&bar[kPhiReady], it & 1, lim, abort_flag)) break;
                 if (!mbar_wait_or_abort(&bar[kSready], it & 1, lim, abort_flag)) break;
-                if (it >= 1 && !mbar_wait_or_abort(&bar[kOfree], (it - 1) & 1, lim, abort_flag)) break;
+                if (it >= 2 && !mbar_wait_or_abort(&bar[kOfree0 + ob], ((it - 2) >> 1) & 1, lim, abort_flag))
+                    break;
                 fence_after_sync();
                 const uint32_t va = sbase + Lay::oV + s * kBlk;
                 const uint64_t dVo = smem_desc_sw128(va, sbase + Lay::oOnes - va, 1024);  // MN-major [V | 1]
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 // MMA3: O = phi(Q) S_bf16;  MMA4: S^T += [V | 1]^T phi(K)
 #pragma unroll
                 for (int kk = 0; kk < kFCols / 16; ++kk)
-                    mma_ss(tbase + kColO, desc_adv(dPhiQ, (kk >> 2) * kBlk + (kk & 3) * 32),
+                    mma_ss(tbase + kColO + ob * kNV, desc_adv(dPhiQ, (kk >> 2) * kBlk + (kk & 3) * 32),
                            desc_adv(dSB, (kk >> 2) * Lay::kSBBlk + (kk & 3) * 32), id_qs, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_ts(tbase + kColO, tbase + kColP + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
+                    mma_ts(tbase + kColO + ob * kNV, tbase + kColP + kk * 8, desc_adv(dVo, kk * 2048), id_pv, 1u);
                 mma_commit(&bar[kOut]);
                 mma_commit(&bar[kEmpty0 + s]);
             }
@@ -360,16 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
             // (skipped when `scale` is false).  Lanes 65..127 hold nothing.
             auto e3 = [&](float decay, bool scale) {
                 if (q4 == 3) return;  // warp-uniform
-                for (int k = 0; k < n_own; ++k) {
-                    const int c0 = (sub + 4 * k) * 32;
-                    uint32_t r[32];
-                    tmem_ld32(tbase + lane_off + kColS + c0, r);
+                for (int hp = sub; hp < 2 * kPieces; hp += 4) {  // 16-column halves: three or two a warp
+                    const int c0 = hp * 16;
+                    uint32_t r[16];
+                    tmem_ld16(tbase + lane_off + kColS + c0, r);
                     tmem_ld_wait();
                     char* base = sm + Lay::oSB + (c0 >> 6) * Lay::kSBBlk;
                     const int cb = c0 & 63;
                     if (row < kDVB) {
 #pragma unroll
-                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                        for (int e8 = 0; e8 < 16; e8 += 8) {
                             uint4 w;
                             w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]), __uint_as_float(r[e8 + 1]));
                             w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]), __uint_as_float(r[e8 + 3]));
@@ -379,15 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                         }
                     } else if (row == kDVB) {
 #pragma unroll
-                        for (int e8 = 0; e8 < 32; e8 += 8) {
+                        for (int e8 = 0; e8 < 16; e8 += 8) {
                             uint32_t hw[4], lw[4];
 #pragma unroll
                             for (int e = 0; e < 8; e += 2) {
                                 const float x0 = __uint_as_float(r[e8 + e]), x1 = __uint_as_float(r[e8 + e + 1]);
-                                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                                hw[e >> 1] = (uint32_t)__bfloat16_as_ushort(h0) |
-                                             ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                                lw[e >> 1] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                                const uint32_t hi = pack_bf16x2(x0, x1);  // x0 in the low half
+                                hw[e >> 1] = hi;
+                                lw[e >> 1] = pack_bf16x2(x0 - __uint_as_float(hi << 16),
+                                                         x1 - __uint_as_float(hi & 0xFFFF0000u));
                             }
                             *reinterpret_cast<uint4*>(base + sw128_offset(kDVB, cb + e8)) =
                                 make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -397,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                     }
                     if (scale) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * decay);
-                        tmem_st32(tbase + lane_off + kColS + c0, r);
+                        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * decay);
+                        tmem_st16(tbase + lane_off + kColS + c0, r);
                     }
                 }
                 if (scale) tmem_st_wait();
@@ -478,9 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 tmem_st_wait();
             };
 
-            // E2: O rows -> global, divided by the normaliser (16 value columns a warp)
-            auto e2 = [&](int it, int L) {
-                const uint32_t ocol = tbase + lane_off + kColO;
+            // E2: O rows, divided by the normaliser, into the staging tile (16 value
+            // columns a warp); one thread then stores the tile with TMA
+            auto e2 = [&](int it) {
+                const uint32_t ocol = tbase + lane_off + kColO + (it & 1) * kNV;
                 uint32_t r[16];
                 tmem_ld16(ocol + 16 * sub, r);
                 float inv = 1.f;
@@ -492,17 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 } else {
                     tmem_ld_wait();
                 }
-                if (row < L) {
-                    __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)it * kC + row) * p.dv + v0 + 16 * sub;
+                char* ost = sm + Lay::oOst;
 #pragma unroll
-                    for (int e8 = 0; e8 < 16; e8 += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + e8) = w;
-                    }
+                for (int e8 = 0; e8 < 16; e8 += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
+                    *reinterpret_cast<uint4*>(ost + sw128_offset(row, 16 * sub + e8)) = w;
                 }
             };
 
@@ -570,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
             // it = -1 hands over the initial state and the first chunk's features
             for (int it = -1; it < n; ++it) {
                 const int L = it >= 0 ? min(kC, p.T - it * kC) : 0;
+                (void)L;
                 bool ok = true;
                 if (it >= 0) {
                     // ---- E1 once MMA1 is done (MMA3 / MMA4 run beside it)
@@ -592,16 +597,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                     write_exit_state();
                 }
                 if (it >= 0) {
-                    // ---- E2 once MMA2 is done, then O is free for the next chunk's MMA3
+                    // ---- E2 once MMA2 is done (and the previous chunk's store has read the
+                    // staging tile); then the O buffer is free for chunk it + 2
+                    if (t == 0) bulk_wait_read0();
                     ok = mbar_wait_or_abort(&bar[kOut], it & 1, lim, abort_flag);
                     if (named_bar_or(kBarW, kThreadsW, !ok)) break;
                     fence_after_sync();
-                    e2(it, L);
+                    e2(it);
+                    fence_proxy_async_smem();
                     fence_before_sync();
                     named_bar_sync(kBarW, kThreadsW);
-                    if (t == 0) mbar_arrive(&bar[kOfree]);
+                    if (t == 0) {
+                        mbar_arrive(&bar[kOfree0 + (it & 1)]);
+                        tma_store_3d(&p.tmO, v0, it * kC, bh, sm + Lay::oOst);  // rows past T are not written
+                        bulk_commit();
+                    }
                 }
             }
+            if (t == 0) bulk_wait0();  // the last stores are done before the CTA leaves
         }
     }
 
@@ -642,7 +655,7 @@ cudaError_t launch_chunk_taylor(const ChunkArgs& a, const KernelGammas& g, cudaS
     const int BH = a.B * a.H;
     if (!tck::make_map_box(&prm.tmQ, a.Q, BH, a.T, kD, kD, false) ||
         !tck::make_map_box(&prm.tmK, a.K, BH, a.T, kD, kD, false) ||
-        !tck::make_map(&prm.tmV, a.V, BH, a.T, a.dv))
+        !tck::make_map(&prm.tmV, a.V, BH, a.T, a.dv) || !tck::make_map(&prm.tmO, a.O, BH, a.T, a.dv))
         return cudaErrorInvalidValue;
     prm.O = static_cast<__nv_bfloat16*>(a.O);
     prm.S0 = a.S0;
