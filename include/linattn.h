@@ -92,13 +92,13 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
  * section "A Taylor feature map", box "Taylor features"):
  *   phi(x) = (1, x_1 .. x_d, vec(x x^T) / sqrt 2),  1 + d + d^2 entries, vec row-major,
  * so that phi(q)^T phi(k) = 1 + s + s^2/2 with s = q^T k (always >= 1/2, a safe
- * denominator).  la_chunk_fwd only (and la_workspace_size, la_chunk_fwd_launches,
- * la_chunk_fwd_noalloc), causal, bf16, d_k = 16 (Based's projected width: 273
- * features), d_v a multiple of 64, not with LA_PHI_ELU1, chunk 0 or 128.  d_k is
- * the width of Q and K; the states S0 / S_out are [B][H][1 + d_k + d_k^2][d_v]
- * fp32 and z0 / z_out [B][H][1 + d_k + d_k^2], rows in the order of phi above.
- * Other calls answer LA_ERR_UNSUPPORTED; so does la_chunk_fwd on a device other
- * than sm_103. */
+ * denominator).  d_k = 16 (Based's projected width: 273 features), not with
+ * LA_PHI_ELU1, causal.  d_k is the width of Q and K; the states S0 / S_out / S are
+ * [B][H][1 + d_k + d_k^2][d_v] fp32 and z0 / z_out / z [B][H][1 + d_k + d_k^2],
+ * rows in the order of phi above.  la_chunk_fwd (and la_workspace_size,
+ * la_chunk_fwd_launches, la_chunk_fwd_noalloc): bf16, d_v a multiple of 64, chunk
+ * 0 or 128, an sm_103 device.  la_recurrent_step: bf16 or fp32, d_v <= 256.
+ * Other calls and shapes answer LA_ERR_UNSUPPORTED. */
 #define LA_PHI_TAYLOR 32u
 
 /* Human-readable text of a status code (static storage, never NULL). */

@@ -243,9 +243,11 @@ la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype d
     const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & LA_PHI_TAYLOR) return LA_ERR_UNSUPPORTED;
-    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | LA_PHI_TAYLOR | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
     if (flags & LA_NONCAUSAL) return LA_ERR_UNSUPPORTED;
+    const bool taylor = (flags & LA_PHI_TAYLOR) != 0;
+    if (taylor && (d_k != 16 || (flags & LA_PHI_ELU1))) return LA_ERR_UNSUPPORTED;
+    const size_t ds = taylor ? (size_t)taylor_feature_dim(d_k) : (size_t)d_k;  // state rows
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
     const size_t nbh = (size_t)B * H;
@@ -267,10 +269,11 @@ la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype d
     const size_t es = elem_size(dtype);
     const size_t n_o = nbh * d_v * es;
     if (overlaps(o, n_o, q, nbh * d_k * es) || overlaps(o, n_o, k, nbh * d_k * es) ||
-        overlaps(o, n_o, v, n_o) || overlaps(o, n_o, S, nbh * d_k * d_v * 4))
+        overlaps(o, n_o, v, n_o) || overlaps(o, n_o, S, nbh * ds * d_v * 4))
         return LA_ERR_INVALID_ARG;
 
     StepArgs a;
+    a.taylor = taylor;
     a.q = q; a.k = k; a.v = v; a.o = o; a.S = S; a.z = normalize ? z : nullptr;
     a.B = B; a.H = H; a.dk = d_k; a.dv = d_v;
     a.bf16 = dtype == LA_DTYPE_BF16;

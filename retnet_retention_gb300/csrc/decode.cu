@@ -16,6 +16,10 @@
 // keeping up to 64 KB per CTA in flight.  The
 // read-out sum over d_k is a register accumulation followed by a shared-
 // memory reduction across the row slots.
+//
+// With the Taylor feature map ("Linear attention", "A Taylor feature map") q
+// and k are 16 wide and the state has 1 + 16 + 256 = 273 rows in the page's
+// order: phi(x) = (1, x, vec(x x^T)/sqrt 2) is built in shared memory first.
 #include "launch.h"
 #include "trace.h"
 
@@ -25,20 +29,24 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBatch = 16;
+constexpr int kMaxRows = 288;  // feature rows held in shared memory (273 with the Taylor map)
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int H, int dk, int dv,
-    int phi, int normalize, float eps, const float* __restrict__ log_a,
+    int phi, int normalize, float eps, const float* __restrict__ log_a, int taylor,
     const __grid_constant__ KernelGammas g) {
-    __shared__ float qf[256];
-    __shared__ float kf[256];
+    __shared__ float qf[kMaxRows];
+    __shared__ float kf[kMaxRows];
+    __shared__ float qk_in[32];
     __shared__ float red[kThreads * 4];
     __shared__ float den_part[kThreads / 32];
 
     const int bh = blockIdx.x;
     const int h = bh % H;
+    const int din = dk;                           // width of q and k
+    if (taylor) dk = 1 + din + din * din;         // rows of the state
     const float gam = log_a ? exp2f(log_a[bh] * 1.44269504088896341f) : g.gamma[h];
     const int tid = threadIdx.x;
     const int tpr = dv >> 2;           // threads per state row
@@ -56,7 +64,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
         int i = rs + u * rpi;
         if (i < dk) s[u] = __ldcs(Sb + (size_t)i * row4 + cg);
     }
-    if (tid < dk) {
+    if (taylor) {
+        if (tid < 2 * din) qk_in[tid] = load_elem(tid < din ? q : k, (size_t)bh * din + tid % din);
+        __syncthreads();
+        for (int f = tid; f < dk; f += kThreads) {  // (1, x, x_a x_b / sqrt 2 row-major)
+            float a = 1.f, b = 1.f;
+            if (f >= 1 && f <= din) {
+                a = qk_in[f - 1];
+                b = qk_in[din + f - 1];
+            } else if (f > din) {
+                const int i = (f - 1 - din) / din, j = (f - 1 - din) % din;
+                a = qk_in[i] * qk_in[j] * 0.70710678118654752f;
+                b = qk_in[din + i] * qk_in[din + j] * 0.70710678118654752f;
+            }
+            qf[f] = a;
+            kf[f] = b;
+        }
+    } else if (tid < dk) {
         float qv = load_elem(q, (size_t)bh * dk + tid);
         float kv = load_elem(k, (size_t)bh * dk + tid);
         qf[tid] = phi ? phi_elu1(qv) : qv;
@@ -102,11 +126,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     float den = 1.f;
     if (normalize) {
         float part = 0.f;
-        if (tid < dk) {
+        for (int f = tid; f < dk; f += kThreads) {
             float* zb = z + (size_t)bh * dk;
-            float zi = fmaf(gam, zb[tid], kf[tid]);
-            zb[tid] = zi;
-            part = qf[tid] * zi;
+            float zi = fmaf(gam, zb[f], kf[f]);
+            zb[f] = zi;
+            part += qf[f] * zi;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -138,11 +162,12 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
         decode_step_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
             (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
             (__nv_bfloat16*)a.o, a.S, a.z, a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps,
-            a.log_a, g);
+            a.log_a, a.taylor ? 1 : 0, g);
     } else {
         decode_step_kernel<float><<<grid, kThreads, 0, s>>>(
             (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.o, a.S, a.z,
-            a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, a.log_a, g);
+            a.H, a.dk, a.dv, a.phi, norm_mode(a.normalize, a.floor_norm), a.eps, a.log_a,
+            a.taylor ? 1 : 0, g);
     }
     return cudaGetLastError();
 }

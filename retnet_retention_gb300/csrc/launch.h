@@ -52,6 +52,7 @@ struct StepArgs {
     bool floor_norm;  // divide by max(|phi(q)^T z|, 1) (normalize is set too)
     float eps;
     const float* log_a;  // per-token decay: device fp32 [B][H] natural logs, or null
+    bool taylor;         // Taylor feature map: dk = 16 wide q, k; states of 1 + dk + dk^2 rows
 };
 
 // Arguments of one backward pass (gradients), validated by the ABI layer.

@@ -238,8 +238,10 @@ def test_taylor_outside_its_kernel_is_unsupported(lib, over):
     assert chunk(lib, **a) == la.LA_ERR_UNSUPPORTED
 
 
-def test_taylor_is_refused_by_the_decode_step_and_the_backward_pass(lib):
-    assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+def test_taylor_is_refused_by_the_backward_pass_and_outside_the_decode_steps_shapes(lib):
+    assert step(lib, dk=64, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR | la.LA_PHI_ELU1) == la.LA_ERR_UNSUPPORTED
+    assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR | la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
     assert bwd(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
     assert chunk_gated(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
     assert lib.la_bwd_workspace_size(2, 8, 64, 16, 64, 1, la.LA_PHI_TAYLOR) == 0

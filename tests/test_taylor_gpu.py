@@ -168,3 +168,52 @@ def test_taylor_linear_attention_bf16_sampled():
         check(f"O[{b},{h}]", np64(O[b, h]), Or[0, 0])
         check(f"S_T[{b},{h}]", np64(S[b, h]), Sr[0, 0])
         check(f"z_T[{b},{h}]", np64(z[b, h]), zr[0, 0])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("normalize", [True, False], ids=["normalised", "plain"])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_taylor_decode_steps(dv, normalize, dtype):
+    """Decode steps with the Taylor map (la_recurrent_step with LA_PHI_TAYLOR): the
+    273-row state updated in place, against the oracle's recurrence one token at a
+    time from a random initial state in the page's feature order."""
+    B, H, steps = 2, 3, 5
+    x = workloads.random_case(31 + dv, B, H, steps, 16, dv, dtype=dtype, scale=0.5)
+    rng = np.random.default_rng(dv)
+    S = torch.from_numpy(rng.standard_normal((B, H, DF, dv)).astype(np.float32) * 0.1)
+    z = torch.from_numpy(np.abs(rng.standard_normal((B, H, DF))).astype(np.float32) + 1.0)
+    Sd, zd = S.to(DEV), z.to(DEV)
+    Sr, zr = S.double().numpy(), z.double().numpy()
+    tol = 1e-4 if dtype == "f32" else TOL
+    for t in range(steps):
+        q, k, v = (x[n][:, :, t].contiguous() for n in ("q", "k", "v"))
+        o = la.recurrent_step(q.to(DEV), k.to(DEV), v.to(DEV), x["gamma"], Sd,
+                              zd if normalize else None, phi="taylor", normalize=normalize)
+        torch.cuda.synchronize()
+        Or, Sr, zr = oracle.recurrent_taylor(q[:, :, None], k[:, :, None], v[:, :, None], x["gamma"],
+                                             normalize=normalize, S0=Sr,
+                                             z0=zr if normalize else None)
+        check(f"o step {t}", np64(o), Or[:, :, 0], tol)
+        check(f"S step {t}", np64(Sd), Sr, tol)
+        if normalize:
+            check(f"z step {t}", np64(zd), zr, tol)
+
+
+def test_taylor_prefill_then_decode_equals_one_prefill():
+    """The chunkwise prefill's final state (the kernel's symmetric coordinates
+    turned back into the page's order) carries on in the decode step exactly as one
+    longer prefill would."""
+    B, H, T, dv, extra = 1, 2, 300, 64, 3
+    x = case((B, H, T + extra, dv), None, "prefill-decode")
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    _, S, z = la.chunk_fwd(q[:, :, :T].contiguous(), k[:, :, :T].contiguous(), v[:, :, :T].contiguous(),
+                           x["gamma"], phi="taylor", normalize=True)
+    outs = []
+    for t in range(T, T + extra):
+        outs.append(la.recurrent_step(q[:, :, t].contiguous(), k[:, :, t].contiguous(),
+                                      v[:, :, t].contiguous(), x["gamma"], S, z, phi="taylor",
+                                      normalize=True))
+    torch.cuda.synchronize()
+    Or, Sr, _ = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"], normalize=True)
+    check("decoded outputs", np.stack([np64(o) for o in outs], axis=2), Or[:, :, T:])
+    check("final state", np64(S), Sr)
