@@ -173,20 +173,39 @@ __device__ __forceinline__ void store_piece(char* tile, int r, int piece, const 
 }
 
 // Pieces [P0, P1) of the pair features of one token (row r of a 128-byte-swizzled
-// tile) from x and y = sc x: y_a x_b for a < b, y_a x_a / sqrt 2 for a = b.  The
-// pair index is a compile-time constant in every unrolled step.
+// tile): y_a x_b for a < b, y_a x_a / sqrt 2 for a = b, with y = sc x.  Two
+// neighbouring features of one row a are one packed bf16 product
+// (y_a, y_a) * (x_b, x_b+1): from the input's own bf16 pairs xp when b is even, from
+// the pairs shifted by one, xs, when b is odd; the diagonal takes the multiplier
+// (y_a / sqrt 2, y_a).  A word that straddles two rows is formed in fp32.  Every
+// index is a compile-time constant in the unrolled steps.
 template <int P0, int P1>
-__device__ __forceinline__ void pair_pieces(char* tile, int r, const float (&x)[kD], const float (&y)[kD]) {
-    float buf[8];
+__device__ __forceinline__ void pair_pieces(char* tile, int r, const float (&y)[kD], const float (&x)[kD],
+                                            const __nv_bfloat162 (&yy)[kD], const __nv_bfloat162 (&yd)[kD],
+                                            const __nv_bfloat162 (&xp)[kD / 2],
+                                            const __nv_bfloat162 (&xs)[kD / 2]) {
+    uint32_t word[4];
 #pragma unroll
     for (int a = 0; a < kD; ++a)
 #pragma unroll
         for (int b = a; b < kD; ++b) {
             const int p = pair_index(a, b);
-            if ((p >> 3) >= P0 && (p >> 3) < P1) {
-                buf[p & 7] = a == b ? y[a] * x[a] * 0.70710678118654752f : y[a] * x[b];
-                if ((p & 7) == 7) store_piece(tile, r, p >> 3, buf);
+            if ((p >> 3) < P0 || (p >> 3) >= P1 || (p & 1)) continue;  // words start at even p
+            // the second feature of the word: (a, b + 1), or the next row's diagonal
+            const bool same_row = b + 1 < kD;
+            __nv_bfloat162 w;
+            if (same_row) {
+                const __nv_bfloat162 m = a == b ? yd[a] : yy[a];
+                w = __hmul2(m, (b & 1) ? xs[b >> 1] : xp[b >> 1]);
+            } else {
+                const float f0 = a == b ? y[a] * x[a] * 0.70710678118654752f : y[a] * x[b];
+                const float f1 = y[a + 1] * x[a + 1] * 0.70710678118654752f;
+                w = __floats2bfloat162_rn(f0, f1);
             }
+            word[(p & 7) >> 1] = *reinterpret_cast<uint32_t*>(&w);
+            if ((p & 7) == 6)
+                *reinterpret_cast<uint4*>(tile + (p >> 6) * kBlk + sw128_offset(r, ((p >> 3) & 7) * 8)) =
+                    make_uint4(word[0], word[1], word[2], word[3]);
         }
 }
 
@@ -422,12 +441,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 if (r < L) sc = unit_gamma ? 1.f : gamma_pow(l2g, (float)(is_q ? r + 1 : L - 1 - r));
                 float x[kD], y[kD];
                 unpack16(src, x);
+                __nv_bfloat162 xp[kD / 2], xs[kD / 2], yy[kD], yd[kD];
 #pragma unroll
-                for (int a = 0; a < kD; ++a) y[a] = x[a] * sc;
+                for (int e = 0; e < kD / 2; ++e) {
+                    xp[e] = reinterpret_cast<const __nv_bfloat162*>(src)[e];  // (x_2e, x_2e+1)
+                    xs[e] = __floats2bfloat162_rn(x[2 * e + 1], 2 * e + 2 < kD ? x[2 * e + 2] : 0.f);
+                }
+#pragma unroll
+                for (int a = 0; a < kD; ++a) {
+                    y[a] = x[a] * sc;
+                    yy[a] = __float2bfloat162_rn(y[a]);
+                    yd[a] = __floats2bfloat162_rn(y[a] * 0.70710678118654752f, y[a]);
+                }
                 if ((sub & 1) == 0) {
-                    pair_pieces<0, 11>(tile, r, x, y);
+                    pair_pieces<0, 11>(tile, r, y, x, yy, yd, xp, xs);
                 } else {
-                    pair_pieces<11, 17>(tile, r, x, y);
+                    pair_pieces<11, 17>(tile, r, y, x, yy, yd, xp, xs);
                     linear_pieces(tile, r, y, sc);
                     if (is_q) {  // the raw rows (the tile loads zero past the end of the sequence)
                         const uint4* qr = reinterpret_cast<const uint4*>(src);
@@ -452,6 +481,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_taylor_kernel(const __grid_
                 if (sub > q4) {  // warp-uniform: above the diagonal
 #pragma unroll
                     for (int e = 0; e < 16; ++e) out[e] = 0u;
+                } else if (sub < q4 && L == kC && unit_gamma) {  // below the diagonal, no mask, no decay
+#pragma unroll
+                    for (int h16 = 0; h16 < 32; h16 += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(tbase + lane_off + kColSc + cc + h16, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float s0 = __uint_as_float(r[e]), s1 = __uint_as_float(r[e + 1]);
+                            out[(h16 + e) >> 1] = pack_bf16x2(fmaf(s0, fmaf(0.5f, s0, 1.f), 1.f),
+                                                              fmaf(s1, fmaf(0.5f, s1, 1.f), 1.f));
+                        }
+                    }
                 } else {
                     const bool diag = sub == q4;
                     const bool live = i < L;
