@@ -47,8 +47,8 @@ KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "t
                   "chunk_tc.cu", "common.cuh", "launch.h")
 TRAFFIC = {
     "chunk_tc_ws_kernel/full": {
-        "bytes": 52_006_656 + 270_080,
-        "sources_sha256": "c4e34d45d4d377febdf0e57cd9704534c7315dcc17b17cd5ce85f06d246735ef",
+        "bytes": 52_004_352 + 258_304,
+        "sources_sha256": "98538441051e49c46a9f8670e30af380a71ddec74fe2519aa9d8bcd3a7996671",
     },
 }
 HEADLINE = "linear_attention_bf16"
