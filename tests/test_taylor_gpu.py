@@ -217,3 +217,26 @@ def test_taylor_prefill_then_decode_equals_one_prefill():
     Or, Sr, _ = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"], normalize=True)
     check("decoded outputs", np.stack([np64(o) for o in outs], axis=2), Or[:, :, T:])
     check("final state", np64(S), Sr)
+
+
+def test_taylor_with_the_floored_normaliser():
+    """LA_PHI_TAYLOR with LA_NORM_FLOOR: divide by max(|phi(q)^T z|, 1), chunkwise and
+    in the decode step (the Taylor kernel is >= 1/2, so short prefixes with gamma < 1
+    sit below the floor)."""
+    B, H, T, dv = 1, 2, 300, 64
+    x = case((B, H, T, dv), [0.3, 0.5], "floor")
+    O, S, z = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"], phi="taylor",
+                           floor=True)
+    torch.cuda.synchronize()
+    Or, Sr, zr = oracle.recurrent_taylor(x["q"], x["k"], x["v"], x["gamma"], floor=True)
+    check("O", np64(O), Or)
+    check("S_T", np64(S), Sr)
+    check("z_T", np64(z), zr)
+    q1, k1, v1 = (workloads.random_case(77, B, H, 1, 16, dv, dtype="bf16", scale=0.5)[n][:, :, 0].contiguous()
+                  for n in ("q", "k", "v"))
+    o = la.recurrent_step(q1.to(DEV), k1.to(DEV), v1.to(DEV), x["gamma"], S, z, phi="taylor", floor=True)
+    torch.cuda.synchronize()
+    Or1, Sr1, _ = oracle.recurrent_taylor(q1[:, :, None], k1[:, :, None], v1[:, :, None], x["gamma"],
+                                          floor=True, S0=Sr, z0=zr)
+    check("decode o", np64(o), Or1[:, :, 0])
+    check("decode S", np64(S), Sr1)
