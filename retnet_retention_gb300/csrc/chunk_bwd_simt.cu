@@ -163,31 +163,72 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         auto xi = [&](int i) { return log_a ? xw[i] : pw[i + 1]; };
         auto zt = [&](int j) { return log_a ? zeta[j] : pw[L - 1 - j]; };
         const float gL = log_a ? exp2f(cum[L - 1]) : pw[L];
-
-        // A_ij = D_ij q~_i . k~_j (j <= i)
-        for (int idx = tid; idx < L * L; idx += kThreads) {
-            const int i = idx / L, j = idx % L;
-            float a = 0.f;
-            if (j <= i) {
-                const float* qi = Qs + i * ldk;
-                const float* kj = Ks + j * ldk;
-                float dot = 0.f;
-                for (int d = 0; d < dk; ++d) dot = fmaf(qi[d], kj[d], dot);
-                a = dot * dmask(i, j);
+        // Register tiles: a thread computes 4 output rows x 2 columns (c = 64 g + slot
+        // and c + 32), so each shared-memory operand it loads feeds 2 or 4 FMAs; the
+        // 32 items of a warp share their rows (broadcast loads) and take consecutive
+        // columns.  Every output keeps its summation order.
+        auto tiles = [&](int R, int D, auto&& body) {
+            const int ng = (D + 63) >> 6;
+            const int items = ((R + 3) >> 2) * ng * 32;
+            for (int item = tid; item < items; item += kThreads) {
+                const int slot = item & 31, rest = item >> 5;
+                const int c0 = 64 * (rest % ng) + slot;
+                body((rest / ng) * 4, c0, c0 + 32);
             }
-            As[i * lda + j] = a;
+        };
+
+        // A_ij = D_ij q~_i . k~_j (j <= i): tiles of 4 rows i and one column j
+        for (int item = tid; item < ((L + 3) >> 2) * 32; item += kThreads) {
+            const int j = item & 31, i0 = (item >> 5) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (j < L && j <= i0 + 3) {
+                const float* kj = Ks + j * ldk;
+                for (int d = 0; d < dk; ++d) {
+                    const float kv = kj[d];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[r] = fmaf(Qs[(i0 + r) * ldk + d], kv, acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r;
+                if (i < L && j < L) As[i * lda + j] = j <= i ? acc[r] * dmask(i, j) : 0.f;
+            }
         }
         __syncthreads();
         if (role == 0) {
             if (normalize) {
-                // n_i = sum_j A_ij v_j + xi_i q~_i S
-                for (int idx = tid; idx < L * dv; idx += kThreads) {
-                    const int i = idx / dv, cc2 = idx % dv;
-                    float intra = 0.f, inter = 0.f;
-                    for (int j = 0; j <= i; ++j) intra = fmaf(As[i * lda + j], Vs[j * ldv + cc2], intra);
-                    for (int d = 0; d < dk; ++d) inter = fmaf(Qs[i * ldk + d], Ss[d * lds + cc2], inter);
-                    Ns[i * ldv + cc2] = intra + xi(i) * inter;
-                }
+                // n_i = sum_j A_ij v_j + xi_i q~_i S  (A_ij = 0 above the diagonal)
+                tiles(L, dv, [&](int i0, int c0, int c1) {
+                    const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
+                    float in[4][2] = {}, it[4][2] = {};
+                    const int jmax = min(i0 + 3, L - 1);
+                    for (int j = 0; j <= jmax; ++j) {
+                        const float x0 = Vs[j * ldv + a0], x1 = Vs[j * ldv + a1];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float a = As[(i0 + r) * lda + j];
+                            in[r][0] = fmaf(a, x0, in[r][0]);
+                            in[r][1] = fmaf(a, x1, in[r][1]);
+                        }
+                    }
+                    for (int d = 0; d < dk; ++d) {
+                        const float s0 = Ss[d * lds + a0], s1 = Ss[d * lds + a1];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float q = Qs[(i0 + r) * ldk + d];
+                            it[r][0] = fmaf(q, s0, it[r][0]);
+                            it[r][1] = fmaf(q, s1, it[r][1]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int i = i0 + r;
+                        if (i >= L) continue;
+                        if (c0 < dv) Ns[i * ldv + c0] = in[r][0] + xi(i) * it[r][0];
+                        if (c1 < dv) Ns[i * ldv + c1] = in[r][1] + xi(i) * it[r][1];
+                    }
+                });
                 __syncthreads();
                 // den_i, du_i (one warp per row: the sums over d_k and d_v)
                 const int warp = tid >> 5, lane = tid & 31;
@@ -225,40 +266,87 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             }
             __syncthreads();
         }
-        // P_ij = D_ij (dn_i . v_j + du_i)  (j <= i)
-        for (int idx = tid; idx < L * L; idx += kThreads) {
-            const int i = idx / L, j = idx % L;
-            float pv = 0.f;
-            if (j <= i) {
-                const float* gi = Gs + i * ldv;
+        // P_ij = D_ij (dn_i . v_j + du_i)  (j <= i): tiles of 4 rows i and one column j
+        for (int item = tid; item < ((L + 3) >> 2) * 32; item += kThreads) {
+            const int j = item & 31, i0 = (item >> 5) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (j < L && j <= i0 + 3) {
                 const float* vj = Vs + j * ldv;
-                float dot = 0.f;
-                for (int cc2 = 0; cc2 < dv; ++cc2) dot = fmaf(gi[cc2], vj[cc2], dot);
-                pv = (dot + (normalize ? du[i] : 0.f)) * dmask(i, j);
+                for (int cc2 = 0; cc2 < dv; ++cc2) {
+                    const float vv = vj[cc2];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[r] = fmaf(Gs[(i0 + r) * ldv + cc2], vv, acc[r]);
+                }
             }
-            Ps[i * lda + j] = pv;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r;
+                if (i < L && j < L)
+                    Ps[i * lda + j] = j <= i ? (acc[r] + (normalize ? du[i] : 0.f)) * dmask(i, j) : 0.f;
+            }
         }
         __syncthreads();
         if (role == 0) {
             // dq~_i = sum_j P_ij k~_j + xi_i (S dn_i + du_i z);  dq = dq~ * phi'(q)
-            for (int idx = tid; idx < L * dk; idx += kThreads) {
-                const int i = idx / dk, d = idx % dk;
-                float intra = 0.f, inter = 0.f;
-                for (int j = 0; j <= i; ++j) intra = fmaf(Ps[i * lda + j], Ks[j * ldk + d], intra);
-                for (int cc2 = 0; cc2 < dv; ++cc2) inter = fmaf(Ss[d * lds + cc2], Gs[i * ldv + cc2], inter);
-                if (normalize) inter = fmaf(du[i], zs[d], inter);
-                float r = intra + xi(i) * inter;
-                if (phi) r *= fminf(1.f, Qs[i * ldk + d]);
-                store_elem(dQ, qk_base + (size_t)(t0 + i) * dk + d, r);
-            }
+            tiles(L, dk, [&](int i0, int c0, int c1) {
+                const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
+                float in[4][2] = {}, it[4][2] = {};
+                const int jmax = min(i0 + 3, L - 1);
+                for (int j = 0; j <= jmax; ++j) {
+                    const float k0 = Ks[j * ldk + a0], k1 = Ks[j * ldk + a1];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float pp = Ps[(i0 + r) * lda + j];
+                        in[r][0] = fmaf(pp, k0, in[r][0]);
+                        in[r][1] = fmaf(pp, k1, in[r][1]);
+                    }
+                }
+                for (int cc2 = 0; cc2 < dv; ++cc2) {
+                    const float s0 = Ss[a0 * lds + cc2], s1 = Ss[a1 * lds + cc2];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float gg = Gs[(i0 + r) * ldv + cc2];
+                        it[r][0] = fmaf(s0, gg, it[r][0]);
+                        it[r][1] = fmaf(s1, gg, it[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r;
+                    if (i >= L) continue;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int d = e ? c1 : c0;
+                        if (d >= dk) continue;
+                        float inter = it[r][e];
+                        if (normalize) inter = fmaf(du[i], zs[d], inter);
+                        float v = in[r][e] + xi(i) * inter;
+                        if (phi) v *= fminf(1.f, Qs[i * ldk + d]);
+                        store_elem(dQ, qk_base + (size_t)(t0 + i) * dk + d, v);
+                    }
+                }
+            });
             __syncthreads();
             // S = gamma^L S + sum_j zeta_j k~_j^T v_j ; z likewise
-            for (int idx = tid; idx < dk * dv; idx += kThreads) {
-                const int d = idx / dv, cc2 = idx % dv;
-                float u = 0.f;
-                for (int j = 0; j < L; ++j) u = fmaf(zt(j) * Ks[j * ldk + d], Vs[j * ldv + cc2], u);
-                Ss[d * lds + cc2] = fmaf(gL, Ss[d * lds + cc2], u);
-            }
+            tiles(dk, dv, [&](int d0, int c0, int c1) {
+                const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
+                float u[4][2] = {};
+                for (int j = 0; j < L; ++j) {
+                    const float x0 = Vs[j * ldv + a0], x1 = Vs[j * ldv + a1], zj = zt(j);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float kk = zj * Ks[j * ldk + d0 + r];
+                        u[r][0] = fmaf(kk, x0, u[r][0]);
+                        u[r][1] = fmaf(kk, x1, u[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int d = d0 + r;
+                    if (c0 < dv) Ss[d * lds + c0] = fmaf(gL, Ss[d * lds + c0], u[r][0]);
+                    if (c1 < dv) Ss[d * lds + c1] = fmaf(gL, Ss[d * lds + c1], u[r][1]);
+                }
+            });
             for (int d = tid; d < dk; d += kThreads) {
                 float u = 0.f;
                 for (int j = 0; j < L; ++j) u = fmaf(zt(j), Ks[j * ldk + d], u);
@@ -267,32 +355,94 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             __syncthreads();
         } else {
             // dv_j = sum_{i>=j} A_ij dn_i + zeta_j k~_j G
-            for (int idx = tid; idx < L * dv; idx += kThreads) {
-                const int j = idx / dv, cc2 = idx % dv;
-                float intra = 0.f, inter = 0.f;
-                for (int i = j; i < L; ++i) intra = fmaf(As[i * lda + j], Gs[i * ldv + cc2], intra);
-                for (int d = 0; d < dk; ++d) inter = fmaf(Ks[j * ldk + d], Ss[d * lds + cc2], inter);
-                store_elem(dV, v_base + (size_t)(t0 + j) * dv + cc2, intra + zt(j) * inter);
-            }
+            tiles(L, dv, [&](int j0, int c0, int c1) {
+                const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
+                float in[4][2] = {}, it[4][2] = {};
+                for (int i = j0; i < L; ++i) {  // A_ij = 0 for i < j
+                    const float g0 = Gs[i * ldv + a0], g1 = Gs[i * ldv + a1];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float a = As[i * lda + j0 + r];
+                        in[r][0] = fmaf(a, g0, in[r][0]);
+                        in[r][1] = fmaf(a, g1, in[r][1]);
+                    }
+                }
+                for (int d = 0; d < dk; ++d) {
+                    const float s0 = Ss[d * lds + a0], s1 = Ss[d * lds + a1];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float kk = Ks[(j0 + r) * ldk + d];
+                        it[r][0] = fmaf(kk, s0, it[r][0]);
+                        it[r][1] = fmaf(kk, s1, it[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int j = j0 + r;
+                    if (j >= L) continue;
+                    if (c0 < dv) store_elem(dV, v_base + (size_t)(t0 + j) * dv + c0, in[r][0] + zt(j) * it[r][0]);
+                    if (c1 < dv) store_elem(dV, v_base + (size_t)(t0 + j) * dv + c1, in[r][1] + zt(j) * it[r][1]);
+                }
+            });
             // dk~_j = sum_{i>=j} P_ij q~_i + zeta_j (G v_j + Gz);  dk = dk~ * phi'(k)
-            for (int idx = tid; idx < L * dk; idx += kThreads) {
-                const int j = idx / dk, d = idx % dk;
-                float intra = 0.f, inter = 0.f;
-                for (int i = j; i < L; ++i) intra = fmaf(Ps[i * lda + j], Qs[i * ldk + d], intra);
-                for (int cc2 = 0; cc2 < dv; ++cc2) inter = fmaf(Ss[d * lds + cc2], Vs[j * ldv + cc2], inter);
-                if (normalize) inter += zs[d];
-                float r = intra + zt(j) * inter;
-                if (phi) r *= fminf(1.f, Ks[j * ldk + d]);
-                store_elem(dK, qk_base + (size_t)(t0 + j) * dk + d, r);
-            }
+            tiles(L, dk, [&](int j0, int c0, int c1) {
+                const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
+                float in[4][2] = {}, it[4][2] = {};
+                for (int i = j0; i < L; ++i) {  // P_ij = 0 for i < j
+                    const float q0 = Qs[i * ldk + a0], q1 = Qs[i * ldk + a1];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float pp = Ps[i * lda + j0 + r];
+                        in[r][0] = fmaf(pp, q0, in[r][0]);
+                        in[r][1] = fmaf(pp, q1, in[r][1]);
+                    }
+                }
+                for (int cc2 = 0; cc2 < dv; ++cc2) {
+                    const float s0 = Ss[a0 * lds + cc2], s1 = Ss[a1 * lds + cc2];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float vv = Vs[(j0 + r) * ldv + cc2];
+                        it[r][0] = fmaf(s0, vv, it[r][0]);
+                        it[r][1] = fmaf(s1, vv, it[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int j = j0 + r;
+                    if (j >= L) continue;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int d = e ? c1 : c0;
+                        if (d >= dk) continue;
+                        float inter = it[r][e];
+                        if (normalize) inter += zs[d];
+                        float v = in[r][e] + zt(j) * inter;
+                        if (phi) v *= fminf(1.f, Ks[j * ldk + d]);
+                        store_elem(dK, qk_base + (size_t)(t0 + j) * dk + d, v);
+                    }
+                }
+            });
             __syncthreads();
             // G = gamma^L G + sum_i xi_i q~_i^T dn_i ;  Gz = gamma^L Gz + sum_i xi_i du_i q~_i
-            for (int idx = tid; idx < dk * dv; idx += kThreads) {
-                const int d = idx / dv, cc2 = idx % dv;
-                float u = 0.f;
-                for (int i = 0; i < L; ++i) u = fmaf(xi(i) * Qs[i * ldk + d], Gs[i * ldv + cc2], u);
-                Ss[d * lds + cc2] = fmaf(gL, Ss[d * lds + cc2], u);
-            }
+            tiles(dk, dv, [&](int d0, int c0, int c1) {
+                const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
+                float u[4][2] = {};
+                for (int i = 0; i < L; ++i) {
+                    const float g0 = Gs[i * ldv + a0], g1 = Gs[i * ldv + a1], x = xi(i);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float qq = x * Qs[i * ldk + d0 + r];
+                        u[r][0] = fmaf(qq, g0, u[r][0]);
+                        u[r][1] = fmaf(qq, g1, u[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int d = d0 + r;
+                    if (c0 < dv) Ss[d * lds + c0] = fmaf(gL, Ss[d * lds + c0], u[r][0]);
+                    if (c1 < dv) Ss[d * lds + c1] = fmaf(gL, Ss[d * lds + c1], u[r][1]);
+                }
+            });
             if (normalize)
                 for (int d = tid; d < dk; d += kThreads) {
                     float u = 0.f;
