@@ -33,7 +33,10 @@
 // lane quarter) that run E1, then E3 together with the feature tiles of the next
 // chunk as soon as MMA3 / MMA4 are done, then E2; mbarriers hand over between the
 // roles, every wait bounded in time.  E1 touches only the score pieces on or
-// below the diagonal.
+// below the diagonal.  O has two TMEM buffers (chunk c uses c mod 2), so MMA3 of
+// the next chunk need not wait for E2; E2 writes O into a swizzled shared-memory
+// tile that one thread stores with TMA.  The pair features are packed bf16
+// products, two features of one row per instruction.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
