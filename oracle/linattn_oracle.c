@@ -179,7 +179,9 @@ static int recurrent(const double* Q, const double* K, const double* V,
                     den = fabs(den) > 1.0 ? fabs(den) : 1.0;
 #endif
                 } else {
+#if ORACLE_MUTANT != 13 /* mutant 13: eps left out of the denominator */
                     den += eps;
+#endif
                 }
                 for (long j = 0; j < dv; ++j) o[j] /= den;
             }
@@ -240,6 +242,16 @@ int oracle_recurrent_gated(const double* Q, const double* K, const double* V,
  *   forward pass.  Returns 0, or -1 when a scratch allocation fails.
  */
 static double phi_grad(double x) { return x > 0.0 ? 1.0 : exp(x); }
+
+/* Token t's own term of dL/dS_t and dL/dz_t: G += q~_t^T dn_t, Gz += du_t q~_t. */
+static void add_query_term(double* G, double* Gz, const double* qf, const double* g_o,
+                           double den_t, double du_t, long dk, long dv)
+{
+    for (long i = 0; i < dk; ++i) {
+        for (long j = 0; j < dv; ++j) G[i * dv + j] += qf[i] * g_o[j] / den_t;
+        Gz[i] += du_t * qf[i];
+    }
+}
 
 static int recurrent_bwd(const double* Q, const double* K, const double* V,
                          const double* gamma, const double* log_a, long B, long H, long T,
@@ -328,10 +340,9 @@ static int recurrent_bwd(const double* Q, const double* K, const double* V,
             const double g = log_a ? exp(log_a[bh * T + t]) : gamma[h];
             feature(q, qf, dk, phi);
             feature(k, kf, dk, phi);
-            for (long i = 0; i < dk; ++i) {
-                for (long j = 0; j < dv; ++j) G[i * dv + j] += qf[i] * g_o[j] / den[t];
-                Gz[i] += du[t] * qf[i];
-            }
+#if ORACLE_MUTANT != 15 /* mutant 15: dv and dk read G before the token's own term */
+            add_query_term(G, Gz, qf, g_o, den[t], du[t], dk, dv);
+#endif
             double* gv = dV + (bh * T + t) * dv;
             for (long j = 0; j < dv; ++j) {
                 double acc = 0.0;
@@ -343,8 +354,13 @@ static int recurrent_bwd(const double* Q, const double* K, const double* V,
                 double acc = 0.0;
                 for (long j = 0; j < dv; ++j) acc += G[i * dv + j] * v[j];
                 gk[i] = acc + Gz[i];
+#if ORACLE_MUTANT != 16 /* mutant 16: dk without the chain rule through phi */
                 if (phi) gk[i] *= phi_grad(k[i]);
+#endif
             }
+#if ORACLE_MUTANT == 15
+            add_query_term(G, Gz, qf, g_o, den[t], du[t], dk, dv);
+#endif
 #if ORACLE_MUTANT != 10 /* mutant 10: the reverse sweep forgets the decay */
             for (long i = 0; i < dk; ++i) {
                 for (long j = 0; j < dv; ++j) G[i * dv + j] *= g;
@@ -393,7 +409,11 @@ int oracle_noncausal(const double* Q, const double* K, const double* V,
             free(S); free(z); free(f);
             continue;
         }
+#if ORACLE_MUTANT == 14 /* mutant: the summary leaves out the last token */
+        for (long t = 0; t < T - 1; ++t) {
+#else
         for (long t = 0; t < T; ++t) {
+#endif
             const double* k = K + (bh * T + t) * dk;
             const double* v = V + (bh * T + t) * dv;
             feature(k, f, dk, phi);
@@ -445,8 +465,16 @@ void oracle_taylor_features(const double* X, long n, long d, double* out)
     for (long t = 0; t < n; ++t) {
         const double* x = X + t * d;
         double* f = out + t * df;
+#if ORACLE_MUTANT == 17 /* mutant: the constant feature left out */
+        f[0] = 0.0;
+#else
         f[0] = 1.0;
+#endif
+#if ORACLE_MUTANT == 18 /* mutant: the linear features left out */
+        for (long i = 0; i < d; ++i) f[1 + i] = 0.0;
+#else
         for (long i = 0; i < d; ++i) f[1 + i] = x[i];
+#endif
         for (long i = 0; i < d; ++i)
             for (long j = 0; j < d; ++j)
 #if ORACLE_MUTANT == 12 /* mutant: the outer product without the 1 / sqrt(2) */

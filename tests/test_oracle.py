@@ -554,6 +554,12 @@ MUTANTS = {
     10: "backward sweep without the decay",
     11: "dq without the normaliser's term",
     12: "Taylor features without the 1/sqrt(2)",
+    13: "eps left out of the denominator",
+    14: "non-causal summary without the last token",
+    15: "backward reads G before the token's own term",
+    16: "dk without the chain rule through phi",
+    17: "Taylor features without the constant",
+    18: "Taylor features without the linear part",
 }
 
 
