@@ -44,6 +44,20 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"{name} declared in linattn.h but not exported"
 
 
+def test_binding_constants_match_the_header():
+    """Every flag, status and dtype value the Python binding passes equals the
+    header's definition (a drift would silently select another operation)."""
+    text = open(HEADER).read()
+    defined = {m[0]: int(m[1]) for m in re.findall(r"#define\s+(LA_[A-Z0-9_]+)\s+(\d+)u?\b", text)}
+    defined.update({m[0]: int(m[1]) for m in re.findall(r"\b(LA_[A-Z0-9_]+)\s*=\s*(\d+)", text)})
+    names = ["LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_UNSUPPORTED", "LA_ERR_CUDA", "LA_ERR_TIMEOUT",
+             "LA_DTYPE_F32", "LA_DTYPE_BF16", "LA_PHI_ELU1", "LA_NORMALIZE", "LA_NONCAUSAL",
+             "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR"]
+    for name in names:
+        assert getattr(la, name) == defined[name], name
+    assert la.abi_version() == defined["LA_ABI_VERSION"]
+
+
 def test_status_strings_and_version(lib):
     assert la.abi_version() == 1
     for code in range(5):
