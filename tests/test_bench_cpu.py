@@ -76,3 +76,38 @@ def test_headline_is_bound_by_bytes_and_taylor_sits_at_the_ridge():
     ratio = bench.alg_flops(t) / bench.alg_bytes(t) / ridge
     assert 0.9 < ratio < 1.1
     assert np.isfinite(ratio)
+
+
+def test_clock_summary_takes_the_median_under_load_and_every_reason():
+    """The clock record: idle samples (under a quarter of the peak power) stay out of
+    the median, and a throttle reason seen in any sample is reported."""
+    s = bench.ClockSampler(0)
+    s.out = "\n".join([
+        "0, 900, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2040, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbled line",
+        "0, [N/A], 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ])
+    c = s.summary()
+    assert c["sm_mhz"] == 2040.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 4
+    assert c["reasons"] == ["sw_power_cap"]
+    s.out = "0, 1500, 2070, 1200.0, 0x8, Active, Not Active, Active, Not Active"
+    assert bench.ClockSampler.summary(s)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    s.out = ""
+    assert s.summary() is None
+
+
+def test_peaks_come_from_the_measured_file(tmp_path, monkeypatch):
+    """The roofline's denominators: the measured file when present (sustained falling
+    back to burst), else the stated fallback figures."""
+    import json
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.peaks()
+    assert p["source"] == "fallback" and p["hbm_gbs"] == 6800.0 and p["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.5,
+                                                              "bf16_tflops": 2000.0}))
+    p = bench.peaks()
+    assert p["source"] == "measured" and p["hbm_gbs"] == 7000.5
+    assert p["bf16_tflops_sustained"] == 2000.0
