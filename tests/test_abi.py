@@ -269,3 +269,15 @@ def test_taylor_plan_queries(lib):
     assert la.state_rows(16, "taylor") == 273 and la.state_rows(16) == 16
     with pytest.raises(ValueError):
         la._flags("softmax", False, True)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library the binding raises: no compute falls back to the host."""
+    monkeypatch.setattr(la, "_LIB", None)
+    monkeypatch.setattr(la, "LIBRARY_PATH", str(tmp_path / "liblinattn.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        la.library()
+    import torch
+    q = torch.zeros(1, 1, 4, 16)
+    with pytest.raises((RuntimeError, ValueError)):
+        la.chunk_fwd(q, q, q, [0.9])
