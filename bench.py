@@ -48,7 +48,7 @@ KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "t
 TRAFFIC = {
     "chunk_tc_ws_kernel/full": {
         "bytes": 52_004_352 + 258_304,
-        "sources_sha256": "98538441051e49c46a9f8670e30af380a71ddec74fe2519aa9d8bcd3a7996671",
+        "sources_sha256": "5a67b81656af89f519c876819897b15768328fea277a8ddad0b8e36824a9f500",
     },
 }
 HEADLINE = "linear_attention_bf16"

@@ -557,7 +557,6 @@ int sm_count() {
     return n > 0 ? n : 1;
 }
 
-// Segments per sequence: enough units to cover the SMs once.
 // Segments per sequence: as many as fit the SMs in one wave (the kernels run
 // one CTA per SM), when that is at least two and each segment keeps two or
 // more chunks.
