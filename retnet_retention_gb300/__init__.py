@@ -153,6 +153,27 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _buffer(t, name: str, numel: int, dtype, device):
+    """Check a caller-supplied tensor before its address goes to the library, which
+    reads or writes `numel` elements of `dtype` there and cannot see the tensor's
+    size: a smaller, differently typed or misplaced tensor is refused (None passes)."""
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the inputs are on {device}")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+
+
+def _states(B: int, H: int, ds: int, dv: int, device, **bufs):
+    """The fp32 states and normalisers of a call: S-like [B,H,ds,dv], z-like [B,H,ds]."""
+    for name, t in bufs.items():
+        _buffer(t, name, B * H * ds * (1 if name.startswith(("z", "dz")) else dv),
+                torch.float32, device)
+
+
 def _gamma_host(gamma, H: int) -> np.ndarray:
     if isinstance(gamma, torch.Tensor):
         gamma = gamma.detach().to("cpu", torch.float32).numpy()
@@ -221,6 +242,10 @@ def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, e
         raise ValueError("pass exactly one of gamma and log_a")
     if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
         raise ValueError(f"log_a must be float32 [B,H,T] = {(B, H, T)}")
+    _buffer(log_a, "log_a", B * H * T, torch.float32, dev)
+    _buffer(out, "out", B * H * T * dv, q.dtype, dev)
+    _states(B, H, ds, dv, dev, S0=S0, z0=z0, S_out=S_out, z_out=z_out)
+    _buffer(dev_status, "dev_status", 1, torch.int32, dev)
     flags = _flags(phi, normalize, causal, floor)
     lib = _load()
     need = int(lib.la_workspace_size(B, H, T, dk, dv, dt,
@@ -254,6 +279,13 @@ def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True
     dv = v.shape[-1]
     if out is None or S_out is None:
         raise ValueError("chunk_fwd_noalloc allocates nothing: pass out and S_out")
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    _buffer(out, "out", B * H * T * dv, q.dtype, q.device)
+    _states(B, H, state_rows(dk, phi), dv, q.device, S0=S0, z0=z0, S_out=S_out, z_out=z_out)
+    _buffer(dev_status, "dev_status", 1, torch.int32, q.device)
     g = _gamma_host(gamma, H)
     st = _load().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
                                       H, T, dk, dv, _flags(phi, normalize, causal, floor), float(eps),
@@ -270,10 +302,18 @@ def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps
     per-token log decays, a [B,H] fp32 device tensor, instead of gamma."""
     B, H, dk = q.shape
     dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:2] != q.shape[:2]:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     if (gamma is None) == (log_a is None):
         raise ValueError("pass exactly one of gamma and log_a")
+    _buffer(out, "out", B * H * dv, q.dtype, q.device)
+    _states(B, H, state_rows(dk, phi), dv, q.device, S=S, z=z)
+    _buffer(dev_status, "dev_status", 1, torch.int32, q.device)
+    _buffer(log_a, "log_a", B * H, torch.float32, q.device)
     flags = _flags(phi, normalize, True, floor)
     if log_a is None:
         g = _gamma_host(gamma, H)
@@ -311,6 +351,13 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
         raise ValueError("pass exactly one of gamma and log_a")
     dt = _dtype_code(q)
     dev = q.device
+    if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
+        raise ValueError(f"log_a must be float32 [B,H,T] = {(B, H, T)}")
+    _buffer(log_a, "log_a", B * H * T, torch.float32, dev)
+    _states(B, H, dk_, dv_, dev, S0=S0, z0=z0, dS_T=dS_T, dz_T=dz_T)
+    _buffer(dq, "dq", B * H * T * dk_, q.dtype, dev)
+    _buffer(dk, "dk", B * H * T * dk_, q.dtype, dev)
+    _buffer(dv, "dv", B * H * T * dv_, q.dtype, dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

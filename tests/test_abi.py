@@ -281,3 +281,47 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     q = torch.zeros(1, 1, 4, 16)
     with pytest.raises((RuntimeError, ValueError)):
         la.chunk_fwd(q, q, q, [0.9])
+
+
+def test_python_binding_checks_caller_buffers():
+    """Caller-supplied outputs, states and gradients are checked for element count,
+    dtype and device before their addresses reach the library (which cannot see a
+    tensor's size): an undersized or mistyped buffer is refused, not written past."""
+    import torch
+    B, H, T, d = 2, 3, 8, 16
+    q = torch.zeros(B, H, T, d, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="out holds"):
+        la.chunk_fwd(q, q, q, [0.5], out=torch.empty(B, H, T - 1, d, dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="out must be"):
+        la.chunk_fwd(q, q, q, [0.5], out=torch.empty(B, H, T, d))
+    with pytest.raises(TypeError, match="S0 must be"):
+        la.chunk_fwd(q, q, q, [0.5], S0=torch.zeros(B, H, d, d, dtype=torch.float64))
+    with pytest.raises(ValueError, match="S0 holds"):  # the Taylor map's states have 273 rows
+        la.chunk_fwd(q, q, torch.zeros(B, H, T, 64, dtype=torch.bfloat16), [0.5], phi="taylor",
+                     S0=torch.zeros(B, H, d, 64))
+    with pytest.raises(ValueError, match="z_out holds"):
+        la.chunk_fwd(q, q, q, [0.5], normalize=True, z_out=torch.empty(B, H, d - 1))
+    with pytest.raises(TypeError, match="dev_status must be"):
+        la.chunk_fwd(q, q, q, [0.5], dev_status=torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(ValueError, match="S_out holds"):
+        la.chunk_fwd_noalloc(q, q, q, [0.5], out=torch.empty_like(q), S_out=torch.empty(B, H, d))
+    with pytest.raises(ValueError, match="shape mismatch"):
+        la.chunk_fwd_noalloc(q, q[:, :, :4], q, [0.5], out=torch.empty_like(q),
+                             S_out=torch.empty(B, H, d, d))
+    s = q[:, :, 0].contiguous()
+    with pytest.raises(ValueError, match="shape mismatch"):
+        la.recurrent_step(s, s[:1], s, [0.5], torch.zeros(B, H, d, d))
+    with pytest.raises(ValueError, match="S holds"):
+        la.recurrent_step(s, s, s, [0.5], torch.zeros(B, H, d, d - 1))
+    with pytest.raises(ValueError, match="z holds"):
+        la.recurrent_step(s, s, s, [0.5], torch.zeros(B, H, d, d), torch.zeros(B, H, 1),
+                          normalize=True)
+    with pytest.raises(ValueError, match="dq holds"):
+        la.chunk_bwd(q, q, q, q, [0.5], dq=torch.empty(B, H, T, d - 1, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="dS_T holds"):
+        la.chunk_bwd(q, q, q, q, [0.5], dS_T=torch.zeros(B, H, d))
+    with pytest.raises(ValueError, match="log_a must be"):
+        la.chunk_bwd(q, q, q, q, log_a=torch.zeros(B, H, T - 1))
+    # buffers of the right size still fail only on being host memory
+    with pytest.raises(ValueError, match="CUDA device tensors"):
+        la.chunk_fwd(q, q, q, [0.5], out=torch.empty_like(q), S_out=torch.empty(B, H, d, d))
