@@ -205,6 +205,7 @@ def workspace_size(B, H, T, dk, dv, dtype=torch.bfloat16, phi=False, normalize=F
 def state_init(S: torch.Tensor, z: torch.Tensor | None = None, stream=None):
     """Zero S [B,H,dk,dv] (and z [B,H,dk]) on the device."""
     B, H, dk, dv = S.shape
+    _states(B, H, dk, dv, S.device, S=S, z=z)
     _check(_load().la_state_init(_ptr(S), _ptr(z), B, H, dk, dv, _stream(stream)),
            "la_state_init")
 

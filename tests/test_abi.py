@@ -322,6 +322,10 @@ def test_python_binding_checks_caller_buffers():
         la.chunk_bwd(q, q, q, q, [0.5], dS_T=torch.zeros(B, H, d))
     with pytest.raises(ValueError, match="log_a must be"):
         la.chunk_bwd(q, q, q, q, log_a=torch.zeros(B, H, T - 1))
+    with pytest.raises(ValueError, match="z holds"):
+        la.state_init(torch.zeros(B, H, d, d), torch.zeros(B, H, d - 1))
+    with pytest.raises(TypeError, match="S must be"):
+        la.state_init(torch.zeros(B, H, d, d, dtype=torch.bfloat16))
     # buffers of the right size still fail only on being host memory
     with pytest.raises(ValueError, match="CUDA device tensors"):
         la.chunk_fwd(q, q, q, [0.5], out=torch.empty_like(q), S_out=torch.empty(B, H, d, d))
