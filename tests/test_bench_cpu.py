@@ -4,7 +4,8 @@ The algorithmic bytes are checked against the sizes of the tensors the workload
 generator actually makes (inputs read once, outputs and final states written
 once), the useful flops against the page's count with the feature width the
 method uses (273 features for the Taylor map), and the workload descriptions
-against the configurations.
+against the configurations.  The clock record (median under load, throttle
+reasons) and the choice of roofline peaks are checked on fake inputs.
 """
 import os
 import sys
