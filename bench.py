@@ -3,10 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One JSON line on rank 0.  A "step" is one chunkwise forward (la_chunk_fwd)
-over the headline workload: causal linear attention, B=4, H=8, T=4096,
-d_k=d_v=64, bf16 inputs, phi = elu+1, normalised.  The same line carries
-sub-measurements of the other workloads (multi-scale retention prefill,
-long-sequence prefill, the recurrent decode step), each timed the same way.
+over the headline workload, the largest that fits one GPU: RetNet multi-scale
+retention, B=8, H=16, T=8192, d_k=128, d_v=256, bf16 inputs, gamma_h =
+1 - 2^(-5-h), no feature map, no normaliser.  The same line carries
+sub-measurements of the other workloads (normalised linear attention, long
+sequences, the floored normaliser, per-token decay, the Taylor feature map,
+the backward pass and the recurrent decode step), each timed the same way.
 
 Timing: CUDA events on the launching stream; W untimed warm-up steps; the K
 timed steps cycle through enough input copies that their footprint exceeds
@@ -39,19 +41,21 @@ import workloads  # noqa: E402
 METRIC = ("retention fwd tokens/s & TFLOP/s (% bf16 TC peak); decode steps/s & HBM GB/s")
 
 # DRAM bytes (read + write) per launch of the headline's dominant kernel, from
-# the ncu capture summarised in profiles/chunk_tc_ws_kernel_linear_attention_bf16.md.
-# It holds only for the kernel sources that capture measured (their SHA-256
-# below); any later change to them makes the reported traffic null until the
-# kernel is captured again.
+# an ncu capture of that kernel on the headline workload (its summary sits under
+# profiles/, named for the kernel and workload).  It holds only for the kernel
+# sources that capture measured (their SHA-256 below); any later change to them
+# makes the reported traffic null until the kernel is captured again.
 KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "tc_ptx.cuh",
                   "chunk_tc.cu", "common.cuh", "launch.h")
 TRAFFIC = {
-    "chunk_tc_ws_kernel/full": {
-        "bytes": 52_004_352 + 258_304,
-        "sources_sha256": "5a67b81656af89f519c876819897b15768328fea277a8ddad0b8e36824a9f500",
-    },
+    # (workload, kernel): bytes per launch
 }
-HEADLINE = "linear_attention_bf16"
+HEADLINE = "msr_retention_bf16"
+# the prefill workloads timed beside the headline
+SUB_PREFILL = ("linear_attention_bf16", "long_retention_bf16", "retention_floor_bf16",
+               "gated_retention_bf16", "taylor_linear_attention_bf16")
+# the backward pass on the CUDA cores: normalised linear attention with phi
+BWD_SIMT = "linear_attention_bf16"
 # the backward pass on the tensor cores: plain retention, d_k = d_v = 128
 BWD_TC = "long_retention_bf16"
 # the second-order Taylor feature map (273 features from d = 16)
@@ -121,8 +125,8 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(kernel: str) -> int | None:
-    t = TRAFFIC.get(kernel)
+def measured_traffic(workload: str, kernel: str) -> int | None:
+    t = TRAFFIC.get((workload, kernel))
     if t is None or t["sources_sha256"] != kernel_sources_sha256():
         return None
     return t["bytes"]
@@ -239,8 +243,10 @@ def kernel_breakdown(la, fn, steps: int, stream) -> dict:
 
 
 def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: int,
-                    e2e: bool = False) -> dict:
+                    e2e: bool = False, batch: int | None = None) -> dict:
     c = dict(workloads.CONFIGS[name])
+    if batch:
+        c["B"] = batch
     B = c["B"]
     pairs = workloads.shard_pairs(rank, world, B, c["H"])
     cw = dict(c)
@@ -297,7 +303,7 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
         zh = torch.empty(B, c["H"], c["dk"], pin_memory=True) if c["normalize"] else None
 
         def step_host(times):
-            la.chunk_fwd_host(qh, kh, vh, gamma, phi=c["phi"], normalize=c["normalize"],
+            la.chunk_fwd_host(qh, kh, vh, gamma, phi=c["phi"], normalize=c["normalize"], pieces=B,
                               out=Oh, S_out=Sh, z_out=zh, timing=times)
 
         for _ in range(warmup):
@@ -464,15 +470,14 @@ def run_ours(args) -> dict | None:
                               "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
         return None
     if only in ("backward", "backward_" + BWD_TC):  # profiling aid: one backward pass alone
-        r = bwd_measure(la, HEADLINE if only == "backward" else BWD_TC, args.steps, args.warmup,
+        r = bwd_measure(la, BWD_SIMT if only == "backward" else BWD_TC, args.steps, args.warmup,
                         rank, world)
         if rank == 0:
             print(json.dumps({"only": only, "ms": r["ms"],
                               "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
         return None
-    if only in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
-                "gated_retention_bf16", TAYLOR):  # profiling aid
-        r = prefill_measure(la, only, args.steps, args.warmup, rank, world)
+    if only in (HEADLINE,) + SUB_PREFILL:  # profiling aid: one prefill workload alone
+        r = prefill_measure(la, only, args.steps, args.warmup, rank, world, batch=args.batch)
         if rank == 0:
             print(json.dumps({"only": only, "ms_per_step": r["ms"],
                               "alg_gbs": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9}))
@@ -487,15 +492,14 @@ def run_ours(args) -> dict | None:
     others = {}
     headline_only = args.headline_only or only == "headline"
     if not headline_only:
-        for name in ("msr_retention_bf16", "long_retention_bf16", "retention_floor_bf16",
-                     "gated_retention_bf16", TAYLOR):
+        for name in SUB_PREFILL:
             r = prefill_measure(la, name, max(3, args.steps // 2), args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             others[name] = r
         dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         dec["ms"] = max_over_ranks(dec["ms"])
         bwds = {}
-        for name in (HEADLINE, BWD_TC):
+        for name in (BWD_SIMT, BWD_TC):
             r = bwd_measure(la, name, 3, args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             bwds[name] = r
@@ -539,7 +543,7 @@ def run_ours(args) -> dict | None:
             "peak": pk["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved_gbs / pk["hbm_gbs"],
-            "traffic": measured_traffic(dom_name),
+            "traffic": measured_traffic(HEADLINE, dom_name),
             "kernel": dom_name,
             "kernel_avg_ms": dom["avg_ms"],
             "peak_source": pk["source"],
@@ -650,11 +654,12 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("headline", "msr_retention_bf16", "long_retention_bf16",
-                                       "retention_floor_bf16", "gated_retention_bf16", "decode",
-                                       "backward", "backward_long_retention_bf16", TAYLOR),
+    ap.add_argument("--only", choices=("headline", HEADLINE) + SUB_PREFILL +
+                    ("decode", "backward", "backward_" + BWD_TC),
                     default=None,
                     help="profiling aid: run one workload only")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling aid (with --only and a prefill workload): a smaller batch B")
     ap.add_argument("--decode-steps", type=int,
                     default=workloads.CONFIGS["decode_bf16"]["decode_steps"],
                     help="decode steps to time (the workload has 1024)")

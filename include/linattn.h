@@ -330,6 +330,32 @@ LA_API la_status la_chunk_fwd_noalloc(const void* Q, const void* K, const void* 
                                       int* dev_status, la_stream_t stream);
 
 /*
+ * Test and diagnostic switches (no counterpart on the pages).  Process-wide,
+ * all 0 by default; they steer no call unless a test sets them.
+ *
+ *   LA_OPT_PATH           0: automatic path choice.  1: la_chunk_fwd and
+ *                         la_chunk_bwd run on the fp32 CUDA-core kernels
+ *                         (la_workspace_size and la_bwd_workspace_size answer
+ *                         for that path).  2: la_chunk_fwd runs on the
+ *                         tensor-core kernels or answers LA_ERR_UNSUPPORTED.
+ *   LA_OPT_TC_LOCKSTEP    1: the tensor-core forward uses its lockstep kernel
+ *                         where it would use the pipelined one.
+ *   LA_OPT_FORCE_TIMEOUT  1: the tensor-core forward kernels first wait 1 ms on
+ *                         a barrier nothing arrives on, then record
+ *                         LA_ERR_TIMEOUT in dev_status and return without
+ *                         computing (the device status path, exercised with
+ *                         neither a hang nor a fault).
+ *
+ * Returns the option's previous value, or -1 (nothing changed) for an unknown
+ * option or an out-of-range value.  Set a switch before enqueuing the calls it
+ * should affect; it is read when a call is made, not when its kernels run.
+ */
+#define LA_OPT_PATH 1
+#define LA_OPT_TC_LOCKSTEP 2
+#define LA_OPT_FORCE_TIMEOUT 3
+LA_API int la_debug_set(int option, int value);
+
+/*
  * Launch tracing (profiling aid; no counterpart on the pages).  While enabled,
  * the library records a pair of CUDA events on the launching stream around
  * every kernel it enqueues, for up to `capacity` launches (capacity <= 0

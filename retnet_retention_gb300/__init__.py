@@ -28,6 +28,7 @@ from . import _build
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
 LA_PHI_ELU1, LA_NORMALIZE, LA_NONCAUSAL, LA_NORM_FLOOR, LA_GATED, LA_PHI_TAYLOR = 1, 2, 4, 8, 16, 32
+LA_OPT_PATH, LA_OPT_TC_LOCKSTEP, LA_OPT_FORCE_TIMEOUT = 1, 2, 3
 
 LIBRARY_PATH = _build.LIBRARY
 _LIB = None
@@ -95,6 +96,8 @@ def _load() -> ctypes.CDLL:
     lib.la_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
                                          vp, i, vp, vp]
     lib.la_chunk_fwd_noalloc.restype = i
+    lib.la_debug_set.argtypes = [i, i]
+    lib.la_debug_set.restype = i
     lib.la_trace_enable.argtypes = [i]
     lib.la_trace_enable.restype = i
     lib.la_trace_collect.argtypes = [ctypes.POINTER(TraceRecord), i]
@@ -106,6 +109,44 @@ def _load() -> ctypes.CDLL:
 def library() -> ctypes.CDLL:
     """The loaded liblinattn.so (raises if it is not built)."""
     return _load()
+
+
+_PATHS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+def debug_set(option: int, value: int) -> int:
+    """la_debug_set: set a test / diagnostic switch, return its previous value."""
+    prev = int(_load().la_debug_set(int(option), int(value)))
+    if prev < 0:
+        raise ValueError(f"la_debug_set: bad option {option} or value {value}")
+    return prev
+
+
+class debug_options:
+    """Context manager over la_debug_set's switches, restoring them on exit:
+    path ("auto", "simt": CUDA cores, "tc": tensor cores), lockstep (the
+    tensor-core forward's lockstep kernel), force_timeout (the kernels' forced
+    1 ms wait and LA_ERR_TIMEOUT status)."""
+
+    def __init__(self, path: str | None = None, lockstep: bool | None = None,
+                 force_timeout: bool | None = None):
+        self._set = []
+        if path is not None:
+            self._set.append((LA_OPT_PATH, _PATHS[path]))
+        if lockstep is not None:
+            self._set.append((LA_OPT_TC_LOCKSTEP, int(bool(lockstep))))
+        if force_timeout is not None:
+            self._set.append((LA_OPT_FORCE_TIMEOUT, int(bool(force_timeout))))
+        self._prev = []
+
+    def __enter__(self):
+        self._prev = [(o, debug_set(o, v)) for o, v in self._set]
+        return self
+
+    def __exit__(self, *exc):
+        for o, v in reversed(self._prev):
+            debug_set(o, v)
+        return False
 
 
 def status_string(status: int) -> str:
@@ -165,6 +206,24 @@ def _buffer(t, name: str, numel: int, dtype, device):
         raise ValueError(f"{name} is on {t.device}; the inputs are on {device}")
     if t.numel() < numel:
         raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+
+
+def _inputs(dev, **ts):
+    """Every input tensor on the device of the first (the library sees addresses only)."""
+    for name, t in ts.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}; the inputs are on {dev}")
+
+
+def _workspace(ws, need: int, dev) -> int:
+    """Check a caller-supplied workspace (uint8, contiguous, on dev, >= need bytes);
+    returns its size in bytes."""
+    if ws is None:
+        return 0
+    _buffer(ws, "workspace", need, torch.uint8, dev)
+    if not ws.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return ws.numel()
 
 
 def _states(B: int, H: int, ds: int, dv: int, device, **bufs):
@@ -232,6 +291,7 @@ def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, e
         raise TypeError("q, k, v must share one dtype")
     dt = _dtype_code(q)
     dev = q.device
+    _inputs(dev, k=k, v=v)
     if out is None:
         out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
     ds = state_rows(dk, phi)
@@ -249,25 +309,33 @@ def chunk_fwd(q, k, v, gamma=None, *, phi=False, normalize=False, causal=True, e
     _buffer(dev_status, "dev_status", 1, torch.int32, dev)
     flags = _flags(phi, normalize, causal, floor)
     lib = _load()
-    need = int(lib.la_workspace_size(B, H, T, dk, dv, dt,
-                                     flags | (LA_GATED if log_a is not None else 0), chunk))
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if log_a is None:
-        g = _gamma_host(gamma, H)
-        st = lib.la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), dt, g.ctypes.data, B, H, T, dk, dv,
-                              flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out),
-                              _ptr(z_out), int(chunk), _ptr(workspace), ws_bytes,
-                              _ptr(dev_status), _stream(stream))
-        _check(st, "la_chunk_fwd")
-    else:
-        st = lib.la_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(log_a), B, H, T, dk, dv,
-                                    flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out),
-                                    _ptr(S_out), _ptr(z_out), int(chunk), _ptr(workspace),
-                                    ws_bytes, _ptr(dev_status), _stream(stream))
-        _check(st, "la_chunk_fwd_gated")
+    with _current(dev):  # the plan (SM count) and the launches are the current device's
+        need = int(lib.la_workspace_size(B, H, T, dk, dv, dt,
+                                         flags | (LA_GATED if log_a is not None else 0), chunk))
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = _workspace(workspace, need, dev)
+        if log_a is None:
+            g = _gamma_host(gamma, H)
+            st = lib.la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), dt, g.ctypes.data, B, H, T, dk, dv,
+                                  flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out),
+                                  _ptr(z_out), int(chunk), _ptr(workspace), ws_bytes,
+                                  _ptr(dev_status), _stream(stream))
+            _check(st, "la_chunk_fwd")
+        else:
+            st = lib.la_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(log_a), B, H, T, dk,
+                                        dv, flags, float(eps), _ptr(S0), _ptr(z0), _ptr(out),
+                                        _ptr(S_out), _ptr(z_out), int(chunk), _ptr(workspace),
+                                        ws_bytes, _ptr(dev_status), _stream(stream))
+            _check(st, "la_chunk_fwd_gated")
     return out, S_out, z_out
+
+
+def _current(dev):
+    """The library plans and launches on the current device: make the tensors' current."""
+    if dev.type != "cuda":
+        raise ValueError("liblinattn takes CUDA device tensors (use chunk_fwd_host for host data)")
+    return torch.cuda.device(dev)
 
 
 def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
@@ -284,14 +352,17 @@ def chunk_fwd_noalloc(q, k, v, gamma, *, phi=False, normalize=False, causal=True
         raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
+    _inputs(q.device, k=k, v=v)
     _buffer(out, "out", B * H * T * dv, q.dtype, q.device)
     _states(B, H, state_rows(dk, phi), dv, q.device, S0=S0, z0=z0, S_out=S_out, z_out=z_out)
     _buffer(dev_status, "dev_status", 1, torch.int32, q.device)
     g = _gamma_host(gamma, H)
-    st = _load().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data, B,
-                                      H, T, dk, dv, _flags(phi, normalize, causal, floor), float(eps),
-                                      _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out), _ptr(z_out),
-                                      int(chunk), _ptr(dev_status), _stream(stream))
+    with _current(q.device):  # the scratch array and the plan are the current device's
+        st = _load().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data,
+                                          B, H, T, dk, dv, _flags(phi, normalize, causal, floor),
+                                          float(eps), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_out),
+                                          _ptr(z_out), int(chunk), _ptr(dev_status),
+                                          _stream(stream))
     _check(st, "la_chunk_fwd_noalloc")
     return out, S_out, z_out
 
@@ -307,6 +378,7 @@ def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps
         raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
+    _inputs(q.device, k=k, v=v)
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     if (gamma is None) == (log_a is None):
@@ -316,20 +388,21 @@ def recurrent_step(q, k, v, gamma, S, z=None, *, phi=False, normalize=False, eps
     _buffer(dev_status, "dev_status", 1, torch.int32, q.device)
     _buffer(log_a, "log_a", B * H, torch.float32, q.device)
     flags = _flags(phi, normalize, True, floor)
-    if log_a is None:
-        g = _gamma_host(gamma, H)
-        st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), g.ctypes.data,
-                                       B, H, dk, dv, flags, float(eps), _ptr(S), _ptr(z),
-                                       _ptr(out), _ptr(dev_status), _stream(stream))
-        _check(st, "la_recurrent_step")
-    else:
-        if log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H):
-            raise ValueError(f"log_a must be float32 [B,H] = {(B, H)}")
-        st = _load().la_recurrent_step_gated(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
-                                             _ptr(log_a), B, H, dk, dv, flags, float(eps),
-                                             _ptr(S), _ptr(z), _ptr(out), _ptr(dev_status),
-                                             _stream(stream))
-        _check(st, "la_recurrent_step_gated")
+    if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H)):
+        raise ValueError(f"log_a must be float32 [B,H] = {(B, H)}")
+    with _current(q.device):
+        if log_a is None:
+            g = _gamma_host(gamma, H)
+            st = _load().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
+                                           g.ctypes.data, B, H, dk, dv, flags, float(eps), _ptr(S),
+                                           _ptr(z), _ptr(out), _ptr(dev_status), _stream(stream))
+            _check(st, "la_recurrent_step")
+        else:
+            st = _load().la_recurrent_step_gated(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
+                                                 _ptr(log_a), B, H, dk, dv, flags, float(eps),
+                                                 _ptr(S), _ptr(z), _ptr(out), _ptr(dev_status),
+                                                 _stream(stream))
+            _check(st, "la_recurrent_step_gated")
     return out
 
 
@@ -352,6 +425,7 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
         raise ValueError("pass exactly one of gamma and log_a")
     dt = _dtype_code(q)
     dev = q.device
+    _inputs(dev, k=k, v=v, dO=dO)
     if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
         raise ValueError(f"log_a must be float32 [B,H,T] = {(B, H, T)}")
     _buffer(log_a, "log_a", B * H * T, torch.float32, dev)
@@ -367,19 +441,20 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
            if state_grads and normalize else None)
     flags = _flags(phi, normalize, True, floor)
     lib = _load()
-    need = int(lib.la_bwd_workspace_size(B, H, T, dk_, dv_, dt, flags))
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(dO), dt)
-    rest = (B, H, T, dk_, dv_, flags, float(eps), _ptr(S0), _ptr(z0), _ptr(dS_T), _ptr(dz_T),
-            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes,
-            None, _stream(stream))
-    if log_a is None:
-        g = _gamma_host(gamma, H)
-        _check(lib.la_chunk_bwd(*args, g.ctypes.data, *rest), "la_chunk_bwd")
-    else:
-        _check(lib.la_chunk_bwd_gated(*args, _ptr(log_a), *rest), "la_chunk_bwd_gated")
+    with _current(dev):
+        need = int(lib.la_bwd_workspace_size(B, H, T, dk_, dv_, dt, flags))
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = _workspace(workspace, need, dev)
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(dO), dt)
+        rest = (B, H, T, dk_, dv_, flags, float(eps), _ptr(S0), _ptr(z0), _ptr(dS_T), _ptr(dz_T),
+                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes,
+                None, _stream(stream))
+        if log_a is None:
+            g = _gamma_host(gamma, H)
+            _check(lib.la_chunk_bwd(*args, g.ctypes.data, *rest), "la_chunk_bwd")
+        else:
+            _check(lib.la_chunk_bwd_gated(*args, _ptr(log_a), *rest), "la_chunk_bwd_gated")
     return dq, dk, dv, dS0, dz0
 
 
@@ -466,6 +541,6 @@ def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, e
 
 
 __all__ = ["chunk_fwd", "chunk_bwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
-           "trace_enable", "trace_collect",
+           "trace_enable", "trace_collect", "debug_set", "debug_options",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
            "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR", "state_rows"]

@@ -1,14 +1,25 @@
 // The exported C ABI of liblinattn.so (declared in include/linattn.h):
 // argument checks on the host, then asynchronous launches on the caller's
 // stream.  Nothing is launched or written when a check fails.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 
 #include "launch.h"
 
 using namespace la;
+
+namespace {
+// la_debug_set's switches (indexed by LA_OPT_*)
+std::atomic<int> g_opt[4] = {};
+}  // namespace
+
+namespace la {
+int opt_path() { return g_opt[LA_OPT_PATH].load(std::memory_order_relaxed); }
+bool opt_tc_lockstep() { return g_opt[LA_OPT_TC_LOCKSTEP].load(std::memory_order_relaxed) != 0; }
+bool opt_force_timeout() { return g_opt[LA_OPT_FORCE_TIMEOUT].load(std::memory_order_relaxed) != 0; }
+}  // namespace la
 
 namespace {
 
@@ -68,13 +79,10 @@ bool plan_ok(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned fla
            !(flags & ~(kCallFlags | LA_GATED | LA_PHI_TAYLOR));
 }
 
-bool simt_pinned() {
-    const char* pin = std::getenv("LA_CHUNK_PATH");
-    return pin && std::strcmp(pin, "simt") == 0;
-}
+bool simt_pinned() { return opt_path() == 1; }
 
 // The backward pass's path: the tensor cores (three forward passes) where they
-// apply, unless LA_CHUNK_PATH=simt pins the CUDA-core kernel.
+// apply, unless LA_OPT_PATH pins the CUDA-core kernel.
 BwdArgs bwd_plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
                       bool gated) {
     BwdArgs a;
@@ -110,6 +118,12 @@ const char* la_status_string(int status) {
 }
 
 int la_abi_version(void) { return LA_ABI_VERSION; }
+
+int la_debug_set(int option, int value) {
+    const int hi = option == LA_OPT_PATH ? 2 : 1;
+    if (option < LA_OPT_PATH || option > LA_OPT_FORCE_TIMEOUT || value < 0 || value > hi) return -1;
+    return g_opt[option].exchange(value);
+}
 
 size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
                          int chunk) {
@@ -219,11 +233,10 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.dev_status = dev_status;
-    // LA_CHUNK_PATH=simt|tc pins the path (tests compare both); default: tensor
-    // cores whenever the shape allows, the fp32 CUDA-core kernel otherwise.
-    const char* pin = std::getenv("LA_CHUNK_PATH");
-    const bool want_simt = pin && std::strcmp(pin, "simt") == 0;
-    const bool want_tc = pin && std::strcmp(pin, "tc") == 0;
+    // LA_OPT_PATH pins the path (tests compare both); default: tensor cores
+    // whenever the shape allows, the fp32 CUDA-core kernel otherwise.
+    const bool want_simt = opt_path() == 1;
+    const bool want_tc = opt_path() == 2;
     if (taylor) {  // its own tensor-core kernel; no CUDA-core version
         if (want_simt || !taylor_supported(a)) return LA_ERR_UNSUPPORTED;
         return cuda_status(launch_chunk_taylor(a, g, s));

@@ -715,8 +715,7 @@ cudaError_t launch_chunk_taylor(const ChunkArgs& a, const KernelGammas& g, cudaS
     prm.eps = a.eps;
     prm.dev_status = a.dev_status;
     prm.wait_ns = 2000000000ull;
-    const char* ft = std::getenv("LA_DEBUG_FORCE_TIMEOUT");
-    if (ft && ft[0] == '1') {
+    if (opt_force_timeout()) {
         prm.force_timeout = 1;
         prm.wait_ns = 1000000ull;  // 1 ms
     }

@@ -39,6 +39,7 @@
 // records LA_ERR_TIMEOUT in dev_status, stops issuing work, frees its tensor
 // memory and returns.
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -785,12 +786,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     prm.eps = a.eps;
     prm.dev_status = a.dev_status;
     prm.wait_ns = 2000000000ull;
-    const char* ft = std::getenv("LA_DEBUG_FORCE_TIMEOUT");
-    if (ft && ft[0] == '1') {
+    if (opt_force_timeout()) {
         prm.force_timeout = 1;
         prm.wait_ns = 1000000ull;  // 1 ms
     }
     prm.g = g;
+    prm.o_align32 = (reinterpret_cast<uintptr_t>(a.O) & 31u) == 0;
+    prm.fact = !a.log_a && !a.phi && !prm.track_z;
+    for (int h = 0; h < a.H && prm.fact; ++h)
+        prm.fact = g.gamma[h] < 1.f && g.log2g[h] * (float)(kC - 1) >= -64.f;
     const int n_chunks = pl.n_chunks;
     const int units = pl.units;
     *launches = 0;

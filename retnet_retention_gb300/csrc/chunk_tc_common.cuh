@@ -54,6 +54,10 @@ struct TcParams {
     int* dev_status;
     unsigned long long wait_ns;
     int force_timeout;
+    // every head's gamma < 1 with gamma^(C-1) >= 2^-64, no feature map, no normaliser,
+    // z not carried: the pipelined kernel's factored-decay build
+    int fact;
+    int o_align32;  // O's base is 32-byte aligned (rows and column blocks then are too)
     KernelGammas g;
 };
 
@@ -237,6 +241,56 @@ __device__ __forceinline__ void scale_rows_zsum(char* tile, F fac, float* part, 
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
+}
+
+// A factor f as a pair of bf16x2 words (both halves equal): h = bf16(f) and
+// l = bf16(f - h), for scale_rows_hl.
+__device__ __forceinline__ void split_bf16x2(float f, uint32_t& h, uint32_t& l) {
+    const __nv_bfloat16 fh = __float2bfloat16_rn(f);
+    const __nv_bfloat16 fl = __float2bfloat16_rn(f - __bfloat162float(fh));
+    const uint32_t uh = __bfloat16_as_ushort(fh), ul = __bfloat16_as_ushort(fl);
+    h = uh | (uh << 16);
+    l = ul | (ul << 16);
+}
+
+// Row r of a [128 x 64*NBLK] K-major swizzled bf16 tile times its factor, in
+// place, by exactly NTHR threads, in packed bf16 arithmetic: each element x
+// becomes fma(x, h, bf16(x l)) with the factor split as h + l (split_bf16x2),
+// one rounding of a sum within about 2^-17 (relative) of x f: the fp32 product
+// rounded to bf16 but for near-ties, at eight instructions per 16-byte piece
+// instead of about twenty.  Thread t holds piece t & 7 of rows
+// (t >> 3) + (NTHR / 8) m, m < 1024 / NTHR, of every block (a row is one
+// 128-byte line, so the swizzle keeps pieces in their row); h[m], l[m] are that
+// row's factor.  Eight pieces are loaded before any is computed.
+template <int NBLK, int NTHR>
+__device__ __forceinline__ void scale_rows_hl(char* tile, const uint32_t (&h)[1024 / NTHR],
+                                              const uint32_t (&l)[1024 / NTHR], int t) {
+    static_assert(NTHR % 8 == 0 && 1024 % NTHR == 0, "thread count");
+    constexpr int R = 1024 / NTHR;
+    constexpr int kB = R < 8 ? R : 8;
+    uint4* base = reinterpret_cast<uint4*>(tile) + t;
+#pragma unroll
+    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+        for (int m0 = 0; m0 < R; m0 += kB) {
+            uint4 u[kB];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) u[j] = base[b * 1024 + (m0 + j) * NTHR];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                uint32_t* x = reinterpret_cast<uint32_t*>(&u[j]);
+                const __nv_bfloat162 hh = *reinterpret_cast<const __nv_bfloat162*>(&h[m0 + j]);
+                const __nv_bfloat162 ll = *reinterpret_cast<const __nv_bfloat162*>(&l[m0 + j]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x[e]);
+                    const __nv_bfloat162 y = __hfma2(v, hh, __hmul2(v, ll));
+                    x[e] = *reinterpret_cast<const uint32_t*>(&y);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kB; ++j) base[b * 1024 + (m0 + j) * NTHR] = u[j];
+        }
 }
 
 // In-place pass over a [128 x 64*nblk] K-major swizzled tile by `nthr`

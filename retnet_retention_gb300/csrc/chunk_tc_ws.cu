@@ -5,8 +5,7 @@
 namespace la {
 
 bool tc_ws_supported(int mode, int dk, int dvb, bool normalize) {
-    const char* pin = std::getenv("LA_TC_KERNEL");
-    if (pin && std::strcmp(pin, "lockstep") == 0) return false;
+    if (opt_tc_lockstep()) return false;
     if (dk != 64 && dk != 128) return false;
     if (dvb != 64 && dvb != 128) return false;
     if (mode == kStateOnly) return true;

@@ -13,17 +13,20 @@
 //               E3 of c and epilogue B have readied S and the tiles (the state
 //               chain), then MMA1 of c+1 into the other of two TMEM score
 //               buffers, then MMA2 of c once E1 has written P (with a single O
-//               buffer: MMA1 of c+1 first, the rest once S and P are ready)
+//               buffer MMA3 also waits for E2 of c-1, and MMA1 of c+1 goes
+//               either last, or first where epilogue B rescales the tiles
+//               after MMA1: then the rest waits for S and P together)
 //   warps 2-9   epilogue A: per chunk, E3 first (bf16 copy of S for MMA3,
 //               S *= gamma^L), then E1 (scores -> decay mask -> bf16 P back into
-//               TMEM); two warps per TMEM lane quarter, each on half of the
-//               columns
+//               TMEM; the other order where MMA1 of c+1 goes first); two warps
+//               per TMEM lane quarter, each on half of the columns
 //   warps 10-13 epilogue B: the entry state, the xi/zeta row scalings, the
 //               z update, and E2 (O of the previous chunk -> global, divided
 //               by the normaliser)
 //   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for
 //               64-wide Q/K and value blocks, else 2), up to a ring's depth
-//               ahead of the tensor work
+//               ahead of the tensor work; in the factored-decay build instead
+//               K *= zeta (see FACT below)
 //
 // so that the state chain (MMA4 of c -> E3 of c+1 -> MMA4 of c+1) waits for
 // nothing but E3 and epilogue B's per-chunk work, and E1, phi and E2 run beside
@@ -113,9 +116,9 @@ constexpr int threads_c(int dk, int dvb, bool phi) { return phi && dk == 64 && d
 constexpr int threads_ws(int dk, int dvb, bool phi) { return 448 + threads_c(dk, dvb, phi); }
 // The block size the compiler budgets registers for: for 64-wide tiles without
 // phi the cap of a 640-thread block (96 registers) measured faster than the
-// 128 that 512 threads would allow.
-constexpr int bound_ws(int dk, int dvb, bool phi) {
-    return !phi && dk == 64 && dvb == 64 ? 640 : threads_ws(dk, dvb, phi);
+// 128 that 512 threads would allow; the factored-decay build (fact) keeps 128.
+constexpr int bound_ws(int dk, int dvb, bool phi, bool fact = false) {
+    return !phi && !fact && dk == 64 && dvb == 64 ? 640 : threads_ws(dk, dvb, phi);
 }
 constexpr int kWgA = 2;   // first warp of epilogue A (8 warps: two per TMEM lane quarter)
 constexpr int kWgB = 10;  // first warp of epilogue B
@@ -183,7 +186,8 @@ struct LayoutWS {
 // o_full / o_empty cannot run ahead.  Per chunk c with two O buffers:
 // sready(c) = the bf16 copy of S and the scaled S and tiles are in place for
 // MMA3/MMA4 (epilogues A and B); pready(c) = P is in TMEM for MMA2 (epilogue A).
-// With one O buffer pready(c) carries both (epilogues A and B).  sdone(c) =
+// With one O buffer and MMA1 of the next chunk issued first, pready(c) carries
+// both (epilogues A and B).  sdone(c) =
 // MMA3/MMA4 of c are complete; in a state walk sdone completes once, after the
 // last MMA4.  A parity wait is sound only while its barrier is at most one phase
 // behind the phase awaited: every wait here is placed so that it is.
@@ -207,8 +211,9 @@ static_assert(kNumBars <= 32, "mbarrier slots");
 // gamma^(i+1) -> 2^(b_i), gamma^(L-1-j) -> 2^(b_(L-1) - b_j), gamma^L ->
 // 2^(b_(L-1)) (b in log2 units), and the score mask's running product steps by
 // a_j instead of gamma.
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED>
-__global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
+__global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    static_assert(!FACT || (!GATED && !PHI && !NORM), "the factored decay is for plain retention");
     constexpr int kThreadsC = threads_c(DK, DVB, PHI);
     constexpr int kThreadsWS = threads_ws(DK, DVB, PHI);
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI, GATED>;
@@ -236,6 +241,32 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
     const float l2g = p.g.log2g[h];
     const float gam = p.g.gamma[h];
     const bool unit_gamma = !GATED && gam == 1.0f;
+    // FACT: factored decay (per-head gamma < 1, no feature map, no normaliser, z not
+    // carried; the host launches this build when every head qualifies).  With
+    // zeta_j = gamma^(L-1-j) taken into K before MMA1 (by the feature-map group,
+    // as the tile lands), the decayed scores are
+    //   P_ij = (q_i . k_j) gamma^(i-j) = gamma^(i+1-L) (q_i . zeta_j k_j),
+    // and the read-out gamma^(i+1) q_i S_{c-1} = gamma^(i+1-L) q_i (gamma^L S_{c-1}),
+    // so the whole output row is gamma^(i+1-L) (P'V + Q gamma^L S_{c-1})_i with
+    // P' = (Q (zeta K)^T) masked to j <= i: E1 only masks, Q is never rescaled,
+    // E3 copies gamma^L S (which MMA4 accumulates onto anyway) and E2 applies the
+    // one per-row factor.  The factor gamma^(i+1-L) reaches gamma^(1-C), so this
+    // form is taken only while gamma^(C-1) >= 2^-64 for every head (every product
+    // stays far inside the float and bf16 ranges); smaller gammas keep the row
+    // scalings.
+    constexpr bool fact = FACT;
+    // Order of the work per chunk with one O buffer.  Where epilogue B rescales the
+    // tiles after MMA1 (gamma < 1 without the factored form, per-token decays),
+    // MMA1 of chunk c+1 goes before the MMAs of chunk c so that E1 and the
+    // rescaling of c+1 overlap them, E1 goes before E3, and S and P hand over
+    // together (kPready).  Otherwise nothing needs that overlap, and waiting for
+    // chunk c+1's tiles first would put their load on every chunk's critical path
+    // (a 96 KB stage, two in the ring): the MMAs of chunk c go first, then MMA1 of
+    // c+1; E3 (released by MMA4 of c) goes before E1 (released by MMA1 of c+1) and
+    // hands S over on its own (kSready), so MMA3 and MMA4 of c+1 run while E1
+    // turns c+1's scores into P.  With two O buffers S and P always hand over apart.
+    const bool mma1_first = Lay::NOB == 1 && !(fact || unit_gamma);
+    const bool e3_first = Lay::NOB == 2 || !mma1_first;  // also: S and P hand over apart
     const int n_chunks = (p.T + kC - 1) / kC;
     const int cb = seg * p.seg_chunks;
     const int ce = min(n_chunks, cb + p.seg_chunks);
@@ -265,12 +296,12 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], 1);
         for (int q = 0; q < NS; ++q) mbar_init(&bar[kEmpty0 + q], 2);  // MMA commit + epilogue B
-        mbar_init(&bar[kSready0], 2);  // epilogue A + epilogue B (two O buffers)
+        mbar_init(&bar[kSready0], 2);  // epilogue A + epilogue B (S and P apart)
         mbar_init(&bar[kSready1], 2);
-        // P ready: epilogue A alone with two O buffers; with one, S and P hand over
-        // together here (epilogue A + epilogue B)
-        mbar_init(&bar[kPready0], NOB == 2 ? 1 : 2);
-        mbar_init(&bar[kPready1], NOB == 2 ? 1 : 2);
+        // P ready: epilogue A alone where S and P hand over apart; else both here
+        // (epilogue A + epilogue B)
+        mbar_init(&bar[kPready0], e3_first ? 1 : 2);
+        mbar_init(&bar[kPready1], e3_first ? 1 : 2);
         // state walk: epilogue B, plus epilogue A when S must be rescaled (gamma < 1)
         for (int q = 0; q < NS; ++q) mbar_init(&bar[kReadyS0 + q], unit_gamma ? 1 : 2);
         *abort_flag = 0;
@@ -445,7 +476,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 const int s = it % NS;
                 const uint32_t par = (it / NS) & 1;
                 if (!mbar_wait_or_abort(&bar[kFull0 + s], par, lim, abort_flag)) return false;
-                if (p.phi && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag)) return false;
+                if ((p.phi || fact) && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag))
+                    return false;
                 fence_after_sync();
                 const uint64_t dq = desc_adv(dQk0, s * Lay::kStage), dk = desc_adv(dq, Lay::kQ);
 #pragma unroll
@@ -479,15 +511,17 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 (void)id_pv;
                 (void)id_qs;
             }
-            // Per chunk, with two O buffers: MMA4/MMA3 as soon as S is ready (the state
+            // Per chunk, with two O buffers: MMA3/MMA4 as soon as S is ready (the state
             // chain), then MMA1 of the next chunk, then MMA2 once P is ready.  With one
-            // O buffer MMA3 must also wait for E2 of the previous chunk, so MMA1 of the
-            // next chunk goes first and MMA4/MMA3/MMA2 follow once S and P are ready.
+            // O buffer MMA3 also waits for E2 of the previous chunk: either MMA1 of the
+            // next chunk goes first and MMA3/MMA4/MMA2 follow once S and P are ready
+            // (mma1_first), or MMA3/MMA4 go once S is ready, MMA2 once P is, and MMA1
+            // of the next chunk last.
             bool ok = !STATE_ONLY && issue_mma1(0);
             for (int it = 0; it < n && ok; ++it) {
                 const int s = it % NS;
-                if (NOB == 1 && it + 1 < n && !(ok = issue_mma1(it + 1))) break;
-                if (!mbar_wait_or_abort(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)], (it >> 1) & 1,
+                if (mma1_first && it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                if (!mbar_wait_or_abort(&bar[(e3_first ? kSready0 : kPready0) + (it & 1)], (it >> 1) & 1,
                                         lim, abort_flag))
                     break;
                 LA_TL(it * 16 + 2);
@@ -515,8 +549,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                     mma_ss(tbase + Lay::kColS, desc_adv(dk, kk * 2048), desc_adv(dv, kk * 2048), id_kv,
                            1u);
                 mma_commit(&bar[kSdone]);
-                if (NOB == 2) {
-                    if (it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                if (NOB == 2 && it + 1 < n && !(ok = issue_mma1(it + 1))) break;
+                if (e3_first) {
                     if (!mbar_wait_or_abort(&bar[kPready0 + (it & 1)], (it >> 1) & 1, lim, abort_flag))
                         break;
                     fence_after_sync();
@@ -529,6 +563,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 mma_commit(&bar[kOfull0 + ob]);
                 mma_commit(&bar[kEmpty0 + s]);
                 LA_TL(it * 16 + 3);
+                if (NOB == 1 && !mma1_first && it + 1 < n && !(ok = issue_mma1(it + 1))) break;
             }
         } else if (warp >= kWgA && warp < kWgB) {
             // ---------------- epilogue A: E1 (P) and E3 (S copies).  Warps kWgA..+3 take
@@ -567,16 +602,17 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
             // Per chunk, E3 (S after MMA3/MMA4 of the previous chunk -> bf16 copy for
             // MMA3, S *= gamma^L before MMA4) and E1 (scores -> P for MMA2).  With two O
             // buffers E3 goes first and hands over on its own (kSready), so the state
-            // chain does not wait for E1 (kPready).  With one, E1 goes first (MMA3 also
-            // waits for E2 of the previous chunk, and E1 overlaps that chunk's MMAs) and
-            // both hand over together (kPready).
+            // chain does not wait for E1 (kPready).  With one, both hand over together
+            // (kPready, after the second of the two); E1 goes first where MMA1 of the
+            // chunk is issued before the previous chunk's MMAs (mma1_first: E1 then
+            // overlaps them), else E3 does.
             for (int it = 0; it < n && !STATE_ONLY; ++it) {
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
                 bool fail = false;
 #pragma unroll
                 for (int step = 0; step < 2; ++step) {
-                    if ((NOB == 2) == (step == 0)) {  // ---- E3
+                    if (e3_first == (step == 0)) {  // ---- E3
                         if (it >= 1 || GATED) {  // MMA3/MMA4 of the previous chunk; the decays
                             bool ok = it < 1 || mbar_wait_or_abort(&bar[kSdone], (it - 1) & 1, lim, abort_flag);
                             if (GATED && ok)
@@ -591,6 +627,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                             uint32_t rs[32];
                             tmem_ld32(tbase + lane_off + Lay::kColS + c0, rs);
                             tmem_ld_wait();
+                            if (fact) {  // MMA3 reads gamma^L S_{c-1}
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                            }
                             if (row < DK) {
 #pragma unroll
                                 for (int e8 = 0; e8 < 32; e8 += 8) {
@@ -605,8 +645,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                                 }
                             }
                             if (!unit_gamma) {
+                                if (!fact) {
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                                    for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                                }
                                 tmem_st32(tbase + lane_off + Lay::kColS + c0, rs);
                             }
                         }
@@ -614,7 +656,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                         fence_proxy_async_smem();
                         fence_before_sync();
                         named_bar_sync(kBarA, kThreadsA);
-                        if (t == 0) mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
+                        if (t == 0)  // S alone (E3 first), or S and P together (E3 second)
+                            mbar_arrive(&bar[(e3_first ? kSready0 : kPready0) + (it & 1)]);
                         if (t == 0) LA_TL(it * 16 + 7);
                     } else {  // ---- E1
                         bool ok1 = mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
@@ -626,96 +669,133 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                         const uint32_t sc = tbase + lane_off + kColScores + (it & 1) * 128;
                         const int i = row;
                         float rsum = 0.f;  // fp32 row sum of this half's scores (normaliser)
-                        // this half's two 32-column pieces of scores, one at a time.  P (bf16
-                        // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
-                        // piece, so half 1 stores only after half 0 has read that piece (kBarP).
-                        // A warp's 32 rows and a piece's 32 columns are the same 32 x 32 block
-                        // for every lane, so a piece above the diagonal is P = 0 for the whole
-                        // warp (no load; not with phi's 8 warps), and only the piece on the
-                        // diagonal needs the mask j <= i.
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int c0 = 64 * half + 32 * q;
-                            const int pq = c0 >> 5, lq = warp & 3;
-                            // (the skip costs registers the 80-register build does not have)
-                            const bool zero = !PHI && pq > lq;
-                            uint32_t r[32];
-                            if (!zero) {
-                                tmem_ld32(sc + c0, r);
-                                tmem_ld_wait();
-                            }
-                            if (half == 0 && q == 1) {
+                        if constexpr (FACT) {
+                            // the scores need only the causal mask (the decay is in K or is 1):
+                            // both pieces loaded at once, one wait, then packed and stored
+                            const int lq = warp & 3, pa = 2 * half;
+                            const bool za = pa > lq, zb = pa + 1 > lq;  // above the diagonal
+                            uint32_t ra[32], rb[32];
+                            if (!za) tmem_ld32(sc + 32 * pa, ra);
+                            if (!zb) tmem_ld32(sc + 32 * pa + 32, rb);
+                            tmem_ld_wait();
+                            if (t == 0) LA_TL(it * 16 + 15);
+                            if (half == 0) {
                                 fence_before_sync();
                                 named_bar_arrive(kBarP, kThreadsA);
                             }
                             uint32_t pk[16];
-                            if (zero) {
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) pk[e] = 0u;
-                            } else {
-                                // gamma^(i-j) by a running product from the piece's top column down
-                                const int jt = min(i, c0 + 31);
-                                float w = unit_gamma ? 1.f : gamma_pow(l2g, (float)(i - jt));
-                                const bool diag = pq == lq;
-                                if constexpr (GATED) {
-                                    // 2^(b_i - b_j), stepping down a column by a_j (the decay
-                                    // of token j); the per-head code below is kept apart: the
-                                    // two forms of the loop compile differently enough to
-                                    // matter for the 80-register build
-                                    const float* gc = gate_of(it % NS);
-                                    const float* ga = gc + 128;
-                                    w = exp2f(gc[i] - gc[jt]);
-#pragma unroll
-                                    for (int e = 30; e >= 0; e -= 2) {
-                                        float x1 = __uint_as_float(r[e + 1]), x0 = __uint_as_float(r[e]);
-                                        const bool in1 = c0 + e + 1 <= i, in0 = c0 + e <= i;
-                                        x1 = in1 ? x1 * w : 0.f;
-                                        if (in1) w *= ga[c0 + e + 1];
-                                        x0 = in0 ? x0 * w : 0.f;
-                                        if (in0) w *= ga[c0 + e];
-                                        if (kE1Sum) rsum += x1 + x0;
-                                        pk[e >> 1] = pack_bf16x2(x0, x1);
-                                    }
-                                } else if constexpr (!PHI) {  // each pair packed as soon as it is scaled
-#pragma unroll
-                                    for (int e = 30; e >= 0; e -= 2) {
-                                        float x1 = __uint_as_float(r[e + 1]), x0 = __uint_as_float(r[e]);
-                                        if (!unit_gamma) {
-                                            x1 *= w;
-                                            if (!diag || c0 + e + 1 <= i) w *= gam;
-                                            x0 *= w;
-                                            if (!diag || c0 + e <= i) w *= gam;
-                                        }
-                                        if (diag) {
-                                            x1 = c0 + e + 1 <= i ? x1 : 0.f;
-                                            x0 = c0 + e <= i ? x0 : 0.f;
-                                        }
-                                        if (kE1Sum) rsum += x1 + x0;
-                                        pk[e >> 1] = pack_bf16x2(x0, x1);
-                                    }
-                                } else {  // (the form that fits 80 registers)
-                                    float a[32];
-#pragma unroll
-                                    for (int e = 31; e >= 0; --e) {
-                                        float x = 0.f;
-                                        if (c0 + e <= i) {
-                                            x = __uint_as_float(r[e]);
-                                            if (!unit_gamma) {
-                                                x *= w;
-                                                w *= gam;
-                                            }
-                                        }
-                                        a[e] = x;
-                                    }
-#pragma unroll
-                                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
-                                }
+                            for (int e = 0; e < 32; e += 2) {
+                                const int j = 32 * pa + e;
+                                pk[e >> 1] = za ? 0u
+                                                : pack_bf16x2(j <= i ? __uint_as_float(ra[e]) : 0.f,
+                                                              j + 1 <= i ? __uint_as_float(ra[e + 1]) : 0.f);
                             }
-                            if (half == 1 && q == 0) {
+                            if (half == 1) {
                                 named_bar_sync(kBarP, kThreadsA);
                                 fence_after_sync();
                             }
-                            tmem_st16(sc + (c0 >> 1), pk);
+                            tmem_st16(sc + 16 * pa, pk);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int j = 32 * pa + 32 + e;
+                                pk[e >> 1] = zb ? 0u
+                                                : pack_bf16x2(j <= i ? __uint_as_float(rb[e]) : 0.f,
+                                                              j + 1 <= i ? __uint_as_float(rb[e + 1]) : 0.f);
+                            }
+                            tmem_st16(sc + 16 * pa + 16, pk);
+                        } else {
+                            // this half's two 32-column pieces of scores, one at a time.  P (bf16
+                            // pairs) goes to columns [0, 64): half 1's P lands on half 0's second
+                            // piece, so half 1 stores only after half 0 has read that piece (kBarP).
+                            // A warp's 32 rows and a piece's 32 columns are the same 32 x 32 block
+                            // for every lane, so a piece above the diagonal is P = 0 for the whole
+                            // warp (no load; not with phi's 8 warps), and only the piece on the
+                            // diagonal needs the mask j <= i.
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const int c0 = 64 * half + 32 * q;
+                                const int pq = c0 >> 5, lq = warp & 3;
+                                // (the skip costs registers the 80-register build does not have)
+                                const bool zero = !PHI && pq > lq;
+                                uint32_t r[32];
+                                if (!zero) {
+                                    tmem_ld32(sc + c0, r);
+                                    tmem_ld_wait();
+                                }
+                                if (half == 0 && q == 1) {
+                                    fence_before_sync();
+                                    named_bar_arrive(kBarP, kThreadsA);
+                                }
+                                uint32_t pk[16];
+                                if (zero) {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                                } else {
+                                    // gamma^(i-j) by a running product from the piece's top column down
+                                    const int jt = min(i, c0 + 31);
+                                    float w = unit_gamma || fact ? 1.f : gamma_pow(l2g, (float)(i - jt));
+                                    const bool diag = pq == lq;
+                                    if constexpr (GATED) {
+                                        // 2^(b_i - b_j), stepping down a column by a_j (the decay
+                                        // of token j); the per-head code below is kept apart: the
+                                        // two forms of the loop compile differently enough to
+                                        // matter for the 80-register build
+                                        const float* gc = gate_of(it % NS);
+                                        const float* ga = gc + 128;
+                                        w = exp2f(gc[i] - gc[jt]);
+#pragma unroll
+                                        for (int e = 30; e >= 0; e -= 2) {
+                                            float x1 = __uint_as_float(r[e + 1]), x0 = __uint_as_float(r[e]);
+                                            const bool in1 = c0 + e + 1 <= i, in0 = c0 + e <= i;
+                                            x1 = in1 ? x1 * w : 0.f;
+                                            if (in1) w *= ga[c0 + e + 1];
+                                            x0 = in0 ? x0 * w : 0.f;
+                                            if (in0) w *= ga[c0 + e];
+                                            if (kE1Sum) rsum += x1 + x0;
+                                            pk[e >> 1] = pack_bf16x2(x0, x1);
+                                        }
+                                    } else if constexpr (!PHI) {  // each pair packed as soon as it is scaled
+#pragma unroll
+                                        for (int e = 30; e >= 0; e -= 2) {
+                                            float x1 = __uint_as_float(r[e + 1]), x0 = __uint_as_float(r[e]);
+                                            if (!unit_gamma && !fact) {
+                                                x1 *= w;
+                                                if (!diag || c0 + e + 1 <= i) w *= gam;
+                                                x0 *= w;
+                                                if (!diag || c0 + e <= i) w *= gam;
+                                            }
+                                            if (diag) {
+                                                x1 = c0 + e + 1 <= i ? x1 : 0.f;
+                                                x0 = c0 + e <= i ? x0 : 0.f;
+                                            }
+                                            if (kE1Sum) rsum += x1 + x0;
+                                            pk[e >> 1] = pack_bf16x2(x0, x1);
+                                        }
+                                    } else {  // (the form that fits 80 registers)
+                                        float a[32];
+#pragma unroll
+                                        for (int e = 31; e >= 0; --e) {
+                                            float x = 0.f;
+                                            if (c0 + e <= i) {
+                                                x = __uint_as_float(r[e]);
+                                                if (!unit_gamma) {
+                                                    x *= w;
+                                                    w *= gam;
+                                                }
+                                            }
+                                            a[e] = x;
+                                        }
+#pragma unroll
+                                        for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(a[e], a[e + 1]);
+                                    }
+                                }
+                                if (half == 1 && q == 0) {
+                                    named_bar_sync(kBarP, kThreadsA);
+                                    fence_after_sync();
+                                }
+                                tmem_st16(sc + (c0 >> 1), pk);
+                            }
                         }
                         // the row sums before rounding P: with signed features the
                         // denominator can be a small difference of large sums, which the
@@ -724,7 +804,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                         // which the issuer starts only after E2 of c has freed c's O buffer)
                         if (kE1Sum) rsb[(it % 3) * 256 + half * 128 + row] = rsum;
                         tmem_st_wait();
-                        if (NOB == 2) {
+                        if (e3_first) {  // E1 second: P on its own
                             fence_before_sync();
                             named_bar_sync(kBarA, kThreadsA);
                             if (t == 0) {
@@ -739,16 +819,30 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
             }
         } else if (warp >= kWgC) {
             // ---------------- feature map: phi on Q and K (K only for a state walk), rows
-            // past the end zeroed, then release the stage to the issuer (kQk)
+            // past the end zeroed, then release the stage to the issuer (kQk); with the
+            // factored decay instead K *= zeta (Q stays as it is)
             const int t = tid - kWgC * 32;
-            for (int it = 0; it < n && p.phi; ++it) {
+            // factored decay: zeta of this thread's rows (t >> 3) + (kThreadsC / 8) m, as
+            // bf16 pairs, for the chunk length zL (recomputed only when it changes)
+            constexpr int kRowsC = 1024 / kThreadsC;
+            uint32_t zh[kRowsC], zl[kRowsC];
+            int zL = -1;
+            for (int it = 0; it < n && (p.phi || fact); ++it) {
                 const int s = it % NS;
                 const int L = min(kC, p.T - (cb + it) * kC);
                 bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
                 if (named_bar_or(kBarC, kThreadsC, !ok)) break;
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
-                if constexpr (STATE_ONLY && kThreadsC % 128 == 0) {  // all loads first
+                if constexpr (FACT) {
+                    if (L != zL) {
+#pragma unroll
+                        for (int m = 0; m < kRowsC; ++m)
+                            split_bf16x2(dec_zeta(nullptr, (t >> 3) + (kThreadsC / 8) * m, L), zh[m], zl[m]);
+                        zL = L;
+                    }
+                    scale_rows_hl<DK / 64, kThreadsC>(st + Lay::kQ, zh, zl, t);
+                } else if constexpr (STATE_ONLY && kThreadsC % 128 == 0) {  // all loads first
                     char* const tiles[1] = {st + Lay::kQ};
                     phi_rows_all<1, DK / 64, kThreadsC>(tiles, L, t);
                 } else if constexpr (STATE_ONLY) {
@@ -813,27 +907,60 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                     }
                     inv = 1.f / norm_den(den, p.normalize, p.eps);
                 }
+                if (fact) inv = gamma_pow(l2g, (float)(row + 1 - L));  // gamma^(i+1-L)
                 const int c = cb + it;
                 __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
-                for (int c0 = 0; c0 < DVB; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(ocol + c0, r);
+                // 64 columns a round in the factored build with 128 registers a thread
+                // (two loads, one wait), else 32.  The O buffer is released once the
+                // last round is in registers; in the factored build the earlier
+                // round's values are packed (bf16) and held until then, so the
+                // release waits for no store.
+                constexpr int kW = FACT && bound_ws(DK, DVB, PHI, FACT) <= 512 ? 2 : 1;  // 32-column loads a round
+                constexpr int kRounds = DVB / (32 * kW);
+                constexpr int kHold = kW == 2 ? kRounds - 1 : 0;  // rounds held packed
+                uint32_t held[kHold > 0 ? kHold : 1][16 * kW];
+                // 16 kW words = 32 kW columns of the row: 32-byte stores where O is
+                // 32-byte aligned (each a whole sector), else 16-byte ones
+                auto store_packed = [&](const uint32_t* pk, int col) {
+                    if (p.o_align32) {
+#pragma unroll
+                        for (int e = 0; e < 16 * kW; e += 8) st_global_v8(orow + col + 2 * e, pk + e);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16 * kW; e += 4)
+                            *reinterpret_cast<uint4*>(orow + col + 2 * e) = make_uint4(pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
+                    }
+                };
+#pragma unroll
+                for (int rd = 0; rd < kRounds; ++rd) {
+                    uint32_t r[kW][32];
+#pragma unroll
+                    for (int hf = 0; hf < kW; ++hf) tmem_ld32(ocol + 32 * (kW * rd + hf), r[hf]);
                     tmem_ld_wait();
+                    if (rd == kRounds - 1) {
+                        fence_before_sync();
+                        named_bar_sync(kBarB, 128);
+                        if (t == 0) mbar_arrive(&bar[kOempty0 + it % NOB]);
+                        if (t == 0) LA_TL(it * 16 + 14);
+                    }
+                    uint32_t pk[16 * kW];
+#pragma unroll
+                    for (int hf = 0; hf < kW; ++hf)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2)
+                            pk[16 * hf + (e >> 1)] =
+                                pack_bf16x2(__uint_as_float(r[hf][e]) * inv, __uint_as_float(r[hf][e + 1]) * inv);
+                    if (rd < kHold) {
+#pragma unroll
+                        for (int e = 0; e < 16 * kW; ++e) held[rd][e] = pk[e];
+                        continue;
+                    }
                     if (row < L) {
 #pragma unroll
-                        for (int e8 = 0; e8 < 32; e8 += 8) {
-                            uint4 wv;
-                            wv.x = pack_bf16x2(__uint_as_float(r[e8 + 0]) * inv, __uint_as_float(r[e8 + 1]) * inv);
-                            wv.y = pack_bf16x2(__uint_as_float(r[e8 + 2]) * inv, __uint_as_float(r[e8 + 3]) * inv);
-                            wv.z = pack_bf16x2(__uint_as_float(r[e8 + 4]) * inv, __uint_as_float(r[e8 + 5]) * inv);
-                            wv.w = pack_bf16x2(__uint_as_float(r[e8 + 6]) * inv, __uint_as_float(r[e8 + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + c0 + e8) = wv;
-                        }
+                        for (int h = 0; h < kHold; ++h) store_packed(held[h], 32 * kW * h);
+                        store_packed(pk, 32 * kW * rd);
                     }
                 }
-                fence_before_sync();
-                named_bar_sync(kBarB, 128);
-                if (t == 0) mbar_arrive(&bar[kOempty0 + it % NOB]);
                 if (t == 0) LA_TL(it * 16 + 11);
                 return true;
             };
@@ -845,7 +972,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                     char* tK = sm + s * Lay::kStage + Lay::kQ;
                     // the tile, and phi(K) from the feature-map group
                     bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
-                    if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
+                    if (ok && (p.phi || fact))  // K^ from the feature-map group
+                        ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                     if (named_bar_or(kBarB, 128, !ok)) {
                         stop = true;
                         break;
@@ -857,8 +985,9 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                     // unscaled tile: with gamma < 1 in the pass that scales K, with gamma = 1
                     // (no scaling) beside MMA4
                     float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
-                    // K^ = zeta . phi(K), rows >= L zeroed; then MMA4 may go (kReadyS)
-                    if (!unit_gamma) {
+                    // K^ = zeta . phi(K), rows >= L zeroed (here unless the feature-map
+                    // group took zeta already); then MMA4 may go (kReadyS)
+                    if (!unit_gamma && !fact) {
                         auto zeta = [&](int r) { return dec_zeta(gc, r, L); };
                         if (p.track_z) {
                             scale_rows_zsum<DK>(tK, zeta, zpart, t);
@@ -907,7 +1036,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 // The tiles of this chunk (phi's writes to them are visible through kQk);
                 // with gamma < 1 they are scaled in place, so MMA1 must be done with the
                 // unscaled ones first
-                bool ok = unit_gamma
+                bool ok = unit_gamma || fact
                               ? mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag)
                               : mbar_wait_or_abort(&bar[kSfull0 + (it & 1)], (it >> 1) & 1, lim, abort_flag);
                 if (ok && p.phi) ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
@@ -925,7 +1054,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 const bool zsum = NORM || p.track_z;
                 if (unit_gamma) {
                     if (zsum) colsum_partial<DK>(tK, t, zpart);
-                } else {
+                } else if (!fact) {  // (factored decay: nothing to scale here)
                     auto xi = [&](int r) { return dec_xi(gc, r); };
                     auto zeta = [&](int r) { return dec_zeta(gc, r, L); };
                     if (kE1Sum)  // and xi_i q^_i . z_{c-1} from the unscaled tile, for E2
@@ -962,7 +1091,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
                 }
                 fence_before_sync();
                 named_bar_sync(kBarB, 128);  // tiles scaled, z block written, z sums stored
-                if (t == 0) mbar_arrive(&bar[(NOB == 2 ? kSready0 : kPready0) + (it & 1)]);
+                if (t == 0) mbar_arrive(&bar[(e3_first ? kSready0 : kPready0) + (it & 1)]);
                 if (zsum && t < DK) {
                     const float gL = unit_gamma ? 1.f : GATED ? gL_gated : gamma_pow(l2g, (float)L);
                     zs[t] = fmaf(gL, zs[t], colsum_total<DK>(zpart, t));
@@ -1007,10 +1136,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI), 1) chunk_tc_ws_kernel(
 // pdl: launch as a programmatic dependent of the previous kernel in the stream
 // (the kernel's entry-state reads wait for that kernel; everything else may
 // start early).
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT = false>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI, GATED>;
-    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1031,9 +1160,10 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
         cudaFuncAttributes fa;
         cudaFuncGetAttributes(&fa, kern);
         std::fprintf(stderr,
-                     "launch_ws<%d,%d,%d,%d,%d,%d>: %s; regs %d, local %zu B, max threads %d, "
+                     "launch_ws<%d,%d,%d,%d,%d,%d,%d>: %s; regs %d, local %zu B, max threads %d, "
                      "dynamic smem %u B, static smem %zu B, grid %d x %d\n",
-                     DK, DVB, (int)NORM, (int)STATE_ONLY, (int)PHI, (int)GATED, cudaGetErrorString(e), fa.numRegs,
+                     DK, DVB, (int)NORM, (int)STATE_ONLY, (int)PHI, (int)GATED, (int)FACT,
+                     cudaGetErrorString(e), fa.numRegs,
                      fa.localSizeBytes, fa.maxThreadsPerBlock, Lay::kAlloc, fa.sharedSizeBytes, grid,
                      threads_ws(DK, DVB, PHI));
     }
@@ -1048,6 +1178,25 @@ template <bool GATED>
 cudaError_t dispatch_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
                         cudaStream_t s, bool pdl) {
     const bool phi = prm.phi != 0;
+    if constexpr (!GATED) {
+        if (prm.fact) {  // plain retention with every head's decay in the factored form's range
+            if (phi || normalize) return cudaErrorInvalidValue;
+            const bool st = prm.mode == kStateOnly;
+            if (dk == 64 && dvb == 64)
+                return st ? launch_ws<64, 64, false, true, false, false, true>(prm, grid, s, pdl)
+                          : launch_ws<64, 64, false, false, false, false, true>(prm, grid, s, pdl);
+            if (dk == 64 && dvb == 128)
+                return st ? launch_ws<64, 128, false, true, false, false, true>(prm, grid, s, pdl)
+                          : launch_ws<64, 128, false, false, false, false, true>(prm, grid, s, pdl);
+            if (dk == 128 && dvb == 64)
+                return st ? launch_ws<128, 64, false, true, false, false, true>(prm, grid, s, pdl)
+                          : launch_ws<128, 64, false, false, false, false, true>(prm, grid, s, pdl);
+            if (dk == 128 && dvb == 128)
+                return st ? launch_ws<128, 128, false, true, false, false, true>(prm, grid, s, pdl)
+                          : launch_ws<128, 128, false, false, false, false, true>(prm, grid, s, pdl);
+            return cudaErrorInvalidValue;
+        }
+    }
     if (prm.mode == kStateOnly) {
         if (dk == 64 && dvb == 64)
             return phi ? launch_ws<64, 64, false, true, true, GATED>(prm, grid, s, pdl)

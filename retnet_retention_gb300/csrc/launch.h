@@ -81,6 +81,11 @@ struct BwdArgs {
     size_t workspace_bytes;
 };
 
+// The test and diagnostic switches of la_debug_set (abi.cu).
+int opt_path();           // 0 automatic, 1 CUDA cores, 2 tensor cores
+bool opt_tc_lockstep();   // the lockstep kernel instead of the pipelined one
+bool opt_force_timeout(); // the kernels' forced 1 ms wait and timeout status
+
 // Normaliser mode passed to the kernels: 0 none, 1 divide by phi(q)^T z + eps,
 // 2 divide by max(|phi(q)^T z|, 1).
 inline int norm_mode(bool normalize, bool floor_norm) { return normalize ? (floor_norm ? 2 : 1) : 0; }

@@ -91,6 +91,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // On a timeout of its own it raises *abort.
 static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t* bar, uint32_t parity,
                                                      uint64_t limit_ns, volatile int* abort) {
+#ifdef LA_SPIN_PROBE
+    for (int i = 0; i < LA_SPIN_PROBE; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+#endif
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -151,6 +155,13 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
         : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
         : "memory");
     return out != 0;
+}
+
+// 32 bytes (eight 32-bit words) to a 32-byte aligned global address in one store.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- TMA

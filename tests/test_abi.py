@@ -52,7 +52,8 @@ def test_binding_constants_match_the_header():
     defined.update({m[0]: int(m[1]) for m in re.findall(r"\b(LA_[A-Z0-9_]+)\s*=\s*(\d+)", text)})
     names = ["LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_UNSUPPORTED", "LA_ERR_CUDA", "LA_ERR_TIMEOUT",
              "LA_DTYPE_F32", "LA_DTYPE_BF16", "LA_PHI_ELU1", "LA_NORMALIZE", "LA_NONCAUSAL",
-             "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR"]
+             "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR", "LA_OPT_PATH", "LA_OPT_TC_LOCKSTEP",
+             "LA_OPT_FORCE_TIMEOUT"]
     for name in names:
         assert getattr(la, name) == defined[name], name
     assert la.abi_version() == defined["LA_ABI_VERSION"]
@@ -63,6 +64,35 @@ def test_status_strings_and_version(lib):
     for code in range(5):
         assert la.status_string(code)
     assert la.status_string(77) == "unknown status"
+
+
+def test_debug_switches_default_off_and_check_their_range(lib):
+    """la_debug_set: every switch starts at 0, returns its previous value, and
+    refuses unknown options and out-of-range values without changing anything."""
+    for opt, hi in ((la.LA_OPT_PATH, 2), (la.LA_OPT_TC_LOCKSTEP, 1), (la.LA_OPT_FORCE_TIMEOUT, 1)):
+        assert lib.la_debug_set(opt, 0) == 0
+        assert lib.la_debug_set(opt, hi + 1) == -1
+        assert lib.la_debug_set(opt, -1) == -1
+        assert lib.la_debug_set(opt, hi) == 0
+        assert lib.la_debug_set(opt, 0) == hi
+    for bad in (0, 4, -1, 99):
+        assert lib.la_debug_set(bad, 0) == -1
+    with la.debug_options(path="simt", lockstep=True):
+        assert lib.la_debug_set(la.LA_OPT_PATH, 1) == 1
+        assert lib.la_debug_set(la.LA_OPT_TC_LOCKSTEP, 1) == 1
+    assert lib.la_debug_set(la.LA_OPT_PATH, 0) == 0
+    assert lib.la_debug_set(la.LA_OPT_TC_LOCKSTEP, 0) == 0
+    with pytest.raises(ValueError):
+        la.debug_set(la.LA_OPT_PATH, 7)
+
+
+def test_library_reads_no_environment():
+    """The shipped library takes no switch from the environment: the test
+    switches go through la_debug_set only."""
+    csrc = os.path.join(ROOT, "retnet_retention_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f)).read()
+        assert "getenv" not in text, f
 
 
 def chunk(lib, **over):

@@ -103,10 +103,10 @@ TC_SHAPES = [  # B, H, T, dk, dv: bf16, per-head decay, no phi, no normaliser
 
 
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_bwd_tensor_core_path(shape, monkeypatch):
+def test_bwd_tensor_core_path(shape, opts):
     """The three forward passes on the tensor cores (dQ; dV and dK over the reversed
     sequences) against the oracle, with an initial state and a final-state gradient."""
-    monkeypatch.delenv("LA_CHUNK_PATH", raising=False)
+    opts.path("auto")
     B, H, T, dk, dv = shape
     seed = zlib.crc32(repr((shape, "bwd-tc")).encode()) % 100000
     x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16")
@@ -127,18 +127,18 @@ def test_bwd_tensor_core_path(shape, monkeypatch):
     check("dv", to_np(dv_), rv, TOL["bf16"])
     check("dS0", to_np(dS0), rS0, TOL["bf16"])
     # the same through the CUDA-core kernel
-    monkeypatch.setenv("LA_CHUNK_PATH", "simt")
+    opts.path("simt")
     sq, sk, sv, sS0, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], S0=S0.to(DEV), dS_T=dST.to(DEV))
     torch.cuda.synchronize()
     check("dq tc vs simt", to_np(dq), to_np(sq), TOL["bf16"])
     check("dS0 tc vs simt", to_np(dS0), to_np(sS0), TOL["bf16"])
 
 
-def test_bwd_tensor_core_path_repeated(monkeypatch):
+def test_bwd_tensor_core_path_repeated(opts):
     """The tensor-core composite twelve times over: its dV pass reads reversed copies
     written just before it (hot in L2), the case that once exposed an exit state read
     before the state walk's last MMA."""
-    monkeypatch.delenv("LA_CHUNK_PATH", raising=False)
+    opts.path("auto")
     B, H, T, dk, dv = 1, 2, 3000, 64, 64
     x = workloads.random_case(9090, B, H, T, dk, dv, dtype="bf16")
     rng = np.random.default_rng(9090)

@@ -1,0 +1,85 @@
+"""The tensor-core kernel's factored per-head decay, checked on the host.
+
+For a chunk of L rows with entry state S (chunkwise form of the "RetNet" page,
+"Chunked Recurrent Representation", written out from the recurrence):
+
+  o_i = sum_{j<=i} (q_i . k_j) gamma^(i-j) v_j + gamma^(i+1) q_i S
+  S'  = gamma^L S + sum_j gamma^(L-1-j) k_j v_j^T
+
+The kernel computes the same with zeta_j = gamma^(L-1-j) folded into K once:
+
+  K'  = zeta . K,   P'_ij = q_i . k'_j (j <= i, else 0),
+  o_i = gamma^(i+1-L) (P' V + Q (gamma^L S))_i,   S' = gamma^L S + K'^T V,
+
+because gamma^(i-j) = gamma^(i+1-L) zeta_j and gamma^(i+1) = gamma^(i+1-L) gamma^L.
+Here both are checked against the fp64 oracle: the factored form in fp64 (exact
+up to rounding order), and the factored form with the kernel's roundings (K' and
+P' and the bf16 copy of gamma^L S rounded to bf16, sums in fp32) within the bf16
+tolerance, down to the smallest gamma the kernel takes it for (gamma^(C-1) =
+2^-64) and for the multi-scale retention heads' gammas.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+C = 128
+
+
+def bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def factored(q, k, v, gamma, round_like_kernel=False):
+    """One (b, h) sequence chunk by chunk in the factored form; returns O, S_T."""
+    T, dk = q.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv))
+    O = np.zeros((T, dv))
+    rnd = bf16 if round_like_kernel else (lambda x: x)
+    f32 = (lambda x: np.asarray(x, np.float32).astype(np.float64)) if round_like_kernel else (lambda x: x)
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        Q, K, V = q[c0:c0 + L], k[c0:c0 + L], v[c0:c0 + L]
+        zeta = gamma ** (L - 1 - np.arange(L, dtype=np.float64))
+        Kp = rnd(K * zeta[:, None])
+        i = np.arange(L)[:, None]
+        j = np.arange(L)[None, :]
+        Pp = rnd(np.where(j <= i, f32(Q @ Kp.T), 0.0))
+        Sg = f32(gamma ** L * S)
+        Op = f32(Pp @ V + Q @ rnd(Sg))
+        O[c0:c0 + L] = Op * (gamma ** (np.arange(L) + 1.0 - L))[:, None]
+        S = f32(Sg + Kp.T @ V)
+    return O, S
+
+
+def case(seed, T, dk, dv, scale):
+    rng = np.random.default_rng(seed)
+    q = bf16(rng.standard_normal((T, dk)) * scale)
+    k = bf16(rng.standard_normal((T, dk)) * scale)
+    v = bf16(rng.standard_normal((T, dv)))
+    return q, k, v
+
+
+def rel(a, b):
+    return np.abs(a - b).max() / np.abs(b).max()
+
+
+@pytest.mark.parametrize("gamma", [0.96875, 0.999, 0.8, 2.0 ** (-64 / 127)])
+@pytest.mark.parametrize("T", [128, 300, 1])
+def test_factored_form_is_the_recurrence(gamma, T):
+    q, k, v = case(T, T, 16, 8, 0.25)
+    Or, Sr, _ = oracle.recurrent(q[None, None], k[None, None], v[None, None], [gamma])
+    O, S = factored(q, k, v, gamma)
+    assert rel(O, Or[0, 0]) < 1e-12
+    assert rel(S, Sr[0, 0]) < 1e-12
+
+
+@pytest.mark.parametrize("gamma", [1 - 2.0 ** -5, 1 - 2.0 ** -12, 0.99, 2.0 ** (-64 / 127)])
+def test_factored_form_with_kernel_roundings_meets_the_bf16_tolerance(gamma):
+    q, k, v = case(7, 700, 64, 32, 64 ** -0.5)
+    Or, Sr, _ = oracle.recurrent(q[None, None], k[None, None], v[None, None], [gamma])
+    O, S = factored(q, k, v, gamma, round_like_kernel=True)
+    assert rel(O, Or[0, 0]) < 2e-2
+    assert rel(S, Sr[0, 0]) < 2e-2

@@ -68,10 +68,10 @@ FLAGS = [(False, False, False), (True, True, False), (False, False, True)]
 
 @pytest.mark.parametrize("flags", FLAGS, ids=["plain", "phi_norm", "floor"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_gated_matches_oracle(shape, flags, monkeypatch):
+def test_gated_matches_oracle(shape, flags, opts):
     B, H, T, dk, dv, dtype, path = shape
     phi, normalize, floor = flags
-    monkeypatch.setenv("LA_CHUNK_PATH", path)
+    opts.path(path)
     seed = zlib.crc32(repr((shape, flags, "gated")).encode()) % 100000
     x = workloads.random_case(seed, B, H, T, dk, dv, dtype=dtype, gate=True,
                               scale=0.5 if floor else None)
@@ -83,9 +83,9 @@ def test_gated_matches_oracle(shape, flags, monkeypatch):
     check("z_T", z, zr, TOL[dtype])
 
 
-def test_gated_launch_count_follows_the_plan(monkeypatch):
+def test_gated_launch_count_follows_the_plan(opts):
     """The decays' prep kernel, then the state walk, [scan,] output walk."""
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    opts.path("tc")
     lib = la.library()
     assert lib.la_chunk_fwd_launches(2, 16, 1000, 64, 64, 1, la.LA_GATED, 0) == 3
     assert lib.la_chunk_fwd_launches(1, 1, 3000, 64, 64, 1, la.LA_GATED, 0) == 4
@@ -101,9 +101,9 @@ def test_gated_launch_count_follows_the_plan(monkeypatch):
     assert len(names) == 4, names
 
 
-def test_gated_resume_from_state(monkeypatch):
+def test_gated_resume_from_state(opts):
     """A split prefill (segments folded) continued from the first part's state."""
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    opts.path("tc")
     x = workloads.random_case(7, 2, 16, 1000, 64, 64, dtype="bf16", gate=True)
     Or, Sr, zr = oracle.recurrent_gated(x["q"], x["k"], x["v"], x["log_a"], phi=True,
                                         normalize=True)
@@ -118,10 +118,10 @@ def test_gated_resume_from_state(monkeypatch):
     check("z_T", z2, zr, TOL["bf16"])
 
 
-def test_constant_gate_equals_gamma(monkeypatch):
+def test_constant_gate_equals_gamma(opts):
     """log a_t = log gamma_h for every token gives the per-head decay's results
     (two different kernel builds)."""
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    opts.path("tc")
     x = workloads.random_case(9, 2, 4, 700, 64, 64, dtype="bf16")
     B, H, T = 2, 4, 700
     lg = np.log(np.asarray(x["gamma"], np.float64)).astype(np.float32)

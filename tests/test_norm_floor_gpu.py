@@ -38,9 +38,9 @@ def check(name, got, want, tol):
     assert err <= tol, f"{name}: rel err {err:.3e} > {tol:.0e}"
 
 
-def run(x, phi, causal=True, S0=None, z0=None, path=None, monkeypatch=None):
-    if path and monkeypatch is not None:
-        monkeypatch.setenv("LA_CHUNK_PATH", path)
+def run(x, phi, causal=True, S0=None, z0=None, path=None, opts=None):
+    if path and opts is not None:
+        opts.path(path)
     q, k, v = (x[n].to(DEV).contiguous() for n in ("q", "k", "v"))
     B, H, T, dk = q.shape
     O, S, z = la.chunk_fwd(q, k, v, x["gamma"], phi=phi, floor=True, causal=causal, S0=S0, z0=z0,
@@ -62,11 +62,11 @@ SHAPES = [  # B, H, T, dk, dv, dtype, path
 
 @pytest.mark.parametrize("phi", [False, True], ids=["identity", "elu1"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_floor_matches_oracle(shape, phi, monkeypatch):
+def test_floor_matches_oracle(shape, phi, opts):
     B, H, T, dk, dv, dtype, path = shape
     seed = zlib.crc32(repr((shape, phi, "floor")).encode()) % 100000
     x = workloads.random_case(seed, B, H, T, dk, dv, dtype=dtype, scale=0.5)
-    O, S, z = run(x, phi, path=path, monkeypatch=monkeypatch)
+    O, S, z = run(x, phi, path=path, opts=opts)
     Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], phi=phi, floor=True)
     check("O", O, Or, TOL[dtype])
     check("S_T", S, Sr, TOL[dtype])
@@ -89,17 +89,17 @@ def test_floor_is_active_and_inactive_in_the_cases():
 
 
 @pytest.mark.parametrize("path", ["simt", "tc"])
-def test_floor_noncausal(path, monkeypatch):
+def test_floor_noncausal(path, opts):
     dtype = "f32" if path == "simt" else "bf16"
     x = workloads.random_case(61, 1, 3, 333, 128 if path == "tc" else 32,
                               128 if path == "tc" else 48, dtype=dtype, gamma=1.0, scale=0.3)
-    O, S, _ = run(x, False, causal=False, path=path, monkeypatch=monkeypatch)
+    O, S, _ = run(x, False, causal=False, path=path, opts=opts)
     Or, Sr, _ = oracle.noncausal(x["q"], x["k"], x["v"], floor=True)
     check("O", O, Or, TOL[dtype])
     check("S", S, Sr, TOL[dtype])
 
 
-def test_floor_resume_from_state(monkeypatch):
+def test_floor_resume_from_state(opts):
     x = workloads.random_case(62, 2, 16, 1000, 64, 64, dtype="bf16", scale=0.5)
     Or, Sr, zr = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"], floor=True)
     t1 = 389

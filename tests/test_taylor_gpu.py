@@ -132,15 +132,15 @@ def test_taylor_normalised_constant_values_return_unchanged():
     np.testing.assert_allclose(np64(O), 0.375, rtol=1e-2)
 
 
-def test_taylor_timeout_is_reported_not_hung(monkeypatch):
-    monkeypatch.setenv("LA_DEBUG_FORCE_TIMEOUT", "1")
+def test_taylor_timeout_is_reported_not_hung(opts):
+    opts.force_timeout(True)
     x = case((1, 2, 256, 64), None, "timeout")
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"], phi="taylor",
                  dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == la.LA_ERR_TIMEOUT
-    monkeypatch.delenv("LA_DEBUG_FORCE_TIMEOUT")
+    opts.force_timeout(False)
     status.zero_()
     O, _, _ = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
                            phi="taylor", dev_status=status)

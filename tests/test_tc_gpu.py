@@ -1,7 +1,8 @@
 """The tensor-core (tcgen05) chunkwise path against the fp64 oracle.
 
-LA_CHUNK_PATH=tc pins la_chunk_fwd to the tensor-core kernels (an error if
-the shape is outside them), LA_CHUNK_PATH=simt to the fp32 CUDA-core kernel;
+la_debug_set(LA_OPT_PATH, 2) pins la_chunk_fwd to the tensor-core kernels (an
+error if the shape is outside them), la_debug_set(LA_OPT_PATH, 1) to the fp32
+CUDA-core kernel;
 both are compared with the oracle on the same seeded inputs, and with each
 other.  Shapes cover one and several chunks of 128, ragged tails, T = 1,
 d_k != d_v, both value-column block widths, the split of a long sequence into
@@ -33,19 +34,19 @@ def _built():
 
 
 @pytest.fixture
-def tc_path(monkeypatch):
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+def tc_path(opts):
+    opts.path("tc")
 
 
 @pytest.fixture(params=["pipelined", "lockstep"])
-def tc_kernel(request, monkeypatch):
+def tc_kernel(request, opts):
     """Both tensor-core output kernels: the warp-specialised pipeline (default
-    where it applies) and the lockstep kernel (LA_TC_KERNEL=lockstep)."""
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    where it applies) and the lockstep kernel (LA_OPT_TC_LOCKSTEP)."""
+    opts.path("tc")
     if request.param == "lockstep":
-        monkeypatch.setenv("LA_TC_KERNEL", "lockstep")
+        opts.lockstep(True)
     else:
-        monkeypatch.delenv("LA_TC_KERNEL", raising=False)
+        opts.lockstep(False)
     return request.param
 
 
@@ -155,11 +156,11 @@ def test_tc_noncausal(flags, tc_path):
     check("S", S, Sr)
 
 
-def test_tc_and_simt_agree(monkeypatch):
+def test_tc_and_simt_agree(opts):
     x = workloads.random_case(61, 2, 4, 640, 64, 64, dtype="bf16")
-    monkeypatch.setenv("LA_CHUNK_PATH", "tc")
+    opts.path("tc")
     Ot, St, zt = run(x, True, True)
-    monkeypatch.setenv("LA_CHUNK_PATH", "simt")
+    opts.path("simt")
     Os, Ss, zs = run(x, True, True)
     check("O", Ot, Os)
     check("S", St, Ss)
@@ -171,15 +172,15 @@ def test_tc_is_the_default_for_supported_shapes():
     assert la.workspace_size(1, 8, 65536, 128, 128) > 0  # long and few: segmented
 
 
-def test_timeout_is_reported_not_hung(monkeypatch, tc_kernel):
+def test_timeout_is_reported_not_hung(opts, tc_kernel):
     """A wait that runs out (on a barrier nothing arrives on) sets dev_status; the
     context stays usable."""
-    monkeypatch.setenv("LA_DEBUG_FORCE_TIMEOUT", "1")
+    opts.force_timeout(True)
     x = workloads.random_case(71, 1, 2, 256, 64, 64, dtype="bf16")
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     run(x, False, False, dev_status=status)
     assert int(status.item()) == la.LA_ERR_TIMEOUT
-    monkeypatch.delenv("LA_DEBUG_FORCE_TIMEOUT")
+    opts.force_timeout(False)
     status.zero_()
     O, S, _ = run(x, False, False, dev_status=status)
     assert int(status.item()) == 0
