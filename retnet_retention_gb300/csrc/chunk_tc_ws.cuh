@@ -26,7 +26,7 @@
 //   warps 14-   phi = elu + 1 on the Q/K tiles as they land (8 warps for
 //               64-wide Q/K and value blocks, else 2), up to a ring's depth
 //               ahead of the tensor work; in the factored-decay build instead
-//               K *= zeta (see FACT below)
+//               V *= zeta (see FACT below)
 //
 // so that the state chain (MMA4 of c -> E3 of c+1 -> MMA4 of c+1) waits for
 // nothing but E3 and epilogue B's per-chunk work, and E1, phi and E2 run beside
@@ -243,14 +243,16 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
     const bool unit_gamma = !GATED && gam == 1.0f;
     // FACT: factored decay (per-head gamma < 1, no feature map, no normaliser, z not
     // carried; the host launches this build when every head qualifies).  With
-    // zeta_j = gamma^(L-1-j) taken into K before MMA1 (by the feature-map group,
-    // as the tile lands), the decayed scores are
-    //   P_ij = (q_i . k_j) gamma^(i-j) = gamma^(i+1-L) (q_i . zeta_j k_j),
-    // and the read-out gamma^(i+1) q_i S_{c-1} = gamma^(i+1-L) q_i (gamma^L S_{c-1}),
-    // so the whole output row is gamma^(i+1-L) (P'V + Q gamma^L S_{c-1})_i with
-    // P' = (Q (zeta K)^T) masked to j <= i: E1 only masks, Q is never rescaled,
-    // E3 copies gamma^L S (which MMA4 accumulates onto anyway) and E2 applies the
-    // one per-row factor.  The factor gamma^(i+1-L) reaches gamma^(1-C), so this
+    // zeta_j = gamma^(L-1-j) taken into V (by the feature-map group, as the tile
+    // lands, while MMA1 already runs on the raw Q and K), the decayed scores times V
+    // are
+    //   sum_j (q_i . k_j) gamma^(i-j) v_j = gamma^(i+1-L) sum_j (q_i . k_j) zeta_j v_j,
+    // the read-out gamma^(i+1) q_i S_{c-1} = gamma^(i+1-L) q_i (gamma^L S_{c-1}), and
+    // the state's update sum_j zeta_j k_j v_j^T = K^T (zeta V); so the whole output
+    // row is gamma^(i+1-L) (P V' + Q gamma^L S_{c-1})_i with P = Q K^T masked to
+    // j <= i and V' = zeta V (MMA2 and MMA4 both read V'): E1 only masks, Q and K
+    // are never rescaled, E3 copies gamma^L S (which MMA4 accumulates onto anyway)
+    // and E2 applies the one per-row factor.  The factor gamma^(i+1-L) reaches gamma^(1-C), so this
     // form is taken only while gamma^(C-1) >= 2^-64 for every head (every product
     // stays far inside the float and bf16 ranges); smaller gammas keep the row
     // scalings.
@@ -476,8 +478,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 const int s = it % NS;
                 const uint32_t par = (it / NS) & 1;
                 if (!mbar_wait_or_abort(&bar[kFull0 + s], par, lim, abort_flag)) return false;
-                if ((p.phi || fact) && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag))
-                    return false;
+                if (p.phi && !mbar_wait_or_abort(&bar[kQk0 + s], par, lim, abort_flag)) return false;
                 fence_after_sync();
                 const uint64_t dq = desc_adv(dQk0, s * Lay::kStage), dk = desc_adv(dq, Lay::kQ);
 #pragma unroll
@@ -542,6 +543,11 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
                     mma_ss(ocol, desc_adv(dq, off), desc_adv(dSB, kk * 2048), id_qs, kk > 0);
+                }
+                // factored decay: V' = zeta V from the feature-map group (MMA4 and MMA2)
+                if (FACT) {
+                    if (!mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag)) break;
+                    fence_after_sync();
                 }
                 // MMA4: S += K^^T V (M = 128, rows >= DK unused; K = 128 tokens)
 #pragma unroll
@@ -820,7 +826,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
         } else if (warp >= kWgC) {
             // ---------------- feature map: phi on Q and K (K only for a state walk), rows
             // past the end zeroed, then release the stage to the issuer (kQk); with the
-            // factored decay instead K *= zeta (Q stays as it is)
+            // factored decay instead V *= zeta (Q and K stay as they are)
             const int t = tid - kWgC * 32;
             // factored decay: zeta of this thread's rows (t >> 3) + (kThreadsC / 8) m, as
             // bf16 pairs, for the chunk length zL (recomputed only when it changes)
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                             split_bf16x2(dec_zeta(nullptr, (t >> 3) + (kThreadsC / 8) * m, L), zh[m], zl[m]);
                         zL = L;
                     }
-                    scale_rows_hl<DK / 64, kThreadsC>(st + Lay::kQ, zh, zl, t);
+                    scale_rows_hl<DVB / 64, kThreadsC>(st + Lay::kQ + Lay::kK, zh, zl, t);
                 } else if constexpr (STATE_ONLY && kThreadsC % 128 == 0) {  // all loads first
                     char* const tiles[1] = {st + Lay::kQ};
                     phi_rows_all<1, DK / 64, kThreadsC>(tiles, L, t);
@@ -972,7 +978,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     char* tK = sm + s * Lay::kStage + Lay::kQ;
                     // the tile, and phi(K) from the feature-map group
                     bool ok = mbar_wait_or_abort(&bar[kFull0 + s], (it / NS) & 1, lim, abort_flag);
-                    if (ok && (p.phi || fact))  // K^ from the feature-map group
+                    if (ok && (p.phi || fact))  // phi(K), or zeta V, from the feature-map group
                         ok = mbar_wait_or_abort(&bar[kQk0 + s], (it / NS) & 1, lim, abort_flag);
                     if (named_bar_or(kBarB, 128, !ok)) {
                         stop = true;
@@ -986,7 +992,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     // (no scaling) beside MMA4
                     float* zpart = reinterpret_cast<float*>(sm + Lay::oZP);
                     // K^ = zeta . phi(K), rows >= L zeroed (here unless the feature-map
-                    // group took zeta already); then MMA4 may go (kReadyS)
+                    // group took zeta into V); then MMA4 may go (kReadyS)
                     if (!unit_gamma && !fact) {
                         auto zeta = [&](int r) { return dec_zeta(gc, r, L); };
                         if (p.track_z) {

@@ -91,10 +91,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // On a timeout of its own it raises *abort.
 static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t* bar, uint32_t parity,
                                                      uint64_t limit_ns, volatile int* abort) {
-#ifdef LA_SPIN_PROBE
-    for (int i = 0; i < LA_SPIN_PROBE; ++i)
-        if (mbar_test_wait(bar, parity)) return true;
-#endif
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;

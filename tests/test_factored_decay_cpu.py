@@ -6,17 +6,18 @@ For a chunk of L rows with entry state S (chunkwise form of the "RetNet" page,
   o_i = sum_{j<=i} (q_i . k_j) gamma^(i-j) v_j + gamma^(i+1) q_i S
   S'  = gamma^L S + sum_j gamma^(L-1-j) k_j v_j^T
 
-The kernel computes the same with zeta_j = gamma^(L-1-j) folded into K once:
+The kernel computes the same with zeta_j = gamma^(L-1-j) folded into V once:
 
-  K'  = zeta . K,   P'_ij = q_i . k'_j (j <= i, else 0),
-  o_i = gamma^(i+1-L) (P' V + Q (gamma^L S))_i,   S' = gamma^L S + K'^T V,
+  V'  = zeta . V,   P_ij = q_i . k_j (j <= i, else 0),
+  o_i = gamma^(i+1-L) (P V' + Q (gamma^L S))_i,   S' = gamma^L S + K^T V',
 
-because gamma^(i-j) = gamma^(i+1-L) zeta_j and gamma^(i+1) = gamma^(i+1-L) gamma^L.
-Here both are checked against the fp64 oracle: the factored form in fp64 (exact
-up to rounding order), and the factored form with the kernel's roundings (K' and
-P' and the bf16 copy of gamma^L S rounded to bf16, sums in fp32) within the bf16
-tolerance, down to the smallest gamma the kernel takes it for (gamma^(C-1) =
-2^-64) and for the multi-scale retention heads' gammas.
+because gamma^(i-j) = gamma^(i+1-L) zeta_j, gamma^(i+1) = gamma^(i+1-L) gamma^L and
+sum_j zeta_j k_j v_j^T = K^T (zeta . V).  Here both are checked against the fp64
+oracle: the factored form in fp64 (exact up to rounding order), and the factored
+form with the kernel's roundings (V', P and the bf16 copy of gamma^L S rounded
+to bf16, sums in fp32) within the bf16 tolerance, down to the smallest gamma the
+kernel takes it for (gamma^(C-1) = 2^-64) and for the multi-scale retention
+heads' gammas.
 """
 import numpy as np
 import pytest
@@ -43,14 +44,14 @@ def factored(q, k, v, gamma, round_like_kernel=False):
         L = min(C, T - c0)
         Q, K, V = q[c0:c0 + L], k[c0:c0 + L], v[c0:c0 + L]
         zeta = gamma ** (L - 1 - np.arange(L, dtype=np.float64))
-        Kp = rnd(K * zeta[:, None])
+        Vp = rnd(V * zeta[:, None])
         i = np.arange(L)[:, None]
         j = np.arange(L)[None, :]
-        Pp = rnd(np.where(j <= i, f32(Q @ Kp.T), 0.0))
+        P = rnd(np.where(j <= i, f32(Q @ K.T), 0.0))
         Sg = f32(gamma ** L * S)
-        Op = f32(Pp @ V + Q @ rnd(Sg))
+        Op = f32(P @ Vp + Q @ rnd(Sg))
         O[c0:c0 + L] = Op * (gamma ** (np.arange(L) + 1.0 - L))[:, None]
-        S = f32(Sg + Kp.T @ V)
+        S = f32(Sg + K.T @ Vp)
     return O, S
 
 
