@@ -442,7 +442,8 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
     flags = _flags(phi, normalize, True, floor)
     lib = _load()
     with _current(dev):
-        need = int(lib.la_bwd_workspace_size(B, H, T, dk_, dv_, dt, flags))
+        need = int(lib.la_bwd_workspace_size(B, H, T, dk_, dv_, dt,
+                                             flags | (LA_GATED if log_a is not None else 0)))
         if need and workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         ws_bytes = _workspace(workspace, need, dev)

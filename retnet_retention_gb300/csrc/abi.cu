@@ -99,7 +99,7 @@ BwdArgs bwd_plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, uns
 
 size_t bwd_bytes_for(const BwdArgs& a) {
     if (!simt_pinned() && bwd_tc_supported(a)) return bwd_tc_workspace_bytes(a);
-    return bwd_workspace_bytes(a.B, a.H, a.T, a.normalize);
+    return bwd_workspace_bytes(a);
 }
 
 }  // namespace

@@ -25,10 +25,22 @@
 //   phi'(x) = min(1, phi(x)) for phi = elu + 1.
 //
 // Without the normaliser (den = 1, du = 0) the two sweeps are independent and
-// run as one launch, one CTA per (b, h) and sweep; with it the backward sweep
-// reads the forward sweep's den_i and du_i (per token, in the workspace), so
-// the forward sweep runs first.  One CTA holds the whole d_k x d_v state of its
-// (b, h) in shared memory (d_k, d_v <= 128).
+// run side by side; with it the backward sweep reads the forward sweep's den_i
+// and du_i (per token, in the workspace), so the forward sweep runs first.  One
+// CTA holds the whole d_k x d_v state of its (b, h) in shared memory (d_k, d_v
+// <= 128).
+//
+// Segments: so that every SM holds several CTAs, each sequence is cut into P
+// segments of whole chunks.  A state-only pass computes each segment's own
+// contribution (forward: S and z from zero over the segment; backward: G and
+// Gz from zero, i.e. the gradient of the segment's own outputs with respect to
+// the state entering it), a scan folds them into entry states (forward:
+// S_entry(q+1) = d(q) S_entry(q) + agg(q) from S_0; backward: G_end(q) =
+// d(q+1) G_end(q+1) + gagg(q+1) from dS_T; d(q) the state's decay over segment
+// q), and the full sweeps run every segment from its entry state.
+#include <algorithm>
+#include <cstring>
+
 #include "launch.h"
 #include "trace.h"
 
@@ -37,6 +49,23 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
+
+// The segment plan of one launch (see the header).
+struct BwdSeg {
+    int n_seg;          // segments per sequence
+    int seg_chunks;     // chunks (of C tokens) per segment
+    int state_only;     // 1: only the segment's own state contribution
+    const float* S_ent; // full forward sweep: entry states [BH][n_seg][dk][dv] (null: S0)
+    const float* z_ent; // [BH][n_seg][dk] (null: z0)
+    const float* G_ent; // full backward sweep: G at each segment's end (null: dS_T)
+    const float* Gz_ent;
+    float* agg;         // state-only forward sweep: [BH][n_seg][dk][dv]
+    float* zagg;        // state-only forward sweep: [BH][n_seg][dk]
+    float* agg1;        // state-only backward sweep: the same for G and Gz
+    float* zagg1;
+    float* seg_l2;      // state-only forward sweep, per-token decay: the segment's
+                        // total log2 decay [BH][n_seg]
+};
 
 struct BwdSmem {  // offsets in floats
     int q, k, v, g, n, a, p, s, z, den, du, pw, cum, xw, total;
@@ -70,7 +99,8 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     const float* __restrict__ dST, const float* __restrict__ dzT, T* __restrict__ dQ,
     T* __restrict__ dK, T* __restrict__ dV, float* __restrict__ dS0, float* __restrict__ dz0,
     float* __restrict__ stats, int H, int T_len, int dk, int dv, int C, int phi, int normalize,
-    float eps, int role0, const float* __restrict__ log_a, const __grid_constant__ KernelGammas g) {
+    float eps, int role0, const float* __restrict__ log_a, const __grid_constant__ KernelGammas g,
+    const __grid_constant__ BwdSeg sg) {
     extern __shared__ float smem[];
     const BwdSmem lay = bwd_layout(C, dk, dv);
     float* Qs = smem + lay.q;
@@ -89,36 +119,54 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     float* xw = smem + lay.xw;
     const int ldk = dk + 1, ldv = dv + 1, lda = C + 1, lds = dv + 1;
 
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / sg.n_seg;
+    const int seg = blockIdx.x % sg.n_seg;
+    const size_t sidx = (size_t)bh * sg.n_seg + seg;  // this unit's entry / contribution slot
     const int role = role0 + (int)blockIdx.y;  // 0: forward sweep (dq), 1: backward sweep (dk, dv)
+    const bool st_only = sg.state_only != 0;
     const int h = bh % H;
     const int tid = threadIdx.x;
     const float l2g = g.log2g[h];
     const size_t qk_base = (size_t)bh * T_len * dk;
     const size_t v_base = (size_t)bh * T_len * dv;
     const int n_chunks = (T_len + C - 1) / C;
+    const int cb = seg * sg.seg_chunks;
+    const int ce = min(n_chunks, cb + sg.seg_chunks);
 
     for (int n = tid; n <= C; n += kThreads) pw[n] = gamma_pow(l2g, (float)n);
-    // entry state: S0, z0 (forward sweep) or dS_T, dz_T (backward sweep)
-    const float* s_in = role == 0 ? S0 : dST;
-    const float* z_in = role == 0 ? z0 : dzT;
+    // entry state: S0, z0 or the segment's entry (forward sweep); dS_T, dz_T or the
+    // state's gradient at the segment's end (backward sweep); zero for a state-only pass
+    const float* s_in = nullptr;
+    const float* z_in = nullptr;
+    if (!st_only) {
+        if (role == 0) {
+            s_in = sg.S_ent ? sg.S_ent + sidx * dk * dv : (S0 ? S0 + (size_t)bh * dk * dv : nullptr);
+            z_in = sg.z_ent ? sg.z_ent + sidx * dk : (z0 ? z0 + (size_t)bh * dk : nullptr);
+        } else {
+            s_in = sg.G_ent ? sg.G_ent + sidx * dk * dv : (dST ? dST + (size_t)bh * dk * dv : nullptr);
+            z_in = sg.Gz_ent ? sg.Gz_ent + sidx * dk : (dzT ? dzT + (size_t)bh * dk : nullptr);
+        }
+    }
     for (int idx = tid; idx < dk * dv; idx += kThreads)
-        Ss[(idx / dv) * lds + idx % dv] = s_in ? s_in[(size_t)bh * dk * dv + idx] : 0.f;
-    for (int d = tid; d < dk; d += kThreads) zs[d] = z_in ? z_in[(size_t)bh * dk + d] : 0.f;
+        Ss[(idx / dv) * lds + idx % dv] = s_in ? s_in[idx] : 0.f;
+    for (int d = tid; d < dk; d += kThreads) zs[d] = z_in ? z_in[d] : 0.f;
+    float seg_lam = 0.f;  // per-token decay: the segment's total log2 decay (thread 0)
     __syncthreads();
 
-    for (int cc = 0; cc < n_chunks; ++cc) {
-        const int c = role == 0 ? cc : n_chunks - 1 - cc;
+    for (int cc = cb; cc < ce; ++cc) {
+        const int c = role == 0 ? cc : ce - 1 - (cc - cb);
         const int t0 = c * C;
         const int L = min(C, T_len - t0);
-        // tiles: phi(Q), phi(K), V, dO (rows >= L zero)
+        // tiles: phi(Q), phi(K), V, dO (rows >= L zero); a state-only pass reads
+        // K and V (forward sweep) or Q and dO (backward sweep) only
+        const bool need_qg = !st_only || role == 1, need_kv = !st_only || role == 0;
         for (int idx = tid; idx < C * dk; idx += kThreads) {
             const int i = idx / dk, d = idx % dk;
             float x = 0.f, y = 0.f;
             if (i < L) {
                 const size_t gi = qk_base + (size_t)(t0 + i) * dk + d;
-                x = load_elem(Q, gi);
-                y = load_elem(K, gi);
+                if (need_qg) x = load_elem(Q, gi);
+                if (need_kv) y = load_elem(K, gi);
                 if (phi) {
                     x = phi_elu1(x);
                     y = phi_elu1(y);
@@ -132,8 +180,8 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             float x = 0.f, y = 0.f;
             if (i < L) {
                 const size_t gi = v_base + (size_t)(t0 + i) * dv + cc2;
-                x = load_elem(V, gi);
-                y = load_elem(dO, gi);
+                if (need_kv) x = load_elem(V, gi);
+                if (need_qg) y = load_elem(dO, gi);
             }
             Vs[i * ldv + cc2] = x;
             Gs[i * ldv + cc2] = y;
@@ -163,6 +211,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         auto xi = [&](int i) { return log_a ? xw[i] : pw[i + 1]; };
         auto zt = [&](int j) { return log_a ? zeta[j] : pw[L - 1 - j]; };
         const float gL = log_a ? exp2f(cum[L - 1]) : pw[L];
+        if (log_a && tid == 0) seg_lam += cum[L - 1];
         // Register tiles: a thread computes 4 output rows x 2 columns (c = 64 g + slot
         // and c + 32), so each shared-memory operand it loads feeds 2 or 4 FMAs; the
         // 32 items of a warp share their rows (broadcast loads) and take consecutive
@@ -178,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         };
 
         // A_ij = D_ij q~_i . k~_j (j <= i): tiles of 4 rows i and one column j
-        for (int item = tid; item < ((L + 3) >> 2) * 32; item += kThreads) {
+        for (int item = tid; item < (st_only ? 0 : ((L + 3) >> 2) * 32); item += kThreads) {
             const int j = item & 31, i0 = (item >> 5) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (j < L && j <= i0 + 3) {
@@ -196,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             }
         }
         __syncthreads();
-        if (role == 0) {
+        if (role == 0 && !st_only) {
             if (normalize) {
                 // n_i = sum_j A_ij v_j + xi_i q~_i S  (A_ij = 0 above the diagonal)
                 tiles(L, dv, [&](int i0, int c0, int c1) {
@@ -259,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             }
         }
         // dn_i = dO_i / den_i (in place)
-        if (normalize) {
+        if (normalize && need_qg) {
             for (int idx = tid; idx < L * dv; idx += kThreads) {
                 const int i = idx / dv, cc2 = idx % dv;
                 Gs[i * ldv + cc2] /= den[i];
@@ -267,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             __syncthreads();
         }
         // P_ij = D_ij (dn_i . v_j + du_i)  (j <= i): tiles of 4 rows i and one column j
-        for (int item = tid; item < ((L + 3) >> 2) * 32; item += kThreads) {
+        for (int item = tid; item < (st_only ? 0 : ((L + 3) >> 2) * 32); item += kThreads) {
             const int j = item & 31, i0 = (item >> 5) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (j < L && j <= i0 + 3) {
@@ -288,7 +337,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         __syncthreads();
         if (role == 0) {
             // dq~_i = sum_j P_ij k~_j + xi_i (S dn_i + du_i z);  dq = dq~ * phi'(q)
-            tiles(L, dk, [&](int i0, int c0, int c1) {
+            if (!st_only) tiles(L, dk, [&](int i0, int c0, int c1) {
                 const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
                 float in[4][2] = {}, it[4][2] = {};
                 const int jmax = min(i0 + 3, L - 1);
@@ -355,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             __syncthreads();
         } else {
             // dv_j = sum_{i>=j} A_ij dn_i + zeta_j k~_j G
-            tiles(L, dv, [&](int j0, int c0, int c1) {
+            if (!st_only) tiles(L, dv, [&](int j0, int c0, int c1) {
                 const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
                 float in[4][2] = {}, it[4][2] = {};
                 for (int i = j0; i < L; ++i) {  // A_ij = 0 for i < j
@@ -385,7 +434,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
                 }
             });
             // dk~_j = sum_{i>=j} P_ij q~_i + zeta_j (G v_j + Gz);  dk = dk~ * phi'(k)
-            tiles(L, dk, [&](int j0, int c0, int c1) {
+            if (!st_only) tiles(L, dk, [&](int j0, int c0, int c1) {
                 const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
                 float in[4][2] = {}, it[4][2] = {};
                 for (int i = j0; i < L; ++i) {  // P_ij = 0 for i < j
@@ -452,12 +501,66 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             __syncthreads();
         }
     }
-    if (role == 1) {  // gradients of the initial state
+    if (st_only) {  // this segment's own contribution (and its total log2 decay)
+        float* agg = role == 0 ? sg.agg : sg.agg1;
+        float* zagg = role == 0 ? sg.zagg : sg.zagg1;
+        for (int idx = tid; idx < dk * dv; idx += kThreads)
+            agg[sidx * dk * dv + idx] = Ss[(idx / dv) * lds + idx % dv];
+        for (int d = tid; d < dk; d += kThreads) zagg[sidx * dk + d] = zs[d];
+        if (role == 0 && log_a && sg.seg_l2 && tid == 0) sg.seg_l2[sidx] = seg_lam;
+    } else if (role == 1 && seg == 0) {  // gradients of the initial state
         if (dS0)
             for (int idx = tid; idx < dk * dv; idx += kThreads)
                 dS0[(size_t)bh * dk * dv + idx] = Ss[(idx / dv) * lds + idx % dv];
         if (dz0)
             for (int d = tid; d < dk; d += kThreads) dz0[(size_t)bh * dk + d] = zs[d];
+    }
+}
+
+// Entry states of the segments from their own contributions (see the header).
+// dir 0 (forward sweep): e(0) = init, e(q) = d(q-1) e(q-1) + agg(q-1);
+// dir 1 (backward sweep): e(P-1) = init, e(q) = d(q+1) e(q+1) + agg(q+1);
+// d(q) = gamma^len(q) (len(q) the tokens of segment q, the last one ragged) or
+// 2^(seg_l2[bh][q]) with the per-token decay.  One thread per element of a
+// sequence's state (d_k x d_v) and, with do_z, of z (d_k more); blockIdx.y
+// picks the direction's arrays from `sc`.
+struct ScanArgs {
+    const float* init[2];
+    const float* zinit[2];
+    const float* agg[2];
+    const float* zagg[2];
+    float* ent[2];
+    float* zent[2];
+    int dir0;  // direction of blockIdx.y == 0
+};
+
+__global__ void bwd_scan_kernel(const __grid_constant__ ScanArgs sc, int BH, int H, int P, int seg_len,
+                                int T, int dk, int dv, int do_z, const float* __restrict__ seg_l2,
+                                const __grid_constant__ KernelGammas g) {
+    const int dir = sc.dir0 + (int)blockIdx.y;
+    const size_t per = (size_t)dk * dv + dk;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)BH * per) return;
+    const size_t bh = idx / per;
+    const size_t e = idx % per;
+    const bool is_z = e >= (size_t)dk * dv;
+    if (is_z && !do_z) return;
+    const size_t n = is_z ? dk : (size_t)dk * dv;
+    const size_t el = is_z ? e - (size_t)dk * dv : e;
+    const float* init = is_z ? sc.zinit[blockIdx.y] : sc.init[blockIdx.y];
+    const float* agg = is_z ? sc.zagg[blockIdx.y] : sc.agg[blockIdx.y];
+    float* ent = is_z ? sc.zent[blockIdx.y] : sc.ent[blockIdx.y];
+    const float l2g = g.log2g[bh % H];
+    auto dec = [&](int q) {
+        return seg_l2 ? exp2f(seg_l2[bh * P + q]) : gamma_pow(l2g, (float)min(seg_len, T - q * seg_len));
+    };
+    float x = init ? init[bh * n + el] : 0.f;
+    for (int s = 0; s < P; ++s) {
+        const int q = dir == 0 ? s : P - 1 - s;
+        ent[(bh * P + q) * n + el] = x;
+        // the next entry: segment q's decay and own contribution (forward: e(q+1);
+        // backward: e(q-1))
+        if (s + 1 < P) x = fmaf(dec(q), x, agg[(bh * P + q) * n + el]);
     }
 }
 
@@ -469,35 +572,140 @@ int bwd_chunk_len(int dk, int dv) {
     return C;
 }
 
-size_t bwd_workspace_bytes(int B, int H, int T, bool normalize) {
-    return normalize ? (size_t)B * H * T * 2 * sizeof(float) : 0;
+namespace {
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// The backward pass's segment plan and workspace layout (byte offsets).
+struct BwdPlan {
+    int C, n_chunks, P, seg_chunks;
+    size_t smem;
+    size_t o_stats, o_a0, o_a0z, o_e0, o_e0z, o_a1, o_a1z, o_e1, o_e1z, o_l2, bytes;
+};
+
+BwdPlan bwd_plan(int B, int H, int T, int dk, int dv, bool normalize) {
+    BwdPlan pl;
+    pl.C = bwd_chunk_len(dk, dv);
+    pl.smem = (size_t)bwd_layout(pl.C, dk, dv).total * sizeof(float);
+    pl.n_chunks = T > 0 ? (T + pl.C - 1) / pl.C : 0;
+    const size_t nbh = (size_t)B * H;
+    // CTAs an SM holds by shared memory (registers allow four), and as many segments
+    // per sequence as fill every SM that often, each of two chunks or more
+    const int per_sm = (int)std::min<size_t>(4, std::max<size_t>(1, (227 * 1024) / pl.smem));
+    size_t want = nbh ? ((size_t)device_sms() * per_sm) / nbh : 1;
+    want = std::min<size_t>(want, (size_t)std::max(1, pl.n_chunks / 2));
+    pl.P = (int)std::max<size_t>(1, want);
+    pl.seg_chunks = pl.P > 1 ? (pl.n_chunks + pl.P - 1) / pl.P : std::max(1, pl.n_chunks);
+    if (pl.P > 1) pl.P = (pl.n_chunks + pl.seg_chunks - 1) / pl.seg_chunks;  // segments used
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) / 256 * 256;
+        return o;
+    };
+    pl.o_stats = normalize ? take(nbh * T * 2 * sizeof(float)) : 0;
+    const size_t st = nbh * pl.P * dk * dv * sizeof(float), zt = nbh * pl.P * dk * sizeof(float);
+    if (pl.P > 1) {
+        pl.o_a0 = take(st), pl.o_a0z = take(zt), pl.o_e0 = take(st), pl.o_e0z = take(zt);
+        pl.o_a1 = take(st), pl.o_a1z = take(zt), pl.o_e1 = take(st), pl.o_e1z = take(zt);
+        pl.o_l2 = take(nbh * pl.P * sizeof(float));
+    } else {
+        pl.o_a0 = pl.o_a0z = pl.o_e0 = pl.o_e0z = pl.o_a1 = pl.o_a1z = pl.o_e1 = pl.o_e1z = pl.o_l2 = 0;
+    }
+    pl.bytes = off;
+    return pl;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(const BwdArgs& a) {
+    return a.T > 0 ? bwd_plan(a.B, a.H, a.T, a.dk, a.dv, a.normalize).bytes : 0;
 }
 
 cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) {
-    const int C = bwd_chunk_len(a.dk, a.dv);
-    const size_t smem = (size_t)bwd_layout(C, a.dk, a.dv).total * sizeof(float);
+    const BwdPlan pl = bwd_plan(a.B, a.H, a.T, a.dk, a.dv, a.normalize);
+    const int C = pl.C;
+    const size_t smem = pl.smem;
     const unsigned nbh = (unsigned)((size_t)a.B * a.H);
     const int nm = norm_mode(a.normalize, a.floor_norm);
-    float* stats = static_cast<float*>(a.workspace);
+    char* ws = static_cast<char*>(a.workspace);
+    float* stats = nm ? reinterpret_cast<float*>(ws + pl.o_stats) : nullptr;
+    auto fp = [&](size_t o) { return reinterpret_cast<float*>(ws + o); };
+    BwdSeg base;
+    std::memset(&base, 0, sizeof(base));
+    base.n_seg = pl.P;
+    base.seg_chunks = pl.seg_chunks;
+    BwdSeg full = base, st = base;
+    if (pl.P > 1) {
+        full.S_ent = fp(pl.o_e0), full.z_ent = fp(pl.o_e0z);
+        full.G_ent = fp(pl.o_e1), full.Gz_ent = fp(pl.o_e1z);
+        st.state_only = 1;
+        st.agg = fp(pl.o_a0), st.zagg = fp(pl.o_a0z), st.agg1 = fp(pl.o_a1), st.zagg1 = fp(pl.o_a1z);
+        st.seg_l2 = a.log_a ? fp(pl.o_l2) : nullptr;
+    }
     cudaError_t e = cudaSuccess;
-    auto launch = [&](auto kern, auto cast, int role0, unsigned roles) {
+    auto launch = [&](auto kern, auto cast, int role0, unsigned roles, const BwdSeg& sg) {
+        if (e != cudaSuccess) return;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return;
-        TraceScope trace(roles == 2 ? "chunk_bwd_simt_kernel"
+        TraceScope trace(sg.state_only ? "chunk_bwd_simt_kernel/state"
+                         : roles == 2 ? "chunk_bwd_simt_kernel"
                          : role0 == 0 ? "chunk_bwd_simt_kernel/dq" : "chunk_bwd_simt_kernel/dkdv",
                          s);
-        kern<<<dim3(nbh, roles), kThreads, smem, s>>>(
+        kern<<<dim3(nbh * pl.P, roles), kThreads, smem, s>>>(
             cast(a.Q), cast(a.K), cast(a.V), cast(a.dO), a.S0, a.z0, a.dS_T, a.dz_T, cast(a.dQ),
             cast(a.dK), cast(a.dV), a.dS0, a.dz0, stats, a.H, a.T, a.dk, a.dv, C, a.phi, nm,
-            a.eps, role0, a.log_a, g);
+            a.eps, role0, a.log_a, g, sg);
+        e = cudaGetLastError();
+    };
+    // the entry states of direction dir0 (and dir0 + 1 when dirs == 2)
+    auto scan = [&](int dir0, int dirs) {
+        if (e != cudaSuccess) return;
+        ScanArgs sc;
+        std::memset(&sc, 0, sizeof(sc));
+        sc.dir0 = dir0;
+        for (int y = 0; y < dirs; ++y) {
+            const int dir = dir0 + y;
+            sc.init[y] = dir == 0 ? a.S0 : a.dS_T;
+            sc.zinit[y] = dir == 0 ? a.z0 : a.dz_T;
+            sc.agg[y] = fp(dir == 0 ? pl.o_a0 : pl.o_a1);
+            sc.zagg[y] = fp(dir == 0 ? pl.o_a0z : pl.o_a1z);
+            sc.ent[y] = fp(dir == 0 ? pl.o_e0 : pl.o_e1);
+            sc.zent[y] = fp(dir == 0 ? pl.o_e0z : pl.o_e1z);
+        }
+        const size_t total = (size_t)nbh * ((size_t)a.dk * a.dv + a.dk);
+        TraceScope trace("bwd_scan_kernel", s);
+        bwd_scan_kernel<<<dim3((unsigned)((total + 255) / 256), dirs), 256, 0, s>>>(
+            sc, (int)nbh, a.H, pl.P, pl.seg_chunks * C, a.T, a.dk, a.dv, nm ? 1 : 0,
+            a.log_a ? fp(pl.o_l2) : nullptr, g);
         e = cudaGetLastError();
     };
     auto run = [&](auto kern, auto cast) {
-        if (nm == 0) {
-            launch(kern, cast, 0, 2);  // the two sweeps are independent
-        } else {
-            launch(kern, cast, 0, 1);  // the backward sweep reads the forward sweep's den, du
-            if (e == cudaSuccess) launch(kern, cast, 1, 1);
+        if (pl.P <= 1) {
+            if (nm == 0) {
+                launch(kern, cast, 0, 2, full);  // the two sweeps are independent
+            } else {
+                launch(kern, cast, 0, 1, full);  // the backward sweep reads the forward sweep's den, du
+                launch(kern, cast, 1, 1, full);
+            }
+            return;
+        }
+        if (nm == 0) {  // both sweeps' contributions, entries, then both sweeps
+            launch(kern, cast, 0, 2, st);
+            scan(0, 2);
+            launch(kern, cast, 0, 2, full);
+        } else {  // the backward sweep's contributions need the forward sweep's den, du
+            launch(kern, cast, 0, 1, st);
+            scan(0, 1);
+            launch(kern, cast, 0, 1, full);
+            launch(kern, cast, 1, 1, st);
+            scan(1, 1);
+            launch(kern, cast, 1, 1, full);
         }
     };
     if (a.bf16)

@@ -63,14 +63,16 @@
 #include "launch.h"
 #include "trace.h"
 
-// Development timeline (compiled only with -DLA_TIMELINE): CTA 0 stamps the
-// global timer at pipeline events into a device array the host reads back.
+// Development timeline (compiled only with -DLA_TIMELINE): CTA 0 stamps its SM's
+// cycle counter at pipeline events into a device array the host reads back (the
+// cycle counter: a read of the global timer costs far more than the events it
+// would time).
 #ifdef LA_TIMELINE
 __device__ unsigned long long la_timeline[4096];
 #define LA_TL(slot)                                                                        \
     do {                                                                                   \
         if (blockIdx.x == 0)                                                               \
-            la_timeline[((slot) + (STATE_ONLY ? 2048 : 0)) & 4095] = la::tc::global_timer_ns() | 1ull; \
+            la_timeline[((slot) + (STATE_ONLY ? 2048 : 0)) & 4095] = (unsigned long long)clock64() | 1ull; \
     } while (0)
 extern "C" __attribute__((visibility("default"))) int la_timeline_read(unsigned long long* host,
                                                                           int n) {

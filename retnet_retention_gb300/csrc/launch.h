@@ -101,9 +101,11 @@ cudaError_t launch_decode_step(const StepArgs& a, const KernelGammas& g, cudaStr
 cudaError_t launch_chunk_simt(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s);
 int simt_chunk_len(int requested, int dk);
 
-// chunk_bwd_simt.cu: the backward pass on the CUDA cores (d_k, d_v <= 128)
+// chunk_bwd_simt.cu: the backward pass on the CUDA cores (d_k, d_v <= 128); long
+// sequences are cut into segments (workspace: per-token denominators when
+// normalising, the segments' states)
 cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s);
-size_t bwd_workspace_bytes(int B, int H, int T, bool normalize);
+size_t bwd_workspace_bytes(const BwdArgs& a);
 
 // chunk_bwd_tc.cu: the backward pass as three forward passes on the tensor cores
 // (bf16, no feature map, no normaliser, per-head decay, d_k, d_v in {64, 128})

@@ -51,6 +51,7 @@ SHAPES = [  # B, H, T, dk, dv, dtype
     (2, 2, 260, 64, 64, "bf16"),
     (1, 2, 130, 128, 128, "bf16"),
     (2, 1, 97, 64, 128, "bf16"),
+    (1, 1, 1000, 64, 64, "bf16"),  # 16 segments of two chunks, the last one ragged
 ]
 FLAGS = [(False, False, False), (True, True, False), (False, False, True)]
 
