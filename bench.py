@@ -295,16 +295,20 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
                alg_bytes=alg_bytes(c), alg_flops=alg_flops(c), launches=launches,
                kernels=kernels)
     if e2e:
-        # through the public host-buffer entry point: pinned inputs in, results out,
-        # every copy inside the timed region (device time, CUDA events)
+        # through the C ABI's host-buffer entry point (la_chunk_fwd_host): pinned
+        # inputs in, results out, every copy inside the timed region (device time,
+        # CUDA events); the batch goes in one piece per batch row, pipelined
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
         Oh = torch.empty(shape_v, dtype=q.dtype, pin_memory=True)
         Sh = torch.empty(B, c["H"], c["dk"], c["dv"], pin_memory=True)
         zh = torch.empty(B, c["H"], c["dk"], pin_memory=True) if c["normalize"] else None
+        arena = torch.empty(la.host_arena_size(B, c["H"], c["T"], c["dk"], c["dv"], q.dtype,
+                                               c["phi"], c["normalize"], pieces=B),
+                            dtype=torch.uint8, device=dev)
 
         def step_host(times):
             la.chunk_fwd_host(qh, kh, vh, gamma, phi=c["phi"], normalize=c["normalize"], pieces=B,
-                              out=Oh, S_out=Sh, z_out=zh, timing=times)
+                              out=Oh, S_out=Sh, z_out=zh, timing=times, arena=arena)
 
         for _ in range(warmup):
             step_host(None)

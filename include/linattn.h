@@ -34,6 +34,9 @@
  *   - `gamma` is a HOST array of H fp32 decays, each in (0, 1]; it is read
  *     during the call (its values travel in the kernel parameters), so the
  *     array may be reused as soon as the call returns.
+ *   - Calls run on the CURRENT device (cudaSetDevice): it must own `stream`
+ *     and every buffer passed; the segment plans and workspace sizes are the
+ *     current device's too (its SM count).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  The return code covers host-side argument
  *     checks and launch errors only.  `dev_status`, if not NULL, is a device
@@ -311,14 +314,18 @@ LA_API size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dt
  *
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  The cached address holds until the device is reset
+ *     (cudaDeviceReset); calls after a reset in the same process are not
+ *     supported.
  *   - Calls whose la_workspace_size exceeds LA_NOALLOC_SCRATCH_BYTES return
  *     LA_ERR_INVALID_ARG without launching anything.
  *   - Every call shares the one array, and the array keeps whatever the last
- *     call left in it.  Nothing needs clearing: each call writes every scratch
- *     byte it later reads.  Calls that overlap on the GPU (different streams,
- *     or host threads) race on the array and give wrong results; serialise
- *     them.
+ *     call left in it.  Nothing needs clearing: within a call every scratch
+ *     byte is written before it is read (the state walk writes each segment's
+ *     contribution, zeros included where no normaliser is carried, before the
+ *     scan or the output walk reads it).  Calls that overlap on the GPU
+ *     (different streams, or host threads) race on the array and give wrong
+ *     results; serialise them.
  *   - Errors otherwise as la_chunk_fwd; LA_ERR_CUDA if the address lookup fails.
  */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -328,6 +335,45 @@ LA_API la_status la_chunk_fwd_noalloc(const void* Q, const void* K, const void* 
                                       const float* S0, const float* z0,
                                       void* O, float* S_out, float* z_out, int chunk,
                                       int* dev_status, la_stream_t stream);
+
+/*
+ * la_chunk_fwd on HOST buffers, the copies included: the end-to-end call for a
+ * caller whose inputs and outputs live in host memory (the operation is
+ * la_chunk_fwd's; the pages have no counterpart to the copies).
+ *
+ *   Q, K, V, S0, z0   as la_chunk_fwd, in HOST memory (pinned, e.g. by
+ *                     cudaHostAlloc, for the copies to run asynchronously and
+ *                     overlap; pageable memory works, with serialised copies)
+ *   O, S_out, z_out   as la_chunk_fwd, in HOST memory; written when the call's
+ *                     work on `stream` completes
+ *   pieces            the batch is cut into `pieces` groups of whole sequences
+ *                     (1 <= pieces <= B); piece i is copied in, computed and
+ *                     copied out in order on one of two streams the call creates
+ *                     (i mod 2), into slot i mod 2 of the arena, so one piece's
+ *                     copies overlap another's compute
+ *   arena, arena_bytes  caller-owned DEVICE memory of at least
+ *                     la_host_arena_size(...) bytes (16-byte aligned): two
+ *                     slots of one piece's inputs, outputs and workspace; the
+ *                     library allocates nothing
+ *   stream            the call's work starts after the work already on `stream`,
+ *                     and work enqueued on `stream` afterwards starts after the
+ *                     call's (events); the call returns without waiting: the host
+ *                     buffers must stay valid, and the outputs are not read, until
+ *                     `stream` has passed the call's work
+ * gamma and the flags as la_chunk_fwd (the per-token decay is not taken here).
+ * Every check of the per-piece calls runs before anything is enqueued.
+ * Errors: as la_chunk_fwd; LA_ERR_INVALID_ARG also for pieces outside [1, B],
+ * a NULL host input or output when T > 0, or an arena that is too small or
+ * misaligned; LA_ERR_CUDA if a copy, stream or event call fails.
+ */
+LA_API size_t la_host_arena_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
+                                 unsigned flags, int chunk, int pieces);
+LA_API la_status la_chunk_fwd_host(const void* Q, const void* K, const void* V, la_dtype dtype,
+                                   const float* gamma, int B, int H, int T, int d_k, int d_v,
+                                   unsigned flags, float eps, const float* S0, const float* z0,
+                                   void* O, float* S_out, float* z_out, int chunk, int pieces,
+                                   void* arena, size_t arena_bytes, int* dev_status,
+                                   la_stream_t stream);
 
 /*
  * Test and diagnostic switches (no counterpart on the pages).  Process-wide,

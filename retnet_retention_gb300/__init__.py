@@ -13,7 +13,7 @@ Names follow the C ABI:
   recurrent_step(q, k, v, gamma, S, z, ...)    one decode step     (la_recurrent_step)
   recurrent_step(q, k, v, None, S, z, log_a=)  per-token decay     (la_recurrent_step_gated)
   workspace_size(...)                          scratch bytes       (la_workspace_size)
-  chunk_fwd_host(...)                          la_chunk_fwd on host buffers, copies included
+  chunk_fwd_host(...)                          host buffers, copies included (la_chunk_fwd_host)
 """
 from __future__ import annotations
 
@@ -96,6 +96,11 @@ def _load() -> ctypes.CDLL:
     lib.la_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp,
                                          vp, i, vp, vp]
     lib.la_chunk_fwd_noalloc.restype = i
+    lib.la_host_arena_size.argtypes = [i, i, i, i, i, i, u, i, i]
+    lib.la_host_arena_size.restype = sz
+    lib.la_chunk_fwd_host.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, u, f, vp, vp, vp, vp, vp,
+                                      i, i, vp, sz, vp, vp]
+    lib.la_chunk_fwd_host.restype = i
     lib.la_debug_set.argtypes = [i, i]
     lib.la_debug_set.restype = i
     lib.la_trace_enable.argtypes = [i]
@@ -459,89 +464,85 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
     return dq, dk, dv, dS0, dz0
 
 
-_SIDE_STREAMS: dict = {}
-
-
-def _side_streams(device, n: int):
-    key = (str(device), n)
-    if key not in _SIDE_STREAMS:
-        _SIDE_STREAMS[key] = [torch.cuda.Stream(device=device) for _ in range(n)]
-    return _SIDE_STREAMS[key]
+def host_arena_size(B, H, T, dk, dv, dtype=torch.bfloat16, phi=False, normalize=False,
+                    causal=True, chunk=0, pieces=1, floor=False) -> int:
+    """Device bytes la_chunk_fwd_host needs for its two slots (la_host_arena_size)."""
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(_load().la_host_arena_size(B, H, T, dk, dv, code, _flags(phi, normalize, causal, floor),
+                                          chunk, pieces))
 
 
 def chunk_fwd_host(q, k, v, gamma, *, phi=False, normalize=False, causal=True, eps=1e-6,
                    S0=None, z0=None, chunk=0, pieces=None, out=None, S_out=None, z_out=None,
-                   device="cuda", timing=None):
-    """la_chunk_fwd on HOST tensors: copy in, compute, copy the results back.
+                   device="cuda", timing=None, arena=None, floor=False):
+    """la_chunk_fwd_host: the chunkwise forward on HOST tensors, copies included.
 
-    q, k, v (and S0, z0) are CPU tensors, pinned for asynchronous copies.  With
-    `pieces` > 1 the batch is cut into that many groups of whole sequences and
-    each group's copy in, la_chunk_fwd and copy out run in order on one of two
-    side streams, so the copies of one group overlap the compute of another
-    (default 1: one pass on the current stream).
-    Returns host (O, S_T, z_T) (z_T when normalising or when z_out is given),
-    written into out / S_out / z_out when those pinned buffers are passed.
-    With `timing` (a list), the device milliseconds from before the first copy
-    to after the last are appended to it.  Synchronises before returning.
+    q, k, v (and S0, z0) are CPU tensors, pinned for asynchronous copies.  The
+    library cuts the batch into `pieces` groups of whole sequences (default: one
+    per batch row, at most 8) and pipelines each group's copy in, forward and copy
+    out over two streams.  `arena` (a uint8 device tensor of host_arena_size(...)
+    bytes) is allocated here when not given.  Returns host (O, S_T, z_T) (z_T when
+    normalising or when z_out is given), written into out / S_out / z_out when
+    those pinned buffers are passed.  With `timing` (a list), the device
+    milliseconds from before the first copy to after the last are appended to it.
+    Synchronises before returning.
     """
+    normalize = normalize or floor
     B, H, T, dk = q.shape
     dv = v.shape[-1]
-    n = max(1, min(B, pieces if pieces else 1))
-    bounds = [(i * B) // n for i in range(n + 1)]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for name, t in (("q", q), ("k", k), ("v", v), ("S0", S0), ("z0", z0), ("out", out),
+                    ("S_out", S_out), ("z_out", z_out)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host tensor")
     dev = torch.device(device)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     pin = dict(pin_memory=True)
+    ds = state_rows(dk, phi)
     if out is None:
         out = torch.empty((B, H, T, dv), dtype=q.dtype, **pin)
-    ds = state_rows(dk, phi)
     if S_out is None:
         S_out = torch.empty((B, H, ds, dv), dtype=torch.float32, **pin)
     if z_out is None and normalize:
         z_out = torch.empty((B, H, ds), dtype=torch.float32, **pin)
-    qd = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    kd = torch.empty(k.shape, dtype=k.dtype, device=dev)
-    vd = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    Od = torch.empty(out.shape, dtype=out.dtype, device=dev)
-    Sd = torch.empty(S_out.shape, dtype=torch.float32, device=dev)
-    zd = torch.empty(z_out.shape, dtype=torch.float32, device=dev) if z_out is not None else None
-    S0d = torch.empty(S0.shape, dtype=torch.float32, device=dev) if S0 is not None else None
-    z0d = torch.empty(z0.shape, dtype=torch.float32, device=dev) if z0 is not None else None
-    main = torch.cuda.current_stream(dev)
-    sides = _side_streams(dev, 2) if n > 1 else [main]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(main)
-    for st in sides:
-        if st is not main:
-            st.wait_event(start)
-    for i in range(n):
-        b0, b1 = bounds[i], bounds[i + 1]
-        if b0 == b1:
-            continue
-        st = sides[i % 2]
-        with torch.cuda.stream(st):
-            for d, h in ((qd, q), (kd, k), (vd, v), (S0d, S0), (z0d, z0)):
-                if d is not None:
-                    d[b0:b1].copy_(h[b0:b1], non_blocking=True)
-            chunk_fwd(qd[b0:b1], kd[b0:b1], vd[b0:b1], gamma, phi=phi, normalize=normalize,
-                      causal=causal, eps=eps,
-                      S0=None if S0d is None else S0d[b0:b1],
-                      z0=None if z0d is None else z0d[b0:b1], chunk=chunk, out=Od[b0:b1],
-                      S_out=Sd[b0:b1], z_out=None if zd is None else zd[b0:b1], stream=st)
-            out[b0:b1].copy_(Od[b0:b1], non_blocking=True)
-            S_out[b0:b1].copy_(Sd[b0:b1], non_blocking=True)
-            if zd is not None:
-                z_out[b0:b1].copy_(zd[b0:b1], non_blocking=True)
-    for st in sides:
-        if st is not main:
-            main.wait_stream(st)
-    end.record(main)
-    end.synchronize()
+    host = torch.device("cpu")
+    _buffer(out, "out", B * H * T * dv, q.dtype, host)
+    _states(B, H, ds, dv, host, S0=S0, z0=z0, S_out=S_out, z_out=z_out)
+    n = max(1, min(B, pieces if pieces else min(B, 8)))
+    dt = _dtype_code(q)
+    flags = _flags(phi, normalize, causal, floor)
+    lib = _load()
+    g = _gamma_host(gamma, H)
+    with torch.cuda.device(dev):
+        need = int(lib.la_host_arena_size(B, H, T, dk, dv, dt, flags, int(chunk), n))
+        if arena is None:
+            arena = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        _buffer(arena, "arena", need, torch.uint8, dev)
+        stream = torch.cuda.current_stream(dev)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        st = lib.la_chunk_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), dt, g.ctypes.data, B, H,
+                                   T, dk, dv, flags, float(eps),
+                                   None if S0 is None else S0.data_ptr(),
+                                   None if z0 is None else z0.data_ptr(), out.data_ptr(),
+                                   S_out.data_ptr(), None if z_out is None else z_out.data_ptr(),
+                                   int(chunk), n, arena.data_ptr(), arena.numel(), None,
+                                   stream.cuda_stream or None)
+        end.record(stream)
+        end.synchronize()
+    _check(st, "la_chunk_fwd_host")
     if timing is not None:
         timing.append(start.elapsed_time(end))
     return out, S_out, z_out
 
 
 __all__ = ["chunk_fwd", "chunk_bwd", "chunk_fwd_noalloc", "recurrent_step", "state_init", "workspace_size", "chunk_fwd_host",
+           "host_arena_size",
            "trace_enable", "trace_collect", "debug_set", "debug_options",
            "library", "status_string", "abi_version", "LinAttnError", "LA_PHI_ELU1",
            "LA_NORMALIZE", "LA_NONCAUSAL", "LA_NORM_FLOOR", "LA_GATED", "LA_PHI_TAYLOR", "state_rows"]

@@ -1,6 +1,7 @@
 // The exported C ABI of liblinattn.so (declared in include/linattn.h):
 // argument checks on the host, then asynchronous launches on the caller's
 // stream.  Nothing is launched or written when a check fails.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -155,12 +156,14 @@ la_status la_state_init(float* S, float* z, int B, int H, int d_k, int d_v, la_s
 namespace {
 
 // la_chunk_fwd and la_chunk_fwd_gated: exactly one of gamma (host [H]) and log_a
-// (device [B][H][T]) is given.
+// (device [B][H][T]) is given.  check_only: return after the checks, launching
+// nothing.
 la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
                     const float* gamma, const float* log_a, int B, int H, int T, int d_k,
                     int d_v, unsigned flags, float eps, const float* S0, const float* z0,
                     void* O, float* S_out, float* z_out, int chunk, void* workspace,
-                    size_t workspace_bytes, int* dev_status, la_stream_t stream) {
+                    size_t workspace_bytes, int* dev_status, la_stream_t stream,
+                    bool check_only = false) {
     const bool gated = gamma == nullptr;
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
@@ -210,6 +213,7 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     const size_t ds = taylor ? (size_t)taylor_feature_dim(d_k) : (size_t)d_k;  // state rows
     const size_t nS = nbh * ds * d_v, nz = nbh * ds;
     if (T == 0) {  // empty sequence: the final state is the initial one
+        if (check_only) return LA_OK;
         cudaError_t e = cudaSuccess;
         if (S_out) e = S0 ? launch_state_copy(S_out, S0, nS, s) : launch_state_zero(S_out, nullptr, nS, 0, s);
         if (e == cudaSuccess && z_out)
@@ -239,14 +243,14 @@ la_status chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dtype,
     const bool want_tc = opt_path() == 2;
     if (taylor) {  // its own tensor-core kernel; no CUDA-core version
         if (want_simt || !taylor_supported(a)) return LA_ERR_UNSUPPORTED;
-        return cuda_status(launch_chunk_taylor(a, g, s));
+        return check_only ? LA_OK : cuda_status(launch_chunk_taylor(a, g, s));
     }
     if (!want_simt && tc_supported(a)) {
         int launches = 0;
-        return cuda_status(launch_chunk_tc(a, g, s, &launches));
+        return check_only ? LA_OK : cuda_status(launch_chunk_tc(a, g, s, &launches));
     }
     if (want_tc) return LA_ERR_UNSUPPORTED;
-    return cuda_status(launch_chunk_simt(a, g, s));
+    return check_only ? LA_OK : cuda_status(launch_chunk_simt(a, g, s));
 }
 
 la_status recurrent_step(const void* q, const void* k, const void* v, la_dtype dtype,
@@ -411,6 +415,146 @@ la_status la_chunk_fwd(const void* Q, const void* K, const void* V, la_dtype dty
     if (!gamma) gamma = &kOneGamma;  // B or H == 0 (or negative: rejected below)
     return chunk_fwd(Q, K, V, dtype, gamma, nullptr, B, H, T, d_k, d_v, flags, eps, S0, z0, O,
                      S_out, z_out, chunk, workspace, workspace_bytes, dev_status, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The device arena of la_chunk_fwd_host: two slots (double buffering), each with
+// one piece's Q, K, V, O, S0, z0, S_out, z_out and chunk workspace; byte offsets
+// within a slot, every region 256-byte aligned.  A piece has at most bmax
+// sequences of the batch (pieces of floor or ceil(B / pieces) rows).
+struct HostPlan {
+    int bmax;
+    size_t o_q, o_k, o_v, o_o, o_s0, o_z0, o_so, o_zo, o_ws, ws, slot, bytes;
+};
+
+bool host_plan(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags, int chunk,
+               int pieces, HostPlan* hp) {
+    std::memset(hp, 0, sizeof(*hp));
+    if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return false;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return false;
+    if (B > 0 && (pieces < 1 || pieces > B)) return false;
+    if (B == 0) return true;
+    const int bmax = (B + pieces - 1) / pieces, bmin = B / pieces;
+    const size_t es = elem_size(dtype);
+    const size_t ds = (flags & LA_PHI_TAYLOR) ? (size_t)taylor_feature_dim(d_k) : (size_t)d_k;
+    const size_t nbh = (size_t)bmax * H;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) / 256 * 256;
+        return o;
+    };
+    hp->bmax = bmax;
+    hp->o_q = take(nbh * T * d_k * es);
+    hp->o_k = take(nbh * T * d_k * es);
+    hp->o_v = take(nbh * T * d_v * es);
+    hp->o_o = take(nbh * T * d_v * es);
+    hp->o_s0 = take(nbh * ds * d_v * 4);
+    hp->o_z0 = take(nbh * ds * 4);
+    hp->o_so = take(nbh * ds * d_v * 4);
+    hp->o_zo = take(nbh * ds * 4);
+    // the smaller pieces can have a plan of their own (more segments per sequence)
+    hp->ws = std::max(la_workspace_size(bmax, H, T, d_k, d_v, dtype, flags, chunk),
+                      bmin > 0 ? la_workspace_size(bmin, H, T, d_k, d_v, dtype, flags, chunk) : 0);
+    hp->o_ws = take(hp->ws);
+    hp->slot = off;
+    hp->bytes = 2 * off;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t la_host_arena_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype, unsigned flags,
+                          int chunk, int pieces) {
+    HostPlan hp;
+    return host_plan(B, H, T, d_k, d_v, dtype, flags, chunk, pieces, &hp) ? hp.bytes : 0;
+}
+
+la_status la_chunk_fwd_host(const void* Q, const void* K, const void* V, la_dtype dtype,
+                            const float* gamma, int B, int H, int T, int d_k, int d_v,
+                            unsigned flags, float eps, const float* S0, const float* z0, void* O,
+                            float* S_out, float* z_out, int chunk, int pieces, void* arena,
+                            size_t arena_bytes, int* dev_status, la_stream_t stream) {
+    HostPlan hp;
+    if (!host_plan(B, H, T, d_k, d_v, dtype, flags, chunk, pieces, &hp)) return LA_ERR_INVALID_ARG;
+    if ((size_t)B * H == 0 || B <= 0 || H <= 0) return LA_OK;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    if (T > 0 && (!Q || !K || !V || !O)) return LA_ERR_INVALID_ARG;
+    if (!arena || !aligned16(arena) || arena_bytes < hp.bytes) return LA_ERR_INVALID_ARG;
+    char* slot[2] = {static_cast<char*>(arena), static_cast<char*>(arena) + hp.slot};
+    auto dev = [&](int sl, size_t o) { return static_cast<void*>(slot[sl] + o); };
+    // every check of the per-piece calls, before anything is enqueued
+    la_status st = chunk_fwd(dev(0, hp.o_q), dev(0, hp.o_k), dev(0, hp.o_v), dtype, gamma, nullptr,
+                             hp.bmax, H, T, d_k, d_v, flags, eps,
+                             S0 ? (const float*)dev(0, hp.o_s0) : nullptr,
+                             z0 ? (const float*)dev(0, hp.o_z0) : nullptr, dev(0, hp.o_o),
+                             S_out ? (float*)dev(0, hp.o_so) : nullptr,
+                             z_out ? (float*)dev(0, hp.o_zo) : nullptr, chunk, dev(0, hp.o_ws),
+                             hp.ws, dev_status, stream, /*check_only=*/true);
+    if (st != LA_OK) return st;
+
+    const size_t es = elem_size(dtype);
+    const size_t ds = (flags & LA_PHI_TAYLOR) ? (size_t)taylor_feature_dim(d_k) : (size_t)d_k;
+    const size_t row_qk = (size_t)H * T * d_k * es, row_v = (size_t)H * T * d_v * es;
+    const size_t row_s = (size_t)H * ds * d_v * 4, row_z = (size_t)H * ds * 4;
+    cudaStream_t main = (cudaStream_t)stream;
+    cudaStream_t ss[2] = {nullptr, nullptr};
+    cudaEvent_t start = nullptr, done[2] = {nullptr, nullptr};
+    cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
+        e = cudaStreamCreateWithFlags(&ss[j], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done[j], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(start, main);
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(ss[j], start, 0);
+    // piece i: copy in, forward, copy out, in order on stream i mod 2 (slot i mod 2),
+    // so piece i + 1's copies overlap piece i's compute and slot reuse is ordered
+    for (int i = 0; i < pieces && e == cudaSuccess && st == LA_OK; ++i) {
+        const int b0 = (int)(((long long)i * B) / pieces), b1 = (int)(((long long)(i + 1) * B) / pieces);
+        const int b = b1 - b0, sl = i & 1;
+        cudaStream_t s = ss[sl];
+        auto h2d = [&](size_t o, const void* src, size_t row) {
+            if (e == cudaSuccess && src)
+                e = cudaMemcpyAsync(dev(sl, o), static_cast<const char*>(src) + (size_t)b0 * row,
+                                    (size_t)b * row, cudaMemcpyHostToDevice, s);
+        };
+        auto d2h = [&](void* dst, size_t o, size_t row) {
+            if (e == cudaSuccess && dst)
+                e = cudaMemcpyAsync(static_cast<char*>(dst) + (size_t)b0 * row, dev(sl, o),
+                                    (size_t)b * row, cudaMemcpyDeviceToHost, s);
+        };
+        h2d(hp.o_q, Q, row_qk);
+        h2d(hp.o_k, K, row_qk);
+        h2d(hp.o_v, V, row_v);
+        h2d(hp.o_s0, S0, row_s);
+        h2d(hp.o_z0, z0, row_z);
+        if (e != cudaSuccess) break;
+        st = chunk_fwd(dev(sl, hp.o_q), dev(sl, hp.o_k), dev(sl, hp.o_v), dtype, gamma, nullptr, b, H,
+                       T, d_k, d_v, flags, eps, S0 ? (const float*)dev(sl, hp.o_s0) : nullptr,
+                       z0 ? (const float*)dev(sl, hp.o_z0) : nullptr, dev(sl, hp.o_o),
+                       S_out ? (float*)dev(sl, hp.o_so) : nullptr,
+                       z_out ? (float*)dev(sl, hp.o_zo) : nullptr, chunk, dev(sl, hp.o_ws), hp.ws,
+                       dev_status, (la_stream_t)s);
+        d2h(O, hp.o_o, row_v);
+        d2h(S_out, hp.o_so, row_s);
+        d2h(z_out, hp.o_zo, row_z);
+    }
+    // the caller's stream waits for both pipelines; the streams and events are
+    // released once their work completes
+    for (int j = 0; j < 2; ++j) {
+        if (ss[j] && done[j] && cudaEventRecord(done[j], ss[j]) == cudaSuccess)
+            cudaStreamWaitEvent(main, done[j], 0);
+        if (done[j]) cudaEventDestroy(done[j]);
+        if (ss[j]) cudaStreamDestroy(ss[j]);
+    }
+    if (start) cudaEventDestroy(start);
+    if (st != LA_OK) return st;
+    return cuda_status(e);
 }
 
 la_status la_chunk_fwd_gated(const void* Q, const void* K, const void* V, la_dtype dtype,

@@ -95,6 +95,31 @@ def test_library_reads_no_environment():
         assert "getenv" not in text, f
 
 
+def test_host_entry_point_sizes_and_rejections(lib):
+    """la_host_arena_size and la_chunk_fwd_host's host checks (nothing is enqueued
+    when they fail; the pointers below are never touched)."""
+    n2 = lib.la_host_arena_size(4, 8, 64, 64, 64, 1, 0, 0, 2)
+    assert n2 > 0
+    assert lib.la_host_arena_size(4, 8, 64, 64, 64, 1, 0, 0, 5) == 0  # pieces > B
+    assert lib.la_host_arena_size(4, 8, 64, 64, 64, 1, 0, 0, 0) == 0
+    assert lib.la_host_arena_size(4, 8, 64, 64, 64, 1, 0, 0, 1) > n2 > lib.la_host_arena_size(
+        4, 8, 64, 64, 64, 1, 0, 0, 4)
+
+    def call(**over):
+        a = dict(Q=FAKE, K=FAKE, V=FAKE, gamma=GAM.ctypes.data, O=FAKE, pieces=2, arena=FAKE,
+                 arena_bytes=n2)
+        a.update(over)
+        return lib.la_chunk_fwd_host(a["Q"], a["K"], a["V"], 1, a["gamma"], 4, 8, 64, 64, 64, 0,
+                                     1e-6, None, None, a["O"], None, None, 0, a["pieces"],
+                                     a["arena"], a["arena_bytes"], None, None)
+
+    for over in (dict(pieces=5), dict(pieces=0), dict(Q=None), dict(O=None), dict(gamma=None),
+                 dict(arena_bytes=n2 - 1), dict(arena=FAKE + 8), dict(arena=None)):
+        assert call(**over) == la.LA_ERR_INVALID_ARG, over
+    bad = np.full(8, 1.5, dtype=np.float32)
+    assert call(gamma=bad.ctypes.data) == la.LA_ERR_INVALID_ARG
+
+
 def chunk(lib, **over):
     a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dtype=1, gamma=GAM.ctypes.data, B=2,
              H=8, T=64, dk=64, dv=64, flags=0, eps=1e-6, S0=None, z0=None, O=FAKE + 0x400000,

@@ -265,11 +265,17 @@ def test_retention_floor_bf16_full():
     check("z_T", np64(z), zr, TOL["bf16"])
 
 
+def _edge_pairs(B, H, n_pairs):
+    """A seeded sample of (b, h) sequences plus the corners of the batch: the last
+    batch row and the last head are where the last CTAs of the grid land."""
+    return sorted(set(workloads.sample_pairs(B, H, n_pairs)) | {(0, H - 1), (B - 1, 0), (B - 1, H - 1)})
+
+
 def _sampled_workload(name, n_pairs, causal=True):
     c = workloads.CONFIGS[name]
     x = workloads.make_inputs(c)
     gq = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
-    pairs = workloads.sample_pairs(c["B"], c["H"], n_pairs)
+    pairs = _edge_pairs(c["B"], c["H"], n_pairs)
     O, S, _ = la.chunk_fwd(*gq, x["gamma"], phi=c["phi"], normalize=c["normalize"],
                            causal=causal)
     torch.cuda.synchronize()
@@ -315,7 +321,7 @@ def test_decode_bf16_sampled():
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     _, S, _ = la.chunk_fwd(q, k, v, x["gamma"])
     del q, k, v
-    pairs = workloads.sample_pairs(c["B"], c["H"], 6)
+    pairs = _edge_pairs(c["B"], c["H"], 6)
     bi = [p[0] for p in pairs]
     hi = [p[1] for p in pairs]
     steps = c["decode_steps"]
@@ -339,7 +345,7 @@ def test_decode_bf16_sampled():
     check("final state", S[bi, hi].double().cpu().numpy(), Sr[0], TOL["bf16"])
 
 
-@pytest.mark.parametrize("pieces", [1, 3])
+@pytest.mark.parametrize("pieces", [1, 2, 3])
 def test_host_entry_point_pipelined(pieces):
     """chunk_fwd_host: pinned host inputs in, host results out, batch split over
     two side streams; equals the oracle (initial state included)."""
@@ -357,3 +363,14 @@ def test_host_entry_point_pipelined(pieces):
     check("O", np64(O), Or, TOL["bf16"])
     check("S_T", np64(S), Sr, TOL["bf16"])
     check("z_T", np64(z), zr, TOL["bf16"])
+
+
+def test_host_entry_point_plain_retention_segments():
+    """la_chunk_fwd_host on plain retention (the factored-decay build) with few
+    sequences, so each piece's plan cuts its sequences into segments."""
+    x = workloads.random_case(93, 2, 2, 3000, 128, 128, dtype="bf16")
+    O, S, _ = la.chunk_fwd_host(x["q"].pin_memory(), x["k"].pin_memory(), x["v"].pin_memory(),
+                                x["gamma"], pieces=2)
+    Or, Sr, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["gamma"])
+    check("O", np64(O), Or, TOL["bf16"])
+    check("S_T", np64(S), Sr, TOL["bf16"])
