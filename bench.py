@@ -49,6 +49,10 @@ KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "t
                   "chunk_tc.cu", "common.cuh", "launch.h")
 TRAFFIC = {
     # (workload, kernel): bytes per launch
+    ("msr_retention_bf16", "chunk_tc_ws_kernel/full"): {
+        "bytes": 1_074_105_344 + 521_304_576,
+        "sources_sha256": "739e2496313f5f5f824747fa49cc056924ca6e548359a983e6c5f8f2c055b99d",
+    },
 }
 HEADLINE = "msr_retention_bf16"
 # the prefill workloads timed beside the headline
