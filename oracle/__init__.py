@@ -37,6 +37,9 @@ taylor_features(x), recurrent_taylor(q, k, v, gamma, normalize, ...)
     The second-order Taylor feature map phi(x) = (1, x, vec(x x^T)/sqrt(2)) of
     the "Linear attention" page (box "Taylor features"), and ``recurrent`` on
     the features it gives (d_phi = 1 + d + d^2; d = 16 gives 273).
+taylor_features_bwd(x, dfeat), recurrent_bwd_taylor(q, k, v, gamma, dO, ...)
+    The map's transpose Jacobian, and the gradients of ``recurrent_taylor``:
+    ``recurrent_bwd`` on the features, then the chain rule through the map.
 noncausal(q, k, v, phi, normalize, eps)
     gamma = 1, every query reads the one summary phi(K)^T V: box "Linear
     attention" on the "Linear attention" page.
@@ -81,6 +84,8 @@ def _load(path: str | None = None):
     lib.oracle_noncausal.restype = ctypes.c_int
     lib.oracle_taylor_features.argtypes = [dp, L, L, dp]
     lib.oracle_taylor_features.restype = None
+    lib.oracle_taylor_features_bwd.argtypes = [dp, dp, L, L, dp]
+    lib.oracle_taylor_features_bwd.restype = None
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
@@ -265,10 +270,37 @@ def recurrent_taylor(q, k, v, gamma, normalize: bool = False, eps: float = 1e-6,
                      _lib=_lib, floor=floor)
 
 
+def taylor_features_bwd(x, dfeat, _lib=None):
+    """The gradient with respect to x of a loss whose gradient with respect to the
+    Taylor features of x is ``dfeat`` ([..., 1 + d + d^2] -> [..., d]): the chain
+    rule through (1, x, vec(x x^T) / sqrt(2))."""
+    X = np.ascontiguousarray(_f64(x))
+    d = X.shape[-1]
+    n = int(np.prod(X.shape[:-1]))
+    G = np.ascontiguousarray(_f64(dfeat)).reshape(n, 1 + d + d * d)
+    out = np.empty(X.shape)
+    (_lib or lib()).oracle_taylor_features_bwd(_ptr(X), _ptr(G), n, d, _ptr(out))
+    return out
+
+
+def recurrent_bwd_taylor(q, k, v, gamma, dO, normalize: bool = False, eps: float = 1e-6,
+                         S0=None, z0=None, dS_T=None, dz_T=None, _lib=None, floor: bool = False):
+    """Gradients of ``recurrent_taylor`` for the loss sum(dO * O) + <dS_T, S_T> +
+    <dz_T, z_T>: ``recurrent_bwd`` on the features (phi = identity, d_phi rows),
+    then the chain rule through the feature map for q and k.  Returns (dq, dk, dv,
+    dS0, dz0); dS0 and dz0 have the features' rows."""
+    fq, fk = taylor_features(q, _lib), taylor_features(k, _lib)
+    dfq, dfk, dv, dS0, dz0 = recurrent_bwd(fq, fk, v, gamma, dO, phi=False, normalize=normalize,
+                                           eps=eps, S0=S0, z0=z0, dS_T=dS_T, dz_T=dz_T,
+                                           _lib=_lib, floor=floor)
+    return (taylor_features_bwd(q, dfq, _lib), taylor_features_bwd(k, dfk, _lib), dv, dS0, dz0)
+
+
 def load_mutant(mutant: int, out_dir: str):
     """Load a build of the oracle with a planted mistake (for pin tests only)."""
     return _load(_build.build_mutant(mutant, out_dir))
 
 
-__all__ = ["recurrent", "recurrent_taylor", "taylor_features", "decode_step", "noncausal",
+__all__ = ["recurrent", "recurrent_taylor", "taylor_features", "taylor_features_bwd",
+           "recurrent_bwd_taylor", "decode_step", "noncausal",
            "num_threads", "load_mutant", "lib"]

@@ -485,6 +485,36 @@ void oracle_taylor_features(const double* X, long n, long d, double* out)
     }
 }
 
+/*
+ * The feature map's transpose Jacobian: given dF = dL/dphi(x) for every row, the
+ * gradient dL/dx of the same map (1, x, vec(x x^T) / sqrt(2)) by the chain rule:
+ * x_c appears in the linear feature c and in the outer product's entries (c, j)
+ * and (i, c), each x_i x_j / sqrt(2), so
+ *
+ *   dX_c = dF_(1+c) + (1/sqrt 2) sum_j (dF_(1+d+c*d+j) + dF_(1+d+j*d+c)) x_j.
+ *
+ *   X : [n][d]     dF : [n][1 + d + d*d]     dX : [n][d]
+ */
+void oracle_taylor_features_bwd(const double* X, const double* dF, long n, long d, double* dX)
+{
+    const long df = 1 + d + d * d;
+    const double r = 1.0 / sqrt(2.0);
+    for (long t = 0; t < n; ++t) {
+        const double* x = X + t * d;
+        const double* g = dF + t * df;
+        for (long c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (long j = 0; j < d; ++j)
+#if ORACLE_MUTANT == 19 /* mutant: only the row of the outer product */
+                acc += g[1 + d + c * d + j] * x[j];
+#else
+                acc += (g[1 + d + c * d + j] + g[1 + d + j * d + c]) * x[j];
+#endif
+            dX[t * d + c] = g[1 + c] + r * acc;
+        }
+    }
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -465,13 +465,40 @@ def pin_taylor_attention(lib=None):
         np.testing.assert_allclose(z[0, h, 0], w.sum(), rtol=1e-12)
 
 
+def pin_taylor_backward_by_differences(lib=None):
+    """The Taylor map's gradients (q, k through the feature map, v, the initial state
+    of the features' rows) against central differences of the forward oracle with
+    the map, normalised and with a per-head decay."""
+    rng = _rng(63)
+    B, H, T, d, dv = 1, 2, 6, 2, 3
+    df = 1 + d + d * d
+    q = rng.standard_normal((B, H, T, d)) * 0.7
+    k = rng.standard_normal((B, H, T, d)) * 0.7
+    v = rng.standard_normal((B, H, T, dv))
+    S0 = rng.standard_normal((B, H, df, dv)) * 0.3
+    z0 = np.abs(rng.standard_normal((B, H, df))) + 0.5
+    W = rng.standard_normal((B, H, T, dv))
+    WS = rng.standard_normal((B, H, df, dv))
+    Wz = rng.standard_normal((B, H, df))
+    gamma = np.array([1.0, 0.93])
+
+    def loss(q_, k_, v_, S0_, z0_):
+        O, S, z = oracle.recurrent_taylor(q_, k_, v_, gamma, normalize=True, S0=S0_, z0=z0_,
+                                          _lib=lib)
+        return float((W * O).sum() + (WS * S).sum() + (Wz * z).sum())
+    grads = oracle.recurrent_bwd_taylor(q, k, v, gamma, W, normalize=True, S0=S0, z0=z0,
+                                        dS_T=WS, dz_T=Wz, _lib=lib)
+    _check_by_differences(loss, [q, k, v, S0, z0], grads)
+
+
 ALL_PINS = [pin_hand_example, pin_parallel_form, pin_masked_kernel_theorem,
             pin_geometric_series, pin_iir_filter, pin_noncausal_orders,
             pin_associative_memory, pin_orthonormal_keys, pin_normalised_invariants,
             pin_chunkwise_invariance, pin_state_handoff, pin_floor_clamped_rows,
             pin_floor_limits, pin_gated_parallel_form, pin_gated_constant_is_gamma,
             pin_gated_reset, pin_gated_chunkwise, pin_backward_by_differences,
-            pin_taylor_pair, pin_taylor_kernel_theorem, pin_taylor_attention]
+            pin_taylor_pair, pin_taylor_kernel_theorem, pin_taylor_attention,
+            pin_taylor_backward_by_differences]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -560,6 +587,7 @@ MUTANTS = {
     16: "dk without the chain rule through phi",
     17: "Taylor features without the constant",
     18: "Taylor features without the linear part",
+    19: "Taylor map's gradient with one half of the outer product",
 }
 
 
