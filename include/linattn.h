@@ -101,7 +101,8 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
  * rows in the order of phi above.  la_chunk_fwd (and la_workspace_size,
  * la_chunk_fwd_launches, la_chunk_fwd_noalloc): bf16, d_v a multiple of 64, chunk
  * 0 or 128, an sm_103 device.  la_recurrent_step: bf16 or fp32, d_v <= 256.
- * Other calls and shapes answer LA_ERR_UNSUPPORTED. */
+ * la_chunk_bwd: bf16 or fp32, d_v <= 128, per-head decay.  Other calls and
+ * shapes answer LA_ERR_UNSUPPORTED. */
 #define LA_PHI_TAYLOR 32u
 
 /* Human-readable text of a status code (static storage, never NULL). */
@@ -274,7 +275,13 @@ LA_API la_status la_recurrent_step_gated(const void* q, const void* k, const voi
  *   workspace: at least la_bwd_workspace_size(...) bytes (per-token
  *          denominators when normalising; 0 otherwise)
  * d_k and d_v must be at most 128 (LA_ERR_UNSUPPORTED otherwise).  The
- * computation runs in fp32 on the CUDA cores.  Errors as la_chunk_fwd.
+ * computation runs in fp32 on the CUDA cores (bf16 calls with per-head decay,
+ * no feature map and no normaliser on the tensor cores).
+ * LA_PHI_TAYLOR: the Taylor feature map as in la_chunk_fwd (d_k = 16, not with
+ * LA_PHI_ELU1, not with per-token decays); S0, z0, dS_T, dz_T, dS0 and dz0 then
+ * have 1 + d_k + d_k^2 = 273 rows in the map's order, and dQ, dK are the
+ * gradients of the raw 16-wide q and k (through the map's transpose Jacobian).
+ * Errors as la_chunk_fwd.
  */
 LA_API la_status la_chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
                               la_dtype dtype, const float* gamma, int B, int H, int T, int d_k,

@@ -418,7 +418,8 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
 
     q, k, v, gamma (or log_a), the flags and S0, z0 as in the forward call; dO
     [B,H,T,dv] like v.  Returns (dq, dk, dv, dS0, dz0); dS0 / dz0 are None when
-    state_grads is False (dz0 also without the normaliser)."""
+    state_grads is False (dz0 also without the normaliser).  phi="taylor": the
+    Taylor feature map (d = 16; the states and their gradients have 273 rows)."""
     normalize = normalize or floor
     B, H, T, dk_ = q.shape
     dv_ = v.shape[-1]
@@ -434,15 +435,16 @@ def chunk_bwd(q, k, v, dO, gamma=None, *, phi=False, normalize=False, eps=1e-6, 
     if log_a is not None and (log_a.dtype != torch.float32 or tuple(log_a.shape) != (B, H, T)):
         raise ValueError(f"log_a must be float32 [B,H,T] = {(B, H, T)}")
     _buffer(log_a, "log_a", B * H * T, torch.float32, dev)
-    _states(B, H, dk_, dv_, dev, S0=S0, z0=z0, dS_T=dS_T, dz_T=dz_T)
+    ds = state_rows(dk_, phi)
+    _states(B, H, ds, dv_, dev, S0=S0, z0=z0, dS_T=dS_T, dz_T=dz_T)
     _buffer(dq, "dq", B * H * T * dk_, q.dtype, dev)
     _buffer(dk, "dk", B * H * T * dk_, q.dtype, dev)
     _buffer(dv, "dv", B * H * T * dv_, q.dtype, dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    dS0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=dev) if state_grads else None
-    dz0 = (torch.empty((B, H, dk_), dtype=torch.float32, device=dev)
+    dS0 = torch.empty((B, H, ds, dv_), dtype=torch.float32, device=dev) if state_grads else None
+    dz0 = (torch.empty((B, H, ds), dtype=torch.float32, device=dev)
            if state_grads and normalize else None)
     flags = _flags(phi, normalize, True, floor)
     lib = _load()

@@ -95,6 +95,7 @@ BwdArgs bwd_plan_args(int B, int H, int T, int d_k, int d_v, la_dtype dtype, uns
     a.floor_norm = (flags & LA_NORM_FLOOR) != 0;
     a.normalize = (flags & LA_NORMALIZE) != 0 || a.floor_norm;
     a.log_a = gated ? &kMarker : nullptr;
+    a.taylor = (flags & LA_PHI_TAYLOR) != 0;
     return a;
 }
 
@@ -309,10 +310,12 @@ la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
                     float* dS0, float* dz0, void* workspace, size_t workspace_bytes,
                     la_stream_t stream) {
     const bool gated = gamma == nullptr;
-    if (flags & LA_PHI_TAYLOR) return LA_ERR_UNSUPPORTED;
+    const bool taylor = (flags & LA_PHI_TAYLOR) != 0;
     if (B < 0 || H < 0 || T < 0 || !valid_dim(d_k) || !valid_dim(d_v)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
-    if (flags & ~(kCallFlags | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    if (flags & ~(kCallFlags | LA_PHI_TAYLOR | (gated ? LA_GATED : 0u))) return LA_ERR_INVALID_ARG;
+    // the Taylor map: 16-wide q and k, per-head decay, not with elu + 1
+    if (taylor && (gated || d_k != 16 || (flags & LA_PHI_ELU1))) return LA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return LA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
     const size_t nbh = (size_t)B * H;
@@ -363,6 +366,7 @@ la_status chunk_bwd(const void* Q, const void* K, const void* V, const void* dO,
     a.floor_norm = floor_norm;
     a.eps = eps;
     a.log_a = gated ? log_a : nullptr;
+    a.taylor = taylor;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     if (T > 0 && !simt_pinned() && bwd_tc_supported(a))
@@ -376,9 +380,8 @@ extern "C" {
 
 size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype dtype,
                              unsigned flags) {
-    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || (flags & LA_PHI_TAYLOR) || d_k > 128 ||
-        d_v > 128)
-        return 0;
+    if (!plan_ok(B, H, T, d_k, d_v, dtype, flags) || d_k > 128 || d_v > 128) return 0;
+    if ((flags & LA_PHI_TAYLOR) && (d_k != 16 || (flags & (LA_PHI_ELU1 | LA_GATED)))) return 0;
     return bwd_bytes_for(bwd_plan_args(B, H, T, d_k, d_v, dtype, flags, (flags & LA_GATED) != 0));
 }
 

@@ -68,10 +68,13 @@ struct BwdSeg {
 };
 
 struct BwdSmem {  // offsets in floats
-    int q, k, v, g, n, a, p, s, z, den, du, pw, cum, xw, total;
+    int q, k, v, g, n, a, p, s, z, den, du, pw, cum, xw, tq, total;
 };
 
-__host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv) {
+// dk: the state's rows (the feature dimension: 1 + d + d^2 with the Taylor map);
+// with the Taylor map a [C][dk + 1] buffer holds the gradient of a chunk's features
+// before the chain rule takes it back to the raw d columns.
+__host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv, bool taylor = false) {
     BwdSmem L;
     const int ldk = dk + 1, ldv = dv + 1, lda = C + 1;
     L.q = 0;
@@ -88,7 +91,8 @@ __host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv) {
     L.pw = L.du + C;
     L.cum = L.pw + C + 2;
     L.xw = L.cum + C;
-    L.total = L.xw + C;
+    L.tq = L.xw + C;
+    L.total = L.tq + (taylor ? C * ldk : 0);
     return L;
 }
 
@@ -100,9 +104,9 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     T* __restrict__ dK, T* __restrict__ dV, float* __restrict__ dS0, float* __restrict__ dz0,
     float* __restrict__ stats, int H, int T_len, int dk, int dv, int C, int phi, int normalize,
     float eps, int role0, const float* __restrict__ log_a, const __grid_constant__ KernelGammas g,
-    const __grid_constant__ BwdSeg sg) {
+    const __grid_constant__ BwdSeg sg, int d_in, int taylor) {
     extern __shared__ float smem[];
-    const BwdSmem lay = bwd_layout(C, dk, dv);
+    const BwdSmem lay = bwd_layout(C, dk, dv, taylor != 0);
     float* Qs = smem + lay.q;
     float* Ks = smem + lay.k;
     float* Vs = smem + lay.v;
@@ -117,7 +121,9 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     float* pw = smem + lay.pw;
     float* cum = smem + lay.cum;
     float* xw = smem + lay.xw;
+    float* TQ = smem + lay.tq;  // Taylor map: a chunk's feature gradients, rows ldk apart
     const int ldk = dk + 1, ldv = dv + 1, lda = C + 1, lds = dv + 1;
+    const float kR2 = 0.70710678118654752f;  // 1 / sqrt 2
 
     const int bh = blockIdx.x / sg.n_seg;
     const int seg = blockIdx.x % sg.n_seg;
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     const int h = bh % H;
     const int tid = threadIdx.x;
     const float l2g = g.log2g[h];
-    const size_t qk_base = (size_t)bh * T_len * dk;
+    const size_t qk_base = (size_t)bh * T_len * d_in;  // rows of Q, K (and dQ, dK): d_in wide
     const size_t v_base = (size_t)bh * T_len * dv;
     const int n_chunks = (T_len + C - 1) / C;
     const int cb = seg * sg.seg_chunks;
@@ -151,6 +157,21 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         Ss[(idx / dv) * lds + idx % dv] = s_in ? s_in[idx] : 0.f;
     for (int d = tid; d < dk; d += kThreads) zs[d] = z_in ? z_in[d] : 0.f;
     float seg_lam = 0.f;  // per-token decay: the segment's total log2 decay (thread 0)
+    // The Taylor map's transpose Jacobian for rows 0 .. L-1 of a chunk: x_c sits in
+    // feature 1 + c and in the outer product's row c and column c (each over
+    // sqrt 2), so dx_c = dF_(1+c) + (sum_b (dF_(1+d_in+c*d_in+b) + dF_(1+d_in+b*d_in+c))
+    // x_b) / sqrt 2, with x the raw row (features 1 .. d_in of F).
+    auto taylor_back = [&](const float* dF, const float* F, T* out, int L, int t0) {
+        for (int idx = tid; idx < L * d_in; idx += kThreads) {
+            const int i = idx / d_in, c = idx % d_in;
+            const float* gr = dF + i * ldk;
+            const float* xr = F + i * ldk + 1;
+            float acc = 0.f;
+            for (int b = 0; b < d_in; ++b)
+                acc = fmaf(gr[1 + d_in + c * d_in + b] + gr[1 + d_in + b * d_in + c], xr[b], acc);
+            store_elem(out, qk_base + (size_t)(t0 + i) * d_in + c, fmaf(kR2, acc, gr[1 + c]));
+        }
+    };
     __syncthreads();
 
     for (int cc = cb; cc < ce; ++cc) {
@@ -163,7 +184,21 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         for (int idx = tid; idx < C * dk; idx += kThreads) {
             const int i = idx / dk, d = idx % dk;
             float x = 0.f, y = 0.f;
-            if (i < L) {
+            if (i < L && taylor) {
+                // feature d of the row: 1, then x_c, then x_a x_b / sqrt 2 (a-major)
+                const size_t r0 = qk_base + (size_t)(t0 + i) * d_in;
+                if (d == 0) {
+                    x = need_qg ? 1.f : 0.f;
+                    y = need_kv ? 1.f : 0.f;
+                } else if (d <= d_in) {
+                    if (need_qg) x = load_elem(Q, r0 + d - 1);
+                    if (need_kv) y = load_elem(K, r0 + d - 1);
+                } else {
+                    const int a = (d - 1 - d_in) / d_in, b = (d - 1 - d_in) % d_in;
+                    if (need_qg) x = load_elem(Q, r0 + a) * load_elem(Q, r0 + b) * kR2;
+                    if (need_kv) y = load_elem(K, r0 + a) * load_elem(K, r0 + b) * kR2;
+                }
+            } else if (i < L) {
                 const size_t gi = qk_base + (size_t)(t0 + i) * dk + d;
                 if (need_qg) x = load_elem(Q, gi);
                 if (need_kv) y = load_elem(K, gi);
@@ -371,11 +406,16 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
                         if (normalize) inter = fmaf(du[i], zs[d], inter);
                         float v = in[r][e] + xi(i) * inter;
                         if (phi) v *= fminf(1.f, Qs[i * ldk + d]);
-                        store_elem(dQ, qk_base + (size_t)(t0 + i) * dk + d, v);
+                        if (taylor)
+                            TQ[i * ldk + d] = v;
+                        else
+                            store_elem(dQ, qk_base + (size_t)(t0 + i) * dk + d, v);
                     }
                 }
             });
             __syncthreads();
+            // Taylor map: dq = the features' gradient through the map's transpose Jacobian
+            if (taylor && !st_only) taylor_back(TQ, Qs, dQ, L, t0);
             // S = gamma^L S + sum_j zeta_j k~_j^T v_j ; z likewise
             tiles(dk, dv, [&](int d0, int c0, int c1) {
                 const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
@@ -392,6 +432,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int d = d0 + r;
+                    if (d >= dk) continue;  // (dk need not be a multiple of 4)
                     if (c0 < dv) Ss[d * lds + c0] = fmaf(gL, Ss[d * lds + c0], u[r][0]);
                     if (c1 < dv) Ss[d * lds + c1] = fmaf(gL, Ss[d * lds + c1], u[r][1]);
                 }
@@ -467,11 +508,15 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
                         if (normalize) inter += zs[d];
                         float v = in[r][e] + zt(j) * inter;
                         if (phi) v *= fminf(1.f, Ks[j * ldk + d]);
-                        store_elem(dK, qk_base + (size_t)(t0 + j) * dk + d, v);
+                        if (taylor)
+                            TQ[j * ldk + d] = v;
+                        else
+                            store_elem(dK, qk_base + (size_t)(t0 + j) * dk + d, v);
                     }
                 }
             });
             __syncthreads();
+            if (taylor && !st_only) taylor_back(TQ, Ks, dK, L, t0);  // dk through the map
             // G = gamma^L G + sum_i xi_i q~_i^T dn_i ;  Gz = gamma^L Gz + sum_i xi_i du_i q~_i
             tiles(dk, dv, [&](int d0, int c0, int c1) {
                 const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
@@ -488,6 +533,7 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int d = d0 + r;
+                    if (d >= dk) continue;
                     if (c0 < dv) Ss[d * lds + c0] = fmaf(gL, Ss[d * lds + c0], u[r][0]);
                     if (c1 < dv) Ss[d * lds + c1] = fmaf(gL, Ss[d * lds + c1], u[r][1]);
                 }
@@ -566,9 +612,9 @@ __global__ void bwd_scan_kernel(const __grid_constant__ ScanArgs sc, int BH, int
 
 }  // namespace
 
-int bwd_chunk_len(int dk, int dv) {
+int bwd_chunk_len(int dk, int dv, bool taylor) {
     int C = 32;
-    while (C > 8 && (size_t)bwd_layout(C, dk, dv).total * 4 > 227 * 1024) C >>= 1;
+    while (C > 8 && (size_t)bwd_layout(C, dk, dv, taylor).total * 4 > 227 * 1024) C >>= 1;
     return C;
 }
 
@@ -588,10 +634,11 @@ struct BwdPlan {
     size_t o_stats, o_a0, o_a0z, o_e0, o_e0z, o_a1, o_a1z, o_e1, o_e1z, o_l2, bytes;
 };
 
-BwdPlan bwd_plan(int B, int H, int T, int dk, int dv, bool normalize) {
+// dk: the state's rows (1 + d + d^2 with the Taylor map)
+BwdPlan bwd_plan(int B, int H, int T, int dk, int dv, bool normalize, bool taylor) {
     BwdPlan pl;
-    pl.C = bwd_chunk_len(dk, dv);
-    pl.smem = (size_t)bwd_layout(pl.C, dk, dv).total * sizeof(float);
+    pl.C = bwd_chunk_len(dk, dv, taylor);
+    pl.smem = (size_t)bwd_layout(pl.C, dk, dv, taylor).total * sizeof(float);
     pl.n_chunks = T > 0 ? (T + pl.C - 1) / pl.C : 0;
     const size_t nbh = (size_t)B * H;
     // CTAs an SM holds by shared memory (registers allow four), and as many segments
@@ -623,12 +670,15 @@ BwdPlan bwd_plan(int B, int H, int T, int dk, int dv, bool normalize) {
 
 }  // namespace
 
+static int bwd_state_rows(const BwdArgs& a) { return a.taylor ? taylor_feature_dim(a.dk) : a.dk; }
+
 size_t bwd_workspace_bytes(const BwdArgs& a) {
-    return a.T > 0 ? bwd_plan(a.B, a.H, a.T, a.dk, a.dv, a.normalize).bytes : 0;
+    return a.T > 0 ? bwd_plan(a.B, a.H, a.T, bwd_state_rows(a), a.dv, a.normalize, a.taylor).bytes : 0;
 }
 
 cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) {
-    const BwdPlan pl = bwd_plan(a.B, a.H, a.T, a.dk, a.dv, a.normalize);
+    const int ds = bwd_state_rows(a);  // the state's rows; a.dk is the width of Q and K
+    const BwdPlan pl = bwd_plan(a.B, a.H, a.T, ds, a.dv, a.normalize, a.taylor);
     const int C = pl.C;
     const size_t smem = pl.smem;
     const unsigned nbh = (unsigned)((size_t)a.B * a.H);
@@ -659,8 +709,8 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
                          s);
         kern<<<dim3(nbh * pl.P, roles), kThreads, smem, s>>>(
             cast(a.Q), cast(a.K), cast(a.V), cast(a.dO), a.S0, a.z0, a.dS_T, a.dz_T, cast(a.dQ),
-            cast(a.dK), cast(a.dV), a.dS0, a.dz0, stats, a.H, a.T, a.dk, a.dv, C, a.phi, nm,
-            a.eps, role0, a.log_a, g, sg);
+            cast(a.dK), cast(a.dV), a.dS0, a.dz0, stats, a.H, a.T, ds, a.dv, C, a.phi, nm,
+            a.eps, role0, a.log_a, g, sg, a.dk, a.taylor ? 1 : 0);
         e = cudaGetLastError();
     };
     // the entry states of direction dir0 (and dir0 + 1 when dirs == 2)
@@ -678,10 +728,10 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
             sc.ent[y] = fp(dir == 0 ? pl.o_e0 : pl.o_e1);
             sc.zent[y] = fp(dir == 0 ? pl.o_e0z : pl.o_e1z);
         }
-        const size_t total = (size_t)nbh * ((size_t)a.dk * a.dv + a.dk);
+        const size_t total = (size_t)nbh * ((size_t)ds * a.dv + ds);
         TraceScope trace("bwd_scan_kernel", s);
         bwd_scan_kernel<<<dim3((unsigned)((total + 255) / 256), dirs), 256, 0, s>>>(
-            sc, (int)nbh, a.H, pl.P, pl.seg_chunks * C, a.T, a.dk, a.dv, nm ? 1 : 0,
+            sc, (int)nbh, a.H, pl.P, pl.seg_chunks * C, a.T, ds, a.dv, nm ? 1 : 0,
             a.log_a ? fp(pl.o_l2) : nullptr, g);
         e = cudaGetLastError();
     };

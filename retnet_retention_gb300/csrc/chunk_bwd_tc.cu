@@ -134,7 +134,7 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
 }  // namespace
 
 bool bwd_tc_supported(const BwdArgs& a) {
-    if (!a.bf16 || a.phi || a.normalize || a.log_a || a.T <= 0) return false;
+    if (!a.bf16 || a.phi || a.taylor || a.normalize || a.log_a || a.T <= 0) return false;
     if ((a.dk != 64 && a.dk != 128) || (a.dv != 64 && a.dv != 128)) return false;
     const ChunkArgs c1 = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H,
                                   a.T, a.dv, a.dk, nullptr, 0, nullptr);

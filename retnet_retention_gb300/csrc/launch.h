@@ -77,6 +77,7 @@ struct BwdArgs {
     bool floor_norm;
     float eps;
     const float* log_a;  // per-token decay, or null
+    bool taylor;         // Taylor feature map: dk = 16 wide q, k; states of 1 + dk + dk^2 rows
     void* workspace;     // the forward sweep's per-token den, du (normalising)
     size_t workspace_bytes;
 };

@@ -307,13 +307,20 @@ def test_taylor_outside_its_kernel_is_unsupported(lib, over):
     assert chunk(lib, **a) == la.LA_ERR_UNSUPPORTED
 
 
-def test_taylor_is_refused_by_the_backward_pass_and_outside_the_decode_steps_shapes(lib):
+def test_taylor_outside_the_decode_steps_and_the_backward_passs_shapes(lib):
+    """The decode step and the backward pass take the Taylor map for 16-wide q and k,
+    not with elu + 1 (and the backward not with per-token decays); the chunkwise
+    forward with per-token decays not at all."""
     assert step(lib, dk=64, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
     assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR | la.LA_PHI_ELU1) == la.LA_ERR_UNSUPPORTED
     assert step(lib, dk=16, flags=la.LA_PHI_TAYLOR | la.LA_NONCAUSAL) == la.LA_ERR_UNSUPPORTED
-    assert bwd(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert bwd(lib, dk=64, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
+    assert bwd(lib, dk=16, flags=la.LA_PHI_TAYLOR | la.LA_PHI_ELU1) == la.LA_ERR_UNSUPPORTED
     assert chunk_gated(lib, dk=16, flags=la.LA_PHI_TAYLOR) == la.LA_ERR_UNSUPPORTED
-    assert lib.la_bwd_workspace_size(2, 8, 64, 16, 64, 1, la.LA_PHI_TAYLOR) == 0
+    assert lib.la_bwd_workspace_size(2, 8, 64, 16, 64, 1, la.LA_PHI_TAYLOR | la.LA_GATED) == 0
+    assert lib.la_bwd_workspace_size(2, 8, 64, 64, 64, 1, la.LA_PHI_TAYLOR) == 0
+    # the normalised call's workspace holds the per-token denominators at least
+    assert lib.la_bwd_workspace_size(2, 8, 64, 16, 64, 1, la.LA_PHI_TAYLOR | la.LA_NORMALIZE) >= 2 * 8 * 64 * 8
 
 
 def test_taylor_plan_queries(lib):

@@ -240,3 +240,47 @@ def test_taylor_with_the_floored_normaliser():
                                           floor=True, S0=Sr, z0=zr)
     check("decode o", np64(o), Or1[:, :, 0])
     check("decode S", np64(S), Sr1)
+
+
+BWD_SHAPES = [  # B, H, T, d_v, dtype
+    (1, 2, 1, 64, "bf16"),
+    (1, 2, 100, 64, "bf16"),
+    (2, 1, 300, 32, "f32"),
+    (1, 1, 1000, 64, "bf16"),  # segments of the backward sweeps
+]
+
+
+@pytest.mark.parametrize("normalize", [True, False], ids=["normalised", "plain"])
+@pytest.mark.parametrize("gamma", [1.0, None], ids=["gamma1", "decay"])
+@pytest.mark.parametrize("shape", BWD_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_taylor_bwd_matches_oracle(shape, gamma, normalize):
+    """la_chunk_bwd with the Taylor map (the features built in shared memory, their
+    gradients taken back to 16 columns through the map's transpose Jacobian) against
+    the oracle's gradients of the recurrence with the map, with an initial state and
+    final-state gradients in the features' order."""
+    B, H, T, dv, dtype = shape
+    seed = zlib.crc32(repr((shape, gamma, normalize, "taylor-bwd")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, 16, dv, dtype=dtype, gamma=gamma, scale=0.5)
+    rng = np.random.default_rng(seed)
+    tdt = workloads.torch_dtype(dtype)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(tdt)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, DF, dv)).astype(np.float32) * 0.05)
+    z0 = torch.from_numpy(np.abs(rng.standard_normal((B, H, DF))).astype(np.float32) * 0.1 + 0.5)
+    dST = torch.from_numpy(rng.standard_normal((B, H, DF, dv)).astype(np.float32) * 0.05)
+    dzT = torch.from_numpy(rng.standard_normal((B, H, DF)).astype(np.float32) * 0.05)
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    dq, dk, dv_, dS0, dz0 = la.chunk_bwd(
+        q, k, v, g_o, x["gamma"], phi="taylor", normalize=normalize, S0=S0.to(DEV),
+        z0=z0.to(DEV) if normalize else None, dS_T=dST.to(DEV),
+        dz_T=dzT.to(DEV) if normalize else None)
+    torch.cuda.synchronize()
+    rq, rk, rv, rS0, rz0 = oracle.recurrent_bwd_taylor(
+        x["q"], x["k"], x["v"], x["gamma"], dO, normalize=normalize, S0=S0,
+        z0=z0 if normalize else None, dS_T=dST, dz_T=dzT if normalize else None)
+    tol = 1e-4 if dtype == "f32" else TOL
+    check("dq", np64(dq), rq, tol)
+    check("dk", np64(dk), rk, tol)
+    check("dv", np64(dv_), rv, tol)
+    check("dS0", np64(dS0), rS0, tol)
+    if normalize:
+        check("dz0", np64(dz0), rz0, tol)
