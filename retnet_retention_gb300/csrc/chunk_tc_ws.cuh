@@ -928,15 +928,17 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 constexpr int kHold = kW == 2 ? kRounds - 1 : 0;  // rounds held packed
                 uint32_t held[kHold > 0 ? kHold : 1][16 * kW];
                 // 16 kW words = 32 kW columns of the row: 32-byte stores where O is
-                // 32-byte aligned (each a whole sector), else 16-byte ones
+                // 32-byte aligned (each a whole sector), else 16-byte ones; O is not
+                // allocated in L1 and is first to leave L2 (nothing here reads it back)
+                const uint64_t opol = l2_evict_first_policy();
                 auto store_packed = [&](const uint32_t* pk, int col) {
                     if (p.o_align32) {
 #pragma unroll
-                        for (int e = 0; e < 16 * kW; e += 8) st_global_v8(orow + col + 2 * e, pk + e);
+                        for (int e = 0; e < 16 * kW; e += 8) st_global_v8(orow + col + 2 * e, pk + e, opol);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16 * kW; e += 4)
-                            *reinterpret_cast<uint4*>(orow + col + 2 * e) = make_uint4(pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
+                            st_global_v4(orow + col + 2 * e, pk[e], pk[e + 1], pk[e + 2], pk[e + 3], opol);
                     }
                 };
 #pragma unroll

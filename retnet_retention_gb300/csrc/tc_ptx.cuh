@@ -153,10 +153,25 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
     return out != 0;
 }
 
-// 32 bytes (eight 32-bit words) to a 32-byte aligned global address in one store.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+// An L2 policy that marks lines first to evict: for output a kernel streams out.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// 32 bytes (eight 32-bit words) to a 32-byte aligned global address in one store,
+// not allocated in L1 and first to leave L2 (output nothing here reads back).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;"
+                 ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7]), "l"(pol)
+                 : "memory");
+}
+// The same for 16 bytes at a 16-byte aligned address.
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "l"(pol)
                  : "memory");
 }
 
