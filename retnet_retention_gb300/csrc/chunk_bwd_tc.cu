@@ -18,7 +18,10 @@
 // "Linear attention" (zerotofrontier 21.2), "Decoding, training, and what each
 // costs": the gradients are cumulative sums, forward in time for the queries and
 // backward in time for the keys and values.  The reversed copies cost one read
-// and one write of Q, K, V and dO and of the two reversed outputs.
+// and one write of Q, K, V and dO and of the two reversed outputs; where the
+// pipelined kernel's factored build applies (every gamma in (0, 1] with
+// gamma^(C-1) >= 2^-64) it walks the sequences backward itself instead, on the
+// original tensors.
 #include <algorithm>
 #include <cstring>
 
@@ -166,15 +169,6 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
     ChunkArgs c1 = fwd_args(a.dO, a.V, a.K, a.dQ, s0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
                             p.fwd_bytes, nullptr);
     if ((e = launch_chunk_tc(c1, g, s, &launches)) != cudaSuccess) return e;
-    // the reversed sequences
-    void* qr = ws + p.o_qr;
-    void* kr = ws + p.o_kr;
-    void* vr = ws + p.o_vr;
-    void* dor = ws + p.o_dor;
-    if ((e = reverse_time(a.Q, qr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
-    if ((e = reverse_time(a.K, kr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
-    if ((e = reverse_time(a.V, vr, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
-    if ((e = reverse_time(a.dO, dor, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
     // initial states of the reversed passes: dS_T / gamma and its transpose
     float* g0 = nullptr;
     float* g0t = nullptr;
@@ -186,19 +180,39 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
         if ((e = state_scale(a.dS_T, g0t, nbh, a.H, a.dk, a.dv, true, true, g, s)) != cudaSuccess)
             return e;
     }
-    // dV (reversed): queries K, keys Q, values dO; its final state is G_0
     float* gfin = a.dS0 ? reinterpret_cast<float*>(ws + p.o_gfin) : nullptr;
-    void* dvr = ws + p.o_dvr;
-    ChunkArgs c2 = fwd_args(kr, qr, dor, dvr, g0, gfin, a.B, a.H, a.T, a.dk, a.dv, fws,
+    // dV: queries K, keys Q, values dO in reversed time, its final state G_0;
+    // dK: queries V, keys dO, values Q in reversed time
+    ChunkArgs c2 = fwd_args(a.K, a.Q, a.dO, a.dV, g0, gfin, a.B, a.H, a.T, a.dk, a.dv, fws,
                             p.fwd_bytes, nullptr);
-    if ((e = launch_chunk_tc(c2, g, s, &launches)) != cudaSuccess) return e;
-    // dK (reversed): queries V, keys dO, values Q
-    void* dkr = ws + p.o_dkr;
-    ChunkArgs c3 = fwd_args(vr, dor, qr, dkr, g0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
+    ChunkArgs c3 = fwd_args(a.V, a.dO, a.Q, a.dK, g0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
                             p.fwd_bytes, nullptr);
-    if ((e = launch_chunk_tc(c3, g, s, &launches)) != cudaSuccess) return e;
-    if ((e = reverse_time(dvr, a.dV, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
-    if ((e = reverse_time(dkr, a.dK, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+    c2.reverse = c3.reverse = true;
+    if (tc_reverse_supported(c2, g) && tc_reverse_supported(c3, g)) {
+        // the kernel walks the sequences backward itself: no copies
+        if ((e = launch_chunk_tc(c2, g, s, &launches)) != cudaSuccess) return e;
+        if ((e = launch_chunk_tc(c3, g, s, &launches)) != cudaSuccess) return e;
+    } else {
+        // reversed copies of the sequences, forward passes over them, the outputs
+        // reversed back
+        void* qr = ws + p.o_qr;
+        void* kr = ws + p.o_kr;
+        void* vr = ws + p.o_vr;
+        void* dor = ws + p.o_dor;
+        void* dvr = ws + p.o_dvr;
+        void* dkr = ws + p.o_dkr;
+        if ((e = reverse_time(a.Q, qr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(a.K, kr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(a.V, vr, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(a.dO, dor, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
+        c2.Q = kr; c2.K = qr; c2.V = dor; c2.O = dvr;
+        c3.Q = vr; c3.K = dor; c3.V = qr; c3.O = dkr;
+        c2.reverse = c3.reverse = false;
+        if ((e = launch_chunk_tc(c2, g, s, &launches)) != cudaSuccess) return e;
+        if ((e = launch_chunk_tc(c3, g, s, &launches)) != cudaSuccess) return e;
+        if ((e = reverse_time(dvr, a.dV, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(dkr, a.dK, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+    }
     if (a.dS0) {  // dS_0 = gamma G_0
         if ((e = state_scale(gfin, a.dS0, nbh, a.H, a.dk, a.dv, false, false, g, s)) != cudaSuccess)
             return e;

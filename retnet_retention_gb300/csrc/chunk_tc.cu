@@ -703,6 +703,18 @@ static int tc_dvb(const ChunkArgs& a) {
     return a.dv == 64 ? 64 : 128;
 }
 
+// Reversed time runs in the pipelined kernel's factored-decay build: plain
+// retention (no feature map, no normaliser, no z), causal, every head's gamma in
+// (0, 1] with gamma^(C-1) >= 2^-64 (gamma = 1 included: the factors are then 1).
+bool tc_reverse_supported(const ChunkArgs& a, const KernelGammas& g) {
+    if (!tc_supported(a) || a.phi || a.normalize || a.log_a || a.noncausal || a.taylor || a.z_out)
+        return false;
+    if (a.H <= 0 || a.H > kMaxHeads) return false;
+    for (int h = 0; h < a.H; ++h)
+        if (!(g.gamma[h] > 0.f && g.gamma[h] <= 1.f && g.log2g[h] * (float)(kC - 1) >= -64.f)) return false;
+    return tc_ws_supported(kFull, a.dk, tc_dvb(a), false) && tc_ws_supported(kStateOnly, a.dk, tc_dvb(a), false);
+}
+
 // Whether the output walk folds the segments' contributions into its entry states
 // itself (no scan kernel): few segments per sequence, and the pipelined kernel runs.
 static bool fold_segments(int P, int dk, int dvb, bool normalize) {
@@ -795,6 +807,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     prm.fact = !a.log_a && !a.phi && !prm.track_z;
     for (int h = 0; h < a.H && prm.fact; ++h)
         prm.fact = g.gamma[h] < 1.f && g.log2g[h] * (float)(kC - 1) >= -64.f;
+    if (a.reverse) {  // the factored build alone walks reversed time
+        if (!tc_reverse_supported(a, g)) return cudaErrorInvalidValue;
+        prm.fact = 1;
+        prm.rev = 1;
+    }
     const int n_chunks = pl.n_chunks;
     const int units = pl.units;
     *launches = 0;

@@ -57,8 +57,21 @@ struct TcParams {
     // every head's gamma < 1 with gamma^(C-1) >= 2^-64, no feature map, no normaliser,
     // z not carried: the pipelined kernel's factored-decay build
     int fact;
+    // reversed time (factored-decay build only): the sums run over s >= t, the
+    // chunks are walked from the end of the sequence (chunk c covers rows
+    // T - (c + 1) C .. T - c C - 1, the last one starting before row 0, where the
+    // tiles read zeros), and tile row r stands at position C - 1 - r of its chunk
+    // in the reversed sequence.  The initial state enters at the end, and the
+    // final state is the one after row 0.
+    int rev;
     int o_align32;  // O's base is 32-byte aligned (rows and column blocks then are too)
     KernelGammas g;
+};
+
+// A compile-time bool for generic lambdas (one instantiation per value).
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
 };
 
 __device__ __forceinline__ void record_status(int* st, int code) {

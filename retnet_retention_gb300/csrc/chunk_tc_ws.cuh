@@ -259,6 +259,15 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
     // stays far inside the float and bf16 ranges); smaller gammas keep the row
     // scalings.
     constexpr bool fact = FACT;
+    // Reversed time (factored build only, p.rev): the same sums over s >= t, by the
+    // mirror image of the chunk.  Chunk c's tiles start at row T - (c + 1) C and its
+    // tile row r stands at position C - 1 - r of the chunk in the reversed sequence
+    // (o_i = sum_{j>=i} (q_i . k_j) gamma^(j-i) v_j + gamma^(L-i) q_i S with i, j
+    // counted from the chunk's first row and L the rows it holds), so every decay
+    // exponent takes the mirrored row mrow(r), the mask keeps j >= i, and the rows
+    // before row 0 (mrow(r) >= L) are the padding, read as zeros.
+    const bool rev = FACT && p.rev;
+    auto mrow = [&](int r) { return rev ? kC - 1 - r : r; };
     // Order of the work per chunk with one O buffer.  Where epilogue B rescales the
     // tiles after MMA1 (gamma < 1 without the factored form, per-token decays),
     // MMA1 of chunk c+1 goes before the MMAs of chunk c so that E1 and the
@@ -445,7 +454,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     !mbar_wait_or_abort(&bar[kEmpty0 + s], ((it - NS) / NS) & 1, lim, abort_flag))
                     break;
                 char* st = sm + s * Lay::kStage;
-                const int y = (cb + it) * kC;
+                const int y = rev ? p.T - (cb + it + 1) * kC : (cb + it) * kC;
                 mbar_arrive_expect_tx(&bar[kFull0 + s],
                                       (STATE_ONLY ? Lay::kK + Lay::kV + Lay::kGate : Lay::kStage));
                 if constexpr (GATED)
@@ -678,10 +687,12 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                         const int i = row;
                         float rsum = 0.f;  // fp32 row sum of this half's scores (normaliser)
                         if constexpr (FACT) {
-                            // the scores need only the causal mask (the decay is in K or is 1):
-                            // both pieces loaded at once, one wait, then packed and stored
+                            // the scores need only the causal mask (the decay is in V or is 1):
+                            // both pieces loaded at once, one wait, then packed and stored.
+                            // Pieces wholly on the masked side of the diagonal are P = 0 for
+                            // the whole warp (above it; below it in reversed time).
                             const int lq = warp & 3, pa = 2 * half;
-                            const bool za = pa > lq, zb = pa + 1 > lq;  // above the diagonal
+                            const bool za = rev ? pa < lq : pa > lq, zb = rev ? pa + 1 < lq : pa + 1 > lq;
                             uint32_t ra[32], rb[32];
                             if (!za) tmem_ld32(sc + 32 * pa, ra);
                             if (!zb) tmem_ld32(sc + 32 * pa + 32, rb);
@@ -691,26 +702,35 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                                 fence_before_sync();
                                 named_bar_arrive(kBarP, kThreadsA);
                             }
-                            uint32_t pk[16];
+                            // one piece of P: columns j0 .. j0 + 31 kept where j <= i (j >= i
+                            // in reversed time), two instantiations so that neither form
+                            // tests the direction per element
+                            auto pack_piece = [&](const uint32_t* r, int j0, bool z, uint32_t* pk, auto dir) {
+                                constexpr bool kRev = decltype(dir)::value;
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int j = 32 * pa + e;
-                                pk[e >> 1] = za ? 0u
-                                                : pack_bf16x2(j <= i ? __uint_as_float(ra[e]) : 0.f,
-                                                              j + 1 <= i ? __uint_as_float(ra[e + 1]) : 0.f);
-                            }
+                                for (int e = 0; e < 32; e += 2) {
+                                    const int j = j0 + e;
+                                    const bool k0 = kRev ? j >= i : j <= i;
+                                    const bool k1 = kRev ? j + 1 >= i : j + 1 <= i;
+                                    pk[e >> 1] = z ? 0u
+                                                   : pack_bf16x2(k0 ? __uint_as_float(r[e]) : 0.f,
+                                                                 k1 ? __uint_as_float(r[e + 1]) : 0.f);
+                                }
+                            };
+                            auto pack = [&](const uint32_t* r, int j0, bool z, uint32_t* pk) {
+                                if (rev)
+                                    pack_piece(r, j0, z, pk, BoolC<true>{});
+                                else
+                                    pack_piece(r, j0, z, pk, BoolC<false>{});
+                            };
+                            uint32_t pk[16];
+                            pack(ra, 32 * pa, za, pk);
                             if (half == 1) {
                                 named_bar_sync(kBarP, kThreadsA);
                                 fence_after_sync();
                             }
                             tmem_st16(sc + 16 * pa, pk);
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int j = 32 * pa + 32 + e;
-                                pk[e >> 1] = zb ? 0u
-                                                : pack_bf16x2(j <= i ? __uint_as_float(rb[e]) : 0.f,
-                                                              j + 1 <= i ? __uint_as_float(rb[e + 1]) : 0.f);
-                            }
+                            pack(rb, 32 * pa + 32, zb, pk);
                             tmem_st16(sc + 16 * pa + 16, pk);
                         } else {
                             // this half's two 32-column pieces of scores, one at a time.  P (bf16
@@ -846,7 +866,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     if (L != zL) {
 #pragma unroll
                         for (int m = 0; m < kRowsC; ++m)
-                            split_bf16x2(dec_zeta(nullptr, (t >> 3) + (kThreadsC / 8) * m, L), zh[m], zl[m]);
+                            split_bf16x2(dec_zeta(nullptr, mrow((t >> 3) + (kThreadsC / 8) * m), L), zh[m],
+                                         zl[m]);
                         zL = L;
                     }
                     scale_rows_hl<DVB / 64, kThreadsC>(st + Lay::kQ + Lay::kK, zh, zl, t);
@@ -915,9 +936,14 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     }
                     inv = 1.f / norm_den(den, p.normalize, p.eps);
                 }
-                if (fact) inv = gamma_pow(l2g, (float)(row + 1 - L));  // gamma^(i+1-L)
+                if (fact) inv = gamma_pow(l2g, (float)(mrow(row) + 1 - L));  // gamma^(i+1-L)
                 const int c = cb + it;
-                __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)c * kC + row) * p.dv + v0;
+                // the row's place in the sequence (reversed time: chunk c starts at row
+                // T - (c + 1) C, before row 0 for the last chunk); rows past the chunk's
+                // L are padding and store nothing
+                const int trow = rev ? p.T - (c + 1) * kC + row : c * kC + row;
+                const bool live = mrow(row) < L;
+                __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)max(trow, 0)) * p.dv + v0;
                 // 64 columns a round in the factored build with 128 registers a thread
                 // (two loads, one wait), else 32.  The O buffer is released once the
                 // last round is in registers; in the factored build the earlier
@@ -965,7 +991,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                         for (int e = 0; e < 16 * kW; ++e) held[rd][e] = pk[e];
                         continue;
                     }
-                    if (row < L) {
+                    if (live) {
 #pragma unroll
                         for (int h = 0; h < kHold; ++h) store_packed(held[h], 32 * kW * h);
                         store_packed(pk, 32 * kW * rd);

@@ -36,6 +36,10 @@ struct ChunkArgs {
     void* workspace;
     size_t workspace_bytes;
     int* dev_status;
+    // reversed time: o_t = q_t S'_t with S'_t = gamma S'_{t+1} + k_t^T v_t, the
+    // initial state entering after the last token and S_out the state after the
+    // first (plain retention with the factored decay only; tc_reverse_supported)
+    bool reverse = false;
 };
 
 struct StepArgs {
@@ -116,6 +120,7 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
 
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);
+bool tc_reverse_supported(const ChunkArgs& a, const KernelGammas& g);
 size_t tc_workspace_bytes(const ChunkArgs& a);
 // Kernel launches of one tensor-core chunkwise call (1 to 4).
 int tc_launch_count(const ChunkArgs& a);

@@ -105,8 +105,9 @@ TC_SHAPES = [  # B, H, T, dk, dv: bf16, per-head decay, no phi, no normaliser
 
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_bwd_tensor_core_path(shape, opts):
-    """The three forward passes on the tensor cores (dQ; dV and dK over the reversed
-    sequences) against the oracle, with an initial state and a final-state gradient."""
+    """The three forward passes on the tensor cores (dQ; dV and dK in reversed time,
+    walked backward by the kernel itself for these gammas) against the oracle, with an
+    initial state and a final-state gradient."""
     opts.path("auto")
     B, H, T, dk, dv = shape
     seed = zlib.crc32(repr((shape, "bwd-tc")).encode()) % 100000
@@ -135,13 +136,61 @@ def test_bwd_tensor_core_path(shape, opts):
     check("dS0 tc vs simt", to_np(dS0), to_np(sS0), TOL["bf16"])
 
 
-def test_bwd_tensor_core_path_repeated(opts):
-    """The tensor-core composite twelve times over: its dV pass reads reversed copies
-    written just before it (hot in L2), the case that once exposed an exit state read
-    before the state walk's last MMA."""
+REVERSE_CASES = [  # shape, gammas, whether the kernel walks reversed time itself
+    ((1, 2, 300, 64, 64), [1.0, 0.9], True),        # gamma = 1 beside gamma < 1; ragged tail
+    ((2, 2, 3000, 64, 128), [0.999, 0.8], True),    # segments (scan), d_k != d_v
+    ((2, 16, 1000, 128, 64), 0.97, True),           # segments folded in the output walk
+    ((1, 1, 129, 128, 128), [0.71], True),         # near the factored form's floor: 0.71^127 = 2^-62.7
+    ((1, 2, 300, 64, 64), [0.5, 0.9], False),       # gamma^127 < 2^-64: reversed copies
+    ((1, 2, 3000, 128, 64), [0.6, 0.99], False),    # the same with segments
+]
+
+
+@pytest.mark.parametrize("shape,gammas,walk", REVERSE_CASES,
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else None)
+def test_bwd_tensor_core_reversed_time(shape, gammas, walk, opts):
+    """dK and dV come from forward passes in reversed time: by the pipelined kernel's
+    own backward walk (chunks from the end, mirrored rows, the last chunk starting
+    before row 0) where every gamma is in the factored form's range, else over
+    reversed copies.  Both against the oracle, with an initial state and a
+    final-state gradient; the trace shows which ran."""
+    opts.path("auto")
+    B, H, T, dk, dv = shape
+    seed = zlib.crc32(repr((shape, gammas, "bwd-rev")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16", gamma=gammas)
+    rng = np.random.default_rng(seed)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.3)
+    dST = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.1)
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    la.trace_enable(4096)
+    try:
+        la.trace_collect()
+        dq, dk_, dv_, dS0, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], S0=S0.to(DEV),
+                                            dS_T=dST.to(DEV))
+        torch.cuda.synchronize()
+        names = [n for n, _ in la.trace_collect()]
+    finally:
+        la.trace_enable(0)
+    assert any(n.startswith("chunk_tc_ws_kernel") for n in names), names
+    assert ("reverse_time_kernel" in names) == (not walk), names
+    rq, rk, rv, rS0, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, S0=S0,
+                                              dS_T=dST)
+    check("dq", to_np(dq), rq, TOL["bf16"])
+    check("dk", to_np(dk_), rk, TOL["bf16"])
+    check("dv", to_np(dv_), rv, TOL["bf16"])
+    check("dS0", to_np(dS0), rS0, TOL["bf16"])
+
+
+@pytest.mark.parametrize("gammas", [None, [0.5, 0.6]], ids=["walk", "copies"])
+def test_bwd_tensor_core_path_repeated(gammas, opts):
+    """The tensor-core composite twelve times over, its dV pass reading inputs written
+    or read just before it (hot in L2): the case that once exposed an exit state read
+    before the state walk's last MMA; both with the kernel's reversed walk and with
+    reversed copies."""
     opts.path("auto")
     B, H, T, dk, dv = 1, 2, 3000, 64, 64
-    x = workloads.random_case(9090, B, H, T, dk, dv, dtype="bf16")
+    x = workloads.random_case(9090, B, H, T, dk, dv, dtype="bf16", gamma=gammas)
     rng = np.random.default_rng(9090)
     dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
     rq, rk, rv, _, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO)
