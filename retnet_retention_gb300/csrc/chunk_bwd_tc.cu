@@ -101,9 +101,16 @@ ChunkArgs fwd_args(const void* Q, const void* K, const void* V, void* O, const f
 }
 
 // Workspace layout: reversed Q, K, V, dO, reversed dV, dK outputs, the states,
-// then the forward calls' own workspace (one call at a time).
+// the dV pass's segment contributions and their transposes, then the forward
+// calls' own workspace (one call at a time).
 struct BwdTcPlan {
-    size_t o_qr, o_kr, o_vr, o_dor, o_dvr, o_dkr, o_s0t, o_g0, o_g0t, o_gfin, o_fwd, fwd_bytes, bytes;
+    size_t o_qr, o_kr, o_vr, o_dor, o_dvr, o_dkr, o_s0t, o_g0, o_g0t, o_gfin, o_agg, o_aggt, o_fwd,
+        fwd_bytes, bytes;
+    // the dV and dK passes have the same segments (more than one): the dK pass's
+    // state walk is the dV pass's transposed (keys dO and values Q instead of keys
+    // Q and values dO), so it is not run again
+    bool share;
+    int n_seg;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -124,11 +131,19 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
     p.o_g0 = off; off += ns;
     p.o_g0t = off; off += ns;
     p.o_gfin = off; off += ns;
-    p.o_fwd = off;
     const ChunkArgs c1 = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H,
                                   a.T, a.dv, a.dk, nullptr, 0, nullptr);
     const ChunkArgs c2 = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H,
                                   a.T, a.dk, a.dv, nullptr, 0, nullptr);
+    int n2 = 1, sc2 = 0, n3 = 1, sc3 = 0;
+    tc_segments(c2, &n2, &sc2);
+    tc_segments(c1, &n3, &sc3);  // (the dK pass has the dQ pass's shape)
+    p.share = n2 > 1 && n2 == n3 && sc2 == sc3;
+    p.n_seg = n2;
+    const size_t nagg = p.share ? align256(nbh * n2 * a.dk * a.dv * 4) : 0;
+    p.o_agg = off; off += nagg;
+    p.o_aggt = off; off += nagg;
+    p.o_fwd = off;
     p.fwd_bytes = std::max(tc_workspace_bytes(c1), tc_workspace_bytes(c2));
     p.bytes = off + p.fwd_bytes;
     return p;
@@ -190,7 +205,20 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
     c2.reverse = c3.reverse = true;
     if (tc_reverse_supported(c2, g) && tc_reverse_supported(c3, g)) {
         // the kernel walks the sequences backward itself: no copies
+        if (p.share) {
+            c2.agg = reinterpret_cast<float*>(ws + p.o_agg);
+            c3.agg = reinterpret_cast<float*>(ws + p.o_aggt);
+            c3.agg_ready = true;
+        }
         if ((e = launch_chunk_tc(c2, g, s, &launches)) != cudaSuccess) return e;
+        if (p.share) {  // the dK pass's contributions: sum dO^T Q = (sum Q^T dO)^T
+            KernelGammas one;
+            std::memset(&one, 0, sizeof(one));
+            for (int h = 0; h < kMaxHeads; ++h) one.gamma[h] = 1.f;
+            if ((e = state_scale(c2.agg, c3.agg, nbh * p.n_seg, a.H, a.dk, a.dv, true, false, one, s)) !=
+                cudaSuccess)
+                return e;
+        }
         if ((e = launch_chunk_tc(c3, g, s, &launches)) != cudaSuccess) return e;
     } else {
         // reversed copies of the sequences, forward passes over them, the outputs

@@ -603,7 +603,7 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
         for (int b = 0; b < kScanBatch; ++b) {  // the last segment's contribution is not needed
             const int q = q0 + b;
             a[b] = q + 1 < P ? agg[(bh * P + q) * per + e] : 0.f;
-            za[b] = (do_z && q + 1 < P) ? zagg[(bh * P + q) * dk + d] : 0.f;
+            za[b] = (do_z && zagg && q + 1 < P) ? zagg[(bh * P + q) * dk + d] : 0.f;
             gq[b] = seg_l2 ? (q + 1 < P ? exp2f(seg_l2[bh * P + q]) : 0.f) : gseg;
         }
 #pragma unroll
@@ -775,6 +775,12 @@ int tc_launch_count(const ChunkArgs& a) {
 
 size_t tc_workspace_bytes(const ChunkArgs& a) { return tc_plan(a).bytes; }
 
+void tc_segments(const ChunkArgs& a, int* n_seg, int* seg_chunks) {
+    const TcPlan pl = tc_plan(a);
+    *n_seg = pl.P > 1 ? pl.Pu : 1;
+    *seg_chunks = pl.seg_chunks;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStream_t s,
                             int* launches) {
     TcParams prm;
@@ -862,9 +868,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     const int seg_chunks = pl.seg_chunks;
     const int Pu = pl.Pu;  // segments actually used
     const size_t nbh = (size_t)BH;
-    float* agg = reinterpret_cast<float*>(ws + pl.o_agg);
+    float* agg = a.agg ? a.agg : reinterpret_cast<float*>(ws + pl.o_agg);
     float* entry = reinterpret_cast<float*>(ws + pl.o_entry);
-    float* zagg = reinterpret_cast<float*>(ws + pl.o_zagg);
+    // (contributions handed in carry no z: nothing reads zagg then)
+    float* zagg = a.agg_ready ? nullptr : reinterpret_cast<float*>(ws + pl.o_zagg);
+    if (a.agg_ready && (prm.track_z || a.log_a || !a.agg)) return cudaErrorInvalidValue;
     float* zentry = reinterpret_cast<float*>(ws + pl.o_zentry);
 
     TcParams pa = prm;  // state-only walks of segments 0 .. Pu-2 (the last one's is not needed)
@@ -875,8 +883,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     pa.z_out = zagg;
     pa.out_nseg = Pu;  // contributions keep the [BH][Pu] layout the scan and the fold read
     pa.out_last_only = 0;
-    cudaError_t e = launch_tc_dispatch(a.dk, dvb, pa, units * (Pu - 1), s);
+    cudaError_t e = a.agg_ready ? cudaSuccess : launch_tc_dispatch(a.dk, dvb, pa, units * (Pu - 1), s);
     if (e != cudaSuccess) return e;
+    const int walk = a.agg_ready ? 0 : 1;  // the state walk's launch, if any
     TcParams pc = prm;
     pc.mode = kFull;
     pc.seg_chunks = seg_chunks;
@@ -893,7 +902,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         pc.in_agg = 1;
         pc.S0 = a.S0;
         pc.z0 = a.z0;
-        *launches += 2;
+        *launches += 1 + walk;
         return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
     }
     const size_t total = nbh * (size_t)a.dk * a.dv;
@@ -915,7 +924,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     if (e != cudaSuccess) return e;
     pc.S_in = entry;
     pc.z_in = zentry;
-    *launches += 3;
+    *launches += 2 + walk;
     return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
 }
 

@@ -40,6 +40,12 @@ struct ChunkArgs {
     // initial state entering after the last token and S_out the state after the
     // first (plain retention with the factored decay only; tc_reverse_supported)
     bool reverse = false;
+    // Segment contributions of a segmented launch ([BH][segments][dk][dv] fp32):
+    // where the state walk writes them (null: the workspace), or, with agg_ready,
+    // already there (from a launch with the same segment plan), so that the state
+    // walk is skipped (no normaliser, no z, no per-token decay).
+    float* agg = nullptr;
+    bool agg_ready = false;
 };
 
 struct StepArgs {
@@ -121,6 +127,9 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
 // chunk_tc.cu: the tcgen05 chunkwise kernels (bf16, d_k in {64,128}, d_v in {64,128,256})
 bool tc_supported(const ChunkArgs& a);
 bool tc_reverse_supported(const ChunkArgs& a, const KernelGammas& g);
+// The segment plan of a tensor-core call: segments per sequence (1: none) and
+// chunks per segment.
+void tc_segments(const ChunkArgs& a, int* n_seg, int* seg_chunks);
 size_t tc_workspace_bytes(const ChunkArgs& a);
 // Kernel launches of one tensor-core chunkwise call (1 to 4).
 int tc_launch_count(const ChunkArgs& a);

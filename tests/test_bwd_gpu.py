@@ -153,7 +153,9 @@ def test_bwd_tensor_core_reversed_time(shape, gammas, walk, opts):
     own backward walk (chunks from the end, mirrored rows, the last chunk starting
     before row 0) where every gamma is in the factored form's range, else over
     reversed copies.  Both against the oracle, with an initial state and a
-    final-state gradient; the trace shows which ran."""
+    final-state gradient; the trace shows which ran.  With segments, the dK pass
+    takes the dV pass's segment contributions transposed (keys dO and values Q give
+    the transpose of keys Q and values dO)."""
     opts.path("auto")
     B, H, T, dk, dv = shape
     seed = zlib.crc32(repr((shape, gammas, "bwd-rev")).encode()) % 100000
@@ -174,6 +176,9 @@ def test_bwd_tensor_core_reversed_time(shape, gammas, walk, opts):
         la.trace_enable(0)
     assert any(n.startswith("chunk_tc_ws_kernel") for n in names), names
     assert ("reverse_time_kernel" in names) == (not walk), names
+    # segmented passes: the reversed walk runs the state walk of the dV pass only
+    # and hands its transpose to the dK pass (two state walks, not three)
+    assert names.count("chunk_tc_ws_kernel/state") in ((0, 2) if walk else (0, 3)), names
     rq, rk, rv, rS0, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, S0=S0,
                                               dS_T=dST)
     check("dq", to_np(dq), rq, TOL["bf16"])
