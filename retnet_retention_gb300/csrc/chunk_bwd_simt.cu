@@ -39,7 +39,9 @@
 // d(q+1) G_end(q+1) + gagg(q+1) from dS_T; d(q) the state's decay over segment
 // q), and the full sweeps run every segment from its entry state.
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "launch.h"
 #include "trace.h"
@@ -610,6 +612,242 @@ __global__ void bwd_scan_kernel(const __grid_constant__ ScanArgs sc, int BH, int
     }
 }
 
+// A segment's own contribution for the scan, as one weighted product over the
+// segment's tokens s .. e-1: a contribution starts from zero, so the chunk
+// recurrences above multiply out to one weight per token and no chunks are needed:
+//   role 0: agg = sum_t w_t k~_t^T v_t,   zagg = sum_t w_t k~_t,
+//           w_t = gamma^(e-1-t), or 2^(b_(e-1) - b_t) with the per-token decay;
+//   role 1: agg = sum_t w_t q~_t^T dn_t,  zagg = sum_t w_t du_t q~_t,
+//           w_t = gamma^(t-s+1), or 2^(b_t);
+// b_t = sum_{u=s..t} log2 a_u, dn_t = do_t / den_t and du_t from the forward
+// sweep's stats (dn = do, and no z, without the normaliser).  Role 0 also writes the
+// segment's total log2 decay b_(e-1) with the per-token decay.
+// 256 threads as a 16 x 16 grid: thread (ty, tx) holds rows ty DK/16 .. and columns
+// tx DV/16 .. of the state.  The tokens pass through shared memory 32 at a time in
+// fp32, double-buffered: the next tile's global loads are in flight while the
+// current tile's products run.  A loader thread holds 8-element pieces of fixed
+// columns, so it also sums its share of z; the shares are added in a fixed order.
+constexpr int kGemmKT = 32;
+
+template <typename T>
+struct Raw8;  // 8 consecutive input elements in registers
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ void to_f32(float (&x)[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = __uint_as_float(w[e] << 16);
+            x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ void load(const float* p) {
+        a = __ldg(reinterpret_cast<const float4*>(p));
+        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ void to_f32(float (&x)[8]) const {
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w;
+        x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+    }
+};
+
+template <int DK, int DV>
+constexpr size_t gemm_smem_bytes() {
+    return (size_t)2 * kGemmKT * (DK + DV) * sizeof(float);
+}
+
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(256) bwd_state_gemm_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+    const T* __restrict__ dO, const float* __restrict__ stats, const float* __restrict__ log_a,
+    int H, int T_len, int phi, int normalize, int role0, int seg_len,
+    const __grid_constant__ KernelGammas g, const __grid_constant__ BwdSeg sg) {
+    constexpr int KT = kGemmKT;
+    constexpr int TM = DK / 16, TN = DV / 16;
+    constexpr int GA = DK / 8, GB = DV / 8;      // 8-element pieces per row
+    constexpr int RA = 256 / GA, RB = 256 / GB;  // rows per loader pass
+    constexpr int NA = KT / RA, NB = KT / RB;    // loader passes per tile
+    static_assert(TM % 4 == 0 && TN % 4 == 0 && NA >= 1 && NB >= 1, "shape");
+    extern __shared__ __align__(16) float gsm[];
+    float* As = gsm;                  // [2][KT][DK]
+    float* Bs = gsm + 2 * KT * DK;    // [2][KT][DV]
+    __shared__ float red[8];
+    const float kLog2e = 1.44269504088896341f;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = tid >> 4, tx = tid & 15;
+    const int bh = blockIdx.x / sg.n_seg, seg = blockIdx.x % sg.n_seg;
+    const size_t sidx = (size_t)bh * sg.n_seg + seg;
+    const int role = role0 + (int)blockIdx.y;
+    const int h = bh % H;
+    const float l2g = g.log2g[h];
+    const int s0 = seg * seg_len;
+    const int e0 = min(T_len, s0 + seg_len);
+    const int n_tiles = e0 > s0 ? (e0 - s0 + KT - 1) / KT : 0;
+    const T* Ain = role == 0 ? K : Q;
+    const T* Bin = role == 0 ? V : dO;
+    const bool norm1 = role == 1 && normalize;
+    const size_t tok0 = (size_t)bh * T_len;
+
+    // the segment's total log2 decay (role 0, per-token decay)
+    float total = 0.f;
+    if (log_a && role == 0) {
+        float acc = 0.f;
+        for (int t = s0 + tid; t < e0; t += 256) acc += log_a[tok0 + t] * kLog2e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) red[warp] = acc;
+        __syncthreads();
+        if (tid == 0) {
+            float x = 0.f;
+            for (int w = 0; w < 8; ++w) x += red[w];
+            red[0] = x;
+            if (sg.seg_l2) sg.seg_l2[sidx] = x;
+        }
+        __syncthreads();
+        total = red[0];
+    }
+
+    const int pa = tid % GA, ra0 = tid / GA;
+    const int pb = tid % GB, rb0 = tid / GB;
+    Raw8<T> rawA[NA], rawB[NB];
+    float lane_la = 0.f;                     // log2 a of token t0 + lane
+    float2 lane_st = make_float2(1.f, 0.f);  // den, du of token t0 + lane
+    float base = 0.f;                        // b up to the tile's first token (exclusive)
+    float zacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    auto fetch = [&](int it) {
+        const int t0 = s0 + it * KT;
+#pragma unroll
+        for (int n = 0; n < NA; ++n) {
+            const int t = t0 + ra0 + RA * n;
+            if (t < e0) rawA[n].load(Ain + (tok0 + t) * DK + pa * 8);
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            const int t = t0 + rb0 + RB * n;
+            if (t < e0) rawB[n].load(Bin + (tok0 + t) * DV + pb * 8);
+        }
+        if (log_a) lane_la = t0 + lane < e0 ? log_a[tok0 + t0 + lane] * kLog2e : 0.f;
+        if (norm1 && t0 + lane < e0) lane_st = *reinterpret_cast<const float2*>(stats + (tok0 + t0 + lane) * 2);
+    };
+    // the fetched tile, weighted, into buffer `buf`
+    auto stage = [&](int it, int buf) {
+        const int t0 = s0 + it * KT;
+        float pre = 0.f;  // b of token t0 + lane (inclusive)
+        if (log_a) {
+            pre = lane_la;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, pre, o);
+                if (lane >= o) pre += y;
+            }
+            pre += base;
+            base = __shfl_sync(0xffffffffu, pre, 31);
+        }
+#pragma unroll
+        for (int n = 0; n < NA; ++n) {
+            const int r = ra0 + RA * n, t = t0 + r;
+            float x[8];
+            rawA[n].to_f32(x);
+            float w;
+            if (log_a) {
+                const float br = __shfl_sync(0xffffffffu, pre, r);
+                w = role == 0 ? exp2f(total - br) : exp2f(br);
+            } else {
+                w = gamma_pow(l2g, role == 0 ? (float)(e0 - 1 - t) : (float)(t - s0 + 1));
+            }
+            const float du = __shfl_sync(0xffffffffu, lane_st.y, r);
+            const bool ok = t < e0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float v = x[j];
+                if (phi) v = phi_elu1(v);
+                v = ok ? v * w : 0.f;  // (past the end: the loads were skipped)
+                x[j] = v;
+                if (normalize) zacc[j] = fmaf(role == 0 ? 1.f : du, v, zacc[j]);
+            }
+            float4* dst = reinterpret_cast<float4*>(As + ((size_t)buf * KT + r) * DK + pa * 8);
+            dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+            dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            const int r = rb0 + RB * n, t = t0 + r;
+            float y[8];
+            rawB[n].to_f32(y);
+            const float den = __shfl_sync(0xffffffffu, lane_st.x, r);
+            const bool ok = t < e0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = ok ? (norm1 ? y[j] / den : y[j]) : 0.f;
+            float4* dst = reinterpret_cast<float4*>(Bs + ((size_t)buf * KT + r) * DV + pb * 8);
+            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int n = 0; n < TN; ++n) acc[m][n] = 0.f;
+    if (n_tiles > 0) {
+        fetch(0);
+        stage(0, 0);
+    }
+    __syncthreads();
+    for (int it = 0; it < n_tiles; ++it) {
+        const int buf = it & 1;
+        if (it + 1 < n_tiles) fetch(it + 1);
+        const float* a_t = As + (size_t)buf * KT * DK + ty * TM;
+        const float* b_t = Bs + (size_t)buf * KT * DV + tx * TN;
+#pragma unroll 4
+        for (int kk = 0; kk < KT; ++kk) {
+            float a[TM], b[TN];
+#pragma unroll
+            for (int m = 0; m < TM; m += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(a_t + kk * DK + m);
+                a[m] = v.x, a[m + 1] = v.y, a[m + 2] = v.z, a[m + 3] = v.w;
+            }
+#pragma unroll
+            for (int n = 0; n < TN; n += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(b_t + kk * DV + n);
+                b[n] = v.x, b[n + 1] = v.y, b[n + 2] = v.z, b[n + 3] = v.w;
+            }
+#pragma unroll
+            for (int m = 0; m < TM; ++m)
+#pragma unroll
+                for (int n = 0; n < TN; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+        }
+        if (it + 1 < n_tiles) stage(it + 1, buf ^ 1);
+        __syncthreads();
+    }
+    float* agg = role == 0 ? sg.agg : sg.agg1;
+    float* zagg = role == 0 ? sg.zagg : sg.zagg1;
+#pragma unroll
+    for (int m = 0; m < TM; ++m) {
+        float* row = agg + (sidx * DK + ty * TM + m) * DV + tx * TN;
+#pragma unroll
+        for (int n = 0; n < TN; n += 4)
+            *reinterpret_cast<float4*>(row + n) = make_float4(acc[m][n], acc[m][n + 1], acc[m][n + 2], acc[m][n + 3]);
+    }
+    // z: the loader threads' shares of each column, added row group by row group
+    float* zpart = gsm;  // [RA][DK] (the tiles are no longer read)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) zpart[ra0 * DK + pa * 8 + j] = zacc[j];
+    __syncthreads();
+    for (int d = tid; d < DK; d += 256) {
+        float z = 0.f;
+        for (int r = 0; r < RA; ++r) z += zpart[r * DK + d];
+        zagg[sidx * DK + d] = z;
+    }
+}
+
 }  // namespace
 
 int bwd_chunk_len(int dk, int dv, bool taylor) {
@@ -669,6 +907,8 @@ BwdPlan bwd_plan(int B, int H, int T, int dk, int dv, bool normalize, bool taylo
 }
 
 }  // namespace
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int bwd_state_rows(const BwdArgs& a) { return a.taylor ? taylor_feature_dim(a.dk) : a.dk; }
 
@@ -735,6 +975,31 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
             a.log_a ? fp(pl.o_l2) : nullptr, g);
         e = cudaGetLastError();
     };
+    // the segments' own contributions: the weighted product where its shape is
+    // built, else a state-only pass of the chunked kernel
+    const bool gemm_ok = !a.taylor && (a.dk == 64 || a.dk == 128) && (a.dv == 64 || a.dv == 128) &&
+                         aligned16(a.Q) && aligned16(a.K) && aligned16(a.V) && aligned16(a.dO);
+    auto contributions = [&](auto kern, auto cast, int role0, unsigned roles) {
+        if (!gemm_ok) {
+            launch(kern, cast, role0, roles, st);
+            return;
+        }
+        if (e != cudaSuccess) return;
+        auto go = [&](auto gk, size_t bytes) {
+            e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e != cudaSuccess) return;
+            TraceScope trace("bwd_state_gemm_kernel", s);
+            gk<<<dim3(nbh * pl.P, roles), 256, bytes, s>>>(
+                cast(a.Q), cast(a.K), cast(a.V), cast(a.dO), stats, a.log_a, a.H, a.T, a.phi, nm,
+                role0, pl.seg_chunks * C, g, st);
+            e = cudaGetLastError();
+        };
+        using E = std::remove_pointer_t<decltype(cast(a.Q))>;
+        if (a.dk == 64 && a.dv == 64) go(bwd_state_gemm_kernel<E, 64, 64>, gemm_smem_bytes<64, 64>());
+        else if (a.dk == 64) go(bwd_state_gemm_kernel<E, 64, 128>, gemm_smem_bytes<64, 128>());
+        else if (a.dv == 64) go(bwd_state_gemm_kernel<E, 128, 64>, gemm_smem_bytes<128, 64>());
+        else go(bwd_state_gemm_kernel<E, 128, 128>, gemm_smem_bytes<128, 128>());
+    };
     auto run = [&](auto kern, auto cast) {
         if (pl.P <= 1) {
             if (nm == 0) {
@@ -746,14 +1011,14 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
             return;
         }
         if (nm == 0) {  // both sweeps' contributions, entries, then both sweeps
-            launch(kern, cast, 0, 2, st);
+            contributions(kern, cast, 0, 2);
             scan(0, 2);
             launch(kern, cast, 0, 2, full);
         } else {  // the backward sweep's contributions need the forward sweep's den, du
-            launch(kern, cast, 0, 1, st);
+            contributions(kern, cast, 0, 1);
             scan(0, 1);
             launch(kern, cast, 0, 1, full);
-            launch(kern, cast, 1, 1, st);
+            contributions(kern, cast, 1, 1);
             scan(1, 1);
             launch(kern, cast, 1, 1, full);
         }
