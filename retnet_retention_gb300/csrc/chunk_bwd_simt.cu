@@ -69,6 +69,34 @@ struct BwdSeg {
                         // total log2 decay [BH][n_seg]
 };
 
+template <typename T>
+struct Raw8;  // 8 consecutive input elements in registers
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ void to_f32(float (&x)[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = __uint_as_float(w[e] << 16);
+            x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ void load(const float* p) {
+        a = __ldg(reinterpret_cast<const float4*>(p));
+        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ void to_f32(float (&x)[8]) const {
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w;
+        x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+    }
+};
+
 struct BwdSmem {  // offsets in floats
     int q, k, v, g, n, a, p, s, z, den, du, pw, cum, xw, tq, total;
 };
@@ -98,15 +126,23 @@ __host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv, bool taylor
     return L;
 }
 
-template <typename T>
+// DKc, DVc, CC: d_k, d_v and the chunk length fixed at compile time (0: the
+// arguments), so that the loops over them unroll and their index arithmetic folds.
+template <typename T, int DKc = 0, int DVc = 0, int CC = 0>
 __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
     const T* __restrict__ dO, const float* __restrict__ S0, const float* __restrict__ z0,
     const float* __restrict__ dST, const float* __restrict__ dzT, T* __restrict__ dQ,
     T* __restrict__ dK, T* __restrict__ dV, float* __restrict__ dS0, float* __restrict__ dz0,
-    float* __restrict__ stats, int H, int T_len, int dk, int dv, int C, int phi, int normalize,
-    float eps, int role0, const float* __restrict__ log_a, const __grid_constant__ KernelGammas g,
-    const __grid_constant__ BwdSeg sg, int d_in, int taylor) {
+    float* __restrict__ stats, int H, int T_len, int dk_arg, int dv_arg, int C_arg, int phi,
+    int normalize, float eps, int role0, const float* __restrict__ log_a,
+    const __grid_constant__ KernelGammas g, const __grid_constant__ BwdSeg sg, int d_in, int taylor) {
+    const int dk = DKc ? DKc : dk_arg;
+    const int dv = DVc ? DVc : dv_arg;
+    const int C = CC ? CC : C_arg;
+    // fixed shapes: rows of Q, K, V and dO loaded 8 elements at a time (16 bytes
+    // of bf16; the host checks the alignment)
+    constexpr bool kVec = DKc > 0 && DVc > 0 && DKc % 8 == 0 && DVc % 8 == 0;
     extern __shared__ float smem[];
     const BwdSmem lay = bwd_layout(C, dk, dv, taylor != 0);
     float* Qs = smem + lay.q;
@@ -183,7 +219,29 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
         // tiles: phi(Q), phi(K), V, dO (rows >= L zero); a state-only pass reads
         // K and V (forward sweep) or Q and dO (backward sweep) only
         const bool need_qg = !st_only || role == 1, need_kv = !st_only || role == 0;
-        for (int idx = tid; idx < C * dk; idx += kThreads) {
+        if constexpr (kVec) {  // Q and K 8 elements a load
+            for (int idx = tid; idx < C * dk / 8; idx += kThreads) {
+                const int i = idx / (dk / 8), d0 = (idx % (dk / 8)) * 8;
+                float x[8], y[8];
+                const size_t gi = qk_base + (size_t)(t0 + i) * dk + d0;
+                Raw8<T> rx, ry;
+                if (i < L && need_qg) rx.load(Q + gi);
+                if (i < L && need_kv) ry.load(K + gi);
+                rx.to_f32(x);
+                ry.to_f32(y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float xv = x[e], yv = y[e];
+                    if (phi) {
+                        xv = phi_elu1(xv);
+                        yv = phi_elu1(yv);
+                    }
+                    Qs[i * ldk + d0 + e] = i < L && need_qg ? xv : 0.f;
+                    Ks[i * ldk + d0 + e] = i < L && need_kv ? yv : 0.f;
+                }
+            }
+        }
+        for (int idx = tid; idx < (kVec ? 0 : C * dk); idx += kThreads) {
             const int i = idx / dk, d = idx % dk;
             float x = 0.f, y = 0.f;
             if (i < L && taylor) {
@@ -212,7 +270,24 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             Qs[i * ldk + d] = x;
             Ks[i * ldk + d] = y;
         }
-        for (int idx = tid; idx < C * dv; idx += kThreads) {
+        if constexpr (kVec) {  // V and dO 8 elements a load
+            for (int idx = tid; idx < C * dv / 8; idx += kThreads) {
+                const int i = idx / (dv / 8), c0 = (idx % (dv / 8)) * 8;
+                float x[8], y[8];
+                const size_t gi = v_base + (size_t)(t0 + i) * dv + c0;
+                Raw8<T> rx, ry;
+                if (i < L && need_kv) rx.load(V + gi);
+                if (i < L && need_qg) ry.load(dO + gi);
+                rx.to_f32(x);
+                ry.to_f32(y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    Vs[i * ldv + c0 + e] = i < L && need_kv ? x[e] : 0.f;
+                    Gs[i * ldv + c0 + e] = i < L && need_qg ? y[e] : 0.f;
+                }
+            }
+        }
+        for (int idx = tid; idx < (kVec ? 0 : C * dv); idx += kThreads) {
             const int i = idx / dv, cc2 = idx % dv;
             float x = 0.f, y = 0.f;
             if (i < L) {
@@ -629,34 +704,6 @@ __global__ void bwd_scan_kernel(const __grid_constant__ ScanArgs sc, int BH, int
 // columns, so it also sums its share of z; the shares are added in a fixed order.
 constexpr int kGemmKT = 32;
 
-template <typename T>
-struct Raw8;  // 8 consecutive input elements in registers
-template <>
-struct Raw8<__nv_bfloat16> {
-    uint4 u;
-    __device__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
-    __device__ void to_f32(float (&x)[8]) const {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            x[2 * e] = __uint_as_float(w[e] << 16);
-            x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-        }
-    }
-};
-template <>
-struct Raw8<float> {
-    float4 a, b;
-    __device__ void load(const float* p) {
-        a = __ldg(reinterpret_cast<const float4*>(p));
-        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    }
-    __device__ void to_f32(float (&x)[8]) const {
-        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w;
-        x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
-    }
-};
-
 template <int DK, int DV>
 constexpr size_t gemm_smem_bytes() {
     return (size_t)2 * kGemmKT * (DK + DV) * sizeof(float);
@@ -1023,9 +1070,14 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
             launch(kern, cast, 1, 1, full);
         }
     };
-    if (a.bf16)
-        run(chunk_bwd_simt_kernel<__nv_bfloat16>,
-            [](const void* p) { return (__nv_bfloat16*)const_cast<void*>(p); });
+    auto bf = [](const void* p) { return (__nv_bfloat16*)const_cast<void*>(p); };
+    const bool plain = !a.taylor && C == 32 && gemm_ok;  // (gemm_ok: 16-byte aligned rows)
+    if (a.bf16 && plain && a.dk == 64 && a.dv == 64)
+        run(chunk_bwd_simt_kernel<__nv_bfloat16, 64, 64, 32>, bf);
+    else if (a.bf16 && plain && a.dk == 128 && a.dv == 128)
+        run(chunk_bwd_simt_kernel<__nv_bfloat16, 128, 128, 32>, bf);
+    else if (a.bf16)
+        run(chunk_bwd_simt_kernel<__nv_bfloat16>, bf);
     else
         run(chunk_bwd_simt_kernel<float>, [](const void* p) { return (float*)const_cast<void*>(p); });
     return e;
