@@ -111,8 +111,8 @@ __host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv, bool taylor
     L.k = L.q + C * ldk;
     L.v = L.k + C * ldk;
     L.g = L.v + C * ldv;   // dO, then dn = dO / den
-    L.n = L.g + C * ldv;   // n_i (forward sweep)
-    L.a = L.n + C * ldv;
+    L.n = L.g + C * ldv;   // n_i (forward sweep); the decayed copy for the state update
+    L.a = L.n + C * (dv + 4);
     L.p = L.a + C * lda;
     L.s = L.p + C * lda;   // S (forward sweep) or G (backward sweep), rows dv + 1 apart
     L.z = L.s + dk * ldv;  // z or Gz
@@ -128,8 +128,11 @@ __host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv, bool taylor
 
 // DKc, DVc, CC: d_k, d_v and the chunk length fixed at compile time (0: the
 // arguments), so that the loops over them unroll and their index arithmetic folds.
+// Registers: 64 a thread for the run-time shapes (four CTAs an SM), 80 for
+// d_k = d_v = 64 (three CTAs, as many as its shared memory allows), no limit for
+// 128 (one CTA).
 template <typename T, int DKc = 0, int DVc = 0, int CC = 0>
-__global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
+__global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 64 ? 3 : 1) chunk_bwd_simt_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
     const T* __restrict__ dO, const float* __restrict__ S0, const float* __restrict__ z0,
     const float* __restrict__ dST, const float* __restrict__ dzT, T* __restrict__ dQ,
@@ -337,6 +340,53 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
                 body((rest / ng) * 4, c0, c0 + 32);
             }
         };
+        // Fixed shapes: the state's update Ss = gL Ss + X^T (w . Y) over the chunk's
+        // rows (X = K~, Y = V, w = zeta forward; X = Q~, Y = dn, w = xi backward).
+        // w . Y goes to the n buffer with rows d_v + 4 apart (16-byte aligned), then
+        // thread t takes the 4 x 4 block at rows 4 (t / (d_v / 4)) and columns
+        // 4 (t % (d_v / 4)): per row of the chunk one 16-byte load of w . Y and four
+        // loads of X that the warp's lanes share, for 16 FMAs.
+        auto state_update = [&](const float* X, const float* Y, auto&& w, float gL) {
+            if constexpr (kVec) {
+                constexpr int ldw = DVc + 4, NG = DVc / 4;
+                float* Ws = Ns;
+                for (int idx = tid; idx < CC * NG; idx += kThreads) {
+                    const int j = idx / NG, c = (idx % NG) * 4;
+                    const float wj = j < L ? w(j) : 0.f;
+                    const float* y = Y + j * ldv + c;
+                    *reinterpret_cast<float4*>(Ws + j * ldw + c) =
+                        make_float4(wj * y[0], wj * y[1], wj * y[2], wj * y[3]);
+                }
+                __syncthreads();
+                for (int tI = tid; tI < DKc * NG / 4; tI += kThreads) {
+                    const int d0 = (tI / NG) * 4, c0 = (tI % NG) * 4;
+                    float u[4][4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) u[r][e] = 0.f;
+#pragma unroll 8
+                    for (int j = 0; j < CC; ++j) {
+                        const float4 wy = *reinterpret_cast<const float4*>(Ws + j * ldw + c0);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float x = X[j * ldk + d0 + r];
+                            u[r][0] = fmaf(x, wy.x, u[r][0]);
+                            u[r][1] = fmaf(x, wy.y, u[r][1]);
+                            u[r][2] = fmaf(x, wy.z, u[r][2]);
+                            u[r][3] = fmaf(x, wy.w, u[r][3]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float* sp = Ss + (d0 + r) * lds + c0 + e;
+                            *sp = fmaf(gL, *sp, u[r][e]);
+                        }
+                }
+            }
+        };
 
         // A_ij = D_ij q~_i . k~_j (j <= i): tiles of 4 rows i and one column j
         for (int item = tid; item < (st_only ? 0 : ((L + 3) >> 2) * 32); item += kThreads) {
@@ -494,7 +544,9 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             // Taylor map: dq = the features' gradient through the map's transpose Jacobian
             if (taylor && !st_only) taylor_back(TQ, Qs, dQ, L, t0);
             // S = gamma^L S + sum_j zeta_j k~_j^T v_j ; z likewise
-            tiles(dk, dv, [&](int d0, int c0, int c1) {
+            if constexpr (kVec) {
+                state_update(Ks, Vs, [&](int j) { return zt(j); }, gL);
+            } else tiles(dk, dv, [&](int d0, int c0, int c1) {
                 const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
                 float u[4][2] = {};
                 for (int j = 0; j < L; ++j) {
@@ -595,7 +647,9 @@ __global__ void __launch_bounds__(kThreads) chunk_bwd_simt_kernel(
             __syncthreads();
             if (taylor && !st_only) taylor_back(TQ, Ks, dK, L, t0);  // dk through the map
             // G = gamma^L G + sum_i xi_i q~_i^T dn_i ;  Gz = gamma^L Gz + sum_i xi_i du_i q~_i
-            tiles(dk, dv, [&](int d0, int c0, int c1) {
+            if constexpr (kVec) {
+                state_update(Qs, Gs, [&](int i) { return xi(i); }, gL);
+            } else tiles(dk, dv, [&](int d0, int c0, int c1) {
                 const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
                 float u[4][2] = {};
                 for (int i = 0; i < L; ++i) {
