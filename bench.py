@@ -50,8 +50,8 @@ KERNEL_SOURCES = ("chunk_tc_ws.cuh", "chunk_tc_ws.cu", "chunk_tc_common.cuh", "t
 TRAFFIC = {
     # (workload, kernel): bytes per launch
     ("msr_retention_bf16", "chunk_tc_ws_kernel/full"): {
-        "bytes": 1_074_105_344 + 521_304_576,
-        "sources_sha256": "739e2496313f5f5f824747fa49cc056924ca6e548359a983e6c5f8f2c055b99d",
+        "bytes": 1_077_857_024 + 519_900_416,
+        "sources_sha256": "148fb15eb52a33fe1b9a4379ac22a1ec86a41a23619a37f5caa3d522899d5bed",
     },
 }
 HEADLINE = "msr_retention_bf16"

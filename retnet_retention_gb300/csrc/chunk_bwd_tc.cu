@@ -66,6 +66,26 @@ __global__ void __launch_bounds__(256) state_scale_kernel(const float* __restric
     (void)total;
 }
 
+// out[b][j][i] = scale[h] * in[b][i][j] for b < nb matrices of R x Cc (R, Cc multiples
+// of 32), through 32 x 32 tiles in shared memory so that both the reads and the
+// writes take whole rows.  Block (32, 8); grid (Cc / 32, R / 32, nb).
+__global__ void __launch_bounds__(256) state_transpose_kernel(const float* __restrict__ in,
+                                                              float* __restrict__ out, int H, int R,
+                                                              int Cc, int inverse,
+                                                              const __grid_constant__ KernelGammas g) {
+    __shared__ float tile[32][33];
+    const size_t b = blockIdx.z;
+    const size_t per = (size_t)R * Cc;
+    const float gm = g.gamma[b % H];
+    const float sc = inverse ? 1.f / gm : gm;
+    const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+    for (int r = threadIdx.y; r < 32; r += 8)
+        tile[r][threadIdx.x] = in[b * per + (size_t)(i0 + r) * Cc + j0 + threadIdx.x];
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8)
+        out[b * per + (size_t)(j0 + r) * R + i0 + threadIdx.x] = sc * tile[threadIdx.x][r];
+}
+
 cudaError_t reverse_time(const void* in, void* out, size_t nbh, int T, int d, cudaStream_t s) {
     const int ppr = d * 2 / 16;
     const size_t total = nbh * (size_t)T * ppr;
@@ -78,6 +98,12 @@ cudaError_t reverse_time(const void* in, void* out, size_t nbh, int T, int d, cu
 
 cudaError_t state_scale(const float* in, float* out, size_t nbh, int H, int R, int Cc,
                         bool transpose, bool inverse, const KernelGammas& g, cudaStream_t s) {
+    if (transpose && R % 32 == 0 && Cc % 32 == 0 && nbh <= 65535) {
+        TraceScope trace("state_transpose_kernel", s);
+        state_transpose_kernel<<<dim3((unsigned)(Cc / 32), (unsigned)(R / 32), (unsigned)nbh), dim3(32, 8),
+                                 0, s>>>(in, out, H, R, Cc, inverse ? 1 : 0, g);
+        return cudaGetLastError();
+    }
     const size_t per = (size_t)R * Cc;
     dim3 grid((unsigned)std::min<size_t>((per + 255) / 256, 64), (unsigned)nbh);
     TraceScope trace("state_scale_kernel", s);
