@@ -414,9 +414,32 @@ def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> 
                bytes=decode_bytes(c), flops=decode_flops(c))
     # (the traced repeat continues the same recurrence; only its timing is used)
     res["kernels"] = kernel_breakdown(la, step, min(steps_total, 64), stream)
+    res["graph"] = decode_graph(la, dq, dk, dv, o, S, gamma, steps_total)
     del dq, dk, dv, o, S
     torch.cuda.empty_cache()
     return res
+
+
+def decode_graph(la, dq, dk, dv, o, S, gamma, steps_total: int) -> dict:
+    """The same decode steps captured once in a CUDA graph and replayed: the
+    launches cost no host work.  The graph runs the recurrence on its own copy of
+    the state.  Reported beside the stream-launched timing, not instead of it."""
+    S_g = S.clone()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    try:
+        with torch.cuda.graph(g, stream=side):
+            for i in range(steps_total):
+                la.recurrent_step(dq[i], dk[i], dv[i], gamma, S_g, out=o[i], stream=side)
+    except RuntimeError as e:
+        del S_g
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    stream = torch.cuda.current_stream()
+    g.replay()  # warm-up replay
+    ms = time_region(lambda i: g.replay(), 1, stream)
+    del g, S_g
+    return {"ms_per_step": ms / steps_total, "steps": steps_total, "launches": steps_total}
 
 
 def oracle_baseline(name: str, budget_s: float = 12.0) -> dict:
@@ -475,7 +498,8 @@ def run_ours(args) -> dict | None:
         dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         if rank == 0:
             print(json.dumps({"only": "decode", "ms_per_step": dec["ms"],
-                              "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9}))
+                              "hbm_gbs": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9,
+                              "graph": dec["graph"]}))
         return None
     if only in ("backward", "backward_" + BWD_TC):  # profiling aid: one backward pass alone
         r = bwd_measure(la, BWD_SIMT if only == "backward" else BWD_TC, args.steps, args.warmup,
@@ -600,7 +624,7 @@ def run_ours(args) -> dict | None:
                      f"state after a {dc['T']}-token prefill, {dec['steps']} steps",
             steps_per_s=1e3 / dec["ms"], ms_per_step=dec["ms"], hbm_gbs=gbs,
             roofline_frac=gbs / pk["hbm_gbs"], kernel="decode_step_kernel",
-            kernels=dec["kernels"])
+            kernels=dec["kernels"], graph=dec["graph"])
         line["workloads"] = sub
     clocks = sampler.summary()
     if clocks is not None:
