@@ -141,6 +141,9 @@ REVERSE_CASES = [  # shape, gammas, whether the kernel walks reversed time itsel
     ((2, 2, 3000, 64, 128), [0.999, 0.8], True),    # segments (scan), d_k != d_v
     ((2, 16, 1000, 128, 64), 0.97, True),           # segments folded in the output walk
     ((1, 1, 129, 128, 128), [0.71], True),         # near the factored form's floor: 0.71^127 = 2^-62.7
+    ((1, 1, 1, 64, 64), [0.9], True),               # one token: the chunk starts 127 rows before 0
+    ((2, 3, 100, 128, 64), [0.95, 1.0, 0.8], True),   # one partial chunk per sequence
+    ((8, 16, 256, 64, 128), 0.99, True),             # more units than SMs: no segments
     ((1, 2, 300, 64, 64), [0.5, 0.9], False),       # gamma^127 < 2^-64: reversed copies
     ((1, 2, 3000, 128, 64), [0.6, 0.99], False),    # the same with segments
 ]
