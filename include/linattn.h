@@ -320,10 +320,9 @@ LA_API size_t la_bwd_workspace_size(int B, int H, int T, int d_k, int d_v, la_dt
  * library holds until the process exits.  It allocates nothing.
  *
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.  The cached address holds until the device is reset
- *     (cudaDeviceReset); calls after a reset in the same process are not
- *     supported.
+ *     that device current) and caches it.  The cached address holds until the
+ *     device is reset (cudaDeviceReset); calls after a reset in the same
+ *     process are not supported.
  *   - Calls whose la_workspace_size exceeds LA_NOALLOC_SCRATCH_BYTES return
  *     LA_ERR_INVALID_ARG without launching anything.
  *   - Every call shares the one array, and the array keeps whatever the last

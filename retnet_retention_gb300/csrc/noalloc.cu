@@ -14,8 +14,7 @@
 // Every GPU that loads this library holds it until the process exits.  Host
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress while that
-// device is current and caches it; that first call should come before any
-// stream capture.
+// device is current and caches it.
 #include <cstdint>
 #include <mutex>
 
