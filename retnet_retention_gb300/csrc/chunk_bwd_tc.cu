@@ -175,10 +175,317 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
     return p;
 }
 
+// ---- The normalised backward (phi or not, floored or not) as a composite.
+//
+// With n_t = q~_t S_t, u_t = q~_t . z_t, dd_t = max(|u_t|, 1) or u_t + eps and
+// o_t = n_t / dd_t, the loss's gradients with respect to n_t and u_t are
+// dn_t = do_t / dd_t and du_t = -(do_t . o_t) / dd_t * dd'(u_t), and
+//   dq~_t = S_t dn_t + du_t z_t = sum_{s<=t} gamma^(t-s) (dn_t . v_s + du_t) k~_s
+//           + gamma^(t+1) (S_0 dn_t + du_t z_0),
+//   dk~_t = G_t v_t + Gz_t = sum_{s>=t} gamma^(s-t) (v_t . dn_s + du_s) q~_s (+ the
+//           final-state terms), dv_t = k~_t G_t,
+// so each is a forward pass with augmented operands: dq~ over queries
+// [dn | du_hi | du_lo | 0], keys [v | 1 | 1 | 0] (128 wide: du split into two bf16
+// parts, so that the sum keeps about 16 bits), values k~; dk~ over the reversed
+// sequence with queries [v | 1 | 1 | 0], keys [dn | du_hi | du_lo | 0], values q~;
+// dv over the reversed sequence with queries k~, keys q~, values dn.  dd and du come
+// from the forward pass itself (its output walk's E2, in fp32), dq = dq~ phi'(q),
+// dk = dk~ phi'(k) ("Linear attention" page, "Decoding, training, and what each
+// costs": the gradients are cumulative sums; the normalised form of "Transformers
+// are RNNs", section 3.2).  d_v = 64 (the augmented width fits one 128-column
+// block).
+
+constexpr int kAugW = 128;  // width of the augmented operands
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Per token row: q~ = phi(q), k~ = phi(k), dn = do / dd (bf16), the augmented
+// [dn | du_hi | du_lo | 0] and [v | 1 | 1 | 0].  One thread per 16-byte piece of a
+// 128-wide row (pieces 0..7 carry the 64 value columns, piece 8 the two extra
+// columns, the rest zeros; pieces below d_k / 8 also carry q~ and k~).
+__global__ void __launch_bounds__(256) aug_prep_kernel(
+    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+    const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ dO,
+    const float* __restrict__ stats, __nv_bfloat16* __restrict__ qt, __nv_bfloat16* __restrict__ kt,
+    __nv_bfloat16* __restrict__ dn, __nv_bfloat16* __restrict__ xq, __nv_bfloat16* __restrict__ xk,
+    size_t rows, int dk, int phi) {
+    constexpr int dv = 64;
+    const size_t total = rows * (kAugW / 8);
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = idx / (kAugW / 8);
+        const int pc = (int)(idx % (kAugW / 8));
+        uint4 wq = make_uint4(0u, 0u, 0u, 0u), wk = make_uint4(0u, 0u, 0u, 0u);
+        if (pc < dv / 8) {
+            const float inv = 1.f / stats[row * 2];
+            const uint4 g = *reinterpret_cast<const uint4*>(dO + row * dv + pc * 8);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[e] = pack2(__uint_as_float(gw[e] << 16) * inv, __uint_as_float(gw[e] & 0xffff0000u) * inv);
+            wq = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dn + row * dv + pc * 8) = wq;
+            wk = *reinterpret_cast<const uint4*>(V + row * dv + pc * 8);
+        } else if (pc == dv / 8) {
+            const float du = stats[row * 2 + 1];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(du);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(du - __bfloat162float(hi));
+            wq.x = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+            wk.x = 0x3F803F80u;  // two bf16 ones
+        }
+        *reinterpret_cast<uint4*>(xq + row * kAugW + pc * 8) = wq;
+        *reinterpret_cast<uint4*>(xk + row * kAugW + pc * 8) = wk;
+        if (pc < dk / 8) {
+            const uint4 a = *reinterpret_cast<const uint4*>(Q + row * dk + pc * 8);
+            const uint4 b = *reinterpret_cast<const uint4*>(K + row * dk + pc * 8);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            uint32_t oq[4], ok[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float q0 = __uint_as_float(aw[e] << 16), q1 = __uint_as_float(aw[e] & 0xffff0000u);
+                float k0 = __uint_as_float(bw[e] << 16), k1 = __uint_as_float(bw[e] & 0xffff0000u);
+                if (phi) {
+                    q0 = phi_elu1(q0), q1 = phi_elu1(q1), k0 = phi_elu1(k0), k1 = phi_elu1(k1);
+                }
+                oq[e] = pack2(q0, q1);
+                ok[e] = pack2(k0, k1);
+            }
+            *reinterpret_cast<uint4*>(qt + row * dk + pc * 8) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+            *reinterpret_cast<uint4*>(kt + row * dk + pc * 8) = make_uint4(ok[0], ok[1], ok[2], ok[3]);
+        }
+    }
+}
+
+// An augmented pass's state [b][128][d_k] from a state S [b][d_k][d_v] (null: zero)
+// and z [b][d_k] (null: zero), times 1 or 1/gamma_h: rows 0 .. d_v-1 hold S's
+// transpose, row d_v holds z, row d_v + 1 z too where both extra query columns read
+// it (dup: du_hi and du_lo each times z) or zero where their sum is read, the rest
+// zeros.
+__global__ void __launch_bounds__(256) aug_state_kernel(const float* __restrict__ S,
+                                                        const float* __restrict__ z,
+                                                        float* __restrict__ out, size_t nbh, int H,
+                                                        int dk, int dv, int inverse, int dup,
+                                                        const __grid_constant__ KernelGammas g) {
+    const size_t total = nbh * kAugW * dk;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (size_t)gridDim.x * blockDim.x) {
+        const size_t b = e / ((size_t)kAugW * dk);
+        const int c = (int)((e / dk) % kAugW), d = (int)(e % dk);
+        const float sc = inverse ? 1.f / g.gamma[b % H] : 1.f;
+        float x = 0.f;
+        if (c < dv && S) x = S[(b * dk + d) * dv + c];
+        else if ((c == dv || (dup && c == dv + 1)) && z) x = z[b * dk + d];
+        out[e] = sc * x;
+    }
+}
+
+// out = bf16(x~ * phi'(x)) elementwise (phi'(x) = 1 above zero, e^x at or below;
+// 1 without phi), 8 elements a thread.
+__global__ void __launch_bounds__(256) phi_grad_kernel(const __nv_bfloat16* __restrict__ g,
+                                                       const __nv_bfloat16* __restrict__ x,
+                                                       __nv_bfloat16* __restrict__ out, size_t n8,
+                                                       int phi) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 a = reinterpret_cast<const uint4*>(g)[i];
+        const uint4 b = reinterpret_cast<const uint4*>(x)[i];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float g0 = __uint_as_float(aw[e] << 16), g1 = __uint_as_float(aw[e] & 0xffff0000u);
+            if (phi) {
+                const float x0 = __uint_as_float(bw[e] << 16), x1 = __uint_as_float(bw[e] & 0xffff0000u);
+                g0 *= x0 > 0.f ? 1.f : expf(x0);
+                g1 *= x1 > 0.f ? 1.f : expf(x1);
+            }
+            o[e] = pack2(g0, g1);
+        }
+        reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// dz_0[b][d] = gamma_h (fin[b][d_v][d] + fin[b][d_v + 1][d]) (the dk~ pass's final
+// state rows of du_hi and du_lo).
+__global__ void __launch_bounds__(256) aug_dz0_kernel(const float* __restrict__ fin,
+                                                      float* __restrict__ dz0, size_t nbh, int H,
+                                                      int dk, int dv,
+                                                      const __grid_constant__ KernelGammas g) {
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= nbh * dk) return;
+    const size_t b = e / dk;
+    const int d = (int)(e % dk);
+    const float* f = fin + b * kAugW * dk;
+    dz0[e] = g.gamma[b % H] * (f[(size_t)dv * dk + d] + f[(size_t)(dv + 1) * dk + d]);
+}
+
+// The augmented composite's workspace (byte offsets), then the passes' own.
+struct BwdAugPlan {
+    size_t o_stats, o_qt, o_kt, o_dn, o_xq, o_xk, o_dqt, o_dkt, o_s0, o_gk0, o_g0, o_gkfin, o_gfin,
+        o_fwd, fwd_bytes, bytes;
+};
+
+// The four passes' arguments (pointers filled in by the launcher).
+ChunkArgs aug_stats_args(const BwdArgs& a) {
+    ChunkArgs c = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H, a.T, a.dk,
+                           a.dv, nullptr, 0, nullptr);
+    c.phi = a.phi;
+    c.normalize = true;
+    c.floor_norm = a.floor_norm;
+    c.eps = a.eps;
+    return c;
+}
+ChunkArgs aug_pass_args(const BwdArgs& a, int width_qk, int width_v, bool reverse) {
+    ChunkArgs c = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H, a.T,
+                           width_qk, width_v, nullptr, 0, nullptr);
+    c.reverse = reverse;
+    return c;
+}
+
+bool aug_shape_ok(const BwdArgs& a) {
+    if (!a.bf16 || !a.normalize || a.taylor || a.log_a || a.T <= 0 || opt_tc_lockstep()) return false;
+    if (a.dv != 64 || (a.dk != 64 && a.dk != 128)) return false;
+    return tc_supported(aug_stats_args(a)) && tc_supported(aug_pass_args(a, kAugW, a.dk, false)) &&
+           tc_supported(aug_pass_args(a, a.dk, a.dv, false));
+}
+
+BwdAugPlan bwd_aug_plan(const BwdArgs& a) {
+    BwdAugPlan p;
+    const size_t nbh = (size_t)a.B * a.H, rows = nbh * a.T;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    p.o_stats = take(rows * 2 * sizeof(float));
+    p.o_qt = take(rows * a.dk * 2);
+    p.o_kt = take(rows * a.dk * 2);
+    p.o_dn = take(rows * a.dv * 2);
+    p.o_xq = take(rows * kAugW * 2);
+    p.o_xk = take(rows * kAugW * 2);
+    p.o_dqt = take(rows * a.dk * 2);
+    p.o_dkt = take(rows * a.dk * 2);
+    p.o_s0 = take(nbh * kAugW * a.dk * sizeof(float));
+    p.o_gk0 = take(nbh * kAugW * a.dk * sizeof(float));
+    p.o_g0 = take(nbh * a.dk * a.dv * sizeof(float));
+    p.o_gkfin = take(nbh * kAugW * a.dk * sizeof(float));
+    p.o_gfin = take(nbh * a.dk * a.dv * sizeof(float));
+    p.o_fwd = off;
+    p.fwd_bytes = std::max({tc_workspace_bytes(aug_stats_args(a)),
+                            tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, false)),
+                            tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, true)),
+                            tc_workspace_bytes(aug_pass_args(a, a.dk, a.dv, true))});
+    p.bytes = off + p.fwd_bytes;
+    return p;
+}
+
+unsigned grid_for(size_t work) {
+    return (unsigned)std::max<size_t>(1, std::min<size_t>((work + 255) / 256, 152 * 16));
+}
+
+cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) {
+    const BwdAugPlan p = bwd_aug_plan(a);
+    if (!a.workspace || a.workspace_bytes < p.bytes) return cudaErrorInvalidValue;
+    char* ws = static_cast<char*>(a.workspace);
+    auto bp = [&](size_t o) { return reinterpret_cast<__nv_bfloat16*>(ws + o); };
+    auto fp = [&](size_t o) { return reinterpret_cast<float*>(ws + o); };
+    const size_t nbh = (size_t)a.B * a.H, rows = nbh * a.T;
+    void* fws = ws + p.o_fwd;
+    cudaError_t e = cudaSuccess;
+    int launches = 0;
+    // 1. the forward pass, writing per token dd and du instead of O
+    float* stats = fp(p.o_stats);
+    ChunkArgs c0 = aug_stats_args(a);
+    c0.Q = a.Q; c0.K = a.K; c0.V = a.V; c0.O = nullptr;
+    c0.S0 = a.S0; c0.z0 = a.z0;
+    c0.workspace = fws; c0.workspace_bytes = p.fwd_bytes;
+    c0.stats_dO = a.dO; c0.stats = stats;
+    if ((e = launch_chunk_tc(c0, g, s, &launches)) != cudaSuccess) return e;
+    // 2. the pass operands
+    __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *dn = bp(p.o_dn), *xq = bp(p.o_xq),
+                  *xk = bp(p.o_xk), *dqt = bp(p.o_dqt), *dkt = bp(p.o_dkt);
+    {
+        TraceScope trace("aug_prep_kernel", s);
+        aug_prep_kernel<<<grid_for(rows * (kAugW / 8)), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
+            static_cast<const __nv_bfloat16*>(a.V), static_cast<const __nv_bfloat16*>(a.dO), stats,
+            qt, kt, dn, xq, xk, rows, a.dk, a.phi ? 1 : 0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 3. initial states: the dq~ pass from S_0^T and z_0; the reversed passes from
+    //    dS_T / gamma (and dz_T / gamma), entering after the last token
+    float* s0 = nullptr;
+    float* gk0 = nullptr;
+    float* g0 = nullptr;
+    auto aug_state = [&](const float* S, const float* z, float* out, int inverse, int dup) {
+        TraceScope trace("aug_state_kernel", s);
+        aug_state_kernel<<<grid_for(nbh * kAugW * a.dk), 256, 0, s>>>(S, z, out, nbh, a.H, a.dk, a.dv,
+                                                                    inverse, dup, g);
+        return cudaGetLastError();
+    };
+    if (a.S0 || a.z0) {
+        s0 = fp(p.o_s0);
+        if ((e = aug_state(a.S0, a.z0, s0, 0, 1)) != cudaSuccess) return e;
+    }
+    if (a.dS_T || a.dz_T) {
+        gk0 = fp(p.o_gk0);
+        if ((e = aug_state(a.dS_T, a.dz_T, gk0, 1, 0)) != cudaSuccess) return e;
+    }
+    if (a.dS_T) {
+        g0 = fp(p.o_g0);
+        if ((e = state_scale(a.dS_T, g0, nbh, a.H, a.dk, a.dv, false, true, g, s)) != cudaSuccess) return e;
+    }
+    // 4. dq~: queries [dn | du], keys [v | 1], values k~
+    ChunkArgs cq = aug_pass_args(a, kAugW, a.dk, false);
+    cq.Q = xq; cq.K = xk; cq.V = kt; cq.O = dqt; cq.S0 = s0;
+    cq.workspace = fws; cq.workspace_bytes = p.fwd_bytes;
+    if ((e = launch_chunk_tc(cq, g, s, &launches)) != cudaSuccess) return e;
+    // 5. dk~ in reversed time: queries [v | 1], keys [dn | du], values q~
+    float* gkfin = a.dz0 ? fp(p.o_gkfin) : nullptr;
+    ChunkArgs ck = aug_pass_args(a, kAugW, a.dk, true);
+    ck.Q = xk; ck.K = xq; ck.V = qt; ck.O = dkt; ck.S0 = gk0; ck.S_out = gkfin;
+    ck.workspace = fws; ck.workspace_bytes = p.fwd_bytes;
+    if ((e = launch_chunk_tc(ck, g, s, &launches)) != cudaSuccess) return e;
+    // 6. dv in reversed time: queries k~, keys q~, values dn; its final state is G_0
+    float* gfin = a.dS0 ? fp(p.o_gfin) : nullptr;
+    ChunkArgs cv = aug_pass_args(a, a.dk, a.dv, true);
+    cv.Q = kt; cv.K = qt; cv.V = dn; cv.O = a.dV; cv.S0 = g0; cv.S_out = gfin;
+    cv.workspace = fws; cv.workspace_bytes = p.fwd_bytes;
+    if ((e = launch_chunk_tc(cv, g, s, &launches)) != cudaSuccess) return e;
+    // 7. through phi: dq = dq~ phi'(q), dk = dk~ phi'(k)
+    {
+        TraceScope trace("phi_grad_kernel", s);
+        const size_t n8 = rows * a.dk / 8;
+        phi_grad_kernel<<<grid_for(n8), 256, 0, s>>>(dqt, static_cast<const __nv_bfloat16*>(a.Q),
+                                                    static_cast<__nv_bfloat16*>(a.dQ), n8, a.phi ? 1 : 0);
+        phi_grad_kernel<<<grid_for(n8), 256, 0, s>>>(dkt, static_cast<const __nv_bfloat16*>(a.K),
+                                                    static_cast<__nv_bfloat16*>(a.dK), n8, a.phi ? 1 : 0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 8. the initial state's gradients: dS_0 = gamma G_0, dz_0 = gamma Gz_0
+    if (a.dS0) {
+        if ((e = state_scale(gfin, a.dS0, nbh, a.H, a.dk, a.dv, false, false, g, s)) != cudaSuccess)
+            return e;
+    }
+    if (a.dz0) {
+        TraceScope trace("aug_dz0_kernel", s);
+        aug_dz0_kernel<<<(unsigned)((nbh * a.dk + 255) / 256), 256, 0, s>>>(gkfin, a.dz0, nbh, a.H, a.dk,
+                                                                          a.dv, g);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 bool bwd_tc_supported(const BwdArgs& a) {
-    if (!a.bf16 || a.phi || a.taylor || a.normalize || a.log_a || a.T <= 0) return false;
+    if (a.normalize) return aug_shape_ok(a);
+    if (!a.bf16 || a.phi || a.taylor || a.log_a || a.T <= 0) return false;
     if ((a.dk != 64 && a.dk != 128) || (a.dv != 64 && a.dv != 128)) return false;
     const ChunkArgs c1 = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H,
                                   a.T, a.dv, a.dk, nullptr, 0, nullptr);
@@ -187,9 +494,19 @@ bool bwd_tc_supported(const BwdArgs& a) {
     return tc_supported(c1) && tc_supported(c2);
 }
 
-size_t bwd_tc_workspace_bytes(const BwdArgs& a) { return bwd_tc_plan(a).bytes; }
+size_t bwd_tc_workspace_bytes(const BwdArgs& a) {
+    // (normalised: the CUDA-core kernel takes over where a gamma rules out the
+    // reversed-time passes, so the workspace covers both)
+    if (a.normalize) return std::max(bwd_aug_plan(a).bytes, bwd_workspace_bytes(a));
+    return bwd_tc_plan(a).bytes;
+}
 
 cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) {
+    if (a.normalize) {
+        ChunkArgs ck = aug_pass_args(a, kAugW, a.dk, true), cv = aug_pass_args(a, a.dk, a.dv, true);
+        if (!tc_reverse_supported(ck, g) || !tc_reverse_supported(cv, g)) return launch_chunk_bwd_simt(a, g, s);
+        return launch_aug(a, g, s);
+    }
     const BwdTcPlan p = bwd_tc_plan(a);
     if (!a.workspace || a.workspace_bytes < p.bytes) return cudaErrorInvalidValue;
     char* ws = static_cast<char*>(a.workspace);

@@ -813,6 +813,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     prm.fact = !a.log_a && !a.phi && !prm.track_z;
     for (int h = 0; h < a.H && prm.fact; ++h)
         prm.fact = g.gamma[h] < 1.f && g.log2g[h] * (float)(kC - 1) >= -64.f;
+    if (a.stats) {  // the backward pass's denominators and du, from the output walk's E2
+        if (!a.normalize || !a.bf16 || a.noncausal || !a.stats_dO || a.dv != dvb ||
+            !tc_ws_supported(kFull, a.dk, dvb, true))
+            return cudaErrorInvalidValue;
+        prm.dO = static_cast<const __nv_bfloat16*>(a.stats_dO);
+        prm.stats = a.stats;
+    }
     if (a.reverse) {  // the factored build alone walks reversed time
         if (!tc_reverse_supported(a, g)) return cudaErrorInvalidValue;
         prm.fact = 1;

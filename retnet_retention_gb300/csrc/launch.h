@@ -46,6 +46,10 @@ struct ChunkArgs {
     // walk is skipped (no normaliser, no z, no per-token decay).
     float* agg = nullptr;
     bool agg_ready = false;
+    // stats for the backward pass (normalising, one value block, pipelined
+    // kernel; O may be null): per token the denominator and du from dO, [B][H][T][2]
+    const void* stats_dO = nullptr;
+    float* stats = nullptr;
 };
 
 struct StepArgs {
