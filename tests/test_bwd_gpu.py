@@ -232,8 +232,9 @@ def test_bwd_matches_autograd_of_the_forward_kernel_inputs_on_fp32():
     check("dv", to_np(gv), v.grad.numpy(), TOL["f32"])
 
 
-def test_bwd_linear_attention_bf16_sampled():
-    """The headline workload's shape, gradients checked on a sample of sequences."""
+def test_bwd_linear_attention_bf16_full():
+    """The linear-attention workload's shape (B4 H8 T4096 d64, phi, normalised, on
+    the tensor-core composite), every sequence's gradients against the oracle."""
     c = workloads.CONFIGS["linear_attention_bf16"]
     x = workloads.make_inputs(c)
     B, H, T, dv = c["B"], c["H"], c["T"], c["dv"]
@@ -242,10 +243,60 @@ def test_bwd_linear_attention_bf16_sampled():
     q, k, v, g_o = (t.to(DEV) for t in (x["q"], x["k"], x["v"], dO))
     dq, dk, dv_, _, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], phi=True, normalize=True)
     torch.cuda.synchronize()
-    for (b, h) in workloads.sample_pairs(B, H, 3):
-        rq, rk, rv, _, _ = oracle.recurrent_bwd(x["q"][b, h][None, None], x["k"][b, h][None, None],
-                                                x["v"][b, h][None, None], [x["gamma"][h]],
-                                                dO[b, h][None, None], phi=True, normalize=True)
-        check(f"dq[{b},{h}]", to_np(dq[b, h]), rq[0, 0], TOL["bf16"])
-        check(f"dk[{b},{h}]", to_np(dk[b, h]), rk[0, 0], TOL["bf16"])
-        check(f"dv[{b},{h}]", to_np(dv_[b, h]), rv[0, 0], TOL["bf16"])
+    rq, rk, rv, _, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, phi=True,
+                                            normalize=True)
+    check("dq", to_np(dq), rq, TOL["bf16"])
+    check("dk", to_np(dk), rk, TOL["bf16"])
+    check("dv", to_np(dv_), rv, TOL["bf16"])
+
+
+NORM_CASES = [  # shape, phi, floor, gammas, the tensor-core composite expected
+    ((2, 2, 260, 64, 64), True, False, None, True),
+    ((1, 3, 300, 128, 64), True, True, [1.0, 0.9, 0.8], True),
+    ((1, 2, 300, 64, 64), False, True, [0.97, 0.99], True),
+    ((2, 16, 1000, 64, 64), True, False, 1.0, True),       # segments folded in the walks
+    ((1, 2, 3000, 64, 64), True, False, [1.0, 0.999], True),  # segments with a scan
+    ((1, 2, 200, 64, 64), True, False, [0.5, 0.9], False),   # gamma^127 < 2^-64: CUDA cores
+    ((1, 2, 130, 64, 128), True, False, None, False),        # d_v = 128: CUDA cores
+]
+
+
+@pytest.mark.parametrize("shape,phi,floor,gammas,composite", NORM_CASES,
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else None)
+def test_bwd_normalised_paths(shape, phi, floor, gammas, composite, opts):
+    """The normalised backward: the augmented tensor-core composite (the forward pass
+    writing dd and du, then forward passes over [dn | du] and [v | 1]) where it applies,
+    the CUDA-core kernel otherwise; which one ran is read from the launch trace.  With
+    an initial state and final-state gradients, and dS_0, dz_0 checked too."""
+    opts.path("auto")
+    B, H, T, dk, dv = shape
+    seed = zlib.crc32(repr((shape, phi, floor, gammas, "bwd-norm")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16", gamma=gammas, phi=phi,
+                              normalize=True)
+    rng = np.random.default_rng(seed)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    S0 = torch.from_numpy(np.abs(rng.standard_normal((B, H, dk, dv))).astype(np.float32) * 0.3)
+    z0 = torch.from_numpy(np.abs(rng.standard_normal((B, H, dk))).astype(np.float32) + 0.5)
+    dST = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.1)
+    dzT = torch.from_numpy(rng.standard_normal((B, H, dk)).astype(np.float32) * 0.1)
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    la.trace_enable(4096)
+    try:
+        la.trace_collect()
+        dq, dk_, dv_, dS0, dz0 = la.chunk_bwd(q, k, v, g_o, x["gamma"], phi=phi, normalize=True,
+                                              floor=floor, S0=S0.to(DEV), z0=z0.to(DEV),
+                                              dS_T=dST.to(DEV), dz_T=dzT.to(DEV))
+        torch.cuda.synchronize()
+        names = [n for n, _ in la.trace_collect()]
+    finally:
+        la.trace_enable(0)
+    assert ("aug_prep_kernel" in names) == composite, names
+    assert any(n.startswith("chunk_bwd_simt_kernel") for n in names) == (not composite), names
+    rq, rk, rv, rS0, rz0 = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, phi=phi,
+                                                normalize=True, floor=floor, S0=S0, z0=z0,
+                                                dS_T=dST, dz_T=dzT)
+    check("dq", to_np(dq), rq, TOL["bf16"])
+    check("dk", to_np(dk_), rk, TOL["bf16"])
+    check("dv", to_np(dv_), rv, TOL["bf16"])
+    check("dS0", to_np(dS0), rS0, TOL["bf16"])
+    check("dz0", to_np(dz0), rz0, TOL["bf16"])
