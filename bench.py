@@ -58,8 +58,8 @@ HEADLINE = "msr_retention_bf16"
 # the prefill workloads timed beside the headline
 SUB_PREFILL = ("linear_attention_bf16", "long_retention_bf16", "retention_floor_bf16",
                "gated_retention_bf16", "taylor_linear_attention_bf16")
-# the backward pass on the CUDA cores: normalised linear attention with phi
-BWD_SIMT = "linear_attention_bf16"
+# the backward pass of normalised linear attention with phi (tensor-core composite)
+BWD_NORM = "linear_attention_bf16"
 # the backward pass on the tensor cores: plain retention, d_k = d_v = 128
 BWD_TC = "long_retention_bf16"
 # the second-order Taylor feature map (273 features from d = 16)
@@ -420,6 +420,15 @@ def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> 
     return res
 
 
+def bwd_path(kernels: dict) -> str:
+    """The backward pass's path, from the kernels its traced step launched."""
+    if "aug_prep_kernel" in kernels:
+        return "tensor cores (forward pass with dd and du, then augmented forward passes)"
+    if any(k.startswith("chunk_tc_ws_kernel") for k in kernels):
+        return "tensor cores (three forward passes)"
+    return "CUDA cores"
+
+
 def decode_graph(la, dq, dk, dv, o, S, gamma, steps_total: int) -> dict:
     """The same decode steps captured once in a CUDA graph and replayed: the
     launches cost no host work.  The graph runs the recurrence on its own copy of
@@ -502,11 +511,13 @@ def run_ours(args) -> dict | None:
                               "graph": dec["graph"]}))
         return None
     if only in ("backward", "backward_" + BWD_TC):  # profiling aid: one backward pass alone
-        r = bwd_measure(la, BWD_SIMT if only == "backward" else BWD_TC, args.steps, args.warmup,
+        r = bwd_measure(la, BWD_NORM if only == "backward" else BWD_TC, args.steps, args.warmup,
                         rank, world)
         if rank == 0:
             print(json.dumps({"only": only, "ms": r["ms"],
-                              "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
+                              "alg_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9,
+                              "kernel_ms_per_step": {k: round(v["total_ms"] / args.steps, 5)
+                                                     for k, v in r["kernels"].items()}}))
         return None
     if only in (HEADLINE,) + SUB_PREFILL:  # profiling aid: one prefill workload alone
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world, batch=args.batch)
@@ -531,7 +542,7 @@ def run_ours(args) -> dict | None:
         dec = decode_measure(la, args.decode_steps, args.warmup, rank, world)
         dec["ms"] = max_over_ranks(dec["ms"])
         bwds = {}
-        for name in (BWD_SIMT, BWD_TC):
+        for name in (BWD_NORM, BWD_TC):
             r = bwd_measure(la, name, 3, args.warmup, rank, world)
             r["ms"] = max_over_ranks(r["ms"])
             bwds[name] = r
@@ -616,7 +627,7 @@ def run_ours(args) -> dict | None:
             sub["backward_" + name] = dict(
                 workload="backward of " + describe(name, bc) + " (gradients of Q, K, V and of "
                          "the initial state for a seeded N(0,1) dO)",
-                path="tensor cores (three forward passes)" if name == BWD_TC else "CUDA cores",
+                path=bwd_path(bwd["kernels"]),
                 tokens_per_s=bwd["tokens"] * world / (bwd["ms"] * 1e-3), ms=bwd["ms"],
                 alg_gbs=bgbs, roofline_frac=bgbs / pk["hbm_gbs"], kernels=bwd["kernels"])
         sub["decode_bf16"] = dict(

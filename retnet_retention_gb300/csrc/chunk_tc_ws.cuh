@@ -213,7 +213,9 @@ static_assert(kNumBars <= 32, "mbarrier slots");
 // gamma^(i+1) -> 2^(b_i), gamma^(L-1-j) -> 2^(b_(L-1) - b_j), gamma^L ->
 // 2^(b_(L-1)) (b in log2 units), and the score mask's running product steps by
 // a_j instead of gamma.
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
+// STATS: the output walk also writes the backward pass's per-token dd and du
+// (p.stats, from p.dO); a build of its own, so that the others carry none of it.
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT, bool STATS = false>
 __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
     static_assert(!FACT || (!GATED && !PHI && !NORM), "the factored decay is for plain retention");
     constexpr int kThreadsC = threads_c(DK, DVB, PHI);
@@ -948,7 +950,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 __nv_bfloat16* orow = p.O + tok * p.dv + v0;
                 // stats for the backward pass (normalised walks over all of d_v in one
                 // block): du = -(do . o) / dd * d dd/du, from the fp32 o of this row
-                const bool stats = NORM && p.stats != nullptr;
+                constexpr bool stats = NORM && STATS && !STATE_ONLY;
                 const __nv_bfloat16* drow = stats ? p.dO + tok * p.dv + v0 : nullptr;
                 float dot = 0.f;
                 // 64 columns a round in the factored build with 128 registers a thread
@@ -1013,7 +1015,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                         for (int e = 0; e < 16 * kW; ++e) held[rd][e] = pk[e];
                         continue;
                     }
-                    if (live && p.O) {
+                    if (live && (!stats || p.O)) {  // (the stats build may run without O)
 #pragma unroll
                         for (int h = 0; h < kHold; ++h) store_packed(held[h], 32 * kW * h);
                         store_packed(pk, 32 * kW * rd);
@@ -1199,10 +1201,11 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
 // pdl: launch as a programmatic dependent of the previous kernel in the stream
 // (the kernel's entry-state reads wait for that kernel; everything else may
 // start early).
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT = false>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT = false,
+          bool STATS = false>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI, GATED>;
-    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT, STATS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1268,6 +1271,17 @@ cudaError_t dispatch_ws(int dk, int dvb, bool normalize, const TcParams& prm, in
         if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true, false, GATED>(prm, grid, s, pdl);
         if constexpr (!GATED)  // (no room for the per-token decays beside two 96 KB stages)
             if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true, false, false>(prm, grid, s, pdl);
+        return cudaErrorInvalidValue;
+    }
+    if (normalize && prm.stats) {  // the backward's forward pass (per-head decay only)
+        if constexpr (!GATED) {
+            if (dk == 64 && dvb == 64)
+                return phi ? launch_ws<64, 64, true, false, true, false, false, true>(prm, grid, s, pdl)
+                           : launch_ws<64, 64, true, false, false, false, false, true>(prm, grid, s, pdl);
+            if (dk == 128 && dvb == 64)
+                return phi ? launch_ws<128, 64, true, false, true, false, false, true>(prm, grid, s, pdl)
+                           : launch_ws<128, 64, true, false, false, false, false, true>(prm, grid, s, pdl);
+        }
         return cudaErrorInvalidValue;
     }
     if (normalize) {
