@@ -67,20 +67,21 @@ __global__ void __launch_bounds__(256) state_scale_kernel(const float* __restric
 }
 
 // out[b][j][i] = scale[h] * in[b][i][j] for b < nb matrices of R x Cc (R, Cc multiples
-// of 32), through 32 x 32 tiles in shared memory so that both the reads and the
-// writes take whole rows.  Block (32, 8); grid (Cc / 32, R / 32, nb).
+// of 32; the input's matrices in_per elements apart, its first R rows read),
+// through 32 x 32 tiles in shared memory so that both the reads and the writes take
+// whole rows.  Block (32, 8); grid (Cc / 32, R / 32, nb).
 __global__ void __launch_bounds__(256) state_transpose_kernel(const float* __restrict__ in,
                                                               float* __restrict__ out, int H, int R,
-                                                              int Cc, int inverse,
+                                                              int Cc, size_t in_per, int inverse,
                                                               const __grid_constant__ KernelGammas g) {
     __shared__ float tile[32][33];
     const size_t b = blockIdx.z;
-    const size_t per = (size_t)R * Cc;
+    const size_t per = (size_t)R * Cc;  // (input matrices are in_per apart)
     const float gm = g.gamma[b % H];
     const float sc = inverse ? 1.f / gm : gm;
     const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
     for (int r = threadIdx.y; r < 32; r += 8)
-        tile[r][threadIdx.x] = in[b * per + (size_t)(i0 + r) * Cc + j0 + threadIdx.x];
+        tile[r][threadIdx.x] = in[b * in_per + (size_t)(i0 + r) * Cc + j0 + threadIdx.x];
     __syncthreads();
     for (int r = threadIdx.y; r < 32; r += 8)
         out[b * per + (size_t)(j0 + r) * R + i0 + threadIdx.x] = sc * tile[threadIdx.x][r];
@@ -101,7 +102,7 @@ cudaError_t state_scale(const float* in, float* out, size_t nbh, int H, int R, i
     if (transpose && R % 32 == 0 && Cc % 32 == 0 && nbh <= 65535) {
         TraceScope trace("state_transpose_kernel", s);
         state_transpose_kernel<<<dim3((unsigned)(Cc / 32), (unsigned)(R / 32), (unsigned)nbh), dim3(32, 8),
-                                 0, s>>>(in, out, H, R, Cc, inverse ? 1 : 0, g);
+                                 0, s>>>(in, out, H, R, Cc, (size_t)R * Cc, inverse ? 1 : 0, g);
         return cudaGetLastError();
     }
     const size_t per = (size_t)R * Cc;
@@ -185,39 +186,43 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
 //   dk~_t = G_t v_t + Gz_t = sum_{s>=t} gamma^(s-t) (v_t . dn_s + du_s) q~_s (+ the
 //           final-state terms), dv_t = k~_t G_t,
 // so each is a forward pass with augmented operands: dq~ over queries
-// [dn | du_hi | du_lo | 0], keys [v | 1 | 1 | 0] (128 wide: du split into two bf16
-// parts, so that the sum keeps about 16 bits), values k~; dk~ over the reversed
-// sequence with queries [v | 1 | 1 | 0], keys [dn | du_hi | du_lo | 0], values q~;
-// dv over the reversed sequence with queries k~, keys q~, values dn.  dd and du come
+// [dn | du_hi | du_lo], keys [v | 1 | 1] (du split into two bf16 parts, so that the
+// sum keeps about 16 bits; stored 72 wide, read as 128 by the d_k = 128 build, the
+// tensor maps filling the columns past the row with zeros), values k~; dk~ over the reversed
+// sequence with queries [v | 1 | 1], keys [dn | du_hi | du_lo], values q~; dv over
+// the reversed sequence with queries k~, keys q~, values dn (the first 64 columns
+// of [dn | du], read in place), its segments' contributions taken from the dk~
+// pass's (the transpose of their first 64 rows).  dd and du come
 // from the forward pass itself (its output walk's E2, in fp32), dq = dq~ phi'(q),
 // dk = dk~ phi'(k) ("Linear attention" page, "Decoding, training, and what each
 // costs": the gradients are cumulative sums; the normalised form of "Transformers
 // are RNNs", section 3.2).  d_v = 64 (the augmented width fits one 128-column
 // block).
 
-constexpr int kAugW = 128;  // width of the augmented operands
+constexpr int kAugW = 128;   // width of the augmented operands in the kernel
+constexpr int kAugCols = 72; // ... as stored (64 value columns, du_hi and du_lo or two ones, 6 zeros)
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Per token row: q~ = phi(q), k~ = phi(k), dn = do / dd (bf16), the augmented
-// [dn | du_hi | du_lo | 0] and [v | 1 | 1 | 0].  One thread per 16-byte piece of a
-// 128-wide row (pieces 0..7 carry the 64 value columns, piece 8 the two extra
-// columns, the rest zeros; pieces below d_k / 8 also carry q~ and k~).
+// Per token row: q~ = phi(q), k~ = phi(k) and the augmented [dn | du_hi | du_lo | 0]
+// and [v | 1 | 1 | 0] (kAugCols wide, dn = do / dd in bf16).  One thread per 16-byte
+// piece of a row (pieces 0..7 carry the 64 value columns, piece 8 the two extra
+// columns and zeros; pieces below d_k / 8 carry q~ and k~).
 __global__ void __launch_bounds__(256) aug_prep_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
     const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ dO,
     const float* __restrict__ stats, __nv_bfloat16* __restrict__ qt, __nv_bfloat16* __restrict__ kt,
-    __nv_bfloat16* __restrict__ dn, __nv_bfloat16* __restrict__ xq, __nv_bfloat16* __restrict__ xk,
-    size_t rows, int dk, int phi) {
+    __nv_bfloat16* __restrict__ xq, __nv_bfloat16* __restrict__ xk, size_t rows, int dk, int phi) {
     constexpr int dv = 64;
-    const size_t total = rows * (kAugW / 8);
+    const int pieces = max(kAugCols / 8, dk / 8);
+    const size_t total = rows * pieces;
     for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x) {
-        const size_t row = idx / (kAugW / 8);
-        const int pc = (int)(idx % (kAugW / 8));
+        const size_t row = idx / pieces;
+        const int pc = (int)(idx % pieces);
         uint4 wq = make_uint4(0u, 0u, 0u, 0u), wk = make_uint4(0u, 0u, 0u, 0u);
         if (pc < dv / 8) {
             const float inv = 1.f / stats[row * 2];
@@ -228,7 +233,6 @@ __global__ void __launch_bounds__(256) aug_prep_kernel(
             for (int e = 0; e < 4; ++e)
                 o[e] = pack2(__uint_as_float(gw[e] << 16) * inv, __uint_as_float(gw[e] & 0xffff0000u) * inv);
             wq = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dn + row * dv + pc * 8) = wq;
             wk = *reinterpret_cast<const uint4*>(V + row * dv + pc * 8);
         } else if (pc == dv / 8) {
             const float du = stats[row * 2 + 1];
@@ -237,8 +241,10 @@ __global__ void __launch_bounds__(256) aug_prep_kernel(
             wq.x = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
             wk.x = 0x3F803F80u;  // two bf16 ones
         }
-        *reinterpret_cast<uint4*>(xq + row * kAugW + pc * 8) = wq;
-        *reinterpret_cast<uint4*>(xk + row * kAugW + pc * 8) = wk;
+        if (pc < kAugCols / 8) {
+            *reinterpret_cast<uint4*>(xq + row * kAugCols + pc * 8) = wq;
+            *reinterpret_cast<uint4*>(xk + row * kAugCols + pc * 8) = wk;
+        }
         if (pc < dk / 8) {
             const uint4 a = *reinterpret_cast<const uint4*>(Q + row * dk + pc * 8);
             const uint4 b = *reinterpret_cast<const uint4*>(K + row * dk + pc * 8);
@@ -283,50 +289,71 @@ __global__ void __launch_bounds__(256) aug_state_kernel(const float* __restrict_
     }
 }
 
-// out = bf16(x~ * phi'(x)) elementwise (phi'(x) = 1 above zero, e^x at or below;
-// 1 without phi), 8 elements a thread.
-__global__ void __launch_bounds__(256) phi_grad_kernel(const __nv_bfloat16* __restrict__ g,
-                                                       const __nv_bfloat16* __restrict__ x,
-                                                       __nv_bfloat16* __restrict__ out, size_t n8,
-                                                       int phi) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const uint4 a = reinterpret_cast<const uint4*>(g)[i];
-        const uint4 b = reinterpret_cast<const uint4*>(x)[i];
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float g0 = __uint_as_float(aw[e] << 16), g1 = __uint_as_float(aw[e] & 0xffff0000u);
-            if (phi) {
-                const float x0 = __uint_as_float(bw[e] << 16), x1 = __uint_as_float(bw[e] & 0xffff0000u);
-                g0 *= x0 > 0.f ? 1.f : expf(x0);
-                g1 *= x1 > 0.f ? 1.f : expf(x1);
-            }
-            o[e] = pack2(g0, g1);
-        }
-        reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
+// The composite's last step, one launch: dq = bf16(dq~ phi'(q)) and dk = bf16(dk~
+// phi'(k)) 8 elements an item (phi'(x) = 1 above zero, e^x at or below; 1 without
+// phi), then dS_0 = gamma_h G_0 (the dv pass's final state, if wanted) and dz_0 =
+// gamma_h (fin[b][d_v][d] + fin[b][d_v + 1][d]) (the dk~ pass's final-state rows of
+// du_hi and du_lo, if wanted), one element an item.
+struct AugFinish {
+    const __nv_bfloat16* gq;  // dq~
+    const __nv_bfloat16* gk;  // dk~
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    __nv_bfloat16* out_q;  // dq
+    __nv_bfloat16* out_k;  // dk
+    const float* gfin;  // [b][d_k][d_v] or null
+    float* dS0;
+    const float* gkfin;  // [b][128][d_k] or null
+    float* dz0;
+    size_t n8, nS, nz;
+    int H, dk, dv, phi;
+};
 
-// dz_0[b][d] = gamma_h (fin[b][d_v][d] + fin[b][d_v + 1][d]) (the dk~ pass's final
-// state rows of du_hi and du_lo).
-__global__ void __launch_bounds__(256) aug_dz0_kernel(const float* __restrict__ fin,
-                                                      float* __restrict__ dz0, size_t nbh, int H,
-                                                      int dk, int dv,
-                                                      const __grid_constant__ KernelGammas g) {
-    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= nbh * dk) return;
-    const size_t b = e / dk;
-    const int d = (int)(e % dk);
-    const float* f = fin + b * kAugW * dk;
-    dz0[e] = g.gamma[b % H] * (f[(size_t)dv * dk + d] + f[(size_t)(dv + 1) * dk + d]);
+__global__ void __launch_bounds__(256) aug_finish_kernel(const __grid_constant__ AugFinish f,
+                                                         const __grid_constant__ KernelGammas g) {
+    const size_t total = 2 * f.n8 + f.nS + f.nz;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        if (i < 2 * f.n8) {
+            const bool second = i >= f.n8;
+            const size_t j = second ? i - f.n8 : i;
+            const uint4 a = reinterpret_cast<const uint4*>(second ? f.gk : f.gq)[j];
+            const uint4 b = reinterpret_cast<const uint4*>(second ? f.k : f.q)[j];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float g0 = __uint_as_float(aw[e] << 16), g1 = __uint_as_float(aw[e] & 0xffff0000u);
+                if (f.phi) {
+                    const float x0 = __uint_as_float(bw[e] << 16), x1 = __uint_as_float(bw[e] & 0xffff0000u);
+                    g0 *= x0 > 0.f ? 1.f : expf(x0);
+                    g1 *= x1 > 0.f ? 1.f : expf(x1);
+                }
+                o[e] = pack2(g0, g1);
+            }
+            reinterpret_cast<uint4*>(second ? f.out_k : f.out_q)[j] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else if (i < 2 * f.n8 + f.nS) {
+            const size_t j = i - 2 * f.n8;
+            const size_t b = j / ((size_t)f.dk * f.dv);
+            f.dS0[j] = g.gamma[b % f.H] * f.gfin[j];
+        } else {
+            const size_t j = i - 2 * f.n8 - f.nS;
+            const size_t b = j / f.dk;
+            const int d = (int)(j % f.dk);
+            const float* r = f.gkfin + b * kAugW * f.dk;
+            f.dz0[j] = g.gamma[b % f.H] * (r[(size_t)f.dv * f.dk + d] + r[(size_t)(f.dv + 1) * f.dk + d]);
+        }
+    }
 }
 
 // The augmented composite's workspace (byte offsets), then the passes' own.
 struct BwdAugPlan {
-    size_t o_stats, o_qt, o_kt, o_dn, o_xq, o_xk, o_dqt, o_dkt, o_s0, o_gk0, o_g0, o_gkfin, o_gfin,
-        o_fwd, fwd_bytes, bytes;
+    size_t o_stats, o_qt, o_kt, o_xq, o_xk, o_dqt, o_dkt, o_s0, o_gk0, o_g0, o_gkfin, o_gfin, o_aggk,
+        o_aggv, o_fwd, fwd_bytes, bytes;
+    // the dk~ and dv passes cut the sequences into the same segments (more than one):
+    // the dv pass takes its contributions from the dk~ pass's state walk
+    bool share;
+    int n_seg;
 };
 
 // The four passes' arguments (pointers filled in by the launcher).
@@ -365,9 +392,8 @@ BwdAugPlan bwd_aug_plan(const BwdArgs& a) {
     p.o_stats = take(rows * 2 * sizeof(float));
     p.o_qt = take(rows * a.dk * 2);
     p.o_kt = take(rows * a.dk * 2);
-    p.o_dn = take(rows * a.dv * 2);
-    p.o_xq = take(rows * kAugW * 2);
-    p.o_xk = take(rows * kAugW * 2);
+    p.o_xq = take(rows * kAugCols * 2);
+    p.o_xk = take(rows * kAugCols * 2);
     p.o_dqt = take(rows * a.dk * 2);
     p.o_dkt = take(rows * a.dk * 2);
     p.o_s0 = take(nbh * kAugW * a.dk * sizeof(float));
@@ -375,6 +401,13 @@ BwdAugPlan bwd_aug_plan(const BwdArgs& a) {
     p.o_g0 = take(nbh * a.dk * a.dv * sizeof(float));
     p.o_gkfin = take(nbh * kAugW * a.dk * sizeof(float));
     p.o_gfin = take(nbh * a.dk * a.dv * sizeof(float));
+    int nk = 1, sk = 0, nv = 1, sv = 0;
+    tc_segments(aug_pass_args(a, kAugW, a.dk, true), &nk, &sk);
+    tc_segments(aug_pass_args(a, a.dk, a.dv, true), &nv, &sv);
+    p.share = nk > 1 && nk == nv && sk == sv;
+    p.n_seg = nk;
+    p.o_aggk = take(p.share ? nbh * nk * kAugW * a.dk * sizeof(float) : 0);
+    p.o_aggv = take(p.share ? nbh * nk * a.dk * a.dv * sizeof(float) : 0);
     p.o_fwd = off;
     p.fwd_bytes = std::max({tc_workspace_bytes(aug_stats_args(a)),
                             tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, false)),
@@ -407,14 +440,14 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     c0.stats_dO = a.dO; c0.stats = stats;
     if ((e = launch_chunk_tc(c0, g, s, &launches)) != cudaSuccess) return e;
     // 2. the pass operands
-    __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *dn = bp(p.o_dn), *xq = bp(p.o_xq),
-                  *xk = bp(p.o_xk), *dqt = bp(p.o_dqt), *dkt = bp(p.o_dkt);
+    __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *xq = bp(p.o_xq), *xk = bp(p.o_xk),
+                  *dqt = bp(p.o_dqt), *dkt = bp(p.o_dkt);
     {
         TraceScope trace("aug_prep_kernel", s);
-        aug_prep_kernel<<<grid_for(rows * (kAugW / 8)), 256, 0, s>>>(
+        aug_prep_kernel<<<grid_for(rows * std::max(kAugCols / 8, a.dk / 8)), 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(a.Q), static_cast<const __nv_bfloat16*>(a.K),
             static_cast<const __nv_bfloat16*>(a.V), static_cast<const __nv_bfloat16*>(a.dO), stats,
-            qt, kt, dn, xq, xk, rows, a.dk, a.phi ? 1 : 0);
+            qt, kt, xq, xk, rows, a.dk, a.phi ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 3. initial states: the dq~ pass from S_0^T and z_0; the reversed passes from
@@ -443,39 +476,50 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     // 4. dq~: queries [dn | du], keys [v | 1], values k~
     ChunkArgs cq = aug_pass_args(a, kAugW, a.dk, false);
     cq.Q = xq; cq.K = xk; cq.V = kt; cq.O = dqt; cq.S0 = s0;
+    cq.qk_cols = cq.qk_pitch = kAugCols;
     cq.workspace = fws; cq.workspace_bytes = p.fwd_bytes;
     if ((e = launch_chunk_tc(cq, g, s, &launches)) != cudaSuccess) return e;
     // 5. dk~ in reversed time: queries [v | 1], keys [dn | du], values q~
     float* gkfin = a.dz0 ? fp(p.o_gkfin) : nullptr;
     ChunkArgs ck = aug_pass_args(a, kAugW, a.dk, true);
     ck.Q = xk; ck.K = xq; ck.V = qt; ck.O = dkt; ck.S0 = gk0; ck.S_out = gkfin;
+    ck.qk_cols = ck.qk_pitch = kAugCols;
     ck.workspace = fws; ck.workspace_bytes = p.fwd_bytes;
+    if (p.share) ck.agg = fp(p.o_aggk);
     if ((e = launch_chunk_tc(ck, g, s, &launches)) != cudaSuccess) return e;
     // 6. dv in reversed time: queries k~, keys q~, values dn; its final state is G_0
     float* gfin = a.dS0 ? fp(p.o_gfin) : nullptr;
     ChunkArgs cv = aug_pass_args(a, a.dk, a.dv, true);
-    cv.Q = kt; cv.K = qt; cv.V = dn; cv.O = a.dV; cv.S0 = g0; cv.S_out = gfin;
+    cv.Q = kt; cv.K = qt; cv.V = xq; cv.O = a.dV; cv.S0 = g0; cv.S_out = gfin;
+    cv.v_pitch = kAugCols;  // dn: the first 64 columns of [dn | du]
     cv.workspace = fws; cv.workspace_bytes = p.fwd_bytes;
-    if ((e = launch_chunk_tc(cv, g, s, &launches)) != cudaSuccess) return e;
-    // 7. through phi: dq = dq~ phi'(q), dk = dk~ phi'(k)
-    {
-        TraceScope trace("phi_grad_kernel", s);
-        const size_t n8 = rows * a.dk / 8;
-        phi_grad_kernel<<<grid_for(n8), 256, 0, s>>>(dqt, static_cast<const __nv_bfloat16*>(a.Q),
-                                                    static_cast<__nv_bfloat16*>(a.dQ), n8, a.phi ? 1 : 0);
-        phi_grad_kernel<<<grid_for(n8), 256, 0, s>>>(dkt, static_cast<const __nv_bfloat16*>(a.K),
-                                                    static_cast<__nv_bfloat16*>(a.dK), n8, a.phi ? 1 : 0);
+    if (p.share) {  // keys q~ with values dn give the transpose of keys dn with values q~
+        cv.agg = fp(p.o_aggv);
+        cv.agg_ready = true;
+        KernelGammas one;
+        std::memset(&one, 0, sizeof(one));
+        for (int h = 0; h < kMaxHeads; ++h) one.gamma[h] = 1.f;
+        TraceScope trace("state_transpose_kernel", s);
+        state_transpose_kernel<<<dim3((unsigned)(a.dk / 32), (unsigned)(a.dv / 32), (unsigned)(nbh * p.n_seg)),
+                                 dim3(32, 8), 0, s>>>(ck.agg, cv.agg, a.H, a.dv, a.dk,
+                                                      (size_t)kAugW * a.dk, 0, one);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // 8. the initial state's gradients: dS_0 = gamma G_0, dz_0 = gamma Gz_0
-    if (a.dS0) {
-        if ((e = state_scale(gfin, a.dS0, nbh, a.H, a.dk, a.dv, false, false, g, s)) != cudaSuccess)
-            return e;
-    }
-    if (a.dz0) {
-        TraceScope trace("aug_dz0_kernel", s);
-        aug_dz0_kernel<<<(unsigned)((nbh * a.dk + 255) / 256), 256, 0, s>>>(gkfin, a.dz0, nbh, a.H, a.dk,
-                                                                          a.dv, g);
+    if ((e = launch_chunk_tc(cv, g, s, &launches)) != cudaSuccess) return e;
+    // 7. through phi (dq = dq~ phi'(q), dk = dk~ phi'(k)) and the initial state's
+    //    gradients (dS_0 = gamma G_0, dz_0 = gamma Gz_0), one launch
+    {
+        AugFinish f;
+        f.gq = dqt; f.gk = dkt;
+        f.q = static_cast<const __nv_bfloat16*>(a.Q); f.k = static_cast<const __nv_bfloat16*>(a.K);
+        f.out_q = static_cast<__nv_bfloat16*>(a.dQ); f.out_k = static_cast<__nv_bfloat16*>(a.dK);
+        f.gfin = gfin; f.dS0 = a.dS0; f.gkfin = gkfin; f.dz0 = a.dz0;
+        f.n8 = rows * a.dk / 8;
+        f.nS = a.dS0 ? nbh * a.dk * a.dv : 0;
+        f.nz = a.dz0 ? nbh * a.dk : 0;
+        f.H = a.H; f.dk = a.dk; f.dv = a.dv; f.phi = a.phi ? 1 : 0;
+        TraceScope trace("aug_finish_kernel", s);
+        aug_finish_kernel<<<grid_for(2 * f.n8 + f.nS + f.nz), 256, 0, s>>>(f, g);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -671,6 +671,20 @@ bool make_map_box(CUtensorMap* m, const void* base, int BH, int T, int d, int bo
 bool make_map(CUtensorMap* m, const void* base, int BH, int T, int d) {
     return make_map_box(m, base, BH, T, d, 64, true);
 }
+// [BH][T] rows of `cols` bf16 columns, `pitch` elements apart (a multiple of 8);
+// boxes of 64 columns past `cols` read zeros.
+bool make_map_pitch(CUtensorMap* m, const void* base, int BH, int T, int cols, int pitch) {
+    auto fn = encode_fn();
+    if (!fn || pitch % 8 != 0 || cols > pitch) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)pitch * 2, (cuuint64_t)T * pitch * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 bool tc_arch_ok() {
     if (!encode_fn()) return false;
     int dev = 0, major = 0, minor = 0;
@@ -786,8 +800,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
     const int BH = a.B * a.H;
-    if (!make_map(&prm.tmQ, a.Q, BH, a.T, a.dk) || !make_map(&prm.tmK, a.K, BH, a.T, a.dk) ||
-        !make_map(&prm.tmV, a.V, BH, a.T, a.dv))
+    const int qk_cols = a.qk_cols ? a.qk_cols : a.dk;
+    const int qk_pitch = a.qk_pitch ? a.qk_pitch : qk_cols;
+    const int v_pitch = a.v_pitch ? a.v_pitch : a.dv;
+    if (qk_cols > a.dk || ((a.qk_cols || a.qk_pitch || a.v_pitch) && !tc_ws_supported(kFull, a.dk, tc_dvb(a), a.normalize)))
+        return cudaErrorInvalidValue;
+    if (!make_map_pitch(&prm.tmQ, a.Q, BH, a.T, qk_cols, qk_pitch) ||
+        !make_map_pitch(&prm.tmK, a.K, BH, a.T, qk_cols, qk_pitch) ||
+        !make_map_pitch(&prm.tmV, a.V, BH, a.T, a.dv, v_pitch))
         return cudaErrorInvalidValue;
     const TcPlan pl = tc_plan(a);
     if (a.workspace_bytes < pl.bytes || (pl.bytes > 0 && !a.workspace)) return cudaErrorInvalidValue;

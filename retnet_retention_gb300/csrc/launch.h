@@ -50,6 +50,10 @@ struct ChunkArgs {
     // kernel; O may be null): per token the denominator and du from dO, [B][H][T][2]
     const void* stats_dO = nullptr;
     float* stats = nullptr;
+    // Rows of Q and K stored qk_cols wide, qk_pitch elements apart (0: d_k), of V
+    // v_pitch apart (0: d_v) (pipelined kernel): columns from qk_cols up to d_k are
+    // read as zeros.
+    int qk_cols = 0, qk_pitch = 0, v_pitch = 0;
 };
 
 struct StepArgs {
