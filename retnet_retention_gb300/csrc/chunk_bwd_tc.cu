@@ -349,7 +349,10 @@ __global__ void __launch_bounds__(256) aug_finish_kernel(const __grid_constant__
 // The augmented composite's workspace (byte offsets), then the passes' own.
 struct BwdAugPlan {
     size_t o_stats, o_qt, o_kt, o_xq, o_xk, o_dqt, o_dkt, o_s0, o_gk0, o_g0, o_gkfin, o_gfin, o_aggk,
-        o_aggv, o_fwd, fwd_bytes, bytes;
+        o_aggv, o_agg0, o_zagg0, o_aggq, o_fwd, fwd_bytes, bytes;
+    // the forward pass and the dq~ pass cut the sequences into the same segments (more
+    // than one): the dq~ pass's contributions [S^T; z; z] come from the forward pass's
+    bool share_q;
     // the dk~ and dv passes cut the sequences into the same segments (more than one):
     // the dv pass takes its contributions from the dk~ pass's state walk
     bool share;
@@ -408,6 +411,13 @@ BwdAugPlan bwd_aug_plan(const BwdArgs& a) {
     p.n_seg = nk;
     p.o_aggk = take(p.share ? nbh * nk * kAugW * a.dk * sizeof(float) : 0);
     p.o_aggv = take(p.share ? nbh * nk * a.dk * a.dv * sizeof(float) : 0);
+    int n0 = 1, s0c = 0, nq = 1, sq = 0;
+    tc_segments(aug_stats_args(a), &n0, &s0c);
+    tc_segments(aug_pass_args(a, kAugW, a.dk, false), &nq, &sq);
+    p.share_q = n0 > 1 && n0 == nq && s0c == sq;
+    p.o_agg0 = take(p.share_q ? nbh * n0 * a.dk * a.dv * sizeof(float) : 0);
+    p.o_zagg0 = take(p.share_q ? nbh * n0 * a.dk * sizeof(float) : 0);
+    p.o_aggq = take(p.share_q ? nbh * n0 * kAugW * a.dk * sizeof(float) : 0);
     p.o_fwd = off;
     p.fwd_bytes = std::max({tc_workspace_bytes(aug_stats_args(a)),
                             tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, false)),
@@ -438,6 +448,10 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     c0.S0 = a.S0; c0.z0 = a.z0;
     c0.workspace = fws; c0.workspace_bytes = p.fwd_bytes;
     c0.stats_dO = a.dO; c0.stats = stats;
+    if (p.share_q) {
+        c0.agg = fp(p.o_agg0);
+        c0.zagg = fp(p.o_zagg0);
+    }
     if ((e = launch_chunk_tc(c0, g, s, &launches)) != cudaSuccess) return e;
     // 2. the pass operands
     __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *xq = bp(p.o_xq), *xk = bp(p.o_xk),
@@ -455,19 +469,21 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     float* s0 = nullptr;
     float* gk0 = nullptr;
     float* g0 = nullptr;
-    auto aug_state = [&](const float* S, const float* z, float* out, int inverse, int dup) {
+    // (nb: the number of states, nbh or nbh x segments)
+    auto aug_state = [&](const float* S, const float* z, float* out, int inverse, int dup,
+                         size_t nb) {
         TraceScope trace("aug_state_kernel", s);
-        aug_state_kernel<<<grid_for(nbh * kAugW * a.dk), 256, 0, s>>>(S, z, out, nbh, a.H, a.dk, a.dv,
-                                                                    inverse, dup, g);
+        aug_state_kernel<<<grid_for(nb * kAugW * a.dk), 256, 0, s>>>(S, z, out, nb, a.H, a.dk, a.dv,
+                                                                   inverse, dup, g);
         return cudaGetLastError();
     };
     if (a.S0 || a.z0) {
         s0 = fp(p.o_s0);
-        if ((e = aug_state(a.S0, a.z0, s0, 0, 1)) != cudaSuccess) return e;
+        if ((e = aug_state(a.S0, a.z0, s0, 0, 1, nbh)) != cudaSuccess) return e;
     }
     if (a.dS_T || a.dz_T) {
         gk0 = fp(p.o_gk0);
-        if ((e = aug_state(a.dS_T, a.dz_T, gk0, 1, 0)) != cudaSuccess) return e;
+        if ((e = aug_state(a.dS_T, a.dz_T, gk0, 1, 0, nbh)) != cudaSuccess) return e;
     }
     if (a.dS_T) {
         g0 = fp(p.o_g0);
@@ -477,6 +493,13 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     ChunkArgs cq = aug_pass_args(a, kAugW, a.dk, false);
     cq.Q = xq; cq.K = xk; cq.V = kt; cq.O = dqt; cq.S0 = s0;
     cq.qk_cols = cq.qk_pitch = kAugCols;
+    if (p.share_q) {  // keys [v | 1 | 1] with values k~: [S^T; z; z] of the forward pass
+        int n0 = 1, sc0 = 0;
+        tc_segments(aug_stats_args(a), &n0, &sc0);
+        cq.agg = fp(p.o_aggq);
+        cq.agg_ready = true;
+        if ((e = aug_state(c0.agg, c0.zagg, cq.agg, 0, 1, nbh * (size_t)n0)) != cudaSuccess) return e;
+    }
     cq.workspace = fws; cq.workspace_bytes = p.fwd_bytes;
     if ((e = launch_chunk_tc(cq, g, s, &launches)) != cudaSuccess) return e;
     // 5. dk~ in reversed time: queries [v | 1], keys [dn | du], values q~

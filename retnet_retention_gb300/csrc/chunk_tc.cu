@@ -898,7 +898,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     float* agg = a.agg ? a.agg : reinterpret_cast<float*>(ws + pl.o_agg);
     float* entry = reinterpret_cast<float*>(ws + pl.o_entry);
     // (contributions handed in carry no z: nothing reads zagg then)
-    float* zagg = a.agg_ready ? nullptr : reinterpret_cast<float*>(ws + pl.o_zagg);
+    float* zagg = a.agg_ready ? nullptr : a.zagg ? a.zagg : reinterpret_cast<float*>(ws + pl.o_zagg);
     if (a.agg_ready && (prm.track_z || a.log_a || !a.agg)) return cudaErrorInvalidValue;
     float* zentry = reinterpret_cast<float*>(ws + pl.o_zentry);
 

@@ -46,6 +46,7 @@ struct ChunkArgs {
     // walk is skipped (no normaliser, no z, no per-token decay).
     float* agg = nullptr;
     bool agg_ready = false;
+    float* zagg = nullptr;  // where the state walk writes z's contributions (null: the workspace)
     // stats for the backward pass (normalising, one value block, pipelined
     // kernel; O may be null): per token the denominator and du from dO, [B][H][T][2]
     const void* stats_dO = nullptr;
