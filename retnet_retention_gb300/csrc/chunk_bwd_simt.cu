@@ -1013,6 +1013,10 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int bwd_state_rows(const BwdArgs& a) { return a.taylor ? taylor_feature_dim(a.dk) : a.dk; }
 
+size_t bwd_stats_offset(const BwdArgs& a) {
+    return a.T > 0 ? bwd_plan(a.B, a.H, a.T, bwd_state_rows(a), a.dv, a.normalize, a.taylor).o_stats : 0;
+}
+
 size_t bwd_workspace_bytes(const BwdArgs& a) {
     return a.T > 0 ? bwd_plan(a.B, a.H, a.T, bwd_state_rows(a), a.dv, a.normalize, a.taylor).bytes : 0;
 }
@@ -1102,6 +1106,14 @@ cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaS
         else go(bwd_state_gemm_kernel<E, 128, 128>, gemm_smem_bytes<128, 128>());
     };
     auto run = [&](auto kern, auto cast) {
+        if (a.dq_only) {  // the forward sweep alone
+            if (pl.P > 1) {
+                contributions(kern, cast, 0, 1);
+                scan(0, 1);
+            }
+            launch(kern, cast, 0, 1, full);
+            return;
+        }
         if (pl.P <= 1) {
             if (nm == 0) {
                 launch(kern, cast, 0, 2, full);  // the two sweeps are independent

@@ -176,28 +176,28 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
     return p;
 }
 
-// ---- The normalised backward (phi or not, floored or not) as a composite.
+// ---- The normalised backward (phi or not, floored or not): dq on the CUDA cores,
+// dk and dv on the tensor cores.
 //
 // With n_t = q~_t S_t, u_t = q~_t . z_t, dd_t = max(|u_t|, 1) or u_t + eps and
 // o_t = n_t / dd_t, the loss's gradients with respect to n_t and u_t are
 // dn_t = do_t / dd_t and du_t = -(do_t . o_t) / dd_t * dd'(u_t), and
-//   dq~_t = S_t dn_t + du_t z_t = sum_{s<=t} gamma^(t-s) (dn_t . v_s + du_t) k~_s
-//           + gamma^(t+1) (S_0 dn_t + du_t z_0),
+//   dq~_t = S_t dn_t + du_t z_t,
 //   dk~_t = G_t v_t + Gz_t = sum_{s>=t} gamma^(s-t) (v_t . dn_s + du_s) q~_s (+ the
-//           final-state terms), dv_t = k~_t G_t,
-// so each is a forward pass with augmented operands: dq~ over queries
-// [dn | du_hi | du_lo], keys [v | 1 | 1] (du split into two bf16 parts, so that the
-// sum keeps about 16 bits; stored 72 wide, read as 128 by the d_k = 128 build, the
-// tensor maps filling the columns past the row with zeros), values k~; dk~ over the reversed
-// sequence with queries [v | 1 | 1], keys [dn | du_hi | du_lo], values q~; dv over
-// the reversed sequence with queries k~, keys q~, values dn (the first 64 columns
-// of [dn | du], read in place), its segments' contributions taken from the dk~
-// pass's (the transpose of their first 64 rows).  dd and du come
-// from the forward pass itself (its output walk's E2, in fp32), dq = dq~ phi'(q),
-// dk = dk~ phi'(k) ("Linear attention" page, "Decoding, training, and what each
-// costs": the gradients are cumulative sums; the normalised form of "Transformers
-// are RNNs", section 3.2).  d_v = 64 (the augmented width fits one 128-column
-// block).
+//           final-state terms),   dv_t = k~_t G_t
+// ("Linear attention" page, "Decoding, training, and what each costs": the gradients
+// are cumulative sums; the normalised form of "Transformers are RNNs", section 3.2).
+// dq~ is a near-cancellation (dn_t . (v_s - o_t) summed against positive k~_s): bf16
+// operands put it at 1-3.5e-2 of its largest element (fp64 emulations of the kernel's
+// roundings on short windows), so dq and the per-token dd, du come from the CUDA-core
+// kernel's forward sweep in fp32.  dk and dv keep 2-3x inside the bf16 tolerance as
+// reversed-time forward passes with augmented operands: dk~ with queries
+// [v | 1 | 1], keys [dn | du_hi | du_lo] (du split into two bf16 parts, so that the
+// sum keeps about 16 bits), values q~; dv with queries k~, keys q~, values dn.  The
+// augmented operands are stored 72 wide and read as 128 by the d_k = 128 build (the
+// tensor maps fill the columns past the row with zeros); dn is read in place as the
+// first 64 columns of [dn | du]; the dv pass takes its segments' contributions from
+// the dk~ pass's (the transpose of their first 64 rows).  d_v = 64.
 
 constexpr int kAugW = 128;   // width of the augmented operands in the kernel
 constexpr int kAugCols = 72; // ... as stored (64 value columns, du_hi and du_lo or two ones, 6 zeros)
@@ -266,44 +266,38 @@ __global__ void __launch_bounds__(256) aug_prep_kernel(
     }
 }
 
-// An augmented pass's state [b][128][d_k] from a state S [b][d_k][d_v] (null: zero)
-// and z [b][d_k] (null: zero), times 1 or 1/gamma_h: rows 0 .. d_v-1 hold S's
-// transpose, row d_v holds z, row d_v + 1 z too where both extra query columns read
-// it (dup: du_hi and du_lo each times z) or zero where their sum is read, the rest
-// zeros.
+// The dk~ pass's initial state [b][128][d_k] from dS_T [b][d_k][d_v] (null: zero) and
+// dz_T [b][d_k] (null: zero), over gamma_h: rows 0 .. d_v-1 hold dS_T's transpose,
+// row d_v dz_T (the queries' two ones read the sum of rows d_v and d_v + 1), the
+// rest zeros.
 __global__ void __launch_bounds__(256) aug_state_kernel(const float* __restrict__ S,
                                                         const float* __restrict__ z,
                                                         float* __restrict__ out, size_t nbh, int H,
-                                                        int dk, int dv, int inverse, int dup,
+                                                        int dk, int dv,
                                                         const __grid_constant__ KernelGammas g) {
     const size_t total = nbh * kAugW * dk;
     for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (size_t)gridDim.x * blockDim.x) {
         const size_t b = e / ((size_t)kAugW * dk);
         const int c = (int)((e / dk) % kAugW), d = (int)(e % dk);
-        const float sc = inverse ? 1.f / g.gamma[b % H] : 1.f;
         float x = 0.f;
         if (c < dv && S) x = S[(b * dk + d) * dv + c];
-        else if ((c == dv || (dup && c == dv + 1)) && z) x = z[b * dk + d];
-        out[e] = sc * x;
+        else if (c == dv && z) x = z[b * dk + d];
+        out[e] = x / g.gamma[b % H];
     }
 }
 
-// The composite's last step, one launch: dq = bf16(dq~ phi'(q)) and dk = bf16(dk~
-// phi'(k)) 8 elements an item (phi'(x) = 1 above zero, e^x at or below; 1 without
-// phi), then dS_0 = gamma_h G_0 (the dv pass's final state, if wanted) and dz_0 =
-// gamma_h (fin[b][d_v][d] + fin[b][d_v + 1][d]) (the dk~ pass's final-state rows of
-// du_hi and du_lo, if wanted), one element an item.
+// The last step, one launch: dk = bf16(dk~ phi'(k)) 8 elements an item (phi'(x) = 1
+// above zero, e^x at or below; 1 without phi), then dS_0 = gamma_h G_0 (the dv pass's
+// final state, if wanted) and dz_0 = gamma_h (fin[b][d_v][d] + fin[b][d_v + 1][d])
+// (the dk~ pass's final-state rows of du_hi and du_lo, if wanted), one element an item.
 struct AugFinish {
-    const __nv_bfloat16* gq;  // dq~
     const __nv_bfloat16* gk;  // dk~
-    const __nv_bfloat16* q;
     const __nv_bfloat16* k;
-    __nv_bfloat16* out_q;  // dq
-    __nv_bfloat16* out_k;  // dk
-    const float* gfin;  // [b][d_k][d_v] or null
+    __nv_bfloat16* out_k;     // dk
+    const float* gfin;        // [b][d_k][d_v] or null
     float* dS0;
-    const float* gkfin;  // [b][128][d_k] or null
+    const float* gkfin;       // [b][128][d_k] or null
     float* dz0;
     size_t n8, nS, nz;
     int H, dk, dv, phi;
@@ -311,14 +305,12 @@ struct AugFinish {
 
 __global__ void __launch_bounds__(256) aug_finish_kernel(const __grid_constant__ AugFinish f,
                                                          const __grid_constant__ KernelGammas g) {
-    const size_t total = 2 * f.n8 + f.nS + f.nz;
+    const size_t total = f.n8 + f.nS + f.nz;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
-        if (i < 2 * f.n8) {
-            const bool second = i >= f.n8;
-            const size_t j = second ? i - f.n8 : i;
-            const uint4 a = reinterpret_cast<const uint4*>(second ? f.gk : f.gq)[j];
-            const uint4 b = reinterpret_cast<const uint4*>(second ? f.k : f.q)[j];
+        if (i < f.n8) {
+            const uint4 a = reinterpret_cast<const uint4*>(f.gk)[i];
+            const uint4 b = reinterpret_cast<const uint4*>(f.k)[i];
             const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
             uint32_t o[4];
 #pragma unroll
@@ -331,13 +323,13 @@ __global__ void __launch_bounds__(256) aug_finish_kernel(const __grid_constant__
                 }
                 o[e] = pack2(g0, g1);
             }
-            reinterpret_cast<uint4*>(second ? f.out_k : f.out_q)[j] = make_uint4(o[0], o[1], o[2], o[3]);
-        } else if (i < 2 * f.n8 + f.nS) {
-            const size_t j = i - 2 * f.n8;
+            reinterpret_cast<uint4*>(f.out_k)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else if (i < f.n8 + f.nS) {
+            const size_t j = i - f.n8;
             const size_t b = j / ((size_t)f.dk * f.dv);
             f.dS0[j] = g.gamma[b % f.H] * f.gfin[j];
         } else {
-            const size_t j = i - 2 * f.n8 - f.nS;
+            const size_t j = i - f.n8 - f.nS;
             const size_t b = j / f.dk;
             const int d = (int)(j % f.dk);
             const float* r = f.gkfin + b * kAugW * f.dk;
@@ -346,83 +338,59 @@ __global__ void __launch_bounds__(256) aug_finish_kernel(const __grid_constant__
     }
 }
 
-// The augmented composite's workspace (byte offsets), then the passes' own.
+// The hybrid's workspace (byte offsets): the CUDA-core kernel's own (its per-token
+// dd, du at offset bwd_stats_offset), then the tensor-core passes' operands and
+// states, then the passes' own workspace.
 struct BwdAugPlan {
-    size_t o_stats, o_qt, o_kt, o_xq, o_xk, o_dqt, o_dkt, o_s0, o_gk0, o_g0, o_gkfin, o_gfin, o_aggk,
-        o_aggv, o_agg0, o_zagg0, o_aggq, o_fwd, fwd_bytes, bytes;
-    // the forward pass and the dq~ pass cut the sequences into the same segments (more
-    // than one): the dq~ pass's contributions [S^T; z; z] come from the forward pass's
-    bool share_q;
+    size_t o_qt, o_kt, o_xq, o_xk, o_dkt, o_gk0, o_g0, o_gkfin, o_gfin, o_aggk, o_aggv, o_fwd,
+        fwd_bytes, bytes;
     // the dk~ and dv passes cut the sequences into the same segments (more than one):
     // the dv pass takes its contributions from the dk~ pass's state walk
     bool share;
     int n_seg;
 };
 
-// The four passes' arguments (pointers filled in by the launcher).
-ChunkArgs aug_stats_args(const BwdArgs& a) {
-    ChunkArgs c = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H, a.T, a.dk,
-                           a.dv, nullptr, 0, nullptr);
-    c.phi = a.phi;
-    c.normalize = true;
-    c.floor_norm = a.floor_norm;
-    c.eps = a.eps;
-    return c;
-}
-ChunkArgs aug_pass_args(const BwdArgs& a, int width_qk, int width_v, bool reverse) {
+ChunkArgs aug_pass_args(const BwdArgs& a, int width_qk, int width_v) {
     ChunkArgs c = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H, a.T,
                            width_qk, width_v, nullptr, 0, nullptr);
-    c.reverse = reverse;
+    c.reverse = true;
     return c;
 }
 
 bool aug_shape_ok(const BwdArgs& a) {
     if (!a.bf16 || !a.normalize || a.taylor || a.log_a || a.T <= 0 || opt_tc_lockstep()) return false;
     if (a.dv != 64 || (a.dk != 64 && a.dk != 128)) return false;
-    return tc_supported(aug_stats_args(a)) && tc_supported(aug_pass_args(a, kAugW, a.dk, false)) &&
-           tc_supported(aug_pass_args(a, a.dk, a.dv, false));
+    return tc_supported(aug_pass_args(a, kAugW, a.dk)) && tc_supported(aug_pass_args(a, a.dk, a.dv));
 }
 
 BwdAugPlan bwd_aug_plan(const BwdArgs& a) {
     BwdAugPlan p;
     const size_t nbh = (size_t)a.B * a.H, rows = nbh * a.T;
-    size_t off = 0;
+    size_t off = align256(bwd_workspace_bytes(a));
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off += align256(bytes);
         return o;
     };
-    p.o_stats = take(rows * 2 * sizeof(float));
     p.o_qt = take(rows * a.dk * 2);
     p.o_kt = take(rows * a.dk * 2);
     p.o_xq = take(rows * kAugCols * 2);
     p.o_xk = take(rows * kAugCols * 2);
-    p.o_dqt = take(rows * a.dk * 2);
     p.o_dkt = take(rows * a.dk * 2);
-    p.o_s0 = take(nbh * kAugW * a.dk * sizeof(float));
     p.o_gk0 = take(nbh * kAugW * a.dk * sizeof(float));
     p.o_g0 = take(nbh * a.dk * a.dv * sizeof(float));
     p.o_gkfin = take(nbh * kAugW * a.dk * sizeof(float));
     p.o_gfin = take(nbh * a.dk * a.dv * sizeof(float));
     int nk = 1, sk = 0, nv = 1, sv = 0;
-    tc_segments(aug_pass_args(a, kAugW, a.dk, true), &nk, &sk);
-    tc_segments(aug_pass_args(a, a.dk, a.dv, true), &nv, &sv);
+    tc_segments(aug_pass_args(a, kAugW, a.dk), &nk, &sk);
+    tc_segments(aug_pass_args(a, a.dk, a.dv), &nv, &sv);
     p.share = nk > 1 && nk == nv && sk == sv;
     p.n_seg = nk;
     p.o_aggk = take(p.share ? nbh * nk * kAugW * a.dk * sizeof(float) : 0);
     p.o_aggv = take(p.share ? nbh * nk * a.dk * a.dv * sizeof(float) : 0);
-    int n0 = 1, s0c = 0, nq = 1, sq = 0;
-    tc_segments(aug_stats_args(a), &n0, &s0c);
-    tc_segments(aug_pass_args(a, kAugW, a.dk, false), &nq, &sq);
-    p.share_q = n0 > 1 && n0 == nq && s0c == sq;
-    p.o_agg0 = take(p.share_q ? nbh * n0 * a.dk * a.dv * sizeof(float) : 0);
-    p.o_zagg0 = take(p.share_q ? nbh * n0 * a.dk * sizeof(float) : 0);
-    p.o_aggq = take(p.share_q ? nbh * n0 * kAugW * a.dk * sizeof(float) : 0);
     p.o_fwd = off;
-    p.fwd_bytes = std::max({tc_workspace_bytes(aug_stats_args(a)),
-                            tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, false)),
-                            tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk, true)),
-                            tc_workspace_bytes(aug_pass_args(a, a.dk, a.dv, true))});
+    p.fwd_bytes = std::max(tc_workspace_bytes(aug_pass_args(a, kAugW, a.dk)),
+                           tc_workspace_bytes(aug_pass_args(a, a.dk, a.dv)));
     p.bytes = off + p.fwd_bytes;
     return p;
 }
@@ -441,21 +409,15 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
     void* fws = ws + p.o_fwd;
     cudaError_t e = cudaSuccess;
     int launches = 0;
-    // 1. the forward pass, writing per token dd and du instead of O
-    float* stats = fp(p.o_stats);
-    ChunkArgs c0 = aug_stats_args(a);
-    c0.Q = a.Q; c0.K = a.K; c0.V = a.V; c0.O = nullptr;
-    c0.S0 = a.S0; c0.z0 = a.z0;
-    c0.workspace = fws; c0.workspace_bytes = p.fwd_bytes;
-    c0.stats_dO = a.dO; c0.stats = stats;
-    if (p.share_q) {
-        c0.agg = fp(p.o_agg0);
-        c0.zagg = fp(p.o_zagg0);
-    }
-    if ((e = launch_chunk_tc(c0, g, s, &launches)) != cudaSuccess) return e;
-    // 2. the pass operands
-    __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *xq = bp(p.o_xq), *xk = bp(p.o_xk),
-                  *dqt = bp(p.o_dqt), *dkt = bp(p.o_dkt);
+    // 1. the forward sweep on the CUDA cores: dq and the per-token dd, du
+    BwdArgs a0 = a;
+    a0.dq_only = true;
+    a0.dK = a0.dV = nullptr;
+    a0.dS0 = a0.dz0 = nullptr;
+    if ((e = launch_chunk_bwd_simt(a0, g, s)) != cudaSuccess) return e;
+    const float* stats = fp(bwd_stats_offset(a));
+    // 2. the passes' operands
+    __nv_bfloat16 *qt = bp(p.o_qt), *kt = bp(p.o_kt), *xq = bp(p.o_xq), *xk = bp(p.o_xk), *dkt = bp(p.o_dkt);
     {
         TraceScope trace("aug_prep_kernel", s);
         aug_prep_kernel<<<grid_for(rows * std::max(kAugCols / 8, a.dk / 8)), 256, 0, s>>>(
@@ -464,55 +426,32 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
             qt, kt, xq, xk, rows, a.dk, a.phi ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // 3. initial states: the dq~ pass from S_0^T and z_0; the reversed passes from
-    //    dS_T / gamma (and dz_T / gamma), entering after the last token
-    float* s0 = nullptr;
+    // 3. initial states of the reversed passes, entering after the last token:
+    //    [dS_T^T; dz_T; 0] / gamma and dS_T / gamma
     float* gk0 = nullptr;
     float* g0 = nullptr;
-    // (nb: the number of states, nbh or nbh x segments)
-    auto aug_state = [&](const float* S, const float* z, float* out, int inverse, int dup,
-                         size_t nb) {
-        TraceScope trace("aug_state_kernel", s);
-        aug_state_kernel<<<grid_for(nb * kAugW * a.dk), 256, 0, s>>>(S, z, out, nb, a.H, a.dk, a.dv,
-                                                                   inverse, dup, g);
-        return cudaGetLastError();
-    };
-    if (a.S0 || a.z0) {
-        s0 = fp(p.o_s0);
-        if ((e = aug_state(a.S0, a.z0, s0, 0, 1, nbh)) != cudaSuccess) return e;
-    }
     if (a.dS_T || a.dz_T) {
         gk0 = fp(p.o_gk0);
-        if ((e = aug_state(a.dS_T, a.dz_T, gk0, 1, 0, nbh)) != cudaSuccess) return e;
+        TraceScope trace("aug_state_kernel", s);
+        aug_state_kernel<<<grid_for(nbh * kAugW * a.dk), 256, 0, s>>>(a.dS_T, a.dz_T, gk0, nbh, a.H,
+                                                                    a.dk, a.dv, g);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.dS_T) {
         g0 = fp(p.o_g0);
         if ((e = state_scale(a.dS_T, g0, nbh, a.H, a.dk, a.dv, false, true, g, s)) != cudaSuccess) return e;
     }
-    // 4. dq~: queries [dn | du], keys [v | 1], values k~
-    ChunkArgs cq = aug_pass_args(a, kAugW, a.dk, false);
-    cq.Q = xq; cq.K = xk; cq.V = kt; cq.O = dqt; cq.S0 = s0;
-    cq.qk_cols = cq.qk_pitch = kAugCols;
-    if (p.share_q) {  // keys [v | 1 | 1] with values k~: [S^T; z; z] of the forward pass
-        int n0 = 1, sc0 = 0;
-        tc_segments(aug_stats_args(a), &n0, &sc0);
-        cq.agg = fp(p.o_aggq);
-        cq.agg_ready = true;
-        if ((e = aug_state(c0.agg, c0.zagg, cq.agg, 0, 1, nbh * (size_t)n0)) != cudaSuccess) return e;
-    }
-    cq.workspace = fws; cq.workspace_bytes = p.fwd_bytes;
-    if ((e = launch_chunk_tc(cq, g, s, &launches)) != cudaSuccess) return e;
-    // 5. dk~ in reversed time: queries [v | 1], keys [dn | du], values q~
+    // 4. dk~ in reversed time: queries [v | 1], keys [dn | du], values q~
     float* gkfin = a.dz0 ? fp(p.o_gkfin) : nullptr;
-    ChunkArgs ck = aug_pass_args(a, kAugW, a.dk, true);
+    ChunkArgs ck = aug_pass_args(a, kAugW, a.dk);
     ck.Q = xk; ck.K = xq; ck.V = qt; ck.O = dkt; ck.S0 = gk0; ck.S_out = gkfin;
     ck.qk_cols = ck.qk_pitch = kAugCols;
     ck.workspace = fws; ck.workspace_bytes = p.fwd_bytes;
     if (p.share) ck.agg = fp(p.o_aggk);
     if ((e = launch_chunk_tc(ck, g, s, &launches)) != cudaSuccess) return e;
-    // 6. dv in reversed time: queries k~, keys q~, values dn; its final state is G_0
+    // 5. dv in reversed time: queries k~, keys q~, values dn; its final state is G_0
     float* gfin = a.dS0 ? fp(p.o_gfin) : nullptr;
-    ChunkArgs cv = aug_pass_args(a, a.dk, a.dv, true);
+    ChunkArgs cv = aug_pass_args(a, a.dk, a.dv);
     cv.Q = kt; cv.K = qt; cv.V = xq; cv.O = a.dV; cv.S0 = g0; cv.S_out = gfin;
     cv.v_pitch = kAugCols;  // dn: the first 64 columns of [dn | du]
     cv.workspace = fws; cv.workspace_bytes = p.fwd_bytes;
@@ -529,23 +468,20 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = launch_chunk_tc(cv, g, s, &launches)) != cudaSuccess) return e;
-    // 7. through phi (dq = dq~ phi'(q), dk = dk~ phi'(k)) and the initial state's
-    //    gradients (dS_0 = gamma G_0, dz_0 = gamma Gz_0), one launch
-    {
-        AugFinish f;
-        f.gq = dqt; f.gk = dkt;
-        f.q = static_cast<const __nv_bfloat16*>(a.Q); f.k = static_cast<const __nv_bfloat16*>(a.K);
-        f.out_q = static_cast<__nv_bfloat16*>(a.dQ); f.out_k = static_cast<__nv_bfloat16*>(a.dK);
-        f.gfin = gfin; f.dS0 = a.dS0; f.gkfin = gkfin; f.dz0 = a.dz0;
-        f.n8 = rows * a.dk / 8;
-        f.nS = a.dS0 ? nbh * a.dk * a.dv : 0;
-        f.nz = a.dz0 ? nbh * a.dk : 0;
-        f.H = a.H; f.dk = a.dk; f.dv = a.dv; f.phi = a.phi ? 1 : 0;
-        TraceScope trace("aug_finish_kernel", s);
-        aug_finish_kernel<<<grid_for(2 * f.n8 + f.nS + f.nz), 256, 0, s>>>(f, g);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    // 6. through phi (dk = dk~ phi'(k)) and the initial state's gradients
+    //    (dS_0 = gamma G_0, dz_0 = gamma Gz_0), one launch
+    AugFinish f;
+    f.gk = dkt;
+    f.k = static_cast<const __nv_bfloat16*>(a.K);
+    f.out_k = static_cast<__nv_bfloat16*>(a.dK);
+    f.gfin = gfin; f.dS0 = a.dS0; f.gkfin = gkfin; f.dz0 = a.dz0;
+    f.n8 = rows * a.dk / 8;
+    f.nS = a.dS0 ? nbh * a.dk * a.dv : 0;
+    f.nz = a.dz0 ? nbh * a.dk : 0;
+    f.H = a.H; f.dk = a.dk; f.dv = a.dv; f.phi = a.phi ? 1 : 0;
+    TraceScope trace("aug_finish_kernel", s);
+    aug_finish_kernel<<<grid_for(f.n8 + f.nS + f.nz), 256, 0, s>>>(f, g);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -564,13 +500,13 @@ bool bwd_tc_supported(const BwdArgs& a) {
 size_t bwd_tc_workspace_bytes(const BwdArgs& a) {
     // (normalised: the CUDA-core kernel takes over where a gamma rules out the
     // reversed-time passes, so the workspace covers both)
-    if (a.normalize) return std::max(bwd_aug_plan(a).bytes, bwd_workspace_bytes(a));
+    if (a.normalize) return bwd_aug_plan(a).bytes;  // (covers the CUDA-core kernel's own)
     return bwd_tc_plan(a).bytes;
 }
 
 cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) {
     if (a.normalize) {
-        ChunkArgs ck = aug_pass_args(a, kAugW, a.dk, true), cv = aug_pass_args(a, a.dk, a.dv, true);
+        ChunkArgs ck = aug_pass_args(a, kAugW, a.dk), cv = aug_pass_args(a, a.dk, a.dv);
         if (!tc_reverse_supported(ck, g) || !tc_reverse_supported(cv, g)) return launch_chunk_bwd_simt(a, g, s);
         return launch_aug(a, g, s);
     }

@@ -833,13 +833,6 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     prm.fact = !a.log_a && !a.phi && !prm.track_z;
     for (int h = 0; h < a.H && prm.fact; ++h)
         prm.fact = g.gamma[h] < 1.f && g.log2g[h] * (float)(kC - 1) >= -64.f;
-    if (a.stats) {  // the backward pass's denominators and du, from the output walk's E2
-        if (!a.normalize || !a.bf16 || a.noncausal || !a.stats_dO || a.dv != dvb ||
-            !tc_ws_supported(kFull, a.dk, dvb, true))
-            return cudaErrorInvalidValue;
-        prm.dO = static_cast<const __nv_bfloat16*>(a.stats_dO);
-        prm.stats = a.stats;
-    }
     if (a.reverse) {  // the factored build alone walks reversed time
         if (!tc_reverse_supported(a, g)) return cudaErrorInvalidValue;
         prm.fact = 1;
@@ -898,7 +891,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     float* agg = a.agg ? a.agg : reinterpret_cast<float*>(ws + pl.o_agg);
     float* entry = reinterpret_cast<float*>(ws + pl.o_entry);
     // (contributions handed in carry no z: nothing reads zagg then)
-    float* zagg = a.agg_ready ? nullptr : a.zagg ? a.zagg : reinterpret_cast<float*>(ws + pl.o_zagg);
+    float* zagg = a.agg_ready ? nullptr : reinterpret_cast<float*>(ws + pl.o_zagg);
     if (a.agg_ready && (prm.track_z || a.log_a || !a.agg)) return cudaErrorInvalidValue;
     float* zentry = reinterpret_cast<float*>(ws + pl.o_zentry);
 

@@ -64,11 +64,6 @@ struct TcParams {
     // in the reversed sequence.  The initial state enters at the end, and the
     // final state is the one after row 0.
     int rev;
-    // stats for the backward pass (normalising walks with one value block; O may
-    // then be null): per token of dO the denominator dd and du = -(do . o) / dd *
-    // d dd/du, [BH][T][2] fp32
-    const __nv_bfloat16* dO;
-    float* stats;
     int o_align32;  // O's base is 32-byte aligned (rows and column blocks then are too)
     KernelGammas g;
 };

@@ -213,9 +213,7 @@ static_assert(kNumBars <= 32, "mbarrier slots");
 // gamma^(i+1) -> 2^(b_i), gamma^(L-1-j) -> 2^(b_(L-1) - b_j), gamma^L ->
 // 2^(b_(L-1)) (b in log2 units), and the score mask's running product steps by
 // a_j instead of gamma.
-// STATS: the output walk also writes the backward pass's per-token dd and du
-// (p.stats, from p.dO); a build of its own, so that the others carry none of it.
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT, bool STATS = false>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
 __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
     static_assert(!FACT || (!GATED && !PHI && !NORM), "the factored decay is for plain retention");
     constexpr int kThreadsC = threads_c(DK, DVB, PHI);
@@ -924,10 +922,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 if (t == 0) LA_TL(it * 16 + 10);
                 const uint32_t ocol = tbase + lane_off + kColO + (it % NOB) * Lay::kOSlot;
                 float inv = 1.f;
-                float den = 0.f, dd = 1.f;  // the normaliser's u before the floor, and after
                 if (NORM) {  // sum_j P_ij + xi_i q^_i . z_{c-1}
                     // O's columns DVB and DVB + 1: MMA3's z block (z_{c-1} and its residual)
                     // and, with positive features, MMA2's ones column (sum_j P_ij)
+                    float den = 0.f;
                     if (PHI || unit_gamma) {
                         den = __uint_as_float(tmem_ld1(ocol + DVB)) + __uint_as_float(tmem_ld1(ocol + DVB + 1));
                         tmem_ld_wait();
@@ -936,8 +934,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                         den += rsb[(it % 3) * 256 + row] + rsb[(it % 3) * 256 + 128 + row];
                         if (!unit_gamma) den += dqz[(it & 1) * 128 + row];
                     }
-                    dd = norm_den(den, p.normalize, p.eps);
-                    inv = 1.f / dd;
+                    inv = 1.f / norm_den(den, p.normalize, p.eps);
                 }
                 if (fact) inv = gamma_pow(l2g, (float)(mrow(row) + 1 - L));  // gamma^(i+1-L)
                 const int c = cb + it;
@@ -946,13 +943,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 // L are padding and store nothing
                 const int trow = rev ? p.T - (c + 1) * kC + row : c * kC + row;
                 const bool live = mrow(row) < L;
-                const size_t tok = (size_t)bh * p.T + (size_t)max(trow, 0);
-                __nv_bfloat16* orow = p.O + tok * p.dv + v0;
-                // stats for the backward pass (normalised walks over all of d_v in one
-                // block): du = -(do . o) / dd * d dd/du, from the fp32 o of this row
-                constexpr bool stats = NORM && STATS && !STATE_ONLY;
-                const __nv_bfloat16* drow = stats ? p.dO + tok * p.dv + v0 : nullptr;
-                float dot = 0.f;
+                __nv_bfloat16* orow = p.O + ((size_t)bh * p.T + (size_t)max(trow, 0)) * p.dv + v0;
                 // 64 columns a round in the factored build with 128 registers a thread
                 // (two loads, one wait), else 32.  The O buffer is released once the
                 // last round is in registers; in the factored build the earlier
@@ -995,36 +986,16 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                         for (int e = 0; e < 32; e += 2)
                             pk[16 * hf + (e >> 1)] =
                                 pack_bf16x2(__uint_as_float(r[hf][e]) * inv, __uint_as_float(r[hf][e + 1]) * inv);
-                    if (stats && live) {
-#pragma unroll
-                        for (int hf = 0; hf < kW; ++hf)
-#pragma unroll
-                            for (int e8 = 0; e8 < 32; e8 += 8) {
-                                const uint4 u = *reinterpret_cast<const uint4*>(drow + 32 * (kW * rd + hf) + e8);
-                                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    dot = fmaf(__uint_as_float(w[e] << 16), __uint_as_float(r[hf][e8 + 2 * e]) * inv, dot);
-                                    dot = fmaf(__uint_as_float(w[e] & 0xffff0000u),
-                                               __uint_as_float(r[hf][e8 + 2 * e + 1]) * inv, dot);
-                                }
-                            }
-                    }
                     if (rd < kHold) {
 #pragma unroll
                         for (int e = 0; e < 16 * kW; ++e) held[rd][e] = pk[e];
                         continue;
                     }
-                    if (live && (!stats || p.O)) {  // (the stats build may run without O)
+                    if (live) {
 #pragma unroll
                         for (int h = 0; h < kHold; ++h) store_packed(held[h], 32 * kW * h);
                         store_packed(pk, 32 * kW * rd);
                     }
-                }
-                if (stats && live) {
-                    const float dd_du = p.normalize == 2 ? (fabsf(den) > 1.f ? (den > 0.f ? 1.f : -1.f) : 0.f) : 1.f;
-                    p.stats[tok * 2] = dd;
-                    p.stats[tok * 2 + 1] = -dot * inv * dd_du;
                 }
                 if (t == 0) LA_TL(it * 16 + 11);
                 return true;
@@ -1201,11 +1172,10 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
 // pdl: launch as a programmatic dependent of the previous kernel in the stream
 // (the kernel's entry-state reads wait for that kernel; everything else may
 // start early).
-template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT = false,
-          bool STATS = false>
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT = false>
 cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI, GATED>;
-    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT, STATS>;
+    auto kern = chunk_tc_ws_kernel<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1271,17 +1241,6 @@ cudaError_t dispatch_ws(int dk, int dvb, bool normalize, const TcParams& prm, in
         if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, true, false, GATED>(prm, grid, s, pdl);
         if constexpr (!GATED)  // (no room for the per-token decays beside two 96 KB stages)
             if (dk == 128 && dvb == 128) return launch_ws<128, 128, false, true, false, false>(prm, grid, s, pdl);
-        return cudaErrorInvalidValue;
-    }
-    if (normalize && prm.stats) {  // the backward's forward pass (per-head decay only)
-        if constexpr (!GATED) {
-            if (dk == 64 && dvb == 64)
-                return phi ? launch_ws<64, 64, true, false, true, false, false, true>(prm, grid, s, pdl)
-                           : launch_ws<64, 64, true, false, false, false, false, true>(prm, grid, s, pdl);
-            if (dk == 128 && dvb == 64)
-                return phi ? launch_ws<128, 64, true, false, true, false, false, true>(prm, grid, s, pdl)
-                           : launch_ws<128, 64, true, false, false, false, false, true>(prm, grid, s, pdl);
-        }
         return cudaErrorInvalidValue;
     }
     if (normalize) {

@@ -46,11 +46,6 @@ struct ChunkArgs {
     // walk is skipped (no normaliser, no z, no per-token decay).
     float* agg = nullptr;
     bool agg_ready = false;
-    float* zagg = nullptr;  // where the state walk writes z's contributions (null: the workspace)
-    // stats for the backward pass (normalising, one value block, pipelined
-    // kernel; O may be null): per token the denominator and du from dO, [B][H][T][2]
-    const void* stats_dO = nullptr;
-    float* stats = nullptr;
     // Rows of Q and K stored qk_cols wide, qk_pitch elements apart (0: d_k), of V
     // v_pitch apart (0: d_v) (pipelined kernel): columns from qk_cols up to d_k are
     // read as zeros.
@@ -99,6 +94,10 @@ struct BwdArgs {
     bool taylor;         // Taylor feature map: dk = 16 wide q, k; states of 1 + dk + dk^2 rows
     void* workspace;     // the forward sweep's per-token den, du (normalising)
     size_t workspace_bytes;
+    // the CUDA-core kernel's forward sweep alone: dq and (normalising) the per-token
+    // dd, du at bwd_stats_offset in the workspace; dk, dv and the state gradients
+    // are left to the caller
+    bool dq_only = false;
 };
 
 // The test and diagnostic switches of la_debug_set (abi.cu).
@@ -126,6 +125,8 @@ int simt_chunk_len(int requested, int dk);
 // normalising, the segments' states)
 cudaError_t launch_chunk_bwd_simt(const BwdArgs& a, const KernelGammas& g, cudaStream_t s);
 size_t bwd_workspace_bytes(const BwdArgs& a);
+// Byte offset in the CUDA-core kernel's workspace of its per-token [B][H][T][2] dd, du.
+size_t bwd_stats_offset(const BwdArgs& a);
 
 // chunk_bwd_tc.cu: the backward pass as three forward passes on the tensor cores
 // (bf16, no feature map, no normaliser, per-head decay, d_k, d_v in {64, 128})

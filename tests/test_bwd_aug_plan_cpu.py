@@ -1,23 +1,24 @@
-"""The algebra of the normalised backward's tensor-core composite, on the host in fp64.
+"""The algebra of the normalised backward's tensor-core passes, on the host in fp64.
 
 With phi (elu + 1 or the identity) and the normaliser, n_t = q~_t S_t, u_t = q~_t . z_t,
 dd_t = u_t + eps (or max(|u_t|, 1) with the floor) and o_t = n_t / dd_t.  For
 L = sum_t do_t . o_t + <dS_T, S_T> + <dz_T, z_T> the gradients with respect to n_t and
-u_t are dn_t = do_t / dd_t and du_t = -(do_t . o_t) / dd_t * dd'(u_t), and the library
-computes the rest as three forward passes of the plain decayed form:
+u_t are dn_t = do_t / dd_t and du_t = -(do_t . o_t) / dd_t * dd'(u_t).  The library
+takes dq, dd and du from the CUDA-core kernel's forward sweep and computes dk and dv
+as two forward passes of the plain decayed form over the reversed sequences:
 
-  dq~ = forward(queries [dn | du_hi | du_lo], keys [v | 1 | 1], values k~,
-                initial state [S_0^T; z_0; z_0]);
   dk~ = reversed forward(queries [v | 1 | 1], keys [dn | du_hi | du_lo], values q~,
                 initial state [dS_T^T; dz_T; 0] / gamma);
   dv  = reversed forward(queries k~, keys q~, values dn, initial state dS_T / gamma);
-  dq = dq~ phi'(q), dk = dk~ phi'(k), dS_0 = gamma (the dv pass's final state),
+  dk = dk~ phi'(k), dS_0 = gamma (the dv pass's final state),
   dz_0 = gamma (the sum of the dk~ pass's two extra final-state rows),
 
 with du = du_hi + du_lo (the kernel splits du into two bf16 parts; here any split).
 This is the chain rule on the recurrence ("Linear attention" page, "Decoding,
 training, and what each costs"); each pass is the brute-force masked form and the
-result is compared with the oracle's own backward sweeps.
+result is compared with the oracle's own backward sweeps.  (dq as a forward pass
+over [dn | du] with keys [v | 1 | 1] holds too, and is checked here as well, but the
+library does not use it: it is a near-cancellation that bf16 operands do not resolve.)
 """
 import numpy as np
 import pytest

@@ -233,8 +233,8 @@ def test_bwd_matches_autograd_of_the_forward_kernel_inputs_on_fp32():
 
 
 def test_bwd_linear_attention_bf16_full():
-    """The linear-attention workload's shape (B4 H8 T4096 d64, phi, normalised, on
-    the tensor-core composite), every sequence's gradients against the oracle."""
+    """The linear-attention workload's shape (B4 H8 T4096 d64, phi, normalised; dk and
+    dv on the tensor cores), every sequence's gradients against the oracle."""
     c = workloads.CONFIGS["linear_attention_bf16"]
     x = workloads.make_inputs(c)
     B, H, T, dv = c["B"], c["H"], c["T"], c["dv"]
@@ -250,7 +250,7 @@ def test_bwd_linear_attention_bf16_full():
     check("dv", to_np(dv_), rv, TOL["bf16"])
 
 
-NORM_CASES = [  # shape, phi, floor, gammas, the tensor-core composite expected
+NORM_CASES = [  # shape, phi, floor, gammas, dk and dv on the tensor cores expected
     ((2, 2, 260, 64, 64), True, False, None, True),
     ((1, 3, 300, 128, 64), True, True, [1.0, 0.9, 0.8], True),
     ((1, 2, 300, 64, 64), False, True, [0.97, 0.99], True),
@@ -264,10 +264,11 @@ NORM_CASES = [  # shape, phi, floor, gammas, the tensor-core composite expected
 @pytest.mark.parametrize("shape,phi,floor,gammas,composite", NORM_CASES,
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else None)
 def test_bwd_normalised_paths(shape, phi, floor, gammas, composite, opts):
-    """The normalised backward: the augmented tensor-core composite (the forward pass
-    writing dd and du, then forward passes over [dn | du] and [v | 1]) where it applies,
-    the CUDA-core kernel otherwise; which one ran is read from the launch trace.  With
-    an initial state and final-state gradients, and dS_0, dz_0 checked too."""
+    """The normalised backward: dq and the per-token dd, du from the CUDA-core kernel's
+    forward sweep, then dk and dv as reversed-time tensor-core passes over [dn | du] and
+    [v | 1] where they apply, the CUDA-core kernel's backward sweep otherwise; which ran
+    is read from the launch trace.  With an initial state and final-state gradients,
+    and dS_0, dz_0 checked too."""
     opts.path("auto")
     B, H, T, dk, dv = shape
     seed = zlib.crc32(repr((shape, phi, floor, gammas, "bwd-norm")).encode()) % 100000
@@ -291,7 +292,8 @@ def test_bwd_normalised_paths(shape, phi, floor, gammas, composite, opts):
     finally:
         la.trace_enable(0)
     assert ("aug_prep_kernel" in names) == composite, names
-    assert any(n.startswith("chunk_bwd_simt_kernel") for n in names) == (not composite), names
+    assert "chunk_bwd_simt_kernel/dq" in names, names
+    assert ("chunk_bwd_simt_kernel/dkdv" in names) == (not composite), names
     rq, rk, rv, rS0, rz0 = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, phi=phi,
                                                 normalize=True, floor=floor, S0=S0, z0=z0,
                                                 dS_T=dST, dz_T=dzT)
