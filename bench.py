@@ -423,7 +423,7 @@ def decode_measure(la, steps_total: int, warmup: int, rank: int, world: int) -> 
 def bwd_path(kernels: dict) -> str:
     """The backward pass's path, from the kernels its traced step launched."""
     if "aug_prep_kernel" in kernels:
-        return "tensor cores (forward pass with dd and du, then augmented forward passes)"
+        return "CUDA cores (dq, per-token dd and du) and tensor cores (dk, dv: reversed-time passes)"
     if any(k.startswith("chunk_tc_ws_kernel") for k in kernels):
         return "tensor cores (three forward passes)"
     return "CUDA cores"
