@@ -272,11 +272,15 @@ LA_API la_status la_recurrent_step_gated(const void* q, const void* k, const voi
  *          overlap any input)
  *   dS0    [B][H][d_k][d_v] fp32 or NULL, dz0 [B][H][d_k] fp32 or NULL: the
  *          initial state's gradients
- *   workspace: at least la_bwd_workspace_size(...) bytes (per-token
- *          denominators when normalising; 0 otherwise)
- * d_k and d_v must be at most 128 (LA_ERR_UNSUPPORTED otherwise).  The
- * computation runs in fp32 on the CUDA cores (bf16 calls with per-head decay,
- * no feature map and no normaliser on the tensor cores).
+ *   workspace: at least la_bwd_workspace_size(...) bytes (the sweeps'
+ *          segment states and, when normalising, per-token denominators; the
+ *          tensor-core passes' operands where they run)
+ * d_k and d_v must be at most 128 (LA_ERR_UNSUPPORTED otherwise).  Paths: bf16
+ * calls with per-head decay and neither feature map nor normaliser run as
+ * three tensor-core forward passes; normalised bf16 calls with per-head decay
+ * and d_v = 64 take dq from the CUDA cores in fp32 and dk, dv from two
+ * tensor-core passes (dq of the normalised form cancels too much for bf16
+ * operands); everything else runs in fp32 on the CUDA cores.
  * LA_PHI_TAYLOR: the Taylor feature map as in la_chunk_fwd (d_k = 16, not with
  * LA_PHI_ELU1, not with per-token decays); S0, z0, dS_T, dz_T, dS0 and dz0 then
  * have 1 + d_k + d_k^2 = 273 rows in the map's order, and dQ, dK are the
