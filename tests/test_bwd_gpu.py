@@ -256,6 +256,8 @@ NORM_CASES = [  # shape, phi, floor, gammas, dk and dv on the tensor cores expec
     ((1, 2, 300, 64, 64), False, True, [0.97, 0.99], True),
     ((2, 16, 1000, 64, 64), True, False, 1.0, True),       # segments folded in the walks
     ((1, 2, 3000, 64, 64), True, False, [1.0, 0.999], True),  # segments with a scan
+    ((1, 1, 1, 64, 64), True, False, 0.9, True),             # one token
+    ((3, 5, 129, 128, 64), True, True, None, True),          # a chunk and one row, d_k = 128
     ((1, 2, 200, 64, 64), True, False, [0.5, 0.9], False),   # gamma^127 < 2^-64: CUDA cores
     ((1, 2, 130, 64, 128), True, False, None, False),        # d_v = 128: CUDA cores
 ]
