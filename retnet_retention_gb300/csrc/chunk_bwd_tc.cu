@@ -22,6 +22,10 @@
 // pipelined kernel's factored build applies (every gamma in (0, 1] with
 // gamma^(C-1) >= 2^-64) it walks the sequences backward itself instead, on the
 // original tensors.
+//
+// Normalised calls (d_v = 64) split: dq and the per-token denominators from the
+// CUDA-core kernel's forward sweep, dk and dv from two reversed-time passes over
+// augmented operands (the section "The normalised backward" below).
 #include <algorithm>
 #include <cstring>
 
@@ -498,9 +502,9 @@ bool bwd_tc_supported(const BwdArgs& a) {
 }
 
 size_t bwd_tc_workspace_bytes(const BwdArgs& a) {
-    // (normalised: the CUDA-core kernel takes over where a gamma rules out the
-    // reversed-time passes, so the workspace covers both)
-    if (a.normalize) return bwd_aug_plan(a).bytes;  // (covers the CUDA-core kernel's own)
+    // (normalised: the plan starts with the CUDA-core kernel's own workspace, which
+    // also covers that kernel alone where a gamma rules out the reversed passes)
+    if (a.normalize) return bwd_aug_plan(a).bytes;
     return bwd_tc_plan(a).bytes;
 }
 
