@@ -276,8 +276,8 @@ LA_API la_status la_recurrent_step_gated(const void* q, const void* k, const voi
  *          segment states and, when normalising, per-token denominators; the
  *          tensor-core passes' operands where they run)
  * d_k and d_v must be at most 128 (LA_ERR_UNSUPPORTED otherwise).  Paths: bf16
- * calls with per-head decay and neither feature map nor normaliser run as
- * three tensor-core forward passes; normalised bf16 calls with per-head decay
+ * calls with per-head decay, no normaliser and LA_PHI_ELU1 or no feature map
+ * run as three tensor-core forward passes; normalised bf16 calls with per-head decay
  * and d_v = 64 take dq from the CUDA cores in fp32 and dk, dv from two
  * tensor-core passes (dq of the normalised form cancels too much for bf16
  * operands); everything else runs in fp32 on the CUDA cores.

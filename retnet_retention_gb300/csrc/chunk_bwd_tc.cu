@@ -23,6 +23,9 @@
 // gamma^(C-1) >= 2^-64) it walks the sequences backward itself instead, on the
 // original tensors.
 //
+// With phi = elu + 1 (no normaliser) the passes run on phi(q), phi(k), and the q and
+// k gradients go through phi'(x) (1 above zero, e^x at or below) at the end.
+//
 // Normalised calls (d_v = 64) split: dq and the per-token denominators from the
 // CUDA-core kernel's forward sweep, dk and dv from two reversed-time passes over
 // augmented operands (the section "The normalised backward" below).
@@ -35,6 +38,55 @@
 namespace la {
 
 namespace {
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// phi = elu + 1 of two bf16 tensors of n8 x 8 elements: a~ = bf16(phi(a)), b~ likewise
+// (8 elements an item).
+__global__ void __launch_bounds__(256) phi_prep_kernel(const __nv_bfloat16* __restrict__ a,
+                                                       const __nv_bfloat16* __restrict__ b,
+                                                       __nv_bfloat16* __restrict__ at,
+                                                       __nv_bfloat16* __restrict__ bt, size_t n8) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const bool second = i >= n8;
+        const size_t j = second ? i - n8 : i;
+        const uint4 u = reinterpret_cast<const uint4*>(second ? b : a)[j];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o[e] = pack2(phi_elu1(__uint_as_float(w[e] << 16)), phi_elu1(__uint_as_float(w[e] & 0xffff0000u)));
+        reinterpret_cast<uint4*>(second ? bt : at)[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Gradients through phi for two tensors of n8 x 8 elements: out = bf16(g phi'(x)),
+// phi'(x) = 1 above zero, e^x at or below (8 elements an item).
+__global__ void __launch_bounds__(256) phi_grad_pair_kernel(
+    const __nv_bfloat16* __restrict__ ga, const __nv_bfloat16* __restrict__ xa, __nv_bfloat16* __restrict__ oa,
+    const __nv_bfloat16* __restrict__ gb, const __nv_bfloat16* __restrict__ xb, __nv_bfloat16* __restrict__ ob,
+    size_t n8) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const bool second = i >= n8;
+        const size_t j = second ? i - n8 : i;
+        const uint4 g = reinterpret_cast<const uint4*>(second ? gb : ga)[j];
+        const uint4 x = reinterpret_cast<const uint4*>(second ? xb : xa)[j];
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, xw[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(xw[e] << 16), x1 = __uint_as_float(xw[e] & 0xffff0000u);
+            o[e] = pack2(__uint_as_float(gw[e] << 16) * (x0 > 0.f ? 1.f : expf(x0)),
+                         __uint_as_float(gw[e] & 0xffff0000u) * (x1 > 0.f ? 1.f : expf(x1)));
+        }
+        reinterpret_cast<uint4*>(second ? ob : oa)[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
 
 // out[bh][t][:] = in[bh][T-1-t][:] for a [BH][T][d] bf16 tensor (16-byte pieces).
 __global__ void __launch_bounds__(256) reverse_time_kernel(const uint4* __restrict__ in,
@@ -135,8 +187,8 @@ ChunkArgs fwd_args(const void* Q, const void* K, const void* V, void* O, const f
 // the dV pass's segment contributions and their transposes, then the forward
 // calls' own workspace (one call at a time).
 struct BwdTcPlan {
-    size_t o_qr, o_kr, o_vr, o_dor, o_dvr, o_dkr, o_s0t, o_g0, o_g0t, o_gfin, o_agg, o_aggt, o_fwd,
-        fwd_bytes, bytes;
+    size_t o_qr, o_kr, o_vr, o_dor, o_dvr, o_dkr, o_s0t, o_g0, o_g0t, o_gfin, o_agg, o_aggt, o_qt,
+        o_kt, o_dqt, o_dkt, o_fwd, fwd_bytes, bytes;
     // the dV and dK passes have the same segments (more than one): the dK pass's
     // state walk is the dV pass's transposed (keys dO and values Q instead of keys
     // Q and values dO), so it is not run again
@@ -174,6 +226,12 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
     const size_t nagg = p.share ? align256(nbh * n2 * a.dk * a.dv * 4) : 0;
     p.o_agg = off; off += nagg;
     p.o_aggt = off; off += nagg;
+    // with phi: phi(q), phi(k) and the gradients before phi'
+    const size_t nphi = a.phi ? nqk : 0;
+    p.o_qt = off; off += nphi;
+    p.o_kt = off; off += nphi;
+    p.o_dqt = off; off += nphi;
+    p.o_dkt = off; off += nphi;
     p.o_fwd = off;
     p.fwd_bytes = std::max(tc_workspace_bytes(c1), tc_workspace_bytes(c2));
     p.bytes = off + p.fwd_bytes;
@@ -205,11 +263,6 @@ BwdTcPlan bwd_tc_plan(const BwdArgs& a) {
 
 constexpr int kAugW = 128;   // width of the augmented operands in the kernel
 constexpr int kAugCols = 72; // ... as stored (64 value columns, du_hi and du_lo or two ones, 6 zeros)
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // Per token row: q~ = phi(q), k~ = phi(k) and the augmented [dn | du_hi | du_lo | 0]
 // and [v | 1 | 1 | 0] (kAugCols wide, dn = do / dd in bf16).  One thread per 16-byte
@@ -492,7 +545,7 @@ cudaError_t launch_aug(const BwdArgs& a, const KernelGammas& g, cudaStream_t s) 
 
 bool bwd_tc_supported(const BwdArgs& a) {
     if (a.normalize) return aug_shape_ok(a);
-    if (!a.bf16 || a.phi || a.taylor || a.log_a || a.T <= 0) return false;
+    if (!a.bf16 || a.taylor || a.log_a || a.T <= 0) return false;
     if ((a.dk != 64 && a.dk != 128) || (a.dv != 64 && a.dv != 128)) return false;
     const ChunkArgs c1 = fwd_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, a.B, a.H,
                                   a.T, a.dv, a.dk, nullptr, 0, nullptr);
@@ -521,6 +574,26 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
     void* fws = ws + p.o_fwd;
     cudaError_t e = cudaSuccess;
     int launches = 0;
+    // with phi = elu + 1 (no normaliser) the passes run on phi(q), phi(k) and their
+    // gradients go through phi' at the end
+    const void* Qp = a.Q;
+    const void* Kp = a.K;
+    void* dQp = a.dQ;
+    void* dKp = a.dK;
+    const size_t n8 = nbh * a.T * a.dk / 8;
+    if (a.phi) {
+        __nv_bfloat16* qt = reinterpret_cast<__nv_bfloat16*>(ws + p.o_qt);
+        __nv_bfloat16* kt = reinterpret_cast<__nv_bfloat16*>(ws + p.o_kt);
+        TraceScope trace("phi_prep_kernel", s);
+        phi_prep_kernel<<<(unsigned)std::max<size_t>(1, std::min<size_t>((2 * n8 + 255) / 256, 152 * 16)), 256,
+                          0, s>>>(static_cast<const __nv_bfloat16*>(a.Q),
+                                  static_cast<const __nv_bfloat16*>(a.K), qt, kt, n8);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        Qp = qt;
+        Kp = kt;
+        dQp = ws + p.o_dqt;
+        dKp = ws + p.o_dkt;
+    }
     // dQ: queries dO, keys V, values K, initial state S_0^T
     float* s0t = nullptr;
     if (a.S0) {
@@ -531,7 +604,7 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
         if ((e = state_scale(a.S0, s0t, nbh, a.H, a.dk, a.dv, true, false, one, s)) != cudaSuccess)
             return e;
     }
-    ChunkArgs c1 = fwd_args(a.dO, a.V, a.K, a.dQ, s0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
+    ChunkArgs c1 = fwd_args(a.dO, a.V, Kp, dQp, s0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
                             p.fwd_bytes, nullptr);
     if ((e = launch_chunk_tc(c1, g, s, &launches)) != cudaSuccess) return e;
     // initial states of the reversed passes: dS_T / gamma and its transpose
@@ -548,9 +621,9 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
     float* gfin = a.dS0 ? reinterpret_cast<float*>(ws + p.o_gfin) : nullptr;
     // dV: queries K, keys Q, values dO in reversed time, its final state G_0;
     // dK: queries V, keys dO, values Q in reversed time
-    ChunkArgs c2 = fwd_args(a.K, a.Q, a.dO, a.dV, g0, gfin, a.B, a.H, a.T, a.dk, a.dv, fws,
+    ChunkArgs c2 = fwd_args(Kp, Qp, a.dO, a.dV, g0, gfin, a.B, a.H, a.T, a.dk, a.dv, fws,
                             p.fwd_bytes, nullptr);
-    ChunkArgs c3 = fwd_args(a.V, a.dO, a.Q, a.dK, g0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
+    ChunkArgs c3 = fwd_args(a.V, a.dO, Qp, dKp, g0t, nullptr, a.B, a.H, a.T, a.dv, a.dk, fws,
                             p.fwd_bytes, nullptr);
     c2.reverse = c3.reverse = true;
     if (tc_reverse_supported(c2, g) && tc_reverse_supported(c3, g)) {
@@ -579,8 +652,8 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
         void* dor = ws + p.o_dor;
         void* dvr = ws + p.o_dvr;
         void* dkr = ws + p.o_dkr;
-        if ((e = reverse_time(a.Q, qr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
-        if ((e = reverse_time(a.K, kr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(Qp, qr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(Kp, kr, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
         if ((e = reverse_time(a.V, vr, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
         if ((e = reverse_time(a.dO, dor, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
         c2.Q = kr; c2.K = qr; c2.V = dor; c2.O = dvr;
@@ -589,11 +662,20 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs& a, const KernelGammas& g, cudaStr
         if ((e = launch_chunk_tc(c2, g, s, &launches)) != cudaSuccess) return e;
         if ((e = launch_chunk_tc(c3, g, s, &launches)) != cudaSuccess) return e;
         if ((e = reverse_time(dvr, a.dV, nbh, a.T, a.dv, s)) != cudaSuccess) return e;
-        if ((e = reverse_time(dkr, a.dK, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
+        if ((e = reverse_time(dkr, dKp, nbh, a.T, a.dk, s)) != cudaSuccess) return e;
     }
     if (a.dS0) {  // dS_0 = gamma G_0
         if ((e = state_scale(gfin, a.dS0, nbh, a.H, a.dk, a.dv, false, false, g, s)) != cudaSuccess)
             return e;
+    }
+    if (a.phi) {  // dq = dq~ phi'(q), dk = dk~ phi'(k)
+        TraceScope trace("phi_grad_pair_kernel", s);
+        phi_grad_pair_kernel<<<(unsigned)std::max<size_t>(1, std::min<size_t>((2 * n8 + 255) / 256, 152 * 16)),
+                               256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(dQp), static_cast<const __nv_bfloat16*>(a.Q),
+            static_cast<__nv_bfloat16*>(a.dQ), static_cast<const __nv_bfloat16*>(dKp),
+            static_cast<const __nv_bfloat16*>(a.K), static_cast<__nv_bfloat16*>(a.dK), n8);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

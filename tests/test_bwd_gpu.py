@@ -136,6 +136,41 @@ def test_bwd_tensor_core_path(shape, opts):
     check("dS0 tc vs simt", to_np(dS0), to_np(sS0), TOL["bf16"])
 
 
+@pytest.mark.parametrize("shape,gammas", [((2, 2, 260, 64, 64), None), ((1, 2, 3000, 128, 64), [1.0, 0.99]),
+                                          ((1, 2, 300, 64, 128), [0.5, 0.9])],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else None)
+def test_bwd_phi_tensor_core_path(shape, gammas, opts):
+    """phi = elu + 1 without the normaliser: the three tensor-core passes over phi(q),
+    phi(k) (reversed copies where a gamma is out of the reversed walk's range), the
+    q and k gradients through phi' at the end, against the oracle."""
+    opts.path("auto")
+    B, H, T, dk, dv = shape
+    seed = zlib.crc32(repr((shape, gammas, "bwd-phi")).encode()) % 100000
+    x = workloads.random_case(seed, B, H, T, dk, dv, dtype="bf16", gamma=gammas, phi=True)
+    rng = np.random.default_rng(seed)
+    dO = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(torch.bfloat16)
+    S0 = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.3)
+    dST = torch.from_numpy(rng.standard_normal((B, H, dk, dv)).astype(np.float32) * 0.1)
+    q, k, v, g_o = (t.to(DEV).contiguous() for t in (x["q"], x["k"], x["v"], dO))
+    la.trace_enable(4096)
+    try:
+        la.trace_collect()
+        dq, dk_, dv_, dS0, _ = la.chunk_bwd(q, k, v, g_o, x["gamma"], phi=True, S0=S0.to(DEV),
+                                            dS_T=dST.to(DEV))
+        torch.cuda.synchronize()
+        names = [n for n, _ in la.trace_collect()]
+    finally:
+        la.trace_enable(0)
+    assert "phi_prep_kernel" in names and "phi_grad_pair_kernel" in names, names
+    assert not any(n.startswith("chunk_bwd_simt") for n in names), names
+    rq, rk, rv, rS0, _ = oracle.recurrent_bwd(x["q"], x["k"], x["v"], x["gamma"], dO, phi=True,
+                                              S0=S0, dS_T=dST)
+    check("dq", to_np(dq), rq, TOL["bf16"])
+    check("dk", to_np(dk_), rk, TOL["bf16"])
+    check("dv", to_np(dv_), rv, TOL["bf16"])
+    check("dS0", to_np(dS0), rS0, TOL["bf16"])
+
+
 REVERSE_CASES = [  # shape, gammas, whether the kernel walks reversed time itself
     ((1, 2, 300, 64, 64), [1.0, 0.9], True),        # gamma = 1 beside gamma < 1; ragged tail
     ((2, 2, 3000, 64, 128), [0.999, 0.8], True),    # segments (scan), d_k != d_v

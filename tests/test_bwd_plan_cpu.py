@@ -57,3 +57,32 @@ def test_three_forward_passes_give_the_gradients(T, dk, dv, gamma):
     np.testing.assert_allclose(dk_, rk[0, 0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dv_, rv[0, 0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dS0, rS0[0, 0], rtol=1e-10, atol=1e-12)
+
+
+def phi(x):
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+@pytest.mark.parametrize("T,dk,dv,gamma", [(37, 8, 5, 0.97), (64, 6, 9, 1.0)])
+def test_three_forward_passes_with_phi(T, dk, dv, gamma):
+    """With phi = elu + 1 and no normaliser the same passes run on phi(q), phi(k), and
+    the chain rule through phi multiplies the q and k gradients by phi'(x) = 1 above
+    zero, e^x at or below."""
+    rng = np.random.default_rng(T * 1000 + dk + 1)
+    q, k = rng.standard_normal((2, T, dk))
+    v, dO = rng.standard_normal((2, T, dv))
+    S0 = rng.standard_normal((dk, dv)) * 0.3
+    dST = rng.standard_normal((dk, dv)) * 0.1
+    qt, kt = phi(q), phi(k)
+    dqt, _ = forward(dO, v, kt, gamma, S0.T)
+    dv_, G0 = reversed_forward(kt, qt, dO, gamma, dST / gamma)
+    dkt, _ = reversed_forward(v, dO, qt, gamma, dST.T / gamma)
+    dq = dqt * np.where(q > 0, 1.0, np.exp(np.minimum(q, 0.0)))
+    dk_ = dkt * np.where(k > 0, 1.0, np.exp(np.minimum(k, 0.0)))
+    rq, rk, rv, rS0, _ = oracle.recurrent_bwd(q[None, None], k[None, None], v[None, None],
+                                              [gamma], dO[None, None], S0=S0[None, None],
+                                              dS_T=dST[None, None], phi=True)
+    np.testing.assert_allclose(dq, rq[0, 0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk_, rk[0, 0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv_, rv[0, 0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gamma * G0, rS0[0, 0], rtol=1e-10, atol=1e-12)
