@@ -31,10 +31,12 @@
 // <= 128).
 //
 // Segments: so that every SM holds several CTAs, each sequence is cut into P
-// segments of whole chunks.  A state-only pass computes each segment's own
-// contribution (forward: S and z from zero over the segment; backward: G and
-// Gz from zero, i.e. the gradient of the segment's own outputs with respect to
-// the state entering it), a scan folds them into entry states (forward:
+// segments of whole chunks.  Each segment's own contribution (forward: S and z
+// from zero over the segment; backward: G and Gz from zero, i.e. the gradient of
+// the segment's own outputs with respect to the state entering it) comes from a
+// weighted product over its tokens (bwd_state_gemm_kernel, d_k and d_v in
+// {64, 128}) or a state-only pass of the chunked kernel, a scan folds them into
+// entry states (forward:
 // S_entry(q+1) = d(q) S_entry(q) + agg(q) from S_0; backward: G_end(q) =
 // d(q+1) G_end(q+1) + gagg(q+1) from dS_T; d(q) the state's decay over segment
 // q), and the full sweeps run every segment from its entry state.
