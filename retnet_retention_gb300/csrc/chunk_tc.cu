@@ -623,8 +623,13 @@ __global__ void segment_scan_kernel(const float* __restrict__ S0, const float* _
 // sequence) and the decays a_i themselves, into gate[bh][c][0..127] and
 // [128..255].  One warp per chunk: each lane scans four tokens, then the lanes'
 // totals are scanned with shuffles.
+// It also flags each chunk whose decay from its first row to its last is below
+// 2^-160, or not a number (flags[bh][c] = 1): the factored build's factors about the
+// chunk's middle exponent reach 2^(+-Delta/2) for a decay of 2^-Delta, and past 2^80
+// products of them with the data would leave the bf16 range, so the chunk's CTA takes
+// the build with row scalings.
 __global__ void gate_prep_kernel(const float* __restrict__ log_a, float* __restrict__ gate, int T,
-                                 int n_chunks, size_t total_chunks) {
+                                 int n_chunks, size_t total_chunks, int* __restrict__ flags) {
     const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= total_chunks) return;  // whole warps only: the block size is a multiple of 32
@@ -650,6 +655,11 @@ __global__ void gate_prep_kernel(const float* __restrict__ log_a, float* __restr
     float* gp = gate + wid * 256;
     reinterpret_cast<float4*>(gp)[lane] = make_float4(l[0] + ex, l[1] + ex, l[2] + ex, l[3] + ex);
     reinterpret_cast<float4*>(gp + 128)[lane] = make_float4(a[0], a[1], a[2], a[3]);
+    if (flags) {  // b_0 - b_(L-1): the sum of lanes' totals past token 0 (rows past T add 0)
+        const float total = __shfl_sync(0xffffffffu, inc, 31);
+        const float first = __shfl_sync(0xffffffffu, l[0], 0);
+        if (lane == 0) flags[wid] = (first - total) <= 160.f ? 0 : 1;
+    }
 }
 
 }  // namespace
@@ -745,7 +755,7 @@ struct TcPlan {
     int Pu;          // segments actually used
     // workspace byte offsets: per-token decays per chunk, segment decays, then the
     // segment states (agg, entry: [BH][Pu][dk][dv]; zagg, zentry: [BH][Pu][dk])
-    size_t o_gate, o_segl2, o_agg, o_entry, o_zagg, o_zentry, bytes;
+    size_t o_gate, o_segl2, o_gflag, o_agg, o_entry, o_zagg, o_zentry, bytes;
 };
 
 TcPlan tc_plan(const ChunkArgs& a) {
@@ -764,6 +774,8 @@ TcPlan tc_plan(const ChunkArgs& a) {
         off += nbh * pl.n_chunks * 256 * sizeof(float);
         pl.o_segl2 = off;
         if (pl.P > 1) off += (nbh * pl.P * sizeof(float) + 15) / 16 * 16;
+        pl.o_gflag = off;  // per chunk: the factored build does not apply
+        off += (nbh * pl.n_chunks * sizeof(int) + 15) / 16 * 16;
     }
     if (pl.P > 1) {
         const size_t st = nbh * pl.P * a.dk * a.dv * sizeof(float), zt = nbh * pl.P * a.dk * sizeof(float);
@@ -783,8 +795,11 @@ int tc_launch_count(const ChunkArgs& a) {
     if (a.noncausal || a.T <= 0) return 1;
     const TcPlan pl = tc_plan(a);
     const int prep = a.log_a ? 1 : 0;
-    if (pl.P <= 1) return 1 + prep;
-    return (fold_segments(pl.Pu, a.dk, pl.dvb, a.normalize) ? 2 : 3) + prep;
+    // per-token decay without normaliser or z: the output walk in two builds (launch_chunk_tc)
+    const int out = a.log_a && !a.phi && !a.normalize && !a.z_out && (a.dk == 64 || pl.dvb == 64) &&
+                            tc_ws_supported(kFull, a.dk, pl.dvb, false) ? 2 : 1;
+    if (pl.P <= 1) return out + prep;
+    return (fold_segments(pl.Pu, a.dk, pl.dvb, a.normalize) ? 1 + out : 2 + out) + prep;
 }
 
 size_t tc_workspace_bytes(const ChunkArgs& a) { return tc_plan(a).bytes; }
@@ -862,14 +877,38 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         {
             TraceScope trace("gate_prep_kernel", s);
             gate_prep_kernel<<<(unsigned)((total_chunks * 32 + 255) / 256), 256, 0, s>>>(
-                a.log_a, gate, a.T, n_chunks, total_chunks);
+                a.log_a, gate, a.T, n_chunks, total_chunks, reinterpret_cast<int*>(ws + pl.o_gflag));
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         prm.gate = gate;
         prm.seg_l2 = pl.P > 1 ? reinterpret_cast<float*>(ws + pl.o_segl2) : nullptr;
+        prm.gate_flags = reinterpret_cast<const int*>(ws + pl.o_gflag);
         *launches = 1;
     }
+    // The per-token decay without normaliser or z in the factored build wherever a
+    // unit's chunks allow it (gate_prep_kernel's flags): the output walk goes out
+    // twice, the factored build's CTAs taking those units and the row-scaling build's
+    // the others (each leaving the units that are not its own).  A state walk has no
+    // row factors and keeps the row scalings.
+    const bool split = a.log_a && !a.phi && !prm.track_z && !a.noncausal && (a.dk == 64 || dvb == 64) &&
+                       tc_ws_supported(kFull, a.dk, dvb, false);
+    auto dispatch = [&](const TcParams& pp, int grid, bool pdl) -> cudaError_t {
+        if (!split || pp.mode != kFull) {
+            *launches += 1;
+            return launch_tc_dispatch(a.dk, dvb, pp, grid, s, pdl);
+        }
+        TcParams p1 = pp;
+        p1.fact = 1;
+        p1.gate_split = 1;
+        cudaError_t e1 = launch_tc_dispatch(a.dk, dvb, p1, grid, s, pdl);
+        if (e1 != cudaSuccess) return e1;
+        TcParams p2 = pp;
+        p2.fact = 0;
+        p2.gate_split = 2;
+        *launches += 2;
+        return launch_tc_dispatch(a.dk, dvb, p2, grid, s, pdl);
+    };
     if (pl.P <= 1) {
         prm.mode = kFull;
         prm.seg_chunks = n_chunks;
@@ -881,8 +920,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         prm.z_out = a.z_out;
         prm.out_nseg = 1;
         prm.out_last_only = 1;
-        *launches += 1;
-        return launch_tc_dispatch(a.dk, dvb, prm, units, s);
+        return dispatch(prm, units, false);
     }
     // segmented: (1) each segment's own state, (2) scan to entry states, (3) outputs
     const int seg_chunks = pl.seg_chunks;
@@ -903,9 +941,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     pa.z_out = zagg;
     pa.out_nseg = Pu;  // contributions keep the [BH][Pu] layout the scan and the fold read
     pa.out_last_only = 0;
-    cudaError_t e = a.agg_ready ? cudaSuccess : launch_tc_dispatch(a.dk, dvb, pa, units * (Pu - 1), s);
+    cudaError_t e = a.agg_ready ? cudaSuccess : dispatch(pa, units * (Pu - 1), false);
     if (e != cudaSuccess) return e;
-    const int walk = a.agg_ready ? 0 : 1;  // the state walk's launch, if any
     TcParams pc = prm;
     pc.mode = kFull;
     pc.seg_chunks = seg_chunks;
@@ -922,8 +959,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         pc.in_agg = 1;
         pc.S0 = a.S0;
         pc.z0 = a.z0;
-        *launches += 1 + walk;
-        return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
+        return dispatch(pc, units * Pu, /*pdl=*/true);
     }
     const size_t total = nbh * (size_t)a.dk * a.dv;
     {
@@ -944,8 +980,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
     if (e != cudaSuccess) return e;
     pc.S_in = entry;
     pc.z_in = zentry;
-    *launches += 2 + walk;
-    return launch_tc_dispatch(a.dk, dvb, pc, units * Pu, s, /*pdl=*/true);
+    *launches += 1;  // the scan
+    return dispatch(pc, units * Pu, /*pdl=*/true);
 }
 
 }  // namespace la

@@ -215,7 +215,8 @@ static_assert(kNumBars <= 32, "mbarrier slots");
 // a_j instead of gamma.
 template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
 __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
-    static_assert(!FACT || (!GATED && !PHI && !NORM), "the factored decay is for plain retention");
+    static_assert(!FACT || (!PHI && !NORM), "the factored decay is for plain retention");
+    static_assert(!(FACT && GATED && STATE_ONLY), "a state walk with per-token decays takes the row scalings");
     constexpr int kThreadsC = threads_c(DK, DVB, PHI);
     constexpr int kThreadsWS = threads_ws(DK, DVB, PHI);
     using Lay = LayoutWS<DK, DVB, NORM && !STATE_ONLY, PHI, GATED>;
@@ -299,6 +300,28 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
     auto dec_total = [&](const float* gc, int L) {  // the state's decay over the chunk: gamma^L
         return GATED ? exp2f(gc[L - 1]) : gamma_pow(l2g, (float)L);
     };
+    // The factored build with the per-token decay takes its factors about the middle
+    // exponent beta = (b_0 + b_(L-1)) / 2 of the chunk: zeta_j = 2^(beta - b_j) into V,
+    // the row factor 2^(b_i - beta), and MMA3 and MMA4 work on 2^beta S_{c-1}, so that
+    // TMEM holds S_c 2^(beta - b_(L-1)) after MMA4, a factor that the next chunk's E3 and
+    // the exit state take out again.  Every factor stays within 2^(+-Delta/2) for a
+    // chunk that decays by 2^-Delta from its first row to its last.
+    auto fact_beta = [&](const float* gc, int L) { return 0.5f * (gc[0] + gc[L - 1]); };
+    // Per-token decay in two launches (p.gate_split, output walks): the factored build
+    // takes the units whose chunks all keep their decay from first row to last at or
+    // above 2^-160, the build with row scalings the others; a unit's CTA in the other
+    // launch leaves at once, after waiting for the previous kernel like every CTA that
+    // works, so that this launch completes after it.
+    if constexpr (GATED) {
+        if (p.gate_split) {
+            int bad = 0;
+            for (int c = cb + lane; c < ce; c += 32) bad |= p.gate_flags[(size_t)bh * n_chunks + c];
+            if ((__any_sync(0xffffffffu, bad) != 0) == FACT) {
+                griddep_wait();
+                return;
+            }
+        }
+    }
     const uint64_t lim = p.wait_ns;
     if (tid == 0) LA_TL(4000);
     LA_CTA_T(0);
@@ -623,6 +646,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
             // (kPready, after the second of the two); E1 goes first where MMA1 of the
             // chunk is issued before the previous chunk's MMAs (mma1_first: E1 then
             // overlaps them), else E3 does.
+            float lc_prev = 0.f;  // factored, per-token decay: TMEM holds S_{c-1} 2^-lc_prev
             for (int it = 0; it < n && !STATE_ONLY; ++it) {
                 const int c = cb + it;
                 const int L = min(kC, p.T - c * kC);
@@ -638,7 +662,13 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                             fence_after_sync();
                             if (t == 0) LA_TL(it * 16 + 6);
                         }
-                        const float gL = unit_gamma ? 1.f : dec_total(gate_of(it % NS), L);
+                        float gL = unit_gamma ? 1.f : dec_total(gate_of(it % NS), L);
+                        if constexpr (FACT && GATED) {  // 2^beta S_{c-1} from TMEM's S_{c-1} 2^-lc
+                            const float* gc = gate_of(it % NS);
+                            const float beta = fact_beta(gc, L);
+                            gL = exp2f(beta + lc_prev);
+                            lc_prev = gc[L - 1] - beta;
+                        }
 #pragma unroll
                         for (int c0 = half * kSHalf; c0 < (half + 1) * kSHalf; c0 += 32) {
                             uint32_t rs[32];
@@ -863,11 +893,15 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 char* st = sm + s * Lay::kStage;
                 if (t == 0) LA_TL(it * 16 + 12);
                 if constexpr (FACT) {
-                    if (L != zL) {
+                    if (GATED || L != zL) {  // (per-token decay: every chunk its own zeta)
+                        const float* gc = GATED ? gate_of(s) : nullptr;
+                        const float beta = GATED ? fact_beta(gc, L) : 0.f;
 #pragma unroll
-                        for (int m = 0; m < kRowsC; ++m)
-                            split_bf16x2(dec_zeta(nullptr, mrow((t >> 3) + (kThreadsC / 8) * m), L), zh[m],
-                                         zl[m]);
+                        for (int m = 0; m < kRowsC; ++m) {
+                            const int r = mrow((t >> 3) + (kThreadsC / 8) * m);
+                            split_bf16x2(GATED ? (r < L ? exp2f(beta - gc[r]) : 0.f) : dec_zeta(nullptr, r, L),
+                                         zh[m], zl[m]);
+                        }
                         zL = L;
                     }
                     scale_rows_hl<DVB / 64, kThreadsC>(st + Lay::kQ + Lay::kK, zh, zl, t);
@@ -892,6 +926,8 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
             load_entry_state();
             named_bar_arrive(kBarEntry, kThreadsA + 128);
             int L_prev = 0;
+            float rho_prev = 1.f;
+            float lc_last = 0.f;  // factored, per-token decay: TMEM holds S 2^-lc_last
             bool stop = false;
             // exit state: S (after the last MMA4, which the caller has waited for) and z
             auto write_exit_state = [&]() {
@@ -902,6 +938,11 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     uint32_t r[32];
                     tmem_ld32(tbase + lane_off + Lay::kColS + c0, r);
                     tmem_ld_wait();
+                    if constexpr (FACT && GATED) {
+                        const float f = exp2f(lc_last);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                    }
                     if (write && row < DK) {
                         float* srow = p.S_out + ((size_t)oidx * DK + row) * p.dv + v0 + c0;
 #pragma unroll
@@ -914,7 +955,9 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 if (write && p.z_out && dvb == 0 && row < DK) p.z_out[(size_t)oidx * DK + row] = zs[row];
             };
             // E2 of chunk `it`: O rows -> global, divided by the normaliser
-            auto do_e2 = [&](int it, int L) -> bool {
+            // rho: the factored build's row factor 2^(b_i - beta) with the per-token decay
+            // (read from the chunk's stage while it was held)
+            auto do_e2 = [&](int it, int L, float rho) -> bool {
                 bool ok = mbar_wait_or_abort(&bar[kOfull0 + it % NOB], (it / NOB) & 1, lim, abort_flag);
                 if (kE1Sum && ok) ok = mbar_wait_or_abort(&bar[kRsum0 + it % 3], (it / 3) & 1, lim, abort_flag);
                 if (named_bar_or(kBarB, 128, !ok)) return false;
@@ -936,7 +979,7 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                     }
                     inv = 1.f / norm_den(den, p.normalize, p.eps);
                 }
-                if (fact) inv = gamma_pow(l2g, (float)(mrow(row) + 1 - L));  // gamma^(i+1-L)
+                if (fact) inv = GATED ? rho : gamma_pow(l2g, (float)(mrow(row) + 1 - L));  // gamma^(i+1-L)
                 const int c = cb + it;
                 // the row's place in the sequence (reversed time: chunk c starts at row
                 // T - (c + 1) C, before row 0 for the last chunk); rows past the chunk's
@@ -1083,6 +1126,12 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 const float* gc = GATED ? gate_of(s) : nullptr;
                 // the chunk's decay of z, read while the stage is ours (per-token decay)
                 const float gL_gated = GATED ? dec_total(gc, L) : 0.f;
+                float rho = 1.f;
+                if constexpr (FACT && GATED) {
+                    const float beta = fact_beta(gc, L);
+                    rho = exp2f(gc[row] - beta);
+                    lc_last = gc[L - 1] - beta;
+                }
                 // z_c = gamma^L z_{c-1} + sum_j zeta_j phi(K)[j], the sums in fp32 from the
                 // unscaled tile: with gamma = 1 while epilogue B would otherwise wait for
                 // MMA3 of the previous chunk, with gamma < 1 in the pass that scales K
@@ -1134,14 +1183,15 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                 }
                 if (t == 0) mbar_arrive(&bar[kEmpty0 + s]);  // our generic reads of stage s are done
                 if (t == 0) LA_TL(it * 16 + 9);
-                if (it >= 1 && !do_e2(it - 1, L_prev)) {
+                if (it >= 1 && !do_e2(it - 1, L_prev, rho_prev)) {
                     stop = true;
                     break;
                 }
                 L_prev = L;
+                rho_prev = rho;
             }
             if (!STATE_ONLY && !stop && !*abort_flag) {
-                if (do_e2(n - 1, L_prev)) write_exit_state();  // do_e2 waited for MMA4
+                if (do_e2(n - 1, L_prev, rho_prev)) write_exit_state();  // do_e2 waited for MMA4
             }
         }
     }
@@ -1214,10 +1264,16 @@ template <bool GATED>
 cudaError_t dispatch_ws(int dk, int dvb, bool normalize, const TcParams& prm, int grid,
                         cudaStream_t s, bool pdl) {
     const bool phi = prm.phi != 0;
-    if constexpr (!GATED) {
-        if (prm.fact) {  // plain retention with every head's decay in the factored form's range
-            if (phi || normalize) return cudaErrorInvalidValue;
-            const bool st = prm.mode == kStateOnly;
+    if (prm.fact) {  // plain retention with its decays in the factored form's range
+        if (phi || normalize) return cudaErrorInvalidValue;
+        const bool st = prm.mode == kStateOnly;
+        if constexpr (GATED) {  // output walks (a state walk with these decays keeps the row scalings)
+            if (st) return cudaErrorInvalidValue;
+            if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false, false, true, true>(prm, grid, s, pdl);
+            if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false, false, true, true>(prm, grid, s, pdl);
+            if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false, false, true, true>(prm, grid, s, pdl);
+            return cudaErrorInvalidValue;  // (no room for the decays beside two 96 KB stages at 128 x 128)
+        } else {
             if (dk == 64 && dvb == 64)
                 return st ? launch_ws<64, 64, false, true, false, false, true>(prm, grid, s, pdl)
                           : launch_ws<64, 64, false, false, false, false, true>(prm, grid, s, pdl);

@@ -87,9 +87,10 @@ def test_gated_launch_count_follows_the_plan(opts):
     """The decays' prep kernel, then the state walk, [scan,] output walk."""
     opts.path("tc")
     lib = la.library()
-    assert lib.la_chunk_fwd_launches(2, 16, 1000, 64, 64, 1, la.LA_GATED, 0) == 3
-    assert lib.la_chunk_fwd_launches(1, 1, 3000, 64, 64, 1, la.LA_GATED, 0) == 4
-    assert lib.la_chunk_fwd_launches(4, 16, 4096, 128, 128, 1, la.LA_GATED, 0) == 2
+    # (no normaliser: the output walk in the factored build and the row-scaling build)
+    assert lib.la_chunk_fwd_launches(2, 16, 1000, 64, 64, 1, la.LA_GATED, 0) == 4
+    assert lib.la_chunk_fwd_launches(1, 1, 3000, 64, 64, 1, la.LA_GATED, 0) == 5
+    assert lib.la_chunk_fwd_launches(4, 16, 4096, 128, 128, 1, la.LA_GATED, 0) == 3
     x = workloads.random_case(5, 1, 1, 3000, 64, 64, dtype="bf16", gate=True)
     la.trace_enable(64)
     try:
@@ -175,3 +176,47 @@ def test_gated_retention_bf16_sampled():
                                        x["v"][bi, hi][None], x["log_a"][bi, hi][None])
     check("O", O[bi, hi].double().cpu().numpy(), Or[0], TOL["bf16"])
     check("S_T", S[bi, hi].double().cpu().numpy(), Sr[0], TOL["bf16"])
+
+
+SPLIT_CASES = [  # B, H, T, dk, dv: per-token decay, no normaliser, no z
+    (2, 16, 1000, 64, 64),   # segments folded in the output walk
+    (1, 1, 3000, 64, 64),    # segments with a scan
+    (4, 4, 300, 128, 128),   # one segment, 64-wide value blocks
+    (2, 3, 200, 64, 128),
+    (1, 2, 129, 64, 64),     # one full chunk and a one-row chunk
+]
+
+
+@pytest.mark.parametrize("strong", [0.3, 0.6], ids=["a0.3", "a0.6"])
+@pytest.mark.parametrize("shape", SPLIT_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_gated_factored_and_row_scaled_builds(shape, strong, opts):
+    """Per-token decay without normaliser or z: the output walk goes out in two builds,
+    the factored one taking the sequences whose chunks all keep their decay from first
+    row to last at or above 2^-160 and the row-scaling one the others.  Every other
+    sequence here decays strongly: a_t around 0.3 (about 2^-220 over a chunk: row
+    scalings) or 0.6 (about 2^-94: the factored build, with factors near 2^+-47 about
+    the chunk's middle); the rest follow the recipe's gates.  Outputs and final states
+    are checked against the oracle, and the trace holds both output walks."""
+    opts.path("tc")
+    B, H, T, dk, dv = shape
+    x = workloads.random_case(zlib.crc32(repr((shape, strong)).encode()) % 100000, B, H, T, dk, dv,
+                              dtype="bf16", gate=True)
+    log_a = x["log_a"].clone()
+    sel = torch.zeros(B * H, dtype=torch.bool)
+    sel[::2] = True
+    sel = sel.view(B, H)
+    log_a[sel] = float(np.log(strong)) + 0.05 * log_a[sel]
+    q, k, v = (x[n].to(DEV).contiguous() for n in ("q", "k", "v"))
+    la.trace_enable(256)
+    try:
+        la.trace_collect()
+        O, S, _ = la.chunk_fwd(q, k, v, log_a=log_a.to(DEV).contiguous())
+        torch.cuda.synchronize()
+        names = [n for n, _ in la.trace_collect()]
+    finally:
+        la.trace_enable(0)
+    assert len(names) == la.library().la_chunk_fwd_launches(B, H, T, dk, dv, 1, la.LA_GATED, 0), names
+    assert sum(n == "chunk_tc_ws_kernel/full" for n in names) == 2, names
+    Or, Sr, _ = oracle.recurrent_gated(x["q"], x["k"], x["v"], log_a)
+    check("O", O.double().cpu().numpy(), Or, TOL["bf16"])
+    check("S_T", S.double().cpu().numpy(), Sr, TOL["bf16"])
