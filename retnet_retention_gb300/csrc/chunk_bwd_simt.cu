@@ -113,8 +113,10 @@ __host__ __device__ inline BwdSmem bwd_layout(int C, int dk, int dv, bool taylor
     L.k = L.q + C * ldk;
     L.v = L.k + C * ldk;
     L.g = L.v + C * ldv;   // dO, then dn = dO / den
-    L.n = L.g + C * ldv;   // n_i (forward sweep); the decayed copy for the state update
-    L.a = L.n + C * (dv + 4);
+    // S dO_i (forward sweep with the normaliser; in the tq buffer with the Taylor
+    // map); the decayed copy for the state update
+    L.n = L.g + C * ldv;
+    L.a = L.n + C * (taylor ? dv + 4 : std::max(dv + 4, ldk));
     L.p = L.a + C * lda;
     L.s = L.p + C * lda;   // S (forward sweep) or G (backward sweep), rows dv + 1 apart
     L.z = L.s + dk * ldv;  // z or Gz
@@ -409,70 +411,97 @@ __global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 6
             }
         }
         __syncthreads();
-        if (role == 0 && !st_only) {
-            if (normalize) {
-                // n_i = sum_j A_ij v_j + xi_i q~_i S  (A_ij = 0 above the diagonal)
-                tiles(L, dv, [&](int i0, int c0, int c1) {
-                    const int a0 = c0 < dv ? c0 : 0, a1 = c1 < dv ? c1 : 0;
-                    float in[4][2] = {}, it[4][2] = {};
-                    const int jmax = min(i0 + 3, L - 1);
-                    for (int j = 0; j <= jmax; ++j) {
-                        const float x0 = Vs[j * ldv + a0], x1 = Vs[j * ldv + a1];
+        // The forward sweep with the normaliser never forms n_i: with X_i = S dO_i and
+        // B_ij = dO_i . v_j (j <= i), dO_i . n_i = sum_j A_ij B_ij + xi_i q~_i . X_i, and
+        // the gradient's terms become P_ij = D_ij (B_ij / den_i + du_i) and
+        // xi_i (X_i / den_i + du_i z), so the products with S and with V run once.
+        const bool fwd_norm = role == 0 && !st_only && normalize;
+        float* Xs = taylor ? TQ : Ns;  // X_i, rows ldk apart
+        if (fwd_norm) {
+            // B_ij into Ps (zero above the diagonal): tiles of 4 rows i and one column j
+            for (int item = tid; item < ((L + 3) >> 2) * 32; item += kThreads) {
+                const int j = item & 31, i0 = (item >> 5) * 4;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (j < L && j <= i0 + 3) {
+                    const float* vj = Vs + j * ldv;
+                    for (int cc2 = 0; cc2 < dv; ++cc2) {
+                        const float vv = vj[cc2];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const float a = As[(i0 + r) * lda + j];
-                            in[r][0] = fmaf(a, x0, in[r][0]);
-                            in[r][1] = fmaf(a, x1, in[r][1]);
-                        }
-                    }
-                    for (int d = 0; d < dk; ++d) {
-                        const float s0 = Ss[d * lds + a0], s1 = Ss[d * lds + a1];
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const float q = Qs[(i0 + r) * ldk + d];
-                            it[r][0] = fmaf(q, s0, it[r][0]);
-                            it[r][1] = fmaf(q, s1, it[r][1]);
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int i = i0 + r;
-                        if (i >= L) continue;
-                        if (c0 < dv) Ns[i * ldv + c0] = in[r][0] + xi(i) * it[r][0];
-                        if (c1 < dv) Ns[i * ldv + c1] = in[r][1] + xi(i) * it[r][1];
-                    }
-                });
-                __syncthreads();
-                // den_i, du_i (one warp per row: the sums over d_k and d_v)
-                const int warp = tid >> 5, lane = tid & 31;
-                for (int i = warp; i < L; i += kThreads / 32) {
-                    float r = 0.f, qz = 0.f, don = 0.f;
-                    for (int j = lane; j <= i; j += 32) r += As[i * lda + j];
-                    for (int d = lane; d < dk; d += 32) qz = fmaf(Qs[i * ldk + d], zs[d], qz);
-                    for (int cc2 = lane; cc2 < dv; cc2 += 32)
-                        don = fmaf(Gs[i * ldv + cc2], Ns[i * ldv + cc2], don);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        r += __shfl_xor_sync(0xffffffffu, r, off);
-                        qz += __shfl_xor_sync(0xffffffffu, qz, off);
-                        don += __shfl_xor_sync(0xffffffffu, don, off);
-                    }
-                    if (lane == 0) {
-                        const float u = r + xi(i) * qz;
-                        const float dd = norm_den(u, normalize, eps);
-                        const float dd_du = normalize == 2 ? (fabsf(u) > 1.f ? (u > 0.f ? 1.f : -1.f) : 0.f)
-                                                           : 1.f;
-                        den[i] = dd;
-                        du[i] = -don / (dd * dd) * dd_du;
-                        stats[((size_t)bh * T_len + t0 + i) * 2] = dd;
-                        stats[((size_t)bh * T_len + t0 + i) * 2 + 1] = du[i];
+                        for (int r = 0; r < 4; ++r) acc[r] = fmaf(Gs[(i0 + r) * ldv + cc2], vv, acc[r]);
                     }
                 }
-                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r;
+                    if (i < L && j < L) Ps[i * lda + j] = j <= i ? acc[r] : 0.f;
+                }
             }
+            // X_i = S dO_i
+            tiles(L, dk, [&](int i0, int c0, int c1) {
+                const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
+                float it[4][2] = {};
+                for (int cc2 = 0; cc2 < dv; ++cc2) {
+                    const float s0 = Ss[a0 * lds + cc2], s1 = Ss[a1 * lds + cc2];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float gg = Gs[(i0 + r) * ldv + cc2];
+                        it[r][0] = fmaf(s0, gg, it[r][0]);
+                        it[r][1] = fmaf(s1, gg, it[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r;
+                    if (i >= L) continue;
+                    if (c0 < dk) Xs[i * ldk + c0] = it[r][0];
+                    if (c1 < dk) Xs[i * ldk + c1] = it[r][1];
+                }
+            });
+            __syncthreads();
+            // den_i, du_i (one warp per row: the sums over j, d_k)
+            const int warp = tid >> 5, lane = tid & 31;
+            for (int i = warp; i < L; i += kThreads / 32) {
+                float r = 0.f, qz = 0.f, don = 0.f, qx = 0.f;
+                for (int j = lane; j <= i; j += 32) {
+                    const float a = As[i * lda + j];
+                    r += a;
+                    don = fmaf(a, Ps[i * lda + j], don);
+                }
+                for (int d = lane; d < dk; d += 32) {
+                    const float q = Qs[i * ldk + d];
+                    qz = fmaf(q, zs[d], qz);
+                    qx = fmaf(q, Xs[i * ldk + d], qx);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    r += __shfl_xor_sync(0xffffffffu, r, off);
+                    qz += __shfl_xor_sync(0xffffffffu, qz, off);
+                    don += __shfl_xor_sync(0xffffffffu, don, off);
+                    qx += __shfl_xor_sync(0xffffffffu, qx, off);
+                }
+                if (lane == 0) {
+                    const float u = r + xi(i) * qz;
+                    const float dd = norm_den(u, normalize, eps);
+                    const float dd_du = normalize == 2 ? (fabsf(u) > 1.f ? (u > 0.f ? 1.f : -1.f) : 0.f)
+                                                       : 1.f;
+                    don = fmaf(xi(i), qx, don);  // dO_i . n_i
+                    den[i] = dd;
+                    du[i] = -don / (dd * dd) * dd_du;
+                    stats[((size_t)bh * T_len + t0 + i) * 2] = dd;
+                    stats[((size_t)bh * T_len + t0 + i) * 2 + 1] = du[i];
+                }
+            }
+            __syncthreads();
+            // P_ij = D_ij (B_ij / den_i + du_i), in place
+            for (int idx = tid; idx < L * 32; idx += kThreads) {
+                const int i = idx >> 5;
+                for (int j = idx & 31; j < L; j += 32)
+                    if (j <= i) Ps[i * lda + j] = (Ps[i * lda + j] / den[i] + du[i]) * dmask(i, j);
+            }
+            __syncthreads();
         }
-        // dn_i = dO_i / den_i (in place)
-        if (normalize && need_qg) {
+        // dn_i = dO_i / den_i (in place; the backward sweep)
+        if (normalize && need_qg && !fwd_norm) {
             for (int idx = tid; idx < L * dv; idx += kThreads) {
                 const int i = idx / dv, cc2 = idx % dv;
                 Gs[i * ldv + cc2] /= den[i];
@@ -480,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 6
             __syncthreads();
         }
         // P_ij = D_ij (dn_i . v_j + du_i)  (j <= i): tiles of 4 rows i and one column j
-        for (int item = tid; item < (st_only ? 0 : ((L + 3) >> 2) * 32); item += kThreads) {
+        for (int item = tid; item < (st_only || fwd_norm ? 0 : ((L + 3) >> 2) * 32); item += kThreads) {
             const int j = item & 31, i0 = (item >> 5) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (j < L && j <= i0 + 3) {
@@ -501,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 6
         __syncthreads();
         if (role == 0) {
             // dq~_i = sum_j P_ij k~_j + xi_i (S dn_i + du_i z);  dq = dq~ * phi'(q)
+            // (with the normaliser S dn_i = X_i / den_i)
             if (!st_only) tiles(L, dk, [&](int i0, int c0, int c1) {
                 const int a0 = c0 < dk ? c0 : 0, a1 = c1 < dk ? c1 : 0;
                 float in[4][2] = {}, it[4][2] = {};
@@ -514,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 6
                         in[r][1] = fmaf(pp, k1, in[r][1]);
                     }
                 }
-                for (int cc2 = 0; cc2 < dv; ++cc2) {
+                for (int cc2 = 0; cc2 < (fwd_norm ? 0 : dv); ++cc2) {
                     const float s0 = Ss[a0 * lds + cc2], s1 = Ss[a1 * lds + cc2];
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -531,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, DKc == 0 ? 4 : DKc == 64 && DVc == 6
                     for (int e = 0; e < 2; ++e) {
                         const int d = e ? c1 : c0;
                         if (d >= dk) continue;
-                        float inter = it[r][e];
+                        float inter = fwd_norm ? Xs[i * ldk + d] / den[i] : it[r][e];
                         if (normalize) inter = fmaf(du[i], zs[d], inter);
                         float v = in[r][e] + xi(i) * inter;
                         if (phi) v *= fminf(1.f, Qs[i * ldk + d]);
