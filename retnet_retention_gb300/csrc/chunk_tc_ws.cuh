@@ -663,10 +663,14 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                             if (t == 0) LA_TL(it * 16 + 6);
                         }
                         float gL = unit_gamma ? 1.f : dec_total(gate_of(it % NS), L);
-                        if constexpr (FACT && GATED) {  // 2^beta S_{c-1} from TMEM's S_{c-1} 2^-lc
+                        float gL2 = 1.f;
+                        if constexpr (FACT && GATED) {
+                            // 2^beta S_{c-1} from TMEM's S_{c-1} 2^-lc, as two factors (each
+                            // >= 2^-80 in range; their product need not be)
                             const float* gc = gate_of(it % NS);
                             const float beta = fact_beta(gc, L);
-                            gL = exp2f(beta + lc_prev);
+                            gL = exp2f(lc_prev);
+                            gL2 = exp2f(beta);
                             lc_prev = gc[L - 1] - beta;
                         }
 #pragma unroll
@@ -676,7 +680,9 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
                             tmem_ld_wait();
                             if (fact) {  // MMA3 reads gamma^L S_{c-1}
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) rs[e] = __float_as_uint(__uint_as_float(rs[e]) * gL);
+                                for (int e = 0; e < 32; ++e)
+                                    rs[e] = __float_as_uint(GATED ? __uint_as_float(rs[e]) * gL * gL2
+                                                                  : __uint_as_float(rs[e]) * gL);
                             }
                             if (row < DK) {
 #pragma unroll

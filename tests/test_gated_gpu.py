@@ -187,15 +187,16 @@ SPLIT_CASES = [  # B, H, T, dk, dv: per-token decay, no normaliser, no z
 ]
 
 
-@pytest.mark.parametrize("strong", [0.3, 0.6], ids=["a0.3", "a0.6"])
+@pytest.mark.parametrize("strong", [0.3, 0.43, 0.6], ids=["a0.3", "a0.43", "a0.6"])
 @pytest.mark.parametrize("shape", SPLIT_CASES, ids=lambda s: "x".join(map(str, s)))
 def test_gated_factored_and_row_scaled_builds(shape, strong, opts):
     """Per-token decay without normaliser or z: the output walk goes out in two builds,
     the factored one taking the sequences whose chunks all keep their decay from first
     row to last at or above 2^-160 and the row-scaling one the others.  Every other
     sequence here decays strongly: a_t around 0.3 (about 2^-220 over a chunk: row
-    scalings) or 0.6 (about 2^-94: the factored build, with factors near 2^+-47 about
-    the chunk's middle); the rest follow the recipe's gates.  Outputs and final states
+    scalings), 0.43 (about 2^-155, chunks on both sides of the bound: factors up to
+    2^+-80 in the factored build) or 0.6 (about 2^-94: factors near 2^+-47 about the
+    chunk's middle); the rest follow the recipe's gates.  Outputs and final states
     are checked against the oracle, and the trace holds both output walks."""
     opts.path("tc")
     B, H, T, dk, dv = shape
