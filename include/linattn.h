@@ -125,9 +125,7 @@ LA_API size_t la_workspace_size(int B, int H, int T, int d_k, int d_v, la_dtype 
  * device (1 for the single-pass paths; 2 or 3 when long sequences are split
  * into segments: segment states, then - for more than four segments per
  * sequence - the scan over them, then the outputs).  LA_GATED adds the decays'
- * preparation, and without a normaliser (and without z_out, which the count
- * assumes) the output walk goes out twice: a factored build and a build with
- * row scalings, each working on the sequences whose chunks suit it.  0 for
+ * preparation.  0 for
  * arguments la_chunk_fwd would reject or T == 0.  Pure host query.
  */
 LA_API int la_chunk_fwd_launches(int B, int H, int T, int d_k, int d_v, la_dtype dtype,

@@ -795,11 +795,8 @@ int tc_launch_count(const ChunkArgs& a) {
     if (a.noncausal || a.T <= 0) return 1;
     const TcPlan pl = tc_plan(a);
     const int prep = a.log_a ? 1 : 0;
-    // per-token decay without normaliser or z: the output walk in two builds (launch_chunk_tc)
-    const int out = a.log_a && !a.phi && !a.normalize && !a.z_out && (a.dk == 64 || pl.dvb == 64) &&
-                            tc_ws_supported(kFull, a.dk, pl.dvb, false) ? 2 : 1;
-    if (pl.P <= 1) return out + prep;
-    return (fold_segments(pl.Pu, a.dk, pl.dvb, a.normalize) ? 1 + out : 2 + out) + prep;
+    if (pl.P <= 1) return 1 + prep;
+    return (fold_segments(pl.Pu, a.dk, pl.dvb, a.normalize) ? 2 : 3) + prep;
 }
 
 size_t tc_workspace_bytes(const ChunkArgs& a) { return tc_plan(a).bytes; }
@@ -887,27 +884,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const KernelGammas& g, cudaStrea
         *launches = 1;
     }
     // The per-token decay without normaliser or z in the factored build wherever a
-    // unit's chunks allow it (gate_prep_kernel's flags): the output walk goes out
-    // twice, the factored build's CTAs taking those units and the row-scaling build's
-    // the others (each leaving the units that are not its own).  A state walk has no
+    // unit's chunks allow it (gate_prep_kernel's flags): the output walk's CTAs pick
+    // the factored build or the row scalings each for itself.  A state walk has no
     // row factors and keeps the row scalings.
-    const bool split = a.log_a && !a.phi && !prm.track_z && !a.noncausal && (a.dk == 64 || dvb == 64) &&
-                       tc_ws_supported(kFull, a.dk, dvb, false);
+    const bool pick = a.log_a && !a.phi && !prm.track_z && !a.noncausal && (a.dk == 64 || dvb == 64) &&
+                      tc_ws_supported(kFull, a.dk, dvb, false);
     auto dispatch = [&](const TcParams& pp, int grid, bool pdl) -> cudaError_t {
-        if (!split || pp.mode != kFull) {
-            *launches += 1;
-            return launch_tc_dispatch(a.dk, dvb, pp, grid, s, pdl);
-        }
+        *launches += 1;
+        if (!pick || pp.mode != kFull) return launch_tc_dispatch(a.dk, dvb, pp, grid, s, pdl);
         TcParams p1 = pp;
-        p1.fact = 1;
-        p1.gate_split = 1;
-        cudaError_t e1 = launch_tc_dispatch(a.dk, dvb, p1, grid, s, pdl);
-        if (e1 != cudaSuccess) return e1;
-        TcParams p2 = pp;
-        p2.fact = 0;
-        p2.gate_split = 2;
-        *launches += 2;
-        return launch_tc_dispatch(a.dk, dvb, p2, grid, s, pdl);
+        p1.fact = 1;  // (the pick kernel)
+        return launch_tc_dispatch(a.dk, dvb, p1, grid, s, pdl);
     };
     if (pl.P <= 1) {
         prm.mode = kFull;

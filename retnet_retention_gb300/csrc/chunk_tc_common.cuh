@@ -64,10 +64,8 @@ struct TcParams {
     // in the reversed sequence.  The initial state enters at the end, and the
     // final state is the one after row 0.
     int rev;
-    // per-token decay in two launches: 1 = this launch runs the units whose chunks
-    // are all unflagged (factored build), 2 = the others (0: one launch runs all);
-    // gate_flags [BH][n_chunks] from gate_prep_kernel
-    int gate_split;
+    // per-token decay, output walk: [BH][n_chunks] flags from gate_prep_kernel (1: the
+    // chunk's decay leaves the factored build's range), read by the pick kernel
     const int* gate_flags;
     int o_align32;  // O's base is 32-byte aligned (rows and column blocks then are too)
     KernelGammas g;

@@ -213,8 +213,10 @@ static_assert(kNumBars <= 32, "mbarrier slots");
 // gamma^(i+1) -> 2^(b_i), gamma^(L-1-j) -> 2^(b_(L-1) - b_j), gamma^L ->
 // 2^(b_(L-1)) (b in log2 units), and the score mask's running product steps by
 // a_j instead of gamma.
+// The kernel body: chunk_tc_ws_kernel runs one build, chunk_tc_ws_pick_kernel (the
+// per-token decay) picks one of two per CTA.
 template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
-__global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+__device__ __forceinline__ void chunk_tc_ws_body(const TcParams& p) {
     static_assert(!FACT || (!PHI && !NORM), "the factored decay is for plain retention");
     static_assert(!(FACT && GATED && STATE_ONLY), "a state walk with per-token decays takes the row scalings");
     constexpr int kThreadsC = threads_c(DK, DVB, PHI);
@@ -307,21 +309,6 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
     // the exit state take out again.  Every factor stays within 2^(+-Delta/2) for a
     // chunk that decays by 2^-Delta from its first row to its last.
     auto fact_beta = [&](const float* gc, int L) { return 0.5f * (gc[0] + gc[L - 1]); };
-    // Per-token decay in two launches (p.gate_split, output walks): the factored build
-    // takes the units whose chunks all keep their decay from first row to last at or
-    // above 2^-160, the build with row scalings the others; a unit's CTA in the other
-    // launch leaves at once, after waiting for the previous kernel like every CTA that
-    // works, so that this launch completes after it.
-    if constexpr (GATED) {
-        if (p.gate_split) {
-            int bad = 0;
-            for (int c = cb + lane; c < ce; c += 32) bad |= p.gate_flags[(size_t)bh * n_chunks + c];
-            if ((__any_sync(0xffffffffu, bad) != 0) == FACT) {
-                griddep_wait();
-                return;
-            }
-        }
-    }
     const uint64_t lim = p.wait_ns;
     if (tid == 0) LA_TL(4000);
     LA_CTA_T(0);
@@ -1225,6 +1212,31 @@ __global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_k
     LA_CTA_T(1);
 }
 
+template <int DK, int DVB, bool NORM, bool STATE_ONLY, bool PHI, bool GATED, bool FACT>
+__global__ void __launch_bounds__(bound_ws(DK, DVB, PHI, FACT), 1) chunk_tc_ws_kernel(const __grid_constant__ TcParams p) {
+    chunk_tc_ws_body<DK, DVB, NORM, STATE_ONLY, PHI, GATED, FACT>(p);
+}
+
+// Per-token decay, output walk without normaliser or z: the CTA takes the factored
+// build when every chunk of its unit keeps its decay from first row to last at or
+// above 2^-160 (p.gate_flags, from gate_prep_kernel), else the row scalings.  Every
+// warp reads the unit's flags and reaches the same answer.
+template <int DK, int DVB>
+__global__ void __launch_bounds__(bound_ws(DK, DVB, false, true), 1) chunk_tc_ws_pick_kernel(const __grid_constant__ TcParams p) {
+    const int unit = blockIdx.x;
+    const int seg = unit % p.n_seg;
+    const int bh = unit / (p.n_seg * p.n_dvb);
+    const int n_chunks = (p.T + kC - 1) / kC;
+    const int cb = seg * p.seg_chunks;
+    const int ce = min(n_chunks, cb + p.seg_chunks);
+    int bad = 0;
+    for (int c = cb + (int)(threadIdx.x & 31); c < ce; c += 32) bad |= p.gate_flags[(size_t)bh * n_chunks + c];
+    if (__any_sync(0xffffffffu, bad))
+        chunk_tc_ws_body<DK, DVB, false, false, false, true, false>(p);
+    else
+        chunk_tc_ws_body<DK, DVB, false, false, false, true, true>(p);
+}
+
 // pdl: launch as a programmatic dependent of the previous kernel in the stream
 // (the kernel's entry-state reads wait for that kernel; everything else may
 // start early).
@@ -1263,6 +1275,27 @@ cudaError_t launch_ws(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
     return e;
 }
 
+template <int DK, int DVB>
+cudaError_t launch_ws_pick(const TcParams& prm, int grid, cudaStream_t s, bool pdl) {
+    using Lay = LayoutWS<DK, DVB, false, false, true>;
+    auto kern = chunk_tc_ws_pick_kernel<DK, DVB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    TraceScope trace("chunk_tc_ws_kernel/full", s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(threads_ws(DK, DVB, false));
+    cfg.dynamicSmemBytes = Lay::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
 // The kernel for the launch's shape, flags and decay.  Kernels with phi are
 // instantiated apart where phi changes the kernel: the feature-map group of
 // 64-wide tiles, and the normaliser's row sums.
@@ -1273,11 +1306,12 @@ cudaError_t dispatch_ws(int dk, int dvb, bool normalize, const TcParams& prm, in
     if (prm.fact) {  // plain retention with its decays in the factored form's range
         if (phi || normalize) return cudaErrorInvalidValue;
         const bool st = prm.mode == kStateOnly;
-        if constexpr (GATED) {  // output walks (a state walk with these decays keeps the row scalings)
+        if constexpr (GATED) {  // output walks, each CTA picking its build (a state walk
+                                // with these decays keeps the row scalings)
             if (st) return cudaErrorInvalidValue;
-            if (dk == 64 && dvb == 64) return launch_ws<64, 64, false, false, false, true, true>(prm, grid, s, pdl);
-            if (dk == 64 && dvb == 128) return launch_ws<64, 128, false, false, false, true, true>(prm, grid, s, pdl);
-            if (dk == 128 && dvb == 64) return launch_ws<128, 64, false, false, false, true, true>(prm, grid, s, pdl);
+            if (dk == 64 && dvb == 64) return launch_ws_pick<64, 64>(prm, grid, s, pdl);
+            if (dk == 64 && dvb == 128) return launch_ws_pick<64, 128>(prm, grid, s, pdl);
+            if (dk == 128 && dvb == 64) return launch_ws_pick<128, 64>(prm, grid, s, pdl);
             return cudaErrorInvalidValue;  // (no room for the decays beside two 96 KB stages at 128 x 128)
         } else {
             if (dk == 64 && dvb == 64)
