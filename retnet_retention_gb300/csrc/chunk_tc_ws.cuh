@@ -761,14 +761,15 @@ __device__ __forceinline__ void chunk_tc_ws_body(const TcParams& p) {
                             // piece, so half 1 stores only after half 0 has read that piece (kBarP).
                             // A warp's 32 rows and a piece's 32 columns are the same 32 x 32 block
                             // for every lane, so a piece above the diagonal is P = 0 for the whole
-                            // warp (no load; not with phi's 8 warps), and only the piece on the
-                            // diagonal needs the mask j <= i.
+                            // warp (no load), and only the piece on the diagonal needs the mask
+                            // j <= i.
 #pragma unroll
                             for (int q = 0; q < 2; ++q) {
                                 const int c0 = 64 * half + 32 * q;
                                 const int pq = c0 >> 5, lq = warp & 3;
-                                // (the skip costs registers the 80-register build does not have)
-                                const bool zero = !PHI && pq > lq;
+                                // (in the 80-register phi build the skip spills a few registers
+                                // and still saves about 3 % of the walk)
+                                const bool zero = pq > lq;
                                 uint32_t r[32];
                                 if (!zero) {
                                     tmem_ld32(sc + c0, r);
