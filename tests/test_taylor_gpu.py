@@ -150,24 +150,31 @@ def test_taylor_timeout_is_reported_not_hung(opts):
     check("O after a reported timeout", np64(O), Or)
 
 
-def test_taylor_linear_attention_bf16_sampled():
+def test_taylor_linear_attention_bf16_full():
     """The Taylor workload at full size (B=8 H=16 T=4096, d=16 -> 273 features,
-    d_v=64, normalised, gamma = 1) in the launch the benchmark times; sampled
-    sequences checked against the oracle one by one, every output finite."""
+    d_v=64, normalised, gamma = 1) in the launch the benchmark times, every sequence
+    against the oracle (one batch row at a time; the errors combine as one
+    max|gpu - oracle| / max|oracle| per tensor)."""
     c = workloads.CONFIGS["taylor_linear_attention_bf16"]
     x = workloads.make_inputs(c)
-    B, H, T = c["B"], c["H"], c["T"]
+    B = c["B"]
     O, S, z = la.chunk_fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["gamma"],
                            phi="taylor", normalize=True)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(O).all())
-    for (b, h) in workloads.sample_pairs(B, H, 4):
-        sl = lambda t: t[b, h][None, None]
-        Or, Sr, zr = oracle.recurrent_taylor(sl(x["q"]), sl(x["k"]), sl(x["v"]), [x["gamma"][h]],
+    err = {"O": 0.0, "S_T": 0.0, "z_T": 0.0}
+    ref = dict(err)
+    for b in range(B):
+        sl = lambda t: t[b:b + 1]
+        Or, Sr, zr = oracle.recurrent_taylor(sl(x["q"]), sl(x["k"]), sl(x["v"]), x["gamma"],
                                              normalize=True)
-        check(f"O[{b},{h}]", np64(O[b, h]), Or[0, 0])
-        check(f"S_T[{b},{h}]", np64(S[b, h]), Sr[0, 0])
-        check(f"z_T[{b},{h}]", np64(z[b, h]), zr[0, 0])
+        for name, got, want in (("O", O[b:b + 1], Or), ("S_T", S[b:b + 1], Sr), ("z_T", z[b:b + 1], zr)):
+            g = np64(got)
+            assert np.all(np.isfinite(g)), f"{name}: non-finite output in batch row {b}"
+            err[name] = max(err[name], float(np.abs(g - want).max()))
+            ref[name] = max(ref[name], float(np.abs(want).max()))
+    for name in err:
+        rel = err[name] / ref[name]
+        assert rel <= 2e-2, f"{name}: rel err {rel:.3e} > 2e-02"
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
