@@ -225,6 +225,29 @@ def time_region(fn, steps: int, stream) -> float:
     return start.elapsed_time(end)
 
 
+def graph_replay_ms(step_on, n_sets: int, steps: int) -> float | None:
+    """Device milliseconds a step when the same steps are replayed from CUDA graphs
+    (one captured step per input set, on a side stream): the launches then cost no
+    host work.  None if capturing fails."""
+    side = torch.cuda.Stream()
+    try:
+        graphs = []
+        torch.cuda.synchronize()
+        for i in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                step_on(i, side)
+            graphs.append(g)
+        with torch.cuda.stream(side):
+            for g in graphs:
+                g.replay()
+            ms = time_region(lambda i: graphs[i % n_sets].replay(), steps, side)
+        return ms / steps
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return None
+
+
 def kernel_breakdown(la, fn, steps: int, stream) -> dict:
     """Per-kernel device time of the same timed loop, from the library's launch
     trace (CUDA events recorded on the launching stream around each kernel)."""
@@ -281,22 +304,27 @@ def prefill_measure(la, name: str, steps: int, warmup: int, rank: int, world: in
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    def step_on(i, s):
         qd, kd, vd, O, S, z, lad = sets[i % n_sets]
         la.chunk_fwd(qd, kd, vd, None if gated else gamma, phi=c["phi"],
                      normalize=c["normalize"], floor=c.get("floor", False), out=O, S_out=S,
-                     z_out=z, workspace=ws, stream=stream, log_a=lad)
+                     z_out=z, workspace=ws, stream=s, log_a=lad)
+
+    def step(i):
+        step_on(i, stream)
 
     for i in range(warmup):
         step(i)
     ms = time_region(step, steps, stream)
     kernels = kernel_breakdown(la, step, steps, stream)
+    graph_ms = graph_replay_ms(step_on, n_sets, steps)
     flags = ((la.LA_PHI_TAYLOR if c["phi"] == "taylor" else la.LA_PHI_ELU1 if c["phi"] else 0)
              | (la.LA_NORMALIZE if c["normalize"] else 0)
              | (la.LA_NORM_FLOOR if c.get("floor") else 0) | (la.LA_GATED if gated else 0))
     launches = la.library().la_chunk_fwd_launches(B, c["H"], c["T"], c["dk"], c["dv"],
                                                   1 if c["dtype"] == "bf16" else 0, flags, 0)
     res = dict(name=name, config=c, ms=ms / steps, tokens=B * c["T"], n_sets=n_sets,
+               graph_ms=graph_ms,
                alg_bytes=alg_bytes(c), alg_flops=alg_flops(c), launches=launches,
                kernels=kernels)
     if e2e:
@@ -524,7 +552,8 @@ def run_ours(args) -> dict | None:
         r = prefill_measure(la, only, args.steps, args.warmup, rank, world, batch=args.batch)
         if rank == 0:
             print(json.dumps({"only": only, "ms_per_step": r["ms"],
-                              "alg_gbs": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9}))
+                              "alg_gbs": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9,
+                              "graph_ms_per_step": r["graph_ms"]}))
         return None
     barrier()
     sampler = ClockSampler(local)
@@ -593,6 +622,8 @@ def run_ours(args) -> dict | None:
             "peak_source": pk["source"],
         },
         "kernels": head["kernels"],
+        # the same steps replayed from CUDA graphs (no host work per launch); context
+        "graph_ms_per_step": head.get("graph_ms"),
         "e2e": {
             "value": tokens_all / (e2e_ms * 1e-3),
             "unit": "tokens/s",
@@ -621,7 +652,7 @@ def run_ours(args) -> dict | None:
                              dominant_kernel=dn, kernel_gbs=kgbs, kernel_tflops=ktf,
                              bound="tensor" if tensor else "hbm",
                              roofline_frac=(ktf / pk["bf16_tflops"]) if tensor else kgbs / pk["hbm_gbs"],
-                             kernels=r["kernels"])
+                             graph_ms=r.get("graph_ms"), kernels=r["kernels"])
         dc = dec["config"]
         gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
         for name, bwd in bwds.items():
