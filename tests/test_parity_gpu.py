@@ -176,6 +176,38 @@ def test_closed_form_geometric_series():
         assert np.all(O[0, h, :, 1:] == 0.0)
 
 
+def test_closed_form_past_2_31_elements():
+    """Index arithmetic past 2^31 elements: B=64, H=16, T=32768, d=64 in bf16 (each of
+    Q, K, V and O holds 2^31 elements, 4 GiB), built on the device.  q = k = e_0 and
+    v = c_(b,h) e_0 with a constant per sequence, so o_n = c (1 - g^(n+1)) / (1 - g) for
+    the head's gamma (the multi-scale heads' 1 - 2^(-5-h)) and every other column is
+    0; a read of another sequence's rows would show as the wrong constant."""
+    B, H, T, d = 64, 16, 32768, 64
+    gam = np.array([1.0 - 2.0 ** (-5 - h) for h in range(H)], dtype=np.float32)
+    c = (np.arange(B * H).reshape(B, H) % 7 + 1).astype(np.float32)
+    q = torch.zeros(B, H, T, d, dtype=torch.bfloat16, device=DEV)
+    q[..., 0] = 1.0
+    v = torch.zeros(B, H, T, d, dtype=torch.bfloat16, device=DEV)
+    v[..., 0] = torch.from_numpy(c).to(DEV, torch.bfloat16)[:, :, None]
+    O, S, _ = la.chunk_fwd(q, q, v, gam)
+    torch.cuda.synchronize()
+    del q, v
+    assert float(O[..., 1:].float().abs().max()) == 0.0
+    got = O[..., 0].double().cpu().numpy()
+    del O
+    n = np.arange(T, dtype=np.float64)
+    g = gam.astype(np.float64)
+    geo = -np.expm1((n[None, :] + 1.0) * np.log(g)[:, None]) / (1.0 - g)[:, None]  # [H][T]
+    want = c.astype(np.float64)[:, :, None] * geo[None, :, :]
+    check("O[..., 0]", got, want, TOL["bf16"])
+    # the final state: S[0][0] = c sum_n g^(T-1-n) = c (1 - g^T) / (1 - g), the rest 0
+    S_np = S.double().cpu().numpy()
+    want_s = c.astype(np.float64) * (-np.expm1(T * np.log(g)) / (1.0 - g))[None, :]
+    check("S_T[0, 0]", S_np[:, :, 0, 0], want_s, TOL["bf16"])
+    S_np[:, :, 0, 0] = 0.0
+    assert np.all(S_np == 0.0)
+
+
 def test_empty_sequence_copies_state():
     B, H, dk, dv = 2, 3, 32, 16
     S0 = torch.randn(B, H, dk, dv, device=DEV)
