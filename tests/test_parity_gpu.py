@@ -176,12 +176,15 @@ def test_closed_form_geometric_series():
         assert np.all(O[0, h, :, 1:] == 0.0)
 
 
-def test_closed_form_past_2_31_elements():
+@pytest.mark.parametrize("gated", [False, True], ids=["gamma", "per_token"])
+def test_closed_form_past_2_31_elements(gated):
     """Index arithmetic past 2^31 elements: B=64, H=16, T=32768, d=64 in bf16 (each of
     Q, K, V and O holds 2^31 elements, 4 GiB), built on the device.  q = k = e_0 and
     v = c_(b,h) e_0 with a constant per sequence, so o_n = c (1 - g^(n+1)) / (1 - g) for
     the head's gamma (the multi-scale heads' 1 - 2^(-5-h)) and every other column is
-    0; a read of another sequence's rows would show as the wrong constant."""
+    0; a read of another sequence's rows would show as the wrong constant.  Per
+    token: the same gamma as a decay at every token (log_a = log gamma), through the
+    per-token decay's kernels."""
     B, H, T, d = 64, 16, 32768, 64
     gam = np.array([1.0 - 2.0 ** (-5 - h) for h in range(H)], dtype=np.float32)
     c = (np.arange(B * H).reshape(B, H) % 7 + 1).astype(np.float32)
@@ -189,7 +192,13 @@ def test_closed_form_past_2_31_elements():
     q[..., 0] = 1.0
     v = torch.zeros(B, H, T, d, dtype=torch.bfloat16, device=DEV)
     v[..., 0] = torch.from_numpy(c).to(DEV, torch.bfloat16)[:, :, None]
-    O, S, _ = la.chunk_fwd(q, q, v, gam)
+    if gated:
+        log_a = torch.from_numpy(np.log(gam.astype(np.float64)).astype(np.float32)).to(DEV)
+        log_a = log_a[None, :, None].expand(B, H, T).contiguous()
+        O, S, _ = la.chunk_fwd(q, q, v, log_a=log_a)
+        del log_a
+    else:
+        O, S, _ = la.chunk_fwd(q, q, v, gam)
     torch.cuda.synchronize()
     del q, v
     assert float(O[..., 1:].float().abs().max()) == 0.0
