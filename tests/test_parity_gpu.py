@@ -217,6 +217,32 @@ def test_closed_form_past_2_31_elements(gated):
     assert np.all(S_np == 0.0)
 
 
+def test_decode_steps_past_2_31_state_elements():
+    """Decode over a state of 2^31 fp32 elements (B=1024, H=128, d_k = d_v = 128; 8 GiB):
+    q = k = e_0 and v = c_(b,h) e_0 from S = 0, two steps: o_1 = c, o_2 = c (1 + g)
+    in column 0, and S = c (1 + g) e_0 e_0^T; a step on another sequence's state
+    block would show as the wrong constant."""
+    B, H, d = 1024, 128, 128
+    gam = np.array([1.0 - 2.0 ** (-5 - (h % 16)) for h in range(H)], dtype=np.float32)
+    c = (np.arange(B * H).reshape(B, H) % 7 + 1).astype(np.float32)
+    S = torch.zeros(B, H, d, d, device=DEV)
+    q = torch.zeros(B, H, d, dtype=torch.bfloat16, device=DEV)
+    q[..., 0] = 1.0
+    v = torch.zeros(B, H, d, dtype=torch.bfloat16, device=DEV)
+    v[..., 0] = torch.from_numpy(c).to(DEV, torch.bfloat16)
+    o1 = la.recurrent_step(q, q, v, gam, S)
+    o2 = la.recurrent_step(q, q, v, gam, S)
+    torch.cuda.synchronize()
+    g = gam.astype(np.float64)[None, :]
+    cc = c.astype(np.float64)
+    check("o_1", np64(o1[..., 0]), cc, TOL["bf16"])
+    check("o_2", np64(o2[..., 0]), cc * (1.0 + g), TOL["bf16"])
+    assert float(o2[..., 1:].float().abs().max()) == 0.0
+    check("S[0, 0]", np64(S[:, :, 0, 0]), cc * (1.0 + g), TOL["f32"])
+    S[:, :, 0, 0] = 0.0
+    assert float(S.abs().max()) == 0.0
+
+
 def test_empty_sequence_copies_state():
     B, H, dk, dv = 2, 3, 32, 16
     S0 = torch.randn(B, H, dk, dv, device=DEV)
